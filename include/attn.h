@@ -1,0 +1,109 @@
+/*
+ * attn.h -- C ABI of libattn: causal scaled dot-product attention forward on
+ * GB300 (sm_103a).
+ *
+ * The operation (one output row per query position i of every batch b and
+ * query head hq) is the five-step naive causal attention that the
+ * "Profiling in PyTorch (Part 3)" retelling lists in its section "Naive
+ * Attention":
+ *     1. S = Q K^T      2. S = S * scale      3. S[j > i] = -inf
+ *     4. P = softmax(S) over keys              5. O = P V
+ * with scale = 1/sqrt(head_dim) in the pages' usage (the NaiveCausalAttention
+ * listing in that section; the ai-manual.ru article, section 1, divides by
+ * sqrt(D), which is the same up to one fp32 rounding).  The library computes
+ * it in one fused pass that never stores S or P in global memory (the
+ * tiled online-softmax idea the same retelling describes for FlashAttention-2,
+ * section "The Flash Backend").
+ *
+ * Additionally the row log-sum-exp  LSE_i = ln sum_j exp(S_ij)  (S after steps
+ * 2 and 3) is written, in fp32, natural log.  The pages do not define it; it
+ * is the usual companion output of a fused attention forward.
+ *
+ * Threading: every entry point may be called from any host thread.  The only
+ * internal state is a cache of TMA descriptors and of per-device properties,
+ * guarded by a mutex.
+ */
+#ifndef LIBATTN_ATTN_H_
+#define LIBATTN_ATTN_H_
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes of every entry point. */
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1, /* NULL pointer, non-positive size, Hq % Hkv != 0, bad scale */
+    ATTN_ERR_UNSUPPORTED = 2, /* head_dim not 64 or 128, or device not compute capability 10.3 */
+    ATTN_ERR_MISALIGNED = 3,  /* a tensor pointer not 16-byte aligned (TMA requirement) */
+    ATTN_ERR_DEVICE = 4,      /* a CUDA runtime/driver query failed */
+    ATTN_ERR_LAUNCH = 5,      /* the kernel launch itself failed */
+    ATTN_ERR_TIMEOUT = 6      /* a device-side wait ran past its limit (read by attn_sync_status) */
+} attn_status_t;
+
+/*
+ * attn_fwd -- O = softmax(mask(Q K^T * scale)) V  and  LSE, on the GPU.
+ *
+ * Arguments (all tensors live in device memory of the current CUDA device and
+ * are owned by the caller; the library keeps no reference after the call):
+ *   q     bf16 [B, Hq,  S, D] contiguous (row-major, D fastest).
+ *   k     bf16 [B, Hkv, S, D] contiguous.
+ *   v     bf16 [B, Hkv, S, D] contiguous.
+ *   out   bf16 [B, Hq,  S, D] contiguous; written.  Must not alias q, k or v.
+ *   lse   fp32 [B, Hq,  S] contiguous; written; may be NULL to skip it.
+ *   B, Hq, Hkv, S   batch, query heads, key/value heads, sequence length (>= 1).
+ *         Hq % Hkv == 0.  Query head hq reads key/value head hq / (Hq / Hkv)
+ *         (grouped-query attention; Hkv == Hq is plain multi-head, Hkv == 1
+ *         is multi-query).
+ *   D     head dimension: 64 or 128.
+ *   scale finite and >= 0; the scores are multiplied by it (usually 1/sqrt(D)).
+ *   causal  non-zero: key j is masked for query i when j > i (query and key
+ *         positions share one index, Sq == Sk == S).  Zero: no mask.
+ *   stream  CUDA stream (cudaStream_t, passed as void*) the work is enqueued
+ *         on; NULL means the legacy default stream.
+ *
+ * Every pointer must be 16-byte aligned.  The call is asynchronous: it
+ * returns once the kernel is enqueued and does not synchronise.  On an
+ * argument error nothing is launched.  Output rows are written for
+ * i < S only; nothing outside out[0 .. B*Hq*S*D) and lse[0 .. B*Hq*S) is
+ * written.  Results are deterministic: repeated calls give the same bits.
+ *
+ * Returns ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED,
+ * ATTN_ERR_MISALIGNED, ATTN_ERR_DEVICE or ATTN_ERR_LAUNCH.
+ */
+int attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse,
+             int B, int Hq, int Hkv, int S, int D, float scale, int causal, void *stream);
+
+/*
+ * attn_sync_status -- synchronise `stream` and report device-side failures of
+ * the attention kernels enqueued on this device since the last call.
+ *
+ * Every wait inside the kernels is bounded in time; a wait that runs out sets
+ * a per-device status word and makes the kernel exit cleanly (it never traps).
+ * This call waits for `stream`, reads and clears that word, and returns
+ * ATTN_OK, ATTN_ERR_TIMEOUT, or ATTN_ERR_DEVICE if the synchronisation itself
+ * failed.
+ */
+int attn_sync_status(void *stream);
+
+/*
+ * attn_selftest_wait_timeout -- launch one tiny kernel that waits on an
+ * mbarrier nobody arrives at, with a limit of `limit_us` microseconds
+ * (1 .. 1000000).  The wait must give up, set the status word and let the
+ * kernel return; attn_sync_status then reports ATTN_ERR_TIMEOUT.  It exists so
+ * the bounded-wait path is exercised without faulting or hanging a GPU.
+ * Returns ATTN_OK once launched, ATTN_ERR_INVALID_ARG for a bad limit.
+ */
+int attn_selftest_wait_timeout(int limit_us, void *stream);
+
+/* Human-readable name of a return code (static storage; never NULL). */
+const char *attn_status_string(int status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int attn_version(void);
+
+#ifdef __cplusplus
+} /* extern "C" */
+#endif
+
+#endif /* LIBATTN_ATTN_H_ */

@@ -1,0 +1,129 @@
+"""fp64 CPU oracle for causal scaled dot-product attention -- TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
+leg import this package.  The CUDA library never links, loads or calls it, and
+it imports nothing from the CUDA library's package.
+
+The arithmetic lives in ``attn_oracle.c`` (plain C, double precision, one query
+row at a time, the five steps of the naive causal attention in the order the
+"Profiling in PyTorch (Part 3)" retelling lists them in its section "Naive
+Attention").  This module only builds that file with gcc and marshals numpy
+arrays into it.
+
+Parity status: pinned.  ``tests/test_oracle_pins.py`` checks it against
+library float64 routines, closed forms and invariants; ``tests/test_oracle_mutants.py``
+plants mistakes into copies of the C source and checks that a pin catches each.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(_HERE, "attn_oracle.c")
+BUILD_DIR = os.path.join(_HERE, "_build")
+LIBRARY = os.path.join(BUILD_DIR, "liboracle.so")
+
+_lock = threading.Lock()
+_lib_cache: dict[str, ctypes.CDLL] = {}
+
+
+def compile_oracle(source: str = SOURCE, output: str = LIBRARY) -> str:
+    """Compile ``source`` into a shared library at ``output`` with gcc.
+
+    Plain ``-O2`` without fast-math or machine-specific flags, so the same
+    results come out on x86_64 and aarch64 hosts.
+    """
+    os.makedirs(os.path.dirname(output), exist_ok=True)
+    tmp = output + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-o", tmp, source, "-lm"]
+    subprocess.run(cmd, check=True, capture_output=True, text=True)
+    os.replace(tmp, output)
+    return output
+
+
+def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
+    f = lib.oracle_attn_rows
+    f.restype = ctypes.c_int
+    f.argtypes = [
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+        ctypes.c_float, ctypes.c_int,
+        ctypes.c_void_p, ctypes.c_int64,
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+    ]
+    return lib
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load (building first if needed) the oracle library at ``path``."""
+    path = path or LIBRARY
+    with _lock:
+        if path in _lib_cache:
+            return _lib_cache[path]
+        if path == LIBRARY:
+            stale = (not os.path.exists(path)) or os.path.getmtime(path) < os.path.getmtime(SOURCE)
+            if stale:
+                compile_oracle()
+        lib = _bind(ctypes.CDLL(path))
+        _lib_cache[path] = lib
+        return lib
+
+
+def default_threads() -> int:
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:  # pragma: no cover
+        return max(1, os.cpu_count() or 1)
+
+
+def _as_bits(x: np.ndarray, name: str) -> np.ndarray:
+    x = np.ascontiguousarray(x)
+    if x.dtype != np.uint16:
+        raise TypeError(f"{name}: expected bf16 bit patterns as uint16, got {x.dtype}")
+    return x
+
+
+def attention(q_bits, k_bits, v_bits, scale: float, causal: bool = True, rows=None,
+              nthreads: int | None = None, lib: ctypes.CDLL | None = None):
+    """O (float64) and LSE (float64, natural log) of causal scaled dot-product attention.
+
+    q_bits: uint16 [B,Hq,S,D]; k_bits, v_bits: uint16 [B,Hkv,S,D] -- bf16 bit patterns.
+    rows: optional int64 array of flat query-row ids (b*Hq + hq)*S + i; then the
+          result has shape [len(rows), D] and [len(rows)].  Without rows the
+          result is [B,Hq,S,D] and [B,Hq,S].
+    """
+    lib = lib or load()
+    q_bits = _as_bits(q_bits, "q")
+    k_bits = _as_bits(k_bits, "k")
+    v_bits = _as_bits(v_bits, "v")
+    if q_bits.ndim != 4 or k_bits.ndim != 4 or v_bits.shape != k_bits.shape:
+        raise ValueError("q must be [B,Hq,S,D]; k and v must both be [B,Hkv,S,D]")
+    B, Hq, S, D = q_bits.shape
+    Bk, Hkv, Sk, Dk = k_bits.shape
+    if (Bk, Sk, Dk) != (B, S, D):
+        raise ValueError("q and k/v disagree on B, S or D")
+    if rows is None:
+        nrows = B * Hq * S
+        rows_arr = None
+        out_shape, lse_shape = (B, Hq, S, D), (B, Hq, S)
+    else:
+        rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        nrows = rows_arr.size
+        out_shape, lse_shape = (nrows, D), (nrows,)
+    out = np.empty(out_shape, dtype=np.float64)
+    lse = np.empty(lse_shape, dtype=np.float64)
+    nt = nthreads or default_threads()
+    rc = lib.oracle_attn_rows(
+        q_bits.ctypes.data, k_bits.ctypes.data, v_bits.ctypes.data,
+        B, Hq, Hkv, S, D, ctypes.c_float(scale), 1 if causal else 0,
+        None if rows_arr is None else rows_arr.ctypes.data, nrows,
+        out.ctypes.data, lse.ctypes.data, nt,
+    )
+    if rc != 0:
+        raise ValueError("oracle_attn_rows rejected its arguments")
+    return out, lse

@@ -1,0 +1,194 @@
+/*
+ * attn_oracle.c -- fp64 CPU oracle for causal scaled dot-product attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path links, loads or
+ * calls this file; only the tests, the smoke check and the benchmark's CPU
+ * baseline leg do.  It shares no code, header or table with the CUDA library.
+ *
+ * What it computes (the method's plain definition, in double precision):
+ *   "Profiling in PyTorch (Part 3)" retelling, section "Naive Attention",
+ *   five-step list and the NaiveCausalAttention listing:
+ *     1. scores = Q . K^T
+ *     2. scores = scores * scale
+ *     3. scores[j > i] = -inf            (causal mask; the diagonal is kept)
+ *     4. attn = softmax(scores) over keys
+ *     5. out = attn . V
+ *   and the definition Attention(Q,K,V) = softmax(Q K^T / sqrt(d_k)) V from
+ *   the ainews.cool article, section "technical deep dive".
+ *   The fully-masked-row convention (output 0 instead of NaN) follows the
+ *   same retelling's description of the SDPA math backend's _safe_softmax
+ *   (section "The Math Backend").  It cannot arise for causal, Sq == Sk.
+ *
+ * The log-sum-exp output (natural log of sum_j exp(s_j), s_j the scaled and
+ * masked scores) is not on the pages; it is the usual companion output of a
+ * fused attention forward and is defined here as written above.
+ *
+ * The oracle works one query row at a time, so the [S,S] score matrix is
+ * never held; within a row it performs the five steps in the order above,
+ * each as its own loop.  A library primitive is not needed.
+ *
+ * Inputs are bf16 bit patterns (uint16) in [B,H,S,D] contiguous layout, the
+ * same bits the GPU receives.  Widening bf16 -> double is exact.
+ *
+ * Parity pins (tests/test_oracle_pins.py): library softmax / SDPA in float64,
+ * closed forms (causal row 0, Q = 0 means, S = 1), key-shift and linearity
+ * invariants, a hand-derived worked example, and row sums.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* bf16 bit pattern -> double.  A bf16 value is the top half of an IEEE-754
+ * binary32, so shifting the 16 bits up gives the float exactly. */
+static double bf16_bits_to_double(uint16_t b) {
+    uint32_t u = ((uint32_t)b) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+typedef struct {
+    const uint16_t *q, *k, *v;
+    int B, Hq, Hkv, S, D;
+    double scale;
+    int causal;
+    const int64_t *rows; /* flat query-row ids, or NULL for all rows */
+    int64_t nrows;
+    double *out; /* [nrows, D] */
+    double *lse; /* [nrows]    */
+    int64_t begin, end;
+    int status;
+} oracle_job_t;
+
+/*
+ * One query row: flat id r = (b*Hq + hq)*S + i.
+ * GQA head mapping: contiguous groups of G = Hq/Hkv query heads share one
+ * key/value head, hkv = hq / G (the grouped-query strategy named in the
+ * ainews.cool strategy table; with Hkv == Hq it is plain multi-head).
+ */
+static void oracle_one_row(const oracle_job_t *J, int64_t r, double *s,
+                           double *o_row, double *lse_out) {
+    const int S = J->S, D = J->D;
+    const int64_t i = r % S;
+    const int64_t bh = r / S;
+    const int64_t b = bh / J->Hq;
+    const int64_t hq = bh % J->Hq;
+    const int64_t G = J->Hq / J->Hkv;
+    const int64_t hkv = hq / G;
+
+    const uint16_t *qi = J->q + (bh * S + i) * (int64_t)D;
+    const uint16_t *kb = J->k + ((b * J->Hkv + hkv) * S) * (int64_t)D;
+    const uint16_t *vb = J->v + ((b * J->Hkv + hkv) * S) * (int64_t)D;
+
+    /* Step 1: scores_j = sum_d q_id * k_jd. */
+    for (int64_t j = 0; j < S; ++j) {
+        double acc = 0.0;
+        for (int d = 0; d < D; ++d)
+            acc += bf16_bits_to_double(qi[d]) * bf16_bits_to_double(kb[j * D + d]);
+        s[j] = acc;
+    }
+    /* Step 2: scale (multiply by the caller's scale). */
+    for (int64_t j = 0; j < S; ++j) s[j] = s[j] * J->scale;
+    /* Step 3: causal mask, keys after the query position get -inf. */
+    if (J->causal)
+        for (int64_t j = i + 1; j < S; ++j) s[j] = -INFINITY;
+    /* Step 4: softmax over keys, max-subtracted ("safe") form. */
+    double m = -INFINITY;
+    for (int64_t j = 0; j < S; ++j)
+        if (s[j] > m) m = s[j];
+    if (m == -INFINITY) { /* every key masked: output 0, LSE -inf */
+        for (int d = 0; d < D; ++d) o_row[d] = 0.0;
+        *lse_out = -INFINITY;
+        return;
+    }
+    double l = 0.0;
+    for (int64_t j = 0; j < S; ++j) {
+        s[j] = exp(s[j] - m); /* exp(-inf) == 0 */
+        l += s[j];
+    }
+    for (int64_t j = 0; j < S; ++j) s[j] = s[j] / l;
+    /* Step 5: out_d = sum_j attn_j * v_jd. */
+    for (int d = 0; d < D; ++d) o_row[d] = 0.0;
+    for (int64_t j = 0; j < S; ++j) {
+        if (s[j] == 0.0) continue; /* masked key contributes nothing */
+        for (int d = 0; d < D; ++d) o_row[d] += s[j] * bf16_bits_to_double(vb[j * D + d]);
+    }
+    *lse_out = m + log(l);
+}
+
+static void *oracle_worker(void *arg) {
+    oracle_job_t *J = (oracle_job_t *)arg;
+    double *s = (double *)malloc(sizeof(double) * (size_t)J->S);
+    if (!s) {
+        J->status = 1;
+        return NULL;
+    }
+    for (int64_t n = J->begin; n < J->end; ++n) {
+        int64_t r = J->rows ? J->rows[n] : n;
+        oracle_one_row(J, r, s, J->out + n * (int64_t)J->D, J->lse + n);
+    }
+    free(s);
+    J->status = 0;
+    return NULL;
+}
+
+/*
+ * oracle_attn_rows -- O and LSE for selected query rows (or all rows).
+ *
+ *   q [B,Hq,S,D], k/v [B,Hkv,S,D]: bf16 bit patterns, contiguous.
+ *   rows: nrows flat ids (b*Hq + hq)*S + i, or NULL for every row in order
+ *         (then nrows must equal B*Hq*S).
+ *   out:  double [nrows, D];  lse: double [nrows] (natural log).
+ *   nthreads: worker threads (>= 1).
+ * Returns 0 on success, 1 on a bad argument or allocation failure.
+ */
+int oracle_attn_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int Hq,
+                     int Hkv, int S, int D, float scale, int causal, const int64_t *rows,
+                     int64_t nrows, double *out, double *lse, int nthreads) {
+    if (!q || !k || !v || !out || !lse) return 1;
+    if (B < 1 || Hq < 1 || Hkv < 1 || S < 1 || D < 1 || Hq % Hkv != 0) return 1;
+    const int64_t total = (int64_t)B * Hq * S;
+    if (!rows && nrows != total) return 1;
+    if (rows)
+        for (int64_t n = 0; n < nrows; ++n)
+            if (rows[n] < 0 || rows[n] >= total) return 1;
+    if (nrows == 0) return 0;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > nrows) nthreads = (int)nrows;
+
+    oracle_job_t *jobs = (oracle_job_t *)calloc((size_t)nthreads, sizeof(oracle_job_t));
+    pthread_t *tid = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    if (!jobs || !tid) {
+        free(jobs);
+        free(tid);
+        return 1;
+    }
+    int status = 0;
+    for (int t = 0; t < nthreads; ++t) {
+        oracle_job_t *J = &jobs[t];
+        J->q = q; J->k = k; J->v = v;
+        J->B = B; J->Hq = Hq; J->Hkv = Hkv; J->S = S; J->D = D;
+        J->scale = (double)scale;
+        J->causal = causal ? 1 : 0;
+        J->rows = rows; J->nrows = nrows;
+        J->out = out; J->lse = lse;
+        J->begin = nrows * t / nthreads;
+        J->end = nrows * (t + 1) / nthreads;
+        J->status = 1;
+    }
+    int started = 0;
+    for (int t = 1; t < nthreads; ++t) {
+        if (pthread_create(&tid[t], NULL, oracle_worker, &jobs[t]) != 0) break;
+        started = t;
+    }
+    /* threads that failed to start: run their share here */
+    oracle_worker(&jobs[0]);
+    for (int t = 1; t <= started; ++t) pthread_join(tid[t], NULL);
+    for (int t = started + 1; t < nthreads; ++t) oracle_worker(&jobs[t]);
+    for (int t = 0; t < nthreads; ++t) status |= jobs[t].status;
+    free(jobs);
+    free(tid);
+    return status;
+}

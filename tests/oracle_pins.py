@@ -1,0 +1,270 @@
+"""Pins for the fp64 oracle: facts fixed by the pages and by mathematics.
+
+Each ``pin_*`` takes ``attn(q_bits, k_bits, v_bits, scale, causal, rows=None)``
+returning ``(O, LSE)`` in float64 and raises AssertionError when the callable
+disagrees with what the pin fixes.  ``tests/test_oracle_pins.py`` runs them on
+the oracle; ``tests/test_oracle_mutants.py`` runs them on copies of the oracle
+with planted mistakes and requires that some pin fails for each.
+
+None of these re-types the oracle's own loops: each compares against a
+library float64 routine, a closed form, an invariant of the definition, or a
+hand-derived worked example (tests/golden/worked_example_s3.json).
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+import torch
+import torch.nn.functional as F
+
+from causal_scaled_dot_gb300.inputs import (bf16_bits_to_float32, float32_to_bf16_bits,
+                                            gaussian_bf16)
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def bits(x) -> np.ndarray:
+    """float values that are exact in bf16 -> bf16 bits (asserts exactness)."""
+    x32 = np.asarray(x, dtype=np.float32)
+    b = float32_to_bf16_bits(x32)
+    assert np.array_equal(bf16_bits_to_float32(b), x32), "value not exact in bf16"
+    return b
+
+
+def f64(b) -> np.ndarray:
+    return bf16_bits_to_float32(b).astype(np.float64)
+
+
+def _rand(shape, seed, stream, sigma=1.0):
+    return gaussian_bf16(shape, seed, stream, sigma)
+
+
+def _grid(shape, rng, lo, hi, step):
+    """Random multiples of ``step`` in [lo, hi] (exact in bf16 for small grids)."""
+    n = int(round((hi - lo) / step))
+    return lo + step * rng.integers(0, n + 1, size=shape)
+
+
+def _sdpa64(q_b, k_b, v_b, scale, causal):
+    """torch's scaled_dot_product_attention on CPU in float64 (a library routine)."""
+    q = torch.from_numpy(f64(q_b))
+    k = torch.from_numpy(f64(k_b))
+    v = torch.from_numpy(f64(v_b))
+    G = q.shape[1] // k.shape[1]
+    k = k.repeat_interleave(G, dim=1)
+    v = v.repeat_interleave(G, dim=1)
+    return F.scaled_dot_product_attention(q, k, v, is_causal=causal,
+                                          scale=float(np.float32(scale))).numpy()
+
+
+# ---------------------------------------------------------------------------
+def pin_sdpa_library(attn):
+    """O equals torch's float64 SDPA (math backend on CPU), causal and not, with GQA."""
+    for (B, Hq, Hkv, S, D), causal, seed in [((2, 4, 2, 37, 16), True, 11),
+                                             ((1, 3, 3, 29, 8), False, 12),
+                                             ((1, 4, 1, 20, 4), True, 13)]:
+        q = _rand((B, Hq, S, D), seed, 0)
+        k = _rand((B, Hkv, S, D), seed, 1)
+        v = _rand((B, Hkv, S, D), seed, 2)
+        scale = 1.0 / math.sqrt(D)
+        O, _ = attn(q, k, v, scale, causal)
+        ref = _sdpa64(q, k, v, scale, causal)
+        np.testing.assert_allclose(O, ref, rtol=0, atol=1e-12)
+
+
+def pin_attention_matrix(attn):
+    """With V = identity rows (D >= S) the output row is the attention row itself:
+    zero above the diagonal (causal), rows summing to 1, and ratios
+    P_ij / P_ik = exp(scale * q_i . (k_j - k_k)) (the softmax closed form)."""
+    rng = np.random.default_rng(21)
+    S, D = 12, 16
+    q = bits(_grid((1, 1, S, D), rng, -1, 1, 0.125))
+    k = bits(_grid((1, 1, S, D), rng, -1, 1, 0.125))
+    v = np.zeros((1, 1, S, D), np.float32)
+    for j in range(S):
+        v[0, 0, j, j] = 1.0
+    v = bits(v)
+    scale = 0.25
+    qf, kf = f64(q)[0, 0], f64(k)[0, 0]
+    for causal in (True, False):
+        O, _ = attn(q, k, v, scale, causal)
+        P = O[0, 0, :, :S]
+        assert np.all(O[0, 0, :, S:] == 0.0)
+        np.testing.assert_allclose(P.sum(axis=1), 1.0, rtol=0, atol=1e-14)
+        for i in range(S):
+            hi = i + 1 if causal else S
+            if causal:
+                assert np.all(P[i, hi:] == 0.0), "masked keys must get weight exactly 0"
+            assert np.all(P[i, :hi] > 0.0)
+            sc = scale * (kf[:hi] @ qf[i])
+            expect = np.exp(sc - sc[0])
+            np.testing.assert_allclose(P[i, :hi] / P[i, 0], expect, rtol=1e-12, atol=0)
+
+
+def pin_row0_and_s1(attn):
+    """Causal row 0 attends to key 0 only: O_0 = V_0 exactly, LSE_0 = scale q_0.k_0.
+    S = 1 (causal or not): O = V, LSE = scale q.k."""
+    B, H, S, D = 2, 2, 9, 8
+    q, k, v = (_rand((B, H, S, D), 31, t) for t in range(3))
+    scale = 0.3
+    O, L = attn(q, k, v, scale, True)
+    assert np.array_equal(O[:, :, 0, :], f64(v)[:, :, 0, :])
+    dots = np.einsum("bhd,bhd->bh", f64(q)[:, :, 0], f64(k)[:, :, 0])
+    np.testing.assert_allclose(L[:, :, 0], float(np.float32(scale)) * dots, rtol=0, atol=1e-12)
+    for causal in (True, False):
+        q1, k1, v1 = q[:, :, :1], k[:, :, :1], v[:, :, :1]
+        O1, L1 = attn(np.ascontiguousarray(q1), np.ascontiguousarray(k1), np.ascontiguousarray(v1),
+                      scale, causal)
+        assert np.array_equal(O1, f64(v1))
+        np.testing.assert_allclose(L1[:, :, 0], float(np.float32(scale)) * dots, rtol=0, atol=1e-12)
+
+
+def pin_q_zero_mean(attn):
+    """Q = 0 makes every score 0: O_i = mean(V_0..V_i) and LSE_i = ln(i+1) (causal);
+    mean of all V and ln S without the mask.  GQA shape."""
+    B, Hq, Hkv, S, D = 2, 4, 2, 23, 8
+    q = np.zeros((B, Hq, S, D), np.uint16)  # +0.0 in bf16
+    k = _rand((B, Hkv, S, D), 41, 1)
+    v = _rand((B, Hkv, S, D), 41, 2)
+    vf = np.repeat(f64(v), Hq // Hkv, axis=1)
+    O, L = attn(q, k, v, 0.125, True)
+    counts = np.arange(1, S + 1, dtype=np.float64)
+    np.testing.assert_allclose(O, np.cumsum(vf, axis=2) / counts[None, None, :, None],
+                               rtol=0, atol=1e-13)
+    np.testing.assert_allclose(L, np.broadcast_to(np.log(counts), L.shape), rtol=0, atol=1e-13)
+    O, L = attn(q, k, v, 0.125, False)
+    np.testing.assert_allclose(O, np.broadcast_to(vf.mean(axis=2, keepdims=True), O.shape),
+                               rtol=0, atol=1e-13)
+    np.testing.assert_allclose(L, math.log(S), rtol=0, atol=1e-13)
+
+
+def pin_key_shift(attn):
+    """Adding one vector c to every key adds scale q_i.c to every score of row i:
+    softmax is unchanged (O unchanged) and LSE_i grows by scale q_i.c."""
+    rng = np.random.default_rng(51)
+    B, H, S, D = 1, 2, 17, 8
+    q = bits(_grid((B, H, S, D), rng, -2, 2, 0.125))
+    k = _grid((B, H, S, D), rng, -2, 2, 0.125)
+    c = _grid((D,), rng, -1, 1, 0.125)
+    v = _rand((B, H, S, D), 51, 2)
+    scale = 0.5
+    for causal in (True, False):
+        O0, L0 = attn(q, bits(k), v, scale, causal)
+        O1, L1 = attn(q, bits(k + c), v, scale, causal)
+        np.testing.assert_allclose(O1, O0, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(L1 - L0, scale * (f64(q) @ c), rtol=0, atol=1e-12)
+
+
+def pin_value_linearity(attn):
+    """O is affine in V with weights summing to 1: V = const gives O = const, and
+    O(V1 + V2) = O(V1) + O(V2)."""
+    rng = np.random.default_rng(61)
+    B, H, S, D = 1, 2, 19, 8
+    q = _rand((B, H, S, D), 61, 0)
+    k = _rand((B, H, S, D), 61, 1)
+    const = bits(np.broadcast_to(_grid((1, 1, 1, D), rng, -3, 3, 0.25), (B, H, S, D)))
+    O, _ = attn(q, k, const, 0.35, True)
+    np.testing.assert_allclose(O, f64(const), rtol=0, atol=1e-13)
+    v1 = _grid((B, H, S, D), rng, -2, 2, 0.25)
+    v2 = _grid((B, H, S, D), rng, -2, 2, 0.25)
+    for causal in (True, False):
+        Oa, _ = attn(q, k, bits(v1), 0.35, causal)
+        Ob, _ = attn(q, k, bits(v2), 0.35, causal)
+        Os, _ = attn(q, k, bits(v1 + v2), 0.35, causal)
+        np.testing.assert_allclose(Os, Oa + Ob, rtol=0, atol=1e-12)
+
+
+def pin_causality(attn):
+    """Changing keys/values after position i leaves row i unchanged (exactly);
+    the last causal row equals the unmasked last row."""
+    B, H, S, D = 1, 2, 16, 8
+    q, k, v = (_rand((B, H, S, D), 71, t) for t in range(3))
+    O, L = attn(q, k, v, 0.3, True)
+    cut = 6
+    k2, v2 = k.copy(), v.copy()
+    k2[:, :, cut + 1:] = _rand((B, H, S - cut - 1, D), 72, 1)
+    v2[:, :, cut + 1:] = _rand((B, H, S - cut - 1, D), 72, 2)
+    O2, L2 = attn(q, k2, v2, 0.3, True)
+    assert np.array_equal(O2[:, :, :cut + 1], O[:, :, :cut + 1])
+    assert np.array_equal(L2[:, :, :cut + 1], L[:, :, :cut + 1])
+    assert not np.allclose(O2[:, :, cut + 1:], O[:, :, cut + 1:])
+    On, Ln = attn(q, k, v, 0.3, False)
+    np.testing.assert_allclose(O[:, :, -1], On[:, :, -1], rtol=0, atol=1e-14)
+    np.testing.assert_allclose(L[:, :, -1], Ln[:, :, -1], rtol=0, atol=1e-14)
+    assert not np.allclose(O[:, :, 0], On[:, :, 0])
+
+
+def pin_heads_and_batches(attn):
+    """GQA equals multi-head attention on key/value heads repeated in contiguous
+    groups; batch entries are independent of each other."""
+    B, Hq, Hkv, S, D = 3, 6, 2, 11, 8
+    q = _rand((B, Hq, S, D), 81, 0)
+    k = _rand((B, Hkv, S, D), 81, 1)
+    v = _rand((B, Hkv, S, D), 81, 2)
+    O, L = attn(q, k, v, 0.3, True)
+    ke = np.ascontiguousarray(np.repeat(k, Hq // Hkv, axis=1))
+    ve = np.ascontiguousarray(np.repeat(v, Hq // Hkv, axis=1))
+    Oe, Le = attn(q, ke, ve, 0.3, True)
+    assert np.array_equal(O, Oe) and np.array_equal(L, Le)
+    for b in range(B):
+        Ob, Lb = attn(np.ascontiguousarray(q[b:b + 1]), np.ascontiguousarray(k[b:b + 1]),
+                      np.ascontiguousarray(v[b:b + 1]), 0.3, True)
+        assert np.array_equal(Ob[0], O[b]) and np.array_equal(Lb[0], L[b])
+
+
+def pin_large_magnitude(attn):
+    """Scores in the thousands (Q x 1024) still give finite results equal to the
+    library's float64 SDPA: the softmax must subtract the row maximum."""
+    B, H, S, D = 1, 2, 24, 16
+    q = _rand((B, H, S, D), 91, 0)
+    k = _rand((B, H, S, D), 91, 1)
+    v = _rand((B, H, S, D), 91, 2)
+    q_big = float32_to_bf16_bits(bf16_bits_to_float32(q) * np.float32(1024.0))
+    for causal in (True, False):
+        O, L = attn(q_big, k, v, 0.25, causal)
+        assert np.all(np.isfinite(O)) and np.all(np.isfinite(L))
+        np.testing.assert_allclose(O, _sdpa64(q_big, k, v, 0.25, causal), rtol=0, atol=1e-10)
+
+
+def pin_worked_example(attn):
+    """The hand-derived S = 3 example in tests/golden/worked_example_s3.json."""
+    with open(os.path.join(GOLDEN, "worked_example_s3.json")) as f:
+        ex = json.load(f)
+    sh = ex["shape"]
+    shp = (sh["B"], sh["Hq"], sh["S"], sh["D"])
+    q = bits(np.array(ex["q"]).reshape(shp))
+    k = bits(np.array(ex["k"]).reshape(shp))
+    v = bits(np.array(ex["v"]).reshape(shp))
+    env = {"e": math.e, "ln": math.log, "__builtins__": {}}
+
+    def ev(s):
+        return eval(s, env)  # expressions from the fixture, e.g. "1/(1+e)"
+
+    O, L = attn(q, k, v, ex["scale"], True)
+    exp_o = np.array([[ev(s) for s in row] for row in ex["causal"]["out"]])
+    exp_l = np.array([ev(s) for s in ex["causal"]["lse"]])
+    np.testing.assert_allclose(O[0, 0], exp_o, rtol=0, atol=1e-15)
+    np.testing.assert_allclose(L[0, 0], exp_l, rtol=0, atol=1e-15)
+    O, L = attn(q, k, v, ex["scale"], False)
+    rows = ex["noncausal"]["rows"]
+    exp_o = np.array([[ev(s) for s in row] for row in ex["noncausal"]["out"]])
+    exp_l = np.array([ev(s) for s in ex["noncausal"]["lse"]])
+    np.testing.assert_allclose(O[0, 0, rows], exp_o, rtol=0, atol=1e-15)
+    np.testing.assert_allclose(L[0, 0, rows], exp_l, rtol=0, atol=1e-15)
+
+
+ALL_PINS = [
+    pin_sdpa_library,
+    pin_attention_matrix,
+    pin_row0_and_s1,
+    pin_q_zero_mean,
+    pin_key_shift,
+    pin_value_linearity,
+    pin_causality,
+    pin_heads_and_batches,
+    pin_large_magnitude,
+    pin_worked_example,
+]

@@ -1,0 +1,65 @@
+"""The fp64 oracle against its pins (CPU only)."""
+import numpy as np
+import pytest
+
+import oracle
+from tests import oracle_pins
+
+
+def _attn(q, k, v, scale, causal, rows=None):
+    return oracle.attention(q, k, v, scale, causal, rows=rows)
+
+
+@pytest.mark.parametrize("pin", oracle_pins.ALL_PINS, ids=lambda p: p.__name__)
+def test_oracle_pin(pin):
+    pin(_attn)
+
+
+def test_rows_subset_matches_full():
+    """The row-selection entry computes exactly the rows of the full call."""
+    from causal_scaled_dot_gb300.inputs import qkv_bf16
+    q, k, v = qkv_bf16(2, 4, 2, 33, 16, seed=7)
+    O, L = oracle.attention(q, k, v, 0.25, True)
+    rows = np.array([0, 1, 32, 33, 100, 2 * 4 * 33 - 1], dtype=np.int64)
+    Or, Lr = oracle.attention(q, k, v, 0.25, True, rows=rows)
+    assert np.array_equal(Or, O.reshape(-1, 16)[rows])
+    assert np.array_equal(Lr, L.reshape(-1)[rows])
+
+
+def test_thread_count_does_not_change_bits():
+    from causal_scaled_dot_gb300.inputs import qkv_bf16
+    q, k, v = qkv_bf16(1, 2, 2, 70, 8, seed=8)
+    a = oracle.attention(q, k, v, 0.3, True, nthreads=1)
+    b = oracle.attention(q, k, v, 0.3, True, nthreads=5)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_oracle_rejects_bad_arguments():
+    from causal_scaled_dot_gb300.inputs import qkv_bf16
+    q, k, v = qkv_bf16(1, 3, 2, 8, 8, seed=9)  # Hq % Hkv != 0
+    with pytest.raises(ValueError):
+        oracle.attention(q, k, v, 0.3, True)
+    q, k, v = qkv_bf16(1, 2, 2, 8, 8, seed=9)
+    with pytest.raises(ValueError):
+        oracle.attention(q, k, v, 0.3, True, rows=np.array([16], np.int64))
+    with pytest.raises(TypeError):
+        oracle.attention(q.astype(np.float32), k, v, 0.3, True)
+
+
+def test_oracle_snapshot_small_workload():
+    """Seeded inputs + oracle reproduce the committed snapshot on this host."""
+    import os
+    from causal_scaled_dot_gb300.inputs import qkv_bf16
+    from causal_scaled_dot_gb300.workloads import SMALL as w
+    path = os.path.join(os.path.dirname(__file__), "golden", "oracle_small_rows.txt")
+    rows, lse_ref, out_ref = [], [], []
+    for line in open(path):
+        if line.startswith("#"):
+            continue
+        f = line.split()
+        rows.append(int(f[0])); lse_ref.append(float(f[1])); out_ref.append([float(x) for x in f[2:]])
+    q, k, v = qkv_bf16(w.B, w.Hq, w.Hkv, w.S, w.D, seed=w.seed, sigma=w.sigma)
+    out, lse = oracle.attention(q, k, v, w.scale, w.causal, rows=np.array(rows, np.int64))
+    out_ref = np.array(out_ref)
+    np.testing.assert_allclose(lse, lse_ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(out[:, :out_ref.shape[1]], out_ref, rtol=0, atol=1e-12)
