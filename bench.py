@@ -1,0 +1,355 @@
+"""Benchmark: causal attention forward TFLOP/s on one GB300 (per rank), with
+the roofline fraction, an end-to-end figure from host buffers, and the fp64
+CPU oracle timed on the host as a reported baseline.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...     # the oracle alone, on host cores
+
+A step is one attn_fwd call over the whole workload (all query rows of every
+batch and head).  FLOPs per step = 4*B*Hq*S^2*D / 2 (causal).  Between timed
+steps a 256 MiB buffer is written to flush L2; each step is timed with CUDA
+events on the launching stream.  Under torchrun every rank runs the same
+workload on its own GPU (independent problems, no collective on the data
+path); rank 0 prints one JSON line with the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from causal_scaled_dot_gb300.workloads import BY_NAME, HEADLINE  # noqa: E402
+
+METRIC = "causal attn fwd TFLOP/s (bf16, 1xGB300) and % of dense bf16 tensor peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    csrc = os.path.join(ROOT, "causal_scaled_dot_gb300", "csrc")
+    h = hashlib.sha256()
+    for fn in sorted(os.listdir(csrc)):
+        if fn.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, fn), "rb") as f:
+                h.update(fn.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources; otherwise None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    want = kernel_source_hash()
+    for line in open(path):
+        f = line.split()
+        if len(f) >= 3 and not line.startswith("#") and f[0] == want and f[1] == workload:
+            return float(f[2])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.15)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+        return False
+
+    def summary(self):
+        rows = [r for r in csv.reader(io.StringIO(self.out or "")) if len(r) >= 9]
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.strip() == "Active"})
+        loaded = [s for s in sm if mx and s > 0.5 * max(mx)] or sm
+        return {"sm_mhz": float(np.median(loaded)) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def dist_init(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "gloo" if args.impl == "reference" else "nccl"
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def reduce_max(value: float, world: int) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# --------------------------------------------------------------------- oracle
+def time_oracle(w, budget_s: float, seed: int = 0):
+    """The fp64 oracle as it stands, on all host cores, over a bounded random
+    sample of the workload's query rows; returns (TFLOP/s, rows, seconds, threads).
+
+    Each query row of a causal workload carries 2*S*D of the metric's FLOPs on
+    average (4*B*Hq*S^2*D/2 spread over B*Hq*S rows), so the sample's FLOPs are
+    rows * 2*S*D and the figure is comparable with the GPU's TFLOP/s.
+    """
+    import oracle
+    from causal_scaled_dot_gb300.inputs import qkv_bf16
+    q, k, v = qkv_bf16(w.B, w.Hq, w.Hkv, w.S, w.D, seed=w.seed, sigma=w.sigma)
+    nthreads = oracle.default_threads()
+    rng = np.random.default_rng(seed)
+    total = w.B * w.Hq * w.S
+    n = max(nthreads, 64)
+    oracle.attention(q, k, v, w.scale, w.causal, rows=rng.integers(0, total, n), nthreads=nthreads)
+    t0 = time.perf_counter()
+    oracle.attention(q, k, v, w.scale, w.causal, rows=rng.integers(0, total, n), nthreads=nthreads)
+    per_row = (time.perf_counter() - t0) / n
+    n = int(min(total, max(n, budget_s / max(per_row, 1e-9))))
+    rows = rng.integers(0, total, n)
+    t0 = time.perf_counter()
+    oracle.attention(q, k, v, w.scale, w.causal, rows=rows, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    per_row_flops = (2.0 if w.causal else 4.0) * w.S * w.D
+    return n * per_row_flops / dt / 1e12, n, dt, nthreads
+
+
+def run_reference(args, w, rank, world):
+    if rank != 0:
+        return 0
+    times, rows_per_step, threads = [], 0, 1
+    for _ in range(args.warmup):
+        time_oracle(w, budget_s=args.ref_step_seconds / 4)
+    for s in range(args.steps):
+        tf, n, dt, threads = time_oracle(w, budget_s=args.ref_step_seconds, seed=s + 1)
+        times.append((tf, n, dt))
+    value = float(np.mean([t[0] for t in times]))
+    rows_per_step = int(np.mean([t[1] for t in times]))
+    ms = float(np.mean([t[2] for t in times])) * 1e3
+    sample = (f"{rows_per_step} random query rows of {w.name} per step "
+              f"(of {w.B * w.Hq * w.S}); fp64 C oracle, {threads} threads")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) bf16)",
+        "config": {"workload": w.name, **w.shape_dict, "causal": w.causal},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------- ours
+def run_ours(args, w, rank, world, local):
+    import torch
+    from causal_scaled_dot_gb300 import native
+    from causal_scaled_dot_gb300.inputs import qkv_bf16
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    native.load()
+    q_bits, k_bits, v_bits = qkv_bf16(w.B, w.Hq, w.Hkv, w.S, w.D, seed=w.seed, sigma=w.sigma)
+
+    def host_pinned(bits):
+        return torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).pin_memory()
+
+    qh, kh, vh = host_pinned(q_bits), host_pinned(k_bits), host_pinned(v_bits)
+    q, k, v = qh.to(dev), kh.to(dev), vh.to(dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq, w.S), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        native.attn_fwd(q, k, v, out, lse, w.B, w.Hq, w.Hkv, w.S, w.D, w.scale, w.causal, stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize(dev)
+    native.attn_sync_status(stream)
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    launches = 0
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            starts[i].record(stream)
+            step()
+            launches += 1
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - wall0
+    barrier(world)
+    native.attn_sync_status(stream)
+    per_step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms_local = float(np.mean(per_step_ms))
+    ms = reduce_max(ms_local, world)
+    value = world * w.flops / (ms * 1e-3) / 1e12
+
+    # End to end: pinned host buffers -> device, attn_fwd, O and LSE back to host.
+    out_h = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        q.copy_(qh, non_blocking=True)
+        k.copy_(kh, non_blocking=True)
+        v.copy_(vh, non_blocking=True)
+        step()
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = reduce_max(e0.elapsed_time(e1) / e2e_steps, world)
+    h2d = (qh.numel() + kh.numel() + vh.numel()) * 2
+    d2h = out_h.numel() * 2 + lse_h.numel() * 4
+
+    if rank != 0:
+        return 0
+    peaks, peak_src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    achieved = w.flops / (ms_local * 1e-3) / 1e12
+    traffic = recorded_traffic(w.name)
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        tf, n, dt, threads = time_oracle(w, budget_s=args.cpu_seconds)
+        cpu = {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": f"{n} random query rows of {w.name} (of {w.B * w.Hq * w.S}), "
+                         f"{dt:.1f} s; fp64 C oracle"}
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16, no weights)",
+        "config": {"workload": w.name, **w.shape_dict, "causal": w.causal,
+                   "l2": "flushed between timed steps (256 MiB write)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "pct_of_peak": 100.0 * achieved / peak,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_src} bf16 dense (burst)",
+                     "hbm_gbs": w.io_bytes / (ms_local * 1e-3) / 1e9},
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * w.flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+        "wall_s_timed_region": wall,
+        "kernel_sources": kernel_source_hash(),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=HEADLINE.name, choices=sorted(BY_NAME))
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="budget of the oracle CPU-baseline sample")
+    ap.add_argument("--ref-step-seconds", type=float, default=8.0,
+                    help="--impl reference: oracle seconds per step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    w = BY_NAME[args.workload]
+    rank, world, local = dist_init(args)
+    if world != args.gpus and rank == 0:
+        print(f"note: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
+    try:
+        if args.impl == "reference":
+            rc = run_reference(args, w, rank, world)
+        else:
+            rc = run_ours(args, w, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+    return rc
+
+
+if __name__ == "__main__":
+    sys.exit(main())

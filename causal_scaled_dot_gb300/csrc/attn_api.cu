@@ -1,0 +1,234 @@
+// attn_api.cu -- the C ABI of libattn (include/attn.h): argument checks, TMA
+// descriptor encoding and caching, per-device setup, kernel launch, and the
+// device status word that bounded waits report timeouts through.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/attn.h"
+#include "common.cuh"
+#include "kernel_simple.cuh"
+
+// Status word: bits set by device-side waits that ran out (ptx::kStatusTimeout).
+__device__ unsigned int g_attn_status;
+
+namespace attn {
+namespace {
+
+constexpr int kVersion = 100;                       // 0.1.0
+constexpr unsigned long long kWaitLimitNs = 4000000000ull;  // 4 s per wait
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    bool ready = false;
+    int status = ATTN_OK;  // ATTN_OK, or why this device cannot run the kernels
+    int sm_count = 0;
+    unsigned int* status_word = nullptr;
+};
+
+std::mutex g_mutex;
+DeviceState g_devices[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+template <typename K>
+cudaError_t allow_smem(K kernel, uint32_t bytes) {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+// Per-device setup, once: capability check, SM count, status-word address,
+// shared-memory opt-in for every kernel.  Caller holds g_mutex.
+int setup_device_locked(int dev) {
+    DeviceState& st = g_devices[dev];
+    if (st.ready) return st.status;
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return ATTN_ERR_DEVICE;  // not cached: may be transient
+    st.ready = true;
+    if (major != 10 || minor != 3) {
+        st.status = ATTN_ERR_UNSUPPORTED;
+        return st.status;
+    }
+    st.sm_count = sms;
+    void* word = nullptr;
+    if (cudaGetSymbolAddress(&word, g_attn_status) != cudaSuccess ||
+        allow_smem(attn_fwd_simple_kernel<64>, SimpleLayout<64>::kDynamicSmem) != cudaSuccess ||
+        allow_smem(attn_fwd_simple_kernel<128>, SimpleLayout<128>::kDynamicSmem) != cudaSuccess) {
+        st.status = ATTN_ERR_DEVICE;
+        return st.status;
+    }
+    st.status_word = static_cast<unsigned int*>(word);
+    if (g_encode == nullptr) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || fn == nullptr) {
+            st.status = ATTN_ERR_DEVICE;
+            return st.status;
+        }
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    st.status = ATTN_OK;
+    return st.status;
+}
+
+int current_device_state(DeviceState** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_DEVICE;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    const int rc = setup_device_locked(dev);
+    *out = &g_devices[dev];
+    return rc;
+}
+
+// Rank-3 view [rows_outer, S, D] of a contiguous bf16 [.., S, D] tensor, box
+// {64, box_rows, 1}, 128-byte swizzle: one box fills box_rows rows of 128 bytes,
+// the canonical K-major (and MN-major) SW128 operand layout.  Rows past S read
+// as zero.
+int encode_bf16_3d(CUtensorMap* map, const void* ptr, int D, int S, long long outer, int box_rows) {
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)outer};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)S * (cuuint64_t)D * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+    cuuint32_t elem[3] = {1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims,
+                          strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_INVALID_ARG;
+}
+
+bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+int check_args(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
+               int Hkv, int S, int D, float scale) {
+    if (!q || !k || !v || !out) return ATTN_ERR_INVALID_ARG;
+    if (B < 1 || Hq < 1 || Hkv < 1 || S < 1) return ATTN_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+    // Sizes that the 32-bit TMA coordinates and grid dimensions can address.
+    if ((long long)B * Hq > (1ll << 30) || S > (1 << 30)) return ATTN_ERR_UNSUPPORTED;
+    const uintptr_t mis = (reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                           reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out)) & 15u;
+    if (mis || (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_MISALIGNED;
+    const size_t q_bytes = (size_t)B * Hq * S * D * 2, kv_bytes = (size_t)B * Hkv * S * D * 2;
+    if (ranges_overlap(out, q_bytes, q, q_bytes) || ranges_overlap(out, q_bytes, k, kv_bytes) ||
+        ranges_overlap(out, q_bytes, v, kv_bytes))
+        return ATTN_ERR_INVALID_ARG;
+    if (lse) {
+        const size_t l_bytes = (size_t)B * Hq * S * 4;
+        if (ranges_overlap(lse, l_bytes, out, q_bytes) || ranges_overlap(lse, l_bytes, q, q_bytes) ||
+            ranges_overlap(lse, l_bytes, k, kv_bytes) || ranges_overlap(lse, l_bytes, v, kv_bytes))
+            return ATTN_ERR_INVALID_ARG;
+    }
+    return ATTN_OK;
+}
+
+template <int D>
+int launch_simple(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                  const FwdParams& p, cudaStream_t stream) {
+    dim3 grid(p.B * p.Hq, p.num_q_tiles), block(128);
+    if (p.num_q_tiles > 65535) return ATTN_ERR_UNSUPPORTED;
+    attn_fwd_simple_kernel<D><<<grid, block, SimpleLayout<D>::kDynamicSmem, stream>>>(tq, tk, tv, p);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+__global__ void selftest_wait_kernel(unsigned long long limit_ns, unsigned int* status) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(ptx::smem_addr(&bar), 1);
+        abort_flag = 0;
+        ptx::fence_barrier_init();
+    }
+    __syncthreads();
+    // Nobody arrives on `bar`: phase 0 never completes and the wait must give up.
+    ptx::mbar_wait(ptx::smem_addr(&bar), 0, &abort_flag, status, limit_ns);
+    __syncthreads();
+    if (threadIdx.x == 0) ptx::mbar_arrive(ptx::smem_addr(&bar));  // leave the barrier balanced
+}
+
+}  // namespace
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B,
+                        int Hq, int Hkv, int S, int D, float scale, int causal, void* stream) {
+    int rc = check_args(q, k, v, out, lse, B, Hq, Hkv, S, D, scale);
+    if (rc != ATTN_OK) return rc;
+    DeviceState* dev = nullptr;
+    rc = current_device_state(&dev);
+    if (rc != ATTN_OK) return rc;
+
+    alignas(64) CUtensorMap tq, tk, tv;
+    if (encode_bf16_3d(&tq, q, D, S, (long long)B * Hq, kTile) != ATTN_OK ||
+        encode_bf16_3d(&tk, k, D, S, (long long)B * Hkv, kTile) != ATTN_OK ||
+        encode_bf16_3d(&tv, v, D, S, (long long)B * Hkv, kTile) != ATTN_OK)
+        return ATTN_ERR_INVALID_ARG;
+
+    FwdParams p;
+    std::memset(&p, 0, sizeof p);
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.S = S;
+    p.group = Hq / Hkv;
+    p.num_q_tiles = (S + kTile - 1) / kTile;
+    p.causal = causal ? 1 : 0;
+    p.scale_log2 = scale * kLog2e;
+    p.out = static_cast<__nv_bfloat16*>(out);
+    p.lse = lse;
+    p.status = dev->status_word;
+    p.wait_limit_ns = kWaitLimitNs;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return D == 64 ? launch_simple<64>(tq, tk, tv, p, st) : launch_simple<128>(tq, tk, tv, p, st);
+}
+
+extern "C" int attn_sync_status(void* stream) {
+    DeviceState* dev = nullptr;
+    int rc = current_device_state(&dev);
+    if (rc != ATTN_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return ATTN_ERR_DEVICE;
+    unsigned int word = 0, zero = 0;
+    if (cudaMemcpy(&word, dev->status_word, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemcpy(dev->status_word, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+        return ATTN_ERR_DEVICE;
+    return (word & ptx::kStatusTimeout) ? ATTN_ERR_TIMEOUT : ATTN_OK;
+}
+
+extern "C" int attn_selftest_wait_timeout(int limit_us, void* stream) {
+    if (limit_us < 1 || limit_us > 1000000) return ATTN_ERR_INVALID_ARG;
+    DeviceState* dev = nullptr;
+    int rc = current_device_state(&dev);
+    if (rc != ATTN_OK) return rc;
+    selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+        (unsigned long long)limit_us * 1000ull, dev->status_word);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+extern "C" const char* attn_status_string(int status) {
+    switch (status) {
+        case ATTN_OK: return "ATTN_OK";
+        case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG: invalid argument";
+        case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED: unsupported head_dim, size or device";
+        case ATTN_ERR_MISALIGNED: return "ATTN_ERR_MISALIGNED: pointer not 16-byte aligned";
+        case ATTN_ERR_DEVICE: return "ATTN_ERR_DEVICE: CUDA device query failed";
+        case ATTN_ERR_LAUNCH: return "ATTN_ERR_LAUNCH: kernel launch failed";
+        case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT: a device-side wait ran out";
+        default: return "unknown attn status";
+    }
+}
+
+extern "C" int attn_version(void) { return kVersion; }

@@ -1,0 +1,151 @@
+"""ctypes binding of libattn (include/attn.h): argument marshalling only.
+
+Every step of the attention forward runs in the CUDA library; this module
+turns PyTorch tensors (or raw integers) into the pointers, sizes and stream
+handle the C ABI takes, and turns return codes into exceptions.  There is no
+CPU path: if the library cannot be built or loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import threading
+
+from . import build as _build
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = 1
+ATTN_ERR_UNSUPPORTED = 2
+ATTN_ERR_MISALIGNED = 3
+ATTN_ERR_DEVICE = 4
+ATTN_ERR_LAUNCH = 5
+ATTN_ERR_TIMEOUT = 6
+
+_lock = threading.Lock()
+_lib: ctypes.CDLL | None = None
+
+
+class AttnError(RuntimeError):
+    """A non-zero return code from libattn."""
+
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {attn_status_string(code)} (code {code})")
+
+
+def load() -> ctypes.CDLL:
+    """Build libattn.so if it is missing or older than its sources, then load it."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.build()  # raises if nvcc fails: no fallback
+        lib = ctypes.CDLL(path)
+        vp, ci = ctypes.c_void_p, ctypes.c_int
+        lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ctypes.c_float, ci, vp]
+        lib.attn_fwd.restype = ci
+        lib.attn_sync_status.argtypes = [vp]
+        lib.attn_sync_status.restype = ci
+        lib.attn_selftest_wait_timeout.argtypes = [ci, vp]
+        lib.attn_selftest_wait_timeout.restype = ci
+        lib.attn_status_string.argtypes = [ci]
+        lib.attn_status_string.restype = ctypes.c_char_p
+        lib.attn_version.argtypes = []
+        lib.attn_version.restype = ci
+        _lib = lib
+        return lib
+
+
+def library_path() -> str:
+    return _build.LIBRARY
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    import torch
+    if isinstance(x, torch.Tensor):
+        if not x.is_cuda:
+            raise ValueError("tensor arguments must live in CUDA device memory")
+        return x.data_ptr()
+    raise TypeError(f"expected a CUDA tensor, an int pointer or None, got {type(x)!r}")
+
+
+def _stream(s):
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    handle = getattr(s, "cuda_stream", None)
+    if handle is None:
+        raise TypeError(f"expected a torch.cuda.Stream, an int handle or None, got {type(s)!r}")
+    return handle
+
+
+def attn_fwd(q, k, v, out, lse, B: int, Hq: int, Hkv: int, S: int, D: int, scale: float,
+             causal: bool | int, stream=None, check: bool = True) -> int:
+    """The C entry point ``attn_fwd`` with the same argument order.
+
+    Tensors may be CUDA tensors (their data pointers are passed) or raw device
+    pointers as ints; ``lse`` may be None.  ``stream`` defaults to PyTorch's
+    current stream.  Raises AttnError on a non-zero code unless check=False.
+    """
+    rc = load().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), int(B), int(Hq),
+                         int(Hkv), int(S), int(D), float(scale), 1 if causal else 0,
+                         _stream(stream))
+    if check and rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd")
+    return rc
+
+
+def attn_sync_status(stream=None, check: bool = True) -> int:
+    rc = load().attn_sync_status(_stream(stream))
+    if check and rc != ATTN_OK:
+        raise AttnError(rc, "attn_sync_status")
+    return rc
+
+
+def attn_selftest_wait_timeout(limit_us: int, stream=None) -> int:
+    return load().attn_selftest_wait_timeout(int(limit_us), _stream(stream))
+
+
+def attn_status_string(code: int) -> str:
+    try:
+        return load().attn_status_string(int(code)).decode()
+    except Exception:  # pragma: no cover - message of last resort
+        return f"status {code}"
+
+
+def attn_version() -> int:
+    return load().attn_version()
+
+
+def attention(q, k, v, causal: bool = True, scale: float | None = None, out=None, lse=None,
+              return_lse: bool = True, stream=None):
+    """O (and LSE) for CUDA tensors q [B,Hq,S,D], k/v [B,Hkv,S,D] in bf16.
+
+    Allocates ``out`` (bf16 [B,Hq,S,D]) and ``lse`` (fp32 [B,Hq,S]) with
+    PyTorch when they are not given, checks dtypes, shapes and contiguity, and
+    calls ``attn_fwd`` on ``stream`` (default: the current stream).
+    """
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.bfloat16:
+            raise ValueError(f"{name} must be a bf16 CUDA tensor")
+        if t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous [B,H,S,D] tensor")
+    B, Hq, S, D = q.shape
+    Bk, Hkv, Sk, Dk = k.shape
+    if tuple(v.shape) != tuple(k.shape) or (Bk, Sk, Dk) != (B, S, D):
+        raise ValueError("q [B,Hq,S,D] and k, v [B,Hkv,S,D] disagree")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
+    attn_fwd(q, k, v, out, lse, B, Hq, Hkv, S, D, scale, causal, stream)
+    return (out, lse) if return_lse else out

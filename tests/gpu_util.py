@@ -1,0 +1,67 @@
+"""Helpers for the GPU parity tests: move seeded bf16 bits to the device, run
+libattn through its C ABI, and compare with the fp64 oracle."""
+from __future__ import annotations
+
+import numpy as np
+
+# Tolerances on bf16 O against the fp64 oracle, and on fp32 LSE.
+TOL_O_MAX_ABS = 2e-2
+TOL_O_REL_L2 = 5e-3
+TOL_LSE_MAX_ABS = 1e-3
+
+
+def to_device(bits: np.ndarray):
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16).copy())
+    return t.view(torch.bfloat16).cuda()
+
+
+def bits_of(t) -> np.ndarray:
+    import torch
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def run_gpu(q_bits, k_bits, v_bits, scale, causal, with_lse=True, stream=None):
+    """attn_fwd through the C ABI; returns (O float64, LSE float64 or None, O bf16 bits)."""
+    import torch
+    from causal_scaled_dot_gb300 import native
+    B, Hq, S, D = q_bits.shape
+    Hkv = k_bits.shape[1]
+    q, k, v = to_device(q_bits), to_device(k_bits), to_device(v_bits)
+    out = torch.full_like(q, float("nan"))  # unwritten rows would stay NaN
+    lse = torch.full((B, Hq, S), float("nan"), dtype=torch.float32, device="cuda") if with_lse else None
+    native.attn_fwd(q, k, v, out, lse, B, Hq, Hkv, S, D, scale, causal, stream=stream)
+    native.attn_sync_status(stream)
+    o = out.double().cpu().numpy()
+    l = lse.double().cpu().numpy() if with_lse else None
+    return o, l, bits_of(out)
+
+
+def compare(o_gpu, o_ref, l_gpu, l_ref, label=""):
+    """Assert the parity bar; returns the error figures."""
+    assert np.all(np.isfinite(o_gpu)), f"{label}: non-finite output (unwritten rows?)"
+    diff = o_gpu - o_ref
+    max_abs = float(np.max(np.abs(diff))) if diff.size else 0.0
+    ref_norm = float(np.linalg.norm(o_ref))
+    rel_l2 = float(np.linalg.norm(diff) / ref_norm) if ref_norm > 0 else float(np.linalg.norm(diff))
+    stats = {"max_abs": max_abs, "rel_l2": rel_l2}
+    assert max_abs <= TOL_O_MAX_ABS, f"{label}: O max abs error {max_abs:.3e} > {TOL_O_MAX_ABS}"
+    assert rel_l2 <= TOL_O_REL_L2, f"{label}: O rel L2 error {rel_l2:.3e} > {TOL_O_REL_L2}"
+    if l_gpu is not None:
+        assert np.all(np.isfinite(l_gpu)), f"{label}: non-finite LSE"
+        lse_err = float(np.max(np.abs(l_gpu - l_ref))) if l_gpu.size else 0.0
+        stats["lse_max_abs"] = lse_err
+        assert lse_err <= TOL_LSE_MAX_ABS, f"{label}: LSE max abs error {lse_err:.3e} > {TOL_LSE_MAX_ABS}"
+    return stats
+
+
+def sample_rows(B, Hq, S, n_random=256, seed=0):
+    """Flat row ids covering both ends of the sequence, tile edges and random rows."""
+    rng = np.random.default_rng(seed)
+    heads = {(0, 0), (B - 1, Hq - 1), (0, Hq - 1), (B - 1, 0)}
+    for _ in range(4):
+        heads.add((int(rng.integers(B)), int(rng.integers(Hq))))
+    positions = {0, 1, 2, 127, 128, 129, 255, 256, S // 2, S - 129, S - 128, S - 127, S - 2, S - 1}
+    rows = {(b * Hq + h) * S + i for (b, h) in heads for i in positions if 0 <= i < S}
+    rows |= set(int(x) for x in rng.integers(0, B * Hq * S, size=n_random))
+    return np.array(sorted(rows), dtype=np.int64)

@@ -1,0 +1,102 @@
+"""The C-ABI library builds, loads and exports every declared symbol; argument
+errors are reported before any device work (no GPU needed)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from causal_scaled_dot_gb300 import native
+from causal_scaled_dot_gb300.native import (ATTN_ERR_INVALID_ARG, ATTN_ERR_MISALIGNED,
+                                            ATTN_ERR_UNSUPPORTED)
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?\w+\s*\**\s*(attn_\w+)\s*\(", text, flags=re.M)
+    return names
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for required in ("attn_fwd", "attn_status_string", "attn_sync_status"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = native.load()
+    for name in declared_functions():
+        assert hasattr(lib, name), f"libattn.so does not export {name}"
+    out = subprocess.run(["nm", "-D", "--defined-only", native.library_path()],
+                         capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\b(attn_\w+)\b", out))
+    assert set(declared_functions()) <= exported
+
+
+def test_status_strings_and_version():
+    for code in range(7):
+        assert native.attn_status_string(code).startswith("ATTN_")
+    assert "unknown" in native.attn_status_string(99)
+    assert native.attn_version() >= 100
+
+
+def _call(q=16, k=32, v=48, out=64, lse=None, B=1, Hq=2, Hkv=2, S=128, D=128, scale=0.1,
+          causal=1):
+    lib = native.load()
+    return lib.attn_fwd(q, k, v, out, lse, B, Hq, Hkv, S, D, ctypes.c_float(scale), causal, None)
+
+
+# Fake, never-dereferenced pointer values far apart so they do not overlap.
+P = dict(q=1 << 40, k=2 << 40, v=3 << 40, out=4 << 40)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), ATTN_ERR_INVALID_ARG),
+    (dict(k=None), ATTN_ERR_INVALID_ARG),
+    (dict(v=None), ATTN_ERR_INVALID_ARG),
+    (dict(out=None), ATTN_ERR_INVALID_ARG),
+    (dict(B=0), ATTN_ERR_INVALID_ARG),
+    (dict(Hq=0), ATTN_ERR_INVALID_ARG),
+    (dict(Hkv=0), ATTN_ERR_INVALID_ARG),
+    (dict(S=0), ATTN_ERR_INVALID_ARG),
+    (dict(S=-5), ATTN_ERR_INVALID_ARG),
+    (dict(Hq=6, Hkv=4), ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), ATTN_ERR_INVALID_ARG),
+    (dict(scale=-0.1), ATTN_ERR_INVALID_ARG),
+    (dict(scale=0.0), ATTN_ERR_INVALID_ARG),
+    (dict(D=96), ATTN_ERR_UNSUPPORTED),
+    (dict(D=256), ATTN_ERR_UNSUPPORTED),
+    (dict(q=(1 << 40) + 8), ATTN_ERR_MISALIGNED),
+    (dict(out=(4 << 40) + 2), ATTN_ERR_MISALIGNED),
+    (dict(lse=(5 << 40) + 2), ATTN_ERR_MISALIGNED),
+    (dict(out=1 << 40), ATTN_ERR_INVALID_ARG),            # out aliases q
+    (dict(out=(2 << 40) + 4096), ATTN_ERR_INVALID_ARG),   # out overlaps k
+    (dict(lse=(4 << 40) + 1024), ATTN_ERR_INVALID_ARG),   # lse overlaps out
+])
+def test_argument_errors_are_rejected_before_launch(kw, code):
+    args = dict(P)
+    args.update(kw)
+    assert _call(**args) == code
+
+
+def test_python_binding_rejects_host_tensors():
+    import torch
+    q = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        native.attn_fwd(q, q, q, q, None, 1, 1, 1, 8, 64, 0.125, True, stream=0)
+    with pytest.raises(ValueError):
+        native.attention(q, q, q)
+
+
+def test_selftest_rejects_bad_limits():
+    lib = native.load()
+    assert lib.attn_selftest_wait_timeout(0, None) == ATTN_ERR_INVALID_ARG
+    assert lib.attn_selftest_wait_timeout(2000000, None) == ATTN_ERR_INVALID_ARG
