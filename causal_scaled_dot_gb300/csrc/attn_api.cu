@@ -7,12 +7,14 @@
 
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
 #include "../../include/attn.h"
 #include "common.cuh"
 #include "kernel_simple.cuh"
+#include "kernel_ws.cuh"
 
 // Status word: bits set by device-side waits that ran out (ptx::kStatusTimeout).
 __device__ unsigned int g_attn_status;
@@ -59,7 +61,9 @@ int setup_device_locked(int dev) {
     void* word = nullptr;
     if (cudaGetSymbolAddress(&word, g_attn_status) != cudaSuccess ||
         allow_smem(attn_fwd_simple_kernel<64>, SimpleLayout<64>::kDynamicSmem) != cudaSuccess ||
-        allow_smem(attn_fwd_simple_kernel<128>, SimpleLayout<128>::kDynamicSmem) != cudaSuccess) {
+        allow_smem(attn_fwd_simple_kernel<128>, SimpleLayout<128>::kDynamicSmem) != cudaSuccess ||
+        allow_smem(attn_fwd_ws_kernel<64>, WsLayout<64>::kDynamicSmem) != cudaSuccess ||
+        allow_smem(attn_fwd_ws_kernel<128>, WsLayout<128>::kDynamicSmem) != cudaSuccess) {
         st.status = ATTN_ERR_DEVICE;
         return st.status;
     }
@@ -143,6 +147,27 @@ int launch_simple(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMa
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
+template <int D>
+int launch_ws(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, FwdParams p,
+              int sm_count, cudaStream_t stream) {
+    const long long npairs = (p.num_q_tiles + 1) / 2;
+    const long long units = (long long)p.B * p.Hq * npairs;
+    if (units > (1ll << 31) - 1) return ATTN_ERR_UNSUPPORTED;
+    p.num_units = (int)units;
+    const int grid = (int)(units < sm_count ? units : sm_count);
+    attn_fwd_ws_kernel<D><<<grid, WsLayout<D>::kThreads, WsLayout<D>::kDynamicSmem, stream>>>(tq, tk,
+                                                                                           tv, p);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+// Kernel choice: the warp-specialised persistent kernel unless the environment
+// variable ATTN_FWD_KERNEL=simple selects the one-tile-per-CTA kernel (kept as
+// an independently scheduled implementation for cross-checks).
+bool use_simple_kernel() {
+    const char* v = std::getenv("ATTN_FWD_KERNEL");
+    return v != nullptr && std::strcmp(v, "simple") == 0;
+}
+
 __global__ void selftest_wait_kernel(unsigned long long limit_ns, unsigned int* status) {
     __shared__ __align__(8) uint64_t bar;
     __shared__ int abort_flag;
@@ -192,7 +217,10 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* out, 
     p.status = dev->status_word;
     p.wait_limit_ns = kWaitLimitNs;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    return D == 64 ? launch_simple<64>(tq, tk, tv, p, st) : launch_simple<128>(tq, tk, tv, p, st);
+    if (use_simple_kernel())
+        return D == 64 ? launch_simple<64>(tq, tk, tv, p, st) : launch_simple<128>(tq, tk, tv, p, st);
+    return D == 64 ? launch_ws<64>(tq, tk, tv, p, dev->sm_count, st)
+                   : launch_ws<128>(tq, tk, tv, p, dev->sm_count, st);
 }
 
 extern "C" int attn_sync_status(void* stream) {

@@ -1,0 +1,474 @@
+// kernel_ws.cuh -- warp-specialised, persistent attention forward for sm_103a.
+//
+// Work unit: one (batch, query head) and a pair of adjacent 128-row query
+// tiles (2m, 2m+1).  One CTA per SM loops over units, heaviest causal units
+// first (pair index descending), query heads that share a key/value head next
+// to each other so their K/V tiles are reused from L2.
+//
+// Roles (384 threads, 12 warps):
+//   warp 0      TMA producer: Q tiles of the unit, then K_j, V_j into a ring
+//               of single-tile shared-memory slots.
+//   warp 1      MMA issuer (one thread) and TMEM owner: S_i = Q_i K_j^T
+//               (both operands in shared memory) and O_i += P_i V_j (P read
+//               from tensor memory).
+//   warps 2-3   idle.
+//   warps 4-7   softmax warpgroup 0: one thread per row of query tile 2m.
+//   warps 8-11  softmax warpgroup 1: one thread per row of query tile 2m+1.
+// The two warpgroups ping-pong: while one runs its softmax the tensor core
+// computes the other's products.
+//
+// Tensor memory (512 columns x 128 lanes, fp32): S_0 [0,128), S_1 [128,256),
+// O_0 [256, 256+D), O_1 [256+D, 256+2D).  P_i (bf16, two per column) is written
+// over the upper half of S_i, columns [64,128) of it, after S_i has been read.
+//
+// Online softmax: the running maximum m (in log2 units, scale*log2(e)*s) is
+// raised only when a tile's maximum exceeds it by more than kRescaleSlack;
+// otherwise probabilities up to 2^kRescaleSlack are kept against the stale
+// m.  O and l are always relative to the same m, so the final O / l and
+// LSE = (m + log2 l) ln 2 are unaffected; O is rescaled in TMEM only when m
+// actually moves.  When S_i(j) is observed complete, every earlier MMA of the
+// issuing thread -- in particular O_i += P_i(j-1) V_{j-1} -- has completed
+// too (tcgen05.commit tracks all prior operations), so the softmax thread may
+// rescale O_i then without a further barrier.
+//
+// The steps are those of the naive causal attention in the "Profiling in
+// PyTorch (Part 3)" retelling (section "Naive Attention": QK^T, scale,
+// causal -inf mask, softmax, times V), fused with the tiled online softmax
+// that the same retelling describes for FlashAttention-2 ("The Flash
+// Backend"); key tiles entirely after a query tile are never loaded, and
+// only diagonal tiles are masked.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace attn {
+
+constexpr float kRescaleSlack = 8.0f;  // log2 units: probabilities stay <= 256
+
+template <int D>
+struct WsLayout {
+    static constexpr int kThreads = 384;
+    static constexpr int kStages = (D == 128) ? 4 : 8;     // K/V ring slots, one tile each
+    static constexpr uint32_t kTileBytes = kTile * D * 2;  // 32 KB at D = 128
+    static constexpr int kChunks = D / 64;                 // 64-column swizzle blocks
+    static constexpr uint32_t kChunkBytes = kTile * 128;   // one block of a tile: 16 KB
+    static constexpr uint32_t kQ0 = 0;
+    static constexpr uint32_t kQ1 = kTileBytes;
+    static constexpr uint32_t kRing = 2 * kTileBytes;
+    static constexpr uint32_t kBars = kRing + kStages * kTileBytes;
+    // mbarrier indices
+    static constexpr int kQFull = 0, kQEmpty = 2, kSFull = 4, kPFull = 6, kOFull = 8;
+    static constexpr int kKVFull = 10, kKVEmpty = 10 + kStages, kDrain = 10 + 2 * kStages;
+    static constexpr int kNumBars = kDrain + 1;
+    static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8;
+    static constexpr uint32_t kAbort = kTmemSlot + 4;
+    static constexpr uint32_t kBytes = kAbort + 4;
+    static constexpr uint32_t kDynamicSmem = kBytes + 1024;  // slack for 1024-byte alignment
+    static constexpr uint32_t kTmemCols = 512;
+    static_assert(kDynamicSmem <= 227 * 1024, "shared memory budget");
+};
+
+// Unit u -> (bh, pair m).  Causal: heaviest pairs first.  Within a pair index
+// consecutive u walk bh = b*Hq + hq, so GQA siblings are adjacent.
+struct Unit {
+    int bh, m, kv_bh, n0, n1, n;
+};
+__device__ __forceinline__ Unit decode_unit(int u, const FwdParams& p) {
+    const int BH = p.B * p.Hq;
+    const int npairs = (p.num_q_tiles + 1) >> 1;
+    Unit w;
+    w.m = npairs - 1 - u / BH;
+    w.bh = u - (u / BH) * BH;
+    const int b = w.bh / p.Hq;
+    const int hq = w.bh - b * p.Hq;
+    w.kv_bh = b * p.Hkv + hq / p.group;
+    const int qt0 = 2 * w.m, qt1 = 2 * w.m + 1;
+    if (p.causal) {
+        w.n0 = min(qt0 + 1, p.num_q_tiles);
+        w.n1 = min(qt1 + 1, p.num_q_tiles);
+    } else {
+        w.n0 = w.n1 = p.num_q_tiles;
+    }
+    w.n = max(w.n0, w.n1);
+    return w;
+}
+
+template <int D>
+__device__ __forceinline__ uint32_t ws_bar(uint32_t base, int i) {
+    return base + WsLayout<D>::kBars + 8u * (uint32_t)i;
+}
+
+// ---------------------------------------------------------------- producer
+template <int D>
+__device__ void ws_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
+                             const CUtensorMap* tm_v, const FwdParams& p, uint32_t base,
+                             volatile int* abort_flag) {
+    using L = WsLayout<D>;
+    uint32_t qe_phase[2] = {0u, 0u};
+    int slot = 0;
+    uint32_t ring_phase = 0;
+    // Loads issued and possibly not yet landed, for the drain after an abort.
+    uint32_t pend_kv = 0, pend_kv_par = 0, pend_q = 0, pend_q_par = 0;
+    const uint64_t lim = p.wait_limit_ns;
+    for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+        const Unit w = decode_unit(u, p);
+        for (int i = 0; i < 2; ++i) {
+            if (!ptx::mbar_wait(ws_bar<D>(base, L::kQEmpty + i), qe_phase[i] ^ 1u, abort_flag,
+                                p.status, lim))
+                goto drain;
+            qe_phase[i] ^= 1u;
+            const uint32_t full = ws_bar<D>(base, L::kQFull + i);
+            ptx::mbar_arrive_expect_tx(full, L::kTileBytes);
+            const uint32_t dst = base + (i == 0 ? L::kQ0 : L::kQ1);
+#pragma unroll
+            for (int c = 0; c < L::kChunks; ++c)
+                ptx::tma_load_3d(dst + c * L::kChunkBytes, tm_q, full, c * 64, (2 * w.m + i) * kTile,
+                                 w.bh);
+            pend_q |= 1u << i;
+            pend_q_par = (pend_q_par & ~(1u << i)) | (((qe_phase[i] ^ 1u) & 1u) << i);
+        }
+        for (int j = 0; j < w.n; ++j) {
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {  // t = 0: K_j, t = 1: V_j
+                if (!ptx::mbar_wait(ws_bar<D>(base, L::kKVEmpty + slot), ring_phase ^ 1u, abort_flag,
+                                    p.status, lim))
+                    goto drain;
+                const uint32_t full = ws_bar<D>(base, L::kKVFull + slot);
+                ptx::mbar_arrive_expect_tx(full, L::kTileBytes);
+                const uint32_t dst = base + L::kRing + (uint32_t)slot * L::kTileBytes;
+                const CUtensorMap* map = t == 0 ? tm_k : tm_v;
+#pragma unroll
+                for (int c = 0; c < L::kChunks; ++c)
+                    ptx::tma_load_3d(dst + c * L::kChunkBytes, map, full, c * 64, j * kTile, w.kv_bh);
+                pend_kv |= 1u << slot;
+                pend_kv_par = (pend_kv_par & ~(1u << slot)) | (ring_phase << slot);
+                if (++slot == L::kStages) {
+                    slot = 0;
+                    ring_phase ^= 1u;
+                }
+            }
+        }
+    }
+    return;
+drain:
+    // Let every copy already issued land before the CTA can exit.
+    for (int s = 0; s < L::kStages; ++s)
+        if (pend_kv & (1u << s))
+            ptx::drain_wait(ws_bar<D>(base, L::kKVFull + s), (pend_kv_par >> s) & 1u, lim);
+    for (int i = 0; i < 2; ++i)
+        if (pend_q & (1u << i))
+            ptx::drain_wait(ws_bar<D>(base, L::kQFull + i), ((pend_q_par >> i) & 1u) ^ 0u, lim);
+}
+
+// ---------------------------------------------------------------- MMA issuer
+template <int D>
+__device__ void ws_mma_role(const FwdParams& p, uint32_t base, uint32_t tmem,
+                            volatile int* abort_flag) {
+    using L = WsLayout<D>;
+    constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(kTile, kTile, false);
+    constexpr uint32_t kIdescO = ptx::idesc_bf16_f32(kTile, D, true);
+    const uint64_t lim = p.wait_limit_ns;
+    uint32_t qf_phase = 0;
+    uint32_t pf_phase[2] = {0u, 0u};
+    int slot = 0;
+    uint32_t ring_phase = 0;
+
+    // S_i = Q_i K^T with K in ring slot `ks`.
+    auto issue_s = [&](int i, int ks) {
+        const uint32_t q = base + (i == 0 ? L::kQ0 : L::kQ1);
+        const uint32_t k = base + L::kRing + (uint32_t)ks * L::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * L::kChunkBytes + (kk & 3) * 32;
+            ptx::mma_ss(tmem + (uint32_t)i * kTile, ptx::sdesc_sw128(q + off, 16, 1024),
+                        ptx::sdesc_sw128(k + off, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
+        }
+        ptx::mma_commit(ws_bar<D>(base, L::kSFull + i));
+    };
+    // O_i (+)= P_i V with P_i in TMEM columns [64,128) of S_i and V in slot `vs`.
+    auto issue_pv = [&](int i, int vs, bool accumulate) {
+        const uint32_t v = base + L::kRing + (uint32_t)vs * L::kTileBytes;
+        const uint32_t o = tmem + 256u + (uint32_t)i * D;
+        const uint32_t pcol = tmem + (uint32_t)i * kTile + 64u;
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+            ptx::mma_ts(o, pcol + kk * 8, ptx::sdesc_sw128(v + kk * 16 * 128, L::kChunkBytes, 1024),
+                        kIdescO, (accumulate || kk > 0) ? 1u : 0u);
+    };
+    auto wait_ring = [&](int& got) -> bool {
+        if (!ptx::mbar_wait(ws_bar<D>(base, L::kKVFull + slot), ring_phase, abort_flag, p.status, lim))
+            return false;
+        got = slot;
+        if (++slot == L::kStages) {
+            slot = 0;
+            ring_phase ^= 1u;
+        }
+        ptx::tc_fence_after();
+        return true;
+    };
+    auto wait_p = [&](int i) -> bool {
+        if (!ptx::mbar_wait(ws_bar<D>(base, L::kPFull + i), pf_phase[i], abort_flag, p.status, lim))
+            return false;
+        pf_phase[i] ^= 1u;
+        ptx::tc_fence_after();
+        return true;
+    };
+
+    for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+        const Unit w = decode_unit(u, p);
+        if (!ptx::mbar_wait(ws_bar<D>(base, L::kQFull + 0), qf_phase, abort_flag, p.status, lim) ||
+            !ptx::mbar_wait(ws_bar<D>(base, L::kQFull + 1), qf_phase, abort_flag, p.status, lim))
+            break;
+        qf_phase ^= 1u;
+        int kslot, vslot;
+        if (!wait_ring(kslot)) break;
+        issue_s(0, kslot);
+        if (w.n0 == 1) ptx::mma_commit(ws_bar<D>(base, L::kQEmpty + 0));
+        issue_s(1, kslot);
+        if (w.n1 == 1) ptx::mma_commit(ws_bar<D>(base, L::kQEmpty + 1));
+        ptx::mma_commit(ws_bar<D>(base, L::kKVEmpty + kslot));
+        bool ok = true;
+        for (int j = 0; j < w.n && ok; ++j) {
+            if (!(ok = wait_ring(vslot))) break;
+            if (j < w.n0) {
+                if (!(ok = wait_p(0))) break;
+                issue_pv(0, vslot, j > 0);
+                if (j == w.n0 - 1) ptx::mma_commit(ws_bar<D>(base, L::kOFull + 0));
+            }
+            const bool more = j + 1 < w.n;
+            if (more) {
+                if (!(ok = wait_ring(kslot))) break;
+                if (j + 1 < w.n0) {
+                    issue_s(0, kslot);
+                    if (j + 1 == w.n0 - 1) ptx::mma_commit(ws_bar<D>(base, L::kQEmpty + 0));
+                }
+            }
+            if (j < w.n1) {
+                if (!(ok = wait_p(1))) break;
+                issue_pv(1, vslot, j > 0);
+                if (j == w.n1 - 1) ptx::mma_commit(ws_bar<D>(base, L::kOFull + 1));
+            }
+            ptx::mma_commit(ws_bar<D>(base, L::kKVEmpty + vslot));
+            if (more) {
+                if (j + 1 < w.n1) {
+                    issue_s(1, kslot);
+                    if (j + 1 == w.n1 - 1) ptx::mma_commit(ws_bar<D>(base, L::kQEmpty + 1));
+                }
+                ptx::mma_commit(ws_bar<D>(base, L::kKVEmpty + kslot));
+            }
+        }
+        if (!ok) break;
+    }
+    // Every MMA issued above completes before TMEM can be released.
+    ptx::mma_commit(ws_bar<D>(base, L::kDrain));
+    ptx::drain_wait(ws_bar<D>(base, L::kDrain), 0u, lim);
+}
+
+// ---------------------------------------------------------------- softmax
+template <int D>
+__device__ void ws_softmax_role(const FwdParams& p, uint32_t base, uint32_t tmem, int wg,
+                                volatile int* abort_flag) {
+    using L = WsLayout<D>;
+    const int r = threadIdx.x - (4 + 4 * wg) * 32;  // row within the query tile, 0..127
+    const int warp_in_wg = r >> 5;
+    const uint32_t lane_off = (uint32_t)(warp_in_wg * 32) << 16;
+    const uint32_t tS = tmem + lane_off + (uint32_t)wg * kTile;
+    const uint32_t tP = tS + 64u;
+    const uint32_t tO = tmem + lane_off + 256u + (uint32_t)wg * D;
+    const uint32_t bar_s = ws_bar<D>(base, L::kSFull + wg);
+    const uint32_t bar_p = ws_bar<D>(base, L::kPFull + wg);
+    const uint32_t bar_o = ws_bar<D>(base, L::kOFull + wg);
+    const float sl2 = p.scale_log2;
+    const uint64_t lim = p.wait_limit_ns;
+    uint32_t s_phase = 0, o_phase = 0;
+
+    for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+        const Unit w = decode_unit(u, p);
+        const int qt = 2 * w.m + wg;
+        const int n_i = wg == 0 ? w.n0 : w.n1;
+        float m_run = 0.f;  // reference maximum (log2 units), set by the first tile
+        float l_run = 0.f;
+        for (int j = 0; j < n_i; ++j) {
+            bool ok = ptx::mbar_wait(bar_s, s_phase, abort_flag, p.status, lim);
+            if (!__all_sync(0xffffffffu, ok)) return;
+            s_phase ^= 1u;
+            ptx::tc_fence_after();
+
+            uint32_t sr[128];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tS + c * 32, sr + c * 32);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 4; ++c) ptx::reg_fence32(sr + c * 32);
+            float s[128];
+#pragma unroll
+            for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
+
+            const int kv0 = j * kTile;
+            if (p.causal && j == qt) {
+#pragma unroll
+                for (int c = 0; c < 128; ++c)
+                    if (c > r) s[c] = -INFINITY;  // key after the query
+            } else if (!p.causal && kv0 + kTile > p.S) {
+                const int lim_c = p.S - kv0;
+#pragma unroll
+                for (int c = 0; c < 128; ++c)
+                    if (c >= lim_c) s[c] = -INFINITY;  // key past the end
+            }
+            float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+            for (int c = 4; c < 128; c += 4) {
+                mx0 = fmaxf(mx0, s[c]);
+                mx1 = fmaxf(mx1, s[c + 1]);
+                mx2 = fmaxf(mx2, s[c + 2]);
+                mx3 = fmaxf(mx3, s[c + 3]);
+            }
+            const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+            // Every row has at least one unmasked key in every tile it visits
+            // (key 0 of tile 0; the diagonal key of a diagonal tile), so mt is finite.
+            float alpha = 1.f;
+            bool rescale = false;
+            if (j == 0) {
+                m_run = mt;
+            } else if (mt > m_run + kRescaleSlack) {
+                alpha = ptx::ex2(m_run - mt);
+                m_run = mt;
+                rescale = true;
+            }
+            const float neg_m = -m_run;
+            float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    const float p0 = ptx::ex2(fmaf(s[64 * h + 2 * c], sl2, neg_m));
+                    const float p1 = ptx::ex2(fmaf(s[64 * h + 2 * c + 1], sl2, neg_m));
+                    sum0 += p0;
+                    sum1 += p1;
+                    pk[c] = ptx::pack_bf16x2(p0, p1);
+                }
+                ptx::tmem_st32(tP + 32 * h, pk);
+            }
+            l_run = l_run * alpha + (sum0 + sum1);
+            if (__any_sync(0xffffffffu, rescale)) {
+                // O_i holds the sum over earlier tiles; its last MMA completed
+                // before S_i(j) did.
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    ptx::tmem_ld32(tO + c * 32, o);
+                    ptx::tmem_ld_wait();
+                    ptx::reg_fence32(o);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                    ptx::tmem_st32(tO + c * 32, o);
+                }
+            }
+            ptx::tmem_st_wait();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar_p);
+        }
+
+        // ---- epilogue: wait for the last O_i += P V, then O / l -> bf16, LSE
+        bool ok = ptx::mbar_wait(bar_o, o_phase, abort_flag, p.status, lim);
+        if (!__all_sync(0xffffffffu, ok)) return;
+        o_phase ^= 1u;
+        ptx::tc_fence_after();
+        const int row = qt * kTile + r;
+        const bool valid = row < p.S;
+        const float inv_l = 1.f / l_run;
+        __nv_bfloat16* orow = p.out + ((size_t)w.bh * p.S + row) * D;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            ptx::tmem_ld32(tO + c * 32, o);
+            ptx::tmem_ld_wait();
+            ptx::reg_fence32(o);
+            if (valid) {
+                uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    uint4 v;
+                    v.x = ptx::pack_bf16x2(__uint_as_float(o[8 * e + 0]) * inv_l,
+                                           __uint_as_float(o[8 * e + 1]) * inv_l);
+                    v.y = ptx::pack_bf16x2(__uint_as_float(o[8 * e + 2]) * inv_l,
+                                           __uint_as_float(o[8 * e + 3]) * inv_l);
+                    v.z = ptx::pack_bf16x2(__uint_as_float(o[8 * e + 4]) * inv_l,
+                                           __uint_as_float(o[8 * e + 5]) * inv_l);
+                    v.w = ptx::pack_bf16x2(__uint_as_float(o[8 * e + 6]) * inv_l,
+                                           __uint_as_float(o[8 * e + 7]) * inv_l);
+                    dst[e] = v;
+                }
+            }
+        }
+        if (valid && p.lse != nullptr)
+            p.lse[(size_t)w.bh * p.S + row] = (m_run + ptx::lg2(l_run)) * kLn2;
+    }
+}
+
+// ---------------------------------------------------------------- kernel
+template <int D>
+__global__ void __launch_bounds__(WsLayout<D>::kThreads, 1)
+    attn_fwd_ws_kernel(const __grid_constant__ CUtensorMap tm_q,
+                       const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+    using L = WsLayout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* smem = smem_raw + (base - raw);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbort);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2; ++i) {
+            ptx::mbar_init(ws_bar<D>(base, L::kQFull + i), 1);
+            ptx::mbar_init(ws_bar<D>(base, L::kQEmpty + i), 1);
+            ptx::mbar_init(ws_bar<D>(base, L::kSFull + i), 1);
+            ptx::mbar_init(ws_bar<D>(base, L::kPFull + i), kTile);  // every softmax thread
+            ptx::mbar_init(ws_bar<D>(base, L::kOFull + i), 1);
+        }
+        for (int s = 0; s < L::kStages; ++s) {
+            ptx::mbar_init(ws_bar<D>(base, L::kKVFull + s), 1);
+            ptx::mbar_init(ws_bar<D>(base, L::kKVEmpty + s), 1);
+        }
+        ptx::mbar_init(ws_bar<D>(base, L::kDrain), 1);
+        *abort_flag = 0;
+        ptx::fence_barrier_init();
+        ptx::prefetch_tensormap(&tm_q);
+        ptx::prefetch_tensormap(&tm_k);
+        ptx::prefetch_tensormap(&tm_v);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_addr(tmem_slot), L::kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) ws_load_role<D>(&tm_q, &tm_k, &tm_v, p, base, abort_flag);
+    } else if (warp == 1) {
+        if (lane == 0) ws_mma_role<D>(p, base, tmem, abort_flag);
+    } else if (warp >= 4) {
+        ws_softmax_role<D>(p, base, tmem, (warp - 4) >> 2, abort_flag);
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, L::kTmemCols);
+    }
+}
+
+}  // namespace attn

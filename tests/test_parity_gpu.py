@@ -15,13 +15,23 @@ from tests.gpu_util import compare, run_gpu, sample_rows
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(scope="module", autouse=True)
-def _cuda():
+@pytest.fixture(scope="module", autouse=True, params=["ws", "simple"])
+def kernel(request):
+    """Every test runs on both kernels: the warp-specialised persistent one
+    (the default) and the one-tile-per-CTA one (ATTN_FWD_KERNEL=simple)."""
     torch = pytest.importorskip("torch")
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
+    import os
     from causal_scaled_dot_gb300 import native
     native.load()
+    old = os.environ.get("ATTN_FWD_KERNEL")
+    os.environ["ATTN_FWD_KERNEL"] = request.param
+    yield request.param
+    if old is None:
+        os.environ.pop("ATTN_FWD_KERNEL", None)
+    else:
+        os.environ["ATTN_FWD_KERNEL"] = old
 
 
 def _check(B, Hq, Hkv, S, D, causal, seed, sigma=1.0, scale=None):
@@ -52,6 +62,19 @@ def test_head_groups_and_batches(B, Hq, Hkv):
 
 def test_d64_multi_tile_gqa():
     _check(2, 8, 2, 700, 64, True, seed=301)
+
+
+@pytest.mark.parametrize("B,H,S,D", [(8, 64, 256, 128), (3, 100, 1024, 128), (5, 40, 640, 64),
+                                     (1, 1, 4096, 128), (2, 3, 2200, 64)])
+def test_many_units_per_cta(B, H, S, D):
+    """More units than SMs, so every CTA of the persistent kernel runs several
+    units and its K/V ring wraps many times; sampled rows against the oracle."""
+    q, k, v = qkv_bf16(B, H, H, S, D, seed=B * 1000 + S)
+    o, l, _ = run_gpu(q, k, v, 1 / math.sqrt(D), True)
+    rows = sample_rows(B, H, S, n_random=512, seed=S)
+    o_ref, l_ref = oracle.attention(q, k, v, 1 / math.sqrt(D), True, rows=rows)
+    compare(o.reshape(-1, D)[rows], o_ref, l.reshape(-1)[rows], l_ref, f"B{B} H{H} S{S} D{D}")
+    assert np.all(np.isfinite(o))
 
 
 @pytest.mark.parametrize("w", WORKLOADS[1:], ids=lambda w: w.name)
