@@ -1,9 +1,12 @@
 // kernel_ws.cuh -- warp-specialised, persistent attention forward for sm_103a.
 //
 // Work unit: one (batch, query head) and a pair of adjacent 128-row query
-// tiles (2m, 2m+1).  One CTA per SM loops over units, heaviest causal units
-// first (pair index descending), query heads that share a key/value head next
-// to each other so their K/V tiles are reused from L2.
+// tiles (2m, 2m+1).  Units are numbered heaviest causal pairs first (pair
+// index descending), query heads that share a key/value head next to each
+// other so their K/V tiles are reused from L2.  One CTA per SM takes one unit
+// per round in boustrophedon order -- round r gives unit r*G + c to CTA c on
+// even rounds and to CTA G-1-c on odd ones -- which balances the sorted unit
+// costs about as well as a dynamic queue, with no global state.
 //
 // Roles (384 threads, 12 warps):
 //   warp 0      TMA producer: Q tiles of the unit, then K_j, V_j into a ring
@@ -96,6 +99,12 @@ __device__ __forceinline__ Unit decode_unit(int u, const FwdParams& p) {
     return w;
 }
 
+// The unit this CTA runs in round r (>= num_units: no more work).
+__device__ __forceinline__ int unit_of_round(int r) {
+    const int G = gridDim.x, c = blockIdx.x;
+    return r * G + ((r & 1) ? (G - 1 - c) : c);
+}
+
 template <int D>
 __device__ __forceinline__ uint32_t ws_bar(uint32_t base, int i) {
     return base + WsLayout<D>::kBars + 8u * (uint32_t)i;
@@ -113,7 +122,7 @@ __device__ void ws_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
     // Loads issued and possibly not yet landed, for the drain after an abort.
     uint32_t pend_kv = 0, pend_kv_par = 0, pend_q = 0, pend_q_par = 0;
     const uint64_t lim = p.wait_limit_ns;
-    for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+    for (int r = 0, u = unit_of_round(0); u < p.num_units; u = unit_of_round(++r)) {
         const Unit w = decode_unit(u, p);
         for (int i = 0; i < 2; ++i) {
             if (!ptx::mbar_wait(ws_bar<D>(base, L::kQEmpty + i), qe_phase[i] ^ 1u, abort_flag,
@@ -217,7 +226,7 @@ __device__ void ws_mma_role(const FwdParams& p, uint32_t base, uint32_t tmem,
         return true;
     };
 
-    for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+    for (int r = 0, u = unit_of_round(0); u < p.num_units; u = unit_of_round(++r)) {
         const Unit w = decode_unit(u, p);
         if (!ptx::mbar_wait(ws_bar<D>(base, L::kQFull + 0), qf_phase, abort_flag, p.status, lim) ||
             !ptx::mbar_wait(ws_bar<D>(base, L::kQFull + 1), qf_phase, abort_flag, p.status, lim))
@@ -285,7 +294,7 @@ __device__ void ws_softmax_role(const FwdParams& p, uint32_t base, uint32_t tmem
     const uint64_t lim = p.wait_limit_ns;
     uint32_t s_phase = 0, o_phase = 0;
 
-    for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+    for (int r = 0, u = unit_of_round(0); u < p.num_units; u = unit_of_round(++r)) {
         const Unit w = decode_unit(u, p);
         const int qt = 2 * w.m + wg;
         const int n_i = wg == 0 ? w.n0 : w.n1;
