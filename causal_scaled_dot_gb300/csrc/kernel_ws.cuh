@@ -122,7 +122,7 @@ __device__ void ws_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
     // Loads issued and possibly not yet landed, for the drain after an abort.
     uint32_t pend_kv = 0, pend_kv_par = 0, pend_q = 0, pend_q_par = 0;
     const uint64_t lim = p.wait_limit_ns;
-    for (int r = 0, u = unit_of_round(0); u < p.num_units; u = unit_of_round(++r)) {
+    for (int rnd = 0, u = unit_of_round(0); u < p.num_units; u = unit_of_round(++rnd)) {
         const Unit w = decode_unit(u, p);
         for (int i = 0; i < 2; ++i) {
             if (!ptx::mbar_wait(ws_bar<D>(base, L::kQEmpty + i), qe_phase[i] ^ 1u, abort_flag,
@@ -226,7 +226,7 @@ __device__ void ws_mma_role(const FwdParams& p, uint32_t base, uint32_t tmem,
         return true;
     };
 
-    for (int r = 0, u = unit_of_round(0); u < p.num_units; u = unit_of_round(++r)) {
+    for (int rnd = 0, u = unit_of_round(0); u < p.num_units; u = unit_of_round(++rnd)) {
         const Unit w = decode_unit(u, p);
         if (!ptx::mbar_wait(ws_bar<D>(base, L::kQFull + 0), qf_phase, abort_flag, p.status, lim) ||
             !ptx::mbar_wait(ws_bar<D>(base, L::kQFull + 1), qf_phase, abort_flag, p.status, lim))
@@ -294,7 +294,7 @@ __device__ void ws_softmax_role(const FwdParams& p, uint32_t base, uint32_t tmem
     const uint64_t lim = p.wait_limit_ns;
     uint32_t s_phase = 0, o_phase = 0;
 
-    for (int r = 0, u = unit_of_round(0); u < p.num_units; u = unit_of_round(++r)) {
+    for (int rnd = 0, u = unit_of_round(0); u < p.num_units; u = unit_of_round(++rnd)) {
         const Unit w = decode_unit(u, p);
         const int qt = 2 * w.m + wg;
         const int n_i = wg == 0 ? w.n0 : w.n1;
