@@ -54,6 +54,12 @@ constexpr float kRescaleSlack = 8.0f;  // log2 units: probabilities stay <= 256
 template <int D>
 struct WsLayout {
     static constexpr int kThreads = 384;
+    // Registers per thread after the split: warps 0-3 (producer, MMA issuer,
+    // idle) shrink, the softmax warps grow.  Launch allocation: 384 x 168 =
+    // 64512 >= 128 x kRegsSmall + 256 x kRegsSoftmax = 62464.
+    static constexpr int kRegsSmall = 56;
+    static constexpr int kRegsSoftmax = 216;
+    static_assert(128 * kRegsSmall + 256 * kRegsSoftmax <= kThreads * 168, "register split");
     static constexpr int kStages = (D == 128) ? 4 : 8;     // K/V ring slots, one tile each
     static constexpr uint32_t kTileBytes = kTile * D * 2;  // 32 KB at D = 128
     static constexpr int kChunks = D / 64;                 // 64-column swizzle blocks
@@ -185,27 +191,25 @@ __device__ void ws_mma_role(const FwdParams& p, uint32_t base, uint32_t tmem,
     int slot = 0;
     uint32_t ring_phase = 0;
 
-    // S_i = Q_i K^T with K in ring slot `ks`.
+    // S_i = Q_i K^T with K in ring slot `ks`: all K steps from one asm block.
     auto issue_s = [&](int i, int ks) {
-        const uint32_t q = base + (i == 0 ? L::kQ0 : L::kQ1);
-        const uint32_t k = base + L::kRing + (uint32_t)ks * L::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * L::kChunkBytes + (kk & 3) * 32;
-            ptx::mma_ss(tmem + (uint32_t)i * kTile, ptx::sdesc_sw128(q + off, 16, 1024),
-                        ptx::sdesc_sw128(k + off, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
-        }
+        const uint64_t a = ptx::sdesc_sw128(base + (i == 0 ? L::kQ0 : L::kQ1), 16, 1024);
+        const uint64_t b = ptx::sdesc_sw128(base + L::kRing + (uint32_t)ks * L::kTileBytes, 16, 1024);
+        if (D == 128)
+            ptx::mma_ss_k128(tmem + (uint32_t)i * kTile, a, b, kIdescS, 0u);
+        else
+            ptx::mma_ss_k64(tmem + (uint32_t)i * kTile, a, b, kIdescS, 0u);
         ptx::mma_commit(ws_bar<D>(base, L::kSFull + i));
     };
-    // O_i (+)= P_i V with P_i in TMEM columns [64,128) of S_i and V in slot `vs`.
+    // O_i (+)= P_i V with P_i in TMEM columns [64,128) of S_i and V in slot `vs`:
+    // keys 0-63 then keys 64-127 (8 KB further into V, 32 TMEM columns further into P).
     auto issue_pv = [&](int i, int vs, bool accumulate) {
-        const uint32_t v = base + L::kRing + (uint32_t)vs * L::kTileBytes;
+        const uint64_t v = ptx::sdesc_sw128(base + L::kRing + (uint32_t)vs * L::kTileBytes,
+                                            L::kChunkBytes, 1024);
         const uint32_t o = tmem + 256u + (uint32_t)i * D;
         const uint32_t pcol = tmem + (uint32_t)i * kTile + 64u;
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-            ptx::mma_ts(o, pcol + kk * 8, ptx::sdesc_sw128(v + kk * 16 * 128, L::kChunkBytes, 1024),
-                        kIdescO, (accumulate || kk > 0) ? 1u : 0u);
+        ptx::mma_ts_k64(o, pcol, v, kIdescO, accumulate ? 1u : 0u);
+        ptx::mma_ts_k64(o, pcol + 32u, v + 512u, kIdescO, 1u);
     };
     auto wait_ring = [&](int& got) -> bool {
         if (!ptx::mbar_wait(ws_bar<D>(base, L::kKVFull + slot), ring_phase, abort_flag, p.status, lim))
@@ -327,13 +331,13 @@ __device__ void ws_softmax_role(const FwdParams& p, uint32_t base, uint32_t tmem
                 for (int c = 0; c < 128; ++c)
                     if (c >= lim_c) s[c] = -INFINITY;  // key past the end
             }
-            float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+            float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-            for (int c = 4; c < 128; c += 4) {
-                mx0 = fmaxf(mx0, s[c]);
-                mx1 = fmaxf(mx1, s[c + 1]);
-                mx2 = fmaxf(mx2, s[c + 2]);
-                mx3 = fmaxf(mx3, s[c + 3]);
+            for (int c = 0; c < 128; c += 8) {
+                mx0 = ptx::max3(mx0, s[c], s[c + 1]);
+                mx1 = ptx::max3(mx1, s[c + 2], s[c + 3]);
+                mx2 = ptx::max3(mx2, s[c + 4], s[c + 5]);
+                mx3 = ptx::max3(mx3, s[c + 6], s[c + 7]);
             }
             const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
             // Every row has at least one unmasked key in every tile it visits
@@ -347,21 +351,32 @@ __device__ void ws_softmax_role(const FwdParams& p, uint32_t base, uint32_t tmem
                 m_run = mt;
                 rescale = true;
             }
-            const float neg_m = -m_run;
-            float sum0 = 0.f, sum1 = 0.f;
+            // p = 2^(s*scale*log2e - m), two elements per paired FMA / add.
+            const uint64_t sl2x2 = ptx::f2(sl2, sl2);
+            const uint64_t negm2 = ptx::f2(-m_run, -m_run);
+            uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 uint32_t pk[32];
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
-                    const float p0 = ptx::ex2(fmaf(s[64 * h + 2 * c], sl2, neg_m));
-                    const float p1 = ptx::ex2(fmaf(s[64 * h + 2 * c + 1], sl2, neg_m));
-                    sum0 += p0;
-                    sum1 += p1;
+                    const int e = 64 * h + 2 * c;
+                    float x0, x1;
+                    ptx::f2_split(ptx::fma2(ptx::f2(s[e], s[e + 1]), sl2x2, negm2), x0, x1);
+                    const float p0 = ptx::ex2(x0);
+                    const float p1 = ptx::ex2(x1);
+                    acc[c & 3] = ptx::add2(acc[c & 3], ptx::f2(p0, p1));
                     pk[c] = ptx::pack_bf16x2(p0, p1);
                 }
                 ptx::tmem_st32(tP + 32 * h, pk);
             }
+            float sum0, sum1, sum2, sum3, sum4, sum5, sum6, sum7;
+            ptx::f2_split(acc[0], sum0, sum1);
+            ptx::f2_split(acc[1], sum2, sum3);
+            ptx::f2_split(acc[2], sum4, sum5);
+            ptx::f2_split(acc[3], sum6, sum7);
+            sum0 = (sum0 + sum1) + (sum2 + sum3);
+            sum1 = (sum4 + sum5) + (sum6 + sum7);
             l_run = l_run * alpha + (sum0 + sum1);
             if (__any_sync(0xffffffffu, rescale)) {
                 // O_i holds the sum over earlier tiles; its last MMA completed
@@ -380,7 +395,8 @@ __device__ void ws_softmax_role(const FwdParams& p, uint32_t base, uint32_t tmem
             }
             ptx::tmem_st_wait();
             ptx::tc_fence_before();
-            ptx::mbar_arrive(bar_p);
+            __syncwarp();
+            if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(bar_p);  // one arrival per warp
         }
 
         // ---- epilogue: wait for the last O_i += P V, then O / l -> bf16, LSE
@@ -441,7 +457,7 @@ __global__ void __launch_bounds__(WsLayout<D>::kThreads, 1)
             ptx::mbar_init(ws_bar<D>(base, L::kQFull + i), 1);
             ptx::mbar_init(ws_bar<D>(base, L::kQEmpty + i), 1);
             ptx::mbar_init(ws_bar<D>(base, L::kSFull + i), 1);
-            ptx::mbar_init(ws_bar<D>(base, L::kPFull + i), kTile);  // every softmax thread
+            ptx::mbar_init(ws_bar<D>(base, L::kPFull + i), 4);  // one per softmax warp
             ptx::mbar_init(ws_bar<D>(base, L::kOFull + i), 1);
         }
         for (int s = 0; s < L::kStages; ++s) {
@@ -464,11 +480,15 @@ __global__ void __launch_bounds__(WsLayout<D>::kThreads, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0) {
-        if (lane == 0) ws_load_role<D>(&tm_q, &tm_k, &tm_v, p, base, abort_flag);
-    } else if (warp == 1) {
-        if (lane == 0) ws_mma_role<D>(p, base, tmem, abort_flag);
-    } else if (warp >= 4) {
+    if (warp < 4) {
+        ptx::regs_dec<L::kRegsSmall>();
+        if (warp == 0) {
+            if (lane == 0) ws_load_role<D>(&tm_q, &tm_k, &tm_v, p, base, abort_flag);
+        } else if (warp == 1) {
+            if (lane == 0) ws_mma_role<D>(p, base, tmem, abort_flag);
+        }
+    } else {
+        ptx::regs_inc<L::kRegsSoftmax>();
         ws_softmax_role<D>(p, base, tmem, (warp - 4) >> 2, abort_flag);
     }
 

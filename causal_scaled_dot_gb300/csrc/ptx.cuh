@@ -167,6 +167,71 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// Whole products issued from one asm block.  The start-address field of a
+// shared-memory descriptor counts 16-byte units, so the per-step offsets are
+// immediates added to a descriptor computed once; keeping the K steps of a
+// product in one block lets them issue back to back at the tensor core's rate.
+//
+// D (+)= A B^T over K = 128 (bf16), A and B K-major SW128 tiles made of two
+// 64-column blocks 16 KB apart: step kk starts 32*(kk%4) + 16384*(kk/4) bytes in.
+__device__ __forceinline__ void mma_ss_k128(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 a, b;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+        "add.s64 a, %1, 2; add.s64 b, %2, 2;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, 1;\n\t"
+        "add.s64 a, %1, 4; add.s64 b, %2, 4;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, 1;\n\t"
+        "add.s64 a, %1, 6; add.s64 b, %2, 6;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, 1;\n\t"
+        "add.s64 a, %1, 1024; add.s64 b, %2, 1024;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, 1;\n\t"
+        "add.s64 a, %1, 1026; add.s64 b, %2, 1026;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, 1;\n\t"
+        "add.s64 a, %1, 1028; add.s64 b, %2, 1028;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, 1;\n\t"
+        "add.s64 a, %1, 1030; add.s64 b, %2, 1030;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, 1;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Same over K = 64: one 64-column block, steps 32 bytes apart.
+__device__ __forceinline__ void mma_ss_k64(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 a, b;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+        "add.s64 a, %1, 2; add.s64 b, %2, 2;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, 1;\n\t"
+        "add.s64 a, %1, 4; add.s64 b, %2, 4;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, 1;\n\t"
+        "add.s64 a, %1, 6; add.s64 b, %2, 6;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, 1;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// D (+)= A B over 64 keys (four K = 16 steps), A read from tensor memory
+// columns a + 8*kk (two bf16 per column), B an MN-major SW128 tile whose K
+// rows advance 16 rows = 2048 bytes per step.
+__device__ __forceinline__ void mma_ts_k64(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 b;\n\t.reg .b32 a;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+        "add.s32 a, %1, 8; add.s64 b, %2, 128;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, 1;\n\t"
+        "add.s32 a, %1, 16; add.s64 b, %2, 256;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, 1;\n\t"
+        "add.s32 a, %1, 24; add.s64 b, %2, 384;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, 1;\n\t}" ::"r"(d),
+        "r"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 async op issued so far by this thread completes.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile(
@@ -249,6 +314,19 @@ __device__ __forceinline__ void tmem_st_wait() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// Per-warp register budget changes (warp-collective).  The block keeps the
+// registers it was launched with; an increase waits until other warps of the
+// block have released enough, so the new counts must add up to at most the
+// launch allocation.
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ---------------------------------------------------------------- math
 // 2^x on the special-function unit (approximate, flush-to-zero).
 __device__ __forceinline__ float ex2(float x) {
@@ -260,6 +338,31 @@ __device__ __forceinline__ float lg2(float x) {
     float y;
     asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+// Maximum of three floats (one instruction on sm_100 and later).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+// Packed fp32 pairs (lo in bits 0-31) for the paired FMA / add pipes.
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_split(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
 }
 // Two floats -> packed bf16x2 (round to nearest even); `lo` in bits 0-15.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
