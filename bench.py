@@ -147,56 +147,71 @@ def barrier(world: int):
 
 
 # --------------------------------------------------------------------- oracle
-def time_oracle(w, budget_s: float, seed: int = 0):
-    """The fp64 oracle as it stands, on all host cores, over a bounded random
-    sample of the workload's query rows; returns (TFLOP/s, rows, seconds, threads).
+class OracleTimer:
+    """The fp64 oracle as it stands, on all host cores, over bounded random
+    samples of a workload's query rows.
 
     Each query row of a causal workload carries 2*S*D of the metric's FLOPs on
-    average (4*B*Hq*S^2*D/2 spread over B*Hq*S rows), so the sample's FLOPs are
-    rows * 2*S*D and the figure is comparable with the GPU's TFLOP/s.
+    average (4*B*Hq*S^2*D/2 spread over B*Hq*S rows), so a sample's FLOPs are
+    rows * 2*S*D and its TFLOP/s is comparable with the GPU's.
     """
-    import oracle
-    from causal_scaled_dot_gb300.inputs import qkv_bf16
-    q, k, v = qkv_bf16(w.B, w.Hq, w.Hkv, w.S, w.D, seed=w.seed, sigma=w.sigma)
-    nthreads = oracle.default_threads()
-    rng = np.random.default_rng(seed)
-    total = w.B * w.Hq * w.S
-    n = max(nthreads, 64)
-    oracle.attention(q, k, v, w.scale, w.causal, rows=rng.integers(0, total, n), nthreads=nthreads)
-    t0 = time.perf_counter()
-    oracle.attention(q, k, v, w.scale, w.causal, rows=rng.integers(0, total, n), nthreads=nthreads)
-    per_row = (time.perf_counter() - t0) / n
-    n = int(min(total, max(n, budget_s / max(per_row, 1e-9))))
-    rows = rng.integers(0, total, n)
-    t0 = time.perf_counter()
-    oracle.attention(q, k, v, w.scale, w.causal, rows=rows, nthreads=nthreads)
-    dt = time.perf_counter() - t0
-    per_row_flops = (2.0 if w.causal else 4.0) * w.S * w.D
-    return n * per_row_flops / dt / 1e12, n, dt, nthreads
+
+    def __init__(self, w):
+        import oracle
+        from causal_scaled_dot_gb300.inputs import qkv_bf16
+        self.oracle = oracle
+        self.w = w
+        self.q, self.k, self.v = qkv_bf16(w.B, w.Hq, w.Hkv, w.S, w.D, seed=w.seed, sigma=w.sigma)
+        self.threads = oracle.default_threads()
+        self.total = w.B * w.Hq * w.S
+        self.row_flops = (2.0 if w.causal else 4.0) * w.S * w.D
+        n = max(self.threads, 32)
+        self.run(n, seed=12345)  # warm the library and the page cache
+        t0 = time.perf_counter()
+        self.run(n, seed=12346)
+        self.sec_per_row = (time.perf_counter() - t0) / n
+
+    def run(self, n, seed):
+        rows = np.random.default_rng(seed).integers(0, self.total, n)
+        self.oracle.attention(self.q, self.k, self.v, self.w.scale, self.w.causal, rows=rows,
+                              nthreads=self.threads)
+
+    def rows_for(self, seconds):
+        return int(min(self.total, max(self.threads, seconds / max(self.sec_per_row, 1e-9))))
+
+    def sample(self, seconds, seed):
+        """Times one sample of about `seconds`; returns (TFLOP/s, rows, wall seconds)."""
+        n = self.rows_for(seconds)
+        t0 = time.perf_counter()
+        self.run(n, seed)
+        dt = time.perf_counter() - t0
+        return n * self.row_flops / dt / 1e12, n, dt
 
 
 def run_reference(args, w, rank, world):
     if rank != 0:
         return 0
-    times, rows_per_step, threads = [], 0, 1
-    for _ in range(args.warmup):
-        time_oracle(w, budget_s=args.ref_step_seconds / 4)
-    for s in range(args.steps):
-        tf, n, dt, threads = time_oracle(w, budget_s=args.ref_step_seconds, seed=s + 1)
-        times.append((tf, n, dt))
-    value = float(np.mean([t[0] for t in times]))
-    rows_per_step = int(np.mean([t[1] for t in times]))
-    ms = float(np.mean([t[2] for t in times])) * 1e3
+    timer = OracleTimer(w)
+    # The whole run (warm-up and timed steps) stays within a few minutes.
+    step_s = min(args.ref_step_seconds, args.ref_total_seconds / max(1, args.steps + args.warmup))
+    for i in range(args.warmup):
+        timer.sample(step_s, seed=1000 + i)
+    samples = [timer.sample(step_s, seed=s + 1) for s in range(args.steps)]
+    flops = sum(n * timer.row_flops for _, n, _ in samples)
+    secs = sum(dt for _, _, dt in samples)
+    value = flops / secs / 1e12
+    rows_per_step = int(np.mean([n for _, n, _ in samples]))
     sample = (f"{rows_per_step} random query rows of {w.name} per step "
-              f"(of {w.B * w.Hq * w.S}); fp64 C oracle, {threads} threads")
+              f"(of {timer.total}); fp64 C oracle, {timer.threads} threads")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
-        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": secs / len(samples) * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded N(0,1) bf16)",
         "config": {"workload": w.name, **w.shape_dict, "causal": w.causal},
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-                         "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": timer.threads,
+                         "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -291,9 +306,10 @@ def run_ours(args, w, rank, world, local):
     traffic = recorded_traffic(w.name)
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        tf, n, dt, threads = time_oracle(w, budget_s=args.cpu_seconds)
-        cpu = {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-               "sample": f"{n} random query rows of {w.name} (of {w.B * w.Hq * w.S}), "
+        timer = OracleTimer(w)
+        tf, n, dt = timer.sample(args.cpu_seconds, seed=7)
+        cpu = {"value": tf, "unit": "TFLOP/s", "cores": timer.threads, "kind": "oracle",
+               "sample": f"{n} random query rows of {w.name} (of {timer.total}), "
                          f"{dt:.1f} s; fp64 C oracle"}
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -323,14 +339,16 @@ def run_ours(args, w, rank, world, local):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=HEADLINE.name, choices=sorted(BY_NAME))
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="budget of the oracle CPU-baseline sample")
     ap.add_argument("--ref-step-seconds", type=float, default=8.0,
-                    help="--impl reference: oracle seconds per step")
+                    help="--impl reference: at most this many oracle seconds per step")
+    ap.add_argument("--ref-total-seconds", type=float, default=120.0,
+                    help="--impl reference: oracle seconds for the whole run")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
