@@ -119,3 +119,26 @@ def qkv_bf16(B: int, Hq: int, Hkv: int, S: int, D: int, seed: int, sigma: float 
     k = gaussian_bf16((B, Hkv, S, D), seed, 1, sigma)
     v = gaussian_bf16((B, Hkv, S, D), seed, 2, sigma)
     return q, k, v
+
+
+def float32_to_e4m3_codes(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to FP8 E4M3 (nearest, ties to even, saturating at
+    +-448 like PyTorch's float8_e4m3fn conversion); returns uint8 codes."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
+    t = t.clamp(-448.0, 448.0).to(torch.float8_e4m3fn)
+    return t.view(torch.uint8).numpy().copy()
+
+
+def gaussian_e4m3(shape, seed: int, stream: int, sigma: float = 1.0) -> np.ndarray:
+    """E4M3 codes (uint8) of N(0, sigma^2) draws: the bf16 draws of the same
+    (seed, stream), widened, then rounded to E4M3."""
+    return float32_to_e4m3_codes(bf16_bits_to_float32(gaussian_bf16(shape, seed, stream, sigma)))
+
+
+def qkv_e4m3(B: int, Hq: int, Hkv: int, S: int, D: int, seed: int, sigma: float = 1.0):
+    """Q [B,Hq,S,D], K and V [B,Hkv,S,D] as E4M3 codes, drawn in the order q, k, v."""
+    q = gaussian_e4m3((B, Hq, S, D), seed, 0, sigma)
+    k = gaussian_e4m3((B, Hkv, S, D), seed, 1, sigma)
+    v = gaussian_e4m3((B, Hkv, S, D), seed, 2, sigma)
+    return q, k, v

@@ -47,15 +47,17 @@ def compile_oracle(source: str = SOURCE, output: str = LIBRARY) -> str:
 
 
 def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
+    vp, ci, cf = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
     f = lib.oracle_attn_rows
-    f.restype = ctypes.c_int
-    f.argtypes = [
-        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
-        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-        ctypes.c_float, ctypes.c_int,
-        ctypes.c_void_p, ctypes.c_int64,
-        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
-    ]
+    f.restype = ci
+    f.argtypes = [vp, vp, vp, ci, ci, ci, ci, ci, cf, ci, vp, ctypes.c_int64, vp, vp, ci]
+    f = lib.oracle_attn_rows_e4m3
+    f.restype = ci
+    f.argtypes = [vp, vp, vp, cf, cf, cf, ci, ci, ci, ci, ci, cf, ci, vp, ctypes.c_int64, vp, vp,
+                  ci]
+    f = lib.oracle_e4m3_decode
+    f.restype = None
+    f.argtypes = [vp, ctypes.c_int64, vp]
     return lib
 
 
@@ -86,6 +88,55 @@ def _as_bits(x: np.ndarray, name: str) -> np.ndarray:
     if x.dtype != np.uint16:
         raise TypeError(f"{name}: expected bf16 bit patterns as uint16, got {x.dtype}")
     return x
+
+
+def _shapes(q, k, v):
+    if q.ndim != 4 or k.ndim != 4 or v.shape != k.shape:
+        raise ValueError("q must be [B,Hq,S,D]; k and v must both be [B,Hkv,S,D]")
+    B, Hq, S, D = q.shape
+    Bk, Hkv, Sk, Dk = k.shape
+    if (Bk, Sk, Dk) != (B, S, D):
+        raise ValueError("q and k/v disagree on B, S or D")
+    return B, Hq, Hkv, S, D
+
+
+def _outputs(B, Hq, S, D, rows):
+    if rows is None:
+        return None, B * Hq * S, np.empty((B, Hq, S, D)), np.empty((B, Hq, S))
+    rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    return rows_arr, rows_arr.size, np.empty((rows_arr.size, D)), np.empty((rows_arr.size,))
+
+
+def attention_e4m3(q_codes, k_codes, v_codes, scale: float, descales=(1.0, 1.0, 1.0),
+                   causal: bool = True, rows=None, nthreads: int | None = None,
+                   lib: ctypes.CDLL | None = None):
+    """As ``attention`` for FP8 E4M3 inputs: uint8 codes [B,H,S,D]; element value =
+    decoded code * descale of its tensor (q, k, v)."""
+    lib = lib or load()
+    q, k, v = (np.ascontiguousarray(x) for x in (q_codes, k_codes, v_codes))
+    for name, x in (("q", q), ("k", k), ("v", v)):
+        if x.dtype != np.uint8:
+            raise TypeError(f"{name}: expected E4M3 codes as uint8, got {x.dtype}")
+    B, Hq, Hkv, S, D = _shapes(q, k, v)
+    rows_arr, nrows, out, lse = _outputs(B, Hq, S, D, rows)
+    dq, dk, dv = (ctypes.c_float(float(x)) for x in descales)
+    rc = lib.oracle_attn_rows_e4m3(
+        q.ctypes.data, k.ctypes.data, v.ctypes.data, dq, dk, dv, B, Hq, Hkv, S, D,
+        ctypes.c_float(scale), 1 if causal else 0,
+        None if rows_arr is None else rows_arr.ctypes.data, nrows,
+        out.ctypes.data, lse.ctypes.data, nthreads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle_attn_rows_e4m3 rejected its arguments")
+    return out, lse
+
+
+def e4m3_decode(codes, lib: ctypes.CDLL | None = None) -> np.ndarray:
+    """The oracle's own E4M3 decoding of uint8 codes, as float64."""
+    lib = lib or load()
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    out = np.empty(c.shape, dtype=np.float64)
+    lib.oracle_e4m3_decode(c.ctypes.data, c.size, out.ctypes.data)
+    return out
 
 
 def attention(q_bits, k_bits, v_bits, scale: float, causal: bool = True, rows=None,

@@ -28,7 +28,10 @@
  * each as its own loop.  A library primitive is not needed.
  *
  * Inputs are bf16 bit patterns (uint16) in [B,H,S,D] contiguous layout, the
- * same bits the GPU receives.  Widening bf16 -> double is exact.
+ * same bits the GPU receives.  Widening bf16 -> double is exact.  A second
+ * entry point takes FP8 E4M3 bit patterns (uint8) with one descale factor per
+ * tensor (value = decoded code * descale, in double): the FP8 attention that
+ * the ai-manual.ru article mentions for newer GPUs (section 6, "FP8 and BF16").
  *
  * Parity pins (tests/test_oracle_pins.py): library softmax / SDPA in float64,
  * closed forms (causal row 0, Q = 0 means, S = 1), key-shift and linearity
@@ -49,8 +52,22 @@ static double bf16_bits_to_double(uint16_t b) {
     return (double)f;
 }
 
+/* FP8 E4M3 (the "fn" variant: no infinities) bit pattern -> double, exactly:
+ * sign, 4 exponent bits with bias 7, 3 mantissa bits; exponent 0 holds the
+ * subnormals m/8 * 2^-6; S.1111.111 is NaN. */
+static double e4m3_bits_to_double(uint8_t b) {
+    const int sign = b >> 7, e = (b >> 3) & 15, m = b & 7;
+    if (e == 15 && m == 7) return NAN;
+    const double v = (e == 0) ? ldexp((double)m / 8.0, -6) : ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+enum { FMT_BF16 = 0, FMT_E4M3 = 1 };
+
 typedef struct {
-    const uint16_t *q, *k, *v;
+    const void *t[3];        /* q, k, v */
+    int format;              /* FMT_BF16 or FMT_E4M3 */
+    double descale[3];       /* FMT_E4M3: value = decoded code * descale */
     int B, Hq, Hkv, S, D;
     double scale;
     int causal;
@@ -61,6 +78,12 @@ typedef struct {
     int64_t begin, end;
     int status;
 } oracle_job_t;
+
+/* Element idx of tensor `which` (0 q, 1 k, 2 v) as a double. */
+static double elem(const oracle_job_t *J, int which, int64_t idx) {
+    if (J->format == FMT_BF16) return bf16_bits_to_double(((const uint16_t *)J->t[which])[idx]);
+    return e4m3_bits_to_double(((const uint8_t *)J->t[which])[idx]) * J->descale[which];
+}
 
 /*
  * One query row: flat id r = (b*Hq + hq)*S + i.
@@ -78,15 +101,15 @@ static void oracle_one_row(const oracle_job_t *J, int64_t r, double *s,
     const int64_t G = J->Hq / J->Hkv;
     const int64_t hkv = hq / G;
 
-    const uint16_t *qi = J->q + (bh * S + i) * (int64_t)D;
-    const uint16_t *kb = J->k + ((b * J->Hkv + hkv) * S) * (int64_t)D;
-    const uint16_t *vb = J->v + ((b * J->Hkv + hkv) * S) * (int64_t)D;
+    const int64_t qi = (bh * S + i) * (int64_t)D;              /* q_i */
+    const int64_t kb = ((b * J->Hkv + hkv) * S) * (int64_t)D;  /* k_0 of this head */
+    const int64_t vb = ((b * J->Hkv + hkv) * S) * (int64_t)D;  /* v_0 of this head */
 
     /* Step 1: scores_j = sum_d q_id * k_jd. */
     for (int64_t j = 0; j < S; ++j) {
         double acc = 0.0;
         for (int d = 0; d < D; ++d)
-            acc += bf16_bits_to_double(qi[d]) * bf16_bits_to_double(kb[j * D + d]);
+            acc += elem(J, 0, qi + d) * elem(J, 1, kb + j * D + d);
         s[j] = acc;
     }
     /* Step 2: scale (multiply by the caller's scale). */
@@ -113,7 +136,7 @@ static void oracle_one_row(const oracle_job_t *J, int64_t r, double *s,
     for (int d = 0; d < D; ++d) o_row[d] = 0.0;
     for (int64_t j = 0; j < S; ++j) {
         if (s[j] == 0.0) continue; /* masked key contributes nothing */
-        for (int d = 0; d < D; ++d) o_row[d] += s[j] * bf16_bits_to_double(vb[j * D + d]);
+        for (int d = 0; d < D; ++d) o_row[d] += s[j] * elem(J, 2, vb + j * D + d);
     }
     *lse_out = m + log(l);
 }
@@ -134,19 +157,9 @@ static void *oracle_worker(void *arg) {
     return NULL;
 }
 
-/*
- * oracle_attn_rows -- O and LSE for selected query rows (or all rows).
- *
- *   q [B,Hq,S,D], k/v [B,Hkv,S,D]: bf16 bit patterns, contiguous.
- *   rows: nrows flat ids (b*Hq + hq)*S + i, or NULL for every row in order
- *         (then nrows must equal B*Hq*S).
- *   out:  double [nrows, D];  lse: double [nrows] (natural log).
- *   nthreads: worker threads (>= 1).
- * Returns 0 on success, 1 on a bad argument or allocation failure.
- */
-int oracle_attn_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int Hq,
-                     int Hkv, int S, int D, float scale, int causal, const int64_t *rows,
-                     int64_t nrows, double *out, double *lse, int nthreads) {
+static int run_rows(const void *q, const void *k, const void *v, int format, const double descale[3],
+                    int B, int Hq, int Hkv, int S, int D, float scale, int causal,
+                    const int64_t *rows, int64_t nrows, double *out, double *lse, int nthreads) {
     if (!q || !k || !v || !out || !lse) return 1;
     if (B < 1 || Hq < 1 || Hkv < 1 || S < 1 || D < 1 || Hq % Hkv != 0) return 1;
     const int64_t total = (int64_t)B * Hq * S;
@@ -168,7 +181,9 @@ int oracle_attn_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v, in
     int status = 0;
     for (int t = 0; t < nthreads; ++t) {
         oracle_job_t *J = &jobs[t];
-        J->q = q; J->k = k; J->v = v;
+        J->t[0] = q; J->t[1] = k; J->t[2] = v;
+        J->format = format;
+        for (int w = 0; w < 3; ++w) J->descale[w] = descale[w];
         J->B = B; J->Hq = Hq; J->Hkv = Hkv; J->S = S; J->D = D;
         J->scale = (double)scale;
         J->causal = causal ? 1 : 0;
@@ -191,4 +206,40 @@ int oracle_attn_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v, in
     free(jobs);
     free(tid);
     return status;
+}
+
+/*
+ * oracle_attn_rows -- O and LSE for selected query rows (or all rows).
+ *
+ *   q [B,Hq,S,D], k/v [B,Hkv,S,D]: bf16 bit patterns, contiguous.
+ *   rows: nrows flat ids (b*Hq + hq)*S + i, or NULL for every row in order
+ *         (then nrows must equal B*Hq*S).
+ *   out:  double [nrows, D];  lse: double [nrows] (natural log).
+ *   nthreads: worker threads (>= 1).
+ * Returns 0 on success, 1 on a bad argument or allocation failure.
+ */
+int oracle_attn_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int Hq,
+                     int Hkv, int S, int D, float scale, int causal, const int64_t *rows,
+                     int64_t nrows, double *out, double *lse, int nthreads) {
+    const double one[3] = {1.0, 1.0, 1.0};
+    return run_rows(q, k, v, FMT_BF16, one, B, Hq, Hkv, S, D, scale, causal, rows, nrows, out, lse,
+                    nthreads);
+}
+
+/*
+ * oracle_attn_rows_e4m3 -- the same for FP8 E4M3 inputs (uint8 bit patterns);
+ * the value of an element is its decoded code times the descale of its tensor.
+ */
+int oracle_attn_rows_e4m3(const uint8_t *q, const uint8_t *k, const uint8_t *v, float q_descale,
+                          float k_descale, float v_descale, int B, int Hq, int Hkv, int S, int D,
+                          float scale, int causal, const int64_t *rows, int64_t nrows,
+                          double *out, double *lse, int nthreads) {
+    const double ds[3] = {(double)q_descale, (double)k_descale, (double)v_descale};
+    return run_rows(q, k, v, FMT_E4M3, ds, B, Hq, Hkv, S, D, scale, causal, rows, nrows, out, lse,
+                    nthreads);
+}
+
+/* Decodes n E4M3 codes to doubles (exposed so the decoding can be pinned). */
+void oracle_e4m3_decode(const uint8_t *codes, int64_t n, double *out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = e4m3_bits_to_double(codes[i]);
 }

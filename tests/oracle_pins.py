@@ -268,3 +268,68 @@ ALL_PINS = [
     pin_large_magnitude,
     pin_worked_example,
 ]
+
+
+# ---------------------------------------------------------------------------
+# FP8 E4M3 inputs (the oracle's second entry point).  The callable for these
+# pins is ``attn8(q_codes, k_codes, v_codes, scale, descales, causal)`` and
+# ``decode(codes)``.
+def _e4m3_codes(shape, seed, stream, sigma=1.0):
+    """Random E4M3 codes from N(0, sigma^2) values, quantised by torch (a library
+    conversion, independent of the oracle's decoding)."""
+    x = bf16_bits_to_float32(gaussian_bf16(shape, seed, stream, sigma))
+    t = torch.from_numpy(np.ascontiguousarray(x)).to(torch.float8_e4m3fn)
+    return t.view(torch.uint8).numpy().copy()
+
+
+def _torch_e4m3(codes):
+    return torch.from_numpy(np.ascontiguousarray(codes)).view(torch.float8_e4m3fn).to(torch.float64)
+
+
+def pin_e4m3_decode(decode):
+    """All 256 codes decode as torch's float8_e4m3fn (NaN codes as NaN)."""
+    codes = np.arange(256, dtype=np.uint8)
+    ref = _torch_e4m3(codes).numpy()
+    got = decode(codes)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9 and got[0x38] == 1.0
+
+
+def pin_e4m3_sdpa_library(attn8):
+    """FP8 inputs with non-trivial descales equal torch's float64 SDPA on the
+    dequantised tensors (causal and not, GQA)."""
+    B, Hq, Hkv, S, D = 2, 4, 2, 33, 16
+    q, k, v = (_e4m3_codes((B, H, S, D), 111, t) for t, H in ((0, Hq), (1, Hkv), (2, Hkv)))
+    ds = tuple(float(np.float32(x)) for x in (0.37, 1.9, 0.61))  # descales travel as fp32
+    scale = 1.0 / math.sqrt(D)
+    for causal in (True, False):
+        O, L = attn8(q, k, v, scale, ds, causal)
+        qf, kf, vf = (_torch_e4m3(c) * d for c, d in zip((q, k, v), ds))
+        kf = kf.repeat_interleave(Hq // Hkv, dim=1)
+        vf = vf.repeat_interleave(Hq // Hkv, dim=1)
+        ref = F.scaled_dot_product_attention(qf, kf, vf, is_causal=causal,
+                                             scale=float(np.float32(scale))).numpy()
+        np.testing.assert_allclose(O, ref, rtol=0, atol=1e-12)
+        # LSE from its definition on the dequantised scores (a library logsumexp)
+        sc = torch.einsum("bhid,bhjd->bhij", qf, kf) * float(np.float32(scale))
+        if causal:
+            sc = sc.masked_fill(torch.ones(S, S, dtype=torch.bool).triu(1), float("-inf"))
+        np.testing.assert_allclose(L, torch.logsumexp(sc, dim=-1).numpy(), rtol=0, atol=1e-12)
+
+
+def pin_e4m3_matches_bf16_path(attn8, attn):
+    """Every E4M3 value is exact in bf16, so with unit descales the FP8 entry equals
+    the bf16 entry on the same values; power-of-two descales scale exactly."""
+    B, H, S, D = 1, 3, 20, 8
+    q, k, v = (_e4m3_codes((B, H, S, D), 121, t) for t in range(3))
+    to_bf16 = lambda c, d: float32_to_bf16_bits(  # noqa: E731
+        (_torch_e4m3(c) * d).to(torch.float32).numpy())
+    for ds in ((1.0, 1.0, 1.0), (2.0, 0.25, 8.0)):
+        O8, L8 = attn8(q, k, v, 0.3, ds, True)
+        O, L = attn(to_bf16(q, ds[0]), to_bf16(k, ds[1]), to_bf16(v, ds[2]), 0.3, True)
+        assert np.array_equal(O8, O) and np.array_equal(L8, L)
+
+
+E4M3_PINS = [pin_e4m3_decode, pin_e4m3_sdpa_library, pin_e4m3_matches_bf16_path]

@@ -17,20 +17,23 @@ MUTANTS = {
     "mask_off_by_one_late": ("for (int64_t j = i + 1; j < S; ++j) s[j] = -INFINITY;",
                              "for (int64_t j = i + 2; j < S; ++j) s[j] = -INFINITY;"),
     "scale_dropped": ("s[j] = s[j] * J->scale;", "s[j] = s[j];"),
-    "key_operand_transposed": ("bf16_bits_to_double(kb[j * D + d])",
-                               "bf16_bits_to_double(kb[d * S + j])"),
+    "key_operand_transposed": ("elem(J, 1, kb + j * D + d)", "elem(J, 1, kb + d * S + j)"),
     "gqa_interleaved": ("const int64_t hkv = hq / G;", "const int64_t hkv = hq % J->Hkv;"),
     "lse_without_max": ("*lse_out = m + log(l);", "*lse_out = log(l);"),
     "no_max_subtraction": ("s[j] = exp(s[j] - m);", "s[j] = exp(s[j]);"),
     "exp_sign_flipped": ("s[j] = exp(s[j] - m);", "s[j] = exp(m - s[j]);"),
     "normalisation_dropped": ("for (int64_t j = 0; j < S; ++j) s[j] = s[j] / l;", ""),
-    "value_row_is_query_row": ("bf16_bits_to_double(vb[j * D + d])",
-                               "bf16_bits_to_double(vb[i * D + d])"),
-    "batch_offset_dropped": ("const uint16_t *kb = J->k + ((b * J->Hkv + hkv) * S) * (int64_t)D;",
-                             "const uint16_t *kb = J->k + ((hkv) * S) * (int64_t)D;"),
-    "query_row_offset_wrong": ("const uint16_t *qi = J->q + (bh * S + i) * (int64_t)D;",
-                               "const uint16_t *qi = J->q + (bh * S) * (int64_t)D;"),
+    "value_row_is_query_row": ("elem(J, 2, vb + j * D + d)", "elem(J, 2, vb + i * D + d)"),
+    "batch_offset_dropped": ("const int64_t kb = ((b * J->Hkv + hkv) * S) * (int64_t)D;",
+                             "const int64_t kb = ((hkv) * S) * (int64_t)D;"),
+    "query_row_offset_wrong": ("const int64_t qi = (bh * S + i) * (int64_t)D;",
+                               "const int64_t qi = (bh * S) * (int64_t)D;"),
     "lse_log2": ("*lse_out = m + log(l);", "*lse_out = m + log2(l);"),
+    "e4m3_exponent_bias": ("ldexp(1.0 + (double)m / 8.0, e - 7)", "ldexp(1.0 + (double)m / 8.0, e - 8)"),
+    "e4m3_subnormal_scale": ("ldexp((double)m / 8.0, -6)", "ldexp((double)m / 8.0, -7)"),
+    "e4m3_descale_ignored": ("e4m3_bits_to_double(((const uint8_t *)J->t[which])[idx]) * J->descale[which]",
+                             "e4m3_bits_to_double(((const uint8_t *)J->t[which])[idx])"),
+    "e4m3_descale_swapped": ("J->descale[which]", "J->descale[2 - which]"),
 }
 
 
@@ -47,10 +50,19 @@ def test_some_pin_catches_mutant(name, tmp_path):
     def attn(q, k, v, scale, causal, rows=None):
         return oracle.attention(q, k, v, scale, causal, rows=rows, lib=lib)
 
+    def attn8(q, k, v, scale, ds, causal, rows=None):
+        return oracle.attention_e4m3(q, k, v, scale, ds, causal, rows=rows, lib=lib)
+
+    checks = [(p.__name__, lambda p=p: p(attn)) for p in oracle_pins.ALL_PINS] + [
+        ("pin_e4m3_decode", lambda: oracle_pins.pin_e4m3_decode(
+            lambda c: oracle.e4m3_decode(c, lib=lib))),
+        ("pin_e4m3_sdpa_library", lambda: oracle_pins.pin_e4m3_sdpa_library(attn8)),
+        ("pin_e4m3_matches_bf16_path", lambda: oracle_pins.pin_e4m3_matches_bf16_path(attn8, attn)),
+    ]
     caught = []
-    for pin in oracle_pins.ALL_PINS:
+    for pin_name, run in checks:
         try:
-            pin(attn)
+            run()
         except (AssertionError, ValueError, FloatingPointError):
-            caught.append(pin.__name__)
+            caught.append(pin_name)
     assert caught, f"no pin caught mutant {name}"

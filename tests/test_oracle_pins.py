@@ -15,6 +15,14 @@ def test_oracle_pin(pin):
     pin(_attn)
 
 
+def test_oracle_e4m3_pins():
+    def attn8(q, k, v, scale, ds, causal, rows=None):
+        return oracle.attention_e4m3(q, k, v, scale, ds, causal, rows=rows)
+    oracle_pins.pin_e4m3_decode(oracle.e4m3_decode)
+    oracle_pins.pin_e4m3_sdpa_library(attn8)
+    oracle_pins.pin_e4m3_matches_bf16_path(attn8, _attn)
+
+
 def test_rows_subset_matches_full():
     """The row-selection entry computes exactly the rows of the full call."""
     from causal_scaled_dot_gb300.inputs import qkv_bf16
