@@ -156,12 +156,14 @@ class OracleTimer:
     rows * 2*S*D and its TFLOP/s is comparable with the GPU's.
     """
 
-    def __init__(self, w):
+    def __init__(self, w, fp8: bool = False):
         import oracle
-        from causal_scaled_dot_gb300.inputs import qkv_bf16
+        from causal_scaled_dot_gb300.inputs import qkv_bf16, qkv_e4m3
         self.oracle = oracle
         self.w = w
-        self.q, self.k, self.v = qkv_bf16(w.B, w.Hq, w.Hkv, w.S, w.D, seed=w.seed, sigma=w.sigma)
+        self.fp8 = fp8
+        gen = qkv_e4m3 if fp8 else qkv_bf16
+        self.q, self.k, self.v = gen(w.B, w.Hq, w.Hkv, w.S, w.D, seed=w.seed, sigma=w.sigma)
         self.threads = oracle.default_threads()
         self.total = w.B * w.Hq * w.S
         self.row_flops = (2.0 if w.causal else 4.0) * w.S * w.D
@@ -173,8 +175,12 @@ class OracleTimer:
 
     def run(self, n, seed):
         rows = np.random.default_rng(seed).integers(0, self.total, n)
-        self.oracle.attention(self.q, self.k, self.v, self.w.scale, self.w.causal, rows=rows,
-                              nthreads=self.threads)
+        if self.fp8:
+            self.oracle.attention_e4m3(self.q, self.k, self.v, self.w.scale, (1.0, 1.0, 1.0),
+                                       self.w.causal, rows=rows, nthreads=self.threads)
+        else:
+            self.oracle.attention(self.q, self.k, self.v, self.w.scale, self.w.causal, rows=rows,
+                                  nthreads=self.threads)
 
     def rows_for(self, seconds):
         return int(min(self.total, max(self.threads, seconds / max(self.sec_per_row, 1e-9))))
@@ -191,7 +197,7 @@ class OracleTimer:
 def run_reference(args, w, rank, world):
     if rank != 0:
         return 0
-    timer = OracleTimer(w)
+    timer = OracleTimer(w, fp8=args.dtype == "fp8")
     # The whole run (warm-up and timed steps) stays within a few minutes.
     step_s = min(args.ref_step_seconds, args.ref_total_seconds / max(1, args.steps + args.warmup))
     for i in range(args.warmup):
@@ -208,8 +214,9 @@ def run_reference(args, w, rank, world):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": secs / len(samples) * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded N(0,1) bf16)",
-        "config": {"workload": w.name, **w.shape_dict, "causal": w.causal},
+        "data": f"synthetic (seeded N(0,1) {'e4m3' if args.dtype == 'fp8' else 'bf16'})",
+        "config": {"workload": w.name, **w.shape_dict, "causal": w.causal,
+                   "inputs": "e4m3" if args.dtype == "fp8" else "bf16"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": timer.threads,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -223,25 +230,32 @@ def run_reference(args, w, rank, world):
 def run_ours(args, w, rank, world, local):
     import torch
     from causal_scaled_dot_gb300 import native
-    from causal_scaled_dot_gb300.inputs import qkv_bf16
+    from causal_scaled_dot_gb300.inputs import qkv_bf16, qkv_e4m3
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     native.load()
-    q_bits, k_bits, v_bits = qkv_bf16(w.B, w.Hq, w.Hkv, w.S, w.D, seed=w.seed, sigma=w.sigma)
-
-    def host_pinned(bits):
-        return torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).pin_memory()
-
-    qh, kh, vh = host_pinned(q_bits), host_pinned(k_bits), host_pinned(v_bits)
+    fp8 = args.dtype == "fp8"
+    if fp8:
+        codes = qkv_e4m3(w.B, w.Hq, w.Hkv, w.S, w.D, seed=w.seed, sigma=w.sigma)
+        qh, kh, vh = (torch.from_numpy(c).pin_memory() for c in codes)
+    else:
+        bits = qkv_bf16(w.B, w.Hq, w.Hkv, w.S, w.D, seed=w.seed, sigma=w.sigma)
+        qh, kh, vh = (torch.from_numpy(b.view(np.int16).copy()).view(torch.bfloat16).pin_memory()
+                      for b in bits)
     q, k, v = qh.to(dev), kh.to(dev), vh.to(dev)
-    out = torch.empty_like(q)
+    out = torch.empty((w.B, w.Hq, w.S, w.D), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((w.B, w.Hq, w.S), dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        native.attn_fwd(q, k, v, out, lse, w.B, w.Hq, w.Hkv, w.S, w.D, w.scale, w.causal, stream)
+        if fp8:
+            native.attn_fwd_fp8(q, k, v, 1.0, 1.0, 1.0, out, lse, w.B, w.Hq, w.Hkv, w.S, w.D,
+                                w.scale, w.causal, stream)
+        else:
+            native.attn_fwd(q, k, v, out, lse, w.B, w.Hq, w.Hkv, w.S, w.D, w.scale, w.causal,
+                            stream)
 
     for _ in range(args.warmup):
         flush.fill_(1.0)
@@ -295,18 +309,24 @@ def run_ours(args, w, rank, world, local):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = reduce_max(e0.elapsed_time(e1) / e2e_steps, world)
-    h2d = (qh.numel() + kh.numel() + vh.numel()) * 2
+    h2d = (qh.numel() + kh.numel() + vh.numel()) * qh.element_size()
     d2h = out_h.numel() * 2 + lse_h.numel() * 4
 
     if rank != 0:
         return 0
     peaks, peak_src = load_peaks()
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    peak_what = f"{peak_src} bf16 dense (burst)"
+    if fp8:  # no measured fp8 peak: the bf16 one times the nominal fp8/bf16 ratio (4.5 / 2.25)
+        peak *= 2.0
+        peak_what = f"{peak_src} bf16 dense (burst) x 2, the nominal fp8/bf16 ratio"
     achieved = w.flops / (ms_local * 1e-3) / 1e12
-    traffic = recorded_traffic(w.name)
+    traffic = None if fp8 else recorded_traffic(w.name)
+    # algorithmic bytes: inputs read once (1 byte per element for E4M3), O and LSE written once
+    io_bytes = w.io_bytes - (w.B * (w.Hq + 2 * w.Hkv) * w.S * w.D if fp8 else 0)
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        timer = OracleTimer(w)
+        timer = OracleTimer(w, fp8=fp8)
         tf, n, dt = timer.sample(args.cpu_seconds, seed=7)
         cpu = {"value": tf, "unit": "TFLOP/s", "cores": timer.threads, "kind": "oracle",
                "sample": f"{n} random query rows of {w.name} (of {timer.total}), "
@@ -314,16 +334,18 @@ def run_ours(args, w, rank, world, local):
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded N(0,1) bf16, no weights)",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8 (e4m3 inputs, bf16 output)" if fp8 else "bf16",
+        "data": f"synthetic (seeded N(0,1) {'e4m3' if fp8 else 'bf16'}, no weights)",
         "config": {"workload": w.name, **w.shape_dict, "causal": w.causal,
+                   "inputs": "e4m3" if fp8 else "bf16",
                    "l2": "flushed between timed steps (256 MiB write)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "pct_of_peak": 100.0 * achieved / peak,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "peak_source": f"{peak_src} bf16 dense (burst)",
-                     "hbm_gbs": w.io_bytes / (ms_local * 1e-3) / 1e9},
+                     "peak_source": peak_what,
+                     "hbm_gbs": io_bytes / (ms_local * 1e-3) / 1e9},
         "cpu_baseline": cpu,
         "e2e": {"value": world * w.flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
@@ -343,6 +365,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=HEADLINE.name, choices=sorted(BY_NAME))
+    ap.add_argument("--dtype", default="bf16", choices=["bf16", "fp8"],
+                    help="input format: bf16 (attn_fwd) or E4M3 (attn_fwd_fp8, D = 128 only)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="budget of the oracle CPU-baseline sample")
     ap.add_argument("--ref-step-seconds", type=float, default=8.0,

@@ -62,8 +62,9 @@ int setup_device_locked(int dev) {
     if (cudaGetSymbolAddress(&word, g_attn_status) != cudaSuccess ||
         allow_smem(attn_fwd_simple_kernel<64>, SimpleLayout<64>::kDynamicSmem) != cudaSuccess ||
         allow_smem(attn_fwd_simple_kernel<128>, SimpleLayout<128>::kDynamicSmem) != cudaSuccess ||
-        allow_smem(attn_fwd_ws_kernel<64>, WsLayout<64>::kDynamicSmem) != cudaSuccess ||
-        allow_smem(attn_fwd_ws_kernel<128>, WsLayout<128>::kDynamicSmem) != cudaSuccess) {
+        allow_smem(attn_fwd_ws_kernel<64, false>, WsLayout<64, false>::kDynamicSmem) != cudaSuccess ||
+        allow_smem(attn_fwd_ws_kernel<128, false>, WsLayout<128, false>::kDynamicSmem) != cudaSuccess ||
+        allow_smem(attn_fwd_ws_kernel<128, true>, WsLayout<128, true>::kDynamicSmem) != cudaSuccess) {
         st.status = ATTN_ERR_DEVICE;
         return st.status;
     }
@@ -92,20 +93,25 @@ int current_device_state(DeviceState** out) {
     return rc;
 }
 
-// Rank-3 view [rows_outer, S, D] of a contiguous bf16 [.., S, D] tensor, box
-// {64, box_rows, 1}, 128-byte swizzle: one box fills box_rows rows of 128 bytes,
-// the canonical K-major (and MN-major) SW128 operand layout.  Rows past S read
-// as zero.
-int encode_bf16_3d(CUtensorMap* map, const void* ptr, int D, int S, long long outer, int box_rows) {
+// Rank-3 view [rows_outer, S, D] of a contiguous [.., S, D] tensor whose
+// elements are `elem_bytes` wide, box {128 bytes of a row, box_rows, 1},
+// 128-byte swizzle: one box fills box_rows rows of 128 bytes, the canonical
+// K-major (and MN-major) SW128 operand layout.  Rows past S read as zero.
+int encode_3d(CUtensorMap* map, const void* ptr, int elem_bytes, int D, int S, long long outer,
+              int box_rows) {
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)outer};
-    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)S * (cuuint64_t)D * 2};
-    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+    cuuint64_t strides[2] = {(cuuint64_t)D * elem_bytes, (cuuint64_t)S * (cuuint64_t)D * elem_bytes};
+    cuuint32_t box[3] = {(cuuint32_t)(128 / elem_bytes), (cuuint32_t)box_rows, 1};
     cuuint32_t elem[3] = {1, 1, 1};
-    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims,
-                          strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    const CUtensorMapDataType type =
+        elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    CUresult r = g_encode(map, type, 3, const_cast<void*>(ptr), dims, strides, box, elem,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_INVALID_ARG;
+}
+int encode_bf16_3d(CUtensorMap* map, const void* ptr, int D, int S, long long outer, int box_rows) {
+    return encode_3d(map, ptr, 2, D, S, outer, box_rows);
 }
 
 bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
@@ -114,7 +120,7 @@ bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
 }
 
 int check_args(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
-               int Hkv, int S, int D, float scale) {
+               int Hkv, int S, int D, float scale, int in_elem_bytes = 2) {
     if (!q || !k || !v || !out) return ATTN_ERR_INVALID_ARG;
     if (B < 1 || Hq < 1 || Hkv < 1 || S < 1) return ATTN_ERR_INVALID_ARG;
     if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
@@ -125,13 +131,15 @@ int check_args(const void* q, const void* k, const void* v, void* out, float* ls
     const uintptr_t mis = (reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
                            reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out)) & 15u;
     if (mis || (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_MISALIGNED;
-    const size_t q_bytes = (size_t)B * Hq * S * D * 2, kv_bytes = (size_t)B * Hkv * S * D * 2;
-    if (ranges_overlap(out, q_bytes, q, q_bytes) || ranges_overlap(out, q_bytes, k, kv_bytes) ||
-        ranges_overlap(out, q_bytes, v, kv_bytes))
+    const size_t q_bytes = (size_t)B * Hq * S * D * in_elem_bytes;
+    const size_t kv_bytes = (size_t)B * Hkv * S * D * in_elem_bytes;
+    const size_t o_bytes = (size_t)B * Hq * S * D * 2;
+    if (ranges_overlap(out, o_bytes, q, q_bytes) || ranges_overlap(out, o_bytes, k, kv_bytes) ||
+        ranges_overlap(out, o_bytes, v, kv_bytes))
         return ATTN_ERR_INVALID_ARG;
     if (lse) {
         const size_t l_bytes = (size_t)B * Hq * S * 4;
-        if (ranges_overlap(lse, l_bytes, out, q_bytes) || ranges_overlap(lse, l_bytes, q, q_bytes) ||
+        if (ranges_overlap(lse, l_bytes, out, o_bytes) || ranges_overlap(lse, l_bytes, q, q_bytes) ||
             ranges_overlap(lse, l_bytes, k, kv_bytes) || ranges_overlap(lse, l_bytes, v, kv_bytes))
             return ATTN_ERR_INVALID_ARG;
     }
@@ -147,7 +155,7 @@ int launch_simple(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMa
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
-template <int D>
+template <int D, bool F>
 int launch_ws(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, FwdParams p,
               int sm_count, cudaStream_t stream) {
     const long long npairs = (p.num_q_tiles + 1) / 2;
@@ -155,8 +163,8 @@ int launch_ws(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& t
     if (units > (1ll << 31) - 1) return ATTN_ERR_UNSUPPORTED;
     p.num_units = (int)units;
     const int grid = (int)(units < sm_count ? units : sm_count);
-    attn_fwd_ws_kernel<D><<<grid, WsLayout<D>::kThreads, WsLayout<D>::kDynamicSmem, stream>>>(tq, tk,
-                                                                                           tv, p);
+    attn_fwd_ws_kernel<D, F><<<grid, WsLayout<D, F>::kThreads, WsLayout<D, F>::kDynamicSmem, stream>>>(
+        tq, tk, tv, p);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
@@ -216,11 +224,50 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* out, 
     p.lse = lse;
     p.status = dev->status_word;
     p.wait_limit_ns = kWaitLimitNs;
+    p.o_scale = 1.f;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (use_simple_kernel())
         return D == 64 ? launch_simple<64>(tq, tk, tv, p, st) : launch_simple<128>(tq, tk, tv, p, st);
-    return D == 64 ? launch_ws<64>(tq, tk, tv, p, dev->sm_count, st)
-                   : launch_ws<128>(tq, tk, tv, p, dev->sm_count, st);
+    return D == 64 ? launch_ws<64, false>(tq, tk, tv, p, dev->sm_count, st)
+                   : launch_ws<128, false>(tq, tk, tv, p, dev->sm_count, st);
+}
+
+extern "C" int attn_fwd_fp8(const void* q, const void* k, const void* v, float q_descale,
+                            float k_descale, float v_descale, void* out, float* lse, int B, int Hq,
+                            int Hkv, int S, int D, float scale, int causal, void* stream) {
+    int rc = check_args(q, k, v, out, lse, B, Hq, Hkv, S, D, scale, 1);
+    if (rc != ATTN_OK) return rc;
+    for (float d : {q_descale, k_descale, v_descale})
+        if (!std::isfinite(d) || !(d > 0.f)) return ATTN_ERR_INVALID_ARG;
+    if (D != 128) return ATTN_ERR_UNSUPPORTED;
+    DeviceState* dev = nullptr;
+    rc = current_device_state(&dev);
+    if (rc != ATTN_OK) return rc;
+
+    alignas(64) CUtensorMap tq, tk, tv;
+    if (encode_3d(&tq, q, 1, D, S, (long long)B * Hq, kTile) != ATTN_OK ||
+        encode_3d(&tk, k, 1, D, S, (long long)B * Hkv, kTile) != ATTN_OK ||
+        encode_3d(&tv, v, 1, D, S, (long long)B * Hkv, kTile) != ATTN_OK)
+        return ATTN_ERR_INVALID_ARG;
+
+    FwdParams p;
+    std::memset(&p, 0, sizeof p);
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.S = S;
+    p.group = Hq / Hkv;
+    p.num_q_tiles = (S + kTile - 1) / kTile;
+    p.causal = causal ? 1 : 0;
+    // Scores come out of the tensor core in code units: the Q and K descales
+    // join the softmax scale, the V descale scales O at the end.
+    p.scale_log2 = scale * q_descale * k_descale * kLog2e;
+    p.o_scale = v_descale;
+    p.out = static_cast<__nv_bfloat16*>(out);
+    p.lse = lse;
+    p.status = dev->status_word;
+    p.wait_limit_ns = kWaitLimitNs;
+    return launch_ws<128, true>(tq, tk, tv, p, dev->sm_count, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int attn_sync_status(void* stream) {

@@ -23,6 +23,7 @@ struct FwdParams {
     unsigned int* status;           // device status word (timeouts)
     unsigned long long wait_limit_ns;  // bound on every mbarrier wait
     int num_units;                  // persistent kernels: total work units
+    float o_scale;                  // multiplies O at the end (FP8: the V descale; else 1)
 };
 
 }  // namespace attn

@@ -51,8 +51,13 @@ namespace attn {
 
 constexpr float kRescaleSlack = 8.0f;  // log2 units: probabilities stay <= 256
 
-template <int D>
+// F selects FP8 E4M3 inputs (one byte per element; D = 128 only, so that a
+// 128-byte swizzle row is one 128-element row of a tile); otherwise bf16.
+template <int D, bool F>
 struct WsLayout {
+    static_assert(!F || D == 128, "FP8 inputs need D = 128");
+    static constexpr int kElemBytes = F ? 1 : 2;
+    static constexpr int kRowElems = 128 / kElemBytes;       // elements per 128-byte row
     static constexpr int kThreads = 384;
     // Registers per thread after the split: warps 0-3 (producer, MMA issuer,
     // idle) shrink, the softmax warps grow.  Launch allocation: 384 x 168 =
@@ -60,9 +65,9 @@ struct WsLayout {
     static constexpr int kRegsSmall = 56;
     static constexpr int kRegsSoftmax = 216;
     static_assert(128 * kRegsSmall + 256 * kRegsSoftmax <= kThreads * 168, "register split");
-    static constexpr int kStages = (D == 128) ? 4 : 8;     // K/V ring slots, one tile each
-    static constexpr uint32_t kTileBytes = kTile * D * 2;  // 32 KB at D = 128
-    static constexpr int kChunks = D / 64;                 // 64-column swizzle blocks
+    static constexpr uint32_t kTileBytes = kTile * D * kElemBytes;  // 32 KB at bf16 D = 128
+    static constexpr int kStages = (kTileBytes == 32768) ? 4 : 8;    // K/V ring slots, one tile each
+    static constexpr int kChunks = D / kRowElems;                    // 128-byte swizzle blocks
     static constexpr uint32_t kChunkBytes = kTile * 128;   // one block of a tile: 16 KB
     static constexpr uint32_t kQ0 = 0;
     static constexpr uint32_t kQ1 = kTileBytes;
@@ -111,17 +116,17 @@ __device__ __forceinline__ int unit_of_round(int r) {
     return r * G + ((r & 1) ? (G - 1 - c) : c);
 }
 
-template <int D>
+template <int D, bool F>
 __device__ __forceinline__ uint32_t ws_bar(uint32_t base, int i) {
-    return base + WsLayout<D>::kBars + 8u * (uint32_t)i;
+    return base + WsLayout<D, F>::kBars + 8u * (uint32_t)i;
 }
 
 // ---------------------------------------------------------------- producer
-template <int D>
+template <int D, bool F>
 __device__ void ws_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                              const CUtensorMap* tm_v, const FwdParams& p, uint32_t base,
                              volatile int* abort_flag) {
-    using L = WsLayout<D>;
+    using L = WsLayout<D, F>;
     uint32_t qe_phase[2] = {0u, 0u};
     int slot = 0;
     uint32_t ring_phase = 0;
@@ -131,16 +136,16 @@ __device__ void ws_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
     for (int rnd = 0, u = unit_of_round(0); u < p.num_units; u = unit_of_round(++rnd)) {
         const Unit w = decode_unit(u, p);
         for (int i = 0; i < 2; ++i) {
-            if (!ptx::mbar_wait(ws_bar<D>(base, L::kQEmpty + i), qe_phase[i] ^ 1u, abort_flag,
+            if (!ptx::mbar_wait(ws_bar<D, F>(base, L::kQEmpty + i), qe_phase[i] ^ 1u, abort_flag,
                                 p.status, lim))
                 goto drain;
             qe_phase[i] ^= 1u;
-            const uint32_t full = ws_bar<D>(base, L::kQFull + i);
+            const uint32_t full = ws_bar<D, F>(base, L::kQFull + i);
             ptx::mbar_arrive_expect_tx(full, L::kTileBytes);
             const uint32_t dst = base + (i == 0 ? L::kQ0 : L::kQ1);
 #pragma unroll
             for (int c = 0; c < L::kChunks; ++c)
-                ptx::tma_load_3d(dst + c * L::kChunkBytes, tm_q, full, c * 64, (2 * w.m + i) * kTile,
+                ptx::tma_load_3d(dst + c * L::kChunkBytes, tm_q, full, c * L::kRowElems, (2 * w.m + i) * kTile,
                                  w.bh);
             pend_q |= 1u << i;
             pend_q_par = (pend_q_par & ~(1u << i)) | (((qe_phase[i] ^ 1u) & 1u) << i);
@@ -148,16 +153,16 @@ __device__ void ws_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
         for (int j = 0; j < w.n; ++j) {
 #pragma unroll
             for (int t = 0; t < 2; ++t) {  // t = 0: K_j, t = 1: V_j
-                if (!ptx::mbar_wait(ws_bar<D>(base, L::kKVEmpty + slot), ring_phase ^ 1u, abort_flag,
+                if (!ptx::mbar_wait(ws_bar<D, F>(base, L::kKVEmpty + slot), ring_phase ^ 1u, abort_flag,
                                     p.status, lim))
                     goto drain;
-                const uint32_t full = ws_bar<D>(base, L::kKVFull + slot);
+                const uint32_t full = ws_bar<D, F>(base, L::kKVFull + slot);
                 ptx::mbar_arrive_expect_tx(full, L::kTileBytes);
                 const uint32_t dst = base + L::kRing + (uint32_t)slot * L::kTileBytes;
                 const CUtensorMap* map = t == 0 ? tm_k : tm_v;
 #pragma unroll
                 for (int c = 0; c < L::kChunks; ++c)
-                    ptx::tma_load_3d(dst + c * L::kChunkBytes, map, full, c * 64, j * kTile, w.kv_bh);
+                    ptx::tma_load_3d(dst + c * L::kChunkBytes, map, full, c * L::kRowElems, j * kTile, w.kv_bh);
                 pend_kv |= 1u << slot;
                 pend_kv_par = (pend_kv_par & ~(1u << slot)) | (ring_phase << slot);
                 if (++slot == L::kStages) {
@@ -172,19 +177,21 @@ drain:
     // Let every copy already issued land before the CTA can exit.
     for (int s = 0; s < L::kStages; ++s)
         if (pend_kv & (1u << s))
-            ptx::drain_wait(ws_bar<D>(base, L::kKVFull + s), (pend_kv_par >> s) & 1u, lim);
+            ptx::drain_wait(ws_bar<D, F>(base, L::kKVFull + s), (pend_kv_par >> s) & 1u, lim);
     for (int i = 0; i < 2; ++i)
         if (pend_q & (1u << i))
-            ptx::drain_wait(ws_bar<D>(base, L::kQFull + i), ((pend_q_par >> i) & 1u) ^ 0u, lim);
+            ptx::drain_wait(ws_bar<D, F>(base, L::kQFull + i), ((pend_q_par >> i) & 1u) ^ 0u, lim);
 }
 
 // ---------------------------------------------------------------- MMA issuer
-template <int D>
+template <int D, bool F>
 __device__ void ws_mma_role(const FwdParams& p, uint32_t base, uint32_t tmem,
                             volatile int* abort_flag) {
-    using L = WsLayout<D>;
-    constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(kTile, kTile, false);
-    constexpr uint32_t kIdescO = ptx::idesc_bf16_f32(kTile, D, true);
+    using L = WsLayout<D, F>;
+    constexpr uint32_t kIdescS = F ? ptx::idesc_e4m3_f32(kTile, kTile, false)
+                                   : ptx::idesc_bf16_f32(kTile, kTile, false);
+    constexpr uint32_t kIdescO = F ? ptx::idesc_e4m3_f32(kTile, D, true)
+                                   : ptx::idesc_bf16_f32(kTile, D, true);
     const uint64_t lim = p.wait_limit_ns;
     uint32_t qf_phase = 0;
     uint32_t pf_phase[2] = {0u, 0u};
@@ -195,24 +202,31 @@ __device__ void ws_mma_role(const FwdParams& p, uint32_t base, uint32_t tmem,
     auto issue_s = [&](int i, int ks) {
         const uint64_t a = ptx::sdesc_sw128(base + (i == 0 ? L::kQ0 : L::kQ1), 16, 1024);
         const uint64_t b = ptx::sdesc_sw128(base + L::kRing + (uint32_t)ks * L::kTileBytes, 16, 1024);
-        if (D == 128)
+        if constexpr (F)
+            ptx::mma_ss_f8_k128(tmem + (uint32_t)i * kTile, a, b, kIdescS, 0u);
+        else if constexpr (D == 128)
             ptx::mma_ss_k128(tmem + (uint32_t)i * kTile, a, b, kIdescS, 0u);
         else
             ptx::mma_ss_k64(tmem + (uint32_t)i * kTile, a, b, kIdescS, 0u);
-        ptx::mma_commit(ws_bar<D>(base, L::kSFull + i));
+        ptx::mma_commit(ws_bar<D, F>(base, L::kSFull + i));
     };
-    // O_i (+)= P_i V with P_i in TMEM columns [64,128) of S_i and V in slot `vs`:
-    // keys 0-63 then keys 64-127 (8 KB further into V, 32 TMEM columns further into P).
+    // O_i (+)= P_i V with V in slot `vs`.  bf16: P_i in TMEM columns [64,128) of
+    // S_i, keys 0-63 then keys 64-127 (8 KB further into V, 32 TMEM columns
+    // further into P).  FP8: P_i in columns [96,128), all 128 keys at once.
     auto issue_pv = [&](int i, int vs, bool accumulate) {
         const uint64_t v = ptx::sdesc_sw128(base + L::kRing + (uint32_t)vs * L::kTileBytes,
                                             L::kChunkBytes, 1024);
         const uint32_t o = tmem + 256u + (uint32_t)i * D;
-        const uint32_t pcol = tmem + (uint32_t)i * kTile + 64u;
-        ptx::mma_ts_k64(o, pcol, v, kIdescO, accumulate ? 1u : 0u);
-        ptx::mma_ts_k64(o, pcol + 32u, v + 512u, kIdescO, 1u);
+        if constexpr (F) {
+            ptx::mma_ts_f8_k128(o, tmem + (uint32_t)i * kTile + 96u, v, kIdescO, accumulate ? 1u : 0u);
+        } else {
+            const uint32_t pcol = tmem + (uint32_t)i * kTile + 64u;
+            ptx::mma_ts_k64(o, pcol, v, kIdescO, accumulate ? 1u : 0u);
+            ptx::mma_ts_k64(o, pcol + 32u, v + 512u, kIdescO, 1u);
+        }
     };
     auto wait_ring = [&](int& got) -> bool {
-        if (!ptx::mbar_wait(ws_bar<D>(base, L::kKVFull + slot), ring_phase, abort_flag, p.status, lim))
+        if (!ptx::mbar_wait(ws_bar<D, F>(base, L::kKVFull + slot), ring_phase, abort_flag, p.status, lim))
             return false;
         got = slot;
         if (++slot == L::kStages) {
@@ -223,7 +237,7 @@ __device__ void ws_mma_role(const FwdParams& p, uint32_t base, uint32_t tmem,
         return true;
     };
     auto wait_p = [&](int i) -> bool {
-        if (!ptx::mbar_wait(ws_bar<D>(base, L::kPFull + i), pf_phase[i], abort_flag, p.status, lim))
+        if (!ptx::mbar_wait(ws_bar<D, F>(base, L::kPFull + i), pf_phase[i], abort_flag, p.status, lim))
             return false;
         pf_phase[i] ^= 1u;
         ptx::tc_fence_after();
@@ -232,68 +246,68 @@ __device__ void ws_mma_role(const FwdParams& p, uint32_t base, uint32_t tmem,
 
     for (int rnd = 0, u = unit_of_round(0); u < p.num_units; u = unit_of_round(++rnd)) {
         const Unit w = decode_unit(u, p);
-        if (!ptx::mbar_wait(ws_bar<D>(base, L::kQFull + 0), qf_phase, abort_flag, p.status, lim) ||
-            !ptx::mbar_wait(ws_bar<D>(base, L::kQFull + 1), qf_phase, abort_flag, p.status, lim))
+        if (!ptx::mbar_wait(ws_bar<D, F>(base, L::kQFull + 0), qf_phase, abort_flag, p.status, lim) ||
+            !ptx::mbar_wait(ws_bar<D, F>(base, L::kQFull + 1), qf_phase, abort_flag, p.status, lim))
             break;
         qf_phase ^= 1u;
         int kslot, vslot;
         if (!wait_ring(kslot)) break;
         issue_s(0, kslot);
-        if (w.n0 == 1) ptx::mma_commit(ws_bar<D>(base, L::kQEmpty + 0));
+        if (w.n0 == 1) ptx::mma_commit(ws_bar<D, F>(base, L::kQEmpty + 0));
         issue_s(1, kslot);
-        if (w.n1 == 1) ptx::mma_commit(ws_bar<D>(base, L::kQEmpty + 1));
-        ptx::mma_commit(ws_bar<D>(base, L::kKVEmpty + kslot));
+        if (w.n1 == 1) ptx::mma_commit(ws_bar<D, F>(base, L::kQEmpty + 1));
+        ptx::mma_commit(ws_bar<D, F>(base, L::kKVEmpty + kslot));
         bool ok = true;
         for (int j = 0; j < w.n && ok; ++j) {
             if (!(ok = wait_ring(vslot))) break;
             if (j < w.n0) {
                 if (!(ok = wait_p(0))) break;
                 issue_pv(0, vslot, j > 0);
-                if (j == w.n0 - 1) ptx::mma_commit(ws_bar<D>(base, L::kOFull + 0));
+                if (j == w.n0 - 1) ptx::mma_commit(ws_bar<D, F>(base, L::kOFull + 0));
             }
             const bool more = j + 1 < w.n;
             if (more) {
                 if (!(ok = wait_ring(kslot))) break;
                 if (j + 1 < w.n0) {
                     issue_s(0, kslot);
-                    if (j + 1 == w.n0 - 1) ptx::mma_commit(ws_bar<D>(base, L::kQEmpty + 0));
+                    if (j + 1 == w.n0 - 1) ptx::mma_commit(ws_bar<D, F>(base, L::kQEmpty + 0));
                 }
             }
             if (j < w.n1) {
                 if (!(ok = wait_p(1))) break;
                 issue_pv(1, vslot, j > 0);
-                if (j == w.n1 - 1) ptx::mma_commit(ws_bar<D>(base, L::kOFull + 1));
+                if (j == w.n1 - 1) ptx::mma_commit(ws_bar<D, F>(base, L::kOFull + 1));
             }
-            ptx::mma_commit(ws_bar<D>(base, L::kKVEmpty + vslot));
+            ptx::mma_commit(ws_bar<D, F>(base, L::kKVEmpty + vslot));
             if (more) {
                 if (j + 1 < w.n1) {
                     issue_s(1, kslot);
-                    if (j + 1 == w.n1 - 1) ptx::mma_commit(ws_bar<D>(base, L::kQEmpty + 1));
+                    if (j + 1 == w.n1 - 1) ptx::mma_commit(ws_bar<D, F>(base, L::kQEmpty + 1));
                 }
-                ptx::mma_commit(ws_bar<D>(base, L::kKVEmpty + kslot));
+                ptx::mma_commit(ws_bar<D, F>(base, L::kKVEmpty + kslot));
             }
         }
         if (!ok) break;
     }
     // Every MMA issued above completes before TMEM can be released.
-    ptx::mma_commit(ws_bar<D>(base, L::kDrain));
-    ptx::drain_wait(ws_bar<D>(base, L::kDrain), 0u, lim);
+    ptx::mma_commit(ws_bar<D, F>(base, L::kDrain));
+    ptx::drain_wait(ws_bar<D, F>(base, L::kDrain), 0u, lim);
 }
 
 // ---------------------------------------------------------------- softmax
-template <int D>
+template <int D, bool F>
 __device__ void ws_softmax_role(const FwdParams& p, uint32_t base, uint32_t tmem, int wg,
                                 volatile int* abort_flag) {
-    using L = WsLayout<D>;
+    using L = WsLayout<D, F>;
     const int r = threadIdx.x - (4 + 4 * wg) * 32;  // row within the query tile, 0..127
     const int warp_in_wg = r >> 5;
     const uint32_t lane_off = (uint32_t)(warp_in_wg * 32) << 16;
     const uint32_t tS = tmem + lane_off + (uint32_t)wg * kTile;
     const uint32_t tP = tS + 64u;
     const uint32_t tO = tmem + lane_off + 256u + (uint32_t)wg * D;
-    const uint32_t bar_s = ws_bar<D>(base, L::kSFull + wg);
-    const uint32_t bar_p = ws_bar<D>(base, L::kPFull + wg);
-    const uint32_t bar_o = ws_bar<D>(base, L::kOFull + wg);
+    const uint32_t bar_s = ws_bar<D, F>(base, L::kSFull + wg);
+    const uint32_t bar_p = ws_bar<D, F>(base, L::kPFull + wg);
+    const uint32_t bar_o = ws_bar<D, F>(base, L::kOFull + wg);
     const float sl2 = p.scale_log2;
     const uint64_t lim = p.wait_limit_ns;
     uint32_t s_phase = 0, o_phase = 0;
@@ -355,20 +369,41 @@ __device__ void ws_softmax_role(const FwdParams& p, uint32_t base, uint32_t tmem
             const uint64_t sl2x2 = ptx::f2(sl2, sl2);
             const uint64_t negm2 = ptx::f2(-m_run, -m_run);
             uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+            if constexpr (F) {
+                // FP8: four E4M3 probabilities per column, 64 keys per store,
+                // over score columns [96,128) of S_i (already read).
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t pk[32];
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t pk[16];
 #pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    const int e = 64 * h + 2 * c;
-                    float x0, x1;
-                    ptx::f2_split(ptx::fma2(ptx::f2(s[e], s[e + 1]), sl2x2, negm2), x0, x1);
-                    const float p0 = ptx::ex2(x0);
-                    const float p1 = ptx::ex2(x1);
-                    acc[c & 3] = ptx::add2(acc[c & 3], ptx::f2(p0, p1));
-                    pk[c] = ptx::pack_bf16x2(p0, p1);
+                    for (int c = 0; c < 16; ++c) {
+                        const int e = 64 * h + 4 * c;
+                        float x0, x1, x2, x3;
+                        ptx::f2_split(ptx::fma2(ptx::f2(s[e], s[e + 1]), sl2x2, negm2), x0, x1);
+                        ptx::f2_split(ptx::fma2(ptx::f2(s[e + 2], s[e + 3]), sl2x2, negm2), x2, x3);
+                        const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
+                        const float p2 = ptx::ex2(x2), p3 = ptx::ex2(x3);
+                        acc[c & 3] = ptx::add2(acc[c & 3], ptx::add2(ptx::f2(p0, p1), ptx::f2(p2, p3)));
+                        pk[c] = ptx::pack_e4m3x4(p0, p1, p2, p3);
+                    }
+                    ptx::tmem_st16(tP + 32u + 16u * h, pk);
                 }
-                ptx::tmem_st32(tP + 32 * h, pk);
+            } else {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        const int e = 64 * h + 2 * c;
+                        float x0, x1;
+                        ptx::f2_split(ptx::fma2(ptx::f2(s[e], s[e + 1]), sl2x2, negm2), x0, x1);
+                        const float p0 = ptx::ex2(x0);
+                        const float p1 = ptx::ex2(x1);
+                        acc[c & 3] = ptx::add2(acc[c & 3], ptx::f2(p0, p1));
+                        pk[c] = ptx::pack_bf16x2(p0, p1);
+                    }
+                    ptx::tmem_st32(tP + 32 * h, pk);
+                }
             }
             float sum0, sum1, sum2, sum3, sum4, sum5, sum6, sum7;
             ptx::f2_split(acc[0], sum0, sum1);
@@ -406,7 +441,7 @@ __device__ void ws_softmax_role(const FwdParams& p, uint32_t base, uint32_t tmem
         ptx::tc_fence_after();
         const int row = qt * kTile + r;
         const bool valid = row < p.S;
-        const float inv_l = 1.f / l_run;
+        const float inv_l = p.o_scale / l_run;  // o_scale: the V descale (1 for bf16)
         __nv_bfloat16* orow = p.out + ((size_t)w.bh * p.S + row) * D;
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
@@ -437,12 +472,12 @@ __device__ void ws_softmax_role(const FwdParams& p, uint32_t base, uint32_t tmem
 }
 
 // ---------------------------------------------------------------- kernel
-template <int D>
-__global__ void __launch_bounds__(WsLayout<D>::kThreads, 1)
+template <int D, bool F>
+__global__ void __launch_bounds__(WsLayout<D, F>::kThreads, 1)
     attn_fwd_ws_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
-    using L = WsLayout<D>;
+    using L = WsLayout<D, F>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -454,17 +489,17 @@ __global__ void __launch_bounds__(WsLayout<D>::kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < 2; ++i) {
-            ptx::mbar_init(ws_bar<D>(base, L::kQFull + i), 1);
-            ptx::mbar_init(ws_bar<D>(base, L::kQEmpty + i), 1);
-            ptx::mbar_init(ws_bar<D>(base, L::kSFull + i), 1);
-            ptx::mbar_init(ws_bar<D>(base, L::kPFull + i), 4);  // one per softmax warp
-            ptx::mbar_init(ws_bar<D>(base, L::kOFull + i), 1);
+            ptx::mbar_init(ws_bar<D, F>(base, L::kQFull + i), 1);
+            ptx::mbar_init(ws_bar<D, F>(base, L::kQEmpty + i), 1);
+            ptx::mbar_init(ws_bar<D, F>(base, L::kSFull + i), 1);
+            ptx::mbar_init(ws_bar<D, F>(base, L::kPFull + i), 4);  // one per softmax warp
+            ptx::mbar_init(ws_bar<D, F>(base, L::kOFull + i), 1);
         }
         for (int s = 0; s < L::kStages; ++s) {
-            ptx::mbar_init(ws_bar<D>(base, L::kKVFull + s), 1);
-            ptx::mbar_init(ws_bar<D>(base, L::kKVEmpty + s), 1);
+            ptx::mbar_init(ws_bar<D, F>(base, L::kKVFull + s), 1);
+            ptx::mbar_init(ws_bar<D, F>(base, L::kKVEmpty + s), 1);
         }
-        ptx::mbar_init(ws_bar<D>(base, L::kDrain), 1);
+        ptx::mbar_init(ws_bar<D, F>(base, L::kDrain), 1);
         *abort_flag = 0;
         ptx::fence_barrier_init();
         ptx::prefetch_tensormap(&tm_q);
@@ -483,13 +518,13 @@ __global__ void __launch_bounds__(WsLayout<D>::kThreads, 1)
     if (warp < 4) {
         ptx::regs_dec<L::kRegsSmall>();
         if (warp == 0) {
-            if (lane == 0) ws_load_role<D>(&tm_q, &tm_k, &tm_v, p, base, abort_flag);
+            if (lane == 0) ws_load_role<D, F>(&tm_q, &tm_k, &tm_v, p, base, abort_flag);
         } else if (warp == 1) {
-            if (lane == 0) ws_mma_role<D>(p, base, tmem, abort_flag);
+            if (lane == 0) ws_mma_role<D, F>(p, base, tmem, abort_flag);
         }
     } else {
         ptx::regs_inc<L::kRegsSoftmax>();
-        ws_softmax_role<D>(p, base, tmem, (warp - 4) >> 2, abort_flag);
+        ws_softmax_role<D, F>(p, base, tmem, (warp - 4) >> 2, abort_flag);
     }
 
     ptx::tc_fence_before();

@@ -236,6 +236,43 @@ __device__ __forceinline__ void mma_ts_k64(uint32_t d, uint32_t a, uint64_t b, u
         : "memory");
 }
 
+// FP8 (E4M3) products, kind::f8f6f4, K = 32 per instruction.  A 128-byte
+// swizzle row holds 128 elements, so K = 128 is one row: four steps 32 bytes
+// apart, with A and B K-major.
+__device__ __forceinline__ void mma_ss_f8_k128(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                               uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 a, b;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t"
+        "add.s64 a, %1, 2; add.s64 b, %2, 2;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a, b, %3, 1;\n\t"
+        "add.s64 a, %1, 4; add.s64 b, %2, 4;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a, b, %3, 1;\n\t"
+        "add.s64 a, %1, 6; add.s64 b, %2, 6;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a, b, %3, 1;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// D (+)= A B over 128 keys in four K = 32 steps, A (E4M3, four per column) read
+// from tensor memory columns a + 8*kk, B an MN-major SW128 E4M3 tile whose K
+// rows advance 32 rows = 4096 bytes per step.
+__device__ __forceinline__ void mma_ts_f8_k128(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc,
+                                               uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 b;\n\t.reg .b32 a;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t"
+        "add.s32 a, %1, 8; add.s64 b, %2, 256;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [a], b, %3, 1;\n\t"
+        "add.s32 a, %1, 16; add.s64 b, %2, 512;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [a], b, %3, 1;\n\t"
+        "add.s32 a, %1, 24; add.s64 b, %2, 768;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [a], b, %3, 1;\n\t}" ::"r"(d),
+        "r"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 async op issued so far by this thread completes.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile(
@@ -250,6 +287,13 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_major) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Instruction descriptor for kind::f8f6f4 with E4M3 A and B, fp32 D, dense:
+// the same fields as above with A and B formats 0 (E4M3).
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N, bool b_mn_major) {
+    return (1u << 4) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
 }
 
 // Shared-memory matrix descriptor, 128-byte swizzle.
@@ -383,6 +427,14 @@ __device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
     uint64_t d;
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
+}
+// Four floats -> four E4M3 codes (round to nearest even, saturating at 448)
+// packed little-endian: x0 in bits 0-7 ... x3 in bits 24-31.
+__device__ __forceinline__ uint32_t pack_e4m3x4(float x0, float x1, float x2, float x3) {
+    uint16_t lo, hi;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(x1), "f"(x0));
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(x3), "f"(x2));
+    return (uint32_t)lo | ((uint32_t)hi << 16);
 }
 // Two floats -> packed bf16x2 (round to nearest even); `lo` in bits 0-15.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

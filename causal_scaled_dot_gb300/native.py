@@ -44,6 +44,9 @@ def load() -> ctypes.CDLL:
         vp, ci = ctypes.c_void_p, ctypes.c_int
         lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ctypes.c_float, ci, vp]
         lib.attn_fwd.restype = ci
+        cf = ctypes.c_float
+        lib.attn_fwd_fp8.argtypes = [vp, vp, vp, cf, cf, cf, vp, vp, ci, ci, ci, ci, ci, cf, ci, vp]
+        lib.attn_fwd_fp8.restype = ci
         lib.attn_sync_status.argtypes = [vp]
         lib.attn_sync_status.restype = ci
         lib.attn_selftest_wait_timeout.argtypes = [ci, vp]
@@ -98,6 +101,19 @@ def attn_fwd(q, k, v, out, lse, B: int, Hq: int, Hkv: int, S: int, D: int, scale
                          _stream(stream))
     if check and rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd")
+    return rc
+
+
+def attn_fwd_fp8(q, k, v, q_descale: float, k_descale: float, v_descale: float, out, lse, B: int,
+                 Hq: int, Hkv: int, S: int, D: int, scale: float, causal: bool | int, stream=None,
+                 check: bool = True) -> int:
+    """The C entry point ``attn_fwd_fp8`` (E4M3 inputs with per-tensor descales),
+    same argument order; tensors or raw device pointers as in ``attn_fwd``."""
+    rc = load().attn_fwd_fp8(_ptr(q), _ptr(k), _ptr(v), float(q_descale), float(k_descale),
+                             float(v_descale), _ptr(out), _ptr(lse), int(B), int(Hq), int(Hkv),
+                             int(S), int(D), float(scale), 1 if causal else 0, _stream(stream))
+    if check and rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_fp8")
     return rc
 
 

@@ -75,6 +75,28 @@ int attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse,
              int B, int Hq, int Hkv, int S, int D, float scale, int causal, void *stream);
 
 /*
+ * attn_fwd_fp8 -- the same attention with FP8 E4M3 inputs and per-tensor
+ * descale factors (the FP8 attention the ai-manual.ru article mentions for
+ * newer GPUs, section 6 "FP8 and BF16").
+ *
+ *   q, k, v  E4M3 codes (one byte each, the OCP "fn" encoding), layouts as in
+ *            attn_fwd: q [B,Hq,S,D], k and v [B,Hkv,S,D], contiguous.  Element
+ *            value = decoded code * its tensor's descale.
+ *   q_descale, k_descale, v_descale   finite and > 0.
+ *   out      bf16 [B,Hq,S,D]; lse fp32 [B,Hq,S] or NULL; scale, causal, stream
+ *            as in attn_fwd.
+ *   D        128 only (ATTN_ERR_UNSUPPORTED otherwise).
+ *
+ * Scores accumulate in fp32 from the exact products of the codes; the
+ * probabilities that multiply V are rounded to E4M3 (round to nearest even),
+ * the row sums and LSE use the unrounded fp32 probabilities.  Same alignment,
+ * asynchrony and error rules as attn_fwd.
+ */
+int attn_fwd_fp8(const void *q, const void *k, const void *v, float q_descale, float k_descale,
+                 float v_descale, void *out, float *lse, int B, int Hq, int Hkv, int S, int D,
+                 float scale, int causal, void *stream);
+
+/*
  * attn_sync_status -- synchronise `stream` and report device-side failures of
  * the attention kernels enqueued on this device since the last call.
  *

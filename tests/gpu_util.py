@@ -65,3 +65,45 @@ def sample_rows(B, Hq, S, n_random=256, seed=0):
     rows = {(b * Hq + h) * S + i for (b, h) in heads for i in positions if 0 <= i < S}
     rows |= set(int(x) for x in rng.integers(0, B * Hq * S, size=n_random))
     return np.array(sorted(rows), dtype=np.int64)
+
+
+def run_gpu_fp8(q_codes, k_codes, v_codes, descales, scale, causal, with_lse=True, stream=None):
+    """attn_fwd_fp8 through the C ABI on E4M3 codes; returns (O float64, LSE float64 or None)."""
+    import torch
+    from causal_scaled_dot_gb300 import native
+    B, Hq, S, D = q_codes.shape
+    Hkv = k_codes.shape[1]
+    dev = lambda c: torch.from_numpy(np.ascontiguousarray(c)).cuda()  # noqa: E731
+    q, k, v = dev(q_codes), dev(k_codes), dev(v_codes)
+    out = torch.full((B, Hq, S, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((B, Hq, S), float("nan"), dtype=torch.float32, device="cuda") if with_lse else None
+    native.attn_fwd_fp8(q, k, v, *descales, out, lse, B, Hq, Hkv, S, D, scale, causal, stream=stream)
+    native.attn_sync_status(stream)
+    return out.double().cpu().numpy(), (lse.double().cpu().numpy() if with_lse else None)
+
+
+def fp8_tolerances(v_values, o_ref):
+    """Bounds for FP8 inputs.  The probabilities that multiply V are rounded to
+    E4M3 (3 mantissa bits, round to nearest: relative error <= 2^-4 each), so a
+    row of O moves by at most 2^-4 * max|V| (the weights sum to 1); bf16 output
+    rounding adds 2^-9 * |O|, taken twice.  The relative L2 bound is the
+    per-weight bound 2^-4.  LSE uses the unrounded fp32 probabilities: 1e-3 as
+    for bf16 inputs."""
+    max_abs = 2.0 ** -4 * float(np.max(np.abs(v_values))) + 2.0 ** -8 * float(np.max(np.abs(o_ref)))
+    return max_abs, 2.0 ** -4, TOL_LSE_MAX_ABS
+
+
+def compare_fp8(o_gpu, o_ref, l_gpu, l_ref, v_values, label=""):
+    tol_abs, tol_rel, tol_lse = fp8_tolerances(v_values, o_ref)
+    assert np.all(np.isfinite(o_gpu)), f"{label}: non-finite output (unwritten rows?)"
+    diff = o_gpu - o_ref
+    max_abs = float(np.max(np.abs(diff)))
+    rel_l2 = float(np.linalg.norm(diff) / np.linalg.norm(o_ref))
+    stats = {"max_abs": max_abs, "rel_l2": rel_l2, "tol_abs": tol_abs}
+    assert max_abs <= tol_abs, f"{label}: O max abs error {max_abs:.3e} > {tol_abs:.3e}"
+    assert rel_l2 <= tol_rel, f"{label}: O rel L2 error {rel_l2:.3e} > {tol_rel:.3e}"
+    if l_gpu is not None:
+        lse_err = float(np.max(np.abs(l_gpu - l_ref)))
+        stats["lse_max_abs"] = lse_err
+        assert lse_err <= tol_lse, f"{label}: LSE max abs error {lse_err:.3e} > {tol_lse}"
+    return stats

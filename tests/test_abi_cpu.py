@@ -26,7 +26,7 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for required in ("attn_fwd", "attn_status_string", "attn_sync_status"):
+    for required in ("attn_fwd", "attn_fwd_fp8", "attn_status_string", "attn_sync_status"):
         assert required in names
 
 
@@ -100,3 +100,25 @@ def test_selftest_rejects_bad_limits():
     lib = native.load()
     assert lib.attn_selftest_wait_timeout(0, None) == ATTN_ERR_INVALID_ARG
     assert lib.attn_selftest_wait_timeout(2000000, None) == ATTN_ERR_INVALID_ARG
+
+
+def _call_fp8(q=1 << 40, k=2 << 40, v=3 << 40, out=4 << 40, lse=None, dq=1.0, dk=1.0, dv=1.0, B=1,
+              Hq=2, Hkv=2, S=128, D=128, scale=0.1, causal=1):
+    lib = native.load()
+    f = ctypes.c_float
+    return lib.attn_fwd_fp8(q, k, v, f(dq), f(dk), f(dv), out, lse, B, Hq, Hkv, S, D, f(scale),
+                            causal, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), ATTN_ERR_INVALID_ARG),
+    (dict(dq=0.0), ATTN_ERR_INVALID_ARG),
+    (dict(dk=-1.0), ATTN_ERR_INVALID_ARG),
+    (dict(dv=float("nan")), ATTN_ERR_INVALID_ARG),
+    (dict(D=64), ATTN_ERR_UNSUPPORTED),
+    (dict(Hq=3, Hkv=2), ATTN_ERR_INVALID_ARG),
+    (dict(k=(2 << 40) + 4), ATTN_ERR_MISALIGNED),
+    (dict(out=(1 << 40) + 64), ATTN_ERR_INVALID_ARG),  # out overlaps q
+])
+def test_fp8_argument_errors_are_rejected_before_launch(kw, code):
+    assert _call_fp8(**kw) == code
