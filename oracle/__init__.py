@@ -55,6 +55,9 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     f.restype = ci
     f.argtypes = [vp, vp, vp, cf, cf, cf, ci, ci, ci, ci, ci, cf, ci, vp, ctypes.c_int64, vp, vp,
                   ci]
+    f = lib.oracle_attn_rows_masked
+    f.restype = ci
+    f.argtypes = [vp, vp, vp, ci, ci, ci, ci, ci, cf, ci, vp, ci, vp, ctypes.c_int64, vp, vp, ci]
     f = lib.oracle_e4m3_decode
     f.restype = None
     f.argtypes = [vp, ctypes.c_int64, vp]
@@ -127,6 +130,29 @@ def attention_e4m3(q_codes, k_codes, v_codes, scale: float, descales=(1.0, 1.0, 
         out.ctypes.data, lse.ctypes.data, nthreads or default_threads())
     if rc != 0:
         raise ValueError("oracle_attn_rows_e4m3 rejected its arguments")
+    return out, lse
+
+
+def attention_masked(q_bits, k_bits, v_bits, scale: float, block_mask, causal: bool = True,
+                     rows=None, nthreads: int | None = None, lib: ctypes.CDLL | None = None):
+    """As ``attention`` plus a block mask: uint8 [Hm, nt, nt] with nt = ceil(S/128)
+    and Hm = 1 (shared by all heads) or Hq; entry 0 drops the 128 x 128 block of
+    (query tile, key tile).  Rows without any visible key: O = 0, LSE = -inf."""
+    lib = lib or load()
+    q, k, v = (_as_bits(x, n) for x, n in ((q_bits, "q"), (k_bits, "k"), (v_bits, "v")))
+    B, Hq, Hkv, S, D = _shapes(q, k, v)
+    nt = (S + 127) // 128
+    m = np.ascontiguousarray(block_mask, dtype=np.uint8)
+    if m.ndim != 3 or m.shape[1:] != (nt, nt) or m.shape[0] not in (1, Hq):
+        raise ValueError(f"block_mask must be [1 or Hq, {nt}, {nt}]")
+    rows_arr, nrows, out, lse = _outputs(B, Hq, S, D, rows)
+    rc = lib.oracle_attn_rows_masked(
+        q.ctypes.data, k.ctypes.data, v.ctypes.data, B, Hq, Hkv, S, D, ctypes.c_float(scale),
+        1 if causal else 0, m.ctypes.data, m.shape[0],
+        None if rows_arr is None else rows_arr.ctypes.data, nrows,
+        out.ctypes.data, lse.ctypes.data, nthreads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle_attn_rows_masked rejected its arguments")
     return out, lse
 
 

@@ -13,6 +13,11 @@
  *     3. scores[j > i] = -inf            (causal mask; the diagonal is kept)
  *     4. attn = softmax(scores) over keys
  *     5. out = attn . V
+ *   An optional block mask drops whole 128 x 128 (query tile, key tile) blocks
+ *   as well -- the block-sparse attention the ai-manual.ru article gives as a
+ *   reason for custom kernels (sections 4 and 7): key j is masked for query i
+ *   when block_mask[h][i / 128][j / 128] == 0, h = 0 for a mask shared by all
+ *   heads, else the query head.
  *   and the definition Attention(Q,K,V) = softmax(Q K^T / sqrt(d_k)) V from
  *   the ainews.cool article, section "technical deep dive".
  *   The fully-masked-row convention (output 0 instead of NaN) follows the
@@ -71,6 +76,8 @@ typedef struct {
     int B, Hq, Hkv, S, D;
     double scale;
     int causal;
+    const uint8_t *block_mask; /* NULL, or [mask_heads][nt][nt], nt = ceil(S / 128) */
+    int mask_heads;            /* 1 (shared by all heads) or Hq */
     const int64_t *rows; /* flat query-row ids, or NULL for all rows */
     int64_t nrows;
     double *out; /* [nrows, D] */
@@ -117,6 +124,13 @@ static void oracle_one_row(const oracle_job_t *J, int64_t r, double *s,
     /* Step 3: causal mask, keys after the query position get -inf. */
     if (J->causal)
         for (int64_t j = i + 1; j < S; ++j) s[j] = -INFINITY;
+    /* ... and keys in a dropped block of the block mask. */
+    if (J->block_mask) {
+        const int64_t nt = (S + 127) / 128;
+        const uint8_t *mrow = J->block_mask + ((J->mask_heads == 1 ? 0 : hq) * nt + i / 128) * nt;
+        for (int64_t j = 0; j < S; ++j)
+            if (mrow[j / 128] == 0) s[j] = -INFINITY;
+    }
     /* Step 4: softmax over keys, max-subtracted ("safe") form. */
     double m = -INFINITY;
     for (int64_t j = 0; j < S; ++j)
@@ -159,8 +173,10 @@ static void *oracle_worker(void *arg) {
 
 static int run_rows(const void *q, const void *k, const void *v, int format, const double descale[3],
                     int B, int Hq, int Hkv, int S, int D, float scale, int causal,
+                    const uint8_t *block_mask, int mask_heads,
                     const int64_t *rows, int64_t nrows, double *out, double *lse, int nthreads) {
     if (!q || !k || !v || !out || !lse) return 1;
+    if (block_mask && mask_heads != 1 && mask_heads != Hq) return 1;
     if (B < 1 || Hq < 1 || Hkv < 1 || S < 1 || D < 1 || Hq % Hkv != 0) return 1;
     const int64_t total = (int64_t)B * Hq * S;
     if (!rows && nrows != total) return 1;
@@ -187,6 +203,7 @@ static int run_rows(const void *q, const void *k, const void *v, int format, con
         J->B = B; J->Hq = Hq; J->Hkv = Hkv; J->S = S; J->D = D;
         J->scale = (double)scale;
         J->causal = causal ? 1 : 0;
+        J->block_mask = block_mask; J->mask_heads = mask_heads;
         J->rows = rows; J->nrows = nrows;
         J->out = out; J->lse = lse;
         J->begin = nrows * t / nthreads;
@@ -222,8 +239,23 @@ int oracle_attn_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v, in
                      int Hkv, int S, int D, float scale, int causal, const int64_t *rows,
                      int64_t nrows, double *out, double *lse, int nthreads) {
     const double one[3] = {1.0, 1.0, 1.0};
-    return run_rows(q, k, v, FMT_BF16, one, B, Hq, Hkv, S, D, scale, causal, rows, nrows, out, lse,
-                    nthreads);
+    return run_rows(q, k, v, FMT_BF16, one, B, Hq, Hkv, S, D, scale, causal, NULL, 1, rows, nrows,
+                    out, lse, nthreads);
+}
+
+/*
+ * oracle_attn_rows_masked -- oracle_attn_rows plus a block mask: uint8
+ * [mask_heads][nt][nt], nt = ceil(S / 128), mask_heads 1 or Hq; 0 drops the
+ * block.  Rows left without any key give O = 0 and LSE = -inf.
+ */
+int oracle_attn_rows_masked(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int Hq,
+                            int Hkv, int S, int D, float scale, int causal,
+                            const uint8_t *block_mask, int mask_heads, const int64_t *rows,
+                            int64_t nrows, double *out, double *lse, int nthreads) {
+    const double one[3] = {1.0, 1.0, 1.0};
+    if (!block_mask) return 1;
+    return run_rows(q, k, v, FMT_BF16, one, B, Hq, Hkv, S, D, scale, causal, block_mask,
+                    mask_heads, rows, nrows, out, lse, nthreads);
 }
 
 /*
@@ -235,8 +267,8 @@ int oracle_attn_rows_e4m3(const uint8_t *q, const uint8_t *k, const uint8_t *v, 
                           float scale, int causal, const int64_t *rows, int64_t nrows,
                           double *out, double *lse, int nthreads) {
     const double ds[3] = {(double)q_descale, (double)k_descale, (double)v_descale};
-    return run_rows(q, k, v, FMT_E4M3, ds, B, Hq, Hkv, S, D, scale, causal, rows, nrows, out, lse,
-                    nthreads);
+    return run_rows(q, k, v, FMT_E4M3, ds, B, Hq, Hkv, S, D, scale, causal, NULL, 1, rows, nrows,
+                    out, lse, nthreads);
 }
 
 /* Decodes n E4M3 codes to doubles (exposed so the decoding can be pinned). */

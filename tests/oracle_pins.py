@@ -333,3 +333,56 @@ def pin_e4m3_matches_bf16_path(attn8, attn):
 
 
 E4M3_PINS = [pin_e4m3_decode, pin_e4m3_sdpa_library, pin_e4m3_matches_bf16_path]
+
+
+# ---------------------------------------------------------------------------
+# Block masks (the oracle's masked entry).  attnm(q, k, v, scale, mask, causal).
+def _expand_block_mask(mask, Hq, S, causal):
+    """Element mask [Hq, S, S] (True = visible) from a [Hm, nt, nt] block mask."""
+    m = torch.from_numpy(np.ascontiguousarray(mask)).bool()
+    m = m.repeat_interleave(128, dim=1).repeat_interleave(128, dim=2)[:, :S, :S]
+    m = m.expand(Hq, S, S)
+    if causal:
+        m = m & torch.ones(S, S, dtype=torch.bool).tril()
+    return m
+
+
+def pin_block_mask_library(attnm):
+    """Random block masks (shared and per head, causal and not, GQA) against torch's
+    float64 SDPA with the expanded boolean mask; rows that see no key are 0 there
+    (its safe softmax) and must have LSE = -inf; other LSEs against logsumexp."""
+    rng = np.random.default_rng(131)
+    B, Hq, Hkv, S, D = 2, 4, 2, 300, 8
+    nt = 3
+    q, k, v = (_rand((B, H, S, D), 131, t) for t, H in ((0, Hq), (1, Hkv), (2, Hkv)))
+    scale = 0.35
+    for hm, causal in ((1, True), (Hq, False), (Hq, True)):
+        mask = (rng.random((hm, nt, nt)) < 0.6).astype(np.uint8)
+        mask[0, 2, :] = 0  # query tile 2 of head 0 sees nothing
+        O, L = attnm(q, k, v, scale, mask, causal)
+        em = _expand_block_mask(mask, Hq, S, causal)
+        qf = torch.from_numpy(f64(q))
+        kf = torch.from_numpy(f64(k)).repeat_interleave(Hq // Hkv, dim=1)
+        vf = torch.from_numpy(f64(v)).repeat_interleave(Hq // Hkv, dim=1)
+        sc32 = float(np.float32(scale))
+        ref = F.scaled_dot_product_attention(qf, kf, vf, attn_mask=em, scale=sc32).numpy()
+        np.testing.assert_allclose(O, ref, rtol=0, atol=1e-12)
+        sc = torch.einsum("bhid,bhjd->bhij", qf, kf) * sc32
+        lse_ref = torch.logsumexp(sc.masked_fill(~em, float("-inf")), dim=-1).numpy()
+        none = ~em.any(dim=-1).numpy()  # [Hq, S]
+        assert none.any()
+        assert np.all(np.isneginf(L[:, none])) and np.all(O[:, none] == 0.0)
+        np.testing.assert_allclose(L[:, ~none], lse_ref[:, ~none], rtol=0, atol=1e-12)
+
+
+def pin_block_mask_all_ones(attnm, attn):
+    """An all-ones block mask changes nothing."""
+    B, H, S, D = 1, 2, 200, 8
+    q, k, v = (_rand((B, H, S, D), 141, t) for t in range(3))
+    for causal in (True, False):
+        Om, Lm = attnm(q, k, v, 0.3, np.ones((1, 2, 2), np.uint8), causal)
+        O, L = attn(q, k, v, 0.3, causal)
+        assert np.array_equal(Om, O) and np.array_equal(Lm, L)
+
+
+MASK_PINS = [pin_block_mask_library, pin_block_mask_all_ones]

@@ -34,6 +34,10 @@ MUTANTS = {
     "e4m3_descale_ignored": ("e4m3_bits_to_double(((const uint8_t *)J->t[which])[idx]) * J->descale[which]",
                              "e4m3_bits_to_double(((const uint8_t *)J->t[which])[idx])"),
     "e4m3_descale_swapped": ("J->descale[which]", "J->descale[2 - which]"),
+    "block_mask_transposed": ("if (mrow[j / 128] == 0) s[j] = -INFINITY;",
+                              "if (J->block_mask[(j / 128) * ((S + 127) / 128) + i / 128] == 0) s[j] = -INFINITY;"),
+    "block_mask_heads_ignored": ("(J->mask_heads == 1 ? 0 : hq)", "(0)"),
+    "block_mask_ignored": ("if (J->block_mask) {", "if (0) {"),
 }
 
 
@@ -53,11 +57,16 @@ def test_some_pin_catches_mutant(name, tmp_path):
     def attn8(q, k, v, scale, ds, causal, rows=None):
         return oracle.attention_e4m3(q, k, v, scale, ds, causal, rows=rows, lib=lib)
 
+    def attnm(q, k, v, scale, mask, causal, rows=None):
+        return oracle.attention_masked(q, k, v, scale, mask, causal, rows=rows, lib=lib)
+
     checks = [(p.__name__, lambda p=p: p(attn)) for p in oracle_pins.ALL_PINS] + [
         ("pin_e4m3_decode", lambda: oracle_pins.pin_e4m3_decode(
             lambda c: oracle.e4m3_decode(c, lib=lib))),
         ("pin_e4m3_sdpa_library", lambda: oracle_pins.pin_e4m3_sdpa_library(attn8)),
         ("pin_e4m3_matches_bf16_path", lambda: oracle_pins.pin_e4m3_matches_bf16_path(attn8, attn)),
+        ("pin_block_mask_library", lambda: oracle_pins.pin_block_mask_library(attnm)),
+        ("pin_block_mask_all_ones", lambda: oracle_pins.pin_block_mask_all_ones(attnm, attn)),
     ]
     caught = []
     for pin_name, run in checks:

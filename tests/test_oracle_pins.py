@@ -23,6 +23,13 @@ def test_oracle_e4m3_pins():
     oracle_pins.pin_e4m3_matches_bf16_path(attn8, _attn)
 
 
+def test_oracle_block_mask_pins():
+    def attnm(q, k, v, scale, mask, causal, rows=None):
+        return oracle.attention_masked(q, k, v, scale, mask, causal, rows=rows)
+    oracle_pins.pin_block_mask_library(attnm)
+    oracle_pins.pin_block_mask_all_ones(attnm, _attn)
+
+
 def test_rows_subset_matches_full():
     """The row-selection entry computes exactly the rows of the full call."""
     from causal_scaled_dot_gb300.inputs import qkv_bf16
