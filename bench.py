@@ -6,7 +6,10 @@ CPU oracle timed on the host as a reported baseline.
     python bench.py --impl reference ...     # the oracle alone, on host cores
 
 A step is one attn_fwd call over the whole workload (all query rows of every
-batch and head).  FLOPs per step = 4*B*Hq*S^2*D / 2 (causal).  Between timed
+batch and head).  FLOPs per step = 4*B*Hq*S^2*D / 2 (causal).  With
+--mask-density P the step is attn_fwd_block_masked with a seeded per-head
+block mask keeping each 128 x 128 block with probability P, and the FLOPs are
+4*D per visible (query, key) pair, counted exactly.  Between timed
 steps a 256 MiB buffer is written to flush L2; each step is timed with CUDA
 events on the launching stream.  Under torchrun every rank runs the same
 workload on its own GPU (independent problems, no collective on the data
@@ -46,13 +49,16 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+# The sources that make the timed forward kernel and its launch.
+FWD_SOURCES = ("attn_api.cu", "common.cuh", "kernel_ws.cuh", "ptx.cuh")
+
+
 def kernel_source_hash() -> str:
     csrc = os.path.join(ROOT, "causal_scaled_dot_gb300", "csrc")
     h = hashlib.sha256()
-    for fn in sorted(os.listdir(csrc)):
-        if fn.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, fn), "rb") as f:
-                h.update(fn.encode() + b"\0" + f.read())
+    for fn in FWD_SOURCES:
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(fn.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
@@ -147,6 +153,22 @@ def barrier(world: int):
 
 
 # --------------------------------------------------------------------- oracle
+def workload_mask(w, density: float):
+    """The seeded per-head block mask of --mask-density: uint8 [Hq, nt, nt]."""
+    from causal_scaled_dot_gb300.inputs import random_block_mask
+    return random_block_mask(w.Hq, w.S, density, seed=w.seed)
+
+
+def visible_keys(mask, S: int, causal: bool) -> np.ndarray:
+    """Keys each query row sees under the block mask (and causality): [Hm, S]."""
+    nt = mask.shape[1]
+    i = np.arange(S)[:, None]
+    start = (np.arange(nt) * 128)[None, :]
+    end = np.minimum(i + 1, S) if causal else np.full_like(i, S)
+    per_tile = np.clip(end - start, 0, 128)                     # [S, nt]
+    return np.einsum("hsk,sk->hs", mask[:, i[:, 0] // 128, :].astype(np.int64), per_tile)
+
+
 class OracleTimer:
     """The fp64 oracle as it stands, on all host cores, over bounded random
     samples of a workload's query rows.
@@ -156,7 +178,7 @@ class OracleTimer:
     rows * 2*S*D and its TFLOP/s is comparable with the GPU's.
     """
 
-    def __init__(self, w, fp8: bool = False):
+    def __init__(self, w, fp8: bool = False, mask=None):
         import oracle
         from causal_scaled_dot_gb300.inputs import qkv_bf16, qkv_e4m3
         self.oracle = oracle
@@ -167,6 +189,10 @@ class OracleTimer:
         self.threads = oracle.default_threads()
         self.total = w.B * w.Hq * w.S
         self.row_flops = (2.0 if w.causal else 4.0) * w.S * w.D
+        self.mask = mask
+        if mask is not None:
+            self.keys = visible_keys(mask, w.S, w.causal)  # [mask heads, S]
+            self.row_flops = 4.0 * w.D * float(self.keys.mean())
         n = max(self.threads, 32)
         self.run(n, seed=12345)  # warm the library and the page cache
         t0 = time.perf_counter()
@@ -175,12 +201,23 @@ class OracleTimer:
 
     def run(self, n, seed):
         rows = np.random.default_rng(seed).integers(0, self.total, n)
-        if self.fp8:
+        if self.mask is not None:
+            self.oracle.attention_masked(self.q, self.k, self.v, self.w.scale, self.mask,
+                                         self.w.causal, rows=rows, nthreads=self.threads)
+        elif self.fp8:
             self.oracle.attention_e4m3(self.q, self.k, self.v, self.w.scale, (1.0, 1.0, 1.0),
                                        self.w.causal, rows=rows, nthreads=self.threads)
         else:
             self.oracle.attention(self.q, self.k, self.v, self.w.scale, self.w.causal, rows=rows,
                                   nthreads=self.threads)
+        return rows
+
+    def flops_of(self, rows) -> float:
+        if self.mask is None:
+            return rows.size * self.row_flops
+        S, Hq = self.w.S, self.w.Hq
+        h = (rows // S) % Hq if self.keys.shape[0] > 1 else np.zeros_like(rows)
+        return 4.0 * self.w.D * float(self.keys[h, rows % S].sum())
 
     def rows_for(self, seconds):
         return int(min(self.total, max(self.threads, seconds / max(self.sec_per_row, 1e-9))))
@@ -189,23 +226,30 @@ class OracleTimer:
         """Times one sample of about `seconds`; returns (TFLOP/s, rows, wall seconds)."""
         n = self.rows_for(seconds)
         t0 = time.perf_counter()
-        self.run(n, seed)
+        rows = self.run(n, seed)
         dt = time.perf_counter() - t0
-        return n * self.row_flops / dt / 1e12, n, dt
+        return self.flops_of(rows) / dt / 1e12, n, dt
+
+
+def mask_config(mask, density):
+    if mask is None:
+        return {}
+    return {"block_mask": {"density": density, "heads": int(mask.shape[0]),
+                           "kept_block_frac": float(mask.mean())}}
 
 
 def run_reference(args, w, rank, world):
     if rank != 0:
         return 0
-    timer = OracleTimer(w, fp8=args.dtype == "fp8")
+    mask = workload_mask(w, args.mask_density) if args.mask_density is not None else None
+    timer = OracleTimer(w, fp8=args.dtype == "fp8", mask=mask)
     # The whole run (warm-up and timed steps) stays within a few minutes.
     step_s = min(args.ref_step_seconds, args.ref_total_seconds / max(1, args.steps + args.warmup))
     for i in range(args.warmup):
         timer.sample(step_s, seed=1000 + i)
     samples = [timer.sample(step_s, seed=s + 1) for s in range(args.steps)]
-    flops = sum(n * timer.row_flops for _, n, _ in samples)
     secs = sum(dt for _, _, dt in samples)
-    value = flops / secs / 1e12
+    value = sum(tf * dt for tf, _, dt in samples) / secs
     rows_per_step = int(np.mean([n for _, n, _ in samples]))
     sample = (f"{rows_per_step} random query rows of {w.name} per step "
               f"(of {timer.total}); fp64 C oracle, {timer.threads} threads")
@@ -216,7 +260,8 @@ def run_reference(args, w, rank, world):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": f"synthetic (seeded N(0,1) {'e4m3' if args.dtype == 'fp8' else 'bf16'})",
         "config": {"workload": w.name, **w.shape_dict, "causal": w.causal,
-                   "inputs": "e4m3" if args.dtype == "fp8" else "bf16"},
+                   "inputs": "e4m3" if args.dtype == "fp8" else "bf16",
+                   **mask_config(mask, args.mask_density)},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": timer.threads,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -244,6 +289,11 @@ def run_ours(args, w, rank, world, local):
         qh, kh, vh = (torch.from_numpy(b.view(np.int16).copy()).view(torch.bfloat16).pin_memory()
                       for b in bits)
     q, k, v = qh.to(dev), kh.to(dev), vh.to(dev)
+    mask = workload_mask(w, args.mask_density) if args.mask_density is not None else None
+    flops = w.flops
+    if mask is not None:
+        flops = 4.0 * w.D * w.B * float(visible_keys(mask, w.S, w.causal).sum())
+        mask_d = torch.from_numpy(mask).to(dev)
     out = torch.empty((w.B, w.Hq, w.S, w.D), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((w.B, w.Hq, w.S), dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -253,6 +303,9 @@ def run_ours(args, w, rank, world, local):
         if fp8:
             native.attn_fwd_fp8(q, k, v, 1.0, 1.0, 1.0, out, lse, w.B, w.Hq, w.Hkv, w.S, w.D,
                                 w.scale, w.causal, stream)
+        elif mask is not None:
+            native.attn_fwd_block_masked(q, k, v, out, lse, w.B, w.Hq, w.Hkv, w.S, w.D, w.scale,
+                                         w.causal, mask_d, mask.shape[0], stream)
         else:
             native.attn_fwd(q, k, v, out, lse, w.B, w.Hq, w.Hkv, w.S, w.D, w.scale, w.causal,
                             stream)
@@ -283,7 +336,7 @@ def run_ours(args, w, rank, world, local):
     per_step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms_local = float(np.mean(per_step_ms))
     ms = reduce_max(ms_local, world)
-    value = world * w.flops / (ms * 1e-3) / 1e12
+    value = world * flops / (ms * 1e-3) / 1e12
 
     # End to end: pinned host buffers -> device, attn_fwd, O and LSE back to host.
     out_h = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
@@ -320,13 +373,13 @@ def run_ours(args, w, rank, world, local):
     if fp8:  # no measured fp8 peak: the bf16 one times the nominal fp8/bf16 ratio (4.5 / 2.25)
         peak *= 2.0
         peak_what = f"{peak_src} bf16 dense (burst) x 2, the nominal fp8/bf16 ratio"
-    achieved = w.flops / (ms_local * 1e-3) / 1e12
-    traffic = None if fp8 else recorded_traffic(w.name)
+    achieved = flops / (ms_local * 1e-3) / 1e12
+    traffic = None if (fp8 or mask is not None) else recorded_traffic(w.name)
     # algorithmic bytes: inputs read once (1 byte per element for E4M3), O and LSE written once
     io_bytes = w.io_bytes - (w.B * (w.Hq + 2 * w.Hkv) * w.S * w.D if fp8 else 0)
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        timer = OracleTimer(w, fp8=fp8)
+        timer = OracleTimer(w, fp8=fp8, mask=mask)
         tf, n, dt = timer.sample(args.cpu_seconds, seed=7)
         cpu = {"value": tf, "unit": "TFLOP/s", "cores": timer.threads, "kind": "oracle",
                "sample": f"{n} random query rows of {w.name} (of {timer.total}), "
@@ -338,7 +391,7 @@ def run_ours(args, w, rank, world, local):
         "dtype": "fp8 (e4m3 inputs, bf16 output)" if fp8 else "bf16",
         "data": f"synthetic (seeded N(0,1) {'e4m3' if fp8 else 'bf16'}, no weights)",
         "config": {"workload": w.name, **w.shape_dict, "causal": w.causal,
-                   "inputs": "e4m3" if fp8 else "bf16",
+                   "inputs": "e4m3" if fp8 else "bf16", **mask_config(mask, args.mask_density),
                    "l2": "flushed between timed steps (256 MiB write)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "pct_of_peak": 100.0 * achieved / peak,
@@ -347,7 +400,7 @@ def run_ours(args, w, rank, world, local):
                      "peak_source": peak_what,
                      "hbm_gbs": io_bytes / (ms_local * 1e-3) / 1e9},
         "cpu_baseline": cpu,
-        "e2e": {"value": world * w.flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": launches,
         "clocks": clk.summary(),
@@ -367,6 +420,9 @@ def main():
     ap.add_argument("--workload", default=HEADLINE.name, choices=sorted(BY_NAME))
     ap.add_argument("--dtype", default="bf16", choices=["bf16", "fp8"],
                     help="input format: bf16 (attn_fwd) or E4M3 (attn_fwd_fp8, D = 128 only)")
+    ap.add_argument("--mask-density", type=float, default=None,
+                    help="bf16 only: run attn_fwd_block_masked with a seeded per-head block mask "
+                         "keeping each 128x128 block with this probability")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="budget of the oracle CPU-baseline sample")
     ap.add_argument("--ref-step-seconds", type=float, default=8.0,
@@ -377,6 +433,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.mask_density is not None and (args.dtype != "bf16" or not 0.0 <= args.mask_density <= 1.0):
+        ap.error("--mask-density takes a probability in [0, 1] and bf16 inputs")
     w = BY_NAME[args.workload]
     rank, world, local = dist_init(args)
     if world != args.gpus and rank == 0:

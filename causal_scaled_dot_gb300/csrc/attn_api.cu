@@ -62,9 +62,11 @@ int setup_device_locked(int dev) {
     if (cudaGetSymbolAddress(&word, g_attn_status) != cudaSuccess ||
         allow_smem(attn_fwd_simple_kernel<64>, SimpleLayout<64>::kDynamicSmem) != cudaSuccess ||
         allow_smem(attn_fwd_simple_kernel<128>, SimpleLayout<128>::kDynamicSmem) != cudaSuccess ||
-        allow_smem(attn_fwd_ws_kernel<64, false>, WsLayout<64, false>::kDynamicSmem) != cudaSuccess ||
-        allow_smem(attn_fwd_ws_kernel<128, false>, WsLayout<128, false>::kDynamicSmem) != cudaSuccess ||
-        allow_smem(attn_fwd_ws_kernel<128, true>, WsLayout<128, true>::kDynamicSmem) != cudaSuccess) {
+        allow_smem(attn_fwd_ws_kernel<64, false, false>, WsLayout<64, false>::kDynamicSmem) != cudaSuccess ||
+        allow_smem(attn_fwd_ws_kernel<128, false, false>, WsLayout<128, false>::kDynamicSmem) != cudaSuccess ||
+        allow_smem(attn_fwd_ws_kernel<128, true, false>, WsLayout<128, true>::kDynamicSmem) != cudaSuccess ||
+        allow_smem(attn_fwd_ws_kernel<64, false, true>, WsLayout<64, false>::kDynamicSmem) != cudaSuccess ||
+        allow_smem(attn_fwd_ws_kernel<128, false, true>, WsLayout<128, false>::kDynamicSmem) != cudaSuccess) {
         st.status = ATTN_ERR_DEVICE;
         return st.status;
     }
@@ -155,7 +157,7 @@ int launch_simple(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMa
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
-template <int D, bool F>
+template <int D, bool F, bool M>
 int launch_ws(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, FwdParams p,
               int sm_count, cudaStream_t stream) {
     const long long npairs = (p.num_q_tiles + 1) / 2;
@@ -163,7 +165,7 @@ int launch_ws(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& t
     if (units > (1ll << 31) - 1) return ATTN_ERR_UNSUPPORTED;
     p.num_units = (int)units;
     const int grid = (int)(units < sm_count ? units : sm_count);
-    attn_fwd_ws_kernel<D, F><<<grid, WsLayout<D, F>::kThreads, WsLayout<D, F>::kDynamicSmem, stream>>>(
+    attn_fwd_ws_kernel<D, F, M><<<grid, WsLayout<D, F>::kThreads, WsLayout<D, F>::kDynamicSmem, stream>>>(
         tq, tk, tv, p);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
@@ -196,8 +198,33 @@ __global__ void selftest_wait_kernel(unsigned long long limit_ns, unsigned int* 
 
 using namespace attn;
 
+namespace attn {
+namespace {
+int fwd_bf16(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
+             int Hkv, int S, int D, float scale, int causal, const uint8_t* block_mask,
+             int mask_heads, void* stream);
+}  // namespace
+}  // namespace attn
+
 extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B,
                         int Hq, int Hkv, int S, int D, float scale, int causal, void* stream) {
+    return attn::fwd_bf16(q, k, v, out, lse, B, Hq, Hkv, S, D, scale, causal, nullptr, 1, stream);
+}
+
+extern "C" int attn_fwd_block_masked(const void* q, const void* k, const void* v, void* out,
+                                     float* lse, int B, int Hq, int Hkv, int S, int D, float scale,
+                                     int causal, const unsigned char* block_mask, int mask_heads,
+                                     void* stream) {
+    if (block_mask == nullptr || (mask_heads != 1 && mask_heads != Hq)) return ATTN_ERR_INVALID_ARG;
+    return attn::fwd_bf16(q, k, v, out, lse, B, Hq, Hkv, S, D, scale, causal, block_mask,
+                          mask_heads, stream);
+}
+
+namespace attn {
+namespace {
+int fwd_bf16(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
+             int Hkv, int S, int D, float scale, int causal, const uint8_t* block_mask,
+             int mask_heads, void* stream) {
     int rc = check_args(q, k, v, out, lse, B, Hq, Hkv, S, D, scale);
     if (rc != ATTN_OK) return rc;
     DeviceState* dev = nullptr;
@@ -210,7 +237,7 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* out, 
         encode_bf16_3d(&tv, v, D, S, (long long)B * Hkv, kTile) != ATTN_OK)
         return ATTN_ERR_INVALID_ARG;
 
-    FwdParams p;
+    FwdParams p{};
     std::memset(&p, 0, sizeof p);
     p.B = B;
     p.Hq = Hq;
@@ -225,12 +252,20 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* out, 
     p.status = dev->status_word;
     p.wait_limit_ns = kWaitLimitNs;
     p.o_scale = 1.f;
+    p.block_mask = block_mask;
+    p.mask_heads = mask_heads;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (use_simple_kernel())
+    // Block masks are handled by the persistent kernel only.
+    if (block_mask == nullptr && use_simple_kernel())
         return D == 64 ? launch_simple<64>(tq, tk, tv, p, st) : launch_simple<128>(tq, tk, tv, p, st);
-    return D == 64 ? launch_ws<64, false>(tq, tk, tv, p, dev->sm_count, st)
-                   : launch_ws<128, false>(tq, tk, tv, p, dev->sm_count, st);
+    if (block_mask != nullptr)
+        return D == 64 ? launch_ws<64, false, true>(tq, tk, tv, p, dev->sm_count, st)
+                       : launch_ws<128, false, true>(tq, tk, tv, p, dev->sm_count, st);
+    return D == 64 ? launch_ws<64, false, false>(tq, tk, tv, p, dev->sm_count, st)
+                   : launch_ws<128, false, false>(tq, tk, tv, p, dev->sm_count, st);
 }
+}  // namespace
+}  // namespace attn
 
 extern "C" int attn_fwd_fp8(const void* q, const void* k, const void* v, float q_descale,
                             float k_descale, float v_descale, void* out, float* lse, int B, int Hq,
@@ -250,7 +285,7 @@ extern "C" int attn_fwd_fp8(const void* q, const void* k, const void* v, float q
         encode_3d(&tv, v, 1, D, S, (long long)B * Hkv, kTile) != ATTN_OK)
         return ATTN_ERR_INVALID_ARG;
 
-    FwdParams p;
+    FwdParams p{};
     std::memset(&p, 0, sizeof p);
     p.B = B;
     p.Hq = Hq;
@@ -267,7 +302,7 @@ extern "C" int attn_fwd_fp8(const void* q, const void* k, const void* v, float q
     p.lse = lse;
     p.status = dev->status_word;
     p.wait_limit_ns = kWaitLimitNs;
-    return launch_ws<128, true>(tq, tk, tv, p, dev->sm_count, static_cast<cudaStream_t>(stream));
+    return launch_ws<128, true, false>(tq, tk, tv, p, dev->sm_count, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int attn_sync_status(void* stream) {

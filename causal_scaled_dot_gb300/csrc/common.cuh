@@ -24,6 +24,8 @@ struct FwdParams {
     unsigned long long wait_limit_ns;  // bound on every mbarrier wait
     int num_units;                  // persistent kernels: total work units
     float o_scale;                  // multiplies O at the end (FP8: the V descale; else 1)
+    const uint8_t* block_mask;      // null, or [mask_heads][nt][nt], nt = num_q_tiles
+    int mask_heads;                 // 1 (one mask for all heads) or Hq
 };
 
 }  // namespace attn

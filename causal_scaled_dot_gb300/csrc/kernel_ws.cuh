@@ -86,9 +86,11 @@ struct WsLayout {
 };
 
 // Unit u -> (bh, pair m).  Causal: heaviest pairs first.  Within a pair index
-// consecutive u walk bh = b*Hq + hq, so GQA siblings are adjacent.
+// consecutive u walk bh = b*Hq + hq, so GQA siblings are adjacent.  n0 / n1
+// bound the key tiles of query tile 2m / 2m+1 (causality, sequence end); with
+// a block mask some tiles below the bound are dropped too (tile_active).
 struct Unit {
-    int bh, m, kv_bh, n0, n1, n;
+    int bh, hq, m, kv_bh, n0, n1, n;
 };
 __device__ __forceinline__ Unit decode_unit(int u, const FwdParams& p) {
     const int BH = p.B * p.Hq;
@@ -98,6 +100,7 @@ __device__ __forceinline__ Unit decode_unit(int u, const FwdParams& p) {
     w.bh = u - (u / BH) * BH;
     const int b = w.bh / p.Hq;
     const int hq = w.bh - b * p.Hq;
+    w.hq = hq;
     w.kv_bh = b * p.Hkv + hq / p.group;
     const int qt0 = 2 * w.m, qt1 = 2 * w.m + 1;
     if (p.causal) {
@@ -108,6 +111,47 @@ __device__ __forceinline__ Unit decode_unit(int u, const FwdParams& p) {
     }
     w.n = max(w.n0, w.n1);
     return w;
+}
+
+// Does query tile 2m + i of unit w use key tile j?  M (block mask present) is
+// a template flag so that the unmasked kernel keeps its plain counting loops:
+// without a mask, tile i uses key tiles [0, n_i) (the odd last query tile of a
+// pair, past the sequence end, runs too and writes nothing).  With a mask, a
+// tile below n_i is used when the mask keeps it, and a query tile past the
+// sequence end uses none.
+template <bool M>
+__device__ __forceinline__ bool tile_active(const FwdParams& p, const Unit& w, int i, int j) {
+    if (j >= (i == 0 ? w.n0 : w.n1)) return false;
+    if constexpr (!M) {
+        return true;
+    } else {
+        const int qt = 2 * w.m + i;
+        if (qt >= p.num_q_tiles) return false;
+        const int nt = p.num_q_tiles;
+        return __ldg(p.block_mask + ((size_t)(p.mask_heads == 1 ? 0 : w.hq) * nt + qt) * nt + j) != 0;
+    }
+}
+// First key tile after j that either query tile uses (w.n if none).
+template <bool M>
+__device__ __forceinline__ int next_union(const FwdParams& p, const Unit& w, int j) {
+    if constexpr (!M) {
+        return j + 1;  // every j < n = max(n0, n1) is used by one of the two
+    } else {
+        for (++j; j < w.n; ++j)
+            if (tile_active<M>(p, w, 0, j) || tile_active<M>(p, w, 1, j)) return j;
+        return w.n;
+    }
+}
+// Last key tile query tile i uses (-1 if none).
+template <bool M>
+__device__ __forceinline__ int last_active(const FwdParams& p, const Unit& w, int i) {
+    if constexpr (!M) {
+        return (i == 0 ? w.n0 : w.n1) - 1;
+    } else {
+        for (int j = (i == 0 ? w.n0 : w.n1) - 1; j >= 0; --j)
+            if (tile_active<M>(p, w, i, j)) return j;
+        return -1;
+    }
 }
 
 // The unit this CTA runs in round r (>= num_units: no more work).
@@ -122,7 +166,7 @@ __device__ __forceinline__ uint32_t ws_bar(uint32_t base, int i) {
 }
 
 // ---------------------------------------------------------------- producer
-template <int D, bool F>
+template <int D, bool F, bool M>
 __device__ void ws_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                              const CUtensorMap* tm_v, const FwdParams& p, uint32_t base,
                              volatile int* abort_flag) {
@@ -150,7 +194,7 @@ __device__ void ws_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
             pend_q |= 1u << i;
             pend_q_par = (pend_q_par & ~(1u << i)) | (((qe_phase[i] ^ 1u) & 1u) << i);
         }
-        for (int j = 0; j < w.n; ++j) {
+        for (int j = next_union<M>(p, w, -1); j < w.n; j = next_union<M>(p, w, j)) {
 #pragma unroll
             for (int t = 0; t < 2; ++t) {  // t = 0: K_j, t = 1: V_j
                 if (!ptx::mbar_wait(ws_bar<D, F>(base, L::kKVEmpty + slot), ring_phase ^ 1u, abort_flag,
@@ -184,7 +228,7 @@ drain:
 }
 
 // ---------------------------------------------------------------- MMA issuer
-template <int D, bool F>
+template <int D, bool F, bool M>
 __device__ void ws_mma_role(const FwdParams& p, uint32_t base, uint32_t tmem,
                             volatile int* abort_flag) {
     using L = WsLayout<D, F>;
@@ -250,44 +294,63 @@ __device__ void ws_mma_role(const FwdParams& p, uint32_t base, uint32_t tmem,
             !ptx::mbar_wait(ws_bar<D, F>(base, L::kQFull + 1), qf_phase, abort_flag, p.status, lim))
             break;
         qf_phase ^= 1u;
+        // Key tiles run over the union of both query tiles' active tiles; each
+        // product is issued only for a query tile that uses the key tile.
+        const int last0 = last_active<M>(p, w, 0), last1 = last_active<M>(p, w, 1);
+        if (last0 < 0) ptx::mma_commit(ws_bar<D, F>(base, L::kQEmpty + 0));
+        if (last1 < 0) ptx::mma_commit(ws_bar<D, F>(base, L::kQEmpty + 1));
+        bool first0 = true, first1 = true, ok = true;
+        int j = next_union<M>(p, w, -1);
         int kslot, vslot;
-        if (!wait_ring(kslot)) break;
-        issue_s(0, kslot);
-        if (w.n0 == 1) ptx::mma_commit(ws_bar<D, F>(base, L::kQEmpty + 0));
-        issue_s(1, kslot);
-        if (w.n1 == 1) ptx::mma_commit(ws_bar<D, F>(base, L::kQEmpty + 1));
-        ptx::mma_commit(ws_bar<D, F>(base, L::kKVEmpty + kslot));
-        bool ok = true;
-        for (int j = 0; j < w.n && ok; ++j) {
-            if (!(ok = wait_ring(vslot))) break;
-            if (j < w.n0) {
-                if (!(ok = wait_p(0))) break;
-                issue_pv(0, vslot, j > 0);
-                if (j == w.n0 - 1) ptx::mma_commit(ws_bar<D, F>(base, L::kOFull + 0));
+        if (j < w.n) {
+            if (!wait_ring(kslot)) break;
+            if (tile_active<M>(p, w, 0, j)) {
+                issue_s(0, kslot);
+                if (j == last0) ptx::mma_commit(ws_bar<D, F>(base, L::kQEmpty + 0));
             }
-            const bool more = j + 1 < w.n;
+            if (tile_active<M>(p, w, 1, j)) {
+                issue_s(1, kslot);
+                if (j == last1) ptx::mma_commit(ws_bar<D, F>(base, L::kQEmpty + 1));
+            }
+            ptx::mma_commit(ws_bar<D, F>(base, L::kKVEmpty + kslot));
+        }
+        while (j < w.n) {
+            const int jn = next_union<M>(p, w, j);
+            if (!(ok = wait_ring(vslot))) break;
+            if (tile_active<M>(p, w, 0, j)) {
+                if (!(ok = wait_p(0))) break;
+                issue_pv(0, vslot, !first0);
+                first0 = false;
+                if (j == last0) ptx::mma_commit(ws_bar<D, F>(base, L::kOFull + 0));
+            }
+            const bool more = jn < w.n;
             if (more) {
                 if (!(ok = wait_ring(kslot))) break;
-                if (j + 1 < w.n0) {
+                if (tile_active<M>(p, w, 0, jn)) {
                     issue_s(0, kslot);
-                    if (j + 1 == w.n0 - 1) ptx::mma_commit(ws_bar<D, F>(base, L::kQEmpty + 0));
+                    if (jn == last0) ptx::mma_commit(ws_bar<D, F>(base, L::kQEmpty + 0));
                 }
             }
-            if (j < w.n1) {
+            if (tile_active<M>(p, w, 1, j)) {
                 if (!(ok = wait_p(1))) break;
-                issue_pv(1, vslot, j > 0);
-                if (j == w.n1 - 1) ptx::mma_commit(ws_bar<D, F>(base, L::kOFull + 1));
+                issue_pv(1, vslot, !first1);
+                first1 = false;
+                if (j == last1) ptx::mma_commit(ws_bar<D, F>(base, L::kOFull + 1));
             }
             ptx::mma_commit(ws_bar<D, F>(base, L::kKVEmpty + vslot));
             if (more) {
-                if (j + 1 < w.n1) {
+                if (tile_active<M>(p, w, 1, jn)) {
                     issue_s(1, kslot);
-                    if (j + 1 == w.n1 - 1) ptx::mma_commit(ws_bar<D, F>(base, L::kQEmpty + 1));
+                    if (jn == last1) ptx::mma_commit(ws_bar<D, F>(base, L::kQEmpty + 1));
                 }
                 ptx::mma_commit(ws_bar<D, F>(base, L::kKVEmpty + kslot));
             }
+            j = jn;
         }
         if (!ok) break;
+        // A query tile with no key tile still completes its O phase.
+        if (last0 < 0) ptx::mma_commit(ws_bar<D, F>(base, L::kOFull + 0));
+        if (last1 < 0) ptx::mma_commit(ws_bar<D, F>(base, L::kOFull + 1));
     }
     // Every MMA issued above completes before TMEM can be released.
     ptx::mma_commit(ws_bar<D, F>(base, L::kDrain));
@@ -295,7 +358,7 @@ __device__ void ws_mma_role(const FwdParams& p, uint32_t base, uint32_t tmem,
 }
 
 // ---------------------------------------------------------------- softmax
-template <int D, bool F>
+template <int D, bool F, bool M>
 __device__ void ws_softmax_role(const FwdParams& p, uint32_t base, uint32_t tmem, int wg,
                                 volatile int* abort_flag) {
     using L = WsLayout<D, F>;
@@ -318,7 +381,9 @@ __device__ void ws_softmax_role(const FwdParams& p, uint32_t base, uint32_t tmem
         const int n_i = wg == 0 ? w.n0 : w.n1;
         float m_run = 0.f;  // reference maximum (log2 units), set by the first tile
         float l_run = 0.f;
+        bool first = true;
         for (int j = 0; j < n_i; ++j) {
+            if (!tile_active<M>(p, w, wg, j)) continue;
             bool ok = ptx::mbar_wait(bar_s, s_phase, abort_flag, p.status, lim);
             if (!__all_sync(0xffffffffu, ok)) return;
             s_phase ^= 1u;
@@ -355,11 +420,13 @@ __device__ void ws_softmax_role(const FwdParams& p, uint32_t base, uint32_t tmem
             }
             const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
             // Every row has at least one unmasked key in every tile it visits
-            // (key 0 of tile 0; the diagonal key of a diagonal tile), so mt is finite.
+            // (all keys of an off-diagonal tile; the first key of a diagonal
+            // tile; key kv0 < S of the last tile), so mt is finite.
             float alpha = 1.f;
             bool rescale = false;
-            if (j == 0) {
+            if (first) {
                 m_run = mt;
+                first = false;
             } else if (mt > m_run + kRescaleSlack) {
                 alpha = ptx::ex2(m_run - mt);
                 m_run = mt;
@@ -441,8 +508,19 @@ __device__ void ws_softmax_role(const FwdParams& p, uint32_t base, uint32_t tmem
         ptx::tc_fence_after();
         const int row = qt * kTile + r;
         const bool valid = row < p.S;
-        const float inv_l = p.o_scale / l_run;  // o_scale: the V descale (1 for bf16)
         __nv_bfloat16* orow = p.out + ((size_t)w.bh * p.S + row) * D;
+        if (M && first) {
+            // No key tile for this query tile (block mask): no key is visible to
+            // any of its rows.  O = 0 and LSE = -inf; TMEM O was never written.
+            if (valid) {
+#pragma unroll 1
+                for (int c = 0; c < D; c += 8)
+                    *reinterpret_cast<uint4*>(orow + c) = make_uint4(0u, 0u, 0u, 0u);
+                if (p.lse != nullptr) p.lse[(size_t)w.bh * p.S + row] = -INFINITY;
+            }
+            continue;
+        }
+        const float inv_l = p.o_scale / l_run;  // o_scale: the V descale (1 for bf16)
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
             uint32_t o[32];
@@ -472,7 +550,7 @@ __device__ void ws_softmax_role(const FwdParams& p, uint32_t base, uint32_t tmem
 }
 
 // ---------------------------------------------------------------- kernel
-template <int D, bool F>
+template <int D, bool F, bool M>
 __global__ void __launch_bounds__(WsLayout<D, F>::kThreads, 1)
     attn_fwd_ws_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
@@ -518,13 +596,13 @@ __global__ void __launch_bounds__(WsLayout<D, F>::kThreads, 1)
     if (warp < 4) {
         ptx::regs_dec<L::kRegsSmall>();
         if (warp == 0) {
-            if (lane == 0) ws_load_role<D, F>(&tm_q, &tm_k, &tm_v, p, base, abort_flag);
+            if (lane == 0) ws_load_role<D, F, M>(&tm_q, &tm_k, &tm_v, p, base, abort_flag);
         } else if (warp == 1) {
-            if (lane == 0) ws_mma_role<D, F>(p, base, tmem, abort_flag);
+            if (lane == 0) ws_mma_role<D, F, M>(p, base, tmem, abort_flag);
         }
     } else {
         ptx::regs_inc<L::kRegsSoftmax>();
-        ws_softmax_role<D, F>(p, base, tmem, (warp - 4) >> 2, abort_flag);
+        ws_softmax_role<D, F, M>(p, base, tmem, (warp - 4) >> 2, abort_flag);
     }
 
     ptx::tc_fence_before();

@@ -142,3 +142,17 @@ def qkv_e4m3(B: int, Hq: int, Hkv: int, S: int, D: int, seed: int, sigma: float 
     k = gaussian_e4m3((B, Hkv, S, D), seed, 1, sigma)
     v = gaussian_e4m3((B, Hkv, S, D), seed, 2, sigma)
     return q, k, v
+
+
+def random_block_mask(mask_heads: int, S: int, density: float, seed: int,
+                      stream: int = 7) -> np.ndarray:
+    """uint8 [mask_heads, nt, nt] (nt = ceil(S/128)) with each entry 1 with
+    probability ``density``, from the same SplitMix64 stream construction as
+    the value draws: entry e keeps its block when its 53-bit uniform < density."""
+    nt = (int(S) + 127) // 128
+    n = int(mask_heads) * nt * nt
+    key = _tensor_key(seed, stream)
+    with np.errstate(over="ignore"):
+        u = _splitmix64(key + (np.arange(n, dtype=np.uint64) + np.uint64(1)) * _GOLDEN)
+    uniform = (u >> np.uint64(11)).astype(np.float64) * (1.0 / 9007199254740992.0)
+    return (uniform < density).astype(np.uint8).reshape(mask_heads, nt, nt)

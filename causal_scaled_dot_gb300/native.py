@@ -45,6 +45,9 @@ def load() -> ctypes.CDLL:
         lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ctypes.c_float, ci, vp]
         lib.attn_fwd.restype = ci
         cf = ctypes.c_float
+        lib.attn_fwd_block_masked.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, ci, vp, ci,
+                                              vp]
+        lib.attn_fwd_block_masked.restype = ci
         lib.attn_fwd_fp8.argtypes = [vp, vp, vp, cf, cf, cf, vp, vp, ci, ci, ci, ci, ci, cf, ci, vp]
         lib.attn_fwd_fp8.restype = ci
         lib.attn_sync_status.argtypes = [vp]
@@ -101,6 +104,20 @@ def attn_fwd(q, k, v, out, lse, B: int, Hq: int, Hkv: int, S: int, D: int, scale
                          _stream(stream))
     if check and rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd")
+    return rc
+
+
+def attn_fwd_block_masked(q, k, v, out, lse, B: int, Hq: int, Hkv: int, S: int, D: int,
+                          scale: float, causal: bool | int, block_mask, mask_heads: int, stream=None,
+                          check: bool = True) -> int:
+    """The C entry point ``attn_fwd_block_masked``: ``block_mask`` is a uint8 CUDA
+    tensor (or device pointer) [mask_heads, ceil(S/128), ceil(S/128)]."""
+    rc = load().attn_fwd_block_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), int(B),
+                                      int(Hq), int(Hkv), int(S), int(D), float(scale),
+                                      1 if causal else 0, _ptr(block_mask), int(mask_heads),
+                                      _stream(stream))
+    if check and rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_block_masked")
     return rc
 
 

@@ -75,6 +75,29 @@ int attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse,
              int B, int Hq, int Hkv, int S, int D, float scale, int causal, void *stream);
 
 /*
+ * attn_fwd_block_masked -- attn_fwd plus a block mask that drops whole
+ * 128 x 128 blocks of (query tile, key tile): the block-sparse attention the
+ * ai-manual.ru article gives as a reason to write custom kernels (sections 4
+ * and 7).  Key j is masked for query i when
+ *     block_mask[h][i / 128][j / 128] == 0
+ * on top of the causal mask when causal != 0.
+ *
+ *   block_mask  device memory, uint8 [mask_heads][nt][nt] with nt = ceil(S / 128),
+ *               contiguous; non-zero keeps the block.  Read-only, caller-owned.
+ *   mask_heads  1 (one mask for every batch entry and head) or Hq (one per
+ *               query head, shared across the batch).
+ * Blocks that are dropped are neither loaded nor computed.  A query whose keys
+ * are all masked gets O = 0 and LSE = -inf (the safe-softmax convention of
+ * the "Profiling in PyTorch (Part 3)" retelling, section "The Math Backend").
+ * Other arguments, errors and rules as attn_fwd; ATTN_ERR_INVALID_ARG also for
+ * a NULL mask or mask_heads not 1 or Hq.  The mask contents are not checked
+ * against the shape: the caller guarantees mask_heads * nt * nt bytes.
+ */
+int attn_fwd_block_masked(const void *q, const void *k, const void *v, void *out, float *lse,
+                          int B, int Hq, int Hkv, int S, int D, float scale, int causal,
+                          const unsigned char *block_mask, int mask_heads, void *stream);
+
+/*
  * attn_fwd_fp8 -- the same attention with FP8 E4M3 inputs and per-tensor
  * descale factors (the FP8 attention the ai-manual.ru article mentions for
  * newer GPUs, section 6 "FP8 and BF16").

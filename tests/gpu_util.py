@@ -107,3 +107,36 @@ def compare_fp8(o_gpu, o_ref, l_gpu, l_ref, v_values, label=""):
         stats["lse_max_abs"] = lse_err
         assert lse_err <= tol_lse, f"{label}: LSE max abs error {lse_err:.3e} > {tol_lse}"
     return stats
+
+
+def run_gpu_masked(q_bits, k_bits, v_bits, scale, causal, block_mask, stream=None):
+    """attn_fwd_block_masked through the C ABI; returns (O float64, LSE float64)."""
+    import torch
+    from causal_scaled_dot_gb300 import native
+    B, Hq, S, D = q_bits.shape
+    Hkv = k_bits.shape[1]
+    q, k, v = to_device(q_bits), to_device(k_bits), to_device(v_bits)
+    m = torch.from_numpy(np.ascontiguousarray(block_mask, dtype=np.uint8)).cuda()
+    out = torch.full_like(q, float("nan"))
+    lse = torch.full((B, Hq, S), float("nan"), dtype=torch.float32, device="cuda")
+    native.attn_fwd_block_masked(q, k, v, out, lse, B, Hq, Hkv, S, D, scale, causal, m,
+                                 block_mask.shape[0], stream=stream)
+    native.attn_sync_status(stream)
+    return out.double().cpu().numpy(), lse.double().cpu().numpy()
+
+
+def compare_masked(o_gpu, o_ref, l_gpu, l_ref, label=""):
+    """The bf16 parity bar on rows that see at least one key; rows that see none
+    must hold exactly O = 0 and LSE = -inf on both sides."""
+    D = o_ref.shape[-1]
+    o_gpu, o_ref = o_gpu.reshape(-1, D), o_ref.reshape(-1, D)
+    l_gpu, l_ref = l_gpu.reshape(-1), l_ref.reshape(-1)
+    empty = np.isneginf(l_ref)
+    assert np.all(np.isneginf(l_gpu[empty])), f"{label}: LSE of rows without keys is not -inf"
+    assert np.all(o_gpu[empty] == 0.0), f"{label}: O of rows without keys is not 0"
+    assert np.all(o_ref[empty] == 0.0)
+    live = ~empty
+    stats = {"empty_rows": int(empty.sum())}
+    if live.any():
+        stats.update(compare(o_gpu[live], o_ref[live], l_gpu[live], l_ref[live], label))
+    return stats

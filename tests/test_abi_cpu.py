@@ -5,6 +5,7 @@ import os
 import re
 import subprocess
 
+import numpy as np
 import pytest
 
 from causal_scaled_dot_gb300 import native
@@ -26,7 +27,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for required in ("attn_fwd", "attn_fwd_fp8", "attn_status_string", "attn_sync_status"):
+    for required in ("attn_fwd", "attn_fwd_fp8", "attn_fwd_block_masked", "attn_status_string",
+                     "attn_sync_status"):
         assert required in names
 
 
@@ -122,3 +124,36 @@ def _call_fp8(q=1 << 40, k=2 << 40, v=3 << 40, out=4 << 40, lse=None, dq=1.0, dk
 ])
 def test_fp8_argument_errors_are_rejected_before_launch(kw, code):
     assert _call_fp8(**kw) == code
+
+
+def _call_masked(mask=5 << 40, mask_heads=1, q=1 << 40, k=2 << 40, v=3 << 40, out=4 << 40,
+                 lse=None, B=1, Hq=2, Hkv=2, S=300, D=128, scale=0.1, causal=1):
+    lib = native.load()
+    return lib.attn_fwd_block_masked(q, k, v, out, lse, B, Hq, Hkv, S, D, ctypes.c_float(scale),
+                                     causal, mask, mask_heads, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(mask=None), ATTN_ERR_INVALID_ARG),
+    (dict(mask_heads=0), ATTN_ERR_INVALID_ARG),
+    (dict(mask_heads=3), ATTN_ERR_INVALID_ARG),   # neither 1 nor Hq
+    (dict(mask_heads=-2), ATTN_ERR_INVALID_ARG),
+    (dict(q=None), ATTN_ERR_INVALID_ARG),
+    (dict(Hq=3, Hkv=2, mask_heads=3), ATTN_ERR_INVALID_ARG),
+    (dict(D=96), ATTN_ERR_UNSUPPORTED),
+    (dict(v=(3 << 40) + 2), ATTN_ERR_MISALIGNED),
+])
+def test_masked_argument_errors_are_rejected_before_launch(kw, code):
+    assert _call_masked(**kw) == code
+
+
+def test_random_block_mask_shape_and_density():
+    from causal_scaled_dot_gb300.inputs import random_block_mask
+    m = random_block_mask(4, 1000, 0.3, seed=9)
+    assert m.shape == (4, 8, 8) and m.dtype == np.uint8
+    assert set(np.unique(m)) <= {0, 1}
+    assert np.array_equal(m, random_block_mask(4, 1000, 0.3, seed=9))
+    big = random_block_mask(1, 128 * 200, 0.3, seed=1)
+    assert abs(float(big.mean()) - 0.3) < 0.01
+    assert random_block_mask(1, 256, 0.0, seed=1).sum() == 0
+    assert random_block_mask(1, 256, 1.0, seed=1).all()

@@ -1,0 +1,25 @@
+"""Host-side FLOP accounting of bench.py's block-masked runs, checked by brute
+force on small shapes."""
+import numpy as np
+import pytest
+
+import bench
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("S", [1, 128, 300])
+def test_visible_keys_brute_force(S, causal):
+    nt = (S + 127) // 128
+    m = np.random.default_rng(S).integers(0, 2, (2, nt, nt)).astype(np.uint8)
+    vk = bench.visible_keys(m, S, causal)
+    for h in range(2):
+        for i in range(S):
+            want = sum(1 for j in range(S) if m[h, i // 128, j // 128] and (not causal or j <= i))
+            assert vk[h, i] == want
+
+
+def test_all_ones_mask_counts_every_visible_pair():
+    S = 1000
+    m = np.ones((1, 8, 8), np.uint8)
+    assert np.array_equal(bench.visible_keys(m, S, True)[0], np.arange(1, S + 1))
+    assert np.all(bench.visible_keys(m, S, False)[0] == S)
