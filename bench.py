@@ -374,7 +374,8 @@ def run_ours(args, w, rank, world, local):
         peak *= 2.0
         peak_what = f"{peak_src} bf16 dense (burst) x 2, the nominal fp8/bf16 ratio"
     achieved = flops / (ms_local * 1e-3) / 1e12
-    traffic = None if (fp8 or mask is not None) else recorded_traffic(w.name)
+    variant = w.name + (":fp8" if fp8 else "") + (f":mask{args.mask_density}" if mask is not None else "")
+    traffic = recorded_traffic(variant)
     # algorithmic bytes: inputs read once (1 byte per element for E4M3), O and LSE written once
     io_bytes = w.io_bytes - (w.B * (w.Hq + 2 * w.Hkv) * w.S * w.D if fp8 else 0)
     cpu = None
