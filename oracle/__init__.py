@@ -10,6 +10,10 @@ row at a time, the five steps of the naive causal attention in the order the
 Attention").  This module only builds that file with gcc and marshals numpy
 arrays into it.
 
+It also holds the gradients of the same function (``attention_bwd``: dQ, dK,
+dV and the row term delta for an upstream gradient dO), written out as the
+plain derivative in double precision.
+
 Parity status: pinned.  ``tests/test_oracle_pins.py`` checks it against
 library float64 routines, closed forms and invariants; ``tests/test_oracle_mutants.py``
 plants mistakes into copies of the C source and checks that a pin catches each.
@@ -61,6 +65,13 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     f = lib.oracle_e4m3_decode
     f.restype = None
     f.argtypes = [vp, ctypes.c_int64, vp]
+    f = lib.oracle_attn_rows_f64
+    f.restype = ci
+    f.argtypes = [vp, vp, vp, ci, ci, ci, ci, ci, cf, ci, vp, ctypes.c_int64, vp, vp, ci]
+    f = lib.oracle_attn_bwd
+    f.restype = ci
+    f.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, vp, ctypes.c_int64, vp, vp, vp,
+                  vp, ci]
     return lib
 
 
@@ -204,3 +215,56 @@ def attention(q_bits, k_bits, v_bits, scale: float, causal: bool = True, rows=No
     if rc != 0:
         raise ValueError("oracle_attn_rows rejected its arguments")
     return out, lse
+
+
+def attention_f64(q, k, v, scale: float, causal: bool = True, nthreads: int | None = None,
+                  lib: ctypes.CDLL | None = None):
+    """``attention`` on float64 inputs (no bf16 rounding), full [B,Hq,S,D] / [B,Hq,S] result."""
+    lib = lib or load()
+    q, k, v = (np.ascontiguousarray(x, dtype=np.float64) for x in (q, k, v))
+    B, Hq, Hkv, S, D = _shapes(q, k, v)
+    rows_arr, nrows, out, lse = _outputs(B, Hq, S, D, None)
+    rc = lib.oracle_attn_rows_f64(q.ctypes.data, k.ctypes.data, v.ctypes.data, B, Hq, Hkv, S, D,
+                                  ctypes.c_float(scale), 1 if causal else 0, None, nrows,
+                                  out.ctypes.data, lse.ctypes.data, nthreads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle_attn_rows_f64 rejected its arguments")
+    return out, lse
+
+
+def attention_bwd(q, k, v, dout, scale: float, causal: bool = True, kv_heads=None,
+                  nthreads: int | None = None, lib: ctypes.CDLL | None = None):
+    """Gradients of the attention output: (dQ, dK, dV, delta) in float64.
+
+    q, dout: [B,Hq,S,D]; k, v: [B,Hkv,S,D]; either all bf16 bit patterns
+    (uint16) or all float64.  kv_heads: optional flat ids b*Hkv + hkv; then
+    dQ and delta cover the G = Hq/Hkv query heads of each selected head,
+    shapes [n, G, S, D] and [n, G, S], and dK, dV are [n, S, D].  Without
+    kv_heads: dQ [B,Hq,S,D], dK and dV [B,Hkv,S,D], delta [B,Hq,S].
+    delta_i = sum_j P_ij (dO_i . V_j), the row term of the softmax gradient.
+    """
+    lib = lib or load()
+    f64 = np.asarray(q).dtype == np.float64
+    conv = (lambda x, n: np.ascontiguousarray(x, dtype=np.float64)) if f64 else _as_bits
+    q, k, v, dout = (conv(x, n) for x, n in ((q, "q"), (k, "k"), (v, "v"), (dout, "dout")))
+    B, Hq, Hkv, S, D = _shapes(q, k, v)
+    if dout.shape != q.shape:
+        raise ValueError("dout must have the shape of q")
+    G = Hq // Hkv
+    if kv_heads is None:
+        heads, n = None, B * Hkv
+        dq_shape, kv_shape, d_shape = (B, Hq, S, D), (B, Hkv, S, D), (B, Hq, S)
+    else:
+        heads = np.ascontiguousarray(np.asarray(kv_heads, dtype=np.int64))
+        n = heads.size
+        dq_shape, kv_shape, d_shape = (n, G, S, D), (n, S, D), (n, G, S)
+    dq, dk, dv = np.empty(dq_shape), np.empty(kv_shape), np.empty(kv_shape)
+    delta = np.empty(d_shape)
+    rc = lib.oracle_attn_bwd(q.ctypes.data, k.ctypes.data, v.ctypes.data, dout.ctypes.data,
+                             1 if f64 else 0, B, Hq, Hkv, S, D, ctypes.c_float(scale),
+                             1 if causal else 0, None if heads is None else heads.ctypes.data, n,
+                             dq.ctypes.data, dk.ctypes.data, dv.ctypes.data, delta.ctypes.data,
+                             nthreads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle_attn_bwd rejected its arguments")
+    return dq, dk, dv, delta

@@ -38,9 +38,15 @@
  * tensor (value = decoded code * descale, in double): the FP8 attention that
  * the ai-manual.ru article mentions for newer GPUs (section 6, "FP8 and BF16").
  *
+ * The gradients of the same function (dQ, dK, dV for an upstream dO) are
+ * defined and computed at the end of this file (oracle_attn_bwd).
+ *
  * Parity pins (tests/test_oracle_pins.py): library softmax / SDPA in float64,
  * closed forms (causal row 0, Q = 0 means, S = 1), key-shift and linearity
- * invariants, a hand-derived worked example, and row sums.
+ * invariants, a hand-derived worked example, and row sums.  The gradients:
+ * central finite differences of the forward oracle on double inputs, torch's
+ * float64 autograd, closed forms (dQ of causal row 0, column sums of dK and
+ * dV, dV for Q = 0) and invariants (key shift, linearity in dO).
  */
 #include <math.h>
 #include <pthread.h>
@@ -67,12 +73,14 @@ static double e4m3_bits_to_double(uint8_t b) {
     return sign ? -v : v;
 }
 
-enum { FMT_BF16 = 0, FMT_E4M3 = 1 };
+/* Element formats: bf16 bit patterns (the GPU's inputs), E4M3 codes, or
+ * plain doubles (used by the finite-difference pins of the gradients). */
+enum { FMT_BF16 = 0, FMT_E4M3 = 1, FMT_F64 = 2 };
 
 typedef struct {
-    const void *t[3];        /* q, k, v */
-    int format;              /* FMT_BF16 or FMT_E4M3 */
-    double descale[3];       /* FMT_E4M3: value = decoded code * descale */
+    const void *t[4];        /* q, k, v, and dO for the gradients */
+    int format;              /* FMT_BF16, FMT_E4M3 or FMT_F64 */
+    double descale[4];       /* FMT_E4M3: value = decoded code * descale */
     int B, Hq, Hkv, S, D;
     double scale;
     int causal;
@@ -86,20 +94,23 @@ typedef struct {
     int status;
 } oracle_job_t;
 
-/* Element idx of tensor `which` (0 q, 1 k, 2 v) as a double. */
+/* Element idx of tensor `which` (0 q, 1 k, 2 v, 3 dO) as a double. */
 static double elem(const oracle_job_t *J, int which, int64_t idx) {
     if (J->format == FMT_BF16) return bf16_bits_to_double(((const uint16_t *)J->t[which])[idx]);
+    if (J->format == FMT_F64) return ((const double *)J->t[which])[idx];
     return e4m3_bits_to_double(((const uint8_t *)J->t[which])[idx]) * J->descale[which];
 }
 
 /*
- * One query row: flat id r = (b*Hq + hq)*S + i.
+ * Steps 1-4 for one query row, flat id r = (b*Hq + hq)*S + i: on return s[j]
+ * holds the attention weight of key j (0 where masked) and *lse_out the
+ * log-sum-exp of the scaled, masked scores (-inf when every key is masked,
+ * and then every weight is 0).
  * GQA head mapping: contiguous groups of G = Hq/Hkv query heads share one
  * key/value head, hkv = hq / G (the grouped-query strategy named in the
  * ainews.cool strategy table; with Hkv == Hq it is plain multi-head).
  */
-static void oracle_one_row(const oracle_job_t *J, int64_t r, double *s,
-                           double *o_row, double *lse_out) {
+static void attn_weights(const oracle_job_t *J, int64_t r, double *s, double *lse_out) {
     const int S = J->S, D = J->D;
     const int64_t i = r % S;
     const int64_t bh = r / S;
@@ -110,7 +121,6 @@ static void oracle_one_row(const oracle_job_t *J, int64_t r, double *s,
 
     const int64_t qi = (bh * S + i) * (int64_t)D;              /* q_i */
     const int64_t kb = ((b * J->Hkv + hkv) * S) * (int64_t)D;  /* k_0 of this head */
-    const int64_t vb = ((b * J->Hkv + hkv) * S) * (int64_t)D;  /* v_0 of this head */
 
     /* Step 1: scores_j = sum_d q_id * k_jd. */
     for (int64_t j = 0; j < S; ++j) {
@@ -135,8 +145,8 @@ static void oracle_one_row(const oracle_job_t *J, int64_t r, double *s,
     double m = -INFINITY;
     for (int64_t j = 0; j < S; ++j)
         if (s[j] > m) m = s[j];
-    if (m == -INFINITY) { /* every key masked: output 0, LSE -inf */
-        for (int d = 0; d < D; ++d) o_row[d] = 0.0;
+    if (m == -INFINITY) { /* every key masked: all weights 0, LSE -inf */
+        for (int64_t j = 0; j < S; ++j) s[j] = 0.0;
         *lse_out = -INFINITY;
         return;
     }
@@ -146,13 +156,25 @@ static void oracle_one_row(const oracle_job_t *J, int64_t r, double *s,
         l += s[j];
     }
     for (int64_t j = 0; j < S; ++j) s[j] = s[j] / l;
-    /* Step 5: out_d = sum_j attn_j * v_jd. */
+    *lse_out = m + log(l);
+}
+
+/* One query row of the forward pass: steps 1-4, then step 5. */
+static void oracle_one_row(const oracle_job_t *J, int64_t r, double *s,
+                           double *o_row, double *lse_out) {
+    const int S = J->S, D = J->D;
+    const int64_t i = r % S;
+    const int64_t b = (r / S) / J->Hq;
+    const int64_t hkv = ((r / S) % J->Hq) / (J->Hq / J->Hkv);
+    const int64_t vb = ((b * J->Hkv + hkv) * S) * (int64_t)D;  /* v_0 of this head */
+    (void)i;
+    attn_weights(J, r, s, lse_out);
+    /* Step 5: out_d = sum_j attn_j * v_jd (every weight 0 when all keys are masked). */
     for (int d = 0; d < D; ++d) o_row[d] = 0.0;
     for (int64_t j = 0; j < S; ++j) {
         if (s[j] == 0.0) continue; /* masked key contributes nothing */
         for (int d = 0; d < D; ++d) o_row[d] += s[j] * elem(J, 2, vb + j * D + d);
     }
-    *lse_out = m + log(l);
 }
 
 static void *oracle_worker(void *arg) {
@@ -197,9 +219,10 @@ static int run_rows(const void *q, const void *k, const void *v, int format, con
     int status = 0;
     for (int t = 0; t < nthreads; ++t) {
         oracle_job_t *J = &jobs[t];
-        J->t[0] = q; J->t[1] = k; J->t[2] = v;
+        J->t[0] = q; J->t[1] = k; J->t[2] = v; J->t[3] = NULL;
         J->format = format;
         for (int w = 0; w < 3; ++w) J->descale[w] = descale[w];
+        J->descale[3] = 1.0;
         J->B = B; J->Hq = Hq; J->Hkv = Hkv; J->S = S; J->D = D;
         J->scale = (double)scale;
         J->causal = causal ? 1 : 0;
@@ -274,4 +297,220 @@ int oracle_attn_rows_e4m3(const uint8_t *q, const uint8_t *k, const uint8_t *v, 
 /* Decodes n E4M3 codes to doubles (exposed so the decoding can be pinned). */
 void oracle_e4m3_decode(const uint8_t *codes, int64_t n, double *out) {
     for (int64_t i = 0; i < n; ++i) out[i] = e4m3_bits_to_double(codes[i]);
+}
+
+/*
+ * oracle_attn_rows_f64 -- oracle_attn_rows on double inputs (no rounding of
+ * the inputs at all); the finite-difference pins of the gradients use it.
+ */
+int oracle_attn_rows_f64(const double *q, const double *k, const double *v, int B, int Hq, int Hkv,
+                         int S, int D, float scale, int causal, const int64_t *rows, int64_t nrows,
+                         double *out, double *lse, int nthreads) {
+    const double one[3] = {1.0, 1.0, 1.0};
+    return run_rows(q, k, v, FMT_F64, one, B, Hq, Hkv, S, D, scale, causal, NULL, 1, rows, nrows,
+                    out, lse, nthreads);
+}
+
+/* ======================================================================
+ * Gradients (backward pass).
+ *
+ * The ai-manual.ru article (section 6, "gradients and backward") warns that
+ * the fused backward pass is the hard part to get right; the pages give no
+ * formula, so the oracle is the plain definition: the gradients of the
+ * forward function above with respect to Q, K and V for an upstream gradient
+ * dO of the output.  With P_ij the attention weight of key j for query i
+ * (steps 1-4; 0 where masked) and O_i = sum_j P_ij V_j, differentiating
+ * steps 5, 4 and 1-2 in turn gives, per query head:
+ *   dV_j    = sum_i P_ij dO_i
+ *   dP_ij   = dO_i . V_j
+ *   delta_i = sum_k P_ik dP_ik
+ *   dS_ij   = P_ij (dP_ij - delta_i)          (softmax Jacobian applied to dP)
+ *   dQ_i    = scale * sum_j dS_ij K_j
+ *   dK_j    = scale * sum_i dS_ij Q_i
+ * and a key/value head's dK and dV add up the contributions of every query
+ * head of its group.  Masked pairs have P_ij = 0, hence dS_ij = 0.
+ *
+ * Work per selected key/value head (b, hkv): pass 1, one query row at a time
+ * (any order, rows independent), stores the rows of P and dS of all G query
+ * heads of the group and writes dQ and delta; pass 2, one key at a time,
+ * sums dK_j and dV_j over query heads and rows in ascending order, so the
+ * result does not depend on the number of threads.
+ * ====================================================================== */
+typedef struct {
+    const oracle_job_t *J;
+    int64_t b, hkv, G;
+    double *P, *dS;            /* [G*S][S] rows of weights and score gradients */
+    double *dq, *dk, *dv;      /* [G][S][D], [S][D], [S][D] of this head */
+    double *delta;             /* [G][S] */
+    int pass;
+    int64_t begin, end;
+    int status;
+} bwd_job_t;
+
+/* Pass 1 for row n = g*S + i of the group: P, dP, delta, dS, dQ. */
+static void bwd_row(const bwd_job_t *W, int64_t n, double *dP) {
+    const oracle_job_t *J = W->J;
+    const int S = J->S, D = J->D;
+    const int64_t g = n / S, i = n % S;
+    const int64_t hq = W->hkv * W->G + g;
+    const int64_t bh = W->b * J->Hq + hq;
+    const int64_t qo = (bh * S + i) * (int64_t)D;                   /* q_i and dO_i */
+    const int64_t kvb = ((W->b * J->Hkv + W->hkv) * S) * (int64_t)D; /* k_0, v_0 */
+    double *p = W->P + n * S, *ds = W->dS + n * S;
+    double lse;
+    attn_weights(J, bh * S + i, p, &lse);
+    /* dP_ij = dO_i . V_j (only where P_ij != 0: elsewhere dS_ij = 0 anyway). */
+    for (int64_t j = 0; j < S; ++j) {
+        dP[j] = 0.0;
+        if (p[j] == 0.0) continue;
+        for (int d = 0; d < D; ++d) dP[j] += elem(J, 3, qo + d) * elem(J, 2, kvb + j * D + d);
+    }
+    /* delta_i = sum_k P_ik dP_ik. */
+    double delta = 0.0;
+    for (int64_t j = 0; j < S; ++j) delta += p[j] * dP[j];
+    /* dS_ij = P_ij (dP_ij - delta_i). */
+    for (int64_t j = 0; j < S; ++j) ds[j] = p[j] * (dP[j] - delta);
+    /* dQ_i = scale * sum_j dS_ij K_j. */
+    double *dq = W->dq + n * (int64_t)D;
+    for (int d = 0; d < D; ++d) dq[d] = 0.0;
+    for (int64_t j = 0; j < S; ++j) {
+        if (ds[j] == 0.0) continue;
+        for (int d = 0; d < D; ++d) dq[d] += ds[j] * elem(J, 1, kvb + j * D + d);
+    }
+    for (int d = 0; d < D; ++d) dq[d] *= J->scale;
+    W->delta[n] = delta;
+}
+
+/* Pass 2 for key j: dK_j and dV_j summed over the group's query heads and rows. */
+static void bwd_key(const bwd_job_t *W, int64_t j) {
+    const oracle_job_t *J = W->J;
+    const int S = J->S, D = J->D;
+    double *dk = W->dk + j * (int64_t)D, *dv = W->dv + j * (int64_t)D;
+    for (int d = 0; d < D; ++d) dk[d] = dv[d] = 0.0;
+    for (int64_t g = 0; g < W->G; ++g) {
+        const int64_t bh = W->b * J->Hq + W->hkv * W->G + g;
+        for (int64_t i = 0; i < S; ++i) {
+            const double pij = W->P[(g * S + i) * S + j], dsij = W->dS[(g * S + i) * S + j];
+            if (pij == 0.0) continue;
+            const int64_t qo = (bh * S + i) * (int64_t)D;
+            for (int d = 0; d < D; ++d) {
+                dv[d] += pij * elem(J, 3, qo + d);
+                dk[d] += dsij * elem(J, 0, qo + d);
+            }
+        }
+    }
+    for (int d = 0; d < D; ++d) dk[d] *= J->scale;
+}
+
+static void *bwd_worker(void *arg) {
+    bwd_job_t *W = (bwd_job_t *)arg;
+    double *dP = NULL;
+    if (W->pass == 1 && !(dP = (double *)malloc(sizeof(double) * (size_t)W->J->S))) {
+        W->status = 1;
+        return NULL;
+    }
+    for (int64_t n = W->begin; n < W->end; ++n) {
+        if (W->pass == 1)
+            bwd_row(W, n, dP);
+        else
+            bwd_key(W, n);
+    }
+    free(dP);
+    W->status = 0;
+    return NULL;
+}
+
+/* Runs pass `pass` over [0, count) on nthreads threads; 0 on success. */
+static int bwd_parallel(const bwd_job_t *proto, int pass, int64_t count, int nthreads) {
+    if (nthreads > count) nthreads = (int)count;
+    if (nthreads < 1) nthreads = 1;
+    bwd_job_t *jobs = (bwd_job_t *)calloc((size_t)nthreads, sizeof(bwd_job_t));
+    pthread_t *tid = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    if (!jobs || !tid) {
+        free(jobs);
+        free(tid);
+        return 1;
+    }
+    for (int t = 0; t < nthreads; ++t) {
+        jobs[t] = *proto;
+        jobs[t].pass = pass;
+        jobs[t].begin = count * t / nthreads;
+        jobs[t].end = count * (t + 1) / nthreads;
+        jobs[t].status = 1;
+    }
+    int started = 0;
+    for (int t = 1; t < nthreads; ++t) {
+        if (pthread_create(&tid[t], NULL, bwd_worker, &jobs[t]) != 0) break;
+        started = t;
+    }
+    bwd_worker(&jobs[0]);
+    for (int t = 1; t <= started; ++t) pthread_join(tid[t], NULL);
+    for (int t = started + 1; t < nthreads; ++t) bwd_worker(&jobs[t]);
+    int status = 0;
+    for (int t = 0; t < nthreads; ++t) status |= jobs[t].status;
+    free(jobs);
+    free(tid);
+    return status;
+}
+
+/*
+ * oracle_attn_bwd -- dQ, dK, dV and delta for selected key/value heads.
+ *
+ *   q, dout [B,Hq,S,D], k, v [B,Hkv,S,D]: bf16 bit patterns (f64_inputs == 0)
+ *        or doubles (f64_inputs != 0), contiguous.
+ *   kv_heads: n_kv_heads flat ids b*Hkv + hkv, or NULL for all of them in
+ *        order (then n_kv_heads must be B*Hkv).
+ *   dq: double [n_kv_heads][G][S][D] -- the G = Hq/Hkv query heads of each
+ *       selected key/value head (with every head selected: [B,Hq,S,D]);
+ *   dk, dv: double [n_kv_heads][S][D];  delta: double [n_kv_heads][G][S].
+ * Returns 0 on success, 1 on a bad argument or allocation failure.
+ */
+int oracle_attn_bwd(const void *q, const void *k, const void *v, const void *dout, int f64_inputs,
+                    int B, int Hq, int Hkv, int S, int D, float scale, int causal,
+                    const int64_t *kv_heads, int64_t n_kv_heads, double *dq, double *dk,
+                    double *dv, double *delta, int nthreads) {
+    if (!q || !k || !v || !dout || !dq || !dk || !dv || !delta) return 1;
+    if (B < 1 || Hq < 1 || Hkv < 1 || S < 1 || D < 1 || Hq % Hkv != 0) return 1;
+    if (!kv_heads && n_kv_heads != (int64_t)B * Hkv) return 1;
+    if (kv_heads)
+        for (int64_t n = 0; n < n_kv_heads; ++n)
+            if (kv_heads[n] < 0 || kv_heads[n] >= (int64_t)B * Hkv) return 1;
+    oracle_job_t J;
+    memset(&J, 0, sizeof J);
+    J.t[0] = q; J.t[1] = k; J.t[2] = v; J.t[3] = dout;
+    J.format = f64_inputs ? FMT_F64 : FMT_BF16;
+    for (int w = 0; w < 4; ++w) J.descale[w] = 1.0;
+    J.B = B; J.Hq = Hq; J.Hkv = Hkv; J.S = S; J.D = D;
+    J.scale = (double)scale;
+    J.causal = causal ? 1 : 0;
+    J.mask_heads = 1;
+    const int64_t G = Hq / Hkv;
+    double *P = (double *)malloc(sizeof(double) * (size_t)(G * S) * (size_t)S);
+    double *dS = (double *)malloc(sizeof(double) * (size_t)(G * S) * (size_t)S);
+    if (!P || !dS) {
+        free(P);
+        free(dS);
+        return 1;
+    }
+    int status = 0;
+    for (int64_t n = 0; n < n_kv_heads && !status; ++n) {
+        const int64_t flat = kv_heads ? kv_heads[n] : n;
+        bwd_job_t W;
+        memset(&W, 0, sizeof W);
+        W.J = &J;
+        W.b = flat / Hkv;
+        W.hkv = flat % Hkv;
+        W.G = G;
+        W.P = P;
+        W.dS = dS;
+        W.dq = dq + n * G * S * (int64_t)D;
+        W.dk = dk + n * S * (int64_t)D;
+        W.dv = dv + n * S * (int64_t)D;
+        W.delta = delta + n * G * S;
+        status |= bwd_parallel(&W, 1, G * S, nthreads);
+        if (!status) status |= bwd_parallel(&W, 2, S, nthreads);
+    }
+    free(P);
+    free(dS);
+    return status;
 }

@@ -386,3 +386,120 @@ def pin_block_mask_all_ones(attnm, attn):
 
 
 MASK_PINS = [pin_block_mask_library, pin_block_mask_all_ones]
+
+
+# ---------------------------------------------------------------- gradients
+# Each takes ``bwd(q, k, v, dout, scale, causal, kv_heads=None)`` returning
+# (dQ, dK, dV, delta) in float64 (bf16 bit patterns or float64 inputs).
+
+def _loss_grad_fd(fwd64, q, k, v, dout, scale, causal, h=1e-5):
+    """Central differences of L = sum(dout * O) with respect to every element
+    of q, k and v, each from two calls of the forward oracle on float64 inputs."""
+    def loss(qq, kk, vv):
+        return float(np.sum(dout * fwd64(qq, kk, vv, scale, causal)[0]))
+    grads = []
+    for which in range(3):
+        base = [q, k, v]
+        g = np.zeros_like(base[which])
+        for idx in np.ndindex(g.shape):
+            plus = [x.copy() for x in base]
+            minus = [x.copy() for x in base]
+            plus[which][idx] += h
+            minus[which][idx] -= h
+            g[idx] = (loss(*plus) - loss(*minus)) / (2 * h)
+        grads.append(g)
+    return grads
+
+
+def pin_bwd_finite_differences(bwd, fwd64):
+    """Gradients against central differences of the forward oracle (float64
+    inputs, step 1e-5: truncation ~1e-10), GQA, causal and not; delta against
+    sum_d dO_id O_id from the forward output."""
+    rng = np.random.default_rng(151)
+    B, Hq, Hkv, S, D = 1, 2, 1, 6, 3
+    q, dout = rng.standard_normal((B, Hq, S, D)), rng.standard_normal((B, Hq, S, D))
+    k, v = rng.standard_normal((B, Hkv, S, D)), rng.standard_normal((B, Hkv, S, D))
+    for causal in (True, False):
+        dq, dk, dv, delta = bwd(q, k, v, dout, 0.6, causal)
+        fq, fk, fv = _loss_grad_fd(fwd64, q, k, v, dout, 0.6, causal)
+        for name, a, b in (("dQ", dq, fq), ("dK", dk, fk), ("dV", dv, fv)):
+            err = float(np.max(np.abs(a - b)))
+            assert err < 1e-7, f"{name} vs finite differences: {err:.2e} (causal={causal})"
+        O = fwd64(q, k, v, 0.6, causal)[0]
+        assert np.max(np.abs(delta - np.sum(dout * O, axis=-1))) < 1e-12
+
+
+def pin_bwd_torch_autograd(bwd):
+    """Gradients against torch's float64 autograd through scaled_dot_product_attention
+    on CPU (key/value heads expanded with repeat_interleave, whose backward sums
+    the group), causal and not, several tiles and a ragged tail."""
+    B, Hq, Hkv, S, D = 2, 4, 2, 150, 16
+    q, k, v = (_rand((B, H, S, D), 161, t) for t, H in ((0, Hq), (1, Hkv), (2, Hkv)))
+    dout = _rand((B, Hq, S, D), 161, 3)
+    scale = 0.3
+    G = Hq // Hkv
+    for causal in (True, False):
+        dq, dk, dv, delta = bwd(q, k, v, dout, scale, causal)
+        tq, tk, tv = (torch.from_numpy(f64(x)).requires_grad_() for x in (q, k, v))
+        o = F.scaled_dot_product_attention(tq, tk.repeat_interleave(G, 1), tv.repeat_interleave(G, 1),
+                                           is_causal=causal, scale=float(np.float32(scale)))
+        o.backward(torch.from_numpy(f64(dout)))
+        for name, a, t in (("dQ", dq, tq), ("dK", dk, tk), ("dV", dv, tv)):
+            ref = t.grad.numpy()
+            err = float(np.max(np.abs(a - ref)))
+            assert err <= 1e-12 * max(1.0, float(np.max(np.abs(ref)))), f"{name}: {err:.2e}"
+        ref_delta = np.sum(f64(dout) * o.detach().numpy(), axis=-1)
+        assert np.max(np.abs(delta - ref_delta)) < 1e-12
+
+
+def pin_bwd_closed_forms(bwd):
+    """Causal row 0 attends to key 0 alone (weight exactly 1), so dQ_0 = 0
+    exactly.  Weights sum to 1 in every row, so the dV rows sum to the dO rows
+    of the group and the dK rows sum to 0.  With Q = 0 the causal weights are
+    1/(i+1), so dV_j = sum_{i>=j} dO_i / (i+1)."""
+    B, Hq, Hkv, S, D = 1, 4, 2, 90, 8
+    q, k, v = (_rand((B, H, S, D), 171, t) for t, H in ((0, Hq), (1, Hkv), (2, Hkv)))
+    dout = _rand((B, Hq, S, D), 171, 3)
+    dq, dk, dv, _ = bwd(q, k, v, dout, 0.4, True)
+    assert np.all(dq[:, :, 0, :] == 0.0), "causal row 0 must have dQ = 0"
+    d64 = f64(dout).reshape(B, Hkv, Hq // Hkv, S, D)
+    assert np.max(np.abs(dv.sum(axis=2) - d64.sum(axis=(2, 3)))) < 1e-11
+    assert np.max(np.abs(dk.sum(axis=2))) < 1e-11
+    qz = bits(np.zeros((1, 1, S, D)))
+    _, _, dvz, _ = bwd(qz, k[:, :1], v[:, :1], dout[:, :1], 0.4, True)
+    do1 = f64(dout[0, 0])
+    want = np.array([sum(do1[i] / (i + 1) for i in range(j, S)) for j in range(S)])
+    assert np.max(np.abs(dvz[0, 0] - want)) < 1e-12
+
+
+def pin_bwd_invariants(bwd):
+    """Adding a constant vector to every key leaves the output unchanged as a
+    function of Q, K, V, so the gradients do not change; the gradients are
+    linear in dO; a subset of key/value heads gives exactly those heads."""
+    B, Hq, Hkv, S, D = 2, 4, 2, 70, 8
+    rng = np.random.default_rng(181)
+    q = bits(_grid((B, Hq, S, D), rng, -2, 2, 0.25))
+    k = bits(_grid((B, Hkv, S, D), rng, -2, 2, 0.25))
+    v = bits(_grid((B, Hkv, S, D), rng, -2, 2, 0.25))
+    d1 = bits(_grid((B, Hq, S, D), rng, -2, 2, 0.25))
+    d2 = bits(_grid((B, Hq, S, D), rng, -2, 2, 0.25))
+    c = bits(_grid((D,), rng, -1, 1, 0.25))
+    ks = bits(f64(k) + f64(c))
+    for causal in (True, False):
+        g = bwd(q, k, v, d1, 0.5, causal)
+        gs = bwd(q, ks, v, d1, 0.5, causal)
+        for a, b in zip(g[:3], gs[:3]):
+            assert np.max(np.abs(a - b)) < 1e-11, "key shift changed a gradient"
+        g2 = bwd(q, k, v, d2, 0.5, causal)
+        g12 = bwd(q, k, v, bits(f64(d1) + f64(d2)), 0.5, causal)
+        for a, b, s in zip(g[:3], g2[:3], g12[:3]):
+            assert np.max(np.abs(a + b - s)) < 1e-11, "gradients not linear in dO"
+        sub = bwd(q, k, v, d1, 0.5, causal, kv_heads=[3, 0])
+        G = Hq // Hkv
+        dq = g[0].reshape(B * Hkv, G, S, D)
+        assert np.array_equal(sub[0], dq[[3, 0]])
+        assert np.array_equal(sub[1], g[1].reshape(B * Hkv, S, D)[[3, 0]])
+        assert np.array_equal(sub[2], g[2].reshape(B * Hkv, S, D)[[3, 0]])
+
+
+BWD_PINS = [pin_bwd_torch_autograd, pin_bwd_closed_forms, pin_bwd_invariants]

@@ -38,6 +38,22 @@ MUTANTS = {
                               "if (J->block_mask[(j / 128) * ((S + 127) / 128) + i / 128] == 0) s[j] = -INFINITY;"),
     "block_mask_heads_ignored": ("(J->mask_heads == 1 ? 0 : hq)", "(0)"),
     "block_mask_ignored": ("if (J->block_mask) {", "if (0) {"),
+    "bwd_delta_not_subtracted": ("ds[j] = p[j] * (dP[j] - delta);", "ds[j] = p[j] * dP[j];"),
+    "bwd_delta_unweighted": ("delta += p[j] * dP[j];", "delta += dP[j];"),
+    "bwd_dq_scale_dropped": ("for (int d = 0; d < D; ++d) dq[d] *= J->scale;", ""),
+    "bwd_dk_scale_dropped": ("for (int d = 0; d < D; ++d) dk[d] *= J->scale;", ""),
+    "bwd_dv_uses_score_gradient": ("dv[d] += pij * elem(J, 3, qo + d);",
+                                   "dv[d] += dsij * elem(J, 3, qo + d);"),
+    "bwd_dk_uses_weights": ("dk[d] += dsij * elem(J, 0, qo + d);",
+                            "dk[d] += pij * elem(J, 0, qo + d);"),
+    "bwd_dq_uses_values": ("dq[d] += ds[j] * elem(J, 1, kvb + j * D + d);",
+                           "dq[d] += ds[j] * elem(J, 2, kvb + j * D + d);"),
+    "bwd_dp_uses_keys": ("dP[j] += elem(J, 3, qo + d) * elem(J, 2, kvb + j * D + d);",
+                         "dP[j] += elem(J, 3, qo + d) * elem(J, 1, kvb + j * D + d);"),
+    "bwd_group_interleaved": ("const int64_t hq = W->hkv * W->G + g;",
+                              "const int64_t hq = W->hkv + g * J->Hkv;"),
+    "bwd_dkdv_first_head_only": ("for (int64_t g = 0; g < W->G; ++g) {",
+                                 "for (int64_t g = 0; g < 1; ++g) {"),
 }
 
 
@@ -60,6 +76,12 @@ def test_some_pin_catches_mutant(name, tmp_path):
     def attnm(q, k, v, scale, mask, causal, rows=None):
         return oracle.attention_masked(q, k, v, scale, mask, causal, rows=rows, lib=lib)
 
+    def bwd(q, k, v, dout, scale, causal, kv_heads=None):
+        return oracle.attention_bwd(q, k, v, dout, scale, causal, kv_heads=kv_heads, lib=lib)
+
+    def fwd64(q, k, v, scale, causal):
+        return oracle.attention_f64(q, k, v, scale, causal, nthreads=1, lib=lib)
+
     checks = [(p.__name__, lambda p=p: p(attn)) for p in oracle_pins.ALL_PINS] + [
         ("pin_e4m3_decode", lambda: oracle_pins.pin_e4m3_decode(
             lambda c: oracle.e4m3_decode(c, lib=lib))),
@@ -67,7 +89,8 @@ def test_some_pin_catches_mutant(name, tmp_path):
         ("pin_e4m3_matches_bf16_path", lambda: oracle_pins.pin_e4m3_matches_bf16_path(attn8, attn)),
         ("pin_block_mask_library", lambda: oracle_pins.pin_block_mask_library(attnm)),
         ("pin_block_mask_all_ones", lambda: oracle_pins.pin_block_mask_all_ones(attnm, attn)),
-    ]
+        ("pin_bwd_finite_differences", lambda: oracle_pins.pin_bwd_finite_differences(bwd, fwd64)),
+    ] + [(p.__name__, lambda p=p: p(bwd)) for p in oracle_pins.BWD_PINS]
     caught = []
     for pin_name, run in checks:
         try:

@@ -30,6 +30,28 @@ def test_oracle_block_mask_pins():
     oracle_pins.pin_block_mask_all_ones(attnm, _attn)
 
 
+def _bwd(q, k, v, dout, scale, causal, kv_heads=None):
+    return oracle.attention_bwd(q, k, v, dout, scale, causal, kv_heads=kv_heads)
+
+
+def test_oracle_bwd_finite_differences():
+    oracle_pins.pin_bwd_finite_differences(_bwd, oracle.attention_f64)
+
+
+@pytest.mark.parametrize("pin", oracle_pins.BWD_PINS, ids=lambda p: p.__name__)
+def test_oracle_bwd_pin(pin):
+    pin(_bwd)
+
+
+def test_oracle_bwd_thread_count_does_not_change_bits():
+    from causal_scaled_dot_gb300.inputs import gaussian_bf16, qkv_bf16
+    q, k, v = qkv_bf16(1, 4, 2, 50, 8, seed=10)
+    do = gaussian_bf16((1, 4, 50, 8), 10, 3)
+    a = oracle.attention_bwd(q, k, v, do, 0.3, True, nthreads=1)
+    b = oracle.attention_bwd(q, k, v, do, 0.3, True, nthreads=6)
+    assert all(np.array_equal(x, y) for x, y in zip(a, b))
+
+
 def test_rows_subset_matches_full():
     """The row-selection entry computes exactly the rows of the full call."""
     from causal_scaled_dot_gb300.inputs import qkv_bf16
