@@ -342,3 +342,31 @@ extern "C" const char* attn_status_string(int status) {
 }
 
 extern "C" int attn_version(void) { return kVersion; }
+
+// ---------------------------------------------------------------- shared host services
+#include "host.h"
+
+namespace attn {
+namespace host {
+
+int current_device(int* sm_count, unsigned int** status_word) {
+    DeviceState* dev = nullptr;
+    const int rc = current_device_state(&dev);
+    if (rc != ATTN_OK) return rc;
+    *sm_count = dev->sm_count;
+    *status_word = dev->status_word;
+    return ATTN_OK;
+}
+
+int encode_bf16_tiles(CUtensorMap* map, const void* ptr, int D, int S, long long outer) {
+    return encode_bf16_3d(map, ptr, D, S, outer, kTile);
+}
+
+bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
+    return attn::ranges_overlap(a, na, b, nb);
+}
+
+unsigned long long wait_limit_ns() { return kWaitLimitNs; }
+
+}  // namespace host
+}  // namespace attn

@@ -1,0 +1,136 @@
+// attn_bwd.cu -- the backward entry point of libattn (include/attn.h):
+// argument checks, TMA descriptors, and the two kernel launches (dQ with
+// delta, then dK/dV) on the caller's stream.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/attn.h"
+#include "common.cuh"
+#include "host.h"
+#include "kernel_bwd.cuh"
+
+namespace attn {
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_bwd_mutex;
+int g_bwd_ready[kMaxDevices];  // 0 not yet, 1 ready, else an ATTN_ERR code
+
+template <typename K>
+cudaError_t allow_smem(K kernel, uint32_t bytes) {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+// Shared-memory opt-in of the backward kernels, once per device.
+int setup_bwd_kernels() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_DEVICE;
+    std::lock_guard<std::mutex> lock(g_bwd_mutex);
+    if (g_bwd_ready[dev] == 0) {
+        const bool ok =
+            allow_smem(attn_bwd_dq_kernel<64>, DqLayout<64>::kDynamicSmem) == cudaSuccess &&
+            allow_smem(attn_bwd_dq_kernel<128>, DqLayout<128>::kDynamicSmem) == cudaSuccess &&
+            allow_smem(attn_bwd_dkdv_kernel<64>, DkvLayout<64>::kDynamicSmem) == cudaSuccess &&
+            allow_smem(attn_bwd_dkdv_kernel<128>, DkvLayout<128>::kDynamicSmem) == cudaSuccess;
+        g_bwd_ready[dev] = ok ? 1 : ATTN_ERR_DEVICE;
+    }
+    return g_bwd_ready[dev] == 1 ? ATTN_OK : g_bwd_ready[dev];
+}
+
+int check_bwd_args(const void* q, const void* k, const void* v, const void* out, const void* dout,
+                   const float* lse, float* delta, void* dq, void* dk, void* dv, int B, int Hq,
+                   int Hkv, int S, int D, float scale) {
+    if (!q || !k || !v || !out || !dout || !lse || !delta || !dq || !dk || !dv) return ATTN_ERR_INVALID_ARG;
+    if (B < 1 || Hq < 1 || Hkv < 1 || S < 1) return ATTN_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+    if ((long long)B * Hq > (1ll << 30) || S > (1 << 30)) return ATTN_ERR_UNSUPPORTED;
+    const uintptr_t mis16 = (reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                             reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out) |
+                             reinterpret_cast<uintptr_t>(dout) | reinterpret_cast<uintptr_t>(dq) |
+                             reinterpret_cast<uintptr_t>(dk) | reinterpret_cast<uintptr_t>(dv)) & 15u;
+    const uintptr_t mis4 = (reinterpret_cast<uintptr_t>(lse) | reinterpret_cast<uintptr_t>(delta)) & 3u;
+    if (mis16 || mis4) return ATTN_ERR_MISALIGNED;
+    // Outputs may overlap nothing else.
+    const size_t qb = (size_t)B * Hq * S * D * 2, kb = (size_t)B * Hkv * S * D * 2, lb = (size_t)B * Hq * S * 4;
+    const void* ins[6] = {q, k, v, out, dout, lse};
+    const size_t in_bytes[6] = {qb, kb, kb, qb, qb, lb};
+    const void* outs[4] = {dq, dk, dv, delta};
+    const size_t out_bytes[4] = {qb, kb, kb, lb};
+    for (int o = 0; o < 4; ++o) {
+        for (int i = 0; i < 6; ++i)
+            if (host::ranges_overlap(outs[o], out_bytes[o], ins[i], in_bytes[i])) return ATTN_ERR_INVALID_ARG;
+        for (int o2 = o + 1; o2 < 4; ++o2)
+            if (host::ranges_overlap(outs[o], out_bytes[o], outs[o2], out_bytes[o2])) return ATTN_ERR_INVALID_ARG;
+    }
+    return ATTN_OK;
+}
+
+template <int D>
+int launch_bwd(const CUtensorMap& tq, const CUtensorMap& tdo, const CUtensorMap& tk,
+               const CUtensorMap& tv, BwdParams p, int sm_count, cudaStream_t stream) {
+    const long long dq_units = (long long)p.B * p.Hq * p.num_tiles;
+    const long long dkv_units = (long long)p.B * p.Hkv * p.num_tiles;
+    if (dq_units > (1ll << 31) - 1) return ATTN_ERR_UNSUPPORTED;
+    p.num_units = (int)dq_units;
+    int grid = (int)(dq_units < sm_count ? dq_units : sm_count);
+    attn_bwd_dq_kernel<D><<<grid, DqLayout<D>::kThreads, DqLayout<D>::kDynamicSmem, stream>>>(tq, tdo, tk, tv, p);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
+    p.num_units = (int)dkv_units;
+    grid = (int)(dkv_units < sm_count ? dkv_units : sm_count);
+    attn_bwd_dkdv_kernel<D><<<grid, DkvLayout<D>::kThreads, DkvLayout<D>::kDynamicSmem, stream>>>(tq, tdo, tk, tv, p);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+}  // namespace
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
+                        const float* lse, float* delta, void* dq, void* dk, void* dv, int B, int Hq,
+                        int Hkv, int S, int D, float scale, int causal, void* stream) {
+    int rc = check_bwd_args(q, k, v, out, dout, lse, delta, dq, dk, dv, B, Hq, Hkv, S, D, scale);
+    if (rc != ATTN_OK) return rc;
+    int sm_count = 0;
+    unsigned int* status = nullptr;
+    rc = host::current_device(&sm_count, &status);
+    if (rc != ATTN_OK) return rc;
+    rc = setup_bwd_kernels();
+    if (rc != ATTN_OK) return rc;
+
+    alignas(64) CUtensorMap tq, tdo, tk, tv;
+    if (host::encode_bf16_tiles(&tq, q, D, S, (long long)B * Hq) != ATTN_OK ||
+        host::encode_bf16_tiles(&tdo, dout, D, S, (long long)B * Hq) != ATTN_OK ||
+        host::encode_bf16_tiles(&tk, k, D, S, (long long)B * Hkv) != ATTN_OK ||
+        host::encode_bf16_tiles(&tv, v, D, S, (long long)B * Hkv) != ATTN_OK)
+        return ATTN_ERR_INVALID_ARG;
+
+    BwdParams p{};
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.S = S;
+    p.group = Hq / Hkv;
+    p.num_tiles = (S + kTile - 1) / kTile;
+    p.causal = causal ? 1 : 0;
+    p.scale = scale;
+    p.scale_log2 = scale * kLog2e;
+    p.out = static_cast<const __nv_bfloat16*>(out);
+    p.dout = static_cast<const __nv_bfloat16*>(dout);
+    p.lse = lse;
+    p.delta = delta;
+    p.dq = static_cast<__nv_bfloat16*>(dq);
+    p.dk = static_cast<__nv_bfloat16*>(dk);
+    p.dv = static_cast<__nv_bfloat16*>(dv);
+    p.status = status;
+    p.wait_limit_ns = host::wait_limit_ns();
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return D == 64 ? launch_bwd<64>(tq, tdo, tk, tv, p, sm_count, st)
+                   : launch_bwd<128>(tq, tdo, tk, tv, p, sm_count, st);
+}

@@ -48,6 +48,9 @@ def load() -> ctypes.CDLL:
         lib.attn_fwd_block_masked.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, ci, vp, ci,
                                               vp]
         lib.attn_fwd_block_masked.restype = ci
+        lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, ci,
+                                 vp]
+        lib.attn_bwd.restype = ci
         lib.attn_fwd_fp8.argtypes = [vp, vp, vp, cf, cf, cf, vp, vp, ci, ci, ci, ci, ci, cf, ci, vp]
         lib.attn_fwd_fp8.restype = ci
         lib.attn_sync_status.argtypes = [vp]
@@ -118,6 +121,17 @@ def attn_fwd_block_masked(q, k, v, out, lse, B: int, Hq: int, Hkv: int, S: int, 
                                       _stream(stream))
     if check and rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_block_masked")
+    return rc
+
+
+def attn_bwd(q, k, v, out, dout, lse, delta, dq, dk, dv, B: int, Hq: int, Hkv: int, S: int, D: int,
+             scale: float, causal: bool | int, stream=None, check: bool = True) -> int:
+    """The C entry point ``attn_bwd``: dQ, dK, dV (and delta) for upstream dO."""
+    rc = load().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(delta),
+                         _ptr(dq), _ptr(dk), _ptr(dv), int(B), int(Hq), int(Hkv), int(S), int(D),
+                         float(scale), 1 if causal else 0, _stream(stream))
+    if check and rc != ATTN_OK:
+        raise AttnError(rc, "attn_bwd")
     return rc
 
 

@@ -120,6 +120,35 @@ int attn_fwd_fp8(const void *q, const void *k, const void *v, float q_descale, f
                  float scale, int causal, void *stream);
 
 /*
+ * attn_bwd -- gradients of attn_fwd's output: dQ, dK, dV for an upstream
+ * gradient dO.  The pages give no formula (the ai-manual.ru article, section 6,
+ * only warns that the fused backward pass is hard to get right); this is the
+ * derivative of the forward:
+ *     P_ij = exp(scale * q_i . k_j - LSE_i)  (0 for masked pairs),
+ *     dP_ij = dO_i . V_j,  delta_i = dO_i . O_i,  dS_ij = P_ij (dP_ij - delta_i),
+ *     dQ_i = scale * sum_j dS_ij K_j,  dK_j = scale * sum_i dS_ij Q_i,
+ *     dV_j = sum_i P_ij dO_i,
+ * with dK and dV of a key/value head summed over its group's query heads.
+ *
+ *   q, k, v, scale, B, Hq, Hkv, S, D, causal   exactly as passed to attn_fwd.
+ *   out      bf16 [B,Hq,S,D]: attn_fwd's output O.
+ *   dout     bf16 [B,Hq,S,D]: the upstream gradient dO.
+ *   lse      fp32 [B,Hq,S]: attn_fwd's LSE (required here).
+ *   delta    fp32 [B,Hq,S], written: delta_i = dO_i . O_i (the kernels'
+ *            row term; callers may read it).
+ *   dq       bf16 [B,Hq,S,D], written.
+ *   dk, dv   bf16 [B,Hkv,S,D], written.
+ * Every pointer is device memory owned by the caller; the bf16 tensors must be
+ * 16-byte aligned, lse and delta 4-byte aligned.  The outputs (delta, dq, dk,
+ * dv) may overlap neither the inputs nor each other (ATTN_ERR_INVALID_ARG).
+ * Two kernels run on `stream` (dQ and delta, then dK and dV); the call is
+ * asynchronous and allocates nothing.  Other errors as attn_fwd.
+ */
+int attn_bwd(const void *q, const void *k, const void *v, const void *out, const void *dout,
+             const float *lse, float *delta, void *dq, void *dk, void *dv, int B, int Hq, int Hkv,
+             int S, int D, float scale, int causal, void *stream);
+
+/*
  * attn_sync_status -- synchronise `stream` and report device-side failures of
  * the attention kernels enqueued on this device since the last call.
  *

@@ -2,6 +2,8 @@
 libattn through its C ABI, and compare with the fp64 oracle."""
 from __future__ import annotations
 
+import math
+
 import numpy as np
 
 # Tolerances on bf16 O against the fp64 oracle, and on fp32 LSE.
@@ -140,3 +142,59 @@ def compare_masked(o_gpu, o_ref, l_gpu, l_ref, label=""):
     if live.any():
         stats.update(compare(o_gpu[live], o_ref[live], l_gpu[live], l_ref[live], label))
     return stats
+
+
+# Backward: tolerances on bf16 dQ, dK, dV against the fp64 oracle.  A term of
+# each product carries at most two bf16 roundings (P or dS, then the output),
+# and delta comes from the bf16 forward output, each <= 2^-9 relative; under
+# independent rounding errors that is about 3 * 2^-9 = 0.006 relative L2, so
+# 1e-2 is the bound; the largest element error stays within 2 % of the
+# tensor's largest magnitude.
+TOL_GRAD_REL_L2 = 1e-2
+TOL_GRAD_MAX_REL = 2e-2
+
+
+def run_gpu_bwd(q_bits, k_bits, v_bits, do_bits, scale, causal, stream=None):
+    """attn_fwd then attn_bwd through the C ABI on the same device buffers.
+    Returns float64 (O, LSE, dQ, dK, dV, delta)."""
+    import torch
+    from causal_scaled_dot_gb300 import native
+    B, Hq, S, D = q_bits.shape
+    Hkv = k_bits.shape[1]
+    q, k, v, do = to_device(q_bits), to_device(k_bits), to_device(v_bits), to_device(do_bits)
+    out = torch.empty_like(q)
+    lse = torch.empty((B, Hq, S), dtype=torch.float32, device="cuda")
+    native.attn_fwd(q, k, v, out, lse, B, Hq, Hkv, S, D, scale, causal, stream=stream)
+    dq = torch.full_like(q, float("nan"))
+    dk = torch.full_like(k, float("nan"))
+    dv = torch.full_like(v, float("nan"))
+    delta = torch.full((B, Hq, S), float("nan"), dtype=torch.float32, device="cuda")
+    native.attn_bwd(q, k, v, out, do, lse, delta, dq, dk, dv, B, Hq, Hkv, S, D, scale, causal,
+                    stream=stream)
+    native.attn_sync_status(stream)
+    return tuple(t.double().cpu().numpy() for t in (out, lse, dq, dk, dv, delta))
+
+
+def compare_grad(g, ref, label):
+    """Relative L2 and largest error against the tensor's largest magnitude, with
+    an absolute floor of 1e-3 per element: a gradient that is exactly 0 (causal
+    row 0's dQ, a single key) is compared absolutely."""
+    assert np.all(np.isfinite(g)), f"{label}: non-finite values (unwritten rows?)"
+    if ref.size == 0:
+        return {}
+    err = np.abs(g - ref)
+    floor = 1e-3
+    rel_l2 = float(np.linalg.norm(g - ref) / max(np.linalg.norm(ref), floor * math.sqrt(ref.size)))
+    max_rel = float(np.max(err)) / max(float(np.max(np.abs(ref))), floor)
+    assert rel_l2 <= TOL_GRAD_REL_L2, f"{label}: rel L2 {rel_l2:.3e} > {TOL_GRAD_REL_L2}"
+    assert max_rel <= TOL_GRAD_MAX_REL, f"{label}: max abs / max|ref| {max_rel:.3e} > {TOL_GRAD_MAX_REL}"
+    return {"rel_l2": rel_l2, "max_rel": max_rel}
+
+
+def compare_delta(delta, delta_ref, o_ref, do, label):
+    """delta_i = dO_i . O_i with O rounded to bf16: per row at most
+    2^-8 * sum_d |dO_id O_id| apart (one bf16 rounding, margin 2), plus fp32 sums."""
+    tol = 2.0 ** -8 * np.sum(np.abs(do * o_ref), axis=-1) + 1e-5
+    err = np.abs(delta - delta_ref)
+    assert np.all(err <= tol), f"{label}: delta error {float(np.max(err - tol)):.3e} over its bound"
+    return float(np.max(err))

@@ -27,8 +27,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for required in ("attn_fwd", "attn_fwd_fp8", "attn_fwd_block_masked", "attn_status_string",
-                     "attn_sync_status"):
+    for required in ("attn_fwd", "attn_fwd_fp8", "attn_fwd_block_masked", "attn_bwd",
+                     "attn_status_string", "attn_sync_status"):
         assert required in names
 
 
@@ -157,3 +157,33 @@ def test_random_block_mask_shape_and_density():
     assert abs(float(big.mean()) - 0.3) < 0.01
     assert random_block_mask(1, 256, 0.0, seed=1).sum() == 0
     assert random_block_mask(1, 256, 1.0, seed=1).all()
+
+
+def _call_bwd(q=1 << 40, k=2 << 40, v=3 << 40, out=4 << 40, dout=5 << 40, lse=6 << 40,
+              delta=7 << 40, dq=8 << 40, dk=9 << 40, dv=10 << 40, B=1, Hq=2, Hkv=2, S=300, D=128,
+              scale=0.1, causal=1):
+    lib = native.load()
+    return lib.attn_bwd(q, k, v, out, dout, lse, delta, dq, dk, dv, B, Hq, Hkv, S, D,
+                        ctypes.c_float(scale), causal, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), ATTN_ERR_INVALID_ARG),
+    (dict(dout=None), ATTN_ERR_INVALID_ARG),
+    (dict(lse=None), ATTN_ERR_INVALID_ARG),
+    (dict(delta=None), ATTN_ERR_INVALID_ARG),
+    (dict(dv=None), ATTN_ERR_INVALID_ARG),
+    (dict(S=0), ATTN_ERR_INVALID_ARG),
+    (dict(Hq=3, Hkv=2), ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), ATTN_ERR_INVALID_ARG),
+    (dict(D=96), ATTN_ERR_UNSUPPORTED),
+    (dict(dout=(5 << 40) + 8), ATTN_ERR_MISALIGNED),
+    (dict(dk=(9 << 40) + 2), ATTN_ERR_MISALIGNED),
+    (dict(delta=(7 << 40) + 2), ATTN_ERR_MISALIGNED),
+    (dict(dq=(1 << 40) + 4096), ATTN_ERR_INVALID_ARG),      # dq overlaps q
+    (dict(dk=(8 << 40) + 4096), ATTN_ERR_INVALID_ARG),      # dk overlaps dq
+    (dict(delta=(10 << 40) + 64), ATTN_ERR_INVALID_ARG),    # delta overlaps dv
+    (dict(dv=(6 << 40)), ATTN_ERR_INVALID_ARG),             # dv overlaps lse
+])
+def test_bwd_argument_errors_are_rejected_before_launch(kw, code):
+    assert _call_bwd(**kw) == code
