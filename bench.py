@@ -9,7 +9,10 @@ A step is one attn_fwd call over the whole workload (all query rows of every
 batch and head).  FLOPs per step = 4*B*Hq*S^2*D / 2 (causal).  With
 --mask-density P the step is attn_fwd_block_masked with a seeded per-head
 block mask keeping each 128 x 128 block with probability P, and the FLOPs are
-4*D per visible (query, key) pair, counted exactly.  Between timed
+4*D per visible (query, key) pair, counted exactly.  With --pass bwd the step
+is one attn_bwd call (dQ, dK, dV for a seeded upstream gradient, O and LSE
+from attn_fwd beforehand) and FLOPs = 2.5x the forward's (five products per
+tile pair instead of two: the usual convention for attention backward).  Between timed
 steps a 256 MiB buffer is written to flush L2; each step is timed with CUDA
 events on the launching stream.  Under torchrun every rank runs the same
 workload on its own GPU (independent problems, no collective on the data
@@ -35,6 +38,7 @@ sys.path.insert(0, ROOT)
 from causal_scaled_dot_gb300.workloads import BY_NAME, HEADLINE  # noqa: E402
 
 METRIC = "causal attn fwd TFLOP/s (bf16, 1xGB300) and % of dense bf16 tensor peak"
+BWD_METRIC = "causal attn bwd TFLOP/s (bf16, 1xGB300; 2.5x forward FLOPs) and % of dense bf16 tensor peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
 
@@ -231,6 +235,54 @@ class OracleTimer:
         return self.flops_of(rows) / dt / 1e12, n, dt
 
 
+class OracleBwdTimer:
+    """The fp64 oracle's gradients on a bounded sample of key/value heads (each
+    with every query head of its group); a head carries 1/(B*Hkv) of the
+    metric's FLOPs."""
+
+    def __init__(self, w):
+        import oracle
+        from causal_scaled_dot_gb300.inputs import gaussian_bf16, qkv_bf16
+        self.oracle = oracle
+        self.w = w
+        self.q, self.k, self.v = qkv_bf16(w.B, w.Hq, w.Hkv, w.S, w.D, seed=w.seed, sigma=w.sigma)
+        self.do = gaussian_bf16((w.B, w.Hq, w.S, w.D), w.seed, 3)
+        self.threads = oracle.default_threads()
+        self.total = w.B * w.Hkv
+        self.row_flops = 2.5 * w.flops / self.total  # per key/value head
+        t0 = time.perf_counter()
+        self.run(1, seed=12345)
+        self.sec_per_row = time.perf_counter() - t0
+
+    def run(self, n, seed):
+        heads = np.random.default_rng(seed).integers(0, self.total, n)
+        self.oracle.attention_bwd(self.q, self.k, self.v, self.do, self.w.scale, self.w.causal,
+                                  kv_heads=heads, nthreads=self.threads)
+        return heads
+
+    def rows_for(self, seconds):
+        return int(min(self.total, max(1, seconds / max(self.sec_per_row, 1e-9))))
+
+    def sample(self, seconds, seed):
+        n = self.rows_for(seconds)
+        t0 = time.perf_counter()
+        self.run(n, seed)
+        dt = time.perf_counter() - t0
+        return n * self.row_flops / dt / 1e12, n, dt
+
+
+def make_oracle_timer(args, w, mask=None):
+    if args.pass_ == "bwd":
+        return OracleBwdTimer(w)
+    return OracleTimer(w, fp8=args.dtype == "fp8", mask=mask)
+
+
+def metric_name(args) -> str:
+    if args.pass_ == "bwd":
+        return BWD_METRIC
+    return METRIC
+
+
 def mask_config(mask, density):
     if mask is None:
         return {}
@@ -242,7 +294,7 @@ def run_reference(args, w, rank, world):
     if rank != 0:
         return 0
     mask = workload_mask(w, args.mask_density) if args.mask_density is not None else None
-    timer = OracleTimer(w, fp8=args.dtype == "fp8", mask=mask)
+    timer = make_oracle_timer(args, w, mask)
     # The whole run (warm-up and timed steps) stays within a few minutes.
     step_s = min(args.ref_step_seconds, args.ref_total_seconds / max(1, args.steps + args.warmup))
     for i in range(args.warmup):
@@ -251,16 +303,17 @@ def run_reference(args, w, rank, world):
     secs = sum(dt for _, _, dt in samples)
     value = sum(tf * dt for tf, _, dt in samples) / secs
     rows_per_step = int(np.mean([n for _, n, _ in samples]))
-    sample = (f"{rows_per_step} random query rows of {w.name} per step "
+    what = "key/value heads (gradients)" if args.pass_ == "bwd" else "query rows"
+    sample = (f"{rows_per_step} random {what} of {w.name} per step "
               f"(of {timer.total}); fp64 C oracle, {timer.threads} threads")
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "impl": "reference", "metric": metric_name(args), "value": value, "unit": "TFLOP/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": secs / len(samples) * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": f"synthetic (seeded N(0,1) {'e4m3' if args.dtype == 'fp8' else 'bf16'})",
         "config": {"workload": w.name, **w.shape_dict, "causal": w.causal,
-                   "inputs": "e4m3" if args.dtype == "fp8" else "bf16",
+                   "inputs": "e4m3" if args.dtype == "fp8" else "bf16", "pass": args.pass_,
                    **mask_config(mask, args.mask_density)},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": timer.threads,
                          "kind": "oracle", "sample": sample},
@@ -412,6 +465,131 @@ def run_ours(args, w, rank, world, local):
     return 0
 
 
+def run_ours_bwd(args, w, rank, world, local):
+    """attn_bwd timed like the forward: inputs (Q, K, V, O, dO, LSE) resident,
+    L2 flushed between steps, CUDA events on the launching stream."""
+    import torch
+    from causal_scaled_dot_gb300 import native
+    from causal_scaled_dot_gb300.inputs import gaussian_bf16, qkv_bf16
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    native.load()
+
+    def host(bits):
+        return torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).pin_memory()
+
+    qh, kh, vh = (host(b) for b in qkv_bf16(w.B, w.Hq, w.Hkv, w.S, w.D, seed=w.seed, sigma=w.sigma))
+    doh = host(gaussian_bf16((w.B, w.Hq, w.S, w.D), w.seed, 3))
+    q, k, v, do = qh.to(dev), kh.to(dev), vh.to(dev), doh.to(dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq, w.S), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    native.attn_fwd(q, k, v, out, lse, w.B, w.Hq, w.Hkv, w.S, w.D, w.scale, w.causal, stream)
+    outh, lseh = out.cpu().pin_memory(), lse.cpu().pin_memory()
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    delta = torch.empty_like(lse)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flops = 2.5 * w.flops
+
+    def step():
+        native.attn_bwd(q, k, v, out, do, lse, delta, dq, dk, dv, w.B, w.Hq, w.Hkv, w.S, w.D,
+                        w.scale, w.causal, stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize(dev)
+    native.attn_sync_status(stream)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    launches = 0
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            starts[i].record(stream)
+            step()
+            launches += 2  # the dQ kernel and the dK/dV kernel
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - wall0
+    barrier(world)
+    native.attn_sync_status(stream)
+    ms_local = float(np.mean([a.elapsed_time(b) for a, b in zip(starts, ends)]))
+    ms = reduce_max(ms_local, world)
+    value = world * flops / (ms * 1e-3) / 1e12
+
+    # End to end: Q, K, V, O, dO, LSE from pinned host buffers, dQ, dK, dV back.
+    dqh, dkh, dvh = (torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dq, dk, dv))
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        for d, h in ((q, qh), (k, kh), (v, vh), (out, outh), (do, doh), (lse, lseh)):
+            d.copy_(h, non_blocking=True)
+        step()
+        for h, d in ((dqh, dq), (dkh, dk), (dvh, dv)):
+            h.copy_(d, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = reduce_max(e0.elapsed_time(e1) / e2e_steps, world)
+    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh, outh, doh, lseh))
+    d2h = sum(t.numel() * t.element_size() for t in (dqh, dkh, dvh))
+
+    if rank != 0:
+        return 0
+    peaks, peak_src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    achieved = flops / (ms_local * 1e-3) / 1e12
+    # algorithmic bytes: Q, K, V, O, dO and LSE read once; dQ, dK, dV written
+    # once; delta written by the first kernel and read by the second.
+    q_b = w.B * w.Hq * w.S * w.D * 2
+    kv_b = w.B * w.Hkv * w.S * w.D * 2
+    row_b = w.B * w.Hq * w.S * 4
+    io_bytes = 3 * q_b + 2 * kv_b + row_b + q_b + 2 * kv_b + 2 * row_b
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        timer = OracleBwdTimer(w)
+        tf, n, dt = timer.sample(args.cpu_seconds, seed=7)
+        cpu = {"value": tf, "unit": "TFLOP/s", "cores": timer.threads, "kind": "oracle",
+               "sample": f"gradients of {n} random key/value heads of {w.name} (of {timer.total}), "
+                         f"{dt:.1f} s; fp64 C oracle"}
+    line = {
+        "metric": BWD_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 Q, K, V, dO; no weights)",
+        "config": {"workload": w.name, **w.shape_dict, "causal": w.causal, "inputs": "bf16",
+                   "pass": "bwd", "l2": "flushed between timed steps (256 MiB write)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "pct_of_peak": 100.0 * achieved / peak,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": recorded_traffic(w.name + ":bwd"),
+                     "peak_source": f"{peak_src} bf16 dense (burst)",
+                     "kernel": "attn_bwd call (dQ kernel + dK/dV kernel)",
+                     "hbm_gbs": io_bytes / (ms_local * 1e-3) / 1e9},
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+        "wall_s_timed_region": wall,
+        "kernel_sources": kernel_source_hash(),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -421,6 +599,8 @@ def main():
     ap.add_argument("--workload", default=HEADLINE.name, choices=sorted(BY_NAME))
     ap.add_argument("--dtype", default="bf16", choices=["bf16", "fp8"],
                     help="input format: bf16 (attn_fwd) or E4M3 (attn_fwd_fp8, D = 128 only)")
+    ap.add_argument("--pass", dest="pass_", default="fwd", choices=["fwd", "bwd"],
+                    help="fwd: attn_fwd (default); bwd: attn_bwd (bf16)")
     ap.add_argument("--mask-density", type=float, default=None,
                     help="bf16 only: run attn_fwd_block_masked with a seeded per-head block mask "
                          "keeping each 128x128 block with this probability")
@@ -436,6 +616,8 @@ def main():
         ap.error("--warmup must be at least 3")
     if args.mask_density is not None and (args.dtype != "bf16" or not 0.0 <= args.mask_density <= 1.0):
         ap.error("--mask-density takes a probability in [0, 1] and bf16 inputs")
+    if args.pass_ == "bwd" and (args.dtype != "bf16" or args.mask_density is not None):
+        ap.error("--pass bwd takes bf16 inputs and no mask")
     w = BY_NAME[args.workload]
     rank, world, local = dist_init(args)
     if world != args.gpus and rank == 0:
@@ -444,7 +626,7 @@ def main():
         if args.impl == "reference":
             rc = run_reference(args, w, rank, world)
         else:
-            rc = run_ours(args, w, rank, world, local)
+            rc = (run_ours_bwd if args.pass_ == "bwd" else run_ours)(args, w, rank, world, local)
     finally:
         if world > 1:
             import torch.distributed as dist
