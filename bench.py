@@ -53,26 +53,27 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-# The sources that make the timed forward kernel and its launch.
+# The sources that make the timed kernels and their launch, per pass.
 FWD_SOURCES = ("attn_api.cu", "common.cuh", "kernel_ws.cuh", "ptx.cuh")
+BWD_SOURCES = ("attn_bwd.cu", "common.cuh", "kernel_bwd.cuh", "ptx.cuh")
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(sources=FWD_SOURCES) -> str:
     csrc = os.path.join(ROOT, "causal_scaled_dot_gb300", "csrc")
     h = hashlib.sha256()
-    for fn in FWD_SOURCES:
+    for fn in sources:
         with open(os.path.join(csrc, fn), "rb") as f:
             h.update(fn.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str):
+def recorded_traffic(workload: str, sources=FWD_SOURCES):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     the current kernel sources; otherwise None."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
-    want = kernel_source_hash()
+    want = kernel_source_hash(sources)
     for line in open(path):
         f = line.split()
         if len(f) >= 3 and not line.startswith("#") and f[0] == want and f[1] == workload:
@@ -574,7 +575,7 @@ def run_ours_bwd(args, w, rank, world, local):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "pct_of_peak": 100.0 * achieved / peak,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": recorded_traffic(w.name + ":bwd"),
+                     "frac": achieved / peak, "traffic": recorded_traffic(w.name + ":bwd", BWD_SOURCES),
                      "peak_source": f"{peak_src} bf16 dense (burst)",
                      "kernel": "attn_bwd call (dQ kernel + dK/dV kernel)",
                      "hbm_gbs": io_bytes / (ms_local * 1e-3) / 1e9},
@@ -584,7 +585,7 @@ def run_ours_bwd(args, w, rank, world, local):
         "gpu_launches": launches,
         "clocks": clk.summary(),
         "wall_s_timed_region": wall,
-        "kernel_sources": kernel_source_hash(),
+        "kernel_sources": kernel_source_hash(BWD_SOURCES),
     }
     print(json.dumps(line), flush=True)
     return 0

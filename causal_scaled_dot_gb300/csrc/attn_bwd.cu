@@ -6,6 +6,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <algorithm>
 #include <mutex>
 
 #include "../../include/attn.h"
@@ -79,10 +80,14 @@ int launch_bwd(const CUtensorMap& tq, const CUtensorMap& tdo, const CUtensorMap&
     if (dq_units > (1ll << 31) - 1) return ATTN_ERR_UNSUPPORTED;
     p.num_units = (int)dq_units;
     int grid = (int)(dq_units < sm_count ? dq_units : sm_count);
+    // About eight units per CTA per head block: nearly the balance of a single
+    // tile-major order, with half or less of the heads' operands live in L2.
+    p.head_block = std::min(p.B * p.Hq, (8 * grid + p.num_tiles - 1) / p.num_tiles);
     attn_bwd_dq_kernel<D><<<grid, DqLayout<D>::kThreads, DqLayout<D>::kDynamicSmem, stream>>>(tq, tdo, tk, tv, p);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
     p.num_units = (int)dkv_units;
     grid = (int)(dkv_units < sm_count ? dkv_units : sm_count);
+    p.head_block = std::min(p.B * p.Hkv, (8 * grid + p.num_tiles - 1) / p.num_tiles);
     attn_bwd_dkdv_kernel<D><<<grid, DkvLayout<D>::kThreads, DkvLayout<D>::kDynamicSmem, stream>>>(tq, tdo, tk, tv, p);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }

@@ -21,7 +21,8 @@
 //     delta_i = dO_i . O_i for its rows and writes it out for the second kernel.
 //
 //  attn_bwd_dkdv_kernel unit = (b, hkv, key tile j), over the query tiles
-//     i >= j of every query head of the group.  Tensor memory: S^T [0,128),
+//     i >= j of every query head of the group (Q_i and dO_i stream through a
+//     ring of single-tile slots).  Tensor memory: S^T [0,128),
 //     dP^T [128,256), dV [256,256+D), dK [256+D,256+2D) -- all 512 columns at
 //     D = 128.  Per query tile: S^T = K Q_i^T and dP^T = V dO_i^T, then
 //     dV += P^T dO_i and dK += dS^T Q_i with P^T and dS^T read from tensor
@@ -33,8 +34,9 @@
 // thread per tensor-memory lane (a row of S, or of S^T), warpgroup w on
 // columns [64w, 64w+64).  Each writes its bf16 P or dS over the first half of
 // its own fp32 columns, so the tensor core reads 64 columns of packed pairs
-// per warpgroup.  In the dK/dV kernel warps 2-3 copy the per-query LSE and
-// delta of each query tile into shared memory.
+// per warpgroup.  Warps 2-3 stage per-query rows in shared memory ahead of
+// use: in the dQ kernel LSE and delta_i = dO_i . O_i (computed there from
+// global O and dO), in the dK/dV kernel LSE and delta of each query tile.
 //
 // Every wait is bounded (ptx::mbar_wait); after a timeout each role returns,
 // the producer first letting its issued copies land, the MMA issuer its
@@ -65,7 +67,23 @@ struct BwdParams {
     unsigned int* status;
     unsigned long long wait_limit_ns;
     int num_units;
+    int head_block;  // heads worked on together (see split_unit)
 };
+
+// Units are (head, tile) pairs.  Heads are taken `head_block` at a time, about
+// one tile of each head per CTA, so the CTAs running together share the
+// streamed operands of a few heads in L2; within a block the tile index `rank`
+// runs from the heaviest tile down, the head index fastest.
+__device__ __forceinline__ void split_unit(int u, int heads, int tiles, int head_block, int& head,
+                                           int& rank) {
+    const int per_block = head_block * tiles;
+    const int blk = u / per_block;
+    const int within = u - blk * per_block;
+    const int first = blk * head_block;
+    const int hb = min(head_block, heads - first);
+    rank = within / hb;
+    head = first + (within - rank * hb);
+}
 
 // The unit this CTA runs in round r: boustrophedon over the CTAs, so sorted
 // unit costs (heaviest first) spread evenly.
@@ -73,6 +91,15 @@ __device__ __forceinline__ int bwd_unit_of_round(int r) {
     const int G = gridDim.x, c = blockIdx.x;
     return r * G + ((r & 1) ? (G - 1 - c) : c);
 }
+
+// The dQ kernel's producer walks a second position kPrefetch key tiles ahead
+// of its loads (across unit boundaries) and prefetches the tiles there into
+// L2, so that the loads themselves mostly hit L2.  (The same in the dK/dV
+// kernel measured slower.)
+constexpr int kPrefetch = 3;
+struct StreamPos {
+    int rnd, u, i;  // round, unit, step within the unit
+};
 
 // ====================================================================== dQ
 template <int D>
@@ -84,13 +111,20 @@ struct DqLayout {
     static constexpr uint32_t kTileBytes = kTile * D * 2;
     static constexpr int kChunks = D / 64;
     static constexpr uint32_t kChunkBytes = kTile * 128;
-    static constexpr int kStages = (kTileBytes == 32768) ? 4 : 8;  // K/V ring, one tile per slot
+    // K/V ring, one tile per slot.  A fifth slot at D = 128 measured slower
+    // (it leaves L1 too small for the row loads).
+    static constexpr int kStages = (kTileBytes == 32768) ? 4 : 8;
+    static constexpr int kStatStages = 2;                  // per-row LSE / delta of a unit
+    static constexpr uint32_t kStatBytes = 2 * kTile * 4;  // stage s: lse2[128], delta[128]
     static constexpr uint32_t kQ = 0;
     static constexpr uint32_t kDO = kTileBytes;
     static constexpr uint32_t kRing = 2 * kTileBytes;
-    static constexpr uint32_t kBars = kRing + kStages * kTileBytes;
+    static constexpr uint32_t kStat = kRing + kStages * kTileBytes;
+    static constexpr uint32_t kBars = kStat + kStatStages * kStatBytes;
     static constexpr int kQFull = 0, kQEmpty = 1, kSFull = 2, kDPFull = 3, kSFree = 4, kDSFull = 5,
-                         kDQFull = 6, kKVFull = 7, kKVEmpty = 7 + kStages, kDrain = 7 + 2 * kStages;
+                         kDQFull = 6, kKVFull = 7, kKVEmpty = 7 + kStages, kStatFull = 7 + 2 * kStages,
+                         kStatEmpty = 7 + 2 * kStages + kStatStages,
+                         kDrain = 7 + 2 * kStages + 2 * kStatStages;
     static constexpr int kNumBars = kDrain + 1;
     static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8;
     static constexpr uint32_t kAbort = kTmemSlot + 4;
@@ -102,10 +136,10 @@ struct DqUnit {
     int bh, kv_bh, qt, n;
 };
 __device__ __forceinline__ DqUnit dq_decode(int u, const BwdParams& p) {
-    const int BH = p.B * p.Hq;
     DqUnit w;
-    w.qt = p.num_tiles - 1 - u / BH;  // heaviest (last) query tiles first
-    w.bh = u - (u / BH) * BH;
+    int rank;
+    split_unit(u, p.B * p.Hq, p.num_tiles, p.head_block, w.bh, rank);
+    w.qt = p.num_tiles - 1 - rank;  // heaviest (last) query tiles first
     const int b = w.bh / p.Hq, hq = w.bh - b * p.Hq;
     w.kv_bh = b * p.Hkv + hq / p.group;
     w.n = p.causal ? w.qt + 1 : p.num_tiles;
@@ -128,6 +162,29 @@ __device__ void dq_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_do,
     // Copies issued and possibly not landed yet, for the drain after an abort.
     bool pend_q = false;
     uint32_t pend_q_par = 0, pend_kv = 0, pend_kv_par = 0;
+    StreamPos ahead{0, bwd_unit_of_round(0), 0};
+    auto advance = [&](StreamPos& a) {
+        if (a.u >= p.num_units) return;
+        if (++a.i >= dq_decode(a.u, p).n) {
+            a.i = 0;
+            a.u = bwd_unit_of_round(++a.rnd);
+        }
+    };
+    auto prefetch = [&](const StreamPos& a) {  // K_i, V_i (and Q, dO at a unit's start)
+        if (a.u >= p.num_units) return;
+        const DqUnit x = dq_decode(a.u, p);
+        if (a.i == 0) {
+            for (int c = 0; c < L::kChunks; ++c) {
+                ptx::tma_prefetch_l2_3d(tm_q, c * 64, x.qt * kTile, x.bh);
+                ptx::tma_prefetch_l2_3d(tm_do, c * 64, x.qt * kTile, x.bh);
+            }
+        }
+        for (int c = 0; c < L::kChunks; ++c) {
+            ptx::tma_prefetch_l2_3d(tm_k, c * 64, a.i * kTile, x.kv_bh);
+            ptx::tma_prefetch_l2_3d(tm_v, c * 64, a.i * kTile, x.kv_bh);
+        }
+    };
+    for (int k = 0; k < kPrefetch; ++k) advance(ahead);
     for (int rnd = 0, u = bwd_unit_of_round(0); u < p.num_units; u = bwd_unit_of_round(++rnd)) {
         const DqUnit w = dq_decode(u, p);
         if (!ptx::mbar_wait(dq_bar<D>(base, L::kQEmpty), qe_phase ^ 1u, abort_flag, p.status, lim))
@@ -145,6 +202,8 @@ __device__ void dq_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_do,
             qe_phase ^= 1u;
         }
         for (int j = 0; j < w.n; ++j) {
+            prefetch(ahead);
+            advance(ahead);
 #pragma unroll
             for (int t = 0; t < 2; ++t) {  // K_j, then V_j
                 if (!ptx::mbar_wait(dq_bar<D>(base, L::kKVEmpty + slot), ring_phase ^ 1u, abort_flag,
@@ -223,6 +282,9 @@ __device__ void dq_mma_role(const BwdParams& p, uint32_t base, uint32_t tmem, vo
         product(tmem + 128u, base + L::kDO, slot_addr(vs));  // dP = dO V_0^T
         ptx::mma_commit(dq_bar<D>(base, L::kDPFull));
         ptx::mma_commit(dq_bar<D>(base, L::kKVEmpty + vs));
+        // Q and dO are read only by S and dP: free them for the next unit as
+        // soon as the last of those has been issued.
+        if (w.n == 1) ptx::mma_commit(dq_bar<D>(base, L::kQEmpty));
         for (int j = 0; j < w.n; ++j) {
             // S_j has been read: the next S may overwrite it.
             if (!(ok = wait_bar(L::kSFree, sfree_phase))) break;
@@ -244,12 +306,12 @@ __device__ void dq_mma_role(const BwdParams& p, uint32_t base, uint32_t tmem, vo
                 product(tmem + 128u, base + L::kDO, slot_addr(vs));
                 ptx::mma_commit(dq_bar<D>(base, L::kDPFull));
                 ptx::mma_commit(dq_bar<D>(base, L::kKVEmpty + vs));
+                if (j + 2 == w.n) ptx::mma_commit(dq_bar<D>(base, L::kQEmpty));
             }
             ks = ks_next;
         }
         if (!ok) break;
         ptx::mma_commit(dq_bar<D>(base, L::kDQFull));
-        ptx::mma_commit(dq_bar<D>(base, L::kQEmpty));
     }
     ptx::mma_commit(dq_bar<D>(base, L::kDrain));
     ptx::drain_wait(dq_bar<D>(base, L::kDrain), 0u, lim);
@@ -276,9 +338,50 @@ __device__ __forceinline__ float row_delta(const __nv_bfloat16* o, const __nv_bf
     return acc0 + acc1;
 }
 
+// Warps 2-3: for each unit, the LSE (as log2) and delta_i = dO_i . O_i of its
+// 128 rows into a shared-memory stage (delta also to global memory for the
+// dK/dV kernel), ahead of the element-wise warps.
 template <int D>
-__device__ void dq_work_role(const BwdParams& p, uint32_t base, uint32_t tmem, int wg,
-                             volatile int* abort_flag) {
+__device__ void dq_stat_role(const BwdParams& p, uint32_t base, uint8_t* smem, volatile int* abort_flag) {
+    using L = DqLayout<D>;
+    const int tid = threadIdx.x - 64;  // 0..63
+    const uint64_t lim = p.wait_limit_ns;
+    uint32_t ring_phase = 0;
+    int st = 0;
+    for (int rnd = 0, u = bwd_unit_of_round(0); u < p.num_units; u = bwd_unit_of_round(++rnd)) {
+        const DqUnit w = dq_decode(u, p);
+        float l2[2], dl[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int row = w.qt * kTile + tid + 64 * h;
+            l2[h] = 0.f;
+            dl[h] = 0.f;
+            if (row < p.S) {
+                const size_t ro = (size_t)w.bh * p.S + row;
+                l2[h] = __ldg(p.lse + ro) * kLog2e;
+                dl[h] = row_delta<D>(p.out + ro * D, p.dout + ro * D);
+                p.delta[ro] = dl[h];
+            }
+        }
+        if (!ptx::mbar_wait(dq_bar<D>(base, L::kStatEmpty + st), ring_phase ^ 1u, abort_flag, p.status, lim))
+            return;
+        float* rows = reinterpret_cast<float*>(smem + L::kStat + (uint32_t)st * L::kStatBytes);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            rows[tid + 64 * h] = l2[h];
+            rows[kTile + tid + 64 * h] = dl[h];
+        }
+        ptx::mbar_arrive(dq_bar<D>(base, L::kStatFull + st));
+        if (++st == L::kStatStages) {
+            st = 0;
+            ring_phase ^= 1u;
+        }
+    }
+}
+
+template <int D>
+__device__ void dq_work_role(const BwdParams& p, uint32_t base, const uint8_t* smem, uint32_t tmem,
+                             int wg, volatile int* abort_flag) {
     using L = DqLayout<D>;
     const int warp = threadIdx.x >> 5;
     const int r = (warp & 3) * 32 + (threadIdx.x & 31);  // row of the tile = TMEM lane
@@ -288,18 +391,27 @@ __device__ void dq_work_role(const BwdParams& p, uint32_t base, uint32_t tmem, i
     const uint32_t tDQ = tmem + lane_off + 256u + (uint32_t)(wg * (D / 2));
     const float sl2 = p.scale_log2;
     const uint64_t lim = p.wait_limit_ns;
-    uint32_t s_phase = 0, dp_phase = 0, dq_phase = 0;
+    uint32_t s_phase = 0, dp_phase = 0, dq_phase = 0, stat_phase = 0;
+    int st = 0;
 
     for (int rnd = 0, u = bwd_unit_of_round(0); u < p.num_units; u = bwd_unit_of_round(++rnd)) {
         const DqUnit w = dq_decode(u, p);
         const int row = w.qt * kTile + r;
         const bool valid = row < p.S;
         const size_t ro = (size_t)w.bh * p.S + row;
-        float lse2 = 0.f, delta = 0.f;
-        if (valid) {
-            lse2 = __ldg(p.lse + ro) * kLog2e;
-            delta = row_delta<D>(p.out + ro * D, p.dout + ro * D);
-            if (wg == 0) p.delta[ro] = delta;
+        // This row's LSE (log2) and delta from the stat warps.
+        {
+            const bool ok = ptx::mbar_wait(dq_bar<D>(base, L::kStatFull + st), stat_phase, abort_flag,
+                                           p.status, lim);
+            if (!__all_sync(0xffffffffu, ok)) return;
+        }
+        const float* rows = reinterpret_cast<const float*>(smem + L::kStat + (uint32_t)st * L::kStatBytes);
+        const float lse2 = rows[r], delta = rows[kTile + r];
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(dq_bar<D>(base, L::kStatEmpty + st));
+        if (++st == L::kStatStages) {
+            st = 0;
+            stat_phase ^= 1u;
         }
         for (int j = 0; j < w.n; ++j) {
             bool ok = ptx::mbar_wait(dq_bar<D>(base, L::kSFull), s_phase, abort_flag, p.status, lim);
@@ -415,6 +527,10 @@ __global__ void __launch_bounds__(DqLayout<D>::kThreads, 1)
             ptx::mbar_init(dq_bar<D>(base, L::kKVFull + s), 1);
             ptx::mbar_init(dq_bar<D>(base, L::kKVEmpty + s), 1);
         }
+        for (int s = 0; s < L::kStatStages; ++s) {
+            ptx::mbar_init(dq_bar<D>(base, L::kStatFull + s), 64);  // one per stat thread
+            ptx::mbar_init(dq_bar<D>(base, L::kStatEmpty + s), 8);  // one per element-wise warp
+        }
         ptx::mbar_init(dq_bar<D>(base, L::kDrain), 1);
         *abort_flag = 0;
         ptx::fence_barrier_init();
@@ -436,9 +552,10 @@ __global__ void __launch_bounds__(DqLayout<D>::kThreads, 1)
         ptx::regs_dec<L::kRegsSmall>();
         if (warp == 0 && lane == 0) dq_load_role<D>(&tm_q, &tm_do, &tm_k, &tm_v, p, base, abort_flag);
         if (warp == 1 && lane == 0) dq_mma_role<D>(p, base, tmem, abort_flag);
+        if (warp >= 2) dq_stat_role<D>(p, base, smem, abort_flag);
     } else {
         ptx::regs_inc<L::kRegsWork>();
-        dq_work_role<D>(p, base, tmem, (warp - 4) >> 2, abort_flag);
+        dq_work_role<D>(p, base, smem, tmem, (warp - 4) >> 2, abort_flag);
     }
 
     ptx::tc_fence_before();
@@ -459,16 +576,21 @@ struct DkvLayout {
     static constexpr uint32_t kTileBytes = kTile * D * 2;
     static constexpr int kChunks = D / 64;
     static constexpr uint32_t kChunkBytes = kTile * 128;
-    static constexpr int kStages = (kTileBytes == 32768) ? 2 : 4;  // (Q_i, dO_i) pairs
+    static constexpr int kStatStages = 4;                  // per-query LSE / delta rows
+    static constexpr uint32_t kStatBytes = 2 * kTile * 4;  // stage s: lse2[128], delta[128]
+    // Q_i, dO_i ring, one tile per slot: as many slots as fit (5 at D = 128, 12 at D = 64).
+    static constexpr int kStages =
+        (227 * 1024 - 2 * (int)kTileBytes - kStatStages * (int)kStatBytes - 2048) / (int)kTileBytes > 12
+            ? 12
+            : (227 * 1024 - 2 * (int)kTileBytes - kStatStages * (int)kStatBytes - 2048) / (int)kTileBytes;
     static constexpr uint32_t kK = 0;
     static constexpr uint32_t kV = kTileBytes;
-    static constexpr uint32_t kStage0 = 2 * kTileBytes;              // stage s: Q at +0, dO at +kTileBytes
-    static constexpr uint32_t kStat = kStage0 + kStages * 2 * kTileBytes;  // stage s: lse2[128], delta[128]
-    static constexpr uint32_t kStatBytes = 2 * kTile * 4;
-    static constexpr uint32_t kBars = kStat + kStages * kStatBytes;
+    static constexpr uint32_t kRing = 2 * kTileBytes;
+    static constexpr uint32_t kStat = kRing + kStages * kTileBytes;
+    static constexpr uint32_t kBars = kStat + kStatStages * kStatBytes;
     static constexpr int kKVFull = 0, kKVEmpty = 1, kSFull = 2, kDPFull = 3, kPFull = 4, kDSFull = 5,
                          kAccFull = 6, kStFull = 7, kStEmpty = 7 + kStages, kStatFull = 7 + 2 * kStages,
-                         kStatEmpty = 7 + 3 * kStages, kDrain = 7 + 4 * kStages;
+                         kStatEmpty = 7 + 2 * kStages + kStatStages, kDrain = 7 + 2 * kStages + 2 * kStatStages;
     static constexpr int kNumBars = kDrain + 1;
     static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8;
     static constexpr uint32_t kAbort = kTmemSlot + 4;
@@ -481,10 +603,8 @@ struct DkvUnit {
     int q0, nq, n;          // query tiles q0 .. q0+nq-1 of each of the group's heads; n = group * nq
 };
 __device__ __forceinline__ DkvUnit dkv_decode(int u, const BwdParams& p) {
-    const int BH = p.B * p.Hkv;
     DkvUnit w;
-    w.kt = u / BH;  // heaviest (first) key tiles first
-    w.kv_bh = u - w.kt * BH;
+    split_unit(u, p.B * p.Hkv, p.num_tiles, p.head_block, w.kv_bh, w.kt);  // heaviest (first) key tiles first
     w.b = w.kv_bh / p.Hkv;
     w.hkv = w.kv_bh - w.b * p.Hkv;
     w.q0 = p.causal ? w.kt : 0;
@@ -511,7 +631,7 @@ __device__ void dkv_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_do,
     using L = DkvLayout<D>;
     const uint64_t lim = p.wait_limit_ns;
     uint32_t kve_phase = 0, ring_phase = 0;
-    int st = 0;
+    int slot = 0;
     bool pend_kv = false;
     uint32_t pend_kv_par = 0, pend_st = 0, pend_st_par = 0;
     for (int rnd = 0, u = bwd_unit_of_round(0); u < p.num_units; u = bwd_unit_of_round(++rnd)) {
@@ -533,21 +653,24 @@ __device__ void dkv_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_do,
         for (int t = 0; t < w.n; ++t) {
             int bh, qt;
             dkv_iter(w, p, t, bh, qt);
-            if (!ptx::mbar_wait(dkv_bar<D>(base, L::kStEmpty + st), ring_phase ^ 1u, abort_flag, p.status, lim))
-                goto drain;
-            const uint32_t full = dkv_bar<D>(base, L::kStFull + st);
-            ptx::mbar_arrive_expect_tx(full, 2 * L::kTileBytes);
-            const uint32_t dst = base + L::kStage0 + (uint32_t)st * 2 * L::kTileBytes;
 #pragma unroll
-            for (int c = 0; c < L::kChunks; ++c) {
-                ptx::tma_load_3d(dst + c * L::kChunkBytes, tm_q, full, c * 64, qt * kTile, bh);
-                ptx::tma_load_3d(dst + L::kTileBytes + c * L::kChunkBytes, tm_do, full, c * 64, qt * kTile, bh);
-            }
-            pend_st |= 1u << st;
-            pend_st_par = (pend_st_par & ~(1u << st)) | (ring_phase << st);
-            if (++st == L::kStages) {
-                st = 0;
-                ring_phase ^= 1u;
+            for (int x = 0; x < 2; ++x) {  // Q_i, then dO_i
+                if (!ptx::mbar_wait(dkv_bar<D>(base, L::kStEmpty + slot), ring_phase ^ 1u, abort_flag,
+                                    p.status, lim))
+                    goto drain;
+                const uint32_t full = dkv_bar<D>(base, L::kStFull + slot);
+                ptx::mbar_arrive_expect_tx(full, L::kTileBytes);
+                const CUtensorMap* map = x == 0 ? tm_q : tm_do;
+#pragma unroll
+                for (int c = 0; c < L::kChunks; ++c)
+                    ptx::tma_load_3d(base + L::kRing + (uint32_t)slot * L::kTileBytes + c * L::kChunkBytes,
+                                     map, full, c * 64, qt * kTile, bh);
+                pend_st |= 1u << slot;
+                pend_st_par = (pend_st_par & ~(1u << slot)) | (ring_phase << slot);
+                if (++slot == L::kStages) {
+                    slot = 0;
+                    ring_phase ^= 1u;
+                }
             }
         }
     }
@@ -591,7 +714,7 @@ __device__ void dkv_stat_role(const BwdParams& p, uint32_t base, uint8_t* smem, 
                 rows[kTile + tid + 64 * h] = dl[h];
             }
             ptx::mbar_arrive(dkv_bar<D>(base, L::kStatFull + st));
-            if (++st == L::kStages) {
+            if (++st == L::kStatStages) {
                 st = 0;
                 ring_phase ^= 1u;
             }
@@ -606,7 +729,7 @@ __device__ void dkv_mma_role(const BwdParams& p, uint32_t base, uint32_t tmem, v
     constexpr uint32_t kIdescA = ptx::idesc_bf16_f32(kTile, D, true);       // dV, dK: N = D, MN-major
     const uint64_t lim = p.wait_limit_ns;
     uint32_t kvf_phase = 0, p_phase = 0, ds_phase = 0, ring_phase = 0;
-    int st = 0;
+    int slot = 0;
 
     auto wait_bar = [&](int bar, uint32_t& phase) -> bool {
         if (!ptx::mbar_wait(dkv_bar<D>(base, bar), phase, abort_flag, p.status, lim)) return false;
@@ -614,18 +737,18 @@ __device__ void dkv_mma_role(const BwdParams& p, uint32_t base, uint32_t tmem, v
         ptx::tc_fence_after();
         return true;
     };
-    auto wait_stage = [&](int& got) -> bool {
-        if (!ptx::mbar_wait(dkv_bar<D>(base, L::kStFull + st), ring_phase, abort_flag, p.status, lim))
+    auto wait_ring = [&](int& got) -> bool {
+        if (!ptx::mbar_wait(dkv_bar<D>(base, L::kStFull + slot), ring_phase, abort_flag, p.status, lim))
             return false;
-        got = st;
-        if (++st == L::kStages) {
-            st = 0;
+        got = slot;
+        if (++slot == L::kStages) {
+            slot = 0;
             ring_phase ^= 1u;
         }
         ptx::tc_fence_after();
         return true;
     };
-    auto q_addr = [&](int s) { return base + L::kStage0 + (uint32_t)s * 2 * L::kTileBytes; };
+    auto slot_addr = [&](int s) { return base + L::kRing + (uint32_t)s * L::kTileBytes; };
     auto product = [&](uint32_t d, uint32_t a_smem, uint32_t b_smem) {
         const uint64_t a = ptx::sdesc_sw128(a_smem, 16, 1024);
         const uint64_t b = ptx::sdesc_sw128(b_smem, 16, 1024);
@@ -640,39 +763,46 @@ __device__ void dkv_mma_role(const BwdParams& p, uint32_t base, uint32_t tmem, v
     for (int rnd = 0, u = bwd_unit_of_round(0); u < p.num_units && ok; u = bwd_unit_of_round(++rnd)) {
         const DkvUnit w = dkv_decode(u, p);
         if (!wait_bar(L::kKVFull, kvf_phase)) break;
-        int cur, nxt = -1;
-        if (!wait_stage(cur)) break;
-        product(tmem, base + L::kK, q_addr(cur));  // S^T = K Q^T
+        int qs, ds, qs_next = -1, ds_next = -1;
+        if (!wait_ring(qs)) break;
+        product(tmem, base + L::kK, slot_addr(qs));  // S^T = K Q^T
         ptx::mma_commit(dkv_bar<D>(base, L::kSFull));
-        product(tmem + 128u, base + L::kV, q_addr(cur) + L::kTileBytes);  // dP^T = V dO^T
+        if (!wait_ring(ds)) break;
+        product(tmem + 128u, base + L::kV, slot_addr(ds));  // dP^T = V dO^T
         ptx::mma_commit(dkv_bar<D>(base, L::kDPFull));
+        // K and V are read only by S^T and dP^T: free them for the next unit
+        // as soon as the last of those has been issued.
+        if (w.n == 1) ptx::mma_commit(dkv_bar<D>(base, L::kKVEmpty));
         for (int t = 0; t < w.n; ++t) {
             // dV += P^T dO: P^T of queries 0-63 in columns [0,32), 64-127 in
             // [64,96); dO as an MN-major operand, queries 64-127 8 KB further in.
             if (!(ok = wait_bar(L::kPFull, p_phase))) break;
-            const uint64_t dod = ptx::sdesc_sw128(q_addr(cur) + L::kTileBytes, L::kChunkBytes, 1024);
+            const uint64_t dod = ptx::sdesc_sw128(slot_addr(ds), L::kChunkBytes, 1024);
             ptx::mma_ts_k64(tDV, tmem, dod, kIdescA, t > 0 ? 1u : 0u);
             ptx::mma_ts_k64(tDV, tmem + 64u, dod + 512u, kIdescA, 1u);
+            ptx::mma_commit(dkv_bar<D>(base, L::kStEmpty + ds));
             if (t + 1 < w.n) {
-                if (!(ok = wait_stage(nxt))) break;
-                product(tmem, base + L::kK, q_addr(nxt));
+                if (!(ok = wait_ring(qs_next))) break;
+                product(tmem, base + L::kK, slot_addr(qs_next));
                 ptx::mma_commit(dkv_bar<D>(base, L::kSFull));
             }
             // dK += dS^T Q: dS^T in columns [128,160) and [192,224).
             if (!(ok = wait_bar(L::kDSFull, ds_phase))) break;
-            const uint64_t qd = ptx::sdesc_sw128(q_addr(cur), L::kChunkBytes, 1024);
+            const uint64_t qd = ptx::sdesc_sw128(slot_addr(qs), L::kChunkBytes, 1024);
             ptx::mma_ts_k64(tDK, tmem + 128u, qd, kIdescA, t > 0 ? 1u : 0u);
             ptx::mma_ts_k64(tDK, tmem + 192u, qd + 512u, kIdescA, 1u);
-            ptx::mma_commit(dkv_bar<D>(base, L::kStEmpty + cur));
+            ptx::mma_commit(dkv_bar<D>(base, L::kStEmpty + qs));
             if (t + 1 < w.n) {
-                product(tmem + 128u, base + L::kV, q_addr(nxt) + L::kTileBytes);
+                if (!(ok = wait_ring(ds_next))) break;
+                product(tmem + 128u, base + L::kV, slot_addr(ds_next));
                 ptx::mma_commit(dkv_bar<D>(base, L::kDPFull));
+                if (t + 2 == w.n) ptx::mma_commit(dkv_bar<D>(base, L::kKVEmpty));
             }
-            cur = nxt;
+            qs = qs_next;
+            ds = ds_next;
         }
         if (!ok) break;
         ptx::mma_commit(dkv_bar<D>(base, L::kAccFull));
-        ptx::mma_commit(dkv_bar<D>(base, L::kKVEmpty));
     }
     ptx::mma_commit(dkv_bar<D>(base, L::kDrain));
     ptx::drain_wait(dkv_bar<D>(base, L::kDrain), 0u, lim);
@@ -762,7 +892,7 @@ __device__ void dkv_work_role(const BwdParams& p, uint32_t base, const uint8_t* 
                 ptx::mbar_arrive(dkv_bar<D>(base, L::kDSFull));
                 ptx::mbar_arrive(dkv_bar<D>(base, L::kStatEmpty + st));
             }
-            if (++st == L::kStages) {
+            if (++st == L::kStatStages) {
                 st = 0;
                 ring_phase ^= 1u;
             }
@@ -824,6 +954,8 @@ __global__ void __launch_bounds__(DkvLayout<D>::kThreads, 1)
         for (int s = 0; s < L::kStages; ++s) {
             ptx::mbar_init(dkv_bar<D>(base, L::kStFull + s), 1);
             ptx::mbar_init(dkv_bar<D>(base, L::kStEmpty + s), 1);
+        }
+        for (int s = 0; s < L::kStatStages; ++s) {
             ptx::mbar_init(dkv_bar<D>(base, L::kStatFull + s), 64);  // one per loader thread
             ptx::mbar_init(dkv_bar<D>(base, L::kStatEmpty + s), 8);  // one per element-wise warp
         }
