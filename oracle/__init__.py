@@ -68,6 +68,13 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     f = lib.oracle_attn_rows_f64
     f.restype = ci
     f.argtypes = [vp, vp, vp, ci, ci, ci, ci, ci, cf, ci, vp, ctypes.c_int64, vp, vp, ci]
+    f = lib.oracle_attn_rows_dropout
+    f.restype = ci
+    f.argtypes = [vp, vp, vp, ci, ci, ci, ci, ci, cf, ci, ci, ctypes.c_uint64, ctypes.c_uint64, vp,
+                  ctypes.c_int64, vp, vp, ci]
+    f = lib.oracle_philox4x64
+    f.restype = None
+    f.argtypes = [vp, vp, vp]
     f = lib.oracle_attn_bwd
     f.restype = ci
     f.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, vp, ctypes.c_int64, vp, vp, vp,
@@ -268,3 +275,33 @@ def attention_bwd(q, k, v, dout, scale: float, causal: bool = True, kv_heads=Non
     if rc != 0:
         raise ValueError("oracle_attn_bwd rejected its arguments")
     return dq, dk, dv, delta
+
+
+def attention_dropout(q_bits, k_bits, v_bits, scale: float, p8: int, seed: int, offset: int,
+                      causal: bool = True, rows=None, nthreads: int | None = None,
+                      lib: ctypes.CDLL | None = None):
+    """``attention`` with dropout of the weights: each dropped with probability
+    p8/256 by Philox4x64-10 (key {seed, offset}), kept ones scaled by 256/(256-p8).
+    The LSE is that of the undropped softmax."""
+    lib = lib or load()
+    q, k, v = (_as_bits(x, n) for x, n in ((q_bits, "q"), (k_bits, "k"), (v_bits, "v")))
+    B, Hq, Hkv, S, D = _shapes(q, k, v)
+    rows_arr, nrows, out, lse = _outputs(B, Hq, S, D, rows)
+    rc = lib.oracle_attn_rows_dropout(
+        q.ctypes.data, k.ctypes.data, v.ctypes.data, B, Hq, Hkv, S, D, ctypes.c_float(scale),
+        1 if causal else 0, int(p8), ctypes.c_uint64(seed), ctypes.c_uint64(offset),
+        None if rows_arr is None else rows_arr.ctypes.data, nrows, out.ctypes.data,
+        lse.ctypes.data, nthreads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle_attn_rows_dropout rejected its arguments")
+    return out, lse
+
+
+def philox4x64(ctr, key, lib: ctypes.CDLL | None = None) -> np.ndarray:
+    """The oracle's Philox4x64-10 block for one counter (4 x uint64) and key (2 x uint64)."""
+    lib = lib or load()
+    c = np.ascontiguousarray(ctr, dtype=np.uint64)
+    k = np.ascontiguousarray(key, dtype=np.uint64)
+    out = np.empty(4, dtype=np.uint64)
+    lib.oracle_philox4x64(c.ctypes.data, k.ctypes.data, out.ctypes.data)
+    return out

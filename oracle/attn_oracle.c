@@ -86,6 +86,8 @@ typedef struct {
     int causal;
     const uint8_t *block_mask; /* NULL, or [mask_heads][nt][nt], nt = ceil(S / 128) */
     int mask_heads;            /* 1 (shared by all heads) or Hq */
+    int dropout_p8;            /* 0: no dropout; else weights dropped with probability p8 / 256 */
+    uint64_t dropout_key[2];   /* Philox key: {seed, offset} */
     const int64_t *rows; /* flat query-row ids, or NULL for all rows */
     int64_t nrows;
     double *out; /* [nrows, D] */
@@ -159,6 +161,49 @@ static void attn_weights(const oracle_job_t *J, int64_t r, double *s, double *ls
     *lse_out = m + log(l);
 }
 
+/*
+ * Philox4x64-10 (Salmon, Moraes, Dror and Shaw, "Parallel random numbers: as
+ * easy as 1, 2, 3", SC 2011): ten rounds of
+ *   (x0, x1, x2, x3) <- (hi(M1 x2) ^ x1 ^ k0, lo(M1 x2), hi(M0 x0) ^ x3 ^ k1, lo(M0 x0))
+ * with the key bumped by the Weyl constants after every round.
+ */
+static void philox4x64_10(const uint64_t ctr[4], const uint64_t key[2], uint64_t out[4]) {
+    const uint64_t M0 = 0xD2E7470EE14C6C93ull, M1 = 0xCA5A826395121157ull;
+    const uint64_t W0 = 0x9E3779B97F4A7C15ull, W1 = 0xBB67AE8584CAA73Bull;
+    uint64_t x0 = ctr[0], x1 = ctr[1], x2 = ctr[2], x3 = ctr[3], k0 = key[0], k1 = key[1];
+    for (int r = 0; r < 10; ++r) {
+        const unsigned __int128 p0 = (unsigned __int128)M0 * x0;
+        const unsigned __int128 p1 = (unsigned __int128)M1 * x2;
+        const uint64_t hi0 = (uint64_t)(p0 >> 64), lo0 = (uint64_t)p0;
+        const uint64_t hi1 = (uint64_t)(p1 >> 64), lo1 = (uint64_t)p1;
+        x0 = hi1 ^ x1 ^ k0;
+        x1 = lo1;
+        x2 = hi0 ^ x3 ^ k1;
+        x3 = lo0;
+        k0 += W0;
+        k1 += W1;
+    }
+    out[0] = x0; out[1] = x1; out[2] = x2; out[3] = x3;
+}
+
+/*
+ * Dropout of the attention weights (the fused dropout the ai-manual.ru
+ * article names in section 6, "Dropout"; the weights are dropped after the
+ * softmax and the kept ones scaled by 1 / (1 - p), as in
+ * scaled_dot_product_attention).  The random draw is Philox4x64-10 with
+ * counter {j / 32, i, b*Hq + hq, 0} and key {seed, offset}: its 32 output
+ * bytes (word 0 first, each word little-endian) give keys j = 32*(j/32) + 0..31
+ * of query row i.  Key j is kept when its byte is >= p8 (probability
+ * 1 - p8/256) and then scaled by 256 / (256 - p8).
+ */
+static int dropout_keeps(const oracle_job_t *J, int64_t bh, int64_t i, int64_t j) {
+    const uint64_t ctr[4] = {(uint64_t)(j / 32), (uint64_t)i, (uint64_t)bh, 0};
+    uint64_t out[4];
+    philox4x64_10(ctr, J->dropout_key, out);
+    const int byte = (int)((out[(j % 32) / 8] >> (8 * (j % 8))) & 0xFF);
+    return byte >= J->dropout_p8;
+}
+
 /* One query row of the forward pass: steps 1-4, then step 5. */
 static void oracle_one_row(const oracle_job_t *J, int64_t r, double *s,
                            double *o_row, double *lse_out) {
@@ -167,8 +212,15 @@ static void oracle_one_row(const oracle_job_t *J, int64_t r, double *s,
     const int64_t b = (r / S) / J->Hq;
     const int64_t hkv = ((r / S) % J->Hq) / (J->Hq / J->Hkv);
     const int64_t vb = ((b * J->Hkv + hkv) * S) * (int64_t)D;  /* v_0 of this head */
-    (void)i;
     attn_weights(J, r, s, lse_out);
+    /* Optional dropout of the weights (the LSE is that of the kept softmax). */
+    if (J->dropout_p8 > 0) {
+        const double keep_scale = 256.0 / (256.0 - (double)J->dropout_p8);
+        for (int64_t j = 0; j < S; ++j) {
+            if (s[j] == 0.0) continue;
+            s[j] = dropout_keeps(J, r / S, i, j) ? s[j] * keep_scale : 0.0;
+        }
+    }
     /* Step 5: out_d = sum_j attn_j * v_jd (every weight 0 when all keys are masked). */
     for (int d = 0; d < D; ++d) o_row[d] = 0.0;
     for (int64_t j = 0; j < S; ++j) {
@@ -193,10 +245,11 @@ static void *oracle_worker(void *arg) {
     return NULL;
 }
 
-static int run_rows(const void *q, const void *k, const void *v, int format, const double descale[3],
-                    int B, int Hq, int Hkv, int S, int D, float scale, int causal,
-                    const uint8_t *block_mask, int mask_heads,
-                    const int64_t *rows, int64_t nrows, double *out, double *lse, int nthreads) {
+static int run_rows_dropout(const void *q, const void *k, const void *v, int format,
+                            const double descale[3], int B, int Hq, int Hkv, int S, int D,
+                            float scale, int causal, const uint8_t *block_mask, int mask_heads,
+                            int dropout_p8, uint64_t seed, uint64_t offset, const int64_t *rows,
+                            int64_t nrows, double *out, double *lse, int nthreads) {
     if (!q || !k || !v || !out || !lse) return 1;
     if (block_mask && mask_heads != 1 && mask_heads != Hq) return 1;
     if (B < 1 || Hq < 1 || Hkv < 1 || S < 1 || D < 1 || Hq % Hkv != 0) return 1;
@@ -227,6 +280,8 @@ static int run_rows(const void *q, const void *k, const void *v, int format, con
         J->scale = (double)scale;
         J->causal = causal ? 1 : 0;
         J->block_mask = block_mask; J->mask_heads = mask_heads;
+        J->dropout_p8 = dropout_p8;
+        J->dropout_key[0] = seed; J->dropout_key[1] = offset;
         J->rows = rows; J->nrows = nrows;
         J->out = out; J->lse = lse;
         J->begin = nrows * t / nthreads;
@@ -246,6 +301,14 @@ static int run_rows(const void *q, const void *k, const void *v, int format, con
     free(jobs);
     free(tid);
     return status;
+}
+
+static int run_rows(const void *q, const void *k, const void *v, int format, const double descale[3],
+                    int B, int Hq, int Hkv, int S, int D, float scale, int causal,
+                    const uint8_t *block_mask, int mask_heads,
+                    const int64_t *rows, int64_t nrows, double *out, double *lse, int nthreads) {
+    return run_rows_dropout(q, k, v, format, descale, B, Hq, Hkv, S, D, scale, causal, block_mask,
+                            mask_heads, 0, 0, 0, rows, nrows, out, lse, nthreads);
 }
 
 /*
@@ -513,4 +576,24 @@ int oracle_attn_bwd(const void *q, const void *k, const void *v, const void *dou
     free(P);
     free(dS);
     return status;
+}
+
+/*
+ * oracle_attn_rows_dropout -- oracle_attn_rows with dropout of the attention
+ * weights: drop probability p8 / 256 (0 <= p8 < 256), Philox key {seed,
+ * offset}; see dropout_keeps for which weights are dropped.
+ */
+int oracle_attn_rows_dropout(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int Hq,
+                             int Hkv, int S, int D, float scale, int causal, int p8, uint64_t seed,
+                             uint64_t offset, const int64_t *rows, int64_t nrows, double *out,
+                             double *lse, int nthreads) {
+    const double one[3] = {1.0, 1.0, 1.0};
+    if (p8 < 0 || p8 > 255) return 1;
+    return run_rows_dropout(q, k, v, FMT_BF16, one, B, Hq, Hkv, S, D, scale, causal, NULL, 1, p8,
+                            seed, offset, rows, nrows, out, lse, nthreads);
+}
+
+/* Philox4x64-10 of one counter block (exposed so the generator can be pinned). */
+void oracle_philox4x64(const uint64_t *ctr, const uint64_t *key, uint64_t *out) {
+    philox4x64_10(ctr, key, out);
 }

@@ -503,3 +503,80 @@ def pin_bwd_invariants(bwd):
 
 
 BWD_PINS = [pin_bwd_torch_autograd, pin_bwd_closed_forms, pin_bwd_invariants]
+
+
+# ---------------------------------------------------------------- dropout
+# ``attnd(q, k, v, scale, p8, seed, offset, causal, rows=None)`` -> (O, LSE).
+
+def numpy_philox_block(ctr, key):
+    """Philox4x64-10 of counter ``ctr`` (four 64-bit words, word 0 least
+    significant) from numpy's own implementation (a library routine).  numpy
+    advances its 256-bit counter before the first block, so it starts one below."""
+    value = sum(int(c) << (64 * w) for w, c in enumerate(ctr))
+    bg = np.random.Philox(counter=(value - 1) % (1 << 256), key=sum(int(x) << (64 * w) for w, x in enumerate(key)))
+    return bg.random_raw(4).astype(np.uint64)
+
+
+def keep_table(bh, S, p8, seed, offset):
+    """[S, S] booleans: is key j of query i kept?  The documented mapping --
+    byte (j mod 32) of Philox(counter {j/32, i, bh, 0}, key {seed, offset}),
+    little-endian words in order, kept when >= p8 -- written from the
+    definition with numpy's Philox."""
+    keep = np.zeros((S, S), dtype=bool)
+    for i in range(S):
+        for blk in range((S + 31) // 32):
+            by = numpy_philox_block([blk, i, bh, 0], [seed, offset]).view(np.uint8)
+            for t in range(32):
+                j = 32 * blk + t
+                if j < S:
+                    keep[i, j] = by[t] >= p8
+    return keep
+
+
+def pin_philox_library(philox):
+    """The oracle's Philox4x64-10 block equals numpy's Philox for assorted counters
+    and keys, and the zero counter and key give the published test vector
+    (Random123 known-answer list, first entry)."""
+    rng = np.random.default_rng(191)
+    for _ in range(20):
+        ctr = [int(x) for x in rng.integers(0, 2**63, 4, dtype=np.int64)]
+        key = [int(x) for x in rng.integers(0, 2**63, 2, dtype=np.int64)]
+        assert np.array_equal(philox(ctr, key), numpy_philox_block(ctr, key))
+    want = [0x16554d9eca36314c, 0xdb20fe9d672d0fdc, 0xd7e772cee186176b, 0x7e68b68aec7ba23b]
+    assert [int(x) for x in philox([0, 0, 0, 0], [0, 0])] == want
+
+
+def pin_dropout_mask_closed_form(attnd, attn):
+    """V = identity rows turns O rows into the weights: with dropout each must be
+    the undropped weight times keep(i, j) * 256/(256-p8), keep from the
+    documented byte mapping over numpy's Philox; the LSE is unchanged."""
+    B, H, S, D = 1, 2, 70, 128
+    q, k = _rand((B, H, S, D), 201, 0), _rand((B, H, S, D), 201, 1)
+    v = bits(np.broadcast_to(np.eye(S, D), (B, H, S, D)))
+    p8, seed, offset = 77, 0x1234abcd, 99
+    for causal in (True, False):
+        O, L = attnd(q, k, v, 0.2, p8, seed, offset, causal)
+        P, L0 = attn(q, k, v, 0.2, causal)
+        assert np.array_equal(L, L0), "dropout changed the LSE"
+        for h in range(H):
+            keep = keep_table(h, S, p8, seed, offset)
+            want = P[0, h, :, :S] * keep * (256.0 / (256 - p8))
+            assert np.max(np.abs(O[0, h, :, :S] - want)) < 1e-15
+
+
+def pin_dropout_rate_and_identity(attnd, attn):
+    """p8 = 0 is no dropout (bit for bit); with p8 = 64 a quarter of the weights
+    are dropped (within five binomial standard deviations)."""
+    B, H, S, D = 1, 4, 128, 128
+    q, k = _rand((B, H, S, D), 211, 0), _rand((B, H, S, D), 211, 1)
+    v = bits(np.broadcast_to(np.eye(S, D), (B, H, S, D)))
+    O0, L0 = attnd(q, k, v, 0.1, 0, 5, 6, False)
+    O, L = attn(q, k, v, 0.1, False)
+    assert np.array_equal(O0, O) and np.array_equal(L0, L)
+    Od, _ = attnd(q, k, v, 0.1, 64, 5, 6, False)
+    dropped = float(np.mean(Od == 0.0))
+    n = Od.size
+    assert abs(dropped - 0.25) < 5 * math.sqrt(0.25 * 0.75 / n), dropped
+
+
+DROPOUT_PINS = [pin_dropout_mask_closed_form, pin_dropout_rate_and_identity]

@@ -38,6 +38,14 @@ MUTANTS = {
                               "if (J->block_mask[(j / 128) * ((S + 127) / 128) + i / 128] == 0) s[j] = -INFINITY;"),
     "block_mask_heads_ignored": ("(J->mask_heads == 1 ? 0 : hq)", "(0)"),
     "block_mask_ignored": ("if (J->block_mask) {", "if (0) {"),
+    "dropout_keep_flipped": ("return byte >= J->dropout_p8;", "return byte < J->dropout_p8;"),
+    "dropout_byte_order": ("(out[(j % 32) / 8] >> (8 * (j % 8)))", "(out[(j % 32) % 4] >> (8 * ((j % 32) / 4)))"),
+    "dropout_counter_swapped": ("const uint64_t ctr[4] = {(uint64_t)(j / 32), (uint64_t)i, (uint64_t)bh, 0};",
+                                "const uint64_t ctr[4] = {(uint64_t)i, (uint64_t)(j / 32), (uint64_t)bh, 0};"),
+    "dropout_unscaled": ("s[j] = dropout_keeps(J, r / S, i, j) ? s[j] * keep_scale : 0.0;",
+                         "s[j] = dropout_keeps(J, r / S, i, j) ? s[j] : 0.0;"),
+    "philox_weyl_swapped": ("k0 += W0;\n        k1 += W1;", "k0 += W1;\n        k1 += W0;"),
+    "philox_round_outputs_swapped": ("x1 = lo1;", "x1 = lo0;"),
     "bwd_delta_not_subtracted": ("ds[j] = p[j] * (dP[j] - delta);", "ds[j] = p[j] * dP[j];"),
     "bwd_delta_unweighted": ("delta += p[j] * dP[j];", "delta += dP[j];"),
     "bwd_dq_scale_dropped": ("for (int d = 0; d < D; ++d) dq[d] *= J->scale;", ""),
@@ -76,6 +84,9 @@ def test_some_pin_catches_mutant(name, tmp_path):
     def attnm(q, k, v, scale, mask, causal, rows=None):
         return oracle.attention_masked(q, k, v, scale, mask, causal, rows=rows, lib=lib)
 
+    def attnd(q, k, v, scale, p8, seed, offset, causal, rows=None):
+        return oracle.attention_dropout(q, k, v, scale, p8, seed, offset, causal, rows=rows, lib=lib)
+
     def bwd(q, k, v, dout, scale, causal, kv_heads=None):
         return oracle.attention_bwd(q, k, v, dout, scale, causal, kv_heads=kv_heads, lib=lib)
 
@@ -90,7 +101,10 @@ def test_some_pin_catches_mutant(name, tmp_path):
         ("pin_block_mask_library", lambda: oracle_pins.pin_block_mask_library(attnm)),
         ("pin_block_mask_all_ones", lambda: oracle_pins.pin_block_mask_all_ones(attnm, attn)),
         ("pin_bwd_finite_differences", lambda: oracle_pins.pin_bwd_finite_differences(bwd, fwd64)),
-    ] + [(p.__name__, lambda p=p: p(bwd)) for p in oracle_pins.BWD_PINS]
+    ] + [(p.__name__, lambda p=p: p(bwd)) for p in oracle_pins.BWD_PINS] + [
+        ("pin_philox_library", lambda: oracle_pins.pin_philox_library(
+            lambda c, k: oracle.philox4x64(c, k, lib=lib))),
+    ] + [(p.__name__, lambda p=p: p(attnd, attn)) for p in oracle_pins.DROPOUT_PINS]
     caught = []
     for pin_name, run in checks:
         try:

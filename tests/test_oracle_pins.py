@@ -52,6 +52,19 @@ def test_oracle_bwd_thread_count_does_not_change_bits():
     assert all(np.array_equal(x, y) for x, y in zip(a, b))
 
 
+def test_oracle_philox_pin():
+    oracle_pins.pin_philox_library(oracle.philox4x64)
+
+
+def _attnd(q, k, v, scale, p8, seed, offset, causal, rows=None):
+    return oracle.attention_dropout(q, k, v, scale, p8, seed, offset, causal, rows=rows)
+
+
+@pytest.mark.parametrize("pin", oracle_pins.DROPOUT_PINS, ids=lambda p: p.__name__)
+def test_oracle_dropout_pin(pin):
+    pin(_attnd, _attn)
+
+
 def test_rows_subset_matches_full():
     """The row-selection entry computes exactly the rows of the full call."""
     from causal_scaled_dot_gb300.inputs import qkv_bf16
