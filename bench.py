@@ -37,6 +37,7 @@ sys.path.insert(0, ROOT)
 
 from causal_scaled_dot_gb300.workloads import BY_NAME, HEADLINE  # noqa: E402
 
+DROPOUT_SEED, DROPOUT_OFFSET = 0x5EED, 0
 METRIC = "causal attn fwd TFLOP/s (bf16, 1xGB300) and % of dense bf16 tensor peak"
 BWD_METRIC = "causal attn bwd TFLOP/s (bf16, 1xGB300; 2.5x forward FLOPs) and % of dense bf16 tensor peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -183,7 +184,7 @@ class OracleTimer:
     rows * 2*S*D and its TFLOP/s is comparable with the GPU's.
     """
 
-    def __init__(self, w, fp8: bool = False, mask=None):
+    def __init__(self, w, fp8: bool = False, mask=None, dropout_p8: int = 0):
         import oracle
         from causal_scaled_dot_gb300.inputs import qkv_bf16, qkv_e4m3
         self.oracle = oracle
@@ -195,6 +196,7 @@ class OracleTimer:
         self.total = w.B * w.Hq * w.S
         self.row_flops = (2.0 if w.causal else 4.0) * w.S * w.D
         self.mask = mask
+        self.p8 = dropout_p8
         if mask is not None:
             self.keys = visible_keys(mask, w.S, w.causal)  # [mask heads, S]
             self.row_flops = 4.0 * w.D * float(self.keys.mean())
@@ -209,6 +211,10 @@ class OracleTimer:
         if self.mask is not None:
             self.oracle.attention_masked(self.q, self.k, self.v, self.w.scale, self.mask,
                                          self.w.causal, rows=rows, nthreads=self.threads)
+        elif self.p8:
+            self.oracle.attention_dropout(self.q, self.k, self.v, self.w.scale, self.p8,
+                                          DROPOUT_SEED, DROPOUT_OFFSET, self.w.causal, rows=rows,
+                                          nthreads=self.threads)
         elif self.fp8:
             self.oracle.attention_e4m3(self.q, self.k, self.v, self.w.scale, (1.0, 1.0, 1.0),
                                        self.w.causal, rows=rows, nthreads=self.threads)
@@ -272,10 +278,14 @@ class OracleBwdTimer:
         return n * self.row_flops / dt / 1e12, n, dt
 
 
+def dropout_p8(args) -> int:
+    return int(round(args.dropout * 256)) if args.dropout is not None else 0
+
+
 def make_oracle_timer(args, w, mask=None):
     if args.pass_ == "bwd":
         return OracleBwdTimer(w)
-    return OracleTimer(w, fp8=args.dtype == "fp8", mask=mask)
+    return OracleTimer(w, fp8=args.dtype == "fp8", mask=mask, dropout_p8=dropout_p8(args))
 
 
 def metric_name(args) -> str:
@@ -315,7 +325,9 @@ def run_reference(args, w, rank, world):
         "data": f"synthetic (seeded N(0,1) {'e4m3' if args.dtype == 'fp8' else 'bf16'})",
         "config": {"workload": w.name, **w.shape_dict, "causal": w.causal,
                    "inputs": "e4m3" if args.dtype == "fp8" else "bf16", "pass": args.pass_,
-                   **mask_config(mask, args.mask_density)},
+                   **mask_config(mask, args.mask_density),
+                   **({"dropout_p": dropout_p8(args) / 256, "dropout_key": [DROPOUT_SEED, DROPOUT_OFFSET]}
+                      if args.dropout is not None else {})},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": timer.threads,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -360,6 +372,9 @@ def run_ours(args, w, rank, world, local):
         elif mask is not None:
             native.attn_fwd_block_masked(q, k, v, out, lse, w.B, w.Hq, w.Hkv, w.S, w.D, w.scale,
                                          w.causal, mask_d, mask.shape[0], stream)
+        elif args.dropout is not None:
+            native.attn_fwd_dropout(q, k, v, out, lse, w.B, w.Hq, w.Hkv, w.S, w.D, w.scale, w.causal,
+                                    args.dropout, DROPOUT_SEED, DROPOUT_OFFSET, stream)
         else:
             native.attn_fwd(q, k, v, out, lse, w.B, w.Hq, w.Hkv, w.S, w.D, w.scale, w.causal,
                             stream)
@@ -428,13 +443,14 @@ def run_ours(args, w, rank, world, local):
         peak *= 2.0
         peak_what = f"{peak_src} bf16 dense (burst) x 2, the nominal fp8/bf16 ratio"
     achieved = flops / (ms_local * 1e-3) / 1e12
-    variant = w.name + (":fp8" if fp8 else "") + (f":mask{args.mask_density}" if mask is not None else "")
+    variant = (w.name + (":fp8" if fp8 else "") + (f":mask{args.mask_density}" if mask is not None else "")
+               + (f":dropout{args.dropout}" if args.dropout is not None else ""))
     traffic = recorded_traffic(variant)
     # algorithmic bytes: inputs read once (1 byte per element for E4M3), O and LSE written once
     io_bytes = w.io_bytes - (w.B * (w.Hq + 2 * w.Hkv) * w.S * w.D if fp8 else 0)
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        timer = OracleTimer(w, fp8=fp8, mask=mask)
+        timer = OracleTimer(w, fp8=fp8, mask=mask, dropout_p8=dropout_p8(args))
         tf, n, dt = timer.sample(args.cpu_seconds, seed=7)
         cpu = {"value": tf, "unit": "TFLOP/s", "cores": timer.threads, "kind": "oracle",
                "sample": f"{n} random query rows of {w.name} (of {timer.total}), "
@@ -447,6 +463,8 @@ def run_ours(args, w, rank, world, local):
         "data": f"synthetic (seeded N(0,1) {'e4m3' if fp8 else 'bf16'}, no weights)",
         "config": {"workload": w.name, **w.shape_dict, "causal": w.causal,
                    "inputs": "e4m3" if fp8 else "bf16", **mask_config(mask, args.mask_density),
+                   **({"dropout_p": dropout_p8(args) / 256, "dropout_key": [DROPOUT_SEED, DROPOUT_OFFSET]}
+                      if args.dropout is not None else {}),
                    "l2": "flushed between timed steps (256 MiB write)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "pct_of_peak": 100.0 * achieved / peak,
@@ -605,6 +623,9 @@ def main():
     ap.add_argument("--mask-density", type=float, default=None,
                     help="bf16 only: run attn_fwd_block_masked with a seeded per-head block mask "
                          "keeping each 128x128 block with this probability")
+    ap.add_argument("--dropout", type=float, default=None,
+                    help="bf16 forward only: attn_fwd_dropout with this drop probability "
+                         "(rounded to a multiple of 1/256)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="budget of the oracle CPU-baseline sample")
     ap.add_argument("--ref-step-seconds", type=float, default=8.0,
@@ -619,6 +640,9 @@ def main():
         ap.error("--mask-density takes a probability in [0, 1] and bf16 inputs")
     if args.pass_ == "bwd" and (args.dtype != "bf16" or args.mask_density is not None):
         ap.error("--pass bwd takes bf16 inputs and no mask")
+    if args.dropout is not None and (args.pass_ != "fwd" or args.dtype != "bf16" or args.mask_density is not None
+                                     or not 0 < round(args.dropout * 256) < 256):
+        ap.error("--dropout takes 0 < p < 1 (at least 1/256), bf16 forward, no mask")
     w = BY_NAME[args.workload]
     rank, world, local = dist_init(args)
     if world != args.gpus and rank == 0:

@@ -62,11 +62,13 @@ int setup_device_locked(int dev) {
     if (cudaGetSymbolAddress(&word, g_attn_status) != cudaSuccess ||
         allow_smem(attn_fwd_simple_kernel<64>, SimpleLayout<64>::kDynamicSmem) != cudaSuccess ||
         allow_smem(attn_fwd_simple_kernel<128>, SimpleLayout<128>::kDynamicSmem) != cudaSuccess ||
-        allow_smem(attn_fwd_ws_kernel<64, false, false>, WsLayout<64, false>::kDynamicSmem) != cudaSuccess ||
-        allow_smem(attn_fwd_ws_kernel<128, false, false>, WsLayout<128, false>::kDynamicSmem) != cudaSuccess ||
-        allow_smem(attn_fwd_ws_kernel<128, true, false>, WsLayout<128, true>::kDynamicSmem) != cudaSuccess ||
-        allow_smem(attn_fwd_ws_kernel<64, false, true>, WsLayout<64, false>::kDynamicSmem) != cudaSuccess ||
-        allow_smem(attn_fwd_ws_kernel<128, false, true>, WsLayout<128, false>::kDynamicSmem) != cudaSuccess) {
+        allow_smem(attn_fwd_ws_kernel<64, false, false, false>, WsLayout<64, false>::kDynamicSmem) != cudaSuccess ||
+        allow_smem(attn_fwd_ws_kernel<128, false, false, false>, WsLayout<128, false>::kDynamicSmem) != cudaSuccess ||
+        allow_smem(attn_fwd_ws_kernel<128, true, false, false>, WsLayout<128, true>::kDynamicSmem) != cudaSuccess ||
+        allow_smem(attn_fwd_ws_kernel<64, false, true, false>, WsLayout<64, false>::kDynamicSmem) != cudaSuccess ||
+        allow_smem(attn_fwd_ws_kernel<128, false, true, false>, WsLayout<128, false>::kDynamicSmem) != cudaSuccess ||
+        allow_smem(attn_fwd_ws_kernel<64, false, false, true>, WsLayout<64, false>::kDynamicSmem) != cudaSuccess ||
+        allow_smem(attn_fwd_ws_kernel<128, false, false, true>, WsLayout<128, false>::kDynamicSmem) != cudaSuccess) {
         st.status = ATTN_ERR_DEVICE;
         return st.status;
     }
@@ -157,7 +159,7 @@ int launch_simple(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMa
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
-template <int D, bool F, bool M>
+template <int D, bool F, bool M, bool DR = false>
 int launch_ws(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, FwdParams p,
               int sm_count, cudaStream_t stream) {
     const long long npairs = (p.num_q_tiles + 1) / 2;
@@ -165,7 +167,7 @@ int launch_ws(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& t
     if (units > (1ll << 31) - 1) return ATTN_ERR_UNSUPPORTED;
     p.num_units = (int)units;
     const int grid = (int)(units < sm_count ? units : sm_count);
-    attn_fwd_ws_kernel<D, F, M><<<grid, WsLayout<D, F>::kThreads, WsLayout<D, F>::kDynamicSmem, stream>>>(
+    attn_fwd_ws_kernel<D, F, M, DR><<<grid, WsLayout<D, F>::kThreads, WsLayout<D, F>::kDynamicSmem, stream>>>(
         tq, tk, tv, p);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
@@ -202,13 +204,15 @@ namespace attn {
 namespace {
 int fwd_bf16(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
              int Hkv, int S, int D, float scale, int causal, const uint8_t* block_mask,
-             int mask_heads, void* stream);
+             int mask_heads, int dropout_p8, unsigned long long seed, unsigned long long offset,
+             void* stream);
 }  // namespace
 }  // namespace attn
 
 extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B,
                         int Hq, int Hkv, int S, int D, float scale, int causal, void* stream) {
-    return attn::fwd_bf16(q, k, v, out, lse, B, Hq, Hkv, S, D, scale, causal, nullptr, 1, stream);
+    return attn::fwd_bf16(q, k, v, out, lse, B, Hq, Hkv, S, D, scale, causal, nullptr, 1, 0, 0, 0,
+                          stream);
 }
 
 extern "C" int attn_fwd_block_masked(const void* q, const void* k, const void* v, void* out,
@@ -217,14 +221,26 @@ extern "C" int attn_fwd_block_masked(const void* q, const void* k, const void* v
                                      void* stream) {
     if (block_mask == nullptr || (mask_heads != 1 && mask_heads != Hq)) return ATTN_ERR_INVALID_ARG;
     return attn::fwd_bf16(q, k, v, out, lse, B, Hq, Hkv, S, D, scale, causal, block_mask,
-                          mask_heads, stream);
+                          mask_heads, 0, 0, 0, stream);
+}
+
+extern "C" int attn_fwd_dropout(const void* q, const void* k, const void* v, void* out, float* lse,
+                                int B, int Hq, int Hkv, int S, int D, float scale, int causal,
+                                float dropout_p, unsigned long long seed, unsigned long long offset,
+                                void* stream) {
+    if (!std::isfinite(dropout_p) || dropout_p < 0.f) return ATTN_ERR_INVALID_ARG;
+    const long p8 = std::lrint((double)dropout_p * 256.0);
+    if (p8 > 255) return ATTN_ERR_INVALID_ARG;
+    return attn::fwd_bf16(q, k, v, out, lse, B, Hq, Hkv, S, D, scale, causal, nullptr, 1, (int)p8,
+                          seed, offset, stream);
 }
 
 namespace attn {
 namespace {
 int fwd_bf16(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
              int Hkv, int S, int D, float scale, int causal, const uint8_t* block_mask,
-             int mask_heads, void* stream) {
+             int mask_heads, int dropout_p8, unsigned long long seed, unsigned long long offset,
+             void* stream) {
     int rc = check_args(q, k, v, out, lse, B, Hq, Hkv, S, D, scale);
     if (rc != ATTN_OK) return rc;
     DeviceState* dev = nullptr;
@@ -255,6 +271,15 @@ int fwd_bf16(const void* q, const void* k, const void* v, void* out, float* lse,
     p.block_mask = block_mask;
     p.mask_heads = mask_heads;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (dropout_p8 > 0) {
+        // Kept weights are scaled by 256 / (256 - p8) along with 1 / l.
+        p.dropout_p8 = dropout_p8;
+        p.dropout_seed = seed;
+        p.dropout_offset = offset;
+        p.o_scale = 256.f / (float)(256 - dropout_p8);
+        return D == 64 ? launch_ws<64, false, false, true>(tq, tk, tv, p, dev->sm_count, st)
+                       : launch_ws<128, false, false, true>(tq, tk, tv, p, dev->sm_count, st);
+    }
     // Block masks are handled by the persistent kernel only.
     if (block_mask == nullptr && use_simple_kernel())
         return D == 64 ? launch_simple<64>(tq, tk, tv, p, st) : launch_simple<128>(tq, tk, tv, p, st);

@@ -26,6 +26,8 @@ struct FwdParams {
     float o_scale;                  // multiplies O at the end (FP8: the V descale; else 1)
     const uint8_t* block_mask;      // null, or [mask_heads][nt][nt], nt = num_q_tiles
     int mask_heads;                 // 1 (one mask for all heads) or Hq
+    int dropout_p8;                 // dropout kernels: weights dropped with probability p8 / 256
+    unsigned long long dropout_seed, dropout_offset;  // Philox key
 };
 
 }  // namespace attn

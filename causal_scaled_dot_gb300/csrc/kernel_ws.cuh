@@ -45,6 +45,7 @@
 #include <cuda_bf16.h>
 
 #include "common.cuh"
+#include "philox.cuh"
 #include "ptx.cuh"
 
 namespace attn {
@@ -166,7 +167,7 @@ __device__ __forceinline__ uint32_t ws_bar(uint32_t base, int i) {
 }
 
 // ---------------------------------------------------------------- producer
-template <int D, bool F, bool M>
+template <int D, bool F, bool M, bool DR>
 __device__ void ws_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                              const CUtensorMap* tm_v, const FwdParams& p, uint32_t base,
                              volatile int* abort_flag) {
@@ -228,7 +229,7 @@ drain:
 }
 
 // ---------------------------------------------------------------- MMA issuer
-template <int D, bool F, bool M>
+template <int D, bool F, bool M, bool DR>
 __device__ void ws_mma_role(const FwdParams& p, uint32_t base, uint32_t tmem,
                             volatile int* abort_flag) {
     using L = WsLayout<D, F>;
@@ -358,7 +359,7 @@ __device__ void ws_mma_role(const FwdParams& p, uint32_t base, uint32_t tmem,
 }
 
 // ---------------------------------------------------------------- softmax
-template <int D, bool F, bool M>
+template <int D, bool F, bool M, bool DR>
 __device__ void ws_softmax_role(const FwdParams& p, uint32_t base, uint32_t tmem, int wg,
                                 volatile int* abort_flag) {
     using L = WsLayout<D, F>;
@@ -455,6 +456,36 @@ __device__ void ws_softmax_role(const FwdParams& p, uint32_t base, uint32_t tmem
                     }
                     ptx::tmem_st16(tP + 32u + 16u * h, pk);
                 }
+            } else if constexpr (DR) {
+                // Dropout: key kv0 + e is kept when byte e mod 32 of the Philox
+                // block {(kv0 + e) / 32, query row, b*Hq + hq, 0} is >= p8.  The
+                // row sum takes every probability; the tensor core gets the kept
+                // ones (the 256 / (256 - p8) factor is in o_scale).
+                const uint64_t qrow = (uint64_t)(qt * kTile + r);
+                const uint32_t p8 = (uint32_t)p.dropout_p8;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int b = 0; b < 2; ++b) {
+                        uint64_t rnd[4];
+                        philox4x64_10((uint64_t)((kv0 + 64 * h + 32 * b) >> 5), qrow, (uint64_t)w.bh, 0ull,
+                                      p.dropout_seed, p.dropout_offset, rnd);
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) {
+                            const int e = 64 * h + 32 * b + 2 * c;
+                            float x0, x1;
+                            ptx::f2_split(ptx::fma2(ptx::f2(s[e], s[e + 1]), sl2x2, negm2), x0, x1);
+                            const float p0 = ptx::ex2(x0);
+                            const float p1 = ptx::ex2(x1);
+                            acc[c & 3] = ptx::add2(acc[c & 3], ptx::f2(p0, p1));
+                            const uint32_t two = (uint32_t)(rnd[c / 4] >> (16 * (c % 4)));
+                            pk[16 * b + c] = ptx::pack_bf16x2((two & 0xFFu) >= p8 ? p0 : 0.f,
+                                                              ((two >> 8) & 0xFFu) >= p8 ? p1 : 0.f);
+                        }
+                    }
+                    ptx::tmem_st32(tP + 32 * h, pk);
+                }
             } else {
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
@@ -550,7 +581,7 @@ __device__ void ws_softmax_role(const FwdParams& p, uint32_t base, uint32_t tmem
 }
 
 // ---------------------------------------------------------------- kernel
-template <int D, bool F, bool M>
+template <int D, bool F, bool M, bool DR>
 __global__ void __launch_bounds__(WsLayout<D, F>::kThreads, 1)
     attn_fwd_ws_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
@@ -596,13 +627,13 @@ __global__ void __launch_bounds__(WsLayout<D, F>::kThreads, 1)
     if (warp < 4) {
         ptx::regs_dec<L::kRegsSmall>();
         if (warp == 0) {
-            if (lane == 0) ws_load_role<D, F, M>(&tm_q, &tm_k, &tm_v, p, base, abort_flag);
+            if (lane == 0) ws_load_role<D, F, M, DR>(&tm_q, &tm_k, &tm_v, p, base, abort_flag);
         } else if (warp == 1) {
-            if (lane == 0) ws_mma_role<D, F, M>(p, base, tmem, abort_flag);
+            if (lane == 0) ws_mma_role<D, F, M, DR>(p, base, tmem, abort_flag);
         }
     } else {
         ptx::regs_inc<L::kRegsSoftmax>();
-        ws_softmax_role<D, F, M>(p, base, tmem, (warp - 4) >> 2, abort_flag);
+        ws_softmax_role<D, F, M, DR>(p, base, tmem, (warp - 4) >> 2, abort_flag);
     }
 
     ptx::tc_fence_before();

@@ -51,6 +51,10 @@ def load() -> ctypes.CDLL:
         lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, ci,
                                  vp]
         lib.attn_bwd.restype = ci
+        u64 = ctypes.c_ulonglong
+        lib.attn_fwd_dropout.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, ci, cf, u64, u64,
+                                         vp]
+        lib.attn_fwd_dropout.restype = ci
         lib.attn_fwd_fp8.argtypes = [vp, vp, vp, cf, cf, cf, vp, vp, ci, ci, ci, ci, ci, cf, ci, vp]
         lib.attn_fwd_fp8.restype = ci
         lib.attn_sync_status.argtypes = [vp]
@@ -121,6 +125,19 @@ def attn_fwd_block_masked(q, k, v, out, lse, B: int, Hq: int, Hkv: int, S: int, 
                                       _stream(stream))
     if check and rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_block_masked")
+    return rc
+
+
+def attn_fwd_dropout(q, k, v, out, lse, B: int, Hq: int, Hkv: int, S: int, D: int, scale: float,
+                     causal: bool | int, dropout_p: float, seed: int, offset: int, stream=None,
+                     check: bool = True) -> int:
+    """The C entry point ``attn_fwd_dropout`` (drop probability rounded to p8/256)."""
+    rc = load().attn_fwd_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), int(B), int(Hq),
+                                 int(Hkv), int(S), int(D), float(scale), 1 if causal else 0,
+                                 float(dropout_p), int(seed) & (2**64 - 1), int(offset) & (2**64 - 1),
+                                 _stream(stream))
+    if check and rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_dropout")
     return rc
 
 

@@ -98,6 +98,28 @@ int attn_fwd_block_masked(const void *q, const void *k, const void *v, void *out
                           const unsigned char *block_mask, int mask_heads, void *stream);
 
 /*
+ * attn_fwd_dropout -- attn_fwd with dropout of the attention weights, fused
+ * into the kernel (the fused SDPA dropout the ai-manual.ru article describes
+ * in section 6, "Dropout"): after the softmax each weight is dropped with
+ * probability p and the kept ones are scaled by 1 / (1 - p).
+ *
+ *   dropout_p   0 <= p < 1, rounded to p8 / 256 with p8 = round(256 p), and
+ *               p8 <= 255 (ATTN_ERR_INVALID_ARG otherwise); p8 = 0 is attn_fwd.
+ *               Kept weights are scaled by 256 / (256 - p8).
+ *   seed, offset  the Philox4x64-10 key {seed, offset}.
+ * Which weights are dropped: key j of query row i of head b*Hq + hq is kept
+ * when byte (j mod 32) of Philox4x64-10(counter {j / 32, i, b*Hq + hq, 0},
+ * key {seed, offset}) -- the four 64-bit output words in order, each
+ * little-endian -- is >= p8 (Philox4x64-10: Salmon et al., "Parallel random
+ * numbers: as easy as 1, 2, 3", SC 2011).  The same call with the same key
+ * drops the same weights.  LSE is that of the undropped softmax.  Other
+ * arguments, errors and rules as attn_fwd (bf16 inputs).
+ */
+int attn_fwd_dropout(const void *q, const void *k, const void *v, void *out, float *lse, int B,
+                     int Hq, int Hkv, int S, int D, float scale, int causal, float dropout_p,
+                     unsigned long long seed, unsigned long long offset, void *stream);
+
+/*
  * attn_fwd_fp8 -- the same attention with FP8 E4M3 inputs and per-tensor
  * descale factors (the FP8 attention the ai-manual.ru article mentions for
  * newer GPUs, section 6 "FP8 and BF16").

@@ -39,15 +39,18 @@ def run_gpu(q_bits, k_bits, v_bits, scale, causal, with_lse=True, stream=None):
     return o, l, bits_of(out)
 
 
-def compare(o_gpu, o_ref, l_gpu, l_ref, label=""):
-    """Assert the parity bar; returns the error figures."""
+def compare(o_gpu, o_ref, l_gpu, l_ref, label="", abs_scale=1.0):
+    """Assert the parity bar; returns the error figures.  ``abs_scale`` widens
+    the max-abs bound for outputs that are a known factor larger (dropout's
+    256 / (256 - p8)); the relative L2 bound does not change."""
     assert np.all(np.isfinite(o_gpu)), f"{label}: non-finite output (unwritten rows?)"
     diff = o_gpu - o_ref
     max_abs = float(np.max(np.abs(diff))) if diff.size else 0.0
     ref_norm = float(np.linalg.norm(o_ref))
     rel_l2 = float(np.linalg.norm(diff) / ref_norm) if ref_norm > 0 else float(np.linalg.norm(diff))
     stats = {"max_abs": max_abs, "rel_l2": rel_l2}
-    assert max_abs <= TOL_O_MAX_ABS, f"{label}: O max abs error {max_abs:.3e} > {TOL_O_MAX_ABS}"
+    assert max_abs <= TOL_O_MAX_ABS * abs_scale, \
+        f"{label}: O max abs error {max_abs:.3e} > {TOL_O_MAX_ABS * abs_scale}"
     assert rel_l2 <= TOL_O_REL_L2, f"{label}: O rel L2 error {rel_l2:.3e} > {TOL_O_REL_L2}"
     if l_gpu is not None:
         assert np.all(np.isfinite(l_gpu)), f"{label}: non-finite LSE"
@@ -198,3 +201,18 @@ def compare_delta(delta, delta_ref, o_ref, do, label):
     err = np.abs(delta - delta_ref)
     assert np.all(err <= tol), f"{label}: delta error {float(np.max(err - tol)):.3e} over its bound"
     return float(np.max(err))
+
+
+def run_gpu_dropout(q_bits, k_bits, v_bits, scale, causal, dropout_p, seed, offset, stream=None):
+    """attn_fwd_dropout through the C ABI; returns (O float64, LSE float64)."""
+    import torch
+    from causal_scaled_dot_gb300 import native
+    B, Hq, S, D = q_bits.shape
+    Hkv = k_bits.shape[1]
+    q, k, v = to_device(q_bits), to_device(k_bits), to_device(v_bits)
+    out = torch.full_like(q, float("nan"))
+    lse = torch.full((B, Hq, S), float("nan"), dtype=torch.float32, device="cuda")
+    native.attn_fwd_dropout(q, k, v, out, lse, B, Hq, Hkv, S, D, scale, causal, dropout_p, seed,
+                            offset, stream=stream)
+    native.attn_sync_status(stream)
+    return out.double().cpu().numpy(), lse.double().cpu().numpy()

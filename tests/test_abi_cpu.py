@@ -27,8 +27,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for required in ("attn_fwd", "attn_fwd_fp8", "attn_fwd_block_masked", "attn_bwd",
-                     "attn_status_string", "attn_sync_status"):
+    for required in ("attn_fwd", "attn_fwd_fp8", "attn_fwd_block_masked", "attn_fwd_dropout",
+                     "attn_bwd", "attn_status_string", "attn_sync_status"):
         assert required in names
 
 
@@ -187,3 +187,24 @@ def _call_bwd(q=1 << 40, k=2 << 40, v=3 << 40, out=4 << 40, dout=5 << 40, lse=6 
 ])
 def test_bwd_argument_errors_are_rejected_before_launch(kw, code):
     assert _call_bwd(**kw) == code
+
+
+def _call_dropout(p=0.1, q=1 << 40, k=2 << 40, v=3 << 40, out=4 << 40, lse=None, B=1, Hq=2, Hkv=2,
+                  S=300, D=128, scale=0.1, causal=1):
+    lib = native.load()
+    return lib.attn_fwd_dropout(q, k, v, out, lse, B, Hq, Hkv, S, D, ctypes.c_float(scale), causal,
+                                ctypes.c_float(p), 1, 2, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(p=-0.01), ATTN_ERR_INVALID_ARG),
+    (dict(p=1.0), ATTN_ERR_INVALID_ARG),          # rounds to p8 = 256
+    (dict(p=0.999), ATTN_ERR_INVALID_ARG),        # rounds to p8 = 256
+    (dict(p=float("nan")), ATTN_ERR_INVALID_ARG),
+    (dict(p=float("inf")), ATTN_ERR_INVALID_ARG),
+    (dict(q=None), ATTN_ERR_INVALID_ARG),
+    (dict(D=80), ATTN_ERR_UNSUPPORTED),
+    (dict(k=(2 << 40) + 8), ATTN_ERR_MISALIGNED),
+])
+def test_dropout_argument_errors_are_rejected_before_launch(kw, code):
+    assert _call_dropout(**kw) == code
