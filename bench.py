@@ -12,7 +12,9 @@ block mask keeping each 128 x 128 block with probability P, and the FLOPs are
 4*D per visible (query, key) pair, counted exactly.  With --pass bwd the step
 is one attn_bwd call (dQ, dK, dV for a seeded upstream gradient, O and LSE
 from attn_fwd beforehand) and FLOPs = 2.5x the forward's (five products per
-tile pair instead of two: the usual convention for attention backward).  Between timed
+tile pair instead of two: the usual convention for attention backward).
+With --pass proj the step is one attn_out_proj call on the workload's
+attention output shape, E = Hq*D output features, FLOPs = 2*B*S*E*Hq*D.  Between timed
 steps a 256 MiB buffer is written to flush L2; each step is timed with CUDA
 events on the launching stream.  Under torchrun every rank runs the same
 workload on its own GPU (independent problems, no collective on the data
@@ -39,6 +41,7 @@ from causal_scaled_dot_gb300.workloads import BY_NAME, HEADLINE  # noqa: E402
 
 DROPOUT_SEED, DROPOUT_OFFSET = 0x5EED, 0
 METRIC = "causal attn fwd TFLOP/s (bf16, 1xGB300) and % of dense bf16 tensor peak"
+PROJ_METRIC = "attn output projection TFLOP/s (bf16, 1xGB300) and % of dense bf16 tensor peak"
 BWD_METRIC = "causal attn bwd TFLOP/s (bf16, 1xGB300; 2.5x forward FLOPs) and % of dense bf16 tensor peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
@@ -57,6 +60,7 @@ def load_peaks():
 # The sources that make the timed kernels and their launch, per pass.
 FWD_SOURCES = ("attn_api.cu", "common.cuh", "kernel_ws.cuh", "ptx.cuh")
 BWD_SOURCES = ("attn_bwd.cu", "common.cuh", "kernel_bwd.cuh", "ptx.cuh")
+PROJ_SOURCES = ("attn_proj.cu", "common.cuh", "kernel_proj.cuh", "ptx.cuh")
 
 
 def kernel_source_hash(sources=FWD_SOURCES) -> str:
@@ -285,13 +289,58 @@ def dropout_p8(args) -> int:
 def make_oracle_timer(args, w, mask=None):
     if args.pass_ == "bwd":
         return OracleBwdTimer(w)
+    if args.pass_ == "proj":
+        return OracleProjTimer(w)
     return OracleTimer(w, fp8=args.dtype == "fp8", mask=mask, dropout_p8=dropout_p8(args))
 
 
 def metric_name(args) -> str:
     if args.pass_ == "bwd":
         return BWD_METRIC
+    if args.pass_ == "proj":
+        return PROJ_METRIC
     return METRIC
+
+
+def proj_inputs(w):
+    """Seeded O [B, Hq, S, D], W [E, Hq*D] (E = Hq*D) and bias [E] of the projection step."""
+    from causal_scaled_dot_gb300.inputs import gaussian_bf16
+    E, K = w.Hq * w.D, w.Hq * w.D
+    o = gaussian_bf16((w.B, w.Hq, w.S, w.D), w.seed, 0)
+    wt = gaussian_bf16((E, K), w.seed, 1, sigma=1.0 / np.sqrt(K))
+    bias = np.random.default_rng(w.seed).standard_normal(E).astype(np.float32)
+    return o, wt, bias
+
+
+class OracleProjTimer:
+    """The oracle's float64 projection on a bounded sample of sequence positions."""
+
+    def __init__(self, w):
+        import oracle
+        self.oracle = oracle
+        self.w = w
+        self.o, self.wt, self.bias = proj_inputs(w)
+        self.threads = os.cpu_count() or 1
+        self.total = w.S
+        self.row_flops = 2.0 * w.B * (w.Hq * w.D) * (w.Hq * w.D)  # per position (all batch entries)
+        t0 = time.perf_counter()
+        self.run(16, seed=12345)
+        self.sec_per_row = (time.perf_counter() - t0) / 16
+
+    def run(self, n, seed):
+        pos = np.sort(np.random.default_rng(seed).choice(self.w.S, size=n, replace=False))
+        self.oracle.out_proj(self.o[:, :, pos], self.wt, self.bias)
+        return pos
+
+    def rows_for(self, seconds):
+        return int(min(self.total, max(1, seconds / max(self.sec_per_row, 1e-9))))
+
+    def sample(self, seconds, seed):
+        n = self.rows_for(seconds)
+        t0 = time.perf_counter()
+        self.run(n, seed)
+        dt = time.perf_counter() - t0
+        return n * self.row_flops / dt / 1e12, n, dt
 
 
 def mask_config(mask, density):
@@ -314,9 +363,11 @@ def run_reference(args, w, rank, world):
     secs = sum(dt for _, _, dt in samples)
     value = sum(tf * dt for tf, _, dt in samples) / secs
     rows_per_step = int(np.mean([n for _, n, _ in samples]))
-    what = "key/value heads (gradients)" if args.pass_ == "bwd" else "query rows"
+    what = {"bwd": "key/value heads (gradients)", "proj": "sequence positions (projection)"}.get(
+        args.pass_, "query rows")
+    how = "float64 numpy matmul" if args.pass_ == "proj" else "fp64 C oracle"
     sample = (f"{rows_per_step} random {what} of {w.name} per step "
-              f"(of {timer.total}); fp64 C oracle, {timer.threads} threads")
+              f"(of {timer.total}); {how}, {timer.threads} threads")
     line = {
         "impl": "reference", "metric": metric_name(args), "value": value, "unit": "TFLOP/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -609,6 +660,119 @@ def run_ours_bwd(args, w, rank, world, local):
     return 0
 
 
+def run_ours_proj(args, w, rank, world, local):
+    """attn_out_proj timed like the forward: O, W, bias resident, L2 flushed
+    between steps, CUDA events on the launching stream."""
+    import torch
+    from causal_scaled_dot_gb300 import native
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    native.load()
+    o_bits, w_bits, bias_np = proj_inputs(w)
+    E, K = w.Hq * w.D, w.Hq * w.D
+
+    def host(bits):
+        return torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).pin_memory()
+
+    oh, wh = host(o_bits), host(w_bits)
+    bh = torch.from_numpy(bias_np).pin_memory()
+    o, wt, bias = oh.to(dev), wh.to(dev), bh.to(dev)
+    y = torch.empty((w.B, w.S, E), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flops = 2.0 * w.B * w.S * E * K
+
+    def step():
+        native.attn_out_proj(o, wt, bias, y, w.B, w.Hq, w.S, w.D, E, stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize(dev)
+    native.attn_sync_status(stream)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    launches = 0
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            starts[i].record(stream)
+            step()
+            launches += 1
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - wall0
+    barrier(world)
+    native.attn_sync_status(stream)
+    ms_local = float(np.mean([a.elapsed_time(b) for a, b in zip(starts, ends)]))
+    ms = reduce_max(ms_local, world)
+    value = world * flops / (ms * 1e-3) / 1e12
+
+    yh = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        o.copy_(oh, non_blocking=True)
+        wt.copy_(wh, non_blocking=True)
+        bias.copy_(bh, non_blocking=True)
+        step()
+        yh.copy_(y, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = reduce_max(e0.elapsed_time(e1) / e2e_steps, world)
+    h2d = sum(t.numel() * t.element_size() for t in (oh, wh, bh))
+    d2h = yh.numel() * yh.element_size()
+
+    if rank != 0:
+        return 0
+    peaks, peak_src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    achieved = flops / (ms_local * 1e-3) / 1e12
+    io_bytes = o.numel() * 2 + wt.numel() * 2 + E * 4 + y.numel() * 2
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        timer = OracleProjTimer(w)
+        tf, n, dt = timer.sample(args.cpu_seconds, seed=7)
+        cpu = {"value": tf, "unit": "TFLOP/s", "cores": timer.threads, "kind": "oracle",
+               "sample": f"{n} random sequence positions of {w.name} (of {timer.total}, all batch "
+                         f"entries), {dt:.1f} s; float64 numpy matmul"}
+    line = {
+        "metric": PROJ_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 attention output, N(0, 1/(H*D)) weights; no trained weights)",
+        "config": {"workload": w.name, **w.shape_dict, "E": E, "inputs": "bf16", "pass": "proj",
+                   "l2": "flushed between timed steps (256 MiB write)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "pct_of_peak": 100.0 * achieved / peak,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": recorded_traffic(w.name + ":proj", PROJ_SOURCES),
+                     "peak_source": f"{peak_src} bf16 dense (burst)",
+                     "hbm_gbs": io_bytes / (ms_local * 1e-3) / 1e9},
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+        "wall_s_timed_region": wall,
+        "kernel_sources": kernel_source_hash(PROJ_SOURCES),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -618,8 +782,8 @@ def main():
     ap.add_argument("--workload", default=HEADLINE.name, choices=sorted(BY_NAME))
     ap.add_argument("--dtype", default="bf16", choices=["bf16", "fp8"],
                     help="input format: bf16 (attn_fwd) or E4M3 (attn_fwd_fp8, D = 128 only)")
-    ap.add_argument("--pass", dest="pass_", default="fwd", choices=["fwd", "bwd"],
-                    help="fwd: attn_fwd (default); bwd: attn_bwd (bf16)")
+    ap.add_argument("--pass", dest="pass_", default="fwd", choices=["fwd", "bwd", "proj"],
+                    help="fwd: attn_fwd (default); bwd: attn_bwd; proj: attn_out_proj (bf16)")
     ap.add_argument("--mask-density", type=float, default=None,
                     help="bf16 only: run attn_fwd_block_masked with a seeded per-head block mask "
                          "keeping each 128x128 block with this probability")
@@ -638,8 +802,8 @@ def main():
         ap.error("--warmup must be at least 3")
     if args.mask_density is not None and (args.dtype != "bf16" or not 0.0 <= args.mask_density <= 1.0):
         ap.error("--mask-density takes a probability in [0, 1] and bf16 inputs")
-    if args.pass_ == "bwd" and (args.dtype != "bf16" or args.mask_density is not None):
-        ap.error("--pass bwd takes bf16 inputs and no mask")
+    if args.pass_ in ("bwd", "proj") and (args.dtype != "bf16" or args.mask_density is not None):
+        ap.error("--pass bwd / proj take bf16 inputs and no mask")
     if args.dropout is not None and (args.pass_ != "fwd" or args.dtype != "bf16" or args.mask_density is not None
                                      or not 0 < round(args.dropout * 256) < 256):
         ap.error("--dropout takes 0 < p < 1 (at least 1/256), bf16 forward, no mask")
@@ -651,7 +815,8 @@ def main():
         if args.impl == "reference":
             rc = run_reference(args, w, rank, world)
         else:
-            rc = (run_ours_bwd if args.pass_ == "bwd" else run_ours)(args, w, rank, world, local)
+            rc = {"bwd": run_ours_bwd, "proj": run_ours_proj}.get(args.pass_, run_ours)(
+                args, w, rank, world, local)
     finally:
         if world > 1:
             import torch.distributed as dist

@@ -387,6 +387,11 @@ int encode_bf16_tiles(CUtensorMap* map, const void* ptr, int D, int S, long long
     return encode_bf16_3d(map, ptr, D, S, outer, kTile);
 }
 
+int encode_bf16_box(CUtensorMap* map, const void* ptr, int D, int S, long long outer, int box_rows) {
+    if (box_rows < 1 || box_rows > 256) return ATTN_ERR_INVALID_ARG;
+    return encode_bf16_3d(map, ptr, D, S, outer, box_rows);
+}
+
 bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
     return attn::ranges_overlap(a, na, b, nb);
 }

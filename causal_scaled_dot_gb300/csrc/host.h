@@ -17,6 +17,8 @@ int current_device(int* sm_count, unsigned int** status_word);
 // Rank-3 bf16 view [outer, S, D] of a contiguous tensor, box {64 elements,
 // 128 rows, 1}, 128-byte swizzle, rows past S read as zero.
 int encode_bf16_tiles(CUtensorMap* map, const void* ptr, int D, int S, long long outer);
+// The same view with a box of `box_rows` rows (at most 256).
+int encode_bf16_box(CUtensorMap* map, const void* ptr, int D, int S, long long outer, int box_rows);
 
 bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb);
 

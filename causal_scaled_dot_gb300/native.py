@@ -55,6 +55,8 @@ def load() -> ctypes.CDLL:
         lib.attn_fwd_dropout.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, ci, cf, u64, u64,
                                          vp]
         lib.attn_fwd_dropout.restype = ci
+        lib.attn_out_proj.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, ci, vp]
+        lib.attn_out_proj.restype = ci
         lib.attn_fwd_fp8.argtypes = [vp, vp, vp, cf, cf, cf, vp, vp, ci, ci, ci, ci, ci, cf, ci, vp]
         lib.attn_fwd_fp8.restype = ci
         lib.attn_sync_status.argtypes = [vp]
@@ -138,6 +140,16 @@ def attn_fwd_dropout(q, k, v, out, lse, B: int, Hq: int, Hkv: int, S: int, D: in
                                  _stream(stream))
     if check and rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_dropout")
+    return rc
+
+
+def attn_out_proj(out, w, bias, y, B: int, H: int, S: int, D: int, E: int, stream=None,
+                  check: bool = True) -> int:
+    """The C entry point ``attn_out_proj``: Y = concat_heads(O) W^T + bias."""
+    rc = load().attn_out_proj(_ptr(out), _ptr(w), _ptr(bias), _ptr(y), int(B), int(H), int(S), int(D),
+                              int(E), _stream(stream))
+    if check and rc != ATTN_OK:
+        raise AttnError(rc, "attn_out_proj")
     return rc
 
 

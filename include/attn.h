@@ -171,6 +171,26 @@ int attn_bwd(const void *q, const void *k, const void *v, const void *out, const
              int S, int D, float scale, int causal, void *stream);
 
 /*
+ * attn_out_proj -- the layer's output projection applied to attention's
+ * output where it lies (the "output projection" operator the ainews.cool
+ * article profiles right after attention, per-operator table):
+ *     Y[b, s, e] = sum_{h, d} O[b, h, s, d] * W[e, h*D + d] + bias[e],
+ * i.e. the heads of each position laid side by side, times W^T.
+ *
+ *   out    bf16 [B, H, S, D]: attn_fwd's output, read in place (no transpose).
+ *   w      bf16 [E, H*D], row-major (the weight of a linear layer with H*D
+ *          inputs and E outputs).
+ *   bias   fp32 [E], or NULL for none.
+ *   y      bf16 [B, S, E], written.
+ *   D      64 or 128; E a multiple of 8 (ATTN_ERR_UNSUPPORTED otherwise).
+ * out, w and y 16-byte aligned, bias 4-byte aligned; y may overlap nothing
+ * else.  fp32 accumulation, one rounding to bf16 at the end.  One kernel on
+ * `stream`, asynchronous; allocates nothing.  Errors as attn_fwd.
+ */
+int attn_out_proj(const void *out, const void *w, const float *bias, void *y, int B, int H, int S,
+                  int D, int E, void *stream);
+
+/*
  * attn_sync_status -- synchronise `stream` and report device-side failures of
  * the attention kernels enqueued on this device since the last call.
  *

@@ -305,3 +305,28 @@ def philox4x64(ctr, key, lib: ctypes.CDLL | None = None) -> np.ndarray:
     out = np.empty(4, dtype=np.uint64)
     lib.oracle_philox4x64(c.ctypes.data, k.ctypes.data, out.ctypes.data)
     return out
+
+
+def out_proj(o, w, bias=None) -> np.ndarray:
+    """The attention output projection, in float64: Y[b, s, e] = sum over
+    k = h*D + d of O[b, h, s, d] * W[e, k] (+ bias[e]).
+
+    o: [B, H, S, D] and w: [E, H*D] as bf16 bit patterns (uint16) or floats;
+    bias: [E] or None.  Written as its definition -- the heads of each position
+    laid side by side into one H*D row (the concatenation that precedes the
+    projection), times W^T -- with numpy's float64 matmul as the one library step.
+    """
+    def wide(x):
+        x = np.asarray(x)
+        if x.dtype == np.uint16:
+            return (x.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+        return x.astype(np.float64)
+    O, W = wide(o), wide(w)
+    B, H, S, D = O.shape
+    if W.ndim != 2 or W.shape[1] != H * D:
+        raise ValueError("w must be [E, H*D]")
+    rows = O.transpose(0, 2, 1, 3).reshape(B, S, H * D)  # [b, s, h*D + d]
+    Y = rows @ W.T
+    if bias is not None:
+        Y = Y + np.asarray(bias, dtype=np.float64)
+    return Y

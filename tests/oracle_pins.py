@@ -580,3 +580,40 @@ def pin_dropout_rate_and_identity(attnd, attn):
 
 
 DROPOUT_PINS = [pin_dropout_mask_closed_form, pin_dropout_rate_and_identity]
+
+
+# ---------------------------------------------------------------- output projection
+# ``proj(o, w, bias)`` -> Y [B, S, E] float64.
+
+def pin_proj_library(proj):
+    """Against torch's float64 linear on the concatenated heads (torch.cat of the
+    per-head outputs along the feature axis, the form the pages' layer uses)."""
+    B, H, S, D, E = 2, 3, 20, 16, 40
+    o = _rand((B, H, S, D), 221, 0)
+    w = _rand((E, H * D), 221, 1)
+    bias = np.random.default_rng(221).standard_normal(E)
+    Y = proj(o, w, bias)
+    heads = [torch.from_numpy(f64(o[:, h])) for h in range(H)]       # [B, S, D] each
+    cat = torch.cat(heads, dim=-1)                                     # [B, S, H*D]
+    ref = F.linear(cat, torch.from_numpy(f64(w)), torch.from_numpy(bias)).numpy()
+    assert np.max(np.abs(Y - ref)) < 1e-12
+
+
+def pin_proj_selection(proj):
+    """W picking one input feature per output (W[e, h*D + d] = 1): Y[b, s, e] is
+    exactly O[b, h, s, d]; with O = 0 the output is the bias."""
+    B, H, S, D = 1, 4, 9, 8
+    o = _rand((B, H, S, D), 231, 0)
+    picks = [(3, 5), (0, 0), (2, 7), (1, 2), (3, 0), (0, 6), (2, 2), (1, 7)]
+    w = np.zeros((len(picks), H * D), dtype=np.float32)
+    for e, (h, d) in enumerate(picks):
+        w[e, h * D + d] = 1.0
+    Y = proj(o, bits(w), None)
+    for e, (h, d) in enumerate(picks):
+        assert np.array_equal(Y[0, :, e], f64(o[0, h, :, d]))
+    bias = np.arange(len(picks), dtype=np.float64) - 2.5
+    Yb = proj(bits(np.zeros((B, H, S, D))), bits(w), bias)
+    assert np.array_equal(Yb, np.broadcast_to(bias, Yb.shape))
+
+
+PROJ_PINS = [pin_proj_library, pin_proj_selection]

@@ -28,7 +28,7 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for required in ("attn_fwd", "attn_fwd_fp8", "attn_fwd_block_masked", "attn_fwd_dropout",
-                     "attn_bwd", "attn_status_string", "attn_sync_status"):
+                     "attn_bwd", "attn_out_proj", "attn_status_string", "attn_sync_status"):
         assert required in names
 
 
@@ -208,3 +208,25 @@ def _call_dropout(p=0.1, q=1 << 40, k=2 << 40, v=3 << 40, out=4 << 40, lse=None,
 ])
 def test_dropout_argument_errors_are_rejected_before_launch(kw, code):
     assert _call_dropout(**kw) == code
+
+
+def _call_proj(out=1 << 40, w=2 << 40, bias=None, y=3 << 40, B=1, H=4, S=300, D=128, E=512):
+    lib = native.load()
+    return lib.attn_out_proj(out, w, bias, y, B, H, S, D, E, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(out=None), ATTN_ERR_INVALID_ARG),
+    (dict(w=None), ATTN_ERR_INVALID_ARG),
+    (dict(y=None), ATTN_ERR_INVALID_ARG),
+    (dict(E=0), ATTN_ERR_INVALID_ARG),
+    (dict(S=0), ATTN_ERR_INVALID_ARG),
+    (dict(E=12), ATTN_ERR_UNSUPPORTED),
+    (dict(D=32), ATTN_ERR_UNSUPPORTED),
+    (dict(w=(2 << 40) + 8), ATTN_ERR_MISALIGNED),
+    (dict(bias=(4 << 40) + 2), ATTN_ERR_MISALIGNED),
+    (dict(y=(1 << 40) + 4096), ATTN_ERR_INVALID_ARG),   # y overlaps out
+    (dict(y=(2 << 40)), ATTN_ERR_INVALID_ARG),          # y is w
+])
+def test_proj_argument_errors_are_rejected_before_launch(kw, code):
+    assert _call_proj(**kw) == code

@@ -65,6 +65,52 @@ def test_oracle_dropout_pin(pin):
     pin(_attnd, _attn)
 
 
+@pytest.mark.parametrize("pin", oracle_pins.PROJ_PINS, ids=lambda p: p.__name__)
+def test_oracle_proj_pin(pin):
+    pin(oracle.out_proj)
+
+
+def test_proj_pins_catch_planted_mistakes():
+    """Plausible slips in the projection's index mapping or bias: some pin fails for each."""
+    import numpy as _np
+
+    def wide(x):
+        x = _np.asarray(x)
+        return (x.astype(_np.uint32) << _np.uint32(16)).view(_np.float32).astype(_np.float64) \
+            if x.dtype == _np.uint16 else x.astype(_np.float64)
+
+    def heads_major(o, w, bias=None):      # k = d*H + h instead of h*D + d
+        O, W = wide(o), wide(w)
+        B, H, S, D = O.shape
+        Y = O.transpose(0, 2, 3, 1).reshape(B, S, H * D) @ W.T
+        return Y + (0 if bias is None else _np.asarray(bias))
+
+    def w_transposed(o, w, bias=None):     # W read as [H*D, E] memory
+        O, W = wide(o), wide(w)
+        B, H, S, D = O.shape
+        Wt = W.reshape(-1).reshape(W.shape[1], W.shape[0]).T
+        Y = O.transpose(0, 2, 1, 3).reshape(B, S, H * D) @ Wt.T
+        return Y + (0 if bias is None else _np.asarray(bias))
+
+    def bias_dropped(o, w, bias=None):
+        return oracle.out_proj(o, w, None)
+
+    def seq_head_swapped(o, w, bias=None):  # O read as [B, S, H, D]
+        O, W = wide(o), wide(w)
+        B, H, S, D = O.shape
+        Y = O.reshape(B, S, H * D) @ W.T
+        return Y + (0 if bias is None else _np.asarray(bias))
+
+    for mutant in (heads_major, w_transposed, bias_dropped, seq_head_swapped):
+        caught = 0
+        for pin in oracle_pins.PROJ_PINS:
+            try:
+                pin(mutant)
+            except (AssertionError, ValueError):
+                caught += 1
+        assert caught, mutant.__name__
+
+
 def test_rows_subset_matches_full():
     """The row-selection entry computes exactly the rows of the full call."""
     from causal_scaled_dot_gb300.inputs import qkv_bf16
