@@ -57,8 +57,10 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-# The sources that make the timed kernels and their launch, per pass.
-FWD_SOURCES = ("attn_api.cu", "common.cuh", "kernel_ws.cuh", "ptx.cuh")
+# The sources of the timed kernels, per pass (the forward's launch geometry --
+# one CTA per SM, 384 threads -- is fixed in attn_api.cu; re-take the record if
+# it changes).
+FWD_SOURCES = ("common.cuh", "kernel_ws.cuh", "philox.cuh", "ptx.cuh")
 BWD_SOURCES = ("attn_bwd.cu", "common.cuh", "kernel_bwd.cuh", "ptx.cuh")
 PROJ_SOURCES = ("attn_proj.cu", "common.cuh", "kernel_proj.cuh", "ptx.cuh")
 
