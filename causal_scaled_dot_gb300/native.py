@@ -84,6 +84,8 @@ def _ptr(x):
     if isinstance(x, torch.Tensor):
         if not x.is_cuda:
             raise ValueError("tensor arguments must live in CUDA device memory")
+        if not x.is_contiguous():
+            raise ValueError("tensor arguments must be contiguous (the C ABI takes dense layouts)")
         return x.data_ptr()
     raise TypeError(f"expected a CUDA tensor, an int pointer or None, got {type(x)!r}")
 

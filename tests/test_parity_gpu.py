@@ -180,3 +180,12 @@ def test_bounded_wait_reports_timeout_and_device_stays_usable():
     assert native.attn_sync_status(check=False) == native.ATTN_ERR_TIMEOUT
     assert native.attn_sync_status(check=False) == native.ATTN_OK  # cleared by the read
     test_small_workload_all_rows()
+
+
+def test_binding_rejects_non_contiguous_tensors():
+    import torch
+    from causal_scaled_dot_gb300 import native
+    q = torch.zeros((1, 2, 128, 64), dtype=torch.bfloat16, device="cuda")
+    qt = q.transpose(2, 3)
+    with pytest.raises(ValueError):
+        native.attn_fwd(qt, q, q, torch.empty_like(q), None, 1, 2, 2, 128, 64, 0.125, True)
