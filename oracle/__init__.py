@@ -68,6 +68,10 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     f = lib.oracle_attn_rows_f64
     f.restype = ci
     f.argtypes = [vp, vp, vp, ci, ci, ci, ci, ci, cf, ci, vp, ctypes.c_int64, vp, vp, ci]
+    f = lib.oracle_attn_bwd_masked
+    f.restype = ci
+    f.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, vp, ci, vp, ctypes.c_int64, vp, vp,
+                  vp, vp, ci]
     f = lib.oracle_attn_rows_dropout
     f.restype = ci
     f.argtypes = [vp, vp, vp, ci, ci, ci, ci, ci, cf, ci, ci, ctypes.c_uint64, ctypes.c_uint64, vp,
@@ -240,7 +244,7 @@ def attention_f64(q, k, v, scale: float, causal: bool = True, nthreads: int | No
 
 
 def attention_bwd(q, k, v, dout, scale: float, causal: bool = True, kv_heads=None,
-                  nthreads: int | None = None, lib: ctypes.CDLL | None = None):
+                  nthreads: int | None = None, lib: ctypes.CDLL | None = None, block_mask=None):
     """Gradients of the attention output: (dQ, dK, dV, delta) in float64.
 
     q, dout: [B,Hq,S,D]; k, v: [B,Hkv,S,D]; either all bf16 bit patterns
@@ -249,6 +253,7 @@ def attention_bwd(q, k, v, dout, scale: float, causal: bool = True, kv_heads=Non
     shapes [n, G, S, D] and [n, G, S], and dK, dV are [n, S, D].  Without
     kv_heads: dQ [B,Hq,S,D], dK and dV [B,Hkv,S,D], delta [B,Hq,S].
     delta_i = sum_j P_ij (dO_i . V_j), the row term of the softmax gradient.
+    block_mask: optional uint8 [1 or Hq, nt, nt] as in ``attention_masked``.
     """
     lib = lib or load()
     f64 = np.asarray(q).dtype == np.float64
@@ -267,11 +272,18 @@ def attention_bwd(q, k, v, dout, scale: float, causal: bool = True, kv_heads=Non
         dq_shape, kv_shape, d_shape = (n, G, S, D), (n, S, D), (n, G, S)
     dq, dk, dv = np.empty(dq_shape), np.empty(kv_shape), np.empty(kv_shape)
     delta = np.empty(d_shape)
-    rc = lib.oracle_attn_bwd(q.ctypes.data, k.ctypes.data, v.ctypes.data, dout.ctypes.data,
-                             1 if f64 else 0, B, Hq, Hkv, S, D, ctypes.c_float(scale),
-                             1 if causal else 0, None if heads is None else heads.ctypes.data, n,
-                             dq.ctypes.data, dk.ctypes.data, dv.ctypes.data, delta.ctypes.data,
-                             nthreads or default_threads())
+    common = (q.ctypes.data, k.ctypes.data, v.ctypes.data, dout.ctypes.data, 1 if f64 else 0, B, Hq,
+              Hkv, S, D, ctypes.c_float(scale), 1 if causal else 0)
+    tail = (None if heads is None else heads.ctypes.data, n, dq.ctypes.data, dk.ctypes.data,
+            dv.ctypes.data, delta.ctypes.data, nthreads or default_threads())
+    if block_mask is None:
+        rc = lib.oracle_attn_bwd(*common, *tail)
+    else:
+        m = np.ascontiguousarray(block_mask, dtype=np.uint8)
+        nt = (S + 127) // 128
+        if m.ndim != 3 or m.shape[1:] != (nt, nt) or m.shape[0] not in (1, Hq):
+            raise ValueError(f"block_mask must be [1 or Hq, {nt}, {nt}]")
+        rc = lib.oracle_attn_bwd_masked(*common, m.ctypes.data, m.shape[0], *tail)
     if rc != 0:
         raise ValueError("oracle_attn_bwd rejected its arguments")
     return dq, dk, dv, delta

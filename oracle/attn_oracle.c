@@ -528,10 +528,11 @@ static int bwd_parallel(const bwd_job_t *proto, int pass, int64_t count, int nth
  *   dk, dv: double [n_kv_heads][S][D];  delta: double [n_kv_heads][G][S].
  * Returns 0 on success, 1 on a bad argument or allocation failure.
  */
-int oracle_attn_bwd(const void *q, const void *k, const void *v, const void *dout, int f64_inputs,
-                    int B, int Hq, int Hkv, int S, int D, float scale, int causal,
-                    const int64_t *kv_heads, int64_t n_kv_heads, double *dq, double *dk,
-                    double *dv, double *delta, int nthreads) {
+static int bwd_run(const void *q, const void *k, const void *v, const void *dout, int f64_inputs,
+                   int B, int Hq, int Hkv, int S, int D, float scale, int causal,
+                   const uint8_t *block_mask, int mask_heads, const int64_t *kv_heads,
+                   int64_t n_kv_heads, double *dq, double *dk, double *dv, double *delta,
+                   int nthreads) {
     if (!q || !k || !v || !dout || !dq || !dk || !dv || !delta) return 1;
     if (B < 1 || Hq < 1 || Hkv < 1 || S < 1 || D < 1 || Hq % Hkv != 0) return 1;
     if (!kv_heads && n_kv_heads != (int64_t)B * Hkv) return 1;
@@ -546,7 +547,9 @@ int oracle_attn_bwd(const void *q, const void *k, const void *v, const void *dou
     J.B = B; J.Hq = Hq; J.Hkv = Hkv; J.S = S; J.D = D;
     J.scale = (double)scale;
     J.causal = causal ? 1 : 0;
-    J.mask_heads = 1;
+    if (block_mask && mask_heads != 1 && mask_heads != Hq) return 1;
+    J.block_mask = block_mask;
+    J.mask_heads = block_mask ? mask_heads : 1;
     const int64_t G = Hq / Hkv;
     double *P = (double *)malloc(sizeof(double) * (size_t)(G * S) * (size_t)S);
     double *dS = (double *)malloc(sizeof(double) * (size_t)(G * S) * (size_t)S);
@@ -596,4 +599,28 @@ int oracle_attn_rows_dropout(const uint16_t *q, const uint16_t *k, const uint16_
 /* Philox4x64-10 of one counter block (exposed so the generator can be pinned). */
 void oracle_philox4x64(const uint64_t *ctr, const uint64_t *key, uint64_t *out) {
     philox4x64_10(ctr, key, out);
+}
+
+int oracle_attn_bwd(const void *q, const void *k, const void *v, const void *dout, int f64_inputs,
+                    int B, int Hq, int Hkv, int S, int D, float scale, int causal,
+                    const int64_t *kv_heads, int64_t n_kv_heads, double *dq, double *dk,
+                    double *dv, double *delta, int nthreads) {
+    return bwd_run(q, k, v, dout, f64_inputs, B, Hq, Hkv, S, D, scale, causal, NULL, 1, kv_heads,
+                   n_kv_heads, dq, dk, dv, delta, nthreads);
+}
+
+/*
+ * oracle_attn_bwd_masked -- oracle_attn_bwd for the block-masked attention
+ * (the weights of steps 1-4 include the block mask, so the same derivative
+ * applies; a row without any visible key has all weights 0, hence dQ = 0 for
+ * it and no contribution to dK or dV).
+ */
+int oracle_attn_bwd_masked(const void *q, const void *k, const void *v, const void *dout,
+                           int f64_inputs, int B, int Hq, int Hkv, int S, int D, float scale,
+                           int causal, const uint8_t *block_mask, int mask_heads,
+                           const int64_t *kv_heads, int64_t n_kv_heads, double *dq, double *dk,
+                           double *dv, double *delta, int nthreads) {
+    if (!block_mask) return 1;
+    return bwd_run(q, k, v, dout, f64_inputs, B, Hq, Hkv, S, D, scale, causal, block_mask,
+                   mask_heads, kv_heads, n_kv_heads, dq, dk, dv, delta, nthreads);
 }

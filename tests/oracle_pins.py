@@ -503,6 +503,7 @@ def pin_bwd_invariants(bwd):
 
 
 BWD_PINS = [pin_bwd_torch_autograd, pin_bwd_closed_forms, pin_bwd_invariants]
+# (the block-masked gradient pins are defined below; see BWD_MASK_PINS)
 
 
 # ---------------------------------------------------------------- dropout
@@ -617,3 +618,43 @@ def pin_proj_selection(proj):
 
 
 PROJ_PINS = [pin_proj_library, pin_proj_selection]
+
+
+def pin_bwd_masked_library(bwdm):
+    """Block-masked gradients against torch's float64 autograd through SDPA with the
+    expanded boolean mask; a query tile that sees no key has zero gradients on
+    both sides (torch's safe softmax)."""
+    B, Hq, Hkv, S, D = 1, 4, 2, 300, 8
+    q, k, v = (_rand((B, H, S, D), 241, t) for t, H in ((0, Hq), (1, Hkv), (2, Hkv)))
+    dout = _rand((B, Hq, S, D), 241, 3)
+    rng = np.random.default_rng(241)
+    nt = 3
+    G = Hq // Hkv
+    for hm, causal in ((Hq, True), (1, False), (Hq, False)):
+        mask = (rng.random((hm, nt, nt)) < 0.7).astype(np.uint8)
+        mask[0, 2, :] = 0
+        dq, dk, dv, _ = bwdm(q, k, v, dout, 0.5, causal, mask)
+        allowed = _expand_block_mask(mask, Hq, S, causal)  # [Hq, S, S], True = visible
+        tq, tk, tv = (torch.from_numpy(f64(x)).requires_grad_() for x in (q, k, v))
+        o = F.scaled_dot_product_attention(tq, tk.repeat_interleave(G, 1), tv.repeat_interleave(G, 1),
+                                           attn_mask=allowed[None], scale=float(np.float32(0.5)))
+        o.backward(torch.from_numpy(f64(dout)))
+        for name, a, t in (("dQ", dq, tq), ("dK", dk, tk), ("dV", dv, tv)):
+            ref = t.grad.numpy()
+            assert not np.isnan(ref).any()
+            assert np.max(np.abs(a - ref)) <= 1e-12 * max(1.0, float(np.max(np.abs(ref)))), name
+        assert np.all(dq[0, 0, 256:] == 0.0)
+
+
+def pin_bwd_masked_all_ones(bwdm, bwd):
+    """The all-ones block mask gives the unmasked gradients bit for bit."""
+    B, H, S, D = 1, 2, 200, 8
+    q, k, v = (_rand((B, H, S, D), 251, t) for t in range(3))
+    dout = _rand((B, H, S, D), 251, 3)
+    for causal in (True, False):
+        a = bwdm(q, k, v, dout, 0.3, causal, np.ones((1, 2, 2), np.uint8))
+        b = bwd(q, k, v, dout, 0.3, causal)
+        assert all(np.array_equal(x, y) for x, y in zip(a, b))
+
+
+BWD_MASK_PINS = [pin_bwd_masked_library]

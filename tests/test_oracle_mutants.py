@@ -104,7 +104,10 @@ def test_some_pin_catches_mutant(name, tmp_path):
     ] + [(p.__name__, lambda p=p: p(bwd)) for p in oracle_pins.BWD_PINS] + [
         ("pin_philox_library", lambda: oracle_pins.pin_philox_library(
             lambda c, k: oracle.philox4x64(c, k, lib=lib))),
-    ] + [(p.__name__, lambda p=p: p(attnd, attn)) for p in oracle_pins.DROPOUT_PINS]
+    ] + [(p.__name__, lambda p=p: p(attnd, attn)) for p in oracle_pins.DROPOUT_PINS] + [
+        ("pin_bwd_masked_library", lambda: oracle_pins.pin_bwd_masked_library(
+            lambda q, k, v, d, sc, c, m: oracle.attention_bwd(q, k, v, d, sc, c, block_mask=m, lib=lib))),
+    ]
     caught = []
     for pin_name, run in checks:
         try:

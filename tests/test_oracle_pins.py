@@ -43,6 +43,15 @@ def test_oracle_bwd_pin(pin):
     pin(_bwd)
 
 
+def _bwdm(q, k, v, dout, scale, causal, mask, kv_heads=None):
+    return oracle.attention_bwd(q, k, v, dout, scale, causal, kv_heads=kv_heads, block_mask=mask)
+
+
+def test_oracle_bwd_masked_pins():
+    oracle_pins.pin_bwd_masked_library(_bwdm)
+    oracle_pins.pin_bwd_masked_all_ones(_bwdm, _bwd)
+
+
 def test_oracle_bwd_thread_count_does_not_change_bits():
     from causal_scaled_dot_gb300.inputs import gaussian_bf16, qkv_bf16
     q, k, v = qkv_bf16(1, 4, 2, 50, 8, seed=10)
