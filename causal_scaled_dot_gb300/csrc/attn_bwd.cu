@@ -33,10 +33,14 @@ int setup_bwd_kernels() {
     std::lock_guard<std::mutex> lock(g_bwd_mutex);
     if (g_bwd_ready[dev] == 0) {
         const bool ok =
-            allow_smem(attn_bwd_dq_kernel<64>, DqLayout<64>::kDynamicSmem) == cudaSuccess &&
-            allow_smem(attn_bwd_dq_kernel<128>, DqLayout<128>::kDynamicSmem) == cudaSuccess &&
-            allow_smem(attn_bwd_dkdv_kernel<64>, DkvLayout<64>::kDynamicSmem) == cudaSuccess &&
-            allow_smem(attn_bwd_dkdv_kernel<128>, DkvLayout<128>::kDynamicSmem) == cudaSuccess;
+            allow_smem(attn_bwd_dq_kernel<64, false>, DqLayout<64>::kDynamicSmem) == cudaSuccess &&
+            allow_smem(attn_bwd_dq_kernel<128, false>, DqLayout<128>::kDynamicSmem) == cudaSuccess &&
+            allow_smem(attn_bwd_dkdv_kernel<64, false>, DkvLayout<64>::kDynamicSmem) == cudaSuccess &&
+            allow_smem(attn_bwd_dkdv_kernel<128, false>, DkvLayout<128>::kDynamicSmem) == cudaSuccess &&
+            allow_smem(attn_bwd_dq_kernel<64, true>, DqLayout<64>::kDynamicSmem) == cudaSuccess &&
+            allow_smem(attn_bwd_dq_kernel<128, true>, DqLayout<128>::kDynamicSmem) == cudaSuccess &&
+            allow_smem(attn_bwd_dkdv_kernel<64, true>, DkvLayout<64>::kDynamicSmem) == cudaSuccess &&
+            allow_smem(attn_bwd_dkdv_kernel<128, true>, DkvLayout<128>::kDynamicSmem) == cudaSuccess;
         g_bwd_ready[dev] = ok ? 1 : ATTN_ERR_DEVICE;
     }
     return g_bwd_ready[dev] == 1 ? ATTN_OK : g_bwd_ready[dev];
@@ -72,7 +76,7 @@ int check_bwd_args(const void* q, const void* k, const void* v, const void* out,
     return ATTN_OK;
 }
 
-template <int D>
+template <int D, bool M>
 int launch_bwd(const CUtensorMap& tq, const CUtensorMap& tdo, const CUtensorMap& tk,
                const CUtensorMap& tv, BwdParams p, int sm_count, cudaStream_t stream) {
     const long long dq_units = (long long)p.B * p.Hq * p.num_tiles;
@@ -83,14 +87,18 @@ int launch_bwd(const CUtensorMap& tq, const CUtensorMap& tdo, const CUtensorMap&
     // About eight units per CTA per head block: nearly the balance of a single
     // tile-major order, with half or less of the heads' operands live in L2.
     p.head_block = std::min(p.B * p.Hq, (8 * grid + p.num_tiles - 1) / p.num_tiles);
-    attn_bwd_dq_kernel<D><<<grid, DqLayout<D>::kThreads, DqLayout<D>::kDynamicSmem, stream>>>(tq, tdo, tk, tv, p);
+    attn_bwd_dq_kernel<D, M><<<grid, DqLayout<D>::kThreads, DqLayout<D>::kDynamicSmem, stream>>>(tq, tdo, tk, tv, p);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
     p.num_units = (int)dkv_units;
     grid = (int)(dkv_units < sm_count ? dkv_units : sm_count);
     p.head_block = std::min(p.B * p.Hkv, (8 * grid + p.num_tiles - 1) / p.num_tiles);
-    attn_bwd_dkdv_kernel<D><<<grid, DkvLayout<D>::kThreads, DkvLayout<D>::kDynamicSmem, stream>>>(tq, tdo, tk, tv, p);
+    attn_bwd_dkdv_kernel<D, M><<<grid, DkvLayout<D>::kThreads, DkvLayout<D>::kDynamicSmem, stream>>>(tq, tdo, tk, tv, p);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
+
+int bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
+        const float* lse, float* delta, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int S,
+        int D, float scale, int causal, const uint8_t* block_mask, int mask_heads, void* stream);
 
 }  // namespace
 }  // namespace attn
@@ -100,6 +108,26 @@ using namespace attn;
 extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
                         const float* lse, float* delta, void* dq, void* dk, void* dv, int B, int Hq,
                         int Hkv, int S, int D, float scale, int causal, void* stream) {
+    return attn::bwd(q, k, v, out, dout, lse, delta, dq, dk, dv, B, Hq, Hkv, S, D, scale, causal,
+                     nullptr, 1, stream);
+}
+
+extern "C" int attn_bwd_block_masked(const void* q, const void* k, const void* v, const void* out,
+                                     const void* dout, const float* lse, float* delta, void* dq,
+                                     void* dk, void* dv, int B, int Hq, int Hkv, int S, int D,
+                                     float scale, int causal, const unsigned char* block_mask,
+                                     int mask_heads, void* stream) {
+    if (block_mask == nullptr || (mask_heads != 1 && mask_heads != Hq)) return ATTN_ERR_INVALID_ARG;
+    return attn::bwd(q, k, v, out, dout, lse, delta, dq, dk, dv, B, Hq, Hkv, S, D, scale, causal,
+                     block_mask, mask_heads, stream);
+}
+
+namespace attn {
+namespace {
+
+int bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
+        const float* lse, float* delta, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int S,
+        int D, float scale, int causal, const uint8_t* block_mask, int mask_heads, void* stream) {
     int rc = check_bwd_args(q, k, v, out, dout, lse, delta, dq, dk, dv, B, Hq, Hkv, S, D, scale);
     if (rc != ATTN_OK) return rc;
     int sm_count = 0;
@@ -135,7 +163,15 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
     p.dv = static_cast<__nv_bfloat16*>(dv);
     p.status = status;
     p.wait_limit_ns = host::wait_limit_ns();
+    p.block_mask = block_mask;
+    p.mask_heads = mask_heads;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    return D == 64 ? launch_bwd<64>(tq, tdo, tk, tv, p, sm_count, st)
-                   : launch_bwd<128>(tq, tdo, tk, tv, p, sm_count, st);
+    if (block_mask != nullptr)
+        return D == 64 ? launch_bwd<64, true>(tq, tdo, tk, tv, p, sm_count, st)
+                       : launch_bwd<128, true>(tq, tdo, tk, tv, p, sm_count, st);
+    return D == 64 ? launch_bwd<64, false>(tq, tdo, tk, tv, p, sm_count, st)
+                   : launch_bwd<128, false>(tq, tdo, tk, tv, p, sm_count, st);
 }
+
+}  // namespace
+}  // namespace attn

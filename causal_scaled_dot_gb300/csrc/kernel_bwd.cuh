@@ -68,7 +68,16 @@ struct BwdParams {
     unsigned long long wait_limit_ns;
     int num_units;
     int head_block;  // heads worked on together (see split_unit)
+    const uint8_t* block_mask;  // masked kernels: [mask_heads][nt][nt], 0 drops a (query, key) tile
+    int mask_heads;             // 1 or Hq
 };
+
+// Block mask entry of (query head bh, query tile qt, key tile kt).
+__device__ __forceinline__ bool bwd_tile_kept(const BwdParams& p, int bh, int qt, int kt) {
+    const int nt = p.num_tiles;
+    const int h = p.mask_heads == 1 ? 0 : bh % p.Hq;
+    return __ldg(p.block_mask + ((size_t)h * nt + qt) * nt + kt) != 0;
+}
 
 // Units are (head, tile) pairs.  Heads are taken `head_block` at a time, about
 // one tile of each head per CTA, so the CTAs running together share the
@@ -124,8 +133,9 @@ struct DqLayout {
     static constexpr int kQFull = 0, kQEmpty = 1, kSFull = 2, kDPFull = 3, kSFree = 4, kDSFull = 5,
                          kDQFull = 6, kKVFull = 7, kKVEmpty = 7 + kStages, kStatFull = 7 + 2 * kStages,
                          kStatEmpty = 7 + 2 * kStages + kStatStages,
-                         kDrain = 7 + 2 * kStages + 2 * kStatStages;
-    static constexpr int kNumBars = kDrain + 1;
+                         kDrain = 7 + 2 * kStages + 2 * kStatStages,
+                         kDQEmpty = kDrain + 1;  // block-masked kernels: dQ read out
+    static constexpr int kNumBars = kDrain + 2;
     static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8;
     static constexpr uint32_t kAbort = kTmemSlot + 4;
     static constexpr uint32_t kDynamicSmem = kAbort + 4 + 1024;
@@ -146,12 +156,21 @@ __device__ __forceinline__ DqUnit dq_decode(int u, const BwdParams& p) {
     return w;
 }
 
+// The key tile after j that query tile w.qt uses (w.n if none): every tile
+// below the causal bound, or with a block mask (M) the kept ones.
+template <bool M>
+__device__ __forceinline__ int dq_next_key(const BwdParams& p, const DqUnit& w, int j) {
+    for (++j; j < w.n; ++j)
+        if (!M || bwd_tile_kept(p, w.bh, w.qt, j)) return j;
+    return w.n;
+}
+
 template <int D>
 __device__ __forceinline__ uint32_t dq_bar(uint32_t base, int i) {
     return base + DqLayout<D>::kBars + 8u * (uint32_t)i;
 }
 
-template <int D>
+template <int D, bool M>
 __device__ void dq_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_do,
                              const CUtensorMap* tm_k, const CUtensorMap* tm_v, const BwdParams& p,
                              uint32_t base, volatile int* abort_flag) {
@@ -201,9 +220,11 @@ __device__ void dq_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_do,
             pend_q_par = qe_phase;
             qe_phase ^= 1u;
         }
-        for (int j = 0; j < w.n; ++j) {
-            prefetch(ahead);
-            advance(ahead);
+        for (int j = dq_next_key<M>(p, w, -1); j < w.n; j = dq_next_key<M>(p, w, j)) {
+            if constexpr (!M) {
+                prefetch(ahead);
+                advance(ahead);
+            }
 #pragma unroll
             for (int t = 0; t < 2; ++t) {  // K_j, then V_j
                 if (!ptx::mbar_wait(dq_bar<D>(base, L::kKVEmpty + slot), ring_phase ^ 1u, abort_flag,
@@ -233,13 +254,18 @@ drain:
     if (pend_q) ptx::drain_wait(dq_bar<D>(base, L::kQFull), pend_q_par, lim);
 }
 
-template <int D>
+template <int D, bool M>
 __device__ void dq_mma_role(const BwdParams& p, uint32_t base, uint32_t tmem, volatile int* abort_flag) {
     using L = DqLayout<D>;
     constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(kTile, kTile, false);  // S, dP: N = 128 keys
     constexpr uint32_t kIdescQ = ptx::idesc_bf16_f32(kTile, D, true);       // dQ: N = D, K MN-major
     const uint64_t lim = p.wait_limit_ns;
     uint32_t qf_phase = 0, sfree_phase = 0, ds_phase = 0, ring_phase = 0;
+    // Block-masked kernels: a unit without key tiles makes no handshake with the
+    // element-wise warps, so before dQ of a unit is produced (or declared zero)
+    // the previous unit's dQ must have been read out -- otherwise the DQFull
+    // barrier could run two phases ahead of its waiters.
+    uint32_t dqe_phase = 1u;
     int slot = 0;
 
     auto wait_ring = [&](int& got) -> bool {
@@ -274,22 +300,31 @@ __device__ void dq_mma_role(const BwdParams& p, uint32_t base, uint32_t tmem, vo
     for (int rnd = 0, u = bwd_unit_of_round(0); u < p.num_units && ok; u = bwd_unit_of_round(++rnd)) {
         const DqUnit w = dq_decode(u, p);
         if (!wait_bar(L::kQFull, qf_phase)) break;
+        const int j0 = dq_next_key<M>(p, w, -1);
+        if (M && j0 >= w.n) {  // no key tile kept: dQ is 0 (written by the element-wise warps)
+            if (!wait_bar(L::kDQEmpty, dqe_phase)) break;
+            ptx::mma_commit(dq_bar<D>(base, L::kQEmpty));
+            ptx::mma_commit(dq_bar<D>(base, L::kDQFull));
+            continue;
+        }
         int ks, vs;
         if (!wait_ring(ks)) break;
-        product(tmem, base + L::kQ, slot_addr(ks));  // S = Q K_0^T
+        product(tmem, base + L::kQ, slot_addr(ks));  // S = Q K_j0^T
         ptx::mma_commit(dq_bar<D>(base, L::kSFull));
         if (!wait_ring(vs)) break;
-        product(tmem + 128u, base + L::kDO, slot_addr(vs));  // dP = dO V_0^T
+        product(tmem + 128u, base + L::kDO, slot_addr(vs));  // dP = dO V_j0^T
         ptx::mma_commit(dq_bar<D>(base, L::kDPFull));
         ptx::mma_commit(dq_bar<D>(base, L::kKVEmpty + vs));
         // Q and dO are read only by S and dP: free them for the next unit as
         // soon as the last of those has been issued.
-        if (w.n == 1) ptx::mma_commit(dq_bar<D>(base, L::kQEmpty));
-        for (int j = 0; j < w.n; ++j) {
+        if (dq_next_key<M>(p, w, j0) >= w.n) ptx::mma_commit(dq_bar<D>(base, L::kQEmpty));
+        bool first = true;
+        for (int j = j0, jn; j < w.n; j = jn, first = false) {
+            jn = dq_next_key<M>(p, w, j);
             // S_j has been read: the next S may overwrite it.
             if (!(ok = wait_bar(L::kSFree, sfree_phase))) break;
             int ks_next = -1;
-            if (j + 1 < w.n) {
+            if (jn < w.n) {
                 if (!(ok = wait_ring(ks_next))) break;
                 product(tmem, base + L::kQ, slot_addr(ks_next));
                 ptx::mma_commit(dq_bar<D>(base, L::kSFull));
@@ -297,16 +332,17 @@ __device__ void dq_mma_role(const BwdParams& p, uint32_t base, uint32_t tmem, vo
             // dQ += dS_j K_j: dS of keys 0-63 in columns [128,160), keys 64-127 in
             // [192,224); K_j as an MN-major operand, keys 64-127 8 KB further in.
             if (!(ok = wait_bar(L::kDSFull, ds_phase))) break;
+            if (M && first && !(ok = wait_bar(L::kDQEmpty, dqe_phase))) break;
             const uint64_t kd = ptx::sdesc_sw128(slot_addr(ks), L::kChunkBytes, 1024);
-            ptx::mma_ts_k64(tmem + 256u, tmem + 128u, kd, kIdescQ, j > 0 ? 1u : 0u);
+            ptx::mma_ts_k64(tmem + 256u, tmem + 128u, kd, kIdescQ, first ? 0u : 1u);
             ptx::mma_ts_k64(tmem + 256u, tmem + 192u, kd + 512u, kIdescQ, 1u);
             ptx::mma_commit(dq_bar<D>(base, L::kKVEmpty + ks));
-            if (j + 1 < w.n) {
+            if (jn < w.n) {
                 if (!(ok = wait_ring(vs))) break;
                 product(tmem + 128u, base + L::kDO, slot_addr(vs));
                 ptx::mma_commit(dq_bar<D>(base, L::kDPFull));
                 ptx::mma_commit(dq_bar<D>(base, L::kKVEmpty + vs));
-                if (j + 2 == w.n) ptx::mma_commit(dq_bar<D>(base, L::kQEmpty));
+                if (dq_next_key<M>(p, w, jn) >= w.n) ptx::mma_commit(dq_bar<D>(base, L::kQEmpty));
             }
             ks = ks_next;
         }
@@ -341,7 +377,7 @@ __device__ __forceinline__ float row_delta(const __nv_bfloat16* o, const __nv_bf
 // Warps 2-3: for each unit, the LSE (as log2) and delta_i = dO_i . O_i of its
 // 128 rows into a shared-memory stage (delta also to global memory for the
 // dK/dV kernel), ahead of the element-wise warps.
-template <int D>
+template <int D, bool M>
 __device__ void dq_stat_role(const BwdParams& p, uint32_t base, uint8_t* smem, volatile int* abort_flag) {
     using L = DqLayout<D>;
     const int tid = threadIdx.x - 64;  // 0..63
@@ -379,7 +415,7 @@ __device__ void dq_stat_role(const BwdParams& p, uint32_t base, uint8_t* smem, v
     }
 }
 
-template <int D>
+template <int D, bool M>
 __device__ void dq_work_role(const BwdParams& p, uint32_t base, const uint8_t* smem, uint32_t tmem,
                              int wg, volatile int* abort_flag) {
     using L = DqLayout<D>;
@@ -413,7 +449,8 @@ __device__ void dq_work_role(const BwdParams& p, uint32_t base, const uint8_t* s
             st = 0;
             stat_phase ^= 1u;
         }
-        for (int j = 0; j < w.n; ++j) {
+        const bool none = M && dq_next_key<M>(p, w, -1) >= w.n;  // no key tile kept: dQ = 0
+        for (int j = dq_next_key<M>(p, w, -1); j < w.n; j = dq_next_key<M>(p, w, j)) {
             bool ok = ptx::mbar_wait(dq_bar<D>(base, L::kSFull), s_phase, abort_flag, p.status, lim);
             if (!__all_sync(0xffffffffu, ok)) return;
             s_phase ^= 1u;
@@ -481,6 +518,10 @@ __device__ void dq_work_role(const BwdParams& p, uint32_t base, const uint8_t* s
             ptx::tmem_ld32(tDQ + c * 32, o);
             ptx::tmem_ld_wait();
             ptx::reg_fence32(o);
+            if (none) {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) o[e] = 0u;
+            }
             if (valid) {
                 uint4* dst = reinterpret_cast<uint4*>(drow + c * 32);
 #pragma unroll
@@ -498,10 +539,15 @@ __device__ void dq_work_role(const BwdParams& p, uint32_t base, const uint8_t* s
                 }
             }
         }
+        if constexpr (M) {  // dQ read out: the next unit may produce its own
+            ptx::tc_fence_before();
+            __syncwarp();
+            if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(dq_bar<D>(base, L::kDQEmpty));
+        }
     }
 }
 
-template <int D>
+template <int D, bool M>
 __global__ void __launch_bounds__(DqLayout<D>::kThreads, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                        const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -532,6 +578,7 @@ __global__ void __launch_bounds__(DqLayout<D>::kThreads, 1)
             ptx::mbar_init(dq_bar<D>(base, L::kStatEmpty + s), 8);  // one per element-wise warp
         }
         ptx::mbar_init(dq_bar<D>(base, L::kDrain), 1);
+        ptx::mbar_init(dq_bar<D>(base, L::kDQEmpty), 8);  // one per element-wise warp
         *abort_flag = 0;
         ptx::fence_barrier_init();
         ptx::prefetch_tensormap(&tm_q);
@@ -550,12 +597,12 @@ __global__ void __launch_bounds__(DqLayout<D>::kThreads, 1)
 
     if (warp < 4) {
         ptx::regs_dec<L::kRegsSmall>();
-        if (warp == 0 && lane == 0) dq_load_role<D>(&tm_q, &tm_do, &tm_k, &tm_v, p, base, abort_flag);
-        if (warp == 1 && lane == 0) dq_mma_role<D>(p, base, tmem, abort_flag);
-        if (warp >= 2) dq_stat_role<D>(p, base, smem, abort_flag);
+        if (warp == 0 && lane == 0) dq_load_role<D, M>(&tm_q, &tm_do, &tm_k, &tm_v, p, base, abort_flag);
+        if (warp == 1 && lane == 0) dq_mma_role<D, M>(p, base, tmem, abort_flag);
+        if (warp >= 2) dq_stat_role<D, M>(p, base, smem, abort_flag);
     } else {
         ptx::regs_inc<L::kRegsWork>();
-        dq_work_role<D>(p, base, smem, tmem, (warp - 4) >> 2, abort_flag);
+        dq_work_role<D, M>(p, base, smem, tmem, (warp - 4) >> 2, abort_flag);
     }
 
     ptx::tc_fence_before();
@@ -590,8 +637,9 @@ struct DkvLayout {
     static constexpr uint32_t kBars = kStat + kStatStages * kStatBytes;
     static constexpr int kKVFull = 0, kKVEmpty = 1, kSFull = 2, kDPFull = 3, kPFull = 4, kDSFull = 5,
                          kAccFull = 6, kStFull = 7, kStEmpty = 7 + kStages, kStatFull = 7 + 2 * kStages,
-                         kStatEmpty = 7 + 2 * kStages + kStatStages, kDrain = 7 + 2 * kStages + 2 * kStatStages;
-    static constexpr int kNumBars = kDrain + 1;
+                         kStatEmpty = 7 + 2 * kStages + kStatStages, kDrain = 7 + 2 * kStages + 2 * kStatStages,
+                         kAccEmpty = kDrain + 1;  // block-masked kernels: dK, dV read out
+    static constexpr int kNumBars = kDrain + 2;
     static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8;
     static constexpr uint32_t kAbort = kTmemSlot + 4;
     static constexpr uint32_t kDynamicSmem = kAbort + 4 + 1024;
@@ -619,12 +667,25 @@ __device__ __forceinline__ void dkv_iter(const DkvUnit& w, const BwdParams& p, i
     bh = w.b * p.Hq + w.hkv * p.group + g;
 }
 
+// The iteration after t whose (query head, query tile) uses key tile w.kt
+// (w.n if none): every iteration, or with a block mask (M) the kept ones.
+template <bool M>
+__device__ __forceinline__ int dkv_next(const BwdParams& p, const DkvUnit& w, int t) {
+    for (++t; t < w.n; ++t) {
+        if (!M) return t;
+        int bh, qt;
+        dkv_iter(w, p, t, bh, qt);
+        if (bwd_tile_kept(p, bh, qt, w.kt)) return t;
+    }
+    return w.n;
+}
+
 template <int D>
 __device__ __forceinline__ uint32_t dkv_bar(uint32_t base, int i) {
     return base + DkvLayout<D>::kBars + 8u * (uint32_t)i;
 }
 
-template <int D>
+template <int D, bool M>
 __device__ void dkv_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_do,
                               const CUtensorMap* tm_k, const CUtensorMap* tm_v, const BwdParams& p,
                               uint32_t base, volatile int* abort_flag) {
@@ -650,7 +711,7 @@ __device__ void dkv_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_do,
             pend_kv_par = kve_phase;
             kve_phase ^= 1u;
         }
-        for (int t = 0; t < w.n; ++t) {
+        for (int t = dkv_next<M>(p, w, -1); t < w.n; t = dkv_next<M>(p, w, t)) {
             int bh, qt;
             dkv_iter(w, p, t, bh, qt);
 #pragma unroll
@@ -685,7 +746,7 @@ drain:
 // Warps 2-3: LSE (as log2) and delta of each query tile into the stage's
 // shared-memory rows; queries past the sequence end get +inf and 0 so that
 // their weights vanish.
-template <int D>
+template <int D, bool M>
 __device__ void dkv_stat_role(const BwdParams& p, uint32_t base, uint8_t* smem, volatile int* abort_flag) {
     using L = DkvLayout<D>;
     const int tid = threadIdx.x - 64;  // 0..63
@@ -694,7 +755,7 @@ __device__ void dkv_stat_role(const BwdParams& p, uint32_t base, uint8_t* smem, 
     int st = 0;
     for (int rnd = 0, u = bwd_unit_of_round(0); u < p.num_units; u = bwd_unit_of_round(++rnd)) {
         const DkvUnit w = dkv_decode(u, p);
-        for (int t = 0; t < w.n; ++t) {
+        for (int t = dkv_next<M>(p, w, -1); t < w.n; t = dkv_next<M>(p, w, t)) {
             int bh, qt;
             dkv_iter(w, p, t, bh, qt);
             float l2[2], dl[2];
@@ -722,13 +783,16 @@ __device__ void dkv_stat_role(const BwdParams& p, uint32_t base, uint8_t* smem, 
     }
 }
 
-template <int D>
+template <int D, bool M>
 __device__ void dkv_mma_role(const BwdParams& p, uint32_t base, uint32_t tmem, volatile int* abort_flag) {
     using L = DkvLayout<D>;
     constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(kTile, kTile, false);  // S^T, dP^T: N = 128 queries
     constexpr uint32_t kIdescA = ptx::idesc_bf16_f32(kTile, D, true);       // dV, dK: N = D, MN-major
     const uint64_t lim = p.wait_limit_ns;
     uint32_t kvf_phase = 0, p_phase = 0, ds_phase = 0, ring_phase = 0;
+    // Block-masked kernels: as in the dQ kernel, dK and dV of the previous unit
+    // must have been read out before this unit produces (or zeroes) its own.
+    uint32_t acce_phase = 1u;
     int slot = 0;
 
     auto wait_bar = [&](int bar, uint32_t& phase) -> bool {
@@ -763,6 +827,13 @@ __device__ void dkv_mma_role(const BwdParams& p, uint32_t base, uint32_t tmem, v
     for (int rnd = 0, u = bwd_unit_of_round(0); u < p.num_units && ok; u = bwd_unit_of_round(++rnd)) {
         const DkvUnit w = dkv_decode(u, p);
         if (!wait_bar(L::kKVFull, kvf_phase)) break;
+        const int t0 = dkv_next<M>(p, w, -1);
+        if (M && t0 >= w.n) {  // no query tile keeps this key tile: dK = dV = 0
+            if (!wait_bar(L::kAccEmpty, acce_phase)) break;
+            ptx::mma_commit(dkv_bar<D>(base, L::kKVEmpty));
+            ptx::mma_commit(dkv_bar<D>(base, L::kAccFull));
+            continue;
+        }
         int qs, ds, qs_next = -1, ds_next = -1;
         if (!wait_ring(qs)) break;
         product(tmem, base + L::kK, slot_addr(qs));  // S^T = K Q^T
@@ -772,16 +843,19 @@ __device__ void dkv_mma_role(const BwdParams& p, uint32_t base, uint32_t tmem, v
         ptx::mma_commit(dkv_bar<D>(base, L::kDPFull));
         // K and V are read only by S^T and dP^T: free them for the next unit
         // as soon as the last of those has been issued.
-        if (w.n == 1) ptx::mma_commit(dkv_bar<D>(base, L::kKVEmpty));
-        for (int t = 0; t < w.n; ++t) {
+        if (dkv_next<M>(p, w, t0) >= w.n) ptx::mma_commit(dkv_bar<D>(base, L::kKVEmpty));
+        bool first = true;
+        for (int t = t0, tn; t < w.n; t = tn, first = false) {
+            tn = dkv_next<M>(p, w, t);
             // dV += P^T dO: P^T of queries 0-63 in columns [0,32), 64-127 in
             // [64,96); dO as an MN-major operand, queries 64-127 8 KB further in.
             if (!(ok = wait_bar(L::kPFull, p_phase))) break;
+            if (M && first && !(ok = wait_bar(L::kAccEmpty, acce_phase))) break;
             const uint64_t dod = ptx::sdesc_sw128(slot_addr(ds), L::kChunkBytes, 1024);
-            ptx::mma_ts_k64(tDV, tmem, dod, kIdescA, t > 0 ? 1u : 0u);
+            ptx::mma_ts_k64(tDV, tmem, dod, kIdescA, first ? 0u : 1u);
             ptx::mma_ts_k64(tDV, tmem + 64u, dod + 512u, kIdescA, 1u);
             ptx::mma_commit(dkv_bar<D>(base, L::kStEmpty + ds));
-            if (t + 1 < w.n) {
+            if (tn < w.n) {
                 if (!(ok = wait_ring(qs_next))) break;
                 product(tmem, base + L::kK, slot_addr(qs_next));
                 ptx::mma_commit(dkv_bar<D>(base, L::kSFull));
@@ -789,14 +863,14 @@ __device__ void dkv_mma_role(const BwdParams& p, uint32_t base, uint32_t tmem, v
             // dK += dS^T Q: dS^T in columns [128,160) and [192,224).
             if (!(ok = wait_bar(L::kDSFull, ds_phase))) break;
             const uint64_t qd = ptx::sdesc_sw128(slot_addr(qs), L::kChunkBytes, 1024);
-            ptx::mma_ts_k64(tDK, tmem + 128u, qd, kIdescA, t > 0 ? 1u : 0u);
+            ptx::mma_ts_k64(tDK, tmem + 128u, qd, kIdescA, first ? 0u : 1u);
             ptx::mma_ts_k64(tDK, tmem + 192u, qd + 512u, kIdescA, 1u);
             ptx::mma_commit(dkv_bar<D>(base, L::kStEmpty + qs));
-            if (t + 1 < w.n) {
+            if (tn < w.n) {
                 if (!(ok = wait_ring(ds_next))) break;
                 product(tmem + 128u, base + L::kV, slot_addr(ds_next));
                 ptx::mma_commit(dkv_bar<D>(base, L::kDPFull));
-                if (t + 2 == w.n) ptx::mma_commit(dkv_bar<D>(base, L::kKVEmpty));
+                if (dkv_next<M>(p, w, tn) >= w.n) ptx::mma_commit(dkv_bar<D>(base, L::kKVEmpty));
             }
             qs = qs_next;
             ds = ds_next;
@@ -808,7 +882,7 @@ __device__ void dkv_mma_role(const BwdParams& p, uint32_t base, uint32_t tmem, v
     ptx::drain_wait(dkv_bar<D>(base, L::kDrain), 0u, lim);
 }
 
-template <int D>
+template <int D, bool M>
 __device__ void dkv_work_role(const BwdParams& p, uint32_t base, const uint8_t* smem, uint32_t tmem,
                               int wg, volatile int* abort_flag) {
     using L = DkvLayout<D>;
@@ -824,7 +898,8 @@ __device__ void dkv_work_role(const BwdParams& p, uint32_t base, const uint8_t* 
 
     for (int rnd = 0, u = bwd_unit_of_round(0); u < p.num_units; u = bwd_unit_of_round(++rnd)) {
         const DkvUnit w = dkv_decode(u, p);
-        for (int t = 0; t < w.n; ++t) {
+        const bool none = M && dkv_next<M>(p, w, -1) >= w.n;  // no query tile kept: dK = dV = 0
+        for (int t = dkv_next<M>(p, w, -1); t < w.n; t = dkv_next<M>(p, w, t)) {
             int bh, qt;
             dkv_iter(w, p, t, bh, qt);
             bool ok = ptx::mbar_wait(dkv_bar<D>(base, L::kStatFull + st), ring_phase, abort_flag, p.status, lim);
@@ -913,6 +988,10 @@ __device__ void dkv_work_role(const BwdParams& p, uint32_t base, const uint8_t* 
             ptx::tmem_ld32(tA + c * 32, o);
             ptx::tmem_ld_wait();
             ptx::reg_fence32(o);
+            if (none) {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) o[e] = 0u;
+            }
             if (valid) {
                 uint4* dst = reinterpret_cast<uint4*>(drow + c * 32);
 #pragma unroll
@@ -926,10 +1005,15 @@ __device__ void dkv_work_role(const BwdParams& p, uint32_t base, const uint8_t* 
                 }
             }
         }
+        if constexpr (M) {  // dK, dV read out: the next unit may produce its own
+            ptx::tc_fence_before();
+            __syncwarp();
+            if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(dkv_bar<D>(base, L::kAccEmpty));
+        }
     }
 }
 
-template <int D>
+template <int D, bool M>
 __global__ void __launch_bounds__(DkvLayout<D>::kThreads, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                          const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -960,6 +1044,7 @@ __global__ void __launch_bounds__(DkvLayout<D>::kThreads, 1)
             ptx::mbar_init(dkv_bar<D>(base, L::kStatEmpty + s), 8);  // one per element-wise warp
         }
         ptx::mbar_init(dkv_bar<D>(base, L::kDrain), 1);
+        ptx::mbar_init(dkv_bar<D>(base, L::kAccEmpty), 8);  // one per element-wise warp
         *abort_flag = 0;
         ptx::fence_barrier_init();
         ptx::prefetch_tensormap(&tm_q);
@@ -978,12 +1063,12 @@ __global__ void __launch_bounds__(DkvLayout<D>::kThreads, 1)
 
     if (warp < 4) {
         ptx::regs_dec<L::kRegsSmall>();
-        if (warp == 0 && lane == 0) dkv_load_role<D>(&tm_q, &tm_do, &tm_k, &tm_v, p, base, abort_flag);
-        if (warp == 1 && lane == 0) dkv_mma_role<D>(p, base, tmem, abort_flag);
-        if (warp >= 2) dkv_stat_role<D>(p, base, smem, abort_flag);
+        if (warp == 0 && lane == 0) dkv_load_role<D, M>(&tm_q, &tm_do, &tm_k, &tm_v, p, base, abort_flag);
+        if (warp == 1 && lane == 0) dkv_mma_role<D, M>(p, base, tmem, abort_flag);
+        if (warp >= 2) dkv_stat_role<D, M>(p, base, smem, abort_flag);
     } else {
         ptx::regs_inc<L::kRegsWork>();
-        dkv_work_role<D>(p, base, smem, tmem, (warp - 4) >> 2, abort_flag);
+        dkv_work_role<D, M>(p, base, smem, tmem, (warp - 4) >> 2, abort_flag);
     }
 
     ptx::tc_fence_before();

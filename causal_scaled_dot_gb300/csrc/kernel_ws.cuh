@@ -77,7 +77,8 @@ struct WsLayout {
     // mbarrier indices
     static constexpr int kQFull = 0, kQEmpty = 2, kSFull = 4, kPFull = 6, kOFull = 8;
     static constexpr int kKVFull = 10, kKVEmpty = 10 + kStages, kDrain = 10 + 2 * kStages;
-    static constexpr int kNumBars = kDrain + 1;
+    static constexpr int kOEmpty = kDrain + 1;  // block-masked kernels: O_i read out (2 barriers)
+    static constexpr int kNumBars = kDrain + 3;
     static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8;
     static constexpr uint32_t kAbort = kTmemSlot + 4;
     static constexpr uint32_t kBytes = kAbort + 4;
@@ -288,6 +289,18 @@ __device__ void ws_mma_role(const FwdParams& p, uint32_t base, uint32_t tmem,
         ptx::tc_fence_after();
         return true;
     };
+    // Block-masked kernels: a query tile without key tiles makes no P handshake,
+    // so before O_i of a unit is produced (or declared empty) the previous
+    // unit's O_i must have been read out -- otherwise OFull_i could run two
+    // phases ahead of the softmax warps waiting on it.  Once per tile per unit.
+    uint32_t oe_phase[2] = {1u, 1u};
+    auto wait_o_empty = [&](int i) -> bool {
+        if (!ptx::mbar_wait(ws_bar<D, F>(base, L::kOEmpty + i), oe_phase[i], abort_flag, p.status, lim))
+            return false;
+        oe_phase[i] ^= 1u;
+        ptx::tc_fence_after();
+        return true;
+    };
 
     for (int rnd = 0, u = unit_of_round(0); u < p.num_units; u = unit_of_round(++rnd)) {
         const Unit w = decode_unit(u, p);
@@ -320,6 +333,7 @@ __device__ void ws_mma_role(const FwdParams& p, uint32_t base, uint32_t tmem,
             if (!(ok = wait_ring(vslot))) break;
             if (tile_active<M>(p, w, 0, j)) {
                 if (!(ok = wait_p(0))) break;
+                if (M && first0 && !(ok = wait_o_empty(0))) break;
                 issue_pv(0, vslot, !first0);
                 first0 = false;
                 if (j == last0) ptx::mma_commit(ws_bar<D, F>(base, L::kOFull + 0));
@@ -334,6 +348,7 @@ __device__ void ws_mma_role(const FwdParams& p, uint32_t base, uint32_t tmem,
             }
             if (tile_active<M>(p, w, 1, j)) {
                 if (!(ok = wait_p(1))) break;
+                if (M && first1 && !(ok = wait_o_empty(1))) break;
                 issue_pv(1, vslot, !first1);
                 first1 = false;
                 if (j == last1) ptx::mma_commit(ws_bar<D, F>(base, L::kOFull + 1));
@@ -350,8 +365,14 @@ __device__ void ws_mma_role(const FwdParams& p, uint32_t base, uint32_t tmem,
         }
         if (!ok) break;
         // A query tile with no key tile still completes its O phase.
-        if (last0 < 0) ptx::mma_commit(ws_bar<D, F>(base, L::kOFull + 0));
-        if (last1 < 0) ptx::mma_commit(ws_bar<D, F>(base, L::kOFull + 1));
+        if (last0 < 0) {
+            if (!wait_o_empty(0)) break;
+            ptx::mma_commit(ws_bar<D, F>(base, L::kOFull + 0));
+        }
+        if (last1 < 0) {
+            if (!wait_o_empty(1)) break;
+            ptx::mma_commit(ws_bar<D, F>(base, L::kOFull + 1));
+        }
     }
     // Every MMA issued above completes before TMEM can be released.
     ptx::mma_commit(ws_bar<D, F>(base, L::kDrain));
@@ -549,6 +570,8 @@ __device__ void ws_softmax_role(const FwdParams& p, uint32_t base, uint32_t tmem
                     *reinterpret_cast<uint4*>(orow + c) = make_uint4(0u, 0u, 0u, 0u);
                 if (p.lse != nullptr) p.lse[(size_t)w.bh * p.S + row] = -INFINITY;
             }
+            __syncwarp();
+            if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(ws_bar<D, F>(base, L::kOEmpty + wg));
             continue;
         }
         const float inv_l = p.o_scale / l_run;  // o_scale: the V descale (1 for bf16)
@@ -577,6 +600,11 @@ __device__ void ws_softmax_role(const FwdParams& p, uint32_t base, uint32_t tmem
         }
         if (valid && p.lse != nullptr)
             p.lse[(size_t)w.bh * p.S + row] = (m_run + ptx::lg2(l_run)) * kLn2;
+        if constexpr (M) {  // O_i read out: the next unit may produce its own
+            ptx::tc_fence_before();
+            __syncwarp();
+            if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(ws_bar<D, F>(base, L::kOEmpty + wg));
+        }
     }
 }
 
@@ -609,6 +637,7 @@ __global__ void __launch_bounds__(WsLayout<D, F>::kThreads, 1)
             ptx::mbar_init(ws_bar<D, F>(base, L::kKVEmpty + s), 1);
         }
         ptx::mbar_init(ws_bar<D, F>(base, L::kDrain), 1);
+        for (int i = 0; i < 2; ++i) ptx::mbar_init(ws_bar<D, F>(base, L::kOEmpty + i), 4);  // one per softmax warp
         *abort_flag = 0;
         ptx::fence_barrier_init();
         ptx::prefetch_tensormap(&tm_q);

@@ -171,6 +171,19 @@ int attn_bwd(const void *q, const void *k, const void *v, const void *out, const
              int S, int D, float scale, int causal, void *stream);
 
 /*
+ * attn_bwd_block_masked -- attn_bwd for attn_fwd_block_masked: the gradients of
+ * the block-masked attention, with the same block_mask and mask_heads as the
+ * forward call (see attn_fwd_block_masked).  Dropped tiles are neither loaded
+ * nor computed; query rows that see no key (LSE = -inf, O = 0) get dQ = 0
+ * and contribute nothing to dK and dV.  ATTN_ERR_INVALID_ARG also for a NULL
+ * mask or mask_heads not 1 or Hq; otherwise as attn_bwd.
+ */
+int attn_bwd_block_masked(const void *q, const void *k, const void *v, const void *out,
+                          const void *dout, const float *lse, float *delta, void *dq, void *dk,
+                          void *dv, int B, int Hq, int Hkv, int S, int D, float scale, int causal,
+                          const unsigned char *block_mask, int mask_heads, void *stream);
+
+/*
  * attn_out_proj -- the layer's output projection applied to attention's
  * output where it lies (the "output projection" operator the ainews.cool
  * article profiles right after attention, per-operator table):

@@ -28,7 +28,8 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for required in ("attn_fwd", "attn_fwd_fp8", "attn_fwd_block_masked", "attn_fwd_dropout",
-                     "attn_bwd", "attn_out_proj", "attn_status_string", "attn_sync_status"):
+                     "attn_bwd", "attn_bwd_block_masked", "attn_out_proj", "attn_status_string",
+                     "attn_sync_status"):
         assert required in names
 
 
@@ -230,3 +231,12 @@ def _call_proj(out=1 << 40, w=2 << 40, bias=None, y=3 << 40, B=1, H=4, S=300, D=
 ])
 def test_proj_argument_errors_are_rejected_before_launch(kw, code):
     assert _call_proj(**kw) == code
+
+
+def test_masked_bwd_rejects_bad_masks_before_launch():
+    lib = native.load()
+    args = [1 << 40, 2 << 40, 3 << 40, 4 << 40, 5 << 40, 6 << 40, 7 << 40, 8 << 40, 9 << 40, 10 << 40,
+            1, 2, 2, 300, 128, ctypes.c_float(0.1), 1]
+    assert lib.attn_bwd_block_masked(*args, None, 1, None) == ATTN_ERR_INVALID_ARG
+    assert lib.attn_bwd_block_masked(*args, 11 << 40, 3, None) == ATTN_ERR_INVALID_ARG
+    assert lib.attn_bwd_block_masked(*args[:14], 96, *args[15:], 11 << 40, 1, None) == ATTN_ERR_UNSUPPORTED

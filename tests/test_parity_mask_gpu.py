@@ -106,3 +106,18 @@ def test_full_size_workloads_masked_sampled_rows(w):
     rows = sample_rows(w.B, w.Hq, w.S, n_random=256, seed=w.seed)
     print(w.name, _check(w.B, w.Hq, w.Hkv, w.S, w.D, True, mask, seed=w.seed, rows=rows,
                          sigma=w.sigma))
+
+
+@pytest.mark.parametrize("density", [0.0, 0.05])
+def test_sparse_masks_many_empty_units(density):
+    """Long runs of query tiles that keep no key tile, in every CTA."""
+    S, Hq = 2048, 32
+    mask = random_block_mask(Hq, S, density, seed=2100)
+    q, k, v = qkv_bf16(1, Hq, Hq, S, 128, seed=2100)
+    o, l = run_gpu_masked(q, k, v, 128 ** -0.5, True, mask)
+    if density == 0.0:
+        assert not o.any() and np.all(np.isneginf(l))
+        return
+    rows = sample_rows(1, Hq, S, n_random=512, seed=2100)
+    o_ref, l_ref = oracle.attention_masked(q, k, v, 128 ** -0.5, mask, True, rows=rows)
+    print(compare_masked(o.reshape(-1, 128)[rows], o_ref, l.reshape(-1)[rows], l_ref, "sparse"))
