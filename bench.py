@@ -253,16 +253,23 @@ class OracleBwdTimer:
     with every query head of its group); a head carries 1/(B*Hkv) of the
     metric's FLOPs."""
 
-    def __init__(self, w):
+    def __init__(self, w, mask=None):
         import oracle
         from causal_scaled_dot_gb300.inputs import gaussian_bf16, qkv_bf16
         self.oracle = oracle
         self.w = w
+        self.mask = mask
         self.q, self.k, self.v = qkv_bf16(w.B, w.Hq, w.Hkv, w.S, w.D, seed=w.seed, sigma=w.sigma)
         self.do = gaussian_bf16((w.B, w.Hq, w.S, w.D), w.seed, 3)
         self.threads = oracle.default_threads()
         self.total = w.B * w.Hkv
         self.row_flops = 2.5 * w.flops / self.total  # per key/value head
+        G = w.Hq // w.Hkv
+        if mask is not None:  # per key/value head: 2.5 x 4D x its group's visible pairs
+            vis = visible_keys(mask, w.S, w.causal).sum(axis=1)  # per mask head
+            per_hq = vis if mask.shape[0] == w.Hq else np.repeat(vis, w.Hq)
+            self.head_flops = np.array([2.5 * 4.0 * w.D * per_hq[(h % w.Hkv) * G:(h % w.Hkv + 1) * G].sum()
+                                        for h in range(self.total)])
         t0 = time.perf_counter()
         self.run(1, seed=12345)
         self.sec_per_row = time.perf_counter() - t0
@@ -270,7 +277,7 @@ class OracleBwdTimer:
     def run(self, n, seed):
         heads = np.random.default_rng(seed).integers(0, self.total, n)
         self.oracle.attention_bwd(self.q, self.k, self.v, self.do, self.w.scale, self.w.causal,
-                                  kv_heads=heads, nthreads=self.threads)
+                                  kv_heads=heads, nthreads=self.threads, block_mask=self.mask)
         return heads
 
     def rows_for(self, seconds):
@@ -279,9 +286,10 @@ class OracleBwdTimer:
     def sample(self, seconds, seed):
         n = self.rows_for(seconds)
         t0 = time.perf_counter()
-        self.run(n, seed)
+        heads = self.run(n, seed)
         dt = time.perf_counter() - t0
-        return n * self.row_flops / dt / 1e12, n, dt
+        flops = n * self.row_flops if self.mask is None else float(self.head_flops[heads].sum())
+        return flops / dt / 1e12, n, dt
 
 
 def dropout_p8(args) -> int:
@@ -290,7 +298,7 @@ def dropout_p8(args) -> int:
 
 def make_oracle_timer(args, w, mask=None):
     if args.pass_ == "bwd":
-        return OracleBwdTimer(w)
+        return OracleBwdTimer(w, mask=mask)
     if args.pass_ == "proj":
         return OracleProjTimer(w)
     return OracleTimer(w, fp8=args.dtype == "fp8", mask=mask, dropout_p8=dropout_p8(args))
@@ -587,16 +595,28 @@ def run_ours_bwd(args, w, rank, world, local):
     out = torch.empty_like(q)
     lse = torch.empty((w.B, w.Hq, w.S), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    native.attn_fwd(q, k, v, out, lse, w.B, w.Hq, w.Hkv, w.S, w.D, w.scale, w.causal, stream)
+    mask = workload_mask(w, args.mask_density) if args.mask_density is not None else None
+    if mask is not None:
+        mask_d = torch.from_numpy(mask).to(dev)
+        native.attn_fwd_block_masked(q, k, v, out, lse, w.B, w.Hq, w.Hkv, w.S, w.D, w.scale, w.causal,
+                                     mask_d, mask.shape[0], stream)
+    else:
+        native.attn_fwd(q, k, v, out, lse, w.B, w.Hq, w.Hkv, w.S, w.D, w.scale, w.causal, stream)
     outh, lseh = out.cpu().pin_memory(), lse.cpu().pin_memory()
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     delta = torch.empty_like(lse)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     flops = 2.5 * w.flops
+    if mask is not None:  # 2.5x the forward's FLOPs over the visible pairs
+        flops = 2.5 * 4.0 * w.D * w.B * float(visible_keys(mask, w.S, w.causal).sum())
 
     def step():
-        native.attn_bwd(q, k, v, out, do, lse, delta, dq, dk, dv, w.B, w.Hq, w.Hkv, w.S, w.D,
-                        w.scale, w.causal, stream)
+        if mask is not None:
+            native.attn_bwd_block_masked(q, k, v, out, do, lse, delta, dq, dk, dv, w.B, w.Hq, w.Hkv,
+                                         w.S, w.D, w.scale, w.causal, mask_d, mask.shape[0], stream)
+        else:
+            native.attn_bwd(q, k, v, out, do, lse, delta, dq, dk, dv, w.B, w.Hq, w.Hkv, w.S, w.D,
+                            w.scale, w.causal, stream)
 
     for _ in range(args.warmup):
         flush.fill_(1.0)
@@ -661,7 +681,7 @@ def run_ours_bwd(args, w, rank, world, local):
     io_bytes = 3 * q_b + 2 * kv_b + row_b + q_b + 2 * kv_b + 2 * row_b
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        timer = OracleBwdTimer(w)
+        timer = OracleBwdTimer(w, mask=mask)
         tf, n, dt = timer.sample(args.cpu_seconds, seed=7)
         cpu = {"value": tf, "unit": "TFLOP/s", "cores": timer.threads, "kind": "oracle",
                "sample": f"gradients of {n} random key/value heads of {w.name} (of {timer.total}), "
@@ -672,11 +692,14 @@ def run_ours_bwd(args, w, rank, world, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16 Q, K, V, dO; no weights)",
         "config": {"workload": w.name, **w.shape_dict, "causal": w.causal, "inputs": "bf16",
-                   "pass": "bwd", "l2": "flushed between timed steps (256 MiB write)",
+                   "pass": "bwd", **mask_config(mask, args.mask_density),
+                   "l2": "flushed between timed steps (256 MiB write)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "pct_of_peak": 100.0 * achieved / peak,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": recorded_traffic(w.name + ":bwd", BWD_SOURCES),
+                     "frac": achieved / peak,
+                     "traffic": recorded_traffic(w.name + ":bwd" + (f":mask{args.mask_density}" if mask is not None
+                                                                   else ""), BWD_SOURCES),
                      "peak_source": f"{peak_src} bf16 dense (burst)",
                      "kernel": "attn_bwd call (dQ kernel + dK/dV kernel)",
                      "hbm_gbs": io_bytes / (ms_local * 1e-3) / 1e9},
@@ -834,8 +857,10 @@ def main():
         ap.error("--warmup must be at least 3")
     if args.mask_density is not None and (args.dtype != "bf16" or not 0.0 <= args.mask_density <= 1.0):
         ap.error("--mask-density takes a probability in [0, 1] and bf16 inputs")
-    if args.pass_ in ("bwd", "proj") and (args.dtype != "bf16" or args.mask_density is not None):
-        ap.error("--pass bwd / proj take bf16 inputs and no mask")
+    if args.pass_ in ("bwd", "proj") and args.dtype != "bf16":
+        ap.error("--pass bwd / proj take bf16 inputs")
+    if args.pass_ == "proj" and args.mask_density is not None:
+        ap.error("--pass proj takes no mask")
     if args.dropout is not None and (args.pass_ != "fwd" or args.dtype != "bf16" or args.mask_density is not None
                                      or not 0 < round(args.dropout * 256) < 256):
         ap.error("--dropout takes 0 < p < 1 (at least 1/256), bf16 forward, no mask")
