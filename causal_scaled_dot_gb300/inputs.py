@@ -156,3 +156,60 @@ def random_block_mask(mask_heads: int, S: int, density: float, seed: int,
         u = _splitmix64(key + (np.arange(n, dtype=np.uint64) + np.uint64(1)) * _GOLDEN)
     uniform = (u >> np.uint64(11)).astype(np.float64) * (1.0 / 9007199254740992.0)
     return (uniform < density).astype(np.uint8).reshape(mask_heads, nt, nt)
+
+
+def keep_row_bytes(S: int) -> int:
+    """Bytes per query row of an element mask: 16 per 128 keys."""
+    return 16 * ((int(S) + 127) // 128)
+
+
+def pack_keep_bits(keep: np.ndarray) -> np.ndarray:
+    """bool [Hm, S, S] (query, key) -> uint8 [Hm, S, keep_row_bytes(S)]: bit
+    j % 8 of byte j / 8 of row i set when key j is kept for query i; the
+    padding bits past key S-1 are 0."""
+    keep = np.asarray(keep, dtype=bool)
+    Hm, S, S2 = keep.shape
+    if S2 != S:
+        raise ValueError("keep must be [Hm, S, S]")
+    padded = np.zeros((Hm, S, keep_row_bytes(S) * 8), dtype=bool)
+    padded[:, :, :S] = keep
+    return np.packbits(padded, axis=-1, bitorder="little")
+
+
+def unpack_keep_bits(bits: np.ndarray, S: int) -> np.ndarray:
+    """Inverse of ``pack_keep_bits``: bool [Hm, S, S]."""
+    return np.unpackbits(np.asarray(bits, dtype=np.uint8), axis=-1, bitorder="little")[:, :, :S].astype(bool)
+
+
+def random_keep_bits(mask_heads: int, S: int, density: float, seed: int,
+                     stream: int = 9) -> np.ndarray:
+    """Element mask with each (query, key) pair kept with probability
+    ``density`` (53-bit SplitMix64 uniforms as in ``random_block_mask``),
+    packed as ``pack_keep_bits`` does."""
+    n = int(mask_heads) * int(S) * int(S)
+    key = _tensor_key(seed, stream)
+    with np.errstate(over="ignore"):
+        u = _splitmix64(key + (np.arange(n, dtype=np.uint64) + np.uint64(1)) * _GOLDEN)
+    uniform = (u >> np.uint64(11)).astype(np.float64) * (1.0 / 9007199254740992.0)
+    return pack_keep_bits((uniform < density).reshape(mask_heads, S, S))
+
+
+def window_keep_bits(S: int, window: int) -> np.ndarray:
+    """Local (sliding-window) element mask shared by all heads: query i keeps
+    keys i - window < j <= i, packed as ``pack_keep_bits`` does."""
+    i = np.arange(S)[:, None]
+    j = np.arange(S)[None, :]
+    return pack_keep_bits(((j <= i) & (j > i - window))[None])
+
+
+def block_mask_of_keep_bits(bits: np.ndarray, S: int) -> np.ndarray:
+    """uint8 [Hm, nt, nt]: 1 where the 128 x 128 (query tile, key tile) block
+    of the element mask keeps at least one pair, so that a kernel may skip the
+    other blocks without changing the result."""
+    bits = np.asarray(bits, dtype=np.uint8)
+    Hm = bits.shape[0]
+    nt = (int(S) + 127) // 128
+    rows = np.zeros((Hm, nt * 128, bits.shape[2]), dtype=np.uint8)
+    rows[:, :S] = bits
+    per_tile = rows.reshape(Hm, nt, 128, nt, 16).any(axis=(2, 4))
+    return per_tile.astype(np.uint8)

@@ -83,6 +83,14 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     f.restype = ci
     f.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, vp, ctypes.c_int64, vp, vp, vp,
                   vp, ci]
+    f = lib.oracle_attn_rows_keep
+    f.restype = ci
+    f.argtypes = [vp, vp, vp, ci, ci, ci, ci, ci, cf, ci, vp, ci, vp, ci, vp, ctypes.c_int64, vp, vp,
+                  ci]
+    f = lib.oracle_attn_bwd_keep
+    f.restype = ci
+    f.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, vp, ci, vp, ci, vp, ctypes.c_int64,
+                  vp, vp, vp, vp, ci]
     return lib
 
 
@@ -178,6 +186,52 @@ def attention_masked(q_bits, k_bits, v_bits, scale: float, block_mask, causal: b
     return out, lse
 
 
+def keep_row_bytes(S: int) -> int:
+    """Bytes per query row of an element mask: 16 per 128 keys."""
+    return 16 * ((S + 127) // 128)
+
+
+def _keep(keep_bits, Hq: int, S: int) -> np.ndarray:
+    m = np.ascontiguousarray(keep_bits, dtype=np.uint8)
+    if m.ndim != 3 or m.shape[1:] != (S, keep_row_bytes(S)) or m.shape[0] not in (1, Hq):
+        raise ValueError(f"keep_bits must be [1 or Hq, {S}, {keep_row_bytes(S)}]")
+    return m
+
+
+def _block(block_mask, Hq: int, S: int):
+    if block_mask is None:
+        return None
+    nt = (S + 127) // 128
+    m = np.ascontiguousarray(block_mask, dtype=np.uint8)
+    if m.ndim != 3 or m.shape[1:] != (nt, nt) or m.shape[0] not in (1, Hq):
+        raise ValueError(f"block_mask must be [1 or Hq, {nt}, {nt}]")
+    return m
+
+
+def attention_keep(q_bits, k_bits, v_bits, scale: float, keep_bits, causal: bool = True,
+                   block_mask=None, rows=None, nthreads: int | None = None,
+                   lib: ctypes.CDLL | None = None):
+    """As ``attention`` plus an element mask: keep_bits uint8 [Hm, S, keep_row_bytes(S)],
+    Hm = 1 or Hq; bit j % 8 of byte j / 8 of row i keeps key j for query i.  An
+    optional block mask (as in ``attention_masked``) applies as well.  Rows
+    without any visible key: O = 0, LSE = -inf."""
+    lib = lib or load()
+    q, k, v = (_as_bits(x, n) for x, n in ((q_bits, "q"), (k_bits, "k"), (v_bits, "v")))
+    B, Hq, Hkv, S, D = _shapes(q, k, v)
+    m = _keep(keep_bits, Hq, S)
+    bm = _block(block_mask, Hq, S)
+    rows_arr, nrows, out, lse = _outputs(B, Hq, S, D, rows)
+    rc = lib.oracle_attn_rows_keep(
+        q.ctypes.data, k.ctypes.data, v.ctypes.data, B, Hq, Hkv, S, D, ctypes.c_float(scale),
+        1 if causal else 0, m.ctypes.data, m.shape[0],
+        None if bm is None else bm.ctypes.data, 1 if bm is None else bm.shape[0],
+        None if rows_arr is None else rows_arr.ctypes.data, nrows,
+        out.ctypes.data, lse.ctypes.data, nthreads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle_attn_rows_keep rejected its arguments")
+    return out, lse
+
+
 def e4m3_decode(codes, lib: ctypes.CDLL | None = None) -> np.ndarray:
     """The oracle's own E4M3 decoding of uint8 codes, as float64."""
     lib = lib or load()
@@ -244,7 +298,8 @@ def attention_f64(q, k, v, scale: float, causal: bool = True, nthreads: int | No
 
 
 def attention_bwd(q, k, v, dout, scale: float, causal: bool = True, kv_heads=None,
-                  nthreads: int | None = None, lib: ctypes.CDLL | None = None, block_mask=None):
+                  nthreads: int | None = None, lib: ctypes.CDLL | None = None, block_mask=None,
+                  keep_bits=None):
     """Gradients of the attention output: (dQ, dK, dV, delta) in float64.
 
     q, dout: [B,Hq,S,D]; k, v: [B,Hkv,S,D]; either all bf16 bit patterns
@@ -253,7 +308,8 @@ def attention_bwd(q, k, v, dout, scale: float, causal: bool = True, kv_heads=Non
     shapes [n, G, S, D] and [n, G, S], and dK, dV are [n, S, D].  Without
     kv_heads: dQ [B,Hq,S,D], dK and dV [B,Hkv,S,D], delta [B,Hq,S].
     delta_i = sum_j P_ij (dO_i . V_j), the row term of the softmax gradient.
-    block_mask: optional uint8 [1 or Hq, nt, nt] as in ``attention_masked``.
+    block_mask: optional uint8 [1 or Hq, nt, nt] as in ``attention_masked``;
+    keep_bits: optional element mask as in ``attention_keep``.
     """
     lib = lib or load()
     f64 = np.asarray(q).dtype == np.float64
@@ -276,14 +332,16 @@ def attention_bwd(q, k, v, dout, scale: float, causal: bool = True, kv_heads=Non
               Hkv, S, D, ctypes.c_float(scale), 1 if causal else 0)
     tail = (None if heads is None else heads.ctypes.data, n, dq.ctypes.data, dk.ctypes.data,
             dv.ctypes.data, delta.ctypes.data, nthreads or default_threads())
-    if block_mask is None:
+    bm = _block(block_mask, Hq, S)
+    if keep_bits is not None:
+        km = _keep(keep_bits, Hq, S)
+        rc = lib.oracle_attn_bwd_keep(*common, km.ctypes.data, km.shape[0],
+                                      None if bm is None else bm.ctypes.data,
+                                      1 if bm is None else bm.shape[0], *tail)
+    elif bm is None:
         rc = lib.oracle_attn_bwd(*common, *tail)
     else:
-        m = np.ascontiguousarray(block_mask, dtype=np.uint8)
-        nt = (S + 127) // 128
-        if m.ndim != 3 or m.shape[1:] != (nt, nt) or m.shape[0] not in (1, Hq):
-            raise ValueError(f"block_mask must be [1 or Hq, {nt}, {nt}]")
-        rc = lib.oracle_attn_bwd_masked(*common, m.ctypes.data, m.shape[0], *tail)
+        rc = lib.oracle_attn_bwd_masked(*common, bm.ctypes.data, bm.shape[0], *tail)
     if rc != 0:
         raise ValueError("oracle_attn_bwd rejected its arguments")
     return dq, dk, dv, delta

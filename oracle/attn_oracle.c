@@ -17,7 +17,12 @@
  *   as well -- the block-sparse attention the ai-manual.ru article gives as a
  *   reason for custom kernels (sections 4 and 7): key j is masked for query i
  *   when block_mask[h][i / 128][j / 128] == 0, h = 0 for a mask shared by all
- *   heads, else the query head.
+ *   heads, else the query head.  An optional element mask (the arbitrary
+ *   masks of the same sections) drops single (query, key) pairs: key j is
+ *   masked for query i when bit j % 8 of byte j / 8 of row i of the mask is
+ *   0, rows 16 * ceil(S / 128) bytes apart, one bit matrix shared by all
+ *   heads or one per query head.  The masks combine: a key is visible only
+ *   when every mask given keeps it.
  *   and the definition Attention(Q,K,V) = softmax(Q K^T / sqrt(d_k)) V from
  *   the ainews.cool article, section "technical deep dive".
  *   The fully-masked-row convention (output 0 instead of NaN) follows the
@@ -86,6 +91,8 @@ typedef struct {
     int causal;
     const uint8_t *block_mask; /* NULL, or [mask_heads][nt][nt], nt = ceil(S / 128) */
     int mask_heads;            /* 1 (shared by all heads) or Hq */
+    const uint8_t *keep_bits;  /* NULL, or [keep_heads][S][16 * nt] bytes, bit j % 8 of byte j / 8 keeps key j */
+    int keep_heads;            /* 1 (shared by all heads) or Hq */
     int dropout_p8;            /* 0: no dropout; else weights dropped with probability p8 / 256 */
     uint64_t dropout_key[2];   /* Philox key: {seed, offset} */
     const int64_t *rows; /* flat query-row ids, or NULL for all rows */
@@ -142,6 +149,13 @@ static void attn_weights(const oracle_job_t *J, int64_t r, double *s, double *ls
         const uint8_t *mrow = J->block_mask + ((J->mask_heads == 1 ? 0 : hq) * nt + i / 128) * nt;
         for (int64_t j = 0; j < S; ++j)
             if (mrow[j / 128] == 0) s[j] = -INFINITY;
+    }
+    /* ... and keys whose bit in the element mask is 0. */
+    if (J->keep_bits) {
+        const int64_t row_bytes = 16 * ((S + 127) / 128);
+        const uint8_t *krow = J->keep_bits + ((J->keep_heads == 1 ? 0 : hq) * (int64_t)S + i) * row_bytes;
+        for (int64_t j = 0; j < S; ++j)
+            if (((krow[j / 8] >> (j % 8)) & 1) == 0) s[j] = -INFINITY;
     }
     /* Step 4: softmax over keys, max-subtracted ("safe") form. */
     double m = -INFINITY;
@@ -248,10 +262,12 @@ static void *oracle_worker(void *arg) {
 static int run_rows_dropout(const void *q, const void *k, const void *v, int format,
                             const double descale[3], int B, int Hq, int Hkv, int S, int D,
                             float scale, int causal, const uint8_t *block_mask, int mask_heads,
-                            int dropout_p8, uint64_t seed, uint64_t offset, const int64_t *rows,
-                            int64_t nrows, double *out, double *lse, int nthreads) {
+                            const uint8_t *keep_bits, int keep_heads, int dropout_p8, uint64_t seed,
+                            uint64_t offset, const int64_t *rows, int64_t nrows, double *out,
+                            double *lse, int nthreads) {
     if (!q || !k || !v || !out || !lse) return 1;
     if (block_mask && mask_heads != 1 && mask_heads != Hq) return 1;
+    if (keep_bits && keep_heads != 1 && keep_heads != Hq) return 1;
     if (B < 1 || Hq < 1 || Hkv < 1 || S < 1 || D < 1 || Hq % Hkv != 0) return 1;
     const int64_t total = (int64_t)B * Hq * S;
     if (!rows && nrows != total) return 1;
@@ -280,6 +296,7 @@ static int run_rows_dropout(const void *q, const void *k, const void *v, int for
         J->scale = (double)scale;
         J->causal = causal ? 1 : 0;
         J->block_mask = block_mask; J->mask_heads = mask_heads;
+        J->keep_bits = keep_bits; J->keep_heads = keep_heads;
         J->dropout_p8 = dropout_p8;
         J->dropout_key[0] = seed; J->dropout_key[1] = offset;
         J->rows = rows; J->nrows = nrows;
@@ -308,7 +325,7 @@ static int run_rows(const void *q, const void *k, const void *v, int format, con
                     const uint8_t *block_mask, int mask_heads,
                     const int64_t *rows, int64_t nrows, double *out, double *lse, int nthreads) {
     return run_rows_dropout(q, k, v, format, descale, B, Hq, Hkv, S, D, scale, causal, block_mask,
-                            mask_heads, 0, 0, 0, rows, nrows, out, lse, nthreads);
+                            mask_heads, NULL, 1, 0, 0, 0, rows, nrows, out, lse, nthreads);
 }
 
 /*
@@ -342,6 +359,25 @@ int oracle_attn_rows_masked(const uint16_t *q, const uint16_t *k, const uint16_t
     if (!block_mask) return 1;
     return run_rows(q, k, v, FMT_BF16, one, B, Hq, Hkv, S, D, scale, causal, block_mask,
                     mask_heads, rows, nrows, out, lse, nthreads);
+}
+
+/*
+ * oracle_attn_rows_keep -- oracle_attn_rows plus an element mask: keep_bits
+ * uint8 [keep_heads][S][16 * ceil(S / 128)], keep_heads 1 or Hq; bit j % 8 of
+ * byte j / 8 of row i keeps key j for query i.  block_mask (optional, NULL
+ * for none) as in oracle_attn_rows_masked.  Rows left without any key give
+ * O = 0 and LSE = -inf.
+ */
+int oracle_attn_rows_keep(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int Hq,
+                          int Hkv, int S, int D, float scale, int causal, const uint8_t *keep_bits,
+                          int keep_heads, const uint8_t *block_mask, int mask_heads,
+                          const int64_t *rows, int64_t nrows, double *out, double *lse,
+                          int nthreads) {
+    const double one[3] = {1.0, 1.0, 1.0};
+    if (!keep_bits) return 1;
+    return run_rows_dropout(q, k, v, FMT_BF16, one, B, Hq, Hkv, S, D, scale, causal, block_mask,
+                            block_mask ? mask_heads : 1, keep_bits, keep_heads, 0, 0, 0, rows,
+                            nrows, out, lse, nthreads);
 }
 
 /*
@@ -530,9 +566,9 @@ static int bwd_parallel(const bwd_job_t *proto, int pass, int64_t count, int nth
  */
 static int bwd_run(const void *q, const void *k, const void *v, const void *dout, int f64_inputs,
                    int B, int Hq, int Hkv, int S, int D, float scale, int causal,
-                   const uint8_t *block_mask, int mask_heads, const int64_t *kv_heads,
-                   int64_t n_kv_heads, double *dq, double *dk, double *dv, double *delta,
-                   int nthreads) {
+                   const uint8_t *block_mask, int mask_heads, const uint8_t *keep_bits,
+                   int keep_heads, const int64_t *kv_heads, int64_t n_kv_heads, double *dq,
+                   double *dk, double *dv, double *delta, int nthreads) {
     if (!q || !k || !v || !dout || !dq || !dk || !dv || !delta) return 1;
     if (B < 1 || Hq < 1 || Hkv < 1 || S < 1 || D < 1 || Hq % Hkv != 0) return 1;
     if (!kv_heads && n_kv_heads != (int64_t)B * Hkv) return 1;
@@ -550,6 +586,9 @@ static int bwd_run(const void *q, const void *k, const void *v, const void *dout
     if (block_mask && mask_heads != 1 && mask_heads != Hq) return 1;
     J.block_mask = block_mask;
     J.mask_heads = block_mask ? mask_heads : 1;
+    if (keep_bits && keep_heads != 1 && keep_heads != Hq) return 1;
+    J.keep_bits = keep_bits;
+    J.keep_heads = keep_bits ? keep_heads : 1;
     const int64_t G = Hq / Hkv;
     double *P = (double *)malloc(sizeof(double) * (size_t)(G * S) * (size_t)S);
     double *dS = (double *)malloc(sizeof(double) * (size_t)(G * S) * (size_t)S);
@@ -592,8 +631,8 @@ int oracle_attn_rows_dropout(const uint16_t *q, const uint16_t *k, const uint16_
                              double *lse, int nthreads) {
     const double one[3] = {1.0, 1.0, 1.0};
     if (p8 < 0 || p8 > 255) return 1;
-    return run_rows_dropout(q, k, v, FMT_BF16, one, B, Hq, Hkv, S, D, scale, causal, NULL, 1, p8,
-                            seed, offset, rows, nrows, out, lse, nthreads);
+    return run_rows_dropout(q, k, v, FMT_BF16, one, B, Hq, Hkv, S, D, scale, causal, NULL, 1, NULL,
+                            1, p8, seed, offset, rows, nrows, out, lse, nthreads);
 }
 
 /* Philox4x64-10 of one counter block (exposed so the generator can be pinned). */
@@ -605,8 +644,8 @@ int oracle_attn_bwd(const void *q, const void *k, const void *v, const void *dou
                     int B, int Hq, int Hkv, int S, int D, float scale, int causal,
                     const int64_t *kv_heads, int64_t n_kv_heads, double *dq, double *dk,
                     double *dv, double *delta, int nthreads) {
-    return bwd_run(q, k, v, dout, f64_inputs, B, Hq, Hkv, S, D, scale, causal, NULL, 1, kv_heads,
-                   n_kv_heads, dq, dk, dv, delta, nthreads);
+    return bwd_run(q, k, v, dout, f64_inputs, B, Hq, Hkv, S, D, scale, causal, NULL, 1, NULL, 1,
+                   kv_heads, n_kv_heads, dq, dk, dv, delta, nthreads);
 }
 
 /*
@@ -622,5 +661,22 @@ int oracle_attn_bwd_masked(const void *q, const void *k, const void *v, const vo
                            double *dv, double *delta, int nthreads) {
     if (!block_mask) return 1;
     return bwd_run(q, k, v, dout, f64_inputs, B, Hq, Hkv, S, D, scale, causal, block_mask,
-                   mask_heads, kv_heads, n_kv_heads, dq, dk, dv, delta, nthreads);
+                   mask_heads, NULL, 1, kv_heads, n_kv_heads, dq, dk, dv, delta, nthreads);
+}
+
+/*
+ * oracle_attn_bwd_keep -- oracle_attn_bwd for the element-masked attention of
+ * oracle_attn_rows_keep (block_mask optional).  Masked pairs have weight 0,
+ * so the same derivative applies.
+ */
+int oracle_attn_bwd_keep(const void *q, const void *k, const void *v, const void *dout,
+                         int f64_inputs, int B, int Hq, int Hkv, int S, int D, float scale,
+                         int causal, const uint8_t *keep_bits, int keep_heads,
+                         const uint8_t *block_mask, int mask_heads, const int64_t *kv_heads,
+                         int64_t n_kv_heads, double *dq, double *dk, double *dv, double *delta,
+                         int nthreads) {
+    if (!keep_bits) return 1;
+    return bwd_run(q, k, v, dout, f64_inputs, B, Hq, Hkv, S, D, scale, causal, block_mask,
+                   mask_heads, keep_bits, keep_heads, kv_heads, n_kv_heads, dq, dk, dv, delta,
+                   nthreads);
 }

@@ -658,3 +658,135 @@ def pin_bwd_masked_all_ones(bwdm, bwd):
 
 
 BWD_MASK_PINS = [pin_bwd_masked_library]
+
+
+# ---------------------------------------------------------------- element masks
+# ``attnk(q, k, v, scale, keep_bits, causal, block_mask=None)`` returns (O, LSE);
+# keep_bits uint8 [Hm, S, 16 * ceil(S/128)], bit j % 8 of byte j / 8 of row i
+# keeps key j for query i.
+
+def _keep_rows(S):
+    return 16 * ((S + 127) // 128)
+
+
+def _keep_to_bool(bits, S):
+    """Element mask [Hm, S, S] (True = kept) unpacked bit by bit, independently of
+    the packing helper the tests use to build masks."""
+    bits = np.asarray(bits, dtype=np.uint8)
+    j = np.arange(S)
+    return ((bits[:, :, j // 8] >> (j % 8)) & 1).astype(bool)
+
+
+def pin_keep_library(attnk):
+    """Random element masks (shared and per head, causal and not, GQA, with and
+    without a block mask on top) against torch's float64 SDPA with the same boolean
+    mask; rows that see no key are 0 there and must have LSE = -inf."""
+    rng = np.random.default_rng(311)
+    B, Hq, Hkv, S, D = 2, 4, 2, 300, 8
+    q, k, v = (_rand((B, H, S, D), 311, t) for t, H in ((0, Hq), (1, Hkv), (2, Hkv)))
+    scale = 0.35
+    sc32 = float(np.float32(scale))
+    qf = torch.from_numpy(f64(q))
+    kf = torch.from_numpy(f64(k)).repeat_interleave(Hq // Hkv, dim=1)
+    vf = torch.from_numpy(f64(v)).repeat_interleave(Hq // Hkv, dim=1)
+    for hm, causal, density, with_block in ((1, True, 0.5, False), (Hq, False, 0.3, False),
+                                            (Hq, True, 0.8, True), (1, False, 0.6, True)):
+        keep = rng.random((hm, S, S)) < density
+        keep[0, 7, :] = False  # query 7 of head 0 sees nothing
+        bits = np.zeros((hm, S, _keep_rows(S)), np.uint8)
+        for jj in range(S):
+            bits[:, :, jj // 8] |= (keep[:, :, jj].astype(np.uint8) << (jj % 8))
+        bm = (rng.random((hm, 3, 3)) < 0.7).astype(np.uint8) if with_block else None
+        O, L = attnk(q, k, v, scale, bits, causal, bm)
+        em = torch.from_numpy(keep).expand(Hq, S, S)
+        if bm is not None:
+            em = em & _expand_block_mask(bm, Hq, S, False)
+        if causal:
+            em = em & torch.ones(S, S, dtype=torch.bool).tril()
+        ref = F.scaled_dot_product_attention(qf, kf, vf, attn_mask=em, scale=sc32).numpy()
+        np.testing.assert_allclose(O, ref, rtol=0, atol=1e-12)
+        sc = torch.einsum("bhid,bhjd->bhij", qf, kf) * sc32
+        lse_ref = torch.logsumexp(sc.masked_fill(~em, float("-inf")), dim=-1).numpy()
+        none = ~em.any(dim=-1).numpy()
+        assert none[0, 7]
+        assert np.all(np.isneginf(L[:, none])) and np.all(O[:, none] == 0.0)
+        np.testing.assert_allclose(L[:, ~none], lse_ref[:, ~none], rtol=0, atol=1e-12)
+
+
+def pin_keep_selects_one_key(attnk):
+    """Bytes written by hand: query i keeping only key j gives O_i = V_j exactly and
+    LSE_i = the scaled score q_i . k_j (pins the bit order, the byte and row
+    offsets and the per-head indexing of the element mask)."""
+    B, H, S, D = 1, 2, 260, 8
+    q, k, v = (_rand((B, H, S, D), 321, t) for t in range(3))
+    R = _keep_rows(S)
+    picks = [(0, 0, 0), (0, 5, 3), (1, 200, 137), (1, 259, 258), (0, 130, 9), (1, 17, 16)]
+    bits = np.zeros((H, S, R), np.uint8)
+    for h, i, j in picks:
+        bits[h, i, j // 8] = np.uint8(1 << (j % 8))
+    O, L = attnk(q, k, v, 0.25, bits, False, None)
+    for h, i, j in picks:
+        assert np.array_equal(O[0, h, i], f64(v[0, h, j]))
+        s = float(np.dot(f64(q[0, h, i]), f64(k[0, h, j]))) * float(np.float32(0.25))
+        assert abs(L[0, h, i] - s) <= 1e-12 * max(1.0, abs(s))
+    others = np.ones((H, S), bool)
+    for h, i, _ in picks:
+        others[h, i] = False
+    assert np.all(O[0][others] == 0.0) and np.all(np.isneginf(L[0][others]))
+
+
+def pin_keep_equals_block_mask(attnk, attnm):
+    """An element mask that keeps exactly the pairs of a block mask gives the
+    block-masked result bit for bit; the all-ones element mask gives the unmasked one."""
+    rng = np.random.default_rng(331)
+    B, H, S, D = 1, 2, 300, 8
+    q, k, v = (_rand((B, H, S, D), 331, t) for t in range(3))
+    bm = (rng.random((H, 3, 3)) < 0.6).astype(np.uint8)
+    keep = np.repeat(np.repeat(bm, 128, axis=1), 128, axis=2)[:, :S, :S].astype(bool)
+    bits = np.zeros((H, S, _keep_rows(S)), np.uint8)
+    for jj in range(S):
+        bits[:, :, jj // 8] |= (keep[:, :, jj].astype(np.uint8) << (jj % 8))
+    for causal in (True, False):
+        Ok, Lk = attnk(q, k, v, 0.3, bits, causal, None)
+        Om, Lm = attnm(q, k, v, 0.3, bm, causal)
+        assert np.array_equal(Ok, Om) and np.array_equal(Lk, Lm)
+        ones = np.full((1, S, _keep_rows(S)), 0xFF, np.uint8)
+        Oa, La = attnk(q, k, v, 0.3, ones, causal, None)
+        Om1, Lm1 = attnm(q, k, v, 0.3, np.ones((1, 3, 3), np.uint8), causal)
+        assert np.array_equal(Oa, Om1) and np.array_equal(La, Lm1)
+        assert np.array_equal(_keep_to_bool(bits, S), keep)
+
+
+KEEP_PINS = [pin_keep_library, pin_keep_selects_one_key]
+
+
+def pin_bwd_keep_library(bwdk):
+    """Element-masked gradients against torch's float64 autograd through SDPA with
+    the same boolean mask (a row that sees no key has zero gradients on both sides)."""
+    B, Hq, Hkv, S, D = 1, 4, 2, 300, 8
+    q, k, v = (_rand((B, H, S, D), 341, t) for t, H in ((0, Hq), (1, Hkv), (2, Hkv)))
+    dout = _rand((B, Hq, S, D), 341, 3)
+    rng = np.random.default_rng(341)
+    G = Hq // Hkv
+    for hm, causal, density in ((Hq, True, 0.6), (1, False, 0.4)):
+        keep = rng.random((hm, S, S)) < density
+        keep[0, 11, :] = False
+        bits = np.zeros((hm, S, _keep_rows(S)), np.uint8)
+        for jj in range(S):
+            bits[:, :, jj // 8] |= (keep[:, :, jj].astype(np.uint8) << (jj % 8))
+        dq, dk, dv, _ = bwdk(q, k, v, dout, 0.5, causal, bits)
+        em = torch.from_numpy(keep).expand(Hq, S, S)
+        if causal:
+            em = em & torch.ones(S, S, dtype=torch.bool).tril()
+        tq, tk, tv = (torch.from_numpy(f64(x)).requires_grad_() for x in (q, k, v))
+        o = F.scaled_dot_product_attention(tq, tk.repeat_interleave(G, 1), tv.repeat_interleave(G, 1),
+                                           attn_mask=em[None], scale=float(np.float32(0.5)))
+        o.backward(torch.from_numpy(f64(dout)))
+        for name, a, t in (("dQ", dq, tq), ("dK", dk, tk), ("dV", dv, tv)):
+            ref = t.grad.numpy()
+            assert not np.isnan(ref).any()
+            assert np.max(np.abs(a - ref)) <= 1e-12 * max(1.0, float(np.max(np.abs(ref)))), name
+        assert np.all(dq[0, 0, 11] == 0.0)
+
+
+BWD_KEEP_PINS = [pin_bwd_keep_library]

@@ -62,6 +62,12 @@ MUTANTS = {
                               "const int64_t hq = W->hkv + g * J->Hkv;"),
     "bwd_dkdv_first_head_only": ("for (int64_t g = 0; g < W->G; ++g) {",
                                  "for (int64_t g = 0; g < 1; ++g) {"),
+    "keep_bit_order_reversed": ("if (((krow[j / 8] >> (j % 8)) & 1) == 0)",
+                                "if (((krow[j / 8] >> (7 - j % 8)) & 1) == 0)"),
+    "keep_row_stride_unpadded": ("const int64_t row_bytes = 16 * ((S + 127) / 128);",
+                                 "const int64_t row_bytes = (S + 7) / 8;"),
+    "keep_heads_ignored": ("(J->keep_heads == 1 ? 0 : hq)", "(0)"),
+    "keep_ignored": ("if (J->keep_bits) {", "if (0) {"),
 }
 
 
@@ -83,6 +89,10 @@ def test_some_pin_catches_mutant(name, tmp_path):
 
     def attnm(q, k, v, scale, mask, causal, rows=None):
         return oracle.attention_masked(q, k, v, scale, mask, causal, rows=rows, lib=lib)
+
+    def attnk(q, k, v, scale, bits, causal, block_mask=None, rows=None):
+        return oracle.attention_keep(q, k, v, scale, bits, causal, block_mask=block_mask, rows=rows,
+                                     lib=lib)
 
     def attnd(q, k, v, scale, p8, seed, offset, causal, rows=None):
         return oracle.attention_dropout(q, k, v, scale, p8, seed, offset, causal, rows=rows, lib=lib)
@@ -107,6 +117,10 @@ def test_some_pin_catches_mutant(name, tmp_path):
     ] + [(p.__name__, lambda p=p: p(attnd, attn)) for p in oracle_pins.DROPOUT_PINS] + [
         ("pin_bwd_masked_library", lambda: oracle_pins.pin_bwd_masked_library(
             lambda q, k, v, d, sc, c, m: oracle.attention_bwd(q, k, v, d, sc, c, block_mask=m, lib=lib))),
+    ] + [(p.__name__, lambda p=p: p(attnk)) for p in oracle_pins.KEEP_PINS] + [
+        ("pin_keep_equals_block_mask", lambda: oracle_pins.pin_keep_equals_block_mask(attnk, attnm)),
+        ("pin_bwd_keep_library", lambda: oracle_pins.pin_bwd_keep_library(
+            lambda q, k, v, d, sc, c, b: oracle.attention_bwd(q, k, v, d, sc, c, keep_bits=b, lib=lib))),
     ]
     caught = []
     for pin_name, run in checks:

@@ -168,3 +168,27 @@ def test_oracle_snapshot_small_workload():
     out_ref = np.array(out_ref)
     np.testing.assert_allclose(lse, lse_ref, rtol=0, atol=1e-12)
     np.testing.assert_allclose(out[:, :out_ref.shape[1]], out_ref, rtol=0, atol=1e-12)
+
+
+def _attnk(q, k, v, scale, bits, causal, block_mask=None, rows=None):
+    return oracle.attention_keep(q, k, v, scale, bits, causal, block_mask=block_mask, rows=rows)
+
+
+@pytest.mark.parametrize("pin", oracle_pins.KEEP_PINS, ids=lambda p: p.__name__)
+def test_oracle_keep_pin(pin):
+    pin(_attnk)
+
+
+def test_oracle_keep_equals_block_mask():
+    def attnm(q, k, v, scale, mask, causal, rows=None):
+        return oracle.attention_masked(q, k, v, scale, mask, causal, rows=rows)
+    oracle_pins.pin_keep_equals_block_mask(_attnk, attnm)
+
+
+def _bwdk(q, k, v, dout, scale, causal, bits, kv_heads=None):
+    return oracle.attention_bwd(q, k, v, dout, scale, causal, kv_heads=kv_heads, keep_bits=bits)
+
+
+@pytest.mark.parametrize("pin", oracle_pins.BWD_KEEP_PINS, ids=lambda p: p.__name__)
+def test_oracle_bwd_keep_pin(pin):
+    pin(_bwdk)
