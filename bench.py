@@ -9,7 +9,10 @@ A step is one attn_fwd call over the whole workload (all query rows of every
 batch and head).  FLOPs per step = 4*B*Hq*S^2*D / 2 (causal).  With
 --mask-density P the step is attn_fwd_block_masked with a seeded per-head
 block mask keeping each 128 x 128 block with probability P, and the FLOPs are
-4*D per visible (query, key) pair, counted exactly.  With --pass bwd the step
+4*D per visible (query, key) pair, counted exactly; with --window W it is
+attn_fwd_elem_masked with a local window (query i keeps keys i-W < j <= i, as
+keep bits) plus the block mask of the blocks the window touches, FLOPs = 4*D
+per kept pair.  With --pass bwd the step
 is one attn_bwd call (dQ, dK, dV for a seeded upstream gradient, O and LSE
 from attn_fwd beforehand) and FLOPs = 2.5x the forward's (five products per
 tile pair instead of two: the usual convention for attention backward).
@@ -171,6 +174,19 @@ def workload_mask(w, density: float):
     return random_block_mask(w.Hq, w.S, density, seed=w.seed)
 
 
+def workload_window(w, window: int):
+    """The element mask of --window: each query keeps the `window` keys ending at
+    itself, shared by all heads, with the block mask of the blocks it touches."""
+    from causal_scaled_dot_gb300.inputs import block_mask_of_keep_bits, window_keep_bits
+    bits = window_keep_bits(w.S, window)
+    return bits, block_mask_of_keep_bits(bits, w.S)
+
+
+def window_keys(S: int, window: int) -> np.ndarray:
+    """Keys each query row sees under the local window: [S]."""
+    return np.minimum(np.arange(S) + 1, window)
+
+
 def visible_keys(mask, S: int, causal: bool) -> np.ndarray:
     """Keys each query row sees under the block mask (and causality): [Hm, S]."""
     nt = mask.shape[1]
@@ -190,7 +206,7 @@ class OracleTimer:
     rows * 2*S*D and its TFLOP/s is comparable with the GPU's.
     """
 
-    def __init__(self, w, fp8: bool = False, mask=None, dropout_p8: int = 0):
+    def __init__(self, w, fp8: bool = False, mask=None, dropout_p8: int = 0, window=None):
         import oracle
         from causal_scaled_dot_gb300.inputs import qkv_bf16, qkv_e4m3
         self.oracle = oracle
@@ -203,8 +219,13 @@ class OracleTimer:
         self.row_flops = (2.0 if w.causal else 4.0) * w.S * w.D
         self.mask = mask
         self.p8 = dropout_p8
+        self.window = window
         if mask is not None:
             self.keys = visible_keys(mask, w.S, w.causal)  # [mask heads, S]
+            self.row_flops = 4.0 * w.D * float(self.keys.mean())
+        if window is not None:
+            self.bits, self.bm = workload_window(w, window)
+            self.keys = window_keys(w.S, window)[None, :]
             self.row_flops = 4.0 * w.D * float(self.keys.mean())
         n = max(self.threads, 32)
         self.run(n, seed=12345)  # warm the library and the page cache
@@ -214,7 +235,10 @@ class OracleTimer:
 
     def run(self, n, seed):
         rows = np.random.default_rng(seed).integers(0, self.total, n)
-        if self.mask is not None:
+        if self.window is not None:
+            self.oracle.attention_keep(self.q, self.k, self.v, self.w.scale, self.bits, self.w.causal,
+                                       block_mask=self.bm, rows=rows, nthreads=self.threads)
+        elif self.mask is not None:
             self.oracle.attention_masked(self.q, self.k, self.v, self.w.scale, self.mask,
                                          self.w.causal, rows=rows, nthreads=self.threads)
         elif self.p8:
@@ -230,7 +254,7 @@ class OracleTimer:
         return rows
 
     def flops_of(self, rows) -> float:
-        if self.mask is None:
+        if self.mask is None and self.window is None:
             return rows.size * self.row_flops
         S, Hq = self.w.S, self.w.Hq
         h = (rows // S) % Hq if self.keys.shape[0] > 1 else np.zeros_like(rows)
@@ -301,7 +325,8 @@ def make_oracle_timer(args, w, mask=None):
         return OracleBwdTimer(w, mask=mask)
     if args.pass_ == "proj":
         return OracleProjTimer(w)
-    return OracleTimer(w, fp8=args.dtype == "fp8", mask=mask, dropout_p8=dropout_p8(args))
+    return OracleTimer(w, fp8=args.dtype == "fp8", mask=mask, dropout_p8=dropout_p8(args),
+                       window=args.window)
 
 
 def metric_name(args) -> str:
@@ -353,6 +378,15 @@ class OracleProjTimer:
         return n * self.row_flops / dt / 1e12, n, dt
 
 
+def window_config(w, window):
+    if window is None:
+        return {}
+    return {"elem_mask": {"kind": "local window: query i keeps keys i-window < j <= i",
+                          "window": window, "heads": 1,
+                          "kept_pair_frac": float(window_keys(w.S, window).sum()) / (w.S * (w.S + 1) / 2),
+                          "block_mask": "derived: the 128x128 blocks holding a kept pair"}}
+
+
 def mask_config(mask, density):
     if mask is None:
         return {}
@@ -386,7 +420,7 @@ def run_reference(args, w, rank, world):
         "data": f"synthetic (seeded N(0,1) {'e4m3' if args.dtype == 'fp8' else 'bf16'})",
         "config": {"workload": w.name, **w.shape_dict, "causal": w.causal,
                    "inputs": "e4m3" if args.dtype == "fp8" else "bf16", "pass": args.pass_,
-                   **mask_config(mask, args.mask_density),
+                   **mask_config(mask, args.mask_density), **window_config(w, args.window),
                    **({"dropout_p": dropout_p8(args) / 256, "dropout_key": [DROPOUT_SEED, DROPOUT_OFFSET]}
                       if args.dropout is not None else {})},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": timer.threads,
@@ -421,6 +455,10 @@ def run_ours(args, w, rank, world, local):
     if mask is not None:
         flops = 4.0 * w.D * w.B * float(visible_keys(mask, w.S, w.causal).sum())
         mask_d = torch.from_numpy(mask).to(dev)
+    if args.window is not None:  # 4*D per kept (query, key) pair
+        keep_bits, keep_block = workload_window(w, args.window)
+        flops = 4.0 * w.D * w.B * w.Hq * float(window_keys(w.S, args.window).sum())
+        keep_d, keep_block_d = torch.from_numpy(keep_bits).to(dev), torch.from_numpy(keep_block).to(dev)
     out = torch.empty((w.B, w.Hq, w.S, w.D), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((w.B, w.Hq, w.S), dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -433,6 +471,9 @@ def run_ours(args, w, rank, world, local):
         elif mask is not None:
             native.attn_fwd_block_masked(q, k, v, out, lse, w.B, w.Hq, w.Hkv, w.S, w.D, w.scale,
                                          w.causal, mask_d, mask.shape[0], stream)
+        elif args.window is not None:
+            native.attn_fwd_elem_masked(q, k, v, out, lse, w.B, w.Hq, w.Hkv, w.S, w.D, w.scale,
+                                        w.causal, keep_d, 1, keep_block_d, 1, stream)
         elif args.dropout is not None:
             native.attn_fwd_dropout(q, k, v, out, lse, w.B, w.Hq, w.Hkv, w.S, w.D, w.scale, w.causal,
                                     args.dropout, DROPOUT_SEED, DROPOUT_OFFSET, stream)
@@ -532,13 +573,14 @@ def run_ours(args, w, rank, world, local):
         peak_what = f"{peak_src} bf16 dense (burst) x 2, the nominal fp8/bf16 ratio"
     achieved = flops / (ms_local * 1e-3) / 1e12
     variant = (w.name + (":fp8" if fp8 else "") + (f":mask{args.mask_density}" if mask is not None else "")
-               + (f":dropout{args.dropout}" if args.dropout is not None else ""))
+               + (f":dropout{args.dropout}" if args.dropout is not None else "")
+               + (f":window{args.window}" if args.window is not None else ""))
     traffic = recorded_traffic(variant)
     # algorithmic bytes: inputs read once (1 byte per element for E4M3), O and LSE written once
     io_bytes = w.io_bytes - (w.B * (w.Hq + 2 * w.Hkv) * w.S * w.D if fp8 else 0)
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        timer = OracleTimer(w, fp8=fp8, mask=mask, dropout_p8=dropout_p8(args))
+        timer = OracleTimer(w, fp8=fp8, mask=mask, dropout_p8=dropout_p8(args), window=args.window)
         tf, n, dt = timer.sample(args.cpu_seconds, seed=7)
         cpu = {"value": tf, "unit": "TFLOP/s", "cores": timer.threads, "kind": "oracle",
                "sample": f"{n} random query rows of {w.name} (of {timer.total}), "
@@ -551,6 +593,7 @@ def run_ours(args, w, rank, world, local):
         "data": f"synthetic (seeded N(0,1) {'e4m3' if fp8 else 'bf16'}, no weights)",
         "config": {"workload": w.name, **w.shape_dict, "causal": w.causal,
                    "inputs": "e4m3" if fp8 else "bf16", **mask_config(mask, args.mask_density),
+                   **window_config(w, args.window),
                    **({"dropout_p": dropout_p8(args) / 256, "dropout_key": [DROPOUT_SEED, DROPOUT_OFFSET]}
                       if args.dropout is not None else {}),
                    "l2": "flushed between timed steps (256 MiB write)",
@@ -845,6 +888,9 @@ def main():
     ap.add_argument("--dropout", type=float, default=None,
                     help="bf16 forward only: attn_fwd_dropout with this drop probability "
                          "(rounded to a multiple of 1/256)")
+    ap.add_argument("--window", type=int, default=None,
+                    help="bf16 forward only: attn_fwd_elem_masked with a local window of this many "
+                         "keys per query (element mask) and the block mask it implies")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="budget of the oracle CPU-baseline sample")
     ap.add_argument("--ref-step-seconds", type=float, default=8.0,
@@ -864,6 +910,9 @@ def main():
     if args.dropout is not None and (args.pass_ != "fwd" or args.dtype != "bf16" or args.mask_density is not None
                                      or not 0 < round(args.dropout * 256) < 256):
         ap.error("--dropout takes 0 < p < 1 (at least 1/256), bf16 forward, no mask")
+    if args.window is not None and (args.window < 1 or args.pass_ != "fwd" or args.dtype != "bf16"
+                                    or args.mask_density is not None or args.dropout is not None):
+        ap.error("--window takes a positive key count, bf16 forward, no other mask or dropout")
     w = BY_NAME[args.workload]
     rank, world, local = dist_init(args)
     if world != args.gpus and rank == 0:

@@ -62,13 +62,17 @@ int setup_device_locked(int dev) {
     if (cudaGetSymbolAddress(&word, g_attn_status) != cudaSuccess ||
         allow_smem(attn_fwd_simple_kernel<64>, SimpleLayout<64>::kDynamicSmem) != cudaSuccess ||
         allow_smem(attn_fwd_simple_kernel<128>, SimpleLayout<128>::kDynamicSmem) != cudaSuccess ||
-        allow_smem(attn_fwd_ws_kernel<64, false, false, false>, WsLayout<64, false>::kDynamicSmem) != cudaSuccess ||
-        allow_smem(attn_fwd_ws_kernel<128, false, false, false>, WsLayout<128, false>::kDynamicSmem) != cudaSuccess ||
-        allow_smem(attn_fwd_ws_kernel<128, true, false, false>, WsLayout<128, true>::kDynamicSmem) != cudaSuccess ||
-        allow_smem(attn_fwd_ws_kernel<64, false, true, false>, WsLayout<64, false>::kDynamicSmem) != cudaSuccess ||
-        allow_smem(attn_fwd_ws_kernel<128, false, true, false>, WsLayout<128, false>::kDynamicSmem) != cudaSuccess ||
-        allow_smem(attn_fwd_ws_kernel<64, false, false, true>, WsLayout<64, false>::kDynamicSmem) != cudaSuccess ||
-        allow_smem(attn_fwd_ws_kernel<128, false, false, true>, WsLayout<128, false>::kDynamicSmem) != cudaSuccess) {
+        allow_smem(attn_fwd_ws_kernel<64, false, false, false, false>, WsLayout<64, false>::kDynamicSmem) != cudaSuccess ||
+        allow_smem(attn_fwd_ws_kernel<128, false, false, false, false>, WsLayout<128, false>::kDynamicSmem) != cudaSuccess ||
+        allow_smem(attn_fwd_ws_kernel<128, true, false, false, false>, WsLayout<128, true>::kDynamicSmem) != cudaSuccess ||
+        allow_smem(attn_fwd_ws_kernel<64, false, true, false, false>, WsLayout<64, false>::kDynamicSmem) != cudaSuccess ||
+        allow_smem(attn_fwd_ws_kernel<128, false, true, false, false>, WsLayout<128, false>::kDynamicSmem) != cudaSuccess ||
+        allow_smem(attn_fwd_ws_kernel<64, false, false, true, false>, WsLayout<64, false>::kDynamicSmem) != cudaSuccess ||
+        allow_smem(attn_fwd_ws_kernel<128, false, false, true, false>, WsLayout<128, false>::kDynamicSmem) != cudaSuccess ||
+        allow_smem(attn_fwd_ws_kernel<64, false, false, false, true>, WsLayout<64, false>::kDynamicSmem) != cudaSuccess ||
+        allow_smem(attn_fwd_ws_kernel<128, false, false, false, true>, WsLayout<128, false>::kDynamicSmem) != cudaSuccess ||
+        allow_smem(attn_fwd_ws_kernel<64, false, true, false, true>, WsLayout<64, false>::kDynamicSmem) != cudaSuccess ||
+        allow_smem(attn_fwd_ws_kernel<128, false, true, false, true>, WsLayout<128, false>::kDynamicSmem) != cudaSuccess) {
         st.status = ATTN_ERR_DEVICE;
         return st.status;
     }
@@ -159,7 +163,7 @@ int launch_simple(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMa
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
-template <int D, bool F, bool M, bool DR = false>
+template <int D, bool F, bool M, bool DR = false, bool E = false>
 int launch_ws(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, FwdParams p,
               int sm_count, cudaStream_t stream) {
     const long long npairs = (p.num_q_tiles + 1) / 2;
@@ -167,7 +171,7 @@ int launch_ws(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& t
     if (units > (1ll << 31) - 1) return ATTN_ERR_UNSUPPORTED;
     p.num_units = (int)units;
     const int grid = (int)(units < sm_count ? units : sm_count);
-    attn_fwd_ws_kernel<D, F, M, DR><<<grid, WsLayout<D, F>::kThreads, WsLayout<D, F>::kDynamicSmem, stream>>>(
+    attn_fwd_ws_kernel<D, F, M, DR, E><<<grid, WsLayout<D, F>::kThreads, WsLayout<D, F>::kDynamicSmem, stream>>>(
         tq, tk, tv, p);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
@@ -205,7 +209,7 @@ namespace {
 int fwd_bf16(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
              int Hkv, int S, int D, float scale, int causal, const uint8_t* block_mask,
              int mask_heads, int dropout_p8, unsigned long long seed, unsigned long long offset,
-             void* stream);
+             void* stream, const uint8_t* keep_bits = nullptr, int keep_heads = 1);
 }  // namespace
 }  // namespace attn
 
@@ -224,6 +228,18 @@ extern "C" int attn_fwd_block_masked(const void* q, const void* k, const void* v
                           mask_heads, 0, 0, 0, stream);
 }
 
+extern "C" int attn_fwd_elem_masked(const void* q, const void* k, const void* v, void* out,
+                                    float* lse, int B, int Hq, int Hkv, int S, int D, float scale,
+                                    int causal, const unsigned char* keep_bits, int keep_heads,
+                                    const unsigned char* block_mask, int mask_heads, void* stream) {
+    if (keep_bits == nullptr || (keep_heads != 1 && keep_heads != Hq)) return ATTN_ERR_INVALID_ARG;
+    if (block_mask != nullptr && mask_heads != 1 && mask_heads != Hq) return ATTN_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(keep_bits) & 15u) return ATTN_ERR_MISALIGNED;
+    return attn::fwd_bf16(q, k, v, out, lse, B, Hq, Hkv, S, D, scale, causal, block_mask,
+                          block_mask != nullptr ? mask_heads : 1, 0, 0, 0, stream, keep_bits,
+                          keep_heads);
+}
+
 extern "C" int attn_fwd_dropout(const void* q, const void* k, const void* v, void* out, float* lse,
                                 int B, int Hq, int Hkv, int S, int D, float scale, int causal,
                                 float dropout_p, unsigned long long seed, unsigned long long offset,
@@ -240,7 +256,7 @@ namespace {
 int fwd_bf16(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
              int Hkv, int S, int D, float scale, int causal, const uint8_t* block_mask,
              int mask_heads, int dropout_p8, unsigned long long seed, unsigned long long offset,
-             void* stream) {
+             void* stream, const uint8_t* keep_bits, int keep_heads) {
     int rc = check_args(q, k, v, out, lse, B, Hq, Hkv, S, D, scale);
     if (rc != ATTN_OK) return rc;
     DeviceState* dev = nullptr;
@@ -270,6 +286,9 @@ int fwd_bf16(const void* q, const void* k, const void* v, void* out, float* lse,
     p.o_scale = 1.f;
     p.block_mask = block_mask;
     p.mask_heads = mask_heads;
+    p.keep_bits = keep_bits;
+    p.keep_heads = keep_heads;
+    p.keep_row_bytes = 16 * p.num_q_tiles;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (dropout_p8 > 0) {
         // Kept weights are scaled by 256 / (256 - p8) along with 1 / l.
@@ -279,6 +298,13 @@ int fwd_bf16(const void* q, const void* k, const void* v, void* out, float* lse,
         p.o_scale = 256.f / (float)(256 - dropout_p8);
         return D == 64 ? launch_ws<64, false, false, true>(tq, tk, tv, p, dev->sm_count, st)
                        : launch_ws<128, false, false, true>(tq, tk, tv, p, dev->sm_count, st);
+    }
+    if (keep_bits != nullptr) {
+        if (block_mask != nullptr)
+            return D == 64 ? launch_ws<64, false, true, false, true>(tq, tk, tv, p, dev->sm_count, st)
+                           : launch_ws<128, false, true, false, true>(tq, tk, tv, p, dev->sm_count, st);
+        return D == 64 ? launch_ws<64, false, false, false, true>(tq, tk, tv, p, dev->sm_count, st)
+                       : launch_ws<128, false, false, false, true>(tq, tk, tv, p, dev->sm_count, st);
     }
     // Block masks are handled by the persistent kernel only.
     if (block_mask == nullptr && use_simple_kernel())

@@ -28,6 +28,9 @@ struct FwdParams {
     int mask_heads;                 // 1 (one mask for all heads) or Hq
     int dropout_p8;                 // dropout kernels: weights dropped with probability p8 / 256
     unsigned long long dropout_seed, dropout_offset;  // Philox key
+    const uint8_t* keep_bits;       // element-masked kernels: [keep_heads][S][keep_row_bytes]
+    int keep_heads;                 // 1 (one mask for all heads) or Hq
+    int keep_row_bytes;             // 16 per 128 keys
 };
 
 }  // namespace attn

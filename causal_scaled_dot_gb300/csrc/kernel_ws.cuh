@@ -168,7 +168,7 @@ __device__ __forceinline__ uint32_t ws_bar(uint32_t base, int i) {
 }
 
 // ---------------------------------------------------------------- producer
-template <int D, bool F, bool M, bool DR>
+template <int D, bool F, bool M, bool DR, bool E>
 __device__ void ws_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                              const CUtensorMap* tm_v, const FwdParams& p, uint32_t base,
                              volatile int* abort_flag) {
@@ -230,7 +230,7 @@ drain:
 }
 
 // ---------------------------------------------------------------- MMA issuer
-template <int D, bool F, bool M, bool DR>
+template <int D, bool F, bool M, bool DR, bool E>
 __device__ void ws_mma_role(const FwdParams& p, uint32_t base, uint32_t tmem,
                             volatile int* abort_flag) {
     using L = WsLayout<D, F>;
@@ -380,7 +380,7 @@ __device__ void ws_mma_role(const FwdParams& p, uint32_t base, uint32_t tmem,
 }
 
 // ---------------------------------------------------------------- softmax
-template <int D, bool F, bool M, bool DR>
+template <int D, bool F, bool M, bool DR, bool E>
 __device__ void ws_softmax_role(const FwdParams& p, uint32_t base, uint32_t tmem, int wg,
                                 volatile int* abort_flag) {
     using L = WsLayout<D, F>;
@@ -403,9 +403,30 @@ __device__ void ws_softmax_role(const FwdParams& p, uint32_t base, uint32_t tmem
         const int n_i = wg == 0 ? w.n0 : w.n1;
         float m_run = 0.f;  // reference maximum (log2 units), set by the first tile
         float l_run = 0.f;
-        bool first = true;
+        bool first = true;  // no visible key yet
+        // Element-masked kernels: this row's 16 keep bytes per key tile, read
+        // one key tile ahead so that the load is not on the tile's critical path.
+        const uint8_t* keep_row = nullptr;
+        uint4 keep_next = make_uint4(~0u, ~0u, ~0u, ~0u);
+        int keep_next_j = -1;
+        if constexpr (E) {
+            const int row = qt * kTile + r;
+            if (row < p.S)
+                keep_row = p.keep_bits +
+                           ((size_t)(p.keep_heads == 1 ? 0 : w.hq) * p.S + row) * (size_t)p.keep_row_bytes;
+        }
         for (int j = 0; j < n_i; ++j) {
             if (!tile_active<M>(p, w, wg, j)) continue;
+            uint4 keep = make_uint4(~0u, ~0u, ~0u, ~0u);
+            if constexpr (E) {
+                if (keep_row != nullptr) {
+                    keep = keep_next_j == j ? keep_next : __ldg(reinterpret_cast<const uint4*>(keep_row + 16 * j));
+                    if (j + 1 < n_i) {
+                        keep_next = __ldg(reinterpret_cast<const uint4*>(keep_row + 16 * (j + 1)));
+                        keep_next_j = j + 1;
+                    }
+                }
+            }
             bool ok = ptx::mbar_wait(bar_s, s_phase, abort_flag, p.status, lim);
             if (!__all_sync(0xffffffffu, ok)) return;
             s_phase ^= 1u;
@@ -432,6 +453,14 @@ __device__ void ws_softmax_role(const FwdParams& p, uint32_t base, uint32_t tmem
                 for (int c = 0; c < 128; ++c)
                     if (c >= lim_c) s[c] = -INFINITY;  // key past the end
             }
+            if constexpr (E) {
+                // Key kv0 + c is kept when bit c % 8 of byte c / 8 of the row's
+                // 16 bytes for this key tile is set.
+                const uint32_t kw[4] = {keep.x, keep.y, keep.z, keep.w};
+#pragma unroll
+                for (int c = 0; c < 128; ++c)
+                    if (((kw[c >> 5] >> (c & 31)) & 1u) == 0u) s[c] = -INFINITY;
+            }
             float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
             for (int c = 0; c < 128; c += 8) {
@@ -441,14 +470,19 @@ __device__ void ws_softmax_role(const FwdParams& p, uint32_t base, uint32_t tmem
                 mx3 = ptx::max3(mx3, s[c + 6], s[c + 7]);
             }
             const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
-            // Every row has at least one unmasked key in every tile it visits
-            // (all keys of an off-diagonal tile; the first key of a diagonal
-            // tile; key kv0 < S of the last tile), so mt is finite.
+            // Without an element mask every row has at least one unmasked key in
+            // every tile it visits (all keys of an off-diagonal tile; the first
+            // key of a diagonal tile; key kv0 < S of the last tile), so mt is
+            // finite.  With one, mt = -inf when the tile shows the row nothing:
+            // the reference maximum stays unset (its finite initial value makes
+            // every probability 0) until a tile shows a key.
             float alpha = 1.f;
             bool rescale = false;
             if (first) {
-                m_run = mt;
-                first = false;
+                if (!E || mt > -INFINITY) {
+                    m_run = mt;
+                    first = false;
+                }
             } else if (mt > m_run + kRescaleSlack) {
                 alpha = ptx::ex2(m_run - mt);
                 m_run = mt;
@@ -561,20 +595,27 @@ __device__ void ws_softmax_role(const FwdParams& p, uint32_t base, uint32_t tmem
         const int row = qt * kTile + r;
         const bool valid = row < p.S;
         __nv_bfloat16* orow = p.out + ((size_t)w.bh * p.S + row) * D;
-        if (M && first) {
-            // No key tile for this query tile (block mask): no key is visible to
-            // any of its rows.  O = 0 and LSE = -inf; TMEM O was never written.
+        // A row that sees no key (a block mask keeping no key tile of the query
+        // tile, or an element mask) gets O = 0 and LSE = -inf.  When no row of
+        // the warp sees a key, TMEM O is not read (with a block mask it was
+        // never written); otherwise the tensor-memory loads stay warp-wide and
+        // such rows write zeros.
+        const bool none = (M || E) && __all_sync(0xffffffffu, first);
+        if (none) {
             if (valid) {
 #pragma unroll 1
                 for (int c = 0; c < D; c += 8)
                     *reinterpret_cast<uint4*>(orow + c) = make_uint4(0u, 0u, 0u, 0u);
                 if (p.lse != nullptr) p.lse[(size_t)w.bh * p.S + row] = -INFINITY;
             }
-            __syncwarp();
-            if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(ws_bar<D, F>(base, L::kOEmpty + wg));
+            if constexpr (M) {
+                __syncwarp();
+                if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(ws_bar<D, F>(base, L::kOEmpty + wg));
+            }
             continue;
         }
-        const float inv_l = p.o_scale / l_run;  // o_scale: the V descale (1 for bf16)
+        const bool row_none = E && first;  // (only element masks leave single rows empty)
+        const float inv_l = row_none ? 0.f : p.o_scale / l_run;  // o_scale: the V descale (1 for bf16)
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
             uint32_t o[32];
@@ -599,7 +640,7 @@ __device__ void ws_softmax_role(const FwdParams& p, uint32_t base, uint32_t tmem
             }
         }
         if (valid && p.lse != nullptr)
-            p.lse[(size_t)w.bh * p.S + row] = (m_run + ptx::lg2(l_run)) * kLn2;
+            p.lse[(size_t)w.bh * p.S + row] = row_none ? -INFINITY : (m_run + ptx::lg2(l_run)) * kLn2;
         if constexpr (M) {  // O_i read out: the next unit may produce its own
             ptx::tc_fence_before();
             __syncwarp();
@@ -609,7 +650,7 @@ __device__ void ws_softmax_role(const FwdParams& p, uint32_t base, uint32_t tmem
 }
 
 // ---------------------------------------------------------------- kernel
-template <int D, bool F, bool M, bool DR>
+template <int D, bool F, bool M, bool DR, bool E>
 __global__ void __launch_bounds__(WsLayout<D, F>::kThreads, 1)
     attn_fwd_ws_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
@@ -656,13 +697,13 @@ __global__ void __launch_bounds__(WsLayout<D, F>::kThreads, 1)
     if (warp < 4) {
         ptx::regs_dec<L::kRegsSmall>();
         if (warp == 0) {
-            if (lane == 0) ws_load_role<D, F, M, DR>(&tm_q, &tm_k, &tm_v, p, base, abort_flag);
+            if (lane == 0) ws_load_role<D, F, M, DR, E>(&tm_q, &tm_k, &tm_v, p, base, abort_flag);
         } else if (warp == 1) {
-            if (lane == 0) ws_mma_role<D, F, M, DR>(p, base, tmem, abort_flag);
+            if (lane == 0) ws_mma_role<D, F, M, DR, E>(p, base, tmem, abort_flag);
         }
     } else {
         ptx::regs_inc<L::kRegsSoftmax>();
-        ws_softmax_role<D, F, M, DR>(p, base, tmem, (warp - 4) >> 2, abort_flag);
+        ws_softmax_role<D, F, M, DR, E>(p, base, tmem, (warp - 4) >> 2, abort_flag);
     }
 
     ptx::tc_fence_before();

@@ -48,6 +48,9 @@ def load() -> ctypes.CDLL:
         lib.attn_fwd_block_masked.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, ci, vp, ci,
                                               vp]
         lib.attn_fwd_block_masked.restype = ci
+        lib.attn_fwd_elem_masked.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, ci, vp, ci,
+                                             vp, ci, vp]
+        lib.attn_fwd_elem_masked.restype = ci
         lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, ci,
                                  vp]
         lib.attn_bwd.restype = ci
@@ -132,6 +135,22 @@ def attn_fwd_block_masked(q, k, v, out, lse, B: int, Hq: int, Hkv: int, S: int, 
                                       _stream(stream))
     if check and rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_block_masked")
+    return rc
+
+
+def attn_fwd_elem_masked(q, k, v, out, lse, B: int, Hq: int, Hkv: int, S: int, D: int,
+                         scale: float, causal: bool | int, keep_bits, keep_heads: int,
+                         block_mask=None, mask_heads: int = 1, stream=None,
+                         check: bool = True) -> int:
+    """The C entry point ``attn_fwd_elem_masked``: ``keep_bits`` is a uint8 CUDA
+    tensor (or device pointer) [keep_heads, S, 16*ceil(S/128)] of keep bits;
+    ``block_mask`` optional as in ``attn_fwd_block_masked``."""
+    rc = load().attn_fwd_elem_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), int(B),
+                                     int(Hq), int(Hkv), int(S), int(D), float(scale),
+                                     1 if causal else 0, _ptr(keep_bits), int(keep_heads),
+                                     _ptr(block_mask), int(mask_heads), _stream(stream))
+    if check and rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_elem_masked")
     return rc
 
 

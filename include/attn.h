@@ -142,6 +142,37 @@ int attn_fwd_fp8(const void *q, const void *k, const void *v, float q_descale, f
                  float scale, int causal, void *stream);
 
 /*
+ * attn_fwd_elem_masked -- attn_fwd plus an element mask that drops single
+ * (query, key) pairs: the arbitrary masks the ai-manual.ru article gives,
+ * with block-sparse ones, as a reason to write custom kernels (sections 4 and
+ * 7).  Key j is masked for query i of head h when
+ *     (keep_bits[h][i][j / 8] >> (j % 8)) & 1 == 0
+ * on top of the causal mask when causal != 0, and on top of an optional block
+ * mask (as in attn_fwd_block_masked).
+ *
+ *   keep_bits   device memory, uint8 [keep_heads][S][16 * ceil(S / 128)],
+ *               contiguous and 16-byte aligned: row i holds one bit per key,
+ *               16 bytes per 128 keys (bits past key S - 1 are ignored).
+ *               Read-only, caller-owned.
+ *   keep_heads  1 (one mask for every batch entry and head) or Hq (one per
+ *               query head, shared across the batch).
+ *   block_mask  NULL, or uint8 [mask_heads][nt][nt] as in attn_fwd_block_masked;
+ *               blocks it drops are neither loaded nor computed.  Without it
+ *               every block within the causal bound is computed, so callers
+ *               whose element mask leaves whole blocks empty should pass the
+ *               matching block mask too.
+ *   mask_heads  1 or Hq (ignored when block_mask is NULL).
+ * A query whose keys are all masked gets O = 0 and LSE = -inf.  Other
+ * arguments, errors and rules as attn_fwd; ATTN_ERR_INVALID_ARG also for a
+ * NULL keep_bits or keep_heads / mask_heads not 1 or Hq, ATTN_ERR_MISALIGNED
+ * for keep_bits not 16-byte aligned.  The caller guarantees the sizes above.
+ */
+int attn_fwd_elem_masked(const void *q, const void *k, const void *v, void *out, float *lse,
+                         int B, int Hq, int Hkv, int S, int D, float scale, int causal,
+                         const unsigned char *keep_bits, int keep_heads,
+                         const unsigned char *block_mask, int mask_heads, void *stream);
+
+/*
  * attn_bwd -- gradients of attn_fwd's output: dQ, dK, dV for an upstream
  * gradient dO.  The pages give no formula (the ai-manual.ru article, section 6,
  * only warns that the fused backward pass is hard to get right); this is the

@@ -240,3 +240,22 @@ def run_gpu_bwd_masked(q_bits, k_bits, v_bits, do_bits, scale, causal, block_mas
                                  causal, m, hm, stream=stream)
     native.attn_sync_status(stream)
     return tuple(t.double().cpu().numpy() for t in (out, lse, dq, dk, dv, delta))
+
+
+def run_gpu_elem_masked(q_bits, k_bits, v_bits, scale, causal, keep_bits, block_mask=None,
+                        stream=None):
+    """attn_fwd_elem_masked through the C ABI; returns (O float64, LSE float64)."""
+    import torch
+    from causal_scaled_dot_gb300 import native
+    B, Hq, S, D = q_bits.shape
+    Hkv = k_bits.shape[1]
+    q, k, v = to_device(q_bits), to_device(k_bits), to_device(v_bits)
+    kb = torch.from_numpy(np.ascontiguousarray(keep_bits, dtype=np.uint8)).cuda()
+    bm = None if block_mask is None else torch.from_numpy(np.ascontiguousarray(block_mask, dtype=np.uint8)).cuda()
+    out = torch.full_like(q, float("nan"))
+    lse = torch.full((B, Hq, S), float("nan"), dtype=torch.float32, device="cuda")
+    native.attn_fwd_elem_masked(q, k, v, out, lse, B, Hq, Hkv, S, D, scale, causal, kb,
+                                keep_bits.shape[0], bm, 1 if block_mask is None else block_mask.shape[0],
+                                stream=stream)
+    native.attn_sync_status(stream)
+    return out.double().cpu().numpy(), lse.double().cpu().numpy()

@@ -27,7 +27,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for required in ("attn_fwd", "attn_fwd_fp8", "attn_fwd_block_masked", "attn_fwd_dropout",
+    for required in ("attn_fwd", "attn_fwd_fp8", "attn_fwd_block_masked", "attn_fwd_elem_masked",
+                     "attn_fwd_dropout",
                      "attn_bwd", "attn_bwd_block_masked", "attn_out_proj", "attn_status_string",
                      "attn_sync_status"):
         assert required in names
@@ -146,6 +147,49 @@ def _call_masked(mask=5 << 40, mask_heads=1, q=1 << 40, k=2 << 40, v=3 << 40, ou
 ])
 def test_masked_argument_errors_are_rejected_before_launch(kw, code):
     assert _call_masked(**kw) == code
+
+
+def _call_elem(keep=6 << 40, keep_heads=1, mask=None, mask_heads=1, q=1 << 40, k=2 << 40,
+               v=3 << 40, out=4 << 40, lse=None, B=1, Hq=2, Hkv=2, S=300, D=128, scale=0.1,
+               causal=1):
+    lib = native.load()
+    return lib.attn_fwd_elem_masked(q, k, v, out, lse, B, Hq, Hkv, S, D, ctypes.c_float(scale),
+                                    causal, keep, keep_heads, mask, mask_heads, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(keep=None), ATTN_ERR_INVALID_ARG),
+    (dict(keep_heads=0), ATTN_ERR_INVALID_ARG),
+    (dict(keep_heads=3), ATTN_ERR_INVALID_ARG),   # neither 1 nor Hq
+    (dict(mask=5 << 40, mask_heads=3), ATTN_ERR_INVALID_ARG),
+    (dict(keep=(6 << 40) + 8), ATTN_ERR_MISALIGNED),
+    (dict(q=None), ATTN_ERR_INVALID_ARG),
+    (dict(D=96), ATTN_ERR_UNSUPPORTED),
+    (dict(k=(2 << 40) + 2), ATTN_ERR_MISALIGNED),
+])
+def test_elem_masked_argument_errors_are_rejected_before_launch(kw, code):
+    assert _call_elem(**kw) == code
+
+
+def test_keep_bit_packing():
+    from causal_scaled_dot_gb300.inputs import (block_mask_of_keep_bits, keep_row_bytes, pack_keep_bits,
+                                                random_keep_bits, unpack_keep_bits, window_keep_bits)
+    assert keep_row_bytes(1) == 16 and keep_row_bytes(128) == 16 and keep_row_bytes(129) == 32
+    b = random_keep_bits(2, 300, 0.4, seed=3)
+    assert b.shape == (2, 300, 48) and np.array_equal(b, random_keep_bits(2, 300, 0.4, seed=3))
+    keep = unpack_keep_bits(b, 300)
+    assert abs(float(keep.mean()) - 0.4) < 0.01
+    assert np.array_equal(pack_keep_bits(keep), b)
+    # bit j % 8 of byte j / 8, padding bits zero
+    one = np.zeros((1, 130, 130), bool)
+    one[0, 5, 129] = True
+    packed = pack_keep_bits(one)
+    assert packed[0, 5, 16] == 2 and packed.sum() == 2
+    w = unpack_keep_bits(window_keep_bits(300, 64), 300)[0]
+    i, j = np.nonzero(w)
+    assert np.all((j <= i) & (j > i - 64)) and w.sum() == sum(min(64, r + 1) for r in range(300))
+    bm = block_mask_of_keep_bits(window_keep_bits(600, 100), 600)[0]
+    assert bm.shape == (5, 5) and np.array_equal(bm, np.eye(5, dtype=np.uint8) + np.eye(5, k=-1, dtype=np.uint8))
 
 
 def test_random_block_mask_shape_and_density():
