@@ -455,11 +455,13 @@ __device__ void ws_softmax_role(const FwdParams& p, uint32_t base, uint32_t tmem
             }
             if constexpr (E) {
                 // Key kv0 + c is kept when bit c % 8 of byte c / 8 of the row's
-                // 16 bytes for this key tile is set.
-                const uint32_t kw[4] = {keep.x, keep.y, keep.z, keep.w};
+                // 16 bytes for this key tile is set (nothing to do when all are).
+                if ((keep.x & keep.y & keep.z & keep.w) != 0xFFFFFFFFu) {
+                    const uint32_t kw[4] = {keep.x, keep.y, keep.z, keep.w};
 #pragma unroll
-                for (int c = 0; c < 128; ++c)
-                    if (((kw[c >> 5] >> (c & 31)) & 1u) == 0u) s[c] = -INFINITY;
+                    for (int c = 0; c < 128; ++c)
+                        if (((kw[c >> 5] >> (c & 31)) & 1u) == 0u) s[c] = -INFINITY;
+                }
             }
             float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
