@@ -277,12 +277,13 @@ class OracleBwdTimer:
     with every query head of its group); a head carries 1/(B*Hkv) of the
     metric's FLOPs."""
 
-    def __init__(self, w, mask=None):
+    def __init__(self, w, mask=None, window=None):
         import oracle
         from causal_scaled_dot_gb300.inputs import gaussian_bf16, qkv_bf16
         self.oracle = oracle
         self.w = w
         self.mask = mask
+        self.keep = None
         self.q, self.k, self.v = qkv_bf16(w.B, w.Hq, w.Hkv, w.S, w.D, seed=w.seed, sigma=w.sigma)
         self.do = gaussian_bf16((w.B, w.Hq, w.S, w.D), w.seed, 3)
         self.threads = oracle.default_threads()
@@ -294,6 +295,9 @@ class OracleBwdTimer:
             per_hq = vis if mask.shape[0] == w.Hq else np.repeat(vis, w.Hq)
             self.head_flops = np.array([2.5 * 4.0 * w.D * per_hq[(h % w.Hkv) * G:(h % w.Hkv + 1) * G].sum()
                                         for h in range(self.total)])
+        if window is not None:  # every head: 2.5 x 4D x G x the window's kept pairs
+            self.keep, self.mask = workload_window(w, window)
+            self.head_flops = np.full(self.total, 2.5 * 4.0 * w.D * G * float(window_keys(w.S, window).sum()))
         t0 = time.perf_counter()
         self.run(1, seed=12345)
         self.sec_per_row = time.perf_counter() - t0
@@ -301,7 +305,8 @@ class OracleBwdTimer:
     def run(self, n, seed):
         heads = np.random.default_rng(seed).integers(0, self.total, n)
         self.oracle.attention_bwd(self.q, self.k, self.v, self.do, self.w.scale, self.w.causal,
-                                  kv_heads=heads, nthreads=self.threads, block_mask=self.mask)
+                                  kv_heads=heads, nthreads=self.threads, block_mask=self.mask,
+                                  keep_bits=self.keep)
         return heads
 
     def rows_for(self, seconds):
@@ -322,7 +327,7 @@ def dropout_p8(args) -> int:
 
 def make_oracle_timer(args, w, mask=None):
     if args.pass_ == "bwd":
-        return OracleBwdTimer(w, mask=mask)
+        return OracleBwdTimer(w, mask=mask, window=args.window)
     if args.pass_ == "proj":
         return OracleProjTimer(w)
     return OracleTimer(w, fp8=args.dtype == "fp8", mask=mask, dropout_p8=dropout_p8(args),
@@ -643,6 +648,11 @@ def run_ours_bwd(args, w, rank, world, local):
         mask_d = torch.from_numpy(mask).to(dev)
         native.attn_fwd_block_masked(q, k, v, out, lse, w.B, w.Hq, w.Hkv, w.S, w.D, w.scale, w.causal,
                                      mask_d, mask.shape[0], stream)
+    elif args.window is not None:
+        keep_bits, keep_block = workload_window(w, args.window)
+        keep_d, keep_block_d = torch.from_numpy(keep_bits).to(dev), torch.from_numpy(keep_block).to(dev)
+        native.attn_fwd_elem_masked(q, k, v, out, lse, w.B, w.Hq, w.Hkv, w.S, w.D, w.scale, w.causal,
+                                    keep_d, 1, keep_block_d, 1, stream)
     else:
         native.attn_fwd(q, k, v, out, lse, w.B, w.Hq, w.Hkv, w.S, w.D, w.scale, w.causal, stream)
     outh, lseh = out.cpu().pin_memory(), lse.cpu().pin_memory()
@@ -652,11 +662,16 @@ def run_ours_bwd(args, w, rank, world, local):
     flops = 2.5 * w.flops
     if mask is not None:  # 2.5x the forward's FLOPs over the visible pairs
         flops = 2.5 * 4.0 * w.D * w.B * float(visible_keys(mask, w.S, w.causal).sum())
+    if args.window is not None:  # ... over the kept pairs
+        flops = 2.5 * 4.0 * w.D * w.B * w.Hq * float(window_keys(w.S, args.window).sum())
 
     def step():
         if mask is not None:
             native.attn_bwd_block_masked(q, k, v, out, do, lse, delta, dq, dk, dv, w.B, w.Hq, w.Hkv,
                                          w.S, w.D, w.scale, w.causal, mask_d, mask.shape[0], stream)
+        elif args.window is not None:
+            native.attn_bwd_elem_masked(q, k, v, out, do, lse, delta, dq, dk, dv, w.B, w.Hq, w.Hkv,
+                                        w.S, w.D, w.scale, w.causal, keep_d, 1, keep_block_d, 1, stream)
         else:
             native.attn_bwd(q, k, v, out, do, lse, delta, dq, dk, dv, w.B, w.Hq, w.Hkv, w.S, w.D,
                             w.scale, w.causal, stream)
@@ -724,7 +739,7 @@ def run_ours_bwd(args, w, rank, world, local):
     io_bytes = 3 * q_b + 2 * kv_b + row_b + q_b + 2 * kv_b + 2 * row_b
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        timer = OracleBwdTimer(w, mask=mask)
+        timer = OracleBwdTimer(w, mask=mask, window=args.window)
         tf, n, dt = timer.sample(args.cpu_seconds, seed=7)
         cpu = {"value": tf, "unit": "TFLOP/s", "cores": timer.threads, "kind": "oracle",
                "sample": f"gradients of {n} random key/value heads of {w.name} (of {timer.total}), "
@@ -735,14 +750,16 @@ def run_ours_bwd(args, w, rank, world, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16 Q, K, V, dO; no weights)",
         "config": {"workload": w.name, **w.shape_dict, "causal": w.causal, "inputs": "bf16",
-                   "pass": "bwd", **mask_config(mask, args.mask_density),
+                   "pass": "bwd", **mask_config(mask, args.mask_density), **window_config(w, args.window),
                    "l2": "flushed between timed steps (256 MiB write)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "pct_of_peak": 100.0 * achieved / peak,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak,
                      "traffic": recorded_traffic(w.name + ":bwd" + (f":mask{args.mask_density}" if mask is not None
-                                                                   else ""), BWD_SOURCES),
+                                                                   else "")
+                                                 + (f":window{args.window}" if args.window is not None else ""),
+                                                 BWD_SOURCES),
                      "peak_source": f"{peak_src} bf16 dense (burst)",
                      "kernel": "attn_bwd call (dQ kernel + dK/dV kernel)",
                      "hbm_gbs": io_bytes / (ms_local * 1e-3) / 1e9},
@@ -889,8 +906,9 @@ def main():
                     help="bf16 forward only: attn_fwd_dropout with this drop probability "
                          "(rounded to a multiple of 1/256)")
     ap.add_argument("--window", type=int, default=None,
-                    help="bf16 forward only: attn_fwd_elem_masked with a local window of this many "
-                         "keys per query (element mask) and the block mask it implies")
+                    help="bf16 only: attn_fwd_elem_masked (with --pass bwd: attn_bwd_elem_masked) with a "
+                         "local window of this many keys per query (element mask) and the block mask it "
+                         "implies")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="budget of the oracle CPU-baseline sample")
     ap.add_argument("--ref-step-seconds", type=float, default=8.0,
@@ -910,9 +928,9 @@ def main():
     if args.dropout is not None and (args.pass_ != "fwd" or args.dtype != "bf16" or args.mask_density is not None
                                      or not 0 < round(args.dropout * 256) < 256):
         ap.error("--dropout takes 0 < p < 1 (at least 1/256), bf16 forward, no mask")
-    if args.window is not None and (args.window < 1 or args.pass_ != "fwd" or args.dtype != "bf16"
+    if args.window is not None and (args.window < 1 or args.pass_ == "proj" or args.dtype != "bf16"
                                     or args.mask_density is not None or args.dropout is not None):
-        ap.error("--window takes a positive key count, bf16 forward, no other mask or dropout")
+        ap.error("--window takes a positive key count, bf16 forward or backward, no other mask or dropout")
     w = BY_NAME[args.workload]
     rank, world, local = dist_init(args)
     if world != args.gpus and rank == 0:

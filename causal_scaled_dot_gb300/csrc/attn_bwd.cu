@@ -26,6 +26,12 @@ cudaError_t allow_smem(K kernel, uint32_t bytes) {
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
+template <int D, bool M, bool E>
+bool allow_all() {
+    return allow_smem(attn_bwd_dq_kernel<D, M, E>, DqLayout<D>::kDynamicSmem) == cudaSuccess &&
+           allow_smem(attn_bwd_dkdv_kernel<D, M, E>, DkvLayout<D>::kDynamicSmem) == cudaSuccess;
+}
+
 // Shared-memory opt-in of the backward kernels, once per device.
 int setup_bwd_kernels() {
     int dev = -1;
@@ -33,14 +39,10 @@ int setup_bwd_kernels() {
     std::lock_guard<std::mutex> lock(g_bwd_mutex);
     if (g_bwd_ready[dev] == 0) {
         const bool ok =
-            allow_smem(attn_bwd_dq_kernel<64, false>, DqLayout<64>::kDynamicSmem) == cudaSuccess &&
-            allow_smem(attn_bwd_dq_kernel<128, false>, DqLayout<128>::kDynamicSmem) == cudaSuccess &&
-            allow_smem(attn_bwd_dkdv_kernel<64, false>, DkvLayout<64>::kDynamicSmem) == cudaSuccess &&
-            allow_smem(attn_bwd_dkdv_kernel<128, false>, DkvLayout<128>::kDynamicSmem) == cudaSuccess &&
-            allow_smem(attn_bwd_dq_kernel<64, true>, DqLayout<64>::kDynamicSmem) == cudaSuccess &&
-            allow_smem(attn_bwd_dq_kernel<128, true>, DqLayout<128>::kDynamicSmem) == cudaSuccess &&
-            allow_smem(attn_bwd_dkdv_kernel<64, true>, DkvLayout<64>::kDynamicSmem) == cudaSuccess &&
-            allow_smem(attn_bwd_dkdv_kernel<128, true>, DkvLayout<128>::kDynamicSmem) == cudaSuccess;
+            allow_all<64, false, false>() && allow_all<128, false, false>() &&
+            allow_all<64, true, false>() && allow_all<128, true, false>() &&
+            allow_all<64, false, true>() && allow_all<128, false, true>() &&
+            allow_all<64, true, true>() && allow_all<128, true, true>();
         g_bwd_ready[dev] = ok ? 1 : ATTN_ERR_DEVICE;
     }
     return g_bwd_ready[dev] == 1 ? ATTN_OK : g_bwd_ready[dev];
@@ -76,7 +78,7 @@ int check_bwd_args(const void* q, const void* k, const void* v, const void* out,
     return ATTN_OK;
 }
 
-template <int D, bool M>
+template <int D, bool M, bool E>
 int launch_bwd(const CUtensorMap& tq, const CUtensorMap& tdo, const CUtensorMap& tk,
                const CUtensorMap& tv, BwdParams p, int sm_count, cudaStream_t stream) {
     const long long dq_units = (long long)p.B * p.Hq * p.num_tiles;
@@ -87,18 +89,19 @@ int launch_bwd(const CUtensorMap& tq, const CUtensorMap& tdo, const CUtensorMap&
     // About eight units per CTA per head block: nearly the balance of a single
     // tile-major order, with half or less of the heads' operands live in L2.
     p.head_block = std::min(p.B * p.Hq, (8 * grid + p.num_tiles - 1) / p.num_tiles);
-    attn_bwd_dq_kernel<D, M><<<grid, DqLayout<D>::kThreads, DqLayout<D>::kDynamicSmem, stream>>>(tq, tdo, tk, tv, p);
+    attn_bwd_dq_kernel<D, M, E><<<grid, DqLayout<D>::kThreads, DqLayout<D>::kDynamicSmem, stream>>>(tq, tdo, tk, tv, p);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
     p.num_units = (int)dkv_units;
     grid = (int)(dkv_units < sm_count ? dkv_units : sm_count);
     p.head_block = std::min(p.B * p.Hkv, (8 * grid + p.num_tiles - 1) / p.num_tiles);
-    attn_bwd_dkdv_kernel<D, M><<<grid, DkvLayout<D>::kThreads, DkvLayout<D>::kDynamicSmem, stream>>>(tq, tdo, tk, tv, p);
+    attn_bwd_dkdv_kernel<D, M, E><<<grid, DkvLayout<D>::kThreads, DkvLayout<D>::kDynamicSmem, stream>>>(tq, tdo, tk, tv, p);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
 int bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
         const float* lse, float* delta, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int S,
-        int D, float scale, int causal, const uint8_t* block_mask, int mask_heads, void* stream);
+        int D, float scale, int causal, const uint8_t* block_mask, int mask_heads, void* stream,
+        const uint8_t* keep_bits = nullptr, int keep_heads = 1);
 
 }  // namespace
 }  // namespace attn
@@ -122,12 +125,26 @@ extern "C" int attn_bwd_block_masked(const void* q, const void* k, const void* v
                      block_mask, mask_heads, stream);
 }
 
+extern "C" int attn_bwd_elem_masked(const void* q, const void* k, const void* v, const void* out,
+                                    const void* dout, const float* lse, float* delta, void* dq,
+                                    void* dk, void* dv, int B, int Hq, int Hkv, int S, int D,
+                                    float scale, int causal, const unsigned char* keep_bits,
+                                    int keep_heads, const unsigned char* block_mask, int mask_heads,
+                                    void* stream) {
+    if (keep_bits == nullptr || (keep_heads != 1 && keep_heads != Hq)) return ATTN_ERR_INVALID_ARG;
+    if (block_mask != nullptr && mask_heads != 1 && mask_heads != Hq) return ATTN_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(keep_bits) & 15u) return ATTN_ERR_MISALIGNED;
+    return attn::bwd(q, k, v, out, dout, lse, delta, dq, dk, dv, B, Hq, Hkv, S, D, scale, causal,
+                     block_mask, block_mask != nullptr ? mask_heads : 1, stream, keep_bits, keep_heads);
+}
+
 namespace attn {
 namespace {
 
 int bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
         const float* lse, float* delta, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int S,
-        int D, float scale, int causal, const uint8_t* block_mask, int mask_heads, void* stream) {
+        int D, float scale, int causal, const uint8_t* block_mask, int mask_heads, void* stream,
+        const uint8_t* keep_bits, int keep_heads) {
     int rc = check_bwd_args(q, k, v, out, dout, lse, delta, dq, dk, dv, B, Hq, Hkv, S, D, scale);
     if (rc != ATTN_OK) return rc;
     int sm_count = 0;
@@ -165,12 +182,20 @@ int bwd(const void* q, const void* k, const void* v, const void* out, const void
     p.wait_limit_ns = host::wait_limit_ns();
     p.block_mask = block_mask;
     p.mask_heads = mask_heads;
+    p.keep_bits = keep_bits;
+    p.keep_heads = keep_heads;
+    p.keep_row_bytes = 16 * p.num_tiles;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (block_mask != nullptr)
-        return D == 64 ? launch_bwd<64, true>(tq, tdo, tk, tv, p, sm_count, st)
-                       : launch_bwd<128, true>(tq, tdo, tk, tv, p, sm_count, st);
-    return D == 64 ? launch_bwd<64, false>(tq, tdo, tk, tv, p, sm_count, st)
-                   : launch_bwd<128, false>(tq, tdo, tk, tv, p, sm_count, st);
+    const bool m = block_mask != nullptr, e = keep_bits != nullptr;
+    if (D == 64)
+        return m ? (e ? launch_bwd<64, true, true>(tq, tdo, tk, tv, p, sm_count, st)
+                      : launch_bwd<64, true, false>(tq, tdo, tk, tv, p, sm_count, st))
+                 : (e ? launch_bwd<64, false, true>(tq, tdo, tk, tv, p, sm_count, st)
+                      : launch_bwd<64, false, false>(tq, tdo, tk, tv, p, sm_count, st));
+    return m ? (e ? launch_bwd<128, true, true>(tq, tdo, tk, tv, p, sm_count, st)
+                  : launch_bwd<128, true, false>(tq, tdo, tk, tv, p, sm_count, st))
+             : (e ? launch_bwd<128, false, true>(tq, tdo, tk, tv, p, sm_count, st)
+                  : launch_bwd<128, false, false>(tq, tdo, tk, tv, p, sm_count, st));
 }
 
 }  // namespace

@@ -70,6 +70,9 @@ struct BwdParams {
     int head_block;  // heads worked on together (see split_unit)
     const uint8_t* block_mask;  // masked kernels: [mask_heads][nt][nt], 0 drops a (query, key) tile
     int mask_heads;             // 1 or Hq
+    const uint8_t* keep_bits;   // element-masked kernels: [keep_heads][S][keep_row_bytes]
+    int keep_heads;             // 1 or Hq
+    int keep_row_bytes;         // 16 per 128 keys
 };
 
 // Block mask entry of (query head bh, query tile qt, key tile kt).
@@ -170,7 +173,7 @@ __device__ __forceinline__ uint32_t dq_bar(uint32_t base, int i) {
     return base + DqLayout<D>::kBars + 8u * (uint32_t)i;
 }
 
-template <int D, bool M>
+template <int D, bool M, bool E>
 __device__ void dq_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_do,
                              const CUtensorMap* tm_k, const CUtensorMap* tm_v, const BwdParams& p,
                              uint32_t base, volatile int* abort_flag) {
@@ -254,7 +257,7 @@ drain:
     if (pend_q) ptx::drain_wait(dq_bar<D>(base, L::kQFull), pend_q_par, lim);
 }
 
-template <int D, bool M>
+template <int D, bool M, bool E>
 __device__ void dq_mma_role(const BwdParams& p, uint32_t base, uint32_t tmem, volatile int* abort_flag) {
     using L = DqLayout<D>;
     constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(kTile, kTile, false);  // S, dP: N = 128 keys
@@ -377,7 +380,7 @@ __device__ __forceinline__ float row_delta(const __nv_bfloat16* o, const __nv_bf
 // Warps 2-3: for each unit, the LSE (as log2) and delta_i = dO_i . O_i of its
 // 128 rows into a shared-memory stage (delta also to global memory for the
 // dK/dV kernel), ahead of the element-wise warps.
-template <int D, bool M>
+template <int D, bool M, bool E>
 __device__ void dq_stat_role(const BwdParams& p, uint32_t base, uint8_t* smem, volatile int* abort_flag) {
     using L = DqLayout<D>;
     const int tid = threadIdx.x - 64;  // 0..63
@@ -415,7 +418,7 @@ __device__ void dq_stat_role(const BwdParams& p, uint32_t base, uint8_t* smem, v
     }
 }
 
-template <int D, bool M>
+template <int D, bool M, bool E>
 __device__ void dq_work_role(const BwdParams& p, uint32_t base, const uint8_t* smem, uint32_t tmem,
                              int wg, volatile int* abort_flag) {
     using L = DqLayout<D>;
@@ -450,7 +453,29 @@ __device__ void dq_work_role(const BwdParams& p, uint32_t base, const uint8_t* s
             stat_phase ^= 1u;
         }
         const bool none = M && dq_next_key<M>(p, w, -1) >= w.n;  // no key tile kept: dQ = 0
+        // Element-masked kernels: this row's 8 keep bytes for the warpgroup's 64
+        // keys of each key tile, read one key tile ahead.
+        const uint8_t* keep_row = nullptr;
+        uint2 keep_next = make_uint2(~0u, ~0u);
+        int keep_next_j = -1;
+        if constexpr (E) {
+            if (valid)
+                keep_row = p.keep_bits +
+                           ((size_t)(p.keep_heads == 1 ? 0 : w.bh % p.Hq) * p.S + row) * (size_t)p.keep_row_bytes +
+                           8 * wg;
+        }
         for (int j = dq_next_key<M>(p, w, -1); j < w.n; j = dq_next_key<M>(p, w, j)) {
+            uint2 keep = make_uint2(~0u, ~0u);
+            if constexpr (E) {
+                if (keep_row != nullptr) {
+                    keep = keep_next_j == j ? keep_next : __ldg(reinterpret_cast<const uint2*>(keep_row + 16 * j));
+                    const int jn = dq_next_key<M>(p, w, j);
+                    if (jn < w.n) {
+                        keep_next = __ldg(reinterpret_cast<const uint2*>(keep_row + 16 * jn));
+                        keep_next_j = jn;
+                    }
+                }
+            }
             bool ok = ptx::mbar_wait(dq_bar<D>(base, L::kSFull), s_phase, abort_flag, p.status, lim);
             if (!__all_sync(0xffffffffu, ok)) return;
             s_phase ^= 1u;
@@ -479,6 +504,13 @@ __device__ void dq_work_role(const BwdParams& p, uint32_t base, const uint8_t* s
 #pragma unroll
                 for (int c = 0; c < 64; ++c)
                     if (key0 + c >= p.S) pr[c] = 0.f;  // key past the end
+            }
+            if constexpr (E) {  // keys whose keep bit is 0 (a row without keys has P = inf there)
+                if ((keep.x & keep.y) != 0xFFFFFFFFu) {
+#pragma unroll
+                    for (int c = 0; c < 64; ++c)
+                        if ((((c < 32 ? keep.x : keep.y) >> (c & 31)) & 1u) == 0u) pr[c] = 0.f;
+                }
             }
 
             ok = ptx::mbar_wait(dq_bar<D>(base, L::kDPFull), dp_phase, abort_flag, p.status, lim);
@@ -547,7 +579,7 @@ __device__ void dq_work_role(const BwdParams& p, uint32_t base, const uint8_t* s
     }
 }
 
-template <int D, bool M>
+template <int D, bool M, bool E>
 __global__ void __launch_bounds__(DqLayout<D>::kThreads, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                        const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -597,12 +629,12 @@ __global__ void __launch_bounds__(DqLayout<D>::kThreads, 1)
 
     if (warp < 4) {
         ptx::regs_dec<L::kRegsSmall>();
-        if (warp == 0 && lane == 0) dq_load_role<D, M>(&tm_q, &tm_do, &tm_k, &tm_v, p, base, abort_flag);
-        if (warp == 1 && lane == 0) dq_mma_role<D, M>(p, base, tmem, abort_flag);
-        if (warp >= 2) dq_stat_role<D, M>(p, base, smem, abort_flag);
+        if (warp == 0 && lane == 0) dq_load_role<D, M, E>(&tm_q, &tm_do, &tm_k, &tm_v, p, base, abort_flag);
+        if (warp == 1 && lane == 0) dq_mma_role<D, M, E>(p, base, tmem, abort_flag);
+        if (warp >= 2) dq_stat_role<D, M, E>(p, base, smem, abort_flag);
     } else {
         ptx::regs_inc<L::kRegsWork>();
-        dq_work_role<D, M>(p, base, smem, tmem, (warp - 4) >> 2, abort_flag);
+        dq_work_role<D, M, E>(p, base, smem, tmem, (warp - 4) >> 2, abort_flag);
     }
 
     ptx::tc_fence_before();
@@ -623,8 +655,11 @@ struct DkvLayout {
     static constexpr uint32_t kTileBytes = kTile * D * 2;
     static constexpr int kChunks = D / 64;
     static constexpr uint32_t kChunkBytes = kTile * 128;
-    static constexpr int kStatStages = 4;                  // per-query LSE / delta rows
-    static constexpr uint32_t kStatBytes = 2 * kTile * 4;  // stage s: lse2[128], delta[128]
+    static constexpr int kStatStages = 4;  // per-query LSE / delta rows
+    // Stage s: lse2[128], delta[128] (fp32), then (element-masked kernels) the
+    // 16 keep bytes of the unit's key tile for each of the 128 queries.
+    static constexpr uint32_t kStatKeep = 2 * kTile * 4;
+    static constexpr uint32_t kStatBytes = kStatKeep + kTile * 16;
     // Q_i, dO_i ring, one tile per slot: as many slots as fit (5 at D = 128, 12 at D = 64).
     static constexpr int kStages =
         (227 * 1024 - 2 * (int)kTileBytes - kStatStages * (int)kStatBytes - 2048) / (int)kTileBytes > 12
@@ -685,7 +720,7 @@ __device__ __forceinline__ uint32_t dkv_bar(uint32_t base, int i) {
     return base + DkvLayout<D>::kBars + 8u * (uint32_t)i;
 }
 
-template <int D, bool M>
+template <int D, bool M, bool E>
 __device__ void dkv_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_do,
                               const CUtensorMap* tm_k, const CUtensorMap* tm_v, const BwdParams& p,
                               uint32_t base, volatile int* abort_flag) {
@@ -746,7 +781,7 @@ drain:
 // Warps 2-3: LSE (as log2) and delta of each query tile into the stage's
 // shared-memory rows; queries past the sequence end get +inf and 0 so that
 // their weights vanish.
-template <int D, bool M>
+template <int D, bool M, bool E>
 __device__ void dkv_stat_role(const BwdParams& p, uint32_t base, uint8_t* smem, volatile int* abort_flag) {
     using L = DkvLayout<D>;
     const int tid = threadIdx.x - 64;  // 0..63
@@ -766,6 +801,18 @@ __device__ void dkv_stat_role(const BwdParams& p, uint32_t base, uint8_t* smem, 
                 l2[h] = valid ? __ldg(p.lse + (size_t)bh * p.S + row) * kLog2e : INFINITY;
                 dl[h] = valid ? p.delta[(size_t)bh * p.S + row] : 0.f;
             }
+            uint4 kb[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
+            if constexpr (E) {  // each query's keep bits for this key tile
+                const int hq = bh % p.Hq;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int row = qt * kTile + tid + 64 * h;
+                    if (row < p.S)
+                        kb[h] = __ldg(reinterpret_cast<const uint4*>(
+                            p.keep_bits + ((size_t)(p.keep_heads == 1 ? 0 : hq) * p.S + row) * (size_t)p.keep_row_bytes +
+                            16 * w.kt));
+                }
+            }
             if (!ptx::mbar_wait(dkv_bar<D>(base, L::kStatEmpty + st), ring_phase ^ 1u, abort_flag, p.status, lim))
                 return;
             float* rows = reinterpret_cast<float*>(smem + L::kStat + (uint32_t)st * L::kStatBytes);
@@ -773,6 +820,11 @@ __device__ void dkv_stat_role(const BwdParams& p, uint32_t base, uint8_t* smem, 
             for (int h = 0; h < 2; ++h) {
                 rows[tid + 64 * h] = l2[h];
                 rows[kTile + tid + 64 * h] = dl[h];
+            }
+            if constexpr (E) {
+                uint4* keep = reinterpret_cast<uint4*>(smem + L::kStat + (uint32_t)st * L::kStatBytes + L::kStatKeep);
+                keep[tid] = kb[0];
+                keep[tid + 64] = kb[1];
             }
             ptx::mbar_arrive(dkv_bar<D>(base, L::kStatFull + st));
             if (++st == L::kStatStages) {
@@ -783,7 +835,7 @@ __device__ void dkv_stat_role(const BwdParams& p, uint32_t base, uint8_t* smem, 
     }
 }
 
-template <int D, bool M>
+template <int D, bool M, bool E>
 __device__ void dkv_mma_role(const BwdParams& p, uint32_t base, uint32_t tmem, volatile int* abort_flag) {
     using L = DkvLayout<D>;
     constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(kTile, kTile, false);  // S^T, dP^T: N = 128 queries
@@ -882,7 +934,7 @@ __device__ void dkv_mma_role(const BwdParams& p, uint32_t base, uint32_t tmem, v
     ptx::drain_wait(dkv_bar<D>(base, L::kDrain), 0u, lim);
 }
 
-template <int D, bool M>
+template <int D, bool M, bool E>
 __device__ void dkv_work_role(const BwdParams& p, uint32_t base, const uint8_t* smem, uint32_t tmem,
                               int wg, volatile int* abort_flag) {
     using L = DkvLayout<D>;
@@ -929,6 +981,16 @@ __device__ void dkv_work_role(const BwdParams& p, uint32_t base, const uint8_t* 
 #pragma unroll
                 for (int c = 0; c < 64; ++c)
                     if (64 * wg + c < r) pr[c] = 0.f;  // query before this key
+            }
+            if constexpr (E) {
+                // Query 64 wg + c keeps this key when bit r of its 16 keep bytes
+                // is set: word r / 32 of that query's row in the stage, the same
+                // word for the whole warp (a broadcast read).
+                const uint32_t* kw = reinterpret_cast<const uint32_t*>(
+                    smem + L::kStat + (uint32_t)st * L::kStatBytes + L::kStatKeep) + (r >> 5);
+#pragma unroll
+                for (int c = 0; c < 64; ++c)
+                    if (((kw[4 * (64 * wg + c)] >> (r & 31)) & 1u) == 0u) pr[c] = 0.f;
             }
             uint32_t pk[32];
 #pragma unroll
@@ -1013,7 +1075,7 @@ __device__ void dkv_work_role(const BwdParams& p, uint32_t base, const uint8_t* 
     }
 }
 
-template <int D, bool M>
+template <int D, bool M, bool E>
 __global__ void __launch_bounds__(DkvLayout<D>::kThreads, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                          const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -1063,12 +1125,12 @@ __global__ void __launch_bounds__(DkvLayout<D>::kThreads, 1)
 
     if (warp < 4) {
         ptx::regs_dec<L::kRegsSmall>();
-        if (warp == 0 && lane == 0) dkv_load_role<D, M>(&tm_q, &tm_do, &tm_k, &tm_v, p, base, abort_flag);
-        if (warp == 1 && lane == 0) dkv_mma_role<D, M>(p, base, tmem, abort_flag);
-        if (warp >= 2) dkv_stat_role<D, M>(p, base, smem, abort_flag);
+        if (warp == 0 && lane == 0) dkv_load_role<D, M, E>(&tm_q, &tm_do, &tm_k, &tm_v, p, base, abort_flag);
+        if (warp == 1 && lane == 0) dkv_mma_role<D, M, E>(p, base, tmem, abort_flag);
+        if (warp >= 2) dkv_stat_role<D, M, E>(p, base, smem, abort_flag);
     } else {
         ptx::regs_inc<L::kRegsWork>();
-        dkv_work_role<D, M>(p, base, smem, tmem, (warp - 4) >> 2, abort_flag);
+        dkv_work_role<D, M, E>(p, base, smem, tmem, (warp - 4) >> 2, abort_flag);
     }
 
     ptx::tc_fence_before();

@@ -57,6 +57,9 @@ def load() -> ctypes.CDLL:
         lib.attn_bwd_block_masked.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci,
                                               ci, cf, ci, vp, ci, vp]
         lib.attn_bwd_block_masked.restype = ci
+        lib.attn_bwd_elem_masked.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci,
+                                             ci, cf, ci, vp, ci, vp, ci, vp]
+        lib.attn_bwd_elem_masked.restype = ci
         u64 = ctypes.c_ulonglong
         lib.attn_fwd_dropout.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, ci, cf, u64, u64,
                                          vp]
@@ -198,6 +201,21 @@ def attn_bwd_block_masked(q, k, v, out, dout, lse, delta, dq, dk, dv, B: int, Hq
                                       _ptr(block_mask), int(mask_heads), _stream(stream))
     if check and rc != ATTN_OK:
         raise AttnError(rc, "attn_bwd_block_masked")
+    return rc
+
+
+def attn_bwd_elem_masked(q, k, v, out, dout, lse, delta, dq, dk, dv, B: int, Hq: int, Hkv: int,
+                         S: int, D: int, scale: float, causal: bool | int, keep_bits,
+                         keep_heads: int, block_mask=None, mask_heads: int = 1, stream=None,
+                         check: bool = True) -> int:
+    """The C entry point ``attn_bwd_elem_masked`` (masks as in ``attn_fwd_elem_masked``)."""
+    rc = load().attn_bwd_elem_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse),
+                                     _ptr(delta), _ptr(dq), _ptr(dk), _ptr(dv), int(B), int(Hq),
+                                     int(Hkv), int(S), int(D), float(scale), 1 if causal else 0,
+                                     _ptr(keep_bits), int(keep_heads), _ptr(block_mask),
+                                     int(mask_heads), _stream(stream))
+    if check and rc != ATTN_OK:
+        raise AttnError(rc, "attn_bwd_elem_masked")
     return rc
 
 

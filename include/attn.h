@@ -215,6 +215,20 @@ int attn_bwd_block_masked(const void *q, const void *k, const void *v, const voi
                           const unsigned char *block_mask, int mask_heads, void *stream);
 
 /*
+ * attn_bwd_elem_masked -- attn_bwd for the element-masked attention of
+ * attn_fwd_elem_masked (same keep_bits, keep_heads, block_mask, mask_heads;
+ * out and lse from that call).  Masked pairs have weight 0, so they add
+ * nothing to any gradient; a query without any visible key gets dQ = 0 and
+ * delta = 0.  Arguments, errors and rules as attn_bwd and
+ * attn_fwd_elem_masked.
+ */
+int attn_bwd_elem_masked(const void *q, const void *k, const void *v, const void *out,
+                         const void *dout, const float *lse, float *delta, void *dq, void *dk,
+                         void *dv, int B, int Hq, int Hkv, int S, int D, float scale, int causal,
+                         const unsigned char *keep_bits, int keep_heads,
+                         const unsigned char *block_mask, int mask_heads, void *stream);
+
+/*
  * attn_out_proj -- the layer's output projection applied to attention's
  * output where it lies (the "output projection" operator the ainews.cool
  * article profiles right after attention, per-operator table):

@@ -259,3 +259,29 @@ def run_gpu_elem_masked(q_bits, k_bits, v_bits, scale, causal, keep_bits, block_
                                 stream=stream)
     native.attn_sync_status(stream)
     return out.double().cpu().numpy(), lse.double().cpu().numpy()
+
+
+def run_gpu_bwd_elem_masked(q_bits, k_bits, v_bits, do_bits, scale, causal, keep_bits,
+                            block_mask=None, stream=None):
+    """attn_fwd_elem_masked then attn_bwd_elem_masked on the same buffers.
+    Returns float64 (O, LSE, dQ, dK, dV, delta)."""
+    import torch
+    from causal_scaled_dot_gb300 import native
+    B, Hq, S, D = q_bits.shape
+    Hkv = k_bits.shape[1]
+    q, k, v, do = to_device(q_bits), to_device(k_bits), to_device(v_bits), to_device(do_bits)
+    kb = torch.from_numpy(np.ascontiguousarray(keep_bits, dtype=np.uint8)).cuda()
+    bm = None if block_mask is None else torch.from_numpy(np.ascontiguousarray(block_mask, dtype=np.uint8)).cuda()
+    hk, hm = keep_bits.shape[0], 1 if block_mask is None else block_mask.shape[0]
+    out = torch.empty_like(q)
+    lse = torch.empty((B, Hq, S), dtype=torch.float32, device="cuda")
+    native.attn_fwd_elem_masked(q, k, v, out, lse, B, Hq, Hkv, S, D, scale, causal, kb, hk, bm, hm,
+                                stream=stream)
+    dq = torch.full_like(q, float("nan"))
+    dk = torch.full_like(k, float("nan"))
+    dv = torch.full_like(v, float("nan"))
+    delta = torch.full((B, Hq, S), float("nan"), dtype=torch.float32, device="cuda")
+    native.attn_bwd_elem_masked(q, k, v, out, do, lse, delta, dq, dk, dv, B, Hq, Hkv, S, D, scale,
+                                causal, kb, hk, bm, hm, stream=stream)
+    native.attn_sync_status(stream)
+    return tuple(t.double().cpu().numpy() for t in (out, lse, dq, dk, dv, delta))
