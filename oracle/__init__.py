@@ -87,6 +87,10 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     f.restype = ci
     f.argtypes = [vp, vp, vp, ci, ci, ci, ci, ci, cf, ci, vp, ci, vp, ci, vp, ctypes.c_int64, vp, vp,
                   ci]
+    f = lib.oracle_attn_bwd_dropout
+    f.restype = ci
+    f.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, ci, ctypes.c_uint64, ctypes.c_uint64,
+                  vp, ctypes.c_int64, vp, vp, vp, vp, ci]
     f = lib.oracle_attn_bwd_keep
     f.restype = ci
     f.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, vp, ci, vp, ci, vp, ctypes.c_int64,
@@ -299,7 +303,7 @@ def attention_f64(q, k, v, scale: float, causal: bool = True, nthreads: int | No
 
 def attention_bwd(q, k, v, dout, scale: float, causal: bool = True, kv_heads=None,
                   nthreads: int | None = None, lib: ctypes.CDLL | None = None, block_mask=None,
-                  keep_bits=None):
+                  keep_bits=None, dropout=None):
     """Gradients of the attention output: (dQ, dK, dV, delta) in float64.
 
     q, dout: [B,Hq,S,D]; k, v: [B,Hkv,S,D]; either all bf16 bit patterns
@@ -310,6 +314,7 @@ def attention_bwd(q, k, v, dout, scale: float, causal: bool = True, kv_heads=Non
     delta_i = sum_j P_ij (dO_i . V_j), the row term of the softmax gradient.
     block_mask: optional uint8 [1 or Hq, nt, nt] as in ``attention_masked``;
     keep_bits: optional element mask as in ``attention_keep``.
+    dropout: optional (p8, seed, offset) as in ``attention_dropout`` (no mask with it).
     """
     lib = lib or load()
     f64 = np.asarray(q).dtype == np.float64
@@ -333,7 +338,13 @@ def attention_bwd(q, k, v, dout, scale: float, causal: bool = True, kv_heads=Non
     tail = (None if heads is None else heads.ctypes.data, n, dq.ctypes.data, dk.ctypes.data,
             dv.ctypes.data, delta.ctypes.data, nthreads or default_threads())
     bm = _block(block_mask, Hq, S)
-    if keep_bits is not None:
+    if dropout is not None:
+        if bm is not None or keep_bits is not None:
+            raise ValueError("dropout gradients take no mask")
+        p8, seed, offset = dropout
+        rc = lib.oracle_attn_bwd_dropout(*common, int(p8), int(seed) & (2**64 - 1),
+                                         int(offset) & (2**64 - 1), *tail)
+    elif keep_bits is not None:
         km = _keep(keep_bits, Hq, S)
         rc = lib.oracle_attn_bwd_keep(*common, km.ctypes.data, km.shape[0],
                                       None if bm is None else bm.ctypes.data,

@@ -427,7 +427,9 @@ int oracle_attn_rows_f64(const double *q, const double *k, const double *v, int 
  *   dQ_i    = scale * sum_j dS_ij K_j
  *   dK_j    = scale * sum_i dS_ij Q_i
  * and a key/value head's dK and dV add up the contributions of every query
- * head of its group.  Masked pairs have P_ij = 0, hence dS_ij = 0.
+ * head of its group.  Masked pairs have P_ij = 0, hence dS_ij = 0.  With
+ * dropout (oracle_attn_bwd_dropout) the output uses P_ij Z_ij s instead of
+ * P_ij, so dV_j = sum_i P_ij Z_ij s dO_i and dP_ij = Z_ij s (dO_i . V_j).
  *
  * Work per selected key/value head (b, hkv): pass 1, one query row at a time
  * (any order, rows independent), stores the rows of P and dS of all G query
@@ -464,6 +466,14 @@ static void bwd_row(const bwd_job_t *W, int64_t n, double *dP) {
         if (p[j] == 0.0) continue;
         for (int d = 0; d < D; ++d) dP[j] += elem(J, 3, qo + d) * elem(J, 2, kvb + j * D + d);
     }
+    /* With dropout the output uses the weights P_ij Z_ij s (Z_ij the keep
+     * decision, s = 256 / (256 - p8)), so the gradient reaching P_ij is
+     * Z_ij s (dO_i . V_j). */
+    if (J->dropout_p8 > 0) {
+        const double keep_scale = 256.0 / (256.0 - (double)J->dropout_p8);
+        for (int64_t j = 0; j < S; ++j)
+            if (p[j] != 0.0) dP[j] = dropout_keeps(J, bh, i, j) ? dP[j] * keep_scale : 0.0;
+    }
     /* delta_i = sum_k P_ik dP_ik. */
     double delta = 0.0;
     for (int64_t j = 0; j < S; ++j) delta += p[j] * dP[j];
@@ -491,9 +501,13 @@ static void bwd_key(const bwd_job_t *W, int64_t j) {
         for (int64_t i = 0; i < S; ++i) {
             const double pij = W->P[(g * S + i) * S + j], dsij = W->dS[(g * S + i) * S + j];
             if (pij == 0.0) continue;
+            /* dV takes the weight the output used: dropped or scaled with dropout. */
+            double wij = pij;
+            if (J->dropout_p8 > 0)
+                wij = dropout_keeps(J, bh, i, j) ? pij * (256.0 / (256.0 - (double)J->dropout_p8)) : 0.0;
             const int64_t qo = (bh * S + i) * (int64_t)D;
             for (int d = 0; d < D; ++d) {
-                dv[d] += pij * elem(J, 3, qo + d);
+                dv[d] += wij * elem(J, 3, qo + d);
                 dk[d] += dsij * elem(J, 0, qo + d);
             }
         }
@@ -567,8 +581,9 @@ static int bwd_parallel(const bwd_job_t *proto, int pass, int64_t count, int nth
 static int bwd_run(const void *q, const void *k, const void *v, const void *dout, int f64_inputs,
                    int B, int Hq, int Hkv, int S, int D, float scale, int causal,
                    const uint8_t *block_mask, int mask_heads, const uint8_t *keep_bits,
-                   int keep_heads, const int64_t *kv_heads, int64_t n_kv_heads, double *dq,
-                   double *dk, double *dv, double *delta, int nthreads) {
+                   int keep_heads, int dropout_p8, uint64_t seed, uint64_t offset,
+                   const int64_t *kv_heads, int64_t n_kv_heads, double *dq, double *dk,
+                   double *dv, double *delta, int nthreads) {
     if (!q || !k || !v || !dout || !dq || !dk || !dv || !delta) return 1;
     if (B < 1 || Hq < 1 || Hkv < 1 || S < 1 || D < 1 || Hq % Hkv != 0) return 1;
     if (!kv_heads && n_kv_heads != (int64_t)B * Hkv) return 1;
@@ -589,6 +604,10 @@ static int bwd_run(const void *q, const void *k, const void *v, const void *dout
     if (keep_bits && keep_heads != 1 && keep_heads != Hq) return 1;
     J.keep_bits = keep_bits;
     J.keep_heads = keep_bits ? keep_heads : 1;
+    if (dropout_p8 < 0 || dropout_p8 > 255) return 1;
+    J.dropout_p8 = dropout_p8;
+    J.dropout_key[0] = seed;
+    J.dropout_key[1] = offset;
     const int64_t G = Hq / Hkv;
     double *P = (double *)malloc(sizeof(double) * (size_t)(G * S) * (size_t)S);
     double *dS = (double *)malloc(sizeof(double) * (size_t)(G * S) * (size_t)S);
@@ -644,8 +663,8 @@ int oracle_attn_bwd(const void *q, const void *k, const void *v, const void *dou
                     int B, int Hq, int Hkv, int S, int D, float scale, int causal,
                     const int64_t *kv_heads, int64_t n_kv_heads, double *dq, double *dk,
                     double *dv, double *delta, int nthreads) {
-    return bwd_run(q, k, v, dout, f64_inputs, B, Hq, Hkv, S, D, scale, causal, NULL, 1, NULL, 1,
-                   kv_heads, n_kv_heads, dq, dk, dv, delta, nthreads);
+    return bwd_run(q, k, v, dout, f64_inputs, B, Hq, Hkv, S, D, scale, causal, NULL, 1, NULL, 1, 0,
+                   0, 0, kv_heads, n_kv_heads, dq, dk, dv, delta, nthreads);
 }
 
 /*
@@ -661,7 +680,7 @@ int oracle_attn_bwd_masked(const void *q, const void *k, const void *v, const vo
                            double *dv, double *delta, int nthreads) {
     if (!block_mask) return 1;
     return bwd_run(q, k, v, dout, f64_inputs, B, Hq, Hkv, S, D, scale, causal, block_mask,
-                   mask_heads, NULL, 1, kv_heads, n_kv_heads, dq, dk, dv, delta, nthreads);
+                   mask_heads, NULL, 1, 0, 0, 0, kv_heads, n_kv_heads, dq, dk, dv, delta, nthreads);
 }
 
 /*
@@ -677,6 +696,22 @@ int oracle_attn_bwd_keep(const void *q, const void *k, const void *v, const void
                          int nthreads) {
     if (!keep_bits) return 1;
     return bwd_run(q, k, v, dout, f64_inputs, B, Hq, Hkv, S, D, scale, causal, block_mask,
-                   mask_heads, keep_bits, keep_heads, kv_heads, n_kv_heads, dq, dk, dv, delta,
-                   nthreads);
+                   mask_heads, keep_bits, keep_heads, 0, 0, 0, kv_heads, n_kv_heads, dq, dk, dv,
+                   delta, nthreads);
+}
+
+/*
+ * oracle_attn_bwd_dropout -- oracle_attn_bwd for the attention with dropout of
+ * oracle_attn_rows_dropout (same p8, seed, offset): the output uses the
+ * weights P_ij Z_ij s, so dV_j = sum_i P_ij Z_ij s dO_i, the gradient reaching
+ * P_ij is Z_ij s (dO_i . V_j), and delta_i = sum_j P_ij Z_ij s (dO_i . V_j)
+ * = dO_i . O_i; the rest as without dropout.
+ */
+int oracle_attn_bwd_dropout(const void *q, const void *k, const void *v, const void *dout,
+                            int f64_inputs, int B, int Hq, int Hkv, int S, int D, float scale,
+                            int causal, int p8, uint64_t seed, uint64_t offset,
+                            const int64_t *kv_heads, int64_t n_kv_heads, double *dq, double *dk,
+                            double *dv, double *delta, int nthreads) {
+    return bwd_run(q, k, v, dout, f64_inputs, B, Hq, Hkv, S, D, scale, causal, NULL, 1, NULL, 1, p8,
+                   seed, offset, kv_heads, n_kv_heads, dq, dk, dv, delta, nthreads);
 }

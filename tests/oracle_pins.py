@@ -790,3 +790,36 @@ def pin_bwd_keep_library(bwdk):
 
 
 BWD_KEEP_PINS = [pin_bwd_keep_library]
+
+
+def pin_bwd_dropout_autograd(bwdd):
+    """Gradients with dropout against torch's float64 autograd of
+    O = ((softmax of the masked scores) * Z * 256/(256-p8)) V, Z the keep table
+    written from the documented byte mapping over numpy's Philox; and p8 = 0
+    gives the gradients without dropout bit for bit."""
+    B, Hq, Hkv, S, D = 1, 4, 2, 70, 8
+    q, k, v = (_rand((B, H, S, D), 261, t) for t, H in ((0, Hq), (1, Hkv), (2, Hkv)))
+    dout = _rand((B, Hq, S, D), 261, 3)
+    G = Hq // Hkv
+    p8, seed, offset = 51, 0xBEEF, 7
+    s = 256.0 / (256 - p8)
+    Z = torch.from_numpy(np.stack([keep_table(h, S, p8, seed, offset) for h in range(Hq)])[None].astype(np.float64))
+    for causal in (True, False):
+        dq, dk, dv, delta = bwdd(q, k, v, dout, 0.4, causal, (p8, seed, offset))
+        tq, tk, tv = (torch.from_numpy(f64(x)).requires_grad_() for x in (q, k, v))
+        sc = torch.einsum("bhid,bhjd->bhij", tq, tk.repeat_interleave(G, 1)) * float(np.float32(0.4))
+        if causal:
+            sc = sc.masked_fill(~torch.ones(S, S, dtype=torch.bool).tril(), float("-inf"))
+        o = torch.einsum("bhij,bhjd->bhid", torch.softmax(sc, dim=-1) * Z * s, tv.repeat_interleave(G, 1))
+        o.backward(torch.from_numpy(f64(dout)))
+        for name, a, t in (("dQ", dq, tq), ("dK", dk, tk), ("dV", dv, tv)):
+            ref = t.grad.numpy()
+            assert np.max(np.abs(a - ref)) <= 1e-12 * max(1.0, float(np.max(np.abs(ref)))), name
+        want_delta = np.sum(f64(dout) * o.detach().numpy(), axis=-1)
+        assert np.max(np.abs(delta - want_delta)) <= 1e-12 * max(1.0, float(np.max(np.abs(want_delta))))
+        a0 = bwdd(q, k, v, dout, 0.4, causal, (0, seed, offset))
+        b0 = bwdd(q, k, v, dout, 0.4, causal, None)
+        assert all(np.array_equal(x, y) for x, y in zip(a0, b0))
+
+
+BWD_DROPOUT_PINS = [pin_bwd_dropout_autograd]

@@ -68,6 +68,10 @@ MUTANTS = {
                                  "const int64_t row_bytes = (S + 7) / 8;"),
     "keep_heads_ignored": ("(J->keep_heads == 1 ? 0 : hq)", "(0)"),
     "keep_ignored": ("if (J->keep_bits) {", "if (0) {"),
+    "bwd_dropout_dv_undropped": ("wij = dropout_keeps(J, bh, i, j) ? pij * (256.0 / (256.0 - (double)J->dropout_p8)) : 0.0;",
+                                 "wij = pij;"),
+    "bwd_dropout_dp_unscaled": ("if (p[j] != 0.0) dP[j] = dropout_keeps(J, bh, i, j) ? dP[j] * keep_scale : 0.0;",
+                                "if (p[j] != 0.0) dP[j] = dropout_keeps(J, bh, i, j) ? dP[j] : 0.0;"),
 }
 
 
@@ -121,6 +125,8 @@ def test_some_pin_catches_mutant(name, tmp_path):
         ("pin_keep_equals_block_mask", lambda: oracle_pins.pin_keep_equals_block_mask(attnk, attnm)),
         ("pin_bwd_keep_library", lambda: oracle_pins.pin_bwd_keep_library(
             lambda q, k, v, d, sc, c, b: oracle.attention_bwd(q, k, v, d, sc, c, keep_bits=b, lib=lib))),
+        ("pin_bwd_dropout_autograd", lambda: oracle_pins.pin_bwd_dropout_autograd(
+            lambda q, k, v, d, sc, c, dr: oracle.attention_bwd(q, k, v, d, sc, c, dropout=dr, lib=lib))),
     ]
     caught = []
     for pin_name, run in checks:

@@ -192,3 +192,12 @@ def _bwdk(q, k, v, dout, scale, causal, bits, kv_heads=None):
 @pytest.mark.parametrize("pin", oracle_pins.BWD_KEEP_PINS, ids=lambda p: p.__name__)
 def test_oracle_bwd_keep_pin(pin):
     pin(_bwdk)
+
+
+def _bwdd(q, k, v, dout, scale, causal, dropout, kv_heads=None):
+    return oracle.attention_bwd(q, k, v, dout, scale, causal, kv_heads=kv_heads, dropout=dropout)
+
+
+@pytest.mark.parametrize("pin", oracle_pins.BWD_DROPOUT_PINS, ids=lambda p: p.__name__)
+def test_oracle_bwd_dropout_pin(pin):
+    pin(_bwdd)
