@@ -50,7 +50,7 @@ MUTANTS = {
     "bwd_delta_unweighted": ("delta += p[j] * dP[j];", "delta += dP[j];"),
     "bwd_dq_scale_dropped": ("for (int d = 0; d < D; ++d) dq[d] *= J->scale;", ""),
     "bwd_dk_scale_dropped": ("for (int d = 0; d < D; ++d) dk[d] *= J->scale;", ""),
-    "bwd_dv_uses_score_gradient": ("dv[d] += pij * elem(J, 3, qo + d);",
+    "bwd_dv_uses_score_gradient": ("dv[d] += wij * elem(J, 3, qo + d);",
                                    "dv[d] += dsij * elem(J, 3, qo + d);"),
     "bwd_dk_uses_weights": ("dk[d] += dsij * elem(J, 0, qo + d);",
                             "dk[d] += pij * elem(J, 0, qo + d);"),
