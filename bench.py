@@ -15,7 +15,9 @@ keep bits) plus the block mask of the blocks the window touches, FLOPs = 4*D
 per kept pair.  With --pass bwd the step
 is one attn_bwd call (dQ, dK, dV for a seeded upstream gradient, O and LSE
 from attn_fwd beforehand) and FLOPs = 2.5x the forward's (five products per
-tile pair instead of two: the usual convention for attention backward).
+tile pair instead of two: the usual convention for attention backward);
+--mask-density, --window and --dropout select the matching backward entry
+points (attn_bwd_block_masked, attn_bwd_elem_masked, attn_bwd_dropout).
 With --pass proj the step is one attn_out_proj call on the workload's
 attention output shape, E = Hq*D output features, FLOPs = 2*B*S*E*Hq*D.  Between timed
 steps a 256 MiB buffer is written to flush L2; each step is timed with CUDA
@@ -277,13 +279,14 @@ class OracleBwdTimer:
     with every query head of its group); a head carries 1/(B*Hkv) of the
     metric's FLOPs."""
 
-    def __init__(self, w, mask=None, window=None):
+    def __init__(self, w, mask=None, window=None, dropout_p8: int = 0):
         import oracle
         from causal_scaled_dot_gb300.inputs import gaussian_bf16, qkv_bf16
         self.oracle = oracle
         self.w = w
         self.mask = mask
         self.keep = None
+        self.dropout = (dropout_p8, DROPOUT_SEED, DROPOUT_OFFSET) if dropout_p8 else None
         self.q, self.k, self.v = qkv_bf16(w.B, w.Hq, w.Hkv, w.S, w.D, seed=w.seed, sigma=w.sigma)
         self.do = gaussian_bf16((w.B, w.Hq, w.S, w.D), w.seed, 3)
         self.threads = oracle.default_threads()
@@ -306,7 +309,7 @@ class OracleBwdTimer:
         heads = np.random.default_rng(seed).integers(0, self.total, n)
         self.oracle.attention_bwd(self.q, self.k, self.v, self.do, self.w.scale, self.w.causal,
                                   kv_heads=heads, nthreads=self.threads, block_mask=self.mask,
-                                  keep_bits=self.keep)
+                                  keep_bits=self.keep, dropout=self.dropout)
         return heads
 
     def rows_for(self, seconds):
@@ -327,7 +330,7 @@ def dropout_p8(args) -> int:
 
 def make_oracle_timer(args, w, mask=None):
     if args.pass_ == "bwd":
-        return OracleBwdTimer(w, mask=mask, window=args.window)
+        return OracleBwdTimer(w, mask=mask, window=args.window, dropout_p8=dropout_p8(args))
     if args.pass_ == "proj":
         return OracleProjTimer(w)
     return OracleTimer(w, fp8=args.dtype == "fp8", mask=mask, dropout_p8=dropout_p8(args),
@@ -653,6 +656,9 @@ def run_ours_bwd(args, w, rank, world, local):
         keep_d, keep_block_d = torch.from_numpy(keep_bits).to(dev), torch.from_numpy(keep_block).to(dev)
         native.attn_fwd_elem_masked(q, k, v, out, lse, w.B, w.Hq, w.Hkv, w.S, w.D, w.scale, w.causal,
                                     keep_d, 1, keep_block_d, 1, stream)
+    elif args.dropout is not None:
+        native.attn_fwd_dropout(q, k, v, out, lse, w.B, w.Hq, w.Hkv, w.S, w.D, w.scale, w.causal,
+                                args.dropout, DROPOUT_SEED, DROPOUT_OFFSET, stream)
     else:
         native.attn_fwd(q, k, v, out, lse, w.B, w.Hq, w.Hkv, w.S, w.D, w.scale, w.causal, stream)
     outh, lseh = out.cpu().pin_memory(), lse.cpu().pin_memory()
@@ -672,6 +678,10 @@ def run_ours_bwd(args, w, rank, world, local):
         elif args.window is not None:
             native.attn_bwd_elem_masked(q, k, v, out, do, lse, delta, dq, dk, dv, w.B, w.Hq, w.Hkv,
                                         w.S, w.D, w.scale, w.causal, keep_d, 1, keep_block_d, 1, stream)
+        elif args.dropout is not None:
+            native.attn_bwd_dropout(q, k, v, out, do, lse, delta, dq, dk, dv, w.B, w.Hq, w.Hkv, w.S,
+                                    w.D, w.scale, w.causal, args.dropout, DROPOUT_SEED, DROPOUT_OFFSET,
+                                    stream)
         else:
             native.attn_bwd(q, k, v, out, do, lse, delta, dq, dk, dv, w.B, w.Hq, w.Hkv, w.S, w.D,
                             w.scale, w.causal, stream)
@@ -739,7 +749,7 @@ def run_ours_bwd(args, w, rank, world, local):
     io_bytes = 3 * q_b + 2 * kv_b + row_b + q_b + 2 * kv_b + 2 * row_b
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        timer = OracleBwdTimer(w, mask=mask, window=args.window)
+        timer = OracleBwdTimer(w, mask=mask, window=args.window, dropout_p8=dropout_p8(args))
         tf, n, dt = timer.sample(args.cpu_seconds, seed=7)
         cpu = {"value": tf, "unit": "TFLOP/s", "cores": timer.threads, "kind": "oracle",
                "sample": f"gradients of {n} random key/value heads of {w.name} (of {timer.total}), "
@@ -751,6 +761,8 @@ def run_ours_bwd(args, w, rank, world, local):
         "data": "synthetic (seeded N(0,1) bf16 Q, K, V, dO; no weights)",
         "config": {"workload": w.name, **w.shape_dict, "causal": w.causal, "inputs": "bf16",
                    "pass": "bwd", **mask_config(mask, args.mask_density), **window_config(w, args.window),
+                   **({"dropout_p": dropout_p8(args) / 256, "dropout_key": [DROPOUT_SEED, DROPOUT_OFFSET]}
+                      if args.dropout is not None else {}),
                    "l2": "flushed between timed steps (256 MiB write)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "pct_of_peak": 100.0 * achieved / peak,
@@ -758,7 +770,8 @@ def run_ours_bwd(args, w, rank, world, local):
                      "frac": achieved / peak,
                      "traffic": recorded_traffic(w.name + ":bwd" + (f":mask{args.mask_density}" if mask is not None
                                                                    else "")
-                                                 + (f":window{args.window}" if args.window is not None else ""),
+                                                 + (f":window{args.window}" if args.window is not None else "")
+                                                 + (f":dropout{args.dropout}" if args.dropout is not None else ""),
                                                  BWD_SOURCES),
                      "peak_source": f"{peak_src} bf16 dense (burst)",
                      "kernel": "attn_bwd call (dQ kernel + dK/dV kernel)",
@@ -903,8 +916,8 @@ def main():
                     help="bf16 only: run attn_fwd_block_masked with a seeded per-head block mask "
                          "keeping each 128x128 block with this probability")
     ap.add_argument("--dropout", type=float, default=None,
-                    help="bf16 forward only: attn_fwd_dropout with this drop probability "
-                         "(rounded to a multiple of 1/256)")
+                    help="bf16 only: attn_fwd_dropout (with --pass bwd: attn_bwd_dropout) with this "
+                         "drop probability (rounded to a multiple of 1/256)")
     ap.add_argument("--window", type=int, default=None,
                     help="bf16 only: attn_fwd_elem_masked (with --pass bwd: attn_bwd_elem_masked) with a "
                          "local window of this many keys per query (element mask) and the block mask it "
@@ -925,9 +938,9 @@ def main():
         ap.error("--pass bwd / proj take bf16 inputs")
     if args.pass_ == "proj" and args.mask_density is not None:
         ap.error("--pass proj takes no mask")
-    if args.dropout is not None and (args.pass_ != "fwd" or args.dtype != "bf16" or args.mask_density is not None
+    if args.dropout is not None and (args.pass_ == "proj" or args.dtype != "bf16" or args.mask_density is not None
                                      or not 0 < round(args.dropout * 256) < 256):
-        ap.error("--dropout takes 0 < p < 1 (at least 1/256), bf16 forward, no mask")
+        ap.error("--dropout takes 0 < p < 1 (at least 1/256), bf16 forward or backward, no mask")
     if args.window is not None and (args.window < 1 or args.pass_ == "proj" or args.dtype != "bf16"
                                     or args.mask_density is not None or args.dropout is not None):
         ap.error("--window takes a positive key count, bf16 forward or backward, no other mask or dropout")

@@ -26,10 +26,10 @@ cudaError_t allow_smem(K kernel, uint32_t bytes) {
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
-template <int D, bool M, bool E>
+template <int D, bool M, bool E, bool DR = false>
 bool allow_all() {
-    return allow_smem(attn_bwd_dq_kernel<D, M, E>, DqLayout<D>::kDynamicSmem) == cudaSuccess &&
-           allow_smem(attn_bwd_dkdv_kernel<D, M, E>, DkvLayout<D>::kDynamicSmem) == cudaSuccess;
+    return allow_smem(attn_bwd_dq_kernel<D, M, E, DR>, DqLayout<D>::kDynamicSmem) == cudaSuccess &&
+           allow_smem(attn_bwd_dkdv_kernel<D, M, E, DR>, DkvLayout<D>::kDynamicSmem) == cudaSuccess;
 }
 
 // Shared-memory opt-in of the backward kernels, once per device.
@@ -42,7 +42,8 @@ int setup_bwd_kernels() {
             allow_all<64, false, false>() && allow_all<128, false, false>() &&
             allow_all<64, true, false>() && allow_all<128, true, false>() &&
             allow_all<64, false, true>() && allow_all<128, false, true>() &&
-            allow_all<64, true, true>() && allow_all<128, true, true>();
+            allow_all<64, true, true>() && allow_all<128, true, true>() &&
+            allow_all<64, false, false, true>() && allow_all<128, false, false, true>();
         g_bwd_ready[dev] = ok ? 1 : ATTN_ERR_DEVICE;
     }
     return g_bwd_ready[dev] == 1 ? ATTN_OK : g_bwd_ready[dev];
@@ -78,7 +79,7 @@ int check_bwd_args(const void* q, const void* k, const void* v, const void* out,
     return ATTN_OK;
 }
 
-template <int D, bool M, bool E>
+template <int D, bool M, bool E, bool DR = false>
 int launch_bwd(const CUtensorMap& tq, const CUtensorMap& tdo, const CUtensorMap& tk,
                const CUtensorMap& tv, BwdParams p, int sm_count, cudaStream_t stream) {
     const long long dq_units = (long long)p.B * p.Hq * p.num_tiles;
@@ -89,19 +90,20 @@ int launch_bwd(const CUtensorMap& tq, const CUtensorMap& tdo, const CUtensorMap&
     // About eight units per CTA per head block: nearly the balance of a single
     // tile-major order, with half or less of the heads' operands live in L2.
     p.head_block = std::min(p.B * p.Hq, (8 * grid + p.num_tiles - 1) / p.num_tiles);
-    attn_bwd_dq_kernel<D, M, E><<<grid, DqLayout<D>::kThreads, DqLayout<D>::kDynamicSmem, stream>>>(tq, tdo, tk, tv, p);
+    attn_bwd_dq_kernel<D, M, E, DR><<<grid, DqLayout<D>::kThreads, DqLayout<D>::kDynamicSmem, stream>>>(tq, tdo, tk, tv, p);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
     p.num_units = (int)dkv_units;
     grid = (int)(dkv_units < sm_count ? dkv_units : sm_count);
     p.head_block = std::min(p.B * p.Hkv, (8 * grid + p.num_tiles - 1) / p.num_tiles);
-    attn_bwd_dkdv_kernel<D, M, E><<<grid, DkvLayout<D>::kThreads, DkvLayout<D>::kDynamicSmem, stream>>>(tq, tdo, tk, tv, p);
+    attn_bwd_dkdv_kernel<D, M, E, DR><<<grid, DkvLayout<D>::kThreads, DkvLayout<D>::kDynamicSmem, stream>>>(tq, tdo, tk, tv, p);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
 int bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
         const float* lse, float* delta, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int S,
         int D, float scale, int causal, const uint8_t* block_mask, int mask_heads, void* stream,
-        const uint8_t* keep_bits = nullptr, int keep_heads = 1);
+        const uint8_t* keep_bits = nullptr, int keep_heads = 1, int dropout_p8 = 0,
+        unsigned long long seed = 0, unsigned long long offset = 0);
 
 }  // namespace
 }  // namespace attn
@@ -138,13 +140,26 @@ extern "C" int attn_bwd_elem_masked(const void* q, const void* k, const void* v,
                      block_mask, block_mask != nullptr ? mask_heads : 1, stream, keep_bits, keep_heads);
 }
 
+extern "C" int attn_bwd_dropout(const void* q, const void* k, const void* v, const void* out,
+                                const void* dout, const float* lse, float* delta, void* dq, void* dk,
+                                void* dv, int B, int Hq, int Hkv, int S, int D, float scale,
+                                int causal, float dropout_p, unsigned long long seed,
+                                unsigned long long offset, void* stream) {
+    if (!std::isfinite(dropout_p) || dropout_p < 0.f) return ATTN_ERR_INVALID_ARG;
+    const long p8 = std::lrint((double)dropout_p * 256.0);
+    if (p8 > 255) return ATTN_ERR_INVALID_ARG;
+    return attn::bwd(q, k, v, out, dout, lse, delta, dq, dk, dv, B, Hq, Hkv, S, D, scale, causal,
+                     nullptr, 1, stream, nullptr, 1, (int)p8, seed, offset);
+}
+
 namespace attn {
 namespace {
 
 int bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
         const float* lse, float* delta, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int S,
         int D, float scale, int causal, const uint8_t* block_mask, int mask_heads, void* stream,
-        const uint8_t* keep_bits, int keep_heads) {
+        const uint8_t* keep_bits, int keep_heads, int dropout_p8, unsigned long long seed,
+        unsigned long long offset) {
     int rc = check_bwd_args(q, k, v, out, dout, lse, delta, dq, dk, dv, B, Hq, Hkv, S, D, scale);
     if (rc != ATTN_OK) return rc;
     int sm_count = 0;
@@ -185,7 +200,14 @@ int bwd(const void* q, const void* k, const void* v, const void* out, const void
     p.keep_bits = keep_bits;
     p.keep_heads = keep_heads;
     p.keep_row_bytes = 16 * p.num_tiles;
+    p.dropout_p8 = dropout_p8;
+    p.dropout_seed = seed;
+    p.dropout_offset = offset;
+    p.keep_scale = dropout_p8 > 0 ? 256.f / (float)(256 - dropout_p8) : 1.f;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (dropout_p8 > 0)
+        return D == 64 ? launch_bwd<64, false, false, true>(tq, tdo, tk, tv, p, sm_count, st)
+                       : launch_bwd<128, false, false, true>(tq, tdo, tk, tv, p, sm_count, st);
     const bool m = block_mask != nullptr, e = keep_bits != nullptr;
     if (D == 64)
         return m ? (e ? launch_bwd<64, true, true>(tq, tdo, tk, tv, p, sm_count, st)

@@ -46,6 +46,7 @@
 #include <cuda_bf16.h>
 
 #include "common.cuh"
+#include "philox.cuh"
 #include "ptx.cuh"
 
 namespace attn {
@@ -73,6 +74,12 @@ struct BwdParams {
     const uint8_t* keep_bits;   // element-masked kernels: [keep_heads][S][keep_row_bytes]
     int keep_heads;             // 1 or Hq
     int keep_row_bytes;         // 16 per 128 keys
+    // Dropout kernels: weight (i, j) of head bh kept when byte j % 32 of the
+    // Philox block {j / 32, i, bh, 0} under key {seed, offset} is >= p8; kept
+    // weights are scaled by keep_scale = 256 / (256 - p8) (as in the forward).
+    int dropout_p8;
+    unsigned long long dropout_seed, dropout_offset;
+    float keep_scale;
 };
 
 // Block mask entry of (query head bh, query tile qt, key tile kt).
@@ -173,7 +180,7 @@ __device__ __forceinline__ uint32_t dq_bar(uint32_t base, int i) {
     return base + DqLayout<D>::kBars + 8u * (uint32_t)i;
 }
 
-template <int D, bool M, bool E>
+template <int D, bool M, bool E, bool DR>
 __device__ void dq_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_do,
                              const CUtensorMap* tm_k, const CUtensorMap* tm_v, const BwdParams& p,
                              uint32_t base, volatile int* abort_flag) {
@@ -257,7 +264,7 @@ drain:
     if (pend_q) ptx::drain_wait(dq_bar<D>(base, L::kQFull), pend_q_par, lim);
 }
 
-template <int D, bool M, bool E>
+template <int D, bool M, bool E, bool DR>
 __device__ void dq_mma_role(const BwdParams& p, uint32_t base, uint32_t tmem, volatile int* abort_flag) {
     using L = DqLayout<D>;
     constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(kTile, kTile, false);  // S, dP: N = 128 keys
@@ -380,7 +387,7 @@ __device__ __forceinline__ float row_delta(const __nv_bfloat16* o, const __nv_bf
 // Warps 2-3: for each unit, the LSE (as log2) and delta_i = dO_i . O_i of its
 // 128 rows into a shared-memory stage (delta also to global memory for the
 // dK/dV kernel), ahead of the element-wise warps.
-template <int D, bool M, bool E>
+template <int D, bool M, bool E, bool DR>
 __device__ void dq_stat_role(const BwdParams& p, uint32_t base, uint8_t* smem, volatile int* abort_flag) {
     using L = DqLayout<D>;
     const int tid = threadIdx.x - 64;  // 0..63
@@ -418,7 +425,7 @@ __device__ void dq_stat_role(const BwdParams& p, uint32_t base, uint8_t* smem, v
     }
 }
 
-template <int D, bool M, bool E>
+template <int D, bool M, bool E, bool DR>
 __device__ void dq_work_role(const BwdParams& p, uint32_t base, const uint8_t* smem, uint32_t tmem,
                              int wg, volatile int* abort_flag) {
     using L = DqLayout<D>;
@@ -512,6 +519,24 @@ __device__ void dq_work_role(const BwdParams& p, uint32_t base, const uint8_t* s
                         if ((((c < 32 ? keep.x : keep.y) >> (c & 31)) & 1u) == 0u) pr[c] = 0.f;
                 }
             }
+            // Dropout: keep decisions of this row's 64 keys (two Philox blocks),
+            // made while the dP product runs.  A dropped weight's dP is 0, a
+            // kept one's is scaled by keep_scale.
+            uint64_t zb = ~0ull;
+            if constexpr (DR) {
+                zb = 0ull;
+#pragma unroll
+                for (int b = 0; b < 2; ++b) {
+                    uint64_t rnd[4];
+                    philox4x64_10((uint64_t)((key0 >> 5) + b), (uint64_t)row, (uint64_t)w.bh, 0ull,
+                                  p.dropout_seed, p.dropout_offset, rnd);
+#pragma unroll
+                    for (int c = 0; c < 32; ++c)
+                        zb |= (uint64_t)(((uint32_t)(rnd[c >> 3] >> (8 * (c & 7))) & 0xFFu) >= (uint32_t)p.dropout_p8)
+                              << (32 * b + c);
+                }
+            }
+            const float ks = DR ? p.keep_scale : 1.f;
 
             ok = ptx::mbar_wait(dq_bar<D>(base, L::kDPFull), dp_phase, abort_flag, p.status, lim);
             if (!__all_sync(0xffffffffu, ok)) return;
@@ -525,11 +550,14 @@ __device__ void dq_work_role(const BwdParams& p, uint32_t base, const uint8_t* s
             ptx::reg_fence32(dr + 32);
             // dS = P (dP - delta), bf16 pairs over the first 32 of this
             // warpgroup's dP columns.
+            auto dp = [&](int e) {
+                return (!DR || ((zb >> e) & 1ull) != 0ull) ? __uint_as_float(dr[e]) * ks : 0.f;
+            };
             uint32_t pk[32];
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
-                const float d0 = pr[2 * c] * (__uint_as_float(dr[2 * c]) - delta);
-                const float d1 = pr[2 * c + 1] * (__uint_as_float(dr[2 * c + 1]) - delta);
+                const float d0 = pr[2 * c] * (dp(2 * c) - delta);
+                const float d1 = pr[2 * c + 1] * (dp(2 * c + 1) - delta);
                 pk[c] = ptx::pack_bf16x2(d0, d1);
             }
             ptx::tmem_st32(tDP, pk);
@@ -579,7 +607,7 @@ __device__ void dq_work_role(const BwdParams& p, uint32_t base, const uint8_t* s
     }
 }
 
-template <int D, bool M, bool E>
+template <int D, bool M, bool E, bool DR>
 __global__ void __launch_bounds__(DqLayout<D>::kThreads, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                        const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -629,12 +657,12 @@ __global__ void __launch_bounds__(DqLayout<D>::kThreads, 1)
 
     if (warp < 4) {
         ptx::regs_dec<L::kRegsSmall>();
-        if (warp == 0 && lane == 0) dq_load_role<D, M, E>(&tm_q, &tm_do, &tm_k, &tm_v, p, base, abort_flag);
-        if (warp == 1 && lane == 0) dq_mma_role<D, M, E>(p, base, tmem, abort_flag);
-        if (warp >= 2) dq_stat_role<D, M, E>(p, base, smem, abort_flag);
+        if (warp == 0 && lane == 0) dq_load_role<D, M, E, DR>(&tm_q, &tm_do, &tm_k, &tm_v, p, base, abort_flag);
+        if (warp == 1 && lane == 0) dq_mma_role<D, M, E, DR>(p, base, tmem, abort_flag);
+        if (warp >= 2) dq_stat_role<D, M, E, DR>(p, base, smem, abort_flag);
     } else {
         ptx::regs_inc<L::kRegsWork>();
-        dq_work_role<D, M, E>(p, base, smem, tmem, (warp - 4) >> 2, abort_flag);
+        dq_work_role<D, M, E, DR>(p, base, smem, tmem, (warp - 4) >> 2, abort_flag);
     }
 
     ptx::tc_fence_before();
@@ -673,8 +701,9 @@ struct DkvLayout {
     static constexpr int kKVFull = 0, kKVEmpty = 1, kSFull = 2, kDPFull = 3, kPFull = 4, kDSFull = 5,
                          kAccFull = 6, kStFull = 7, kStEmpty = 7 + kStages, kStatFull = 7 + 2 * kStages,
                          kStatEmpty = 7 + 2 * kStages + kStatStages, kDrain = 7 + 2 * kStages + 2 * kStatStages,
-                         kAccEmpty = kDrain + 1;  // block-masked kernels: dK, dV read out
-    static constexpr int kNumBars = kDrain + 2;
+                         kAccEmpty = kDrain + 1,  // block-masked kernels: dK, dV read out
+                         kBitsReady = kDrain + 2;  // dropout kernels: a tile's keep bits written
+    static constexpr int kNumBars = kDrain + 3;
     static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8;
     static constexpr uint32_t kAbort = kTmemSlot + 4;
     static constexpr uint32_t kDynamicSmem = kAbort + 4 + 1024;
@@ -720,7 +749,7 @@ __device__ __forceinline__ uint32_t dkv_bar(uint32_t base, int i) {
     return base + DkvLayout<D>::kBars + 8u * (uint32_t)i;
 }
 
-template <int D, bool M, bool E>
+template <int D, bool M, bool E, bool DR>
 __device__ void dkv_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_do,
                               const CUtensorMap* tm_k, const CUtensorMap* tm_v, const BwdParams& p,
                               uint32_t base, volatile int* abort_flag) {
@@ -781,7 +810,7 @@ drain:
 // Warps 2-3: LSE (as log2) and delta of each query tile into the stage's
 // shared-memory rows; queries past the sequence end get +inf and 0 so that
 // their weights vanish.
-template <int D, bool M, bool E>
+template <int D, bool M, bool E, bool DR>
 __device__ void dkv_stat_role(const BwdParams& p, uint32_t base, uint8_t* smem, volatile int* abort_flag) {
     using L = DkvLayout<D>;
     const int tid = threadIdx.x - 64;  // 0..63
@@ -835,7 +864,7 @@ __device__ void dkv_stat_role(const BwdParams& p, uint32_t base, uint8_t* smem, 
     }
 }
 
-template <int D, bool M, bool E>
+template <int D, bool M, bool E, bool DR>
 __device__ void dkv_mma_role(const BwdParams& p, uint32_t base, uint32_t tmem, volatile int* abort_flag) {
     using L = DkvLayout<D>;
     constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(kTile, kTile, false);  // S^T, dP^T: N = 128 queries
@@ -934,7 +963,7 @@ __device__ void dkv_mma_role(const BwdParams& p, uint32_t base, uint32_t tmem, v
     ptx::drain_wait(dkv_bar<D>(base, L::kDrain), 0u, lim);
 }
 
-template <int D, bool M, bool E>
+template <int D, bool M, bool E, bool DR>
 __device__ void dkv_work_role(const BwdParams& p, uint32_t base, const uint8_t* smem, uint32_t tmem,
                               int wg, volatile int* abort_flag) {
     using L = DkvLayout<D>;
@@ -945,7 +974,7 @@ __device__ void dkv_work_role(const BwdParams& p, uint32_t base, const uint8_t* 
     const uint32_t tDP = tmem + lane_off + 128u + 64u * (uint32_t)wg;  // dS^T (bf16) written over it
     const float sl2 = p.scale_log2;
     const uint64_t lim = p.wait_limit_ns;
-    uint32_t s_phase = 0, dp_phase = 0, acc_phase = 0, ring_phase = 0;
+    uint32_t s_phase = 0, dp_phase = 0, acc_phase = 0, ring_phase = 0, bits_phase = 0;
     int st = 0;
 
     for (int rnd = 0, u = bwd_unit_of_round(0); u < p.num_units; u = bwd_unit_of_round(++rnd)) {
@@ -955,6 +984,31 @@ __device__ void dkv_work_role(const BwdParams& p, uint32_t base, const uint8_t* 
             int bh, qt;
             dkv_iter(w, p, t, bh, qt);
             bool ok = ptx::mbar_wait(dkv_bar<D>(base, L::kStatFull + st), ring_phase, abort_flag, p.status, lim);
+            if constexpr (DR) {
+                // The tile's 128 x 128 keep decisions: 512 Philox blocks (a query
+                // and 32 keys each), two per element-wise thread, written as bits
+                // into the stage in the element-mask layout while S^T is being
+                // computed; every thread then waits for all 256 to have written.
+                if (!__all_sync(0xffffffffu, ok)) return;
+                uint32_t* keepw = reinterpret_cast<uint32_t*>(
+                    const_cast<uint8_t*>(smem) + L::kStat + (uint32_t)st * L::kStatBytes + L::kStatKeep);
+                const int et = threadIdx.x - 128;  // 0 .. 255
+#pragma unroll
+                for (int y = 0; y < 2; ++y) {
+                    const int x = 2 * et + y, qq = x >> 2, b = x & 3;
+                    uint64_t rnd[4];
+                    philox4x64_10((uint64_t)(w.kt * 4 + b), (uint64_t)(qt * kTile + qq), (uint64_t)bh, 0ull,
+                                  p.dropout_seed, p.dropout_offset, rnd);
+                    uint32_t bits = 0u;
+#pragma unroll
+                    for (int c = 0; c < 32; ++c)
+                        bits |= (((uint32_t)(rnd[c >> 3] >> (8 * (c & 7))) & 0xFFu) >= (uint32_t)p.dropout_p8 ? 1u : 0u) << c;
+                    keepw[4 * qq + b] = bits;
+                }
+                ptx::mbar_arrive(dkv_bar<D>(base, L::kBitsReady));
+                ok = ptx::mbar_wait(dkv_bar<D>(base, L::kBitsReady), bits_phase, abort_flag, p.status, lim);
+                bits_phase ^= 1u;
+            }
             ok = ok && ptx::mbar_wait(dkv_bar<D>(base, L::kSFull), s_phase, abort_flag, p.status, lim);
             if (!__all_sync(0xffffffffu, ok)) return;
             s_phase ^= 1u;
@@ -992,9 +1046,28 @@ __device__ void dkv_work_role(const BwdParams& p, uint32_t base, const uint8_t* 
                 for (int c = 0; c < 64; ++c)
                     if (((kw[4 * (64 * wg + c)] >> (r & 31)) & 1u) == 0u) pr[c] = 0.f;
             }
+            // Dropout: bit c of zb keeps (query 64 wg + c, this key), read from
+            // the stage like an element mask.  dV takes the kept weights times
+            // keep_scale, and dP of a dropped weight is 0.
+            uint64_t zb = ~0ull;
+            const float ks = DR ? p.keep_scale : 1.f;
+            if constexpr (DR) {
+                const uint32_t* kw = reinterpret_cast<const uint32_t*>(
+                    smem + L::kStat + (uint32_t)st * L::kStatBytes + L::kStatKeep) + (r >> 5);
+                zb = 0ull;
+#pragma unroll
+                for (int c = 0; c < 64; ++c) zb |= (uint64_t)((kw[4 * (64 * wg + c)] >> (r & 31)) & 1u) << c;
+            }
+            auto kept = [&](int c) -> bool { return !DR || ((zb >> c) & 1ull) != 0ull; };
             uint32_t pk[32];
 #pragma unroll
-            for (int c = 0; c < 32; ++c) pk[c] = ptx::pack_bf16x2(pr[2 * c], pr[2 * c + 1]);
+            for (int c = 0; c < 32; ++c) {
+                if constexpr (DR)
+                    pk[c] = ptx::pack_bf16x2(kept(2 * c) ? pr[2 * c] * ks : 0.f,
+                                             kept(2 * c + 1) ? pr[2 * c + 1] * ks : 0.f);
+                else
+                    pk[c] = ptx::pack_bf16x2(pr[2 * c], pr[2 * c + 1]);
+            }
             ptx::tmem_st32(tS, pk);
             ptx::tmem_st_wait();
             ptx::tc_fence_before();
@@ -1014,10 +1087,11 @@ __device__ void dkv_work_role(const BwdParams& p, uint32_t base, const uint8_t* 
 #pragma unroll
             for (int c = 0; c < 64; c += 4) {
                 const float4 d4 = *reinterpret_cast<const float4*>(dlt + c);
-                const float a0 = pr[c + 0] * (__uint_as_float(dr[c + 0]) - d4.x);
-                const float a1 = pr[c + 1] * (__uint_as_float(dr[c + 1]) - d4.y);
-                const float a2 = pr[c + 2] * (__uint_as_float(dr[c + 2]) - d4.z);
-                const float a3 = pr[c + 3] * (__uint_as_float(dr[c + 3]) - d4.w);
+                auto dp = [&](int e) { return kept(e) ? __uint_as_float(dr[e]) * ks : 0.f; };
+                const float a0 = pr[c + 0] * (dp(c + 0) - d4.x);
+                const float a1 = pr[c + 1] * (dp(c + 1) - d4.y);
+                const float a2 = pr[c + 2] * (dp(c + 2) - d4.z);
+                const float a3 = pr[c + 3] * (dp(c + 3) - d4.w);
                 pk[c / 2] = ptx::pack_bf16x2(a0, a1);
                 pk[c / 2 + 1] = ptx::pack_bf16x2(a2, a3);
             }
@@ -1075,7 +1149,7 @@ __device__ void dkv_work_role(const BwdParams& p, uint32_t base, const uint8_t* 
     }
 }
 
-template <int D, bool M, bool E>
+template <int D, bool M, bool E, bool DR>
 __global__ void __launch_bounds__(DkvLayout<D>::kThreads, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                          const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -1107,6 +1181,7 @@ __global__ void __launch_bounds__(DkvLayout<D>::kThreads, 1)
         }
         ptx::mbar_init(dkv_bar<D>(base, L::kDrain), 1);
         ptx::mbar_init(dkv_bar<D>(base, L::kAccEmpty), 8);  // one per element-wise warp
+        ptx::mbar_init(dkv_bar<D>(base, L::kBitsReady), 256);  // one per element-wise thread
         *abort_flag = 0;
         ptx::fence_barrier_init();
         ptx::prefetch_tensormap(&tm_q);
@@ -1125,12 +1200,12 @@ __global__ void __launch_bounds__(DkvLayout<D>::kThreads, 1)
 
     if (warp < 4) {
         ptx::regs_dec<L::kRegsSmall>();
-        if (warp == 0 && lane == 0) dkv_load_role<D, M, E>(&tm_q, &tm_do, &tm_k, &tm_v, p, base, abort_flag);
-        if (warp == 1 && lane == 0) dkv_mma_role<D, M, E>(p, base, tmem, abort_flag);
-        if (warp >= 2) dkv_stat_role<D, M, E>(p, base, smem, abort_flag);
+        if (warp == 0 && lane == 0) dkv_load_role<D, M, E, DR>(&tm_q, &tm_do, &tm_k, &tm_v, p, base, abort_flag);
+        if (warp == 1 && lane == 0) dkv_mma_role<D, M, E, DR>(p, base, tmem, abort_flag);
+        if (warp >= 2) dkv_stat_role<D, M, E, DR>(p, base, smem, abort_flag);
     } else {
         ptx::regs_inc<L::kRegsWork>();
-        dkv_work_role<D, M, E>(p, base, smem, tmem, (warp - 4) >> 2, abort_flag);
+        dkv_work_role<D, M, E, DR>(p, base, smem, tmem, (warp - 4) >> 2, abort_flag);
     }
 
     ptx::tc_fence_before();

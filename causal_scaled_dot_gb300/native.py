@@ -60,6 +60,9 @@ def load() -> ctypes.CDLL:
         lib.attn_bwd_elem_masked.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci,
                                              ci, cf, ci, vp, ci, vp, ci, vp]
         lib.attn_bwd_elem_masked.restype = ci
+        lib.attn_bwd_dropout.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf,
+                                         ci, cf, ctypes.c_ulonglong, ctypes.c_ulonglong, vp]
+        lib.attn_bwd_dropout.restype = ci
         u64 = ctypes.c_ulonglong
         lib.attn_fwd_dropout.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, ci, cf, u64, u64,
                                          vp]
@@ -216,6 +219,19 @@ def attn_bwd_elem_masked(q, k, v, out, dout, lse, delta, dq, dk, dv, B: int, Hq:
                                      int(mask_heads), _stream(stream))
     if check and rc != ATTN_OK:
         raise AttnError(rc, "attn_bwd_elem_masked")
+    return rc
+
+
+def attn_bwd_dropout(q, k, v, out, dout, lse, delta, dq, dk, dv, B: int, Hq: int, Hkv: int, S: int,
+                     D: int, scale: float, causal: bool | int, dropout_p: float, seed: int, offset: int,
+                     stream=None, check: bool = True) -> int:
+    """The C entry point ``attn_bwd_dropout`` (the dropout of the forward call)."""
+    rc = load().attn_bwd_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse),
+                                 _ptr(delta), _ptr(dq), _ptr(dk), _ptr(dv), int(B), int(Hq), int(Hkv),
+                                 int(S), int(D), float(scale), 1 if causal else 0, float(dropout_p),
+                                 int(seed) & (2**64 - 1), int(offset) & (2**64 - 1), _stream(stream))
+    if check and rc != ATTN_OK:
+        raise AttnError(rc, "attn_bwd_dropout")
     return rc
 
 

@@ -229,6 +229,23 @@ int attn_bwd_elem_masked(const void *q, const void *k, const void *v, const void
                          const unsigned char *block_mask, int mask_heads, void *stream);
 
 /*
+ * attn_bwd_dropout -- attn_bwd for the attention with dropout of
+ * attn_fwd_dropout (same dropout_p, seed, offset; out and lse from that
+ * call).  With Z_ij the keep decision of attn_fwd_dropout and s = 256 /
+ * (256 - p8) the output uses the weights P_ij Z_ij s, so
+ *     dV_j = sum_i P_ij Z_ij s dO_i,   dP_ij = Z_ij s (dO_i . V_j),
+ *     delta_i = dO_i . O_i,            dS_ij = P_ij (dP_ij - delta_i),
+ * and dQ, dK as in attn_bwd.  The keep decisions are regenerated from the
+ * same counter-based generator, not stored.  Arguments, errors and rules as
+ * attn_bwd and attn_fwd_dropout (dropout_p rounds to p8 = round(256 p) <= 255;
+ * p8 = 0 is attn_bwd).
+ */
+int attn_bwd_dropout(const void *q, const void *k, const void *v, const void *out,
+                     const void *dout, const float *lse, float *delta, void *dq, void *dk, void *dv,
+                     int B, int Hq, int Hkv, int S, int D, float scale, int causal, float dropout_p,
+                     unsigned long long seed, unsigned long long offset, void *stream);
+
+/*
  * attn_out_proj -- the layer's output projection applied to attention's
  * output where it lies (the "output projection" operator the ainews.cool
  * article profiles right after attention, per-operator table):

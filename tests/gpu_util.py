@@ -178,16 +178,18 @@ def run_gpu_bwd(q_bits, k_bits, v_bits, do_bits, scale, causal, stream=None):
     return tuple(t.double().cpu().numpy() for t in (out, lse, dq, dk, dv, delta))
 
 
-def compare_grad(g, ref, label):
+def compare_grad(g, ref, label, abs_err: float = 0.0):
     """Relative L2 and largest error against the tensor's largest magnitude, with
     an absolute floor of 1e-3 per element: a gradient that is exactly 0 (causal
-    row 0's dQ, a single key) is compared absolutely."""
+    row 0's dQ, a single key) is compared absolutely.  ``abs_err`` is a bound on
+    an additive per-element error known from the arithmetic (it is taken off
+    each element's error before the relative checks)."""
     assert np.all(np.isfinite(g)), f"{label}: non-finite values (unwritten rows?)"
     if ref.size == 0:
         return {}
-    err = np.abs(g - ref)
+    err = np.maximum(np.abs(g - ref) - abs_err, 0.0)
     floor = 1e-3
-    rel_l2 = float(np.linalg.norm(g - ref) / max(np.linalg.norm(ref), floor * math.sqrt(ref.size)))
+    rel_l2 = float(np.linalg.norm(err) / max(np.linalg.norm(ref), floor * math.sqrt(ref.size)))
     max_rel = float(np.max(err)) / max(float(np.max(np.abs(ref))), floor)
     assert rel_l2 <= TOL_GRAD_REL_L2, f"{label}: rel L2 {rel_l2:.3e} > {TOL_GRAD_REL_L2}"
     assert max_rel <= TOL_GRAD_MAX_REL, f"{label}: max abs / max|ref| {max_rel:.3e} > {TOL_GRAD_MAX_REL}"
@@ -283,5 +285,28 @@ def run_gpu_bwd_elem_masked(q_bits, k_bits, v_bits, do_bits, scale, causal, keep
     delta = torch.full((B, Hq, S), float("nan"), dtype=torch.float32, device="cuda")
     native.attn_bwd_elem_masked(q, k, v, out, do, lse, delta, dq, dk, dv, B, Hq, Hkv, S, D, scale,
                                 causal, kb, hk, bm, hm, stream=stream)
+    native.attn_sync_status(stream)
+    return tuple(t.double().cpu().numpy() for t in (out, lse, dq, dk, dv, delta))
+
+
+def run_gpu_bwd_dropout(q_bits, k_bits, v_bits, do_bits, scale, causal, dropout_p, seed, offset,
+                        stream=None):
+    """attn_fwd_dropout then attn_bwd_dropout on the same buffers.
+    Returns float64 (O, LSE, dQ, dK, dV, delta)."""
+    import torch
+    from causal_scaled_dot_gb300 import native
+    B, Hq, S, D = q_bits.shape
+    Hkv = k_bits.shape[1]
+    q, k, v, do = to_device(q_bits), to_device(k_bits), to_device(v_bits), to_device(do_bits)
+    out = torch.empty_like(q)
+    lse = torch.empty((B, Hq, S), dtype=torch.float32, device="cuda")
+    native.attn_fwd_dropout(q, k, v, out, lse, B, Hq, Hkv, S, D, scale, causal, dropout_p, seed, offset,
+                            stream=stream)
+    dq = torch.full_like(q, float("nan"))
+    dk = torch.full_like(k, float("nan"))
+    dv = torch.full_like(v, float("nan"))
+    delta = torch.full((B, Hq, S), float("nan"), dtype=torch.float32, device="cuda")
+    native.attn_bwd_dropout(q, k, v, out, do, lse, delta, dq, dk, dv, B, Hq, Hkv, S, D, scale, causal,
+                            dropout_p, seed, offset, stream=stream)
     native.attn_sync_status(stream)
     return tuple(t.double().cpu().numpy() for t in (out, lse, dq, dk, dv, delta))

@@ -183,6 +183,15 @@ def test_elem_masked_bwd_rejects_bad_masks_before_launch():
     assert lib.attn_bwd_elem_masked(*args[:14], 96, *args[15:], ok_bits, 1, None, 1, None) == ATTN_ERR_UNSUPPORTED
 
 
+def test_dropout_bwd_rejects_bad_rates_before_launch():
+    lib = native.load()
+    args = [1 << 40, 2 << 40, 3 << 40, 4 << 40, 5 << 40, 6 << 40, 7 << 40, 8 << 40, 9 << 40,
+            10 << 40, 1, 2, 2, 300, 128, ctypes.c_float(0.1), 1]
+    for bad in (-0.1, float("nan"), float("inf"), 0.999):
+        assert lib.attn_bwd_dropout(*args, ctypes.c_float(bad), 1, 2, None) == ATTN_ERR_INVALID_ARG
+    assert lib.attn_bwd_dropout(*args[:14], 96, *args[15:], ctypes.c_float(0.1), 1, 2, None) == ATTN_ERR_UNSUPPORTED
+
+
 def test_keep_bit_packing():
     from causal_scaled_dot_gb300.inputs import (block_mask_of_keep_bits, keep_row_bytes, pack_keep_bits,
                                                 random_keep_bits, unpack_keep_bits, window_keep_bits)
