@@ -1,6 +1,14 @@
 /*
- * attn.h -- C ABI of libattn: causal scaled dot-product attention forward on
- * GB300 (sm_103a).
+ * attn.h -- C ABI of libattn: causal scaled dot-product attention on GB300
+ * (sm_103a).
+ *
+ * Entry points: the forward (attn_fwd; FP8 inputs attn_fwd_fp8; block masks
+ * attn_fwd_block_masked; per-pair keep bits attn_fwd_elem_masked; dropout of
+ * the weights attn_fwd_dropout), the matching gradients (attn_bwd,
+ * attn_bwd_block_masked, attn_bwd_elem_masked, attn_bwd_dropout), the output
+ * projection of the attention output (attn_out_proj), and status helpers
+ * (attn_sync_status, attn_selftest_wait_timeout, attn_status_string,
+ * attn_version).
  *
  * The operation (one output row per query position i of every batch b and
  * query head hq) is the five-step naive causal attention that the
