@@ -38,6 +38,15 @@
 // use: in the dQ kernel LSE and delta_i = dO_i . O_i (computed there from
 // global O and dO), in the dK/dV kernel LSE and delta of each query tile.
 //
+// Template flags: M, a block mask (dropped tiles are neither loaded nor
+// computed; units without kept tiles write zeros); E, per-pair keep bits (the
+// dQ element-wise threads read their row's bytes a key tile ahead, the dK/dV
+// statistics warps stage each query tile's bytes in shared memory); DR,
+// dropout of the weights with the forward's Philox keep decisions regenerated
+// (in the dQ kernel per row, in the dK/dV kernel by all 256 element-wise
+// threads into shared memory), dV taking the kept weights times
+// 256 / (256 - p8) and dP of a dropped weight being 0.
+//
 // Every wait is bounded (ptx::mbar_wait); after a timeout each role returns,
 // the producer first letting its issued copies land, the MMA issuer its
 // issued products complete, so that the CTA can release its memory.
