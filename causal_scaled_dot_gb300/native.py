@@ -296,3 +296,82 @@ def attention(q, k, v, causal: bool = True, scale: float | None = None, out=None
         lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
     attn_fwd(q, k, v, out, lse, B, Hq, Hkv, S, D, scale, causal, stream)
     return (out, lse) if return_lse else out
+
+
+def _attention_function():
+    """A torch.autograd.Function over the C ABI: forward and backward are the
+    library's entry points (argument marshalling only)."""
+    import torch
+
+    class AttentionFunction(torch.autograd.Function):
+        @staticmethod
+        def forward(ctx, q, k, v, causal, scale, block_mask, keep_bits, dropout_p, seed, offset):
+            B, Hq, S, D = q.shape
+            Hkv = k.shape[1]
+            out = torch.empty_like(q)
+            lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
+            hm = 1 if block_mask is None else block_mask.shape[0]
+            if dropout_p > 0.0:
+                attn_fwd_dropout(q, k, v, out, lse, B, Hq, Hkv, S, D, scale, causal, dropout_p, seed, offset)
+            elif keep_bits is not None:
+                attn_fwd_elem_masked(q, k, v, out, lse, B, Hq, Hkv, S, D, scale, causal, keep_bits,
+                                     keep_bits.shape[0], block_mask, hm)
+            elif block_mask is not None:
+                attn_fwd_block_masked(q, k, v, out, lse, B, Hq, Hkv, S, D, scale, causal, block_mask, hm)
+            else:
+                attn_fwd(q, k, v, out, lse, B, Hq, Hkv, S, D, scale, causal)
+            ctx.save_for_backward(q, k, v, out, lse)
+            ctx.masks = (block_mask, keep_bits)
+            ctx.args = (causal, scale, dropout_p, seed, offset)
+            return out
+
+        @staticmethod
+        def backward(ctx, dout):
+            q, k, v, out, lse = ctx.saved_tensors
+            block_mask, keep_bits = ctx.masks
+            causal, scale, dropout_p, seed, offset = ctx.args
+            B, Hq, S, D = q.shape
+            Hkv = k.shape[1]
+            dout = dout.contiguous()
+            dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+            delta = torch.empty_like(lse)
+            hm = 1 if block_mask is None else block_mask.shape[0]
+            if dropout_p > 0.0:
+                attn_bwd_dropout(q, k, v, out, dout, lse, delta, dq, dk, dv, B, Hq, Hkv, S, D, scale, causal,
+                                 dropout_p, seed, offset)
+            elif keep_bits is not None:
+                attn_bwd_elem_masked(q, k, v, out, dout, lse, delta, dq, dk, dv, B, Hq, Hkv, S, D, scale,
+                                     causal, keep_bits, keep_bits.shape[0], block_mask, hm)
+            elif block_mask is not None:
+                attn_bwd_block_masked(q, k, v, out, dout, lse, delta, dq, dk, dv, B, Hq, Hkv, S, D, scale,
+                                      causal, block_mask, hm)
+            else:
+                attn_bwd(q, k, v, out, dout, lse, delta, dq, dk, dv, B, Hq, Hkv, S, D, scale, causal)
+            return dq, dk, dv, None, None, None, None, None, None, None
+
+    return AttentionFunction
+
+
+_ATTENTION_FUNCTION = None
+
+
+def attention_trainable(q, k, v, causal: bool = True, scale: float | None = None, block_mask=None,
+                        keep_bits=None, dropout_p: float = 0.0, seed: int = 0, offset: int = 0):
+    """O = attention(q, k, v) with gradients: forward and backward run the C ABI
+    (attn_fwd / attn_bwd, or their block-masked, element-masked or dropout
+    forms).  q [B,Hq,S,D], k/v [B,Hkv,S,D] bf16 CUDA tensors; block_mask uint8
+    [1 or Hq, nt, nt]; keep_bits uint8 [1 or Hq, S, 16*nt] (may come with a
+    block mask); dropout takes no mask."""
+    global _ATTENTION_FUNCTION
+    import torch
+    if dropout_p > 0.0 and (block_mask is not None or keep_bits is not None):
+        raise ValueError("dropout with a mask is not supported")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 CUDA [B,H,S,D] tensor")
+    if scale is None:
+        scale = 1.0 / math.sqrt(q.shape[-1])
+    if _ATTENTION_FUNCTION is None:
+        _ATTENTION_FUNCTION = _attention_function()
+    return _ATTENTION_FUNCTION.apply(q, k, v, bool(causal), float(scale), block_mask, keep_bits,
+                                     float(dropout_p), int(seed), int(offset))
