@@ -154,6 +154,16 @@ int check_args(const void* q, const void* k, const void* v, void* out, float* ls
     return ATTN_OK;
 }
 
+// A mask input (bytes at m) may not overlap the outputs it would be read
+// alongside: O (and LSE when given).
+int check_mask_overlap(const void* m, size_t m_bytes, const void* out, const float* lse, int B, int Hq,
+                       int S, int D) {
+    if (m == nullptr) return ATTN_OK;
+    if (ranges_overlap(m, m_bytes, out, (size_t)B * Hq * S * D * 2)) return ATTN_ERR_INVALID_ARG;
+    if (lse != nullptr && ranges_overlap(m, m_bytes, lse, (size_t)B * Hq * S * 4)) return ATTN_ERR_INVALID_ARG;
+    return ATTN_OK;
+}
+
 template <int D>
 int launch_simple(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                   const FwdParams& p, cudaStream_t stream) {
@@ -259,6 +269,10 @@ int fwd_bf16(const void* q, const void* k, const void* v, void* out, float* lse,
              void* stream, const uint8_t* keep_bits, int keep_heads) {
     int rc = check_args(q, k, v, out, lse, B, Hq, Hkv, S, D, scale);
     if (rc != ATTN_OK) return rc;
+    const size_t nt = (size_t)((S + kTile - 1) / kTile);
+    if (check_mask_overlap(block_mask, (size_t)mask_heads * nt * nt, out, lse, B, Hq, S, D) != ATTN_OK ||
+        check_mask_overlap(keep_bits, (size_t)keep_heads * S * 16 * nt, out, lse, B, Hq, S, D) != ATTN_OK)
+        return ATTN_ERR_INVALID_ARG;
     DeviceState* dev = nullptr;
     rc = current_device_state(&dev);
     if (rc != ATTN_OK) return rc;

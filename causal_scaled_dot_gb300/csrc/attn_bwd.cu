@@ -162,6 +162,19 @@ int bwd(const void* q, const void* k, const void* v, const void* out, const void
         unsigned long long offset) {
     int rc = check_bwd_args(q, k, v, out, dout, lse, delta, dq, dk, dv, B, Hq, Hkv, S, D, scale);
     if (rc != ATTN_OK) return rc;
+    {  // mask inputs may not overlap the outputs
+        const size_t nt = (size_t)((S + kTile - 1) / kTile);
+        const size_t qb = (size_t)B * Hq * S * D * 2, kb = (size_t)B * Hkv * S * D * 2, lb = (size_t)B * Hq * S * 4;
+        const void* masks[2] = {block_mask, keep_bits};
+        const size_t mask_bytes[2] = {(size_t)mask_heads * nt * nt, (size_t)keep_heads * S * 16 * nt};
+        for (int m = 0; m < 2; ++m)
+            if (masks[m] != nullptr &&
+                (host::ranges_overlap(masks[m], mask_bytes[m], dq, qb) ||
+                 host::ranges_overlap(masks[m], mask_bytes[m], dk, kb) ||
+                 host::ranges_overlap(masks[m], mask_bytes[m], dv, kb) ||
+                 host::ranges_overlap(masks[m], mask_bytes[m], delta, lb)))
+                return ATTN_ERR_INVALID_ARG;
+    }
     int sm_count = 0;
     unsigned int* status = nullptr;
     rc = host::current_device(&sm_count, &status);

@@ -192,6 +192,25 @@ def test_dropout_bwd_rejects_bad_rates_before_launch():
     assert lib.attn_bwd_dropout(*args[:14], 96, *args[15:], ctypes.c_float(0.1), 1, 2, None) == ATTN_ERR_UNSUPPORTED
 
 
+def test_masks_overlapping_outputs_are_rejected_before_launch():
+    """A block mask or keep bits that overlap O / LSE (forward) or dQ / dK / dV /
+    delta (backward) is an argument error."""
+    lib = native.load()
+    q, k, v, out = 1 << 40, 2 << 40, 3 << 40, 4 << 40
+    B, Hq, Hkv, S, D = 1, 2, 2, 300, 128
+    f = ctypes.c_float(0.1)
+    # forward: a block mask inside O, keep bits inside LSE
+    assert lib.attn_fwd_block_masked(q, k, v, out, None, B, Hq, Hkv, S, D, f, 1, out + 4096, 1,
+                                     None) == ATTN_ERR_INVALID_ARG
+    lse = 5 << 40
+    assert lib.attn_fwd_elem_masked(q, k, v, out, lse, B, Hq, Hkv, S, D, f, 1, lse + 1024, 1, None, 1,
+                                    None) == ATTN_ERR_INVALID_ARG
+    # backward: keep bits inside dK
+    bargs = [q, k, v, out, 6 << 40, lse, 7 << 40, 8 << 40, 9 << 40, 10 << 40, B, Hq, Hkv, S, D, f, 1]
+    assert lib.attn_bwd_elem_masked(*bargs, (9 << 40) + 4096, 1, None, 1, None) == ATTN_ERR_INVALID_ARG
+    assert lib.attn_bwd_block_masked(*bargs, (7 << 40) + 64, 1, None) == ATTN_ERR_INVALID_ARG
+
+
 def test_keep_bit_packing():
     from causal_scaled_dot_gb300.inputs import (block_mask_of_keep_bits, keep_row_bytes, pack_keep_bits,
                                                 random_keep_bits, unpack_keep_bits, window_keep_bits)
