@@ -91,6 +91,14 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     f.restype = ci
     f.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, ci, ctypes.c_uint64, ctypes.c_uint64,
                   vp, ctypes.c_int64, vp, vp, vp, vp, ci]
+    f = lib.oracle_attn_rows_ex
+    f.restype = ci
+    f.argtypes = [vp, vp, vp, ci, cf, cf, cf, ci, ci, ci, ci, ci, cf, ci, vp, ci, vp, ci, ci,
+                  ctypes.c_uint64, ctypes.c_uint64, vp, ctypes.c_int64, vp, vp, ci]
+    f = lib.oracle_attn_bwd_ex
+    f.restype = ci
+    f.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, vp, ci, vp, ci, ci, ctypes.c_uint64,
+                  ctypes.c_uint64, vp, ctypes.c_int64, vp, vp, vp, vp, ci]
     f = lib.oracle_attn_bwd_keep
     f.restype = ci
     f.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, vp, ci, vp, ci, vp, ctypes.c_int64,
@@ -236,6 +244,38 @@ def attention_keep(q_bits, k_bits, v_bits, scale: float, keep_bits, causal: bool
     return out, lse
 
 
+def attention_ex(q, k, v, scale: float, causal: bool = True, descales=None, block_mask=None,
+                 keep_bits=None, dropout=None, rows=None, nthreads: int | None = None,
+                 lib: ctypes.CDLL | None = None):
+    """Every forward variant at once: q, k, v as bf16 bit patterns (uint16) or,
+    with ``descales`` = (q, k, v) factors, E4M3 codes (uint8); optional block
+    mask and keep bits (as in ``attention_masked`` / ``attention_keep``, both
+    applying when given) and dropout = (p8, seed, offset)."""
+    lib = lib or load()
+    fp8 = descales is not None
+    if fp8:
+        q, k, v = (np.ascontiguousarray(x, dtype=np.uint8) for x in (q, k, v))
+    else:
+        q, k, v = (_as_bits(x, n) for x, n in ((q, "q"), (k, "k"), (v, "v")))
+    B, Hq, Hkv, S, D = _shapes(q, k, v)
+    bm = _block(block_mask, Hq, S)
+    km = None if keep_bits is None else _keep(keep_bits, Hq, S)
+    p8, seed, offset = dropout if dropout is not None else (0, 0, 0)
+    ds = descales if fp8 else (1.0, 1.0, 1.0)
+    rows_arr, nrows, out, lse = _outputs(B, Hq, S, D, rows)
+    rc = lib.oracle_attn_rows_ex(
+        q.ctypes.data, k.ctypes.data, v.ctypes.data, 1 if fp8 else 0,
+        *(ctypes.c_float(float(x)) for x in ds), B, Hq, Hkv, S, D, ctypes.c_float(scale),
+        1 if causal else 0, None if bm is None else bm.ctypes.data, 1 if bm is None else bm.shape[0],
+        None if km is None else km.ctypes.data, 1 if km is None else km.shape[0], int(p8),
+        int(seed) & (2**64 - 1), int(offset) & (2**64 - 1),
+        None if rows_arr is None else rows_arr.ctypes.data, nrows,
+        out.ctypes.data, lse.ctypes.data, nthreads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle_attn_rows_ex rejected its arguments")
+    return out, lse
+
+
 def e4m3_decode(codes, lib: ctypes.CDLL | None = None) -> np.ndarray:
     """The oracle's own E4M3 decoding of uint8 codes, as float64."""
     lib = lib or load()
@@ -314,7 +354,7 @@ def attention_bwd(q, k, v, dout, scale: float, causal: bool = True, kv_heads=Non
     delta_i = sum_j P_ij (dO_i . V_j), the row term of the softmax gradient.
     block_mask: optional uint8 [1 or Hq, nt, nt] as in ``attention_masked``;
     keep_bits: optional element mask as in ``attention_keep``.
-    dropout: optional (p8, seed, offset) as in ``attention_dropout`` (no mask with it).
+    dropout: optional (p8, seed, offset) as in ``attention_dropout`` (masks may come with it).
     """
     lib = lib or load()
     f64 = np.asarray(q).dtype == np.float64
@@ -338,9 +378,15 @@ def attention_bwd(q, k, v, dout, scale: float, causal: bool = True, kv_heads=Non
     tail = (None if heads is None else heads.ctypes.data, n, dq.ctypes.data, dk.ctypes.data,
             dv.ctypes.data, delta.ctypes.data, nthreads or default_threads())
     bm = _block(block_mask, Hq, S)
-    if dropout is not None:
-        if bm is not None or keep_bits is not None:
-            raise ValueError("dropout gradients take no mask")
+    if dropout is not None and (bm is not None or keep_bits is not None):
+        km = None if keep_bits is None else _keep(keep_bits, Hq, S)
+        p8, seed, offset = dropout
+        rc = lib.oracle_attn_bwd_ex(*common, None if bm is None else bm.ctypes.data,
+                                    1 if bm is None else bm.shape[0],
+                                    None if km is None else km.ctypes.data,
+                                    1 if km is None else km.shape[0], int(p8),
+                                    int(seed) & (2**64 - 1), int(offset) & (2**64 - 1), *tail)
+    elif dropout is not None:
         p8, seed, offset = dropout
         rc = lib.oracle_attn_bwd_dropout(*common, int(p8), int(seed) & (2**64 - 1),
                                          int(offset) & (2**64 - 1), *tail)

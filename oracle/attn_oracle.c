@@ -715,3 +715,40 @@ int oracle_attn_bwd_dropout(const void *q, const void *k, const void *v, const v
     return bwd_run(q, k, v, dout, f64_inputs, B, Hq, Hkv, S, D, scale, causal, NULL, 1, NULL, 1, p8,
                    seed, offset, kv_heads, n_kv_heads, dq, dk, dv, delta, nthreads);
 }
+
+/*
+ * oracle_attn_rows_ex -- every forward variant at once: inputs as bf16 bit
+ * patterns (format 0) or E4M3 codes with per-tensor descales (format 1); an
+ * optional block mask and optional keep bits (NULL for none; the masks
+ * combine); dropout of the weights with p8 > 0 (key {seed, offset}).
+ */
+int oracle_attn_rows_ex(const void *q, const void *k, const void *v, int format, float q_descale,
+                        float k_descale, float v_descale, int B, int Hq, int Hkv, int S, int D,
+                        float scale, int causal, const uint8_t *block_mask, int mask_heads,
+                        const uint8_t *keep_bits, int keep_heads, int p8, uint64_t seed,
+                        uint64_t offset, const int64_t *rows, int64_t nrows, double *out,
+                        double *lse, int nthreads) {
+    const double ds[3] = {(double)q_descale, (double)k_descale, (double)v_descale};
+    const double one[3] = {1.0, 1.0, 1.0};
+    if (format != FMT_BF16 && format != FMT_E4M3) return 1;
+    if (p8 < 0 || p8 > 255) return 1;
+    return run_rows_dropout(q, k, v, format, format == FMT_E4M3 ? ds : one, B, Hq, Hkv, S, D, scale,
+                            causal, block_mask, block_mask ? mask_heads : 1, keep_bits,
+                            keep_bits ? keep_heads : 1, p8, seed, offset, rows, nrows, out, lse,
+                            nthreads);
+}
+
+/*
+ * oracle_attn_bwd_ex -- the gradients of oracle_attn_rows_ex's bf16 (or
+ * double) variants: optional block mask, optional keep bits and dropout.
+ */
+int oracle_attn_bwd_ex(const void *q, const void *k, const void *v, const void *dout, int f64_inputs,
+                       int B, int Hq, int Hkv, int S, int D, float scale, int causal,
+                       const uint8_t *block_mask, int mask_heads, const uint8_t *keep_bits,
+                       int keep_heads, int p8, uint64_t seed, uint64_t offset,
+                       const int64_t *kv_heads, int64_t n_kv_heads, double *dq, double *dk,
+                       double *dv, double *delta, int nthreads) {
+    return bwd_run(q, k, v, dout, f64_inputs, B, Hq, Hkv, S, D, scale, causal, block_mask,
+                   block_mask ? mask_heads : 1, keep_bits, keep_bits ? keep_heads : 1, p8, seed, offset,
+                   kv_heads, n_kv_heads, dq, dk, dv, delta, nthreads);
+}

@@ -823,3 +823,96 @@ def pin_bwd_dropout_autograd(bwdd):
 
 
 BWD_DROPOUT_PINS = [pin_bwd_dropout_autograd]
+
+
+# ---------------------------------------------------------------- combined variants
+# ``attnx(q, k, v, scale, causal, descales=None, block_mask=None, keep_bits=None,
+# dropout=None)`` and ``bwdx(q, k, v, dout, scale, causal, block_mask, keep_bits, dropout)``.
+
+def _combo_inputs(seed, S=200, Hq=4, Hkv=2, D=8):
+    q, k, v = (_rand((1, H, S, D), seed, t) for t, H in ((0, Hq), (1, Hkv), (2, Hkv)))
+    rng = np.random.default_rng(seed)
+    nt = (S + 127) // 128
+    bm = (rng.random((Hq, nt, nt)) < 0.8).astype(np.uint8)
+    keep = rng.random((1, S, S)) < 0.7
+    bits = np.zeros((1, S, _keep_rows(S)), np.uint8)
+    for jj in range(S):
+        bits[:, :, jj // 8] |= (keep[:, :, jj].astype(np.uint8) << (jj % 8))
+    return q, k, v, bm, keep, bits
+
+
+def _combo_torch(qf, kf, vf, scale, causal, bm, keep, Z, s):
+    Hq, S = qf.shape[1], qf.shape[2]
+    em = _expand_block_mask(bm, Hq, S, False) & torch.from_numpy(keep).expand(Hq, S, S)
+    if causal:
+        em = em & torch.ones(S, S, dtype=torch.bool).tril()
+    sc = torch.einsum("bhid,bhjd->bhij", qf, kf) * scale
+    sc = sc.masked_fill(~em, float("-inf"))
+    none = ~em.any(dim=-1)
+    p = torch.softmax(sc.masked_fill(none[None, :, :, None], 0.0), dim=-1).masked_fill(~em, 0.0)
+    return torch.einsum("bhij,bhjd->bhid", p * Z * s, vf), torch.logsumexp(sc, dim=-1), none
+
+
+def pin_combo_library(attnx):
+    """Block mask, keep bits and dropout together against the float64 formula in
+    torch (masked softmax, rows without keys 0, weights times Z * 256/(256-p8) with
+    Z from numpy's Philox)."""
+    q, k, v, bm, keep, bits = _combo_inputs(351)
+    Hq, Hkv, S = 4, 2, 200
+    p8, seed, offset = 60, 0xABC, 3
+    Z = torch.from_numpy(np.stack([keep_table(h, S, p8, seed, offset) for h in range(Hq)])[None].astype(np.float64))
+    sc32 = float(np.float32(0.3))
+    qf = torch.from_numpy(f64(q))
+    kf = torch.from_numpy(f64(k)).repeat_interleave(Hq // Hkv, 1)
+    vf = torch.from_numpy(f64(v)).repeat_interleave(Hq // Hkv, 1)
+    for causal in (True, False):
+        O, L = attnx(q, k, v, 0.3, causal, block_mask=bm, keep_bits=bits, dropout=(p8, seed, offset))
+        ref, lse, none = _combo_torch(qf, kf, vf, sc32, causal, bm, keep, Z, 256.0 / (256 - p8))
+        np.testing.assert_allclose(O, ref.numpy(), rtol=0, atol=1e-12)
+        live = ~none.numpy()
+        np.testing.assert_allclose(L[0][live], lse.numpy()[0][live], rtol=0, atol=1e-12)
+        assert np.all(np.isneginf(L[0][~live]))
+
+
+def pin_combo_e4m3_masks(attnx):
+    """E4M3 inputs with a block mask and keep bits against torch's float64 SDPA on
+    the decoded values (torch's own float8_e4m3fn conversion) with the same mask."""
+    from causal_scaled_dot_gb300.inputs import float32_to_e4m3_codes
+    q, k, v, bm, keep, bits = _combo_inputs(361)
+    Hq, Hkv, S = 4, 2, 200
+    codes = [float32_to_e4m3_codes(f64(x).astype(np.float32)) for x in (q, k, v)]
+    ds = (0.5, 2.0, 0.25)
+    dec = [torch.from_numpy(c).view(torch.float8_e4m3fn).to(torch.float64) * d for c, d in zip(codes, ds)]
+    qf, kf, vf = dec[0], dec[1].repeat_interleave(Hq // Hkv, 1), dec[2].repeat_interleave(Hq // Hkv, 1)
+    for causal in (True, False):
+        O, L = attnx(*codes, 0.3, causal, descales=ds, block_mask=bm, keep_bits=bits)
+        ref, lse, none = _combo_torch(qf, kf, vf, float(np.float32(0.3)), causal, bm, keep, 1.0, 1.0)
+        np.testing.assert_allclose(O, ref.numpy(), rtol=0, atol=1e-12)
+        live = ~none.numpy()
+        np.testing.assert_allclose(L[0][live], lse.numpy()[0][live], rtol=0, atol=1e-12)
+
+
+COMBO_PINS = [pin_combo_library, pin_combo_e4m3_masks]
+
+
+def pin_bwd_combo_autograd(bwdx):
+    """Gradients with a block mask, keep bits and dropout together against torch's
+    float64 autograd of the same formula."""
+    q, k, v, bm, keep, bits = _combo_inputs(371)
+    Hq, Hkv, S, D = 4, 2, 200, 8
+    dout = _rand((1, Hq, S, D), 371, 3)
+    G = Hq // Hkv
+    p8, seed, offset = 25, 0x77, 1
+    Z = torch.from_numpy(np.stack([keep_table(h, S, p8, seed, offset) for h in range(Hq)])[None].astype(np.float64))
+    for causal in (True, False):
+        dq, dk, dv, _ = bwdx(q, k, v, dout, 0.4, causal, bm, bits, (p8, seed, offset))
+        tq, tk, tv = (torch.from_numpy(f64(x)).requires_grad_() for x in (q, k, v))
+        o, _, _ = _combo_torch(tq, tk.repeat_interleave(G, 1), tv.repeat_interleave(G, 1),
+                               float(np.float32(0.4)), causal, bm, keep, Z, 256.0 / (256 - p8))
+        o.backward(torch.from_numpy(f64(dout)))
+        for name, a, t in (("dQ", dq, tq), ("dK", dk, tk), ("dV", dv, tv)):
+            ref = t.grad.numpy()
+            assert np.max(np.abs(a - ref)) <= 1e-12 * max(1.0, float(np.max(np.abs(ref)))), name
+
+
+BWD_COMBO_PINS = [pin_bwd_combo_autograd]

@@ -201,3 +201,23 @@ def _bwdd(q, k, v, dout, scale, causal, dropout, kv_heads=None):
 @pytest.mark.parametrize("pin", oracle_pins.BWD_DROPOUT_PINS, ids=lambda p: p.__name__)
 def test_oracle_bwd_dropout_pin(pin):
     pin(_bwdd)
+
+
+def _attnx(q, k, v, scale, causal, descales=None, block_mask=None, keep_bits=None, dropout=None):
+    return oracle.attention_ex(q, k, v, scale, causal, descales=descales, block_mask=block_mask,
+                               keep_bits=keep_bits, dropout=dropout)
+
+
+@pytest.mark.parametrize("pin", oracle_pins.COMBO_PINS, ids=lambda p: p.__name__)
+def test_oracle_combo_pin(pin):
+    pin(_attnx)
+
+
+def _bwdx(q, k, v, dout, scale, causal, block_mask, keep_bits, dropout):
+    return oracle.attention_bwd(q, k, v, dout, scale, causal, block_mask=block_mask, keep_bits=keep_bits,
+                                dropout=dropout)
+
+
+@pytest.mark.parametrize("pin", oracle_pins.BWD_COMBO_PINS, ids=lambda p: p.__name__)
+def test_oracle_bwd_combo_pin(pin):
+    pin(_bwdx)
