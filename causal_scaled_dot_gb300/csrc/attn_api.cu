@@ -42,6 +42,25 @@ cudaError_t allow_smem(K kernel, uint32_t bytes) {
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
+template <int D, bool F, bool M, bool DR, bool E>
+bool allow_ws() {
+    return allow_smem(attn_fwd_ws_kernel<D, F, M, DR, E>, WsLayout<D, F>::kDynamicSmem) == cudaSuccess;
+}
+
+// Every instantiation of the persistent forward kernel that launch_any uses.
+template <int D>
+bool allow_ws_bf16() {
+    return allow_ws<D, false, false, false, false>() && allow_ws<D, false, true, false, false>() &&
+           allow_ws<D, false, false, true, false>() && allow_ws<D, false, false, false, true>() &&
+           allow_ws<D, false, true, false, true>() && allow_ws<D, false, true, true, false>() &&
+           allow_ws<D, false, false, true, true>() && allow_ws<D, false, true, true, true>();
+}
+bool allow_ws_all() {
+    return allow_ws_bf16<64>() && allow_ws_bf16<128>() && allow_ws<128, true, false, false, false>() &&
+           allow_ws<128, true, true, false, false>() && allow_ws<128, true, false, false, true>() &&
+           allow_ws<128, true, true, false, true>();
+}
+
 // Per-device setup, once: capability check, SM count, status-word address,
 // shared-memory opt-in for every kernel.  Caller holds g_mutex.
 int setup_device_locked(int dev) {
@@ -62,17 +81,7 @@ int setup_device_locked(int dev) {
     if (cudaGetSymbolAddress(&word, g_attn_status) != cudaSuccess ||
         allow_smem(attn_fwd_simple_kernel<64>, SimpleLayout<64>::kDynamicSmem) != cudaSuccess ||
         allow_smem(attn_fwd_simple_kernel<128>, SimpleLayout<128>::kDynamicSmem) != cudaSuccess ||
-        allow_smem(attn_fwd_ws_kernel<64, false, false, false, false>, WsLayout<64, false>::kDynamicSmem) != cudaSuccess ||
-        allow_smem(attn_fwd_ws_kernel<128, false, false, false, false>, WsLayout<128, false>::kDynamicSmem) != cudaSuccess ||
-        allow_smem(attn_fwd_ws_kernel<128, true, false, false, false>, WsLayout<128, true>::kDynamicSmem) != cudaSuccess ||
-        allow_smem(attn_fwd_ws_kernel<64, false, true, false, false>, WsLayout<64, false>::kDynamicSmem) != cudaSuccess ||
-        allow_smem(attn_fwd_ws_kernel<128, false, true, false, false>, WsLayout<128, false>::kDynamicSmem) != cudaSuccess ||
-        allow_smem(attn_fwd_ws_kernel<64, false, false, true, false>, WsLayout<64, false>::kDynamicSmem) != cudaSuccess ||
-        allow_smem(attn_fwd_ws_kernel<128, false, false, true, false>, WsLayout<128, false>::kDynamicSmem) != cudaSuccess ||
-        allow_smem(attn_fwd_ws_kernel<64, false, false, false, true>, WsLayout<64, false>::kDynamicSmem) != cudaSuccess ||
-        allow_smem(attn_fwd_ws_kernel<128, false, false, false, true>, WsLayout<128, false>::kDynamicSmem) != cudaSuccess ||
-        allow_smem(attn_fwd_ws_kernel<64, false, true, false, true>, WsLayout<64, false>::kDynamicSmem) != cudaSuccess ||
-        allow_smem(attn_fwd_ws_kernel<128, false, true, false, true>, WsLayout<128, false>::kDynamicSmem) != cudaSuccess) {
+        !allow_ws_all()) {
         st.status = ATTN_ERR_DEVICE;
         return st.status;
     }
@@ -95,6 +104,11 @@ int setup_device_locked(int dev) {
 int current_device_state(DeviceState** out) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_DEVICE;
+    // A thread that has made no context-binding runtime call reports device 0
+    // with no driver context current, and the tensor-map encoder is a driver
+    // call that then fails; binding the device's primary context here makes
+    // every entry point callable from any thread (an autograd worker, say).
+    if (cudaSetDevice(dev) != cudaSuccess) return ATTN_ERR_DEVICE;
     std::lock_guard<std::mutex> lock(g_mutex);
     const int rc = setup_device_locked(dev);
     *out = &g_devices[dev];
@@ -117,9 +131,6 @@ int encode_3d(CUtensorMap* map, const void* ptr, int elem_bytes, int D, int S, l
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_INVALID_ARG;
-}
-int encode_bf16_3d(CUtensorMap* map, const void* ptr, int D, int S, long long outer, int box_rows) {
-    return encode_3d(map, ptr, 2, D, S, outer, box_rows);
 }
 
 bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
@@ -186,6 +197,31 @@ int launch_ws(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& t
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
+// The persistent kernel's instantiation for the features a call uses: block
+// mask (M), dropout (DR, bf16 only) and keep bits (E).
+template <int D, bool F>
+int launch_any(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
+               int sm, cudaStream_t st, bool m, bool dr, bool e) {
+    if constexpr (F) {
+        if (dr) return ATTN_ERR_UNSUPPORTED;
+        if (m) return e ? launch_ws<D, F, true, false, true>(tq, tk, tv, p, sm, st)
+                        : launch_ws<D, F, true, false, false>(tq, tk, tv, p, sm, st);
+        return e ? launch_ws<D, F, false, false, true>(tq, tk, tv, p, sm, st)
+                 : launch_ws<D, F, false, false, false>(tq, tk, tv, p, sm, st);
+    } else {
+        if (m) {
+            if (dr) return e ? launch_ws<D, F, true, true, true>(tq, tk, tv, p, sm, st)
+                             : launch_ws<D, F, true, true, false>(tq, tk, tv, p, sm, st);
+            return e ? launch_ws<D, F, true, false, true>(tq, tk, tv, p, sm, st)
+                     : launch_ws<D, F, true, false, false>(tq, tk, tv, p, sm, st);
+        }
+        if (dr) return e ? launch_ws<D, F, false, true, true>(tq, tk, tv, p, sm, st)
+                         : launch_ws<D, F, false, true, false>(tq, tk, tv, p, sm, st);
+        return e ? launch_ws<D, F, false, false, true>(tq, tk, tv, p, sm, st)
+                 : launch_ws<D, F, false, false, false>(tq, tk, tv, p, sm, st);
+    }
+}
+
 // Kernel choice: the warp-specialised persistent kernel unless the environment
 // variable ATTN_FWD_KERNEL=simple selects the one-tile-per-CTA kernel (kept as
 // an independently scheduled implementation for cross-checks).
@@ -219,7 +255,8 @@ namespace {
 int fwd_bf16(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
              int Hkv, int S, int D, float scale, int causal, const uint8_t* block_mask,
              int mask_heads, int dropout_p8, unsigned long long seed, unsigned long long offset,
-             void* stream, const uint8_t* keep_bits = nullptr, int keep_heads = 1);
+             void* stream, const uint8_t* keep_bits = nullptr, int keep_heads = 1,
+             const float* descales = nullptr);
 }  // namespace
 }  // namespace attn
 
@@ -266,9 +303,17 @@ namespace {
 int fwd_bf16(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
              int Hkv, int S, int D, float scale, int causal, const uint8_t* block_mask,
              int mask_heads, int dropout_p8, unsigned long long seed, unsigned long long offset,
-             void* stream, const uint8_t* keep_bits, int keep_heads) {
-    int rc = check_args(q, k, v, out, lse, B, Hq, Hkv, S, D, scale);
+             void* stream, const uint8_t* keep_bits, int keep_heads, const float* descales) {
+    // descales != nullptr: E4M3 inputs (one byte per element, D = 128) with
+    // per-tensor descales {q, k, v}.
+    const bool fp8 = descales != nullptr;
+    int rc = check_args(q, k, v, out, lse, B, Hq, Hkv, S, D, scale, fp8 ? 1 : 2);
     if (rc != ATTN_OK) return rc;
+    if (fp8) {
+        for (int i = 0; i < 3; ++i)
+            if (!std::isfinite(descales[i]) || !(descales[i] > 0.f)) return ATTN_ERR_INVALID_ARG;
+        if (D != 128 || dropout_p8 > 0) return ATTN_ERR_UNSUPPORTED;
+    }
     const size_t nt = (size_t)((S + kTile - 1) / kTile);
     if (check_mask_overlap(block_mask, (size_t)mask_heads * nt * nt, out, lse, B, Hq, S, D) != ATTN_OK ||
         check_mask_overlap(keep_bits, (size_t)keep_heads * S * 16 * nt, out, lse, B, Hq, S, D) != ATTN_OK)
@@ -278,9 +323,10 @@ int fwd_bf16(const void* q, const void* k, const void* v, void* out, float* lse,
     if (rc != ATTN_OK) return rc;
 
     alignas(64) CUtensorMap tq, tk, tv;
-    if (encode_bf16_3d(&tq, q, D, S, (long long)B * Hq, kTile) != ATTN_OK ||
-        encode_bf16_3d(&tk, k, D, S, (long long)B * Hkv, kTile) != ATTN_OK ||
-        encode_bf16_3d(&tv, v, D, S, (long long)B * Hkv, kTile) != ATTN_OK)
+    const int eb = fp8 ? 1 : 2;
+    if (encode_3d(&tq, q, eb, D, S, (long long)B * Hq, kTile) != ATTN_OK ||
+        encode_3d(&tk, k, eb, D, S, (long long)B * Hkv, kTile) != ATTN_OK ||
+        encode_3d(&tv, v, eb, D, S, (long long)B * Hkv, kTile) != ATTN_OK)
         return ATTN_ERR_INVALID_ARG;
 
     FwdParams p{};
@@ -303,31 +349,27 @@ int fwd_bf16(const void* q, const void* k, const void* v, void* out, float* lse,
     p.keep_bits = keep_bits;
     p.keep_heads = keep_heads;
     p.keep_row_bytes = 16 * p.num_q_tiles;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (fp8) {
+        // Scores come out of the tensor core in code units: the Q and K descales
+        // join the softmax scale, the V descale scales O at the end.
+        p.scale_log2 = scale * descales[0] * descales[1] * kLog2e;
+        p.o_scale = descales[2];
+    }
     if (dropout_p8 > 0) {
         // Kept weights are scaled by 256 / (256 - p8) along with 1 / l.
         p.dropout_p8 = dropout_p8;
         p.dropout_seed = seed;
         p.dropout_offset = offset;
         p.o_scale = 256.f / (float)(256 - dropout_p8);
-        return D == 64 ? launch_ws<64, false, false, true>(tq, tk, tv, p, dev->sm_count, st)
-                       : launch_ws<128, false, false, true>(tq, tk, tv, p, dev->sm_count, st);
     }
-    if (keep_bits != nullptr) {
-        if (block_mask != nullptr)
-            return D == 64 ? launch_ws<64, false, true, false, true>(tq, tk, tv, p, dev->sm_count, st)
-                           : launch_ws<128, false, true, false, true>(tq, tk, tv, p, dev->sm_count, st);
-        return D == 64 ? launch_ws<64, false, false, false, true>(tq, tk, tv, p, dev->sm_count, st)
-                       : launch_ws<128, false, false, false, true>(tq, tk, tv, p, dev->sm_count, st);
-    }
-    // Block masks are handled by the persistent kernel only.
-    if (block_mask == nullptr && use_simple_kernel())
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const bool m = block_mask != nullptr, dr = dropout_p8 > 0, e = keep_bits != nullptr;
+    if (fp8) return launch_any<128, true>(tq, tk, tv, p, dev->sm_count, st, m, false, e);
+    // The one-tile-per-CTA cross-check kernel covers the plain forward only.
+    if (!m && !dr && !e && use_simple_kernel())
         return D == 64 ? launch_simple<64>(tq, tk, tv, p, st) : launch_simple<128>(tq, tk, tv, p, st);
-    if (block_mask != nullptr)
-        return D == 64 ? launch_ws<64, false, true>(tq, tk, tv, p, dev->sm_count, st)
-                       : launch_ws<128, false, true>(tq, tk, tv, p, dev->sm_count, st);
-    return D == 64 ? launch_ws<64, false, false>(tq, tk, tv, p, dev->sm_count, st)
-                   : launch_ws<128, false, false>(tq, tk, tv, p, dev->sm_count, st);
+    return D == 64 ? launch_any<64, false>(tq, tk, tv, p, dev->sm_count, st, m, dr, e)
+                   : launch_any<128, false>(tq, tk, tv, p, dev->sm_count, st, m, dr, e);
 }
 }  // namespace
 }  // namespace attn
@@ -335,39 +377,34 @@ int fwd_bf16(const void* q, const void* k, const void* v, void* out, float* lse,
 extern "C" int attn_fwd_fp8(const void* q, const void* k, const void* v, float q_descale,
                             float k_descale, float v_descale, void* out, float* lse, int B, int Hq,
                             int Hkv, int S, int D, float scale, int causal, void* stream) {
-    int rc = check_args(q, k, v, out, lse, B, Hq, Hkv, S, D, scale, 1);
-    if (rc != ATTN_OK) return rc;
-    for (float d : {q_descale, k_descale, v_descale})
-        if (!std::isfinite(d) || !(d > 0.f)) return ATTN_ERR_INVALID_ARG;
-    if (D != 128) return ATTN_ERR_UNSUPPORTED;
-    DeviceState* dev = nullptr;
-    rc = current_device_state(&dev);
-    if (rc != ATTN_OK) return rc;
+    const float ds[3] = {q_descale, k_descale, v_descale};
+    return attn::fwd_bf16(q, k, v, out, lse, B, Hq, Hkv, S, D, scale, causal, nullptr, 1, 0, 0, 0, stream,
+                          nullptr, 1, ds);
+}
 
-    alignas(64) CUtensorMap tq, tk, tv;
-    if (encode_3d(&tq, q, 1, D, S, (long long)B * Hq, kTile) != ATTN_OK ||
-        encode_3d(&tk, k, 1, D, S, (long long)B * Hkv, kTile) != ATTN_OK ||
-        encode_3d(&tv, v, 1, D, S, (long long)B * Hkv, kTile) != ATTN_OK)
+extern "C" int attn_fwd_ex(const void* q, const void* k, const void* v, void* out, float* lse, int B,
+                           int Hq, int Hkv, int S, int D, float scale, int causal,
+                           const attn_options_t* opts, void* stream) {
+    if (opts == nullptr)
+        return attn::fwd_bf16(q, k, v, out, lse, B, Hq, Hkv, S, D, scale, causal, nullptr, 1, 0, 0, 0,
+                              stream);
+    if (opts->input_format != ATTN_INPUT_BF16 && opts->input_format != ATTN_INPUT_E4M3)
         return ATTN_ERR_INVALID_ARG;
-
-    FwdParams p{};
-    std::memset(&p, 0, sizeof p);
-    p.B = B;
-    p.Hq = Hq;
-    p.Hkv = Hkv;
-    p.S = S;
-    p.group = Hq / Hkv;
-    p.num_q_tiles = (S + kTile - 1) / kTile;
-    p.causal = causal ? 1 : 0;
-    // Scores come out of the tensor core in code units: the Q and K descales
-    // join the softmax scale, the V descale scales O at the end.
-    p.scale_log2 = scale * q_descale * k_descale * kLog2e;
-    p.o_scale = v_descale;
-    p.out = static_cast<__nv_bfloat16*>(out);
-    p.lse = lse;
-    p.status = dev->status_word;
-    p.wait_limit_ns = kWaitLimitNs;
-    return launch_ws<128, true, false>(tq, tk, tv, p, dev->sm_count, static_cast<cudaStream_t>(stream));
+    if (opts->block_mask != nullptr && opts->mask_heads != 1 && opts->mask_heads != Hq)
+        return ATTN_ERR_INVALID_ARG;
+    if (opts->keep_bits != nullptr) {
+        if (opts->keep_heads != 1 && opts->keep_heads != Hq) return ATTN_ERR_INVALID_ARG;
+        if (reinterpret_cast<uintptr_t>(opts->keep_bits) & 15u) return ATTN_ERR_MISALIGNED;
+    }
+    if (!std::isfinite(opts->dropout_p) || opts->dropout_p < 0.f) return ATTN_ERR_INVALID_ARG;
+    const long p8 = std::lrint((double)opts->dropout_p * 256.0);
+    if (p8 > 255) return ATTN_ERR_INVALID_ARG;
+    const float ds[3] = {opts->q_descale, opts->k_descale, opts->v_descale};
+    return attn::fwd_bf16(q, k, v, out, lse, B, Hq, Hkv, S, D, scale, causal, opts->block_mask,
+                          opts->block_mask != nullptr ? opts->mask_heads : 1, (int)p8, opts->seed,
+                          opts->offset, stream, opts->keep_bits,
+                          opts->keep_bits != nullptr ? opts->keep_heads : 1,
+                          opts->input_format == ATTN_INPUT_E4M3 ? ds : nullptr);
 }
 
 extern "C" int attn_sync_status(void* stream) {
@@ -424,12 +461,12 @@ int current_device(int* sm_count, unsigned int** status_word) {
 }
 
 int encode_bf16_tiles(CUtensorMap* map, const void* ptr, int D, int S, long long outer) {
-    return encode_bf16_3d(map, ptr, D, S, outer, kTile);
+    return encode_3d(map, ptr, 2, D, S, outer, kTile);
 }
 
 int encode_bf16_box(CUtensorMap* map, const void* ptr, int D, int S, long long outer, int box_rows) {
     if (box_rows < 1 || box_rows > 256) return ATTN_ERR_INVALID_ARG;
-    return encode_bf16_3d(map, ptr, D, S, outer, box_rows);
+    return encode_3d(map, ptr, 2, D, S, outer, box_rows);
 }
 
 bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {

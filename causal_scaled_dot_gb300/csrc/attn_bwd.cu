@@ -43,7 +43,8 @@ int setup_bwd_kernels() {
             allow_all<64, true, false>() && allow_all<128, true, false>() &&
             allow_all<64, false, true>() && allow_all<128, false, true>() &&
             allow_all<64, true, true>() && allow_all<128, true, true>() &&
-            allow_all<64, false, false, true>() && allow_all<128, false, false, true>();
+            allow_all<64, false, false, true>() && allow_all<128, false, false, true>() &&
+            allow_all<64, true, false, true>() && allow_all<128, true, false, true>();
         g_bwd_ready[dev] = ok ? 1 : ATTN_ERR_DEVICE;
     }
     return g_bwd_ready[dev] == 1 ? ATTN_OK : g_bwd_ready[dev];
@@ -140,6 +141,30 @@ extern "C" int attn_bwd_elem_masked(const void* q, const void* k, const void* v,
                      block_mask, block_mask != nullptr ? mask_heads : 1, stream, keep_bits, keep_heads);
 }
 
+extern "C" int attn_bwd_ex(const void* q, const void* k, const void* v, const void* out,
+                           const void* dout, const float* lse, float* delta, void* dq, void* dk,
+                           void* dv, int B, int Hq, int Hkv, int S, int D, float scale, int causal,
+                           const attn_options_t* opts, void* stream) {
+    if (opts == nullptr)
+        return attn::bwd(q, k, v, out, dout, lse, delta, dq, dk, dv, B, Hq, Hkv, S, D, scale, causal,
+                         nullptr, 1, stream);
+    if (opts->input_format != ATTN_INPUT_BF16) return ATTN_ERR_UNSUPPORTED;
+    if (opts->block_mask != nullptr && opts->mask_heads != 1 && opts->mask_heads != Hq)
+        return ATTN_ERR_INVALID_ARG;
+    if (opts->keep_bits != nullptr) {
+        if (opts->keep_heads != 1 && opts->keep_heads != Hq) return ATTN_ERR_INVALID_ARG;
+        if (reinterpret_cast<uintptr_t>(opts->keep_bits) & 15u) return ATTN_ERR_MISALIGNED;
+    }
+    if (!std::isfinite(opts->dropout_p) || opts->dropout_p < 0.f) return ATTN_ERR_INVALID_ARG;
+    const long p8 = std::lrint((double)opts->dropout_p * 256.0);
+    if (p8 > 255) return ATTN_ERR_INVALID_ARG;
+    if (p8 > 0 && opts->keep_bits != nullptr) return ATTN_ERR_UNSUPPORTED;
+    return attn::bwd(q, k, v, out, dout, lse, delta, dq, dk, dv, B, Hq, Hkv, S, D, scale, causal,
+                     opts->block_mask, opts->block_mask != nullptr ? opts->mask_heads : 1, stream,
+                     opts->keep_bits, opts->keep_bits != nullptr ? opts->keep_heads : 1, (int)p8,
+                     opts->seed, opts->offset);
+}
+
 extern "C" int attn_bwd_dropout(const void* q, const void* k, const void* v, const void* out,
                                 const void* dout, const float* lse, float* delta, void* dq, void* dk,
                                 void* dv, int B, int Hq, int Hkv, int S, int D, float scale,
@@ -218,10 +243,15 @@ int bwd(const void* q, const void* k, const void* v, const void* out, const void
     p.dropout_offset = offset;
     p.keep_scale = dropout_p8 > 0 ? 256.f / (float)(256 - dropout_p8) : 1.f;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (dropout_p8 > 0)
+    const bool m = block_mask != nullptr, e = keep_bits != nullptr;
+    if (dropout_p8 > 0) {
+        if (e) return ATTN_ERR_UNSUPPORTED;  // the dK/dV stage holds one bit set per tile
+        if (m)
+            return D == 64 ? launch_bwd<64, true, false, true>(tq, tdo, tk, tv, p, sm_count, st)
+                           : launch_bwd<128, true, false, true>(tq, tdo, tk, tv, p, sm_count, st);
         return D == 64 ? launch_bwd<64, false, false, true>(tq, tdo, tk, tv, p, sm_count, st)
                        : launch_bwd<128, false, false, true>(tq, tdo, tk, tv, p, sm_count, st);
-    const bool m = block_mask != nullptr, e = keep_bits != nullptr;
+    }
     if (D == 64)
         return m ? (e ? launch_bwd<64, true, true>(tq, tdo, tk, tv, p, sm_count, st)
                       : launch_bwd<64, true, false>(tq, tdo, tk, tv, p, sm_count, st))

@@ -63,6 +63,12 @@ def load() -> ctypes.CDLL:
         lib.attn_bwd_dropout.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf,
                                          ci, cf, ctypes.c_ulonglong, ctypes.c_ulonglong, vp]
         lib.attn_bwd_dropout.restype = ci
+        opts_p = ctypes.POINTER(AttnOptions)
+        lib.attn_fwd_ex.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, ci, opts_p, vp]
+        lib.attn_fwd_ex.restype = ci
+        lib.attn_bwd_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, ci,
+                                    opts_p, vp]
+        lib.attn_bwd_ex.restype = ci
         u64 = ctypes.c_ulonglong
         lib.attn_fwd_dropout.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, ci, cf, u64, u64,
                                          vp]
@@ -85,6 +91,38 @@ def load() -> ctypes.CDLL:
 
 def library_path() -> str:
     return _build.LIBRARY
+
+
+class AttnOptions(ctypes.Structure):
+    """The C struct attn_options_t (include/attn.h), field for field."""
+    _fields_ = [("input_format", ctypes.c_int), ("q_descale", ctypes.c_float),
+                ("k_descale", ctypes.c_float), ("v_descale", ctypes.c_float),
+                ("block_mask", ctypes.c_void_p), ("mask_heads", ctypes.c_int),
+                ("keep_bits", ctypes.c_void_p), ("keep_heads", ctypes.c_int),
+                ("dropout_p", ctypes.c_float), ("seed", ctypes.c_ulonglong),
+                ("offset", ctypes.c_ulonglong)]
+
+
+ATTN_INPUT_BF16, ATTN_INPUT_E4M3 = 0, 1
+
+
+def options(e4m3_descales=None, block_mask=None, keep_bits=None, dropout_p: float = 0.0, seed: int = 0,
+            offset: int = 0) -> AttnOptions:
+    """An attn_options_t: E4M3 inputs when ``e4m3_descales`` = (q, k, v) is given; masks
+    as CUDA uint8 tensors (their first dimension gives mask_heads / keep_heads).  The
+    structure keeps only the masks' addresses: the tensors must stay alive until the
+    calls that use it have run."""
+    o = AttnOptions()
+    o.input_format = ATTN_INPUT_E4M3 if e4m3_descales is not None else ATTN_INPUT_BF16
+    o.q_descale, o.k_descale, o.v_descale = e4m3_descales if e4m3_descales is not None else (1.0, 1.0, 1.0)
+    o.block_mask = _ptr(block_mask)
+    o.mask_heads = 1 if block_mask is None else int(block_mask.shape[0])
+    o.keep_bits = _ptr(keep_bits)
+    o.keep_heads = 1 if keep_bits is None else int(keep_bits.shape[0])
+    o.dropout_p = float(dropout_p)
+    o.seed = int(seed) & (2**64 - 1)
+    o.offset = int(offset) & (2**64 - 1)
+    return o
 
 
 def _ptr(x):
@@ -235,6 +273,30 @@ def attn_bwd_dropout(q, k, v, out, dout, lse, delta, dq, dk, dv, B: int, Hq: int
     return rc
 
 
+def attn_fwd_ex(q, k, v, out, lse, B: int, Hq: int, Hkv: int, S: int, D: int, scale: float,
+                causal: bool | int, opts: AttnOptions | None, stream=None, check: bool = True) -> int:
+    """The C entry point ``attn_fwd_ex`` (``opts`` from ``options``, or None)."""
+    rc = load().attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), int(B), int(Hq), int(Hkv),
+                            int(S), int(D), float(scale), 1 if causal else 0,
+                            None if opts is None else ctypes.byref(opts), _stream(stream))
+    if check and rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_ex")
+    return rc
+
+
+def attn_bwd_ex(q, k, v, out, dout, lse, delta, dq, dk, dv, B: int, Hq: int, Hkv: int, S: int, D: int,
+                scale: float, causal: bool | int, opts: AttnOptions | None, stream=None,
+                check: bool = True) -> int:
+    """The C entry point ``attn_bwd_ex`` (``opts`` as given to ``attn_fwd_ex``)."""
+    rc = load().attn_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(delta),
+                            _ptr(dq), _ptr(dk), _ptr(dv), int(B), int(Hq), int(Hkv), int(S), int(D),
+                            float(scale), 1 if causal else 0, None if opts is None else ctypes.byref(opts),
+                            _stream(stream))
+    if check and rc != ATTN_OK:
+        raise AttnError(rc, "attn_bwd_ex")
+    return rc
+
+
 def attn_fwd_fp8(q, k, v, q_descale: float, k_descale: float, v_descale: float, out, lse, B: int,
                  Hq: int, Hkv: int, S: int, D: int, scale: float, causal: bool | int, stream=None,
                  check: bool = True) -> int:
@@ -310,16 +372,9 @@ def _attention_function():
             Hkv = k.shape[1]
             out = torch.empty_like(q)
             lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
-            hm = 1 if block_mask is None else block_mask.shape[0]
-            if dropout_p > 0.0:
-                attn_fwd_dropout(q, k, v, out, lse, B, Hq, Hkv, S, D, scale, causal, dropout_p, seed, offset)
-            elif keep_bits is not None:
-                attn_fwd_elem_masked(q, k, v, out, lse, B, Hq, Hkv, S, D, scale, causal, keep_bits,
-                                     keep_bits.shape[0], block_mask, hm)
-            elif block_mask is not None:
-                attn_fwd_block_masked(q, k, v, out, lse, B, Hq, Hkv, S, D, scale, causal, block_mask, hm)
-            else:
-                attn_fwd(q, k, v, out, lse, B, Hq, Hkv, S, D, scale, causal)
+            opts = options(block_mask=block_mask, keep_bits=keep_bits, dropout_p=dropout_p, seed=seed,
+                           offset=offset)
+            attn_fwd_ex(q, k, v, out, lse, B, Hq, Hkv, S, D, scale, causal, opts)
             ctx.save_for_backward(q, k, v, out, lse)
             ctx.masks = (block_mask, keep_bits)
             ctx.args = (causal, scale, dropout_p, seed, offset)
@@ -335,18 +390,9 @@ def _attention_function():
             dout = dout.contiguous()
             dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
             delta = torch.empty_like(lse)
-            hm = 1 if block_mask is None else block_mask.shape[0]
-            if dropout_p > 0.0:
-                attn_bwd_dropout(q, k, v, out, dout, lse, delta, dq, dk, dv, B, Hq, Hkv, S, D, scale, causal,
-                                 dropout_p, seed, offset)
-            elif keep_bits is not None:
-                attn_bwd_elem_masked(q, k, v, out, dout, lse, delta, dq, dk, dv, B, Hq, Hkv, S, D, scale,
-                                     causal, keep_bits, keep_bits.shape[0], block_mask, hm)
-            elif block_mask is not None:
-                attn_bwd_block_masked(q, k, v, out, dout, lse, delta, dq, dk, dv, B, Hq, Hkv, S, D, scale,
-                                      causal, block_mask, hm)
-            else:
-                attn_bwd(q, k, v, out, dout, lse, delta, dq, dk, dv, B, Hq, Hkv, S, D, scale, causal)
+            opts = options(block_mask=block_mask, keep_bits=keep_bits, dropout_p=dropout_p, seed=seed,
+                           offset=offset)
+            attn_bwd_ex(q, k, v, out, dout, lse, delta, dq, dk, dv, B, Hq, Hkv, S, D, scale, causal, opts)
             return dq, dk, dv, None, None, None, None, None, None, None
 
     return AttentionFunction
@@ -358,14 +404,14 @@ _ATTENTION_FUNCTION = None
 def attention_trainable(q, k, v, causal: bool = True, scale: float | None = None, block_mask=None,
                         keep_bits=None, dropout_p: float = 0.0, seed: int = 0, offset: int = 0):
     """O = attention(q, k, v) with gradients: forward and backward run the C ABI
-    (attn_fwd / attn_bwd, or their block-masked, element-masked or dropout
-    forms).  q [B,Hq,S,D], k/v [B,Hkv,S,D] bf16 CUDA tensors; block_mask uint8
-    [1 or Hq, nt, nt]; keep_bits uint8 [1 or Hq, S, 16*nt] (may come with a
-    block mask); dropout takes no mask."""
+    (attn_fwd_ex / attn_bwd_ex with the given options).  q [B,Hq,S,D], k/v
+    [B,Hkv,S,D] bf16 CUDA tensors; block_mask uint8 [1 or Hq, nt, nt]; keep_bits
+    uint8 [1 or Hq, S, 16*nt]; dropout combines with a block mask (keep bits with
+    dropout have no backward)."""
     global _ATTENTION_FUNCTION
     import torch
-    if dropout_p > 0.0 and (block_mask is not None or keep_bits is not None):
-        raise ValueError("dropout with a mask is not supported")
+    if dropout_p > 0.0 and keep_bits is not None:
+        raise ValueError("keep bits with dropout have no backward")
     for name, t in (("q", q), ("k", k), ("v", v)):
         if t.dtype != torch.bfloat16 or not t.is_cuda or t.dim() != 4 or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous bf16 CUDA [B,H,S,D] tensor")

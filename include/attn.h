@@ -4,8 +4,9 @@
  *
  * Entry points: the forward (attn_fwd; FP8 inputs attn_fwd_fp8; block masks
  * attn_fwd_block_masked; per-pair keep bits attn_fwd_elem_masked; dropout of
- * the weights attn_fwd_dropout), the matching gradients (attn_bwd,
- * attn_bwd_block_masked, attn_bwd_elem_masked, attn_bwd_dropout), the output
+ * the weights attn_fwd_dropout; their combinations attn_fwd_ex), the matching
+ * gradients (attn_bwd, attn_bwd_block_masked, attn_bwd_elem_masked,
+ * attn_bwd_dropout, attn_bwd_ex), the output
  * projection of the attention output (attn_out_proj), and status helpers
  * (attn_sync_status, attn_selftest_wait_timeout, attn_status_string,
  * attn_version).
@@ -48,6 +49,32 @@ typedef enum {
     ATTN_ERR_LAUNCH = 5,      /* the kernel launch itself failed */
     ATTN_ERR_TIMEOUT = 6      /* a device-side wait ran past its limit (read by attn_sync_status) */
 } attn_status_t;
+
+/* Input formats of attn_options_t. */
+enum { ATTN_INPUT_BF16 = 0, ATTN_INPUT_E4M3 = 1 };
+
+/*
+ * attn_options_t -- the optional features of attn_fwd_ex / attn_bwd_ex, each
+ * as documented for its own entry point, combinable in one call:
+ *   input_format      ATTN_INPUT_BF16, or ATTN_INPUT_E4M3 (attn_fwd_fp8's codes
+ *                     with q_descale, k_descale, v_descale; forward only).
+ *   block_mask, mask_heads   as attn_fwd_block_masked (NULL: none).
+ *   keep_bits, keep_heads    as attn_fwd_elem_masked (NULL: none).
+ *   dropout_p, seed, offset  as attn_fwd_dropout (dropout_p = 0: none).
+ * Supported together: forward, any of the masks with dropout (bf16) and any of
+ * the masks with E4M3 inputs; backward (bf16), any of the masks, or dropout
+ * with a block mask.  Other combinations return ATTN_ERR_UNSUPPORTED.
+ */
+typedef struct {
+    int input_format;
+    float q_descale, k_descale, v_descale;
+    const unsigned char *block_mask;
+    int mask_heads;
+    const unsigned char *keep_bits;
+    int keep_heads;
+    float dropout_p;
+    unsigned long long seed, offset;
+} attn_options_t;
 
 /*
  * attn_fwd -- O = softmax(mask(Q K^T * scale)) V  and  LSE, on the GPU.
@@ -181,6 +208,14 @@ int attn_fwd_elem_masked(const void *q, const void *k, const void *v, void *out,
                          const unsigned char *block_mask, int mask_heads, void *stream);
 
 /*
+ * attn_fwd_ex -- attn_fwd with the options above (opts NULL: attn_fwd).
+ * Errors as the entry points of the features used.
+ */
+int attn_fwd_ex(const void *q, const void *k, const void *v, void *out, float *lse, int B, int Hq,
+                int Hkv, int S, int D, float scale, int causal, const attn_options_t *opts,
+                void *stream);
+
+/*
  * attn_bwd -- gradients of attn_fwd's output: dQ, dK, dV for an upstream
  * gradient dO.  The pages give no formula (the ai-manual.ru article, section 6,
  * only warns that the fused backward pass is hard to get right); this is the
@@ -252,6 +287,15 @@ int attn_bwd_dropout(const void *q, const void *k, const void *v, const void *ou
                      const void *dout, const float *lse, float *delta, void *dq, void *dk, void *dv,
                      int B, int Hq, int Hkv, int S, int D, float scale, int causal, float dropout_p,
                      unsigned long long seed, unsigned long long offset, void *stream);
+
+/*
+ * attn_bwd_ex -- the gradients of attn_fwd_ex's output for the same options
+ * (bf16 inputs; opts NULL: attn_bwd).  Keep bits with dropout is not
+ * supported (ATTN_ERR_UNSUPPORTED).
+ */
+int attn_bwd_ex(const void *q, const void *k, const void *v, const void *out, const void *dout,
+                const float *lse, float *delta, void *dq, void *dk, void *dv, int B, int Hq, int Hkv,
+                int S, int D, float scale, int causal, const attn_options_t *opts, void *stream);
 
 /*
  * attn_out_proj -- the layer's output projection applied to attention's

@@ -130,7 +130,7 @@ def run_gpu_masked(q_bits, k_bits, v_bits, scale, causal, block_mask, stream=Non
     return out.double().cpu().numpy(), lse.double().cpu().numpy()
 
 
-def compare_masked(o_gpu, o_ref, l_gpu, l_ref, label=""):
+def compare_masked(o_gpu, o_ref, l_gpu, l_ref, label="", abs_scale=1.0):
     """The bf16 parity bar on rows that see at least one key; rows that see none
     must hold exactly O = 0 and LSE = -inf on both sides."""
     D = o_ref.shape[-1]
@@ -143,7 +143,7 @@ def compare_masked(o_gpu, o_ref, l_gpu, l_ref, label=""):
     live = ~empty
     stats = {"empty_rows": int(empty.sum())}
     if live.any():
-        stats.update(compare(o_gpu[live], o_ref[live], l_gpu[live], l_ref[live], label))
+        stats.update(compare(o_gpu[live], o_ref[live], l_gpu[live], l_ref[live], label, abs_scale))
     return stats
 
 

@@ -211,6 +211,44 @@ def test_masks_overlapping_outputs_are_rejected_before_launch():
     assert lib.attn_bwd_block_masked(*bargs, (7 << 40) + 64, 1, None) == ATTN_ERR_INVALID_ARG
 
 
+def test_options_struct_layout_matches_the_header(tmp_path):
+    """attn_options_t as gcc lays it out from include/attn.h equals the binding's ctypes
+    structure, field by field."""
+    fields = [f for f, _ in native.AttnOptions._fields_]
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "attn.h"\nint main(void) {\n'
+                   '  printf("%zu\\n", sizeof(attn_options_t));\n'
+                   + "".join(f'  printf("%zu\\n", offsetof(attn_options_t, {f}));\n' for f in fields)
+                   + "  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), "-o", str(exe), str(src)], check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    want = [ctypes.sizeof(native.AttnOptions)] + [getattr(native.AttnOptions, f).offset for f in fields]
+    assert got == want
+
+
+def test_unsupported_option_combinations_are_rejected_before_launch():
+    lib = native.load()
+    q, k, v, out = 1 << 40, 2 << 40, 3 << 40, 4 << 40
+    f = ctypes.c_float(0.1)
+    fp8_drop = native.options(e4m3_descales=(1.0, 1.0, 1.0), dropout_p=0.1)
+    assert lib.attn_fwd_ex(q, k, v, out, None, 1, 2, 2, 300, 128, f, 1, ctypes.byref(fp8_drop),
+                           None) == ATTN_ERR_UNSUPPORTED
+    fp8_d64 = native.options(e4m3_descales=(1.0, 1.0, 1.0))
+    assert lib.attn_fwd_ex(q, k, v, out, None, 1, 2, 2, 300, 64, f, 1, ctypes.byref(fp8_d64),
+                           None) == ATTN_ERR_UNSUPPORTED
+    bad_fmt = native.options()
+    bad_fmt.input_format = 7
+    assert lib.attn_fwd_ex(q, k, v, out, None, 1, 2, 2, 300, 128, f, 1, ctypes.byref(bad_fmt),
+                           None) == ATTN_ERR_INVALID_ARG
+    bargs = [q, k, v, out, 6 << 40, 5 << 40, 7 << 40, 8 << 40, 9 << 40, 10 << 40, 1, 2, 2, 300, 128, f, 1]
+    keep_drop = native.options(keep_bits=None, dropout_p=0.1)
+    keep_drop.keep_bits = 11 << 40
+    keep_drop.keep_heads = 1
+    assert lib.attn_bwd_ex(*bargs, ctypes.byref(keep_drop), None) == ATTN_ERR_UNSUPPORTED
+    assert lib.attn_bwd_ex(*bargs, ctypes.byref(fp8_d64), None) == ATTN_ERR_UNSUPPORTED
+
+
 def test_keep_bit_packing():
     from causal_scaled_dot_gb300.inputs import (block_mask_of_keep_bits, keep_row_bytes, pack_keep_bits,
                                                 random_keep_bits, unpack_keep_bits, window_keep_bits)

@@ -49,3 +49,50 @@ def test_autograd_matches_direct_backward(variant):
     assert np.array_equal(o.detach().double().cpu().numpy(), want[0])
     for g, w_ in zip(got, want[2:5]):
         assert np.array_equal(g, w_)
+
+
+def test_entry_points_from_a_thread_with_no_cuda_call():
+    """A thread that has made no CUDA call has no driver context bound (the
+    autograd engine's worker is one); the forward and backward entry points
+    called from such a thread give the same bits as from the main thread."""
+    import threading
+
+    import torch
+    from causal_scaled_dot_gb300 import native
+    B, Hq, Hkv, S, D = 1, 2, 1, 200, 64
+    q, k, v = (to_device(x) for x in qkv_bf16(B, Hq, Hkv, S, D, seed=9200))
+    do = to_device(gaussian_bf16((B, Hq, S, D), 9200, 3))
+    scale = 1.0 / math.sqrt(D)
+
+    def buffers():
+        lse = torch.empty((B, Hq, S), device=q.device, dtype=torch.float32)
+        return (torch.empty_like(q), lse, torch.empty_like(lse), torch.empty_like(q),
+                torch.empty_like(k), torch.empty_like(v))
+
+    def run(bufs, stream):
+        o, lse, delta, dq, dk, dv = bufs
+        native.attn_fwd(q, k, v, o, lse, B, Hq, Hkv, S, D, scale, True, stream=stream)
+        native.attn_bwd(q, k, v, o, do, lse, delta, dq, dk, dv, B, Hq, Hkv, S, D, scale, True,
+                        stream=stream)
+
+    side = torch.cuda.Stream()
+    handle = side.cuda_stream  # an int: the thread itself touches no torch CUDA state
+    in_thread, in_main = buffers(), buffers()
+    torch.cuda.synchronize()
+    errors = []
+
+    def worker():
+        try:
+            run(in_thread, handle)
+        except Exception as e:  # re-raised in the main thread below
+            errors.append(e)
+
+    t = threading.Thread(target=worker)
+    t.start()
+    t.join()
+    side.synchronize()
+    assert not errors, errors
+    run(in_main, handle)
+    side.synchronize()
+    for a, b in zip(in_thread, in_main):
+        assert torch.equal(a, b)
