@@ -30,7 +30,10 @@
  *
  * Threading: every entry point may be called from any host thread.  The only
  * internal state is a cache of TMA descriptors and of per-device properties,
- * guarded by a mutex.
+ * guarded by a mutex.  The work runs on the calling thread's current device
+ * (cudaGetDevice), which must hold every buffer; its primary context is
+ * bound to the thread on entry, so a thread that has made no CUDA call yet
+ * (an autograd engine's worker, say) can call too.
  */
 #ifndef LIBATTN_ATTN_H_
 #define LIBATTN_ATTN_H_
