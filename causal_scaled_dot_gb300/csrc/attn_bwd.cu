@@ -26,10 +26,19 @@ cudaError_t allow_smem(K kernel, uint32_t bytes) {
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
-template <int D, bool M, bool E, bool DR = false>
+template <int D, bool M, bool E, bool DR>
 bool allow_all() {
     return allow_smem(attn_bwd_dq_kernel<D, M, E, DR>, DqLayout<D>::kDynamicSmem) == cudaSuccess &&
-           allow_smem(attn_bwd_dkdv_kernel<D, M, E, DR>, DkvLayout<D>::kDynamicSmem) == cudaSuccess;
+           allow_smem(attn_bwd_dkdv_kernel<D, M, E, DR>, DkvLayout<D, E && DR>::kDynamicSmem) == cudaSuccess;
+}
+
+// Every combination of block mask (M), keep bits (E) and dropout (DR).
+template <int D>
+bool allow_variants() {
+    return allow_all<D, false, false, false>() && allow_all<D, true, false, false>() &&
+           allow_all<D, false, true, false>() && allow_all<D, true, true, false>() &&
+           allow_all<D, false, false, true>() && allow_all<D, true, false, true>() &&
+           allow_all<D, false, true, true>() && allow_all<D, true, true, true>();
 }
 
 // Shared-memory opt-in of the backward kernels, once per device.
@@ -39,12 +48,7 @@ int setup_bwd_kernels() {
     std::lock_guard<std::mutex> lock(g_bwd_mutex);
     if (g_bwd_ready[dev] == 0) {
         const bool ok =
-            allow_all<64, false, false>() && allow_all<128, false, false>() &&
-            allow_all<64, true, false>() && allow_all<128, true, false>() &&
-            allow_all<64, false, true>() && allow_all<128, false, true>() &&
-            allow_all<64, true, true>() && allow_all<128, true, true>() &&
-            allow_all<64, false, false, true>() && allow_all<128, false, false, true>() &&
-            allow_all<64, true, false, true>() && allow_all<128, true, false, true>();
+            allow_variants<64>() && allow_variants<128>();
         g_bwd_ready[dev] = ok ? 1 : ATTN_ERR_DEVICE;
     }
     return g_bwd_ready[dev] == 1 ? ATTN_OK : g_bwd_ready[dev];
@@ -80,7 +84,7 @@ int check_bwd_args(const void* q, const void* k, const void* v, const void* out,
     return ATTN_OK;
 }
 
-template <int D, bool M, bool E, bool DR = false>
+template <int D, bool M, bool E, bool DR>
 int launch_bwd(const CUtensorMap& tq, const CUtensorMap& tdo, const CUtensorMap& tk,
                const CUtensorMap& tv, BwdParams p, int sm_count, cudaStream_t stream) {
     const long long dq_units = (long long)p.B * p.Hq * p.num_tiles;
@@ -96,8 +100,25 @@ int launch_bwd(const CUtensorMap& tq, const CUtensorMap& tdo, const CUtensorMap&
     p.num_units = (int)dkv_units;
     grid = (int)(dkv_units < sm_count ? dkv_units : sm_count);
     p.head_block = std::min(p.B * p.Hkv, (8 * grid + p.num_tiles - 1) / p.num_tiles);
-    attn_bwd_dkdv_kernel<D, M, E, DR><<<grid, DkvLayout<D>::kThreads, DkvLayout<D>::kDynamicSmem, stream>>>(tq, tdo, tk, tv, p);
+    using KL = DkvLayout<D, E && DR>;
+    attn_bwd_dkdv_kernel<D, M, E, DR><<<grid, KL::kThreads, KL::kDynamicSmem, stream>>>(tq, tdo, tk, tv, p);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+// The instantiation for a block mask (m), keep bits (e) and dropout (dr).
+template <int D>
+int launch_variant(bool m, bool e, bool dr, const CUtensorMap& tq, const CUtensorMap& tdo,
+                   const CUtensorMap& tk, const CUtensorMap& tv, const BwdParams& p, int sm_count,
+                   cudaStream_t st) {
+    if (dr)
+        return m ? (e ? launch_bwd<D, true, true, true>(tq, tdo, tk, tv, p, sm_count, st)
+                      : launch_bwd<D, true, false, true>(tq, tdo, tk, tv, p, sm_count, st))
+                 : (e ? launch_bwd<D, false, true, true>(tq, tdo, tk, tv, p, sm_count, st)
+                      : launch_bwd<D, false, false, true>(tq, tdo, tk, tv, p, sm_count, st));
+    return m ? (e ? launch_bwd<D, true, true, false>(tq, tdo, tk, tv, p, sm_count, st)
+                  : launch_bwd<D, true, false, false>(tq, tdo, tk, tv, p, sm_count, st))
+             : (e ? launch_bwd<D, false, true, false>(tq, tdo, tk, tv, p, sm_count, st)
+                  : launch_bwd<D, false, false, false>(tq, tdo, tk, tv, p, sm_count, st));
 }
 
 int bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
@@ -158,7 +179,6 @@ extern "C" int attn_bwd_ex(const void* q, const void* k, const void* v, const vo
     if (!std::isfinite(opts->dropout_p) || opts->dropout_p < 0.f) return ATTN_ERR_INVALID_ARG;
     const long p8 = std::lrint((double)opts->dropout_p * 256.0);
     if (p8 > 255) return ATTN_ERR_INVALID_ARG;
-    if (p8 > 0 && opts->keep_bits != nullptr) return ATTN_ERR_UNSUPPORTED;
     return attn::bwd(q, k, v, out, dout, lse, delta, dq, dk, dv, B, Hq, Hkv, S, D, scale, causal,
                      opts->block_mask, opts->block_mask != nullptr ? opts->mask_heads : 1, stream,
                      opts->keep_bits, opts->keep_bits != nullptr ? opts->keep_heads : 1, (int)p8,
@@ -243,24 +263,9 @@ int bwd(const void* q, const void* k, const void* v, const void* out, const void
     p.dropout_offset = offset;
     p.keep_scale = dropout_p8 > 0 ? 256.f / (float)(256 - dropout_p8) : 1.f;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const bool m = block_mask != nullptr, e = keep_bits != nullptr;
-    if (dropout_p8 > 0) {
-        if (e) return ATTN_ERR_UNSUPPORTED;  // the dK/dV stage holds one bit set per tile
-        if (m)
-            return D == 64 ? launch_bwd<64, true, false, true>(tq, tdo, tk, tv, p, sm_count, st)
-                           : launch_bwd<128, true, false, true>(tq, tdo, tk, tv, p, sm_count, st);
-        return D == 64 ? launch_bwd<64, false, false, true>(tq, tdo, tk, tv, p, sm_count, st)
-                       : launch_bwd<128, false, false, true>(tq, tdo, tk, tv, p, sm_count, st);
-    }
-    if (D == 64)
-        return m ? (e ? launch_bwd<64, true, true>(tq, tdo, tk, tv, p, sm_count, st)
-                      : launch_bwd<64, true, false>(tq, tdo, tk, tv, p, sm_count, st))
-                 : (e ? launch_bwd<64, false, true>(tq, tdo, tk, tv, p, sm_count, st)
-                      : launch_bwd<64, false, false>(tq, tdo, tk, tv, p, sm_count, st));
-    return m ? (e ? launch_bwd<128, true, true>(tq, tdo, tk, tv, p, sm_count, st)
-                  : launch_bwd<128, true, false>(tq, tdo, tk, tv, p, sm_count, st))
-             : (e ? launch_bwd<128, false, true>(tq, tdo, tk, tv, p, sm_count, st)
-                  : launch_bwd<128, false, false>(tq, tdo, tk, tv, p, sm_count, st));
+    const bool m = block_mask != nullptr, e = keep_bits != nullptr, dr = dropout_p8 > 0;
+    return D == 64 ? launch_variant<64>(m, e, dr, tq, tdo, tk, tv, p, sm_count, st)
+                   : launch_variant<128>(m, e, dr, tq, tdo, tk, tv, p, sm_count, st);
 }
 
 }  // namespace

@@ -683,7 +683,9 @@ __global__ void __launch_bounds__(DqLayout<D>::kThreads, 1)
 }
 
 // ====================================================================== dK, dV
-template <int D>
+// ED: the kernel applies keep bits and dropout together, and each statistics
+// stage holds both bit sets.
+template <int D, bool ED = false>
 struct DkvLayout {
     static constexpr int kThreads = 384;
     static constexpr int kRegsSmall = 56;
@@ -694,9 +696,12 @@ struct DkvLayout {
     static constexpr uint32_t kChunkBytes = kTile * 128;
     static constexpr int kStatStages = 4;  // per-query LSE / delta rows
     // Stage s: lse2[128], delta[128] (fp32), then (element-masked kernels) the
-    // 16 keep bytes of the unit's key tile for each of the 128 queries.
+    // 16 keep bytes of the unit's key tile for each of the 128 queries; the
+    // dropout bits of the tile take the same layout, at kStatDrop: in place of
+    // the keep bytes, or after them when the kernel applies both.
     static constexpr uint32_t kStatKeep = 2 * kTile * 4;
-    static constexpr uint32_t kStatBytes = kStatKeep + kTile * 16;
+    static constexpr uint32_t kStatDrop = kStatKeep + (ED ? kTile * 16 : 0);
+    static constexpr uint32_t kStatBytes = kStatDrop + kTile * 16;
     // Q_i, dO_i ring, one tile per slot: as many slots as fit (5 at D = 128, 12 at D = 64).
     static constexpr int kStages =
         (227 * 1024 - 2 * (int)kTileBytes - kStatStages * (int)kStatBytes - 2048) / (int)kTileBytes > 12
@@ -753,16 +758,16 @@ __device__ __forceinline__ int dkv_next(const BwdParams& p, const DkvUnit& w, in
     return w.n;
 }
 
-template <int D>
+template <class L>
 __device__ __forceinline__ uint32_t dkv_bar(uint32_t base, int i) {
-    return base + DkvLayout<D>::kBars + 8u * (uint32_t)i;
+    return base + L::kBars + 8u * (uint32_t)i;
 }
 
 template <int D, bool M, bool E, bool DR>
 __device__ void dkv_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_do,
                               const CUtensorMap* tm_k, const CUtensorMap* tm_v, const BwdParams& p,
                               uint32_t base, volatile int* abort_flag) {
-    using L = DkvLayout<D>;
+    using L = DkvLayout<D, E && DR>;
     const uint64_t lim = p.wait_limit_ns;
     uint32_t kve_phase = 0, ring_phase = 0;
     int slot = 0;
@@ -770,10 +775,10 @@ __device__ void dkv_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_do,
     uint32_t pend_kv_par = 0, pend_st = 0, pend_st_par = 0;
     for (int rnd = 0, u = bwd_unit_of_round(0); u < p.num_units; u = bwd_unit_of_round(++rnd)) {
         const DkvUnit w = dkv_decode(u, p);
-        if (!ptx::mbar_wait(dkv_bar<D>(base, L::kKVEmpty), kve_phase ^ 1u, abort_flag, p.status, lim))
+        if (!ptx::mbar_wait(dkv_bar<L>(base, L::kKVEmpty), kve_phase ^ 1u, abort_flag, p.status, lim))
             goto drain;
         {
-            const uint32_t full = dkv_bar<D>(base, L::kKVFull);
+            const uint32_t full = dkv_bar<L>(base, L::kKVFull);
             ptx::mbar_arrive_expect_tx(full, 2 * L::kTileBytes);
 #pragma unroll
             for (int c = 0; c < L::kChunks; ++c) {
@@ -789,10 +794,10 @@ __device__ void dkv_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_do,
             dkv_iter(w, p, t, bh, qt);
 #pragma unroll
             for (int x = 0; x < 2; ++x) {  // Q_i, then dO_i
-                if (!ptx::mbar_wait(dkv_bar<D>(base, L::kStEmpty + slot), ring_phase ^ 1u, abort_flag,
+                if (!ptx::mbar_wait(dkv_bar<L>(base, L::kStEmpty + slot), ring_phase ^ 1u, abort_flag,
                                     p.status, lim))
                     goto drain;
-                const uint32_t full = dkv_bar<D>(base, L::kStFull + slot);
+                const uint32_t full = dkv_bar<L>(base, L::kStFull + slot);
                 ptx::mbar_arrive_expect_tx(full, L::kTileBytes);
                 const CUtensorMap* map = x == 0 ? tm_q : tm_do;
 #pragma unroll
@@ -812,8 +817,8 @@ __device__ void dkv_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_do,
 drain:
     for (int s = 0; s < L::kStages; ++s)
         if (pend_st & (1u << s))
-            ptx::drain_wait(dkv_bar<D>(base, L::kStFull + s), (pend_st_par >> s) & 1u, lim);
-    if (pend_kv) ptx::drain_wait(dkv_bar<D>(base, L::kKVFull), pend_kv_par, lim);
+            ptx::drain_wait(dkv_bar<L>(base, L::kStFull + s), (pend_st_par >> s) & 1u, lim);
+    if (pend_kv) ptx::drain_wait(dkv_bar<L>(base, L::kKVFull), pend_kv_par, lim);
 }
 
 // Warps 2-3: LSE (as log2) and delta of each query tile into the stage's
@@ -821,7 +826,7 @@ drain:
 // their weights vanish.
 template <int D, bool M, bool E, bool DR>
 __device__ void dkv_stat_role(const BwdParams& p, uint32_t base, uint8_t* smem, volatile int* abort_flag) {
-    using L = DkvLayout<D>;
+    using L = DkvLayout<D, E && DR>;
     const int tid = threadIdx.x - 64;  // 0..63
     const uint64_t lim = p.wait_limit_ns;
     uint32_t ring_phase = 0;
@@ -851,7 +856,7 @@ __device__ void dkv_stat_role(const BwdParams& p, uint32_t base, uint8_t* smem, 
                             16 * w.kt));
                 }
             }
-            if (!ptx::mbar_wait(dkv_bar<D>(base, L::kStatEmpty + st), ring_phase ^ 1u, abort_flag, p.status, lim))
+            if (!ptx::mbar_wait(dkv_bar<L>(base, L::kStatEmpty + st), ring_phase ^ 1u, abort_flag, p.status, lim))
                 return;
             float* rows = reinterpret_cast<float*>(smem + L::kStat + (uint32_t)st * L::kStatBytes);
 #pragma unroll
@@ -864,7 +869,7 @@ __device__ void dkv_stat_role(const BwdParams& p, uint32_t base, uint8_t* smem, 
                 keep[tid] = kb[0];
                 keep[tid + 64] = kb[1];
             }
-            ptx::mbar_arrive(dkv_bar<D>(base, L::kStatFull + st));
+            ptx::mbar_arrive(dkv_bar<L>(base, L::kStatFull + st));
             if (++st == L::kStatStages) {
                 st = 0;
                 ring_phase ^= 1u;
@@ -875,7 +880,7 @@ __device__ void dkv_stat_role(const BwdParams& p, uint32_t base, uint8_t* smem, 
 
 template <int D, bool M, bool E, bool DR>
 __device__ void dkv_mma_role(const BwdParams& p, uint32_t base, uint32_t tmem, volatile int* abort_flag) {
-    using L = DkvLayout<D>;
+    using L = DkvLayout<D, E && DR>;
     constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(kTile, kTile, false);  // S^T, dP^T: N = 128 queries
     constexpr uint32_t kIdescA = ptx::idesc_bf16_f32(kTile, D, true);       // dV, dK: N = D, MN-major
     const uint64_t lim = p.wait_limit_ns;
@@ -886,13 +891,13 @@ __device__ void dkv_mma_role(const BwdParams& p, uint32_t base, uint32_t tmem, v
     int slot = 0;
 
     auto wait_bar = [&](int bar, uint32_t& phase) -> bool {
-        if (!ptx::mbar_wait(dkv_bar<D>(base, bar), phase, abort_flag, p.status, lim)) return false;
+        if (!ptx::mbar_wait(dkv_bar<L>(base, bar), phase, abort_flag, p.status, lim)) return false;
         phase ^= 1u;
         ptx::tc_fence_after();
         return true;
     };
     auto wait_ring = [&](int& got) -> bool {
-        if (!ptx::mbar_wait(dkv_bar<D>(base, L::kStFull + slot), ring_phase, abort_flag, p.status, lim))
+        if (!ptx::mbar_wait(dkv_bar<L>(base, L::kStFull + slot), ring_phase, abort_flag, p.status, lim))
             return false;
         got = slot;
         if (++slot == L::kStages) {
@@ -920,20 +925,20 @@ __device__ void dkv_mma_role(const BwdParams& p, uint32_t base, uint32_t tmem, v
         const int t0 = dkv_next<M>(p, w, -1);
         if (M && t0 >= w.n) {  // no query tile keeps this key tile: dK = dV = 0
             if (!wait_bar(L::kAccEmpty, acce_phase)) break;
-            ptx::mma_commit(dkv_bar<D>(base, L::kKVEmpty));
-            ptx::mma_commit(dkv_bar<D>(base, L::kAccFull));
+            ptx::mma_commit(dkv_bar<L>(base, L::kKVEmpty));
+            ptx::mma_commit(dkv_bar<L>(base, L::kAccFull));
             continue;
         }
         int qs, ds, qs_next = -1, ds_next = -1;
         if (!wait_ring(qs)) break;
         product(tmem, base + L::kK, slot_addr(qs));  // S^T = K Q^T
-        ptx::mma_commit(dkv_bar<D>(base, L::kSFull));
+        ptx::mma_commit(dkv_bar<L>(base, L::kSFull));
         if (!wait_ring(ds)) break;
         product(tmem + 128u, base + L::kV, slot_addr(ds));  // dP^T = V dO^T
-        ptx::mma_commit(dkv_bar<D>(base, L::kDPFull));
+        ptx::mma_commit(dkv_bar<L>(base, L::kDPFull));
         // K and V are read only by S^T and dP^T: free them for the next unit
         // as soon as the last of those has been issued.
-        if (dkv_next<M>(p, w, t0) >= w.n) ptx::mma_commit(dkv_bar<D>(base, L::kKVEmpty));
+        if (dkv_next<M>(p, w, t0) >= w.n) ptx::mma_commit(dkv_bar<L>(base, L::kKVEmpty));
         bool first = true;
         for (int t = t0, tn; t < w.n; t = tn, first = false) {
             tn = dkv_next<M>(p, w, t);
@@ -944,38 +949,38 @@ __device__ void dkv_mma_role(const BwdParams& p, uint32_t base, uint32_t tmem, v
             const uint64_t dod = ptx::sdesc_sw128(slot_addr(ds), L::kChunkBytes, 1024);
             ptx::mma_ts_k64(tDV, tmem, dod, kIdescA, first ? 0u : 1u);
             ptx::mma_ts_k64(tDV, tmem + 64u, dod + 512u, kIdescA, 1u);
-            ptx::mma_commit(dkv_bar<D>(base, L::kStEmpty + ds));
+            ptx::mma_commit(dkv_bar<L>(base, L::kStEmpty + ds));
             if (tn < w.n) {
                 if (!(ok = wait_ring(qs_next))) break;
                 product(tmem, base + L::kK, slot_addr(qs_next));
-                ptx::mma_commit(dkv_bar<D>(base, L::kSFull));
+                ptx::mma_commit(dkv_bar<L>(base, L::kSFull));
             }
             // dK += dS^T Q: dS^T in columns [128,160) and [192,224).
             if (!(ok = wait_bar(L::kDSFull, ds_phase))) break;
             const uint64_t qd = ptx::sdesc_sw128(slot_addr(qs), L::kChunkBytes, 1024);
             ptx::mma_ts_k64(tDK, tmem + 128u, qd, kIdescA, first ? 0u : 1u);
             ptx::mma_ts_k64(tDK, tmem + 192u, qd + 512u, kIdescA, 1u);
-            ptx::mma_commit(dkv_bar<D>(base, L::kStEmpty + qs));
+            ptx::mma_commit(dkv_bar<L>(base, L::kStEmpty + qs));
             if (tn < w.n) {
                 if (!(ok = wait_ring(ds_next))) break;
                 product(tmem + 128u, base + L::kV, slot_addr(ds_next));
-                ptx::mma_commit(dkv_bar<D>(base, L::kDPFull));
-                if (dkv_next<M>(p, w, tn) >= w.n) ptx::mma_commit(dkv_bar<D>(base, L::kKVEmpty));
+                ptx::mma_commit(dkv_bar<L>(base, L::kDPFull));
+                if (dkv_next<M>(p, w, tn) >= w.n) ptx::mma_commit(dkv_bar<L>(base, L::kKVEmpty));
             }
             qs = qs_next;
             ds = ds_next;
         }
         if (!ok) break;
-        ptx::mma_commit(dkv_bar<D>(base, L::kAccFull));
+        ptx::mma_commit(dkv_bar<L>(base, L::kAccFull));
     }
-    ptx::mma_commit(dkv_bar<D>(base, L::kDrain));
-    ptx::drain_wait(dkv_bar<D>(base, L::kDrain), 0u, lim);
+    ptx::mma_commit(dkv_bar<L>(base, L::kDrain));
+    ptx::drain_wait(dkv_bar<L>(base, L::kDrain), 0u, lim);
 }
 
 template <int D, bool M, bool E, bool DR>
 __device__ void dkv_work_role(const BwdParams& p, uint32_t base, const uint8_t* smem, uint32_t tmem,
                               int wg, volatile int* abort_flag) {
-    using L = DkvLayout<D>;
+    using L = DkvLayout<D, E && DR>;
     const int warp = threadIdx.x >> 5;
     const int r = (warp & 3) * 32 + (threadIdx.x & 31);  // key row of the tile = TMEM lane
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
@@ -992,7 +997,7 @@ __device__ void dkv_work_role(const BwdParams& p, uint32_t base, const uint8_t* 
         for (int t = dkv_next<M>(p, w, -1); t < w.n; t = dkv_next<M>(p, w, t)) {
             int bh, qt;
             dkv_iter(w, p, t, bh, qt);
-            bool ok = ptx::mbar_wait(dkv_bar<D>(base, L::kStatFull + st), ring_phase, abort_flag, p.status, lim);
+            bool ok = ptx::mbar_wait(dkv_bar<L>(base, L::kStatFull + st), ring_phase, abort_flag, p.status, lim);
             if constexpr (DR) {
                 // The tile's 128 x 128 keep decisions: 512 Philox blocks (a query
                 // and 32 keys each), two per element-wise thread, written as bits
@@ -1000,7 +1005,7 @@ __device__ void dkv_work_role(const BwdParams& p, uint32_t base, const uint8_t* 
                 // computed; every thread then waits for all 256 to have written.
                 if (!__all_sync(0xffffffffu, ok)) return;
                 uint32_t* keepw = reinterpret_cast<uint32_t*>(
-                    const_cast<uint8_t*>(smem) + L::kStat + (uint32_t)st * L::kStatBytes + L::kStatKeep);
+                    const_cast<uint8_t*>(smem) + L::kStat + (uint32_t)st * L::kStatBytes + L::kStatDrop);
                 const int et = threadIdx.x - 128;  // 0 .. 255
 #pragma unroll
                 for (int y = 0; y < 2; ++y) {
@@ -1014,11 +1019,11 @@ __device__ void dkv_work_role(const BwdParams& p, uint32_t base, const uint8_t* 
                         bits |= (((uint32_t)(rnd[c >> 3] >> (8 * (c & 7))) & 0xFFu) >= (uint32_t)p.dropout_p8 ? 1u : 0u) << c;
                     keepw[4 * qq + b] = bits;
                 }
-                ptx::mbar_arrive(dkv_bar<D>(base, L::kBitsReady));
-                ok = ptx::mbar_wait(dkv_bar<D>(base, L::kBitsReady), bits_phase, abort_flag, p.status, lim);
+                ptx::mbar_arrive(dkv_bar<L>(base, L::kBitsReady));
+                ok = ptx::mbar_wait(dkv_bar<L>(base, L::kBitsReady), bits_phase, abort_flag, p.status, lim);
                 bits_phase ^= 1u;
             }
-            ok = ok && ptx::mbar_wait(dkv_bar<D>(base, L::kSFull), s_phase, abort_flag, p.status, lim);
+            ok = ok && ptx::mbar_wait(dkv_bar<L>(base, L::kSFull), s_phase, abort_flag, p.status, lim);
             if (!__all_sync(0xffffffffu, ok)) return;
             s_phase ^= 1u;
             ptx::tc_fence_after();
@@ -1062,7 +1067,7 @@ __device__ void dkv_work_role(const BwdParams& p, uint32_t base, const uint8_t* 
             const float ks = DR ? p.keep_scale : 1.f;
             if constexpr (DR) {
                 const uint32_t* kw = reinterpret_cast<const uint32_t*>(
-                    smem + L::kStat + (uint32_t)st * L::kStatBytes + L::kStatKeep) + (r >> 5);
+                    smem + L::kStat + (uint32_t)st * L::kStatBytes + L::kStatDrop) + (r >> 5);
                 zb = 0ull;
 #pragma unroll
                 for (int c = 0; c < 64; ++c) zb |= (uint64_t)((kw[4 * (64 * wg + c)] >> (r & 31)) & 1u) << c;
@@ -1081,9 +1086,9 @@ __device__ void dkv_work_role(const BwdParams& p, uint32_t base, const uint8_t* 
             ptx::tmem_st_wait();
             ptx::tc_fence_before();
             __syncwarp();
-            if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(dkv_bar<D>(base, L::kPFull));
+            if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(dkv_bar<L>(base, L::kPFull));
 
-            ok = ptx::mbar_wait(dkv_bar<D>(base, L::kDPFull), dp_phase, abort_flag, p.status, lim);
+            ok = ptx::mbar_wait(dkv_bar<L>(base, L::kDPFull), dp_phase, abort_flag, p.status, lim);
             if (!__all_sync(0xffffffffu, ok)) return;
             dp_phase ^= 1u;
             ptx::tc_fence_after();
@@ -1109,8 +1114,8 @@ __device__ void dkv_work_role(const BwdParams& p, uint32_t base, const uint8_t* 
             ptx::tc_fence_before();
             __syncwarp();
             if ((threadIdx.x & 31) == 0) {
-                ptx::mbar_arrive(dkv_bar<D>(base, L::kDSFull));
-                ptx::mbar_arrive(dkv_bar<D>(base, L::kStatEmpty + st));
+                ptx::mbar_arrive(dkv_bar<L>(base, L::kDSFull));
+                ptx::mbar_arrive(dkv_bar<L>(base, L::kStatEmpty + st));
             }
             if (++st == L::kStatStages) {
                 st = 0;
@@ -1118,7 +1123,7 @@ __device__ void dkv_work_role(const BwdParams& p, uint32_t base, const uint8_t* 
             }
         }
         // Epilogue: warpgroup 0 writes dV, warpgroup 1 writes dK * scale.
-        bool ok = ptx::mbar_wait(dkv_bar<D>(base, L::kAccFull), acc_phase, abort_flag, p.status, lim);
+        bool ok = ptx::mbar_wait(dkv_bar<L>(base, L::kAccFull), acc_phase, abort_flag, p.status, lim);
         if (!__all_sync(0xffffffffu, ok)) return;
         acc_phase ^= 1u;
         ptx::tc_fence_after();
@@ -1153,7 +1158,7 @@ __device__ void dkv_work_role(const BwdParams& p, uint32_t base, const uint8_t* 
         if constexpr (M) {  // dK, dV read out: the next unit may produce its own
             ptx::tc_fence_before();
             __syncwarp();
-            if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(dkv_bar<D>(base, L::kAccEmpty));
+            if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(dkv_bar<L>(base, L::kAccEmpty));
         }
     }
 }
@@ -1163,7 +1168,7 @@ __global__ void __launch_bounds__(DkvLayout<D>::kThreads, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                          const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                          const BwdParams p) {
-    using L = DkvLayout<D>;
+    using L = DkvLayout<D, E && DR>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -1173,24 +1178,24 @@ __global__ void __launch_bounds__(DkvLayout<D>::kThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        ptx::mbar_init(dkv_bar<D>(base, L::kKVFull), 1);
-        ptx::mbar_init(dkv_bar<D>(base, L::kKVEmpty), 1);
-        ptx::mbar_init(dkv_bar<D>(base, L::kSFull), 1);
-        ptx::mbar_init(dkv_bar<D>(base, L::kDPFull), 1);
-        ptx::mbar_init(dkv_bar<D>(base, L::kPFull), 8);   // one per element-wise warp
-        ptx::mbar_init(dkv_bar<D>(base, L::kDSFull), 8);
-        ptx::mbar_init(dkv_bar<D>(base, L::kAccFull), 1);
+        ptx::mbar_init(dkv_bar<L>(base, L::kKVFull), 1);
+        ptx::mbar_init(dkv_bar<L>(base, L::kKVEmpty), 1);
+        ptx::mbar_init(dkv_bar<L>(base, L::kSFull), 1);
+        ptx::mbar_init(dkv_bar<L>(base, L::kDPFull), 1);
+        ptx::mbar_init(dkv_bar<L>(base, L::kPFull), 8);   // one per element-wise warp
+        ptx::mbar_init(dkv_bar<L>(base, L::kDSFull), 8);
+        ptx::mbar_init(dkv_bar<L>(base, L::kAccFull), 1);
         for (int s = 0; s < L::kStages; ++s) {
-            ptx::mbar_init(dkv_bar<D>(base, L::kStFull + s), 1);
-            ptx::mbar_init(dkv_bar<D>(base, L::kStEmpty + s), 1);
+            ptx::mbar_init(dkv_bar<L>(base, L::kStFull + s), 1);
+            ptx::mbar_init(dkv_bar<L>(base, L::kStEmpty + s), 1);
         }
         for (int s = 0; s < L::kStatStages; ++s) {
-            ptx::mbar_init(dkv_bar<D>(base, L::kStatFull + s), 64);  // one per loader thread
-            ptx::mbar_init(dkv_bar<D>(base, L::kStatEmpty + s), 8);  // one per element-wise warp
+            ptx::mbar_init(dkv_bar<L>(base, L::kStatFull + s), 64);  // one per loader thread
+            ptx::mbar_init(dkv_bar<L>(base, L::kStatEmpty + s), 8);  // one per element-wise warp
         }
-        ptx::mbar_init(dkv_bar<D>(base, L::kDrain), 1);
-        ptx::mbar_init(dkv_bar<D>(base, L::kAccEmpty), 8);  // one per element-wise warp
-        ptx::mbar_init(dkv_bar<D>(base, L::kBitsReady), 256);  // one per element-wise thread
+        ptx::mbar_init(dkv_bar<L>(base, L::kDrain), 1);
+        ptx::mbar_init(dkv_bar<L>(base, L::kAccEmpty), 8);  // one per element-wise warp
+        ptx::mbar_init(dkv_bar<L>(base, L::kBitsReady), 256);  // one per element-wise thread
         *abort_flag = 0;
         ptx::fence_barrier_init();
         ptx::prefetch_tensormap(&tm_q);

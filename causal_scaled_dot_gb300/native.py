@@ -406,12 +406,9 @@ def attention_trainable(q, k, v, causal: bool = True, scale: float | None = None
     """O = attention(q, k, v) with gradients: forward and backward run the C ABI
     (attn_fwd_ex / attn_bwd_ex with the given options).  q [B,Hq,S,D], k/v
     [B,Hkv,S,D] bf16 CUDA tensors; block_mask uint8 [1 or Hq, nt, nt]; keep_bits
-    uint8 [1 or Hq, S, 16*nt]; dropout combines with a block mask (keep bits with
-    dropout have no backward)."""
+    uint8 [1 or Hq, S, 16*nt]; dropout combines with either or both."""
     global _ATTENTION_FUNCTION
     import torch
-    if dropout_p > 0.0 and keep_bits is not None:
-        raise ValueError("keep bits with dropout have no backward")
     for name, t in (("q", q), ("k", k), ("v", v)):
         if t.dtype != torch.bfloat16 or not t.is_cuda or t.dim() != 4 or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous bf16 CUDA [B,H,S,D] tensor")

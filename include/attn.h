@@ -293,8 +293,8 @@ int attn_bwd_dropout(const void *q, const void *k, const void *v, const void *ou
 
 /*
  * attn_bwd_ex -- the gradients of attn_fwd_ex's output for the same options
- * (bf16 inputs; opts NULL: attn_bwd).  Keep bits with dropout is not
- * supported (ATTN_ERR_UNSUPPORTED).
+ * (bf16 inputs, every combination of block mask, keep bits and dropout;
+ * opts NULL: attn_bwd).  E4M3 inputs: ATTN_ERR_UNSUPPORTED.
  */
 int attn_bwd_ex(const void *q, const void *k, const void *v, const void *out, const void *dout,
                 const float *lse, float *delta, void *dq, void *dk, void *dv, int B, int Hq, int Hkv,

@@ -242,10 +242,6 @@ def test_unsupported_option_combinations_are_rejected_before_launch():
     assert lib.attn_fwd_ex(q, k, v, out, None, 1, 2, 2, 300, 128, f, 1, ctypes.byref(bad_fmt),
                            None) == ATTN_ERR_INVALID_ARG
     bargs = [q, k, v, out, 6 << 40, 5 << 40, 7 << 40, 8 << 40, 9 << 40, 10 << 40, 1, 2, 2, 300, 128, f, 1]
-    keep_drop = native.options(keep_bits=None, dropout_p=0.1)
-    keep_drop.keep_bits = 11 << 40
-    keep_drop.keep_heads = 1
-    assert lib.attn_bwd_ex(*bargs, ctypes.byref(keep_drop), None) == ATTN_ERR_UNSUPPORTED
     assert lib.attn_bwd_ex(*bargs, ctypes.byref(fp8_d64), None) == ATTN_ERR_UNSUPPORTED
 
 

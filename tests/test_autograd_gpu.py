@@ -20,7 +20,26 @@ def _cuda():
         pytest.skip("no CUDA device")
 
 
-@pytest.mark.parametrize("variant", ["plain", "block", "keep", "dropout"])
+def _direct_ex(q, k, v, do, scale, kb, p):
+    """(O, LSE, dQ, dK, dV) from attn_fwd_ex / attn_bwd_ex called directly."""
+    import torch
+    from causal_scaled_dot_gb300 import native
+    B, Hq, S, D = q.shape
+    Hkv = k.shape[1]
+    qd, kd, vd, dod = (to_device(x) for x in (q, k, v, do))
+    kbd = torch.from_numpy(kb).cuda()
+    opts = native.options(keep_bits=kbd, dropout_p=p, seed=5, offset=6)
+    out = torch.empty_like(qd)
+    lse = torch.empty((B, Hq, S), dtype=torch.float32, device="cuda")
+    native.attn_fwd_ex(qd, kd, vd, out, lse, B, Hq, Hkv, S, D, scale, True, opts)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    delta = torch.empty_like(lse)
+    native.attn_bwd_ex(qd, kd, vd, out, dod, lse, delta, dq, dk, dv, B, Hq, Hkv, S, D, scale, True, opts)
+    torch.cuda.synchronize()
+    return tuple(t.double().cpu().numpy() for t in (out, lse, dq, dk, dv))
+
+
+@pytest.mark.parametrize("variant", ["plain", "block", "keep", "dropout", "keep+dropout"])
 def test_autograd_matches_direct_backward(variant):
     import torch
     from causal_scaled_dot_gb300 import native
@@ -29,8 +48,8 @@ def test_autograd_matches_direct_backward(variant):
     do = gaussian_bf16((B, Hq, S, D), 9100, 3)
     scale = 1.0 / math.sqrt(D)
     bm = random_block_mask(Hq, S, 0.7, seed=91) if variant == "block" else None
-    kb = random_keep_bits(1, S, 0.6, seed=92) if variant == "keep" else None
-    p = 0.2 if variant == "dropout" else 0.0
+    kb = random_keep_bits(1, S, 0.6, seed=92) if "keep" in variant else None
+    p = 0.2 if "dropout" in variant else 0.0
     tq, tk, tv = (to_device(x).requires_grad_() for x in (q, k, v))
     o = native.attention_trainable(tq, tk, tv, True, scale,
                                    block_mask=None if bm is None else torch.from_numpy(bm).cuda(),
@@ -44,6 +63,8 @@ def test_autograd_matches_direct_backward(variant):
         want = run_gpu_bwd_masked(q, k, v, do, scale, True, bm)
     elif variant == "keep":
         want = run_gpu_bwd_elem_masked(q, k, v, do, scale, True, kb)
+    elif variant == "keep+dropout":
+        want = _direct_ex(q, k, v, do, scale, kb, p)
     else:
         want = run_gpu_bwd_dropout(q, k, v, do, scale, True, p, 5, 6)
     assert np.array_equal(o.detach().double().cpu().numpy(), want[0])

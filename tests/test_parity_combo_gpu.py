@@ -1,7 +1,7 @@
 """GPU parity of the combined options (attn_fwd_ex / attn_bwd_ex) against the
 oracle's combined variants: masks with dropout, masks with E4M3 inputs, and the
-gradients of a block mask with dropout; single options through the options
-entry equal their own entry points bit for bit."""
+gradients of block masks and keep bits with dropout; single options through the
+options entry equal their own entry points bit for bit."""
 import math
 
 import numpy as np
@@ -93,7 +93,7 @@ def test_options_with_one_feature_equal_their_own_entry_points():
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
 
 
-def _bwd_ex(q, k, v, do, scale, causal, bm, p):
+def _bwd_ex(q, k, v, do, scale, causal, bm, p, kb=None):
     import torch
     from causal_scaled_dot_gb300 import native
     B, Hq, S, D = q.shape
@@ -101,8 +101,8 @@ def _bwd_ex(q, k, v, do, scale, causal, bm, p):
     qd, kd, vd, dod = to_device(q), to_device(k), to_device(v), to_device(do)
     out = torch.empty_like(qd)
     lse = torch.empty((B, Hq, S), dtype=torch.float32, device="cuda")
-    bmd = _dev(bm)  # held here: the options keep only its address
-    opts = native.options(block_mask=bmd, dropout_p=p, seed=SEED, offset=OFFSET)
+    bmd, kbd = _dev(bm), _dev(kb)  # held here: the options keep only their addresses
+    opts = native.options(block_mask=bmd, keep_bits=kbd, dropout_p=p, seed=SEED, offset=OFFSET)
     native.attn_fwd_ex(qd, kd, vd, out, lse, B, Hq, Hkv, S, D, scale, causal, opts)
     dq, dk, dv = (torch.full_like(t, float("nan")) for t in (qd, kd, vd))
     delta = torch.full_like(lse, float("nan"))
@@ -130,6 +130,43 @@ def test_bwd_block_mask_with_dropout(S, D, causal):
     print(compare_grad(dq, rq, label + " dQ", scale * e * float(np.max(np.abs(f64(k))))),
           compare_grad(dk, rk, label + " dK", scale * e * float(np.max(np.abs(f64(q)))) * 2),
           compare_grad(dv, rv, label + " dV"))
+
+
+def _check_bwd_combo(q, k, v, do, scale, causal, bm, kb, p, label):
+    o, _, dq, dk, dv, _ = _bwd_ex(q, k, v, do, scale, causal, bm, p, kb)
+    rq, rk, rv, _ = oracle.attention_bwd(q, k, v, do, scale, causal, block_mask=bm, keep_bits=kb,
+                                         dropout=(int(round(p * 256)), SEED, OFFSET))
+    # delta from the rounded bf16 output, as in test_bwd_block_mask_with_dropout
+    f64 = lambda b: bf16_bits_to_float32(b).astype(np.float64)  # noqa: E731
+    e = 2.0 ** -8 * float(np.max(np.sum(np.abs(f64(do) * o), axis=-1)))
+    return (compare_grad(dq, rq, label + " dQ", scale * e * float(np.max(np.abs(f64(k))))),
+            compare_grad(dk, rk, label + " dK", scale * e * float(np.max(np.abs(f64(q)))) * 2),
+            compare_grad(dv, rv, label + " dV"))
+
+
+@pytest.mark.parametrize("S", [129, 700])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("combo", ["keep+dropout", "block+keep+dropout"])
+def test_bwd_keep_bits_with_dropout(S, D, causal, combo):
+    Hq, Hkv, p = 4, 2, 0.2
+    q, k, v = qkv_bf16(2, Hq, Hkv, S, D, seed=9800 + S + D)
+    do = gaussian_bf16((2, Hq, S, D), 9800 + S + D, 3)
+    kb = random_keep_bits(1 if D == 64 else Hq, S, 0.7, seed=S + 3)
+    bm = random_block_mask(Hq, S, 0.7, seed=S + 4) if "block" in combo else None
+    print(_check_bwd_combo(q, k, v, do, 1 / math.sqrt(D), causal, bm, kb, p,
+                           f"{combo} bwd S{S} D{D} causal={causal}"))
+
+
+def test_bwd_keep_bits_with_dropout_on_a_window():
+    """A 256-key local window (rows that see few keys) with dropout 0.1, GQA 4:1."""
+    from causal_scaled_dot_gb300.inputs import block_mask_of_keep_bits, window_keep_bits
+    B, Hq, Hkv, S, D = 1, 8, 2, 1000, 128
+    q, k, v = qkv_bf16(B, Hq, Hkv, S, D, seed=9900)
+    do = gaussian_bf16((B, Hq, S, D), 9900, 3)
+    kb = window_keep_bits(S, 256)
+    bm = block_mask_of_keep_bits(kb, S)
+    print(_check_bwd_combo(q, k, v, do, 1 / math.sqrt(D), True, bm, kb, 0.1, "window256+dropout bwd"))
 
 
 def test_bwd_options_dropout_equals_its_own_entry_point():
