@@ -702,7 +702,7 @@ struct DkvLayout {
     static constexpr uint32_t kStatKeep = 2 * kTile * 4;
     static constexpr uint32_t kStatDrop = kStatKeep + (ED ? kTile * 16 : 0);
     static constexpr uint32_t kStatBytes = kStatDrop + kTile * 16;
-    // Q_i, dO_i ring, one tile per slot: as many slots as fit (5 at D = 128, 12 at D = 64).
+    // Q_i, dO_i ring, one tile per slot: as many as fit (4 at D = 128, 10 or 11 at D = 64).
     static constexpr int kStages =
         (227 * 1024 - 2 * (int)kTileBytes - kStatStages * (int)kStatBytes - 2048) / (int)kTileBytes > 12
             ? 12

@@ -177,3 +177,40 @@ def test_bwd_options_dropout_equals_its_own_entry_point():
     b = run_gpu_bwd_dropout(q, k, v, do, 0.088, True, 0.25, SEED, OFFSET)
     for x, y in zip(a, b):
         assert np.array_equal(x, y)
+
+
+@pytest.mark.parametrize("w", [x for x in WORKLOADS[1:] if x.name.startswith(("profile", "gqa"))],
+                         ids=lambda w: w.name)
+def test_window_with_dropout_full_size(w):
+    """A 1024-key local window (keep bits and their block mask) with dropout 0.1
+    at a timed size: the forward on sampled rows, the gradients on the first
+    and last key/value heads."""
+    from causal_scaled_dot_gb300.inputs import block_mask_of_keep_bits, window_keep_bits
+    from tests.gpu_util import sample_rows
+    p = 0.1
+    p8 = int(round(p * 256))
+    q, k, v = qkv_bf16(w.B, w.Hq, w.Hkv, w.S, w.D, seed=w.seed, sigma=w.sigma)
+    do = gaussian_bf16((w.B, w.Hq, w.S, w.D), w.seed, 3)
+    kb = window_keep_bits(w.S, 1024)
+    bm = block_mask_of_keep_bits(kb, w.S)
+    scale = 1 / math.sqrt(w.D)
+    o, l, dq, dk, dv, _ = _bwd_ex(q, k, v, do, scale, True, bm, p, kb)
+    rows = sample_rows(w.B, w.Hq, w.S, n_random=128, seed=w.seed)
+    ro, rl = oracle.attention_ex(q, k, v, scale, True, block_mask=bm, keep_bits=kb,
+                                 dropout=(p8, SEED, OFFSET), rows=rows)
+    fwd = compare_masked(o.reshape(-1, w.D)[rows], ro, l.reshape(-1)[rows], rl, f"{w.name} window+dropout",
+                         abs_scale=256 / (256 - p8))
+    heads = [0, w.B * w.Hkv - 1]
+    G = w.Hq // w.Hkv
+    rq, rk, rv, _ = oracle.attention_bwd(q, k, v, do, scale, True, kv_heads=heads, block_mask=bm, keep_bits=kb,
+                                         dropout=(p8, SEED, OFFSET))
+    f64 = lambda b: bf16_bits_to_float32(b).astype(np.float64)  # noqa: E731
+    e = 2.0 ** -8 * float(np.max(np.sum(np.abs(f64(do) * o), axis=-1)))
+    sel = np.asarray(heads)
+    label = f"{w.name} window+dropout bwd"
+    print(fwd,
+          compare_grad(dq.reshape(w.B * w.Hkv, G, w.S, w.D)[sel], rq, label + " dQ",
+                       scale * e * float(np.max(np.abs(f64(k))))),
+          compare_grad(dk.reshape(w.B * w.Hkv, w.S, w.D)[sel], rk, label + " dK",
+                       scale * e * float(np.max(np.abs(f64(q)))) * G),
+          compare_grad(dv.reshape(w.B * w.Hkv, w.S, w.D)[sel], rv, label + " dV"))
