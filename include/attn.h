@@ -64,9 +64,10 @@ enum { ATTN_INPUT_BF16 = 0, ATTN_INPUT_E4M3 = 1 };
  *   block_mask, mask_heads   as attn_fwd_block_masked (NULL: none).
  *   keep_bits, keep_heads    as attn_fwd_elem_masked (NULL: none).
  *   dropout_p, seed, offset  as attn_fwd_dropout (dropout_p = 0: none).
- * Supported together: forward, any of the masks with dropout (bf16) and any of
- * the masks with E4M3 inputs; backward (bf16), any of the masks, or dropout
- * with a block mask.  Other combinations return ATTN_ERR_UNSUPPORTED.
+ * Supported together: bf16 inputs with any combination of the block mask,
+ * keep bits and dropout (forward and backward); E4M3 inputs with either or
+ * both masks (forward only, D = 128).  E4M3 with dropout, and E4M3 in the
+ * backward, return ATTN_ERR_UNSUPPORTED.
  */
 typedef struct {
     int input_format;
