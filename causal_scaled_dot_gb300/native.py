@@ -110,9 +110,11 @@ def options(e4m3_descales=None, block_mask=None, keep_bits=None, dropout_p: floa
             offset: int = 0) -> AttnOptions:
     """An attn_options_t: E4M3 inputs when ``e4m3_descales`` = (q, k, v) is given; masks
     as CUDA uint8 tensors (their first dimension gives mask_heads / keep_heads).  The
-    structure keeps only the masks' addresses: the tensors must stay alive until the
-    calls that use it have run."""
+    returned object also holds the mask tensors, which keeps them alive while it is in
+    use and lets the entry points check their sizes (a mask given as an int pointer must
+    be kept alive by the caller)."""
     o = AttnOptions()
+    o.tensors = (block_mask, keep_bits)
     o.input_format = ATTN_INPUT_E4M3 if e4m3_descales is not None else ATTN_INPUT_BF16
     o.q_descale, o.k_descale, o.v_descale = e4m3_descales if e4m3_descales is not None else (1.0, 1.0, 1.0)
     o.block_mask = _ptr(block_mask)
@@ -123,6 +125,56 @@ def options(e4m3_descales=None, block_mask=None, keep_bits=None, dropout_p: floa
     o.seed = int(seed) & (2**64 - 1)
     o.offset = int(offset) & (2**64 - 1)
     return o
+
+
+def _sizes(*items):
+    """Raise ValueError when a tensor argument holds fewer bytes than the sizes
+    passed with it imply: the C entry points read and write exactly that many
+    bytes from the addresses they receive and cannot check them.  ``items`` are
+    (name, tensor / int pointer / None, bytes needed); only tensors are checked."""
+    for name, x, need in items:
+        if hasattr(x, "element_size") and hasattr(x, "numel"):
+            have = int(x.numel()) * int(x.element_size())
+            if need > 0 and have < need:
+                raise ValueError(f"{name} holds {have} bytes; the sizes given need {need}")
+
+
+def _attn_bytes(B, Hq, Hkv, S, D, in_bytes=2):
+    """Bytes of q, of k (= v), of out (= dout, dq) and of lse (= delta)."""
+    return (B * Hq * S * D * in_bytes, B * Hkv * S * D * in_bytes, B * Hq * S * D * 2, B * Hq * S * 4)
+
+
+def _mask_bytes(S, mask_heads=1, keep_heads=1):
+    """Bytes of a block mask [mask_heads, nt, nt] and of keep bits [keep_heads, S, 16 nt]."""
+    nt = -(-S // 128)
+    return mask_heads * nt * nt, keep_heads * S * 16 * nt
+
+
+def _fwd_sizes(q, k, v, out, lse, B, Hq, Hkv, S, D, in_bytes=2, block_mask=None, mask_heads=1,
+               keep_bits=None, keep_heads=1):
+    qb, kb, ob, lb = _attn_bytes(B, Hq, Hkv, S, D, in_bytes)
+    mb, eb = _mask_bytes(S, mask_heads, keep_heads)
+    _sizes(("q", q, qb), ("k", k, kb), ("v", v, kb), ("out", out, ob), ("lse", lse, lb),
+           ("block_mask", block_mask, mb), ("keep_bits", keep_bits, eb))
+
+
+def _bwd_sizes(q, k, v, out, dout, lse, delta, dq, dk, dv, B, Hq, Hkv, S, D, block_mask=None,
+               mask_heads=1, keep_bits=None, keep_heads=1):
+    qb, kb, ob, lb = _attn_bytes(B, Hq, Hkv, S, D)
+    mb, eb = _mask_bytes(S, mask_heads, keep_heads)
+    _sizes(("q", q, qb), ("k", k, kb), ("v", v, kb), ("out", out, ob), ("dout", dout, ob), ("lse", lse, lb),
+           ("delta", delta, lb), ("dq", dq, ob), ("dk", dk, kb), ("dv", dv, kb),
+           ("block_mask", block_mask, mb), ("keep_bits", keep_bits, eb))
+
+
+def _opts_masks(opts):
+    """The mask tensors an AttnOptions holds and still points at (None otherwise)."""
+    if opts is None:
+        return None, None
+    held = getattr(opts, "tensors", (None, None))
+    addr = (opts.block_mask, opts.keep_bits)
+    return tuple(t if t is not None and hasattr(t, "data_ptr") and a and t.data_ptr() == a else None
+                 for t, a in zip(held, addr))
 
 
 def _ptr(x):
@@ -160,6 +212,7 @@ def attn_fwd(q, k, v, out, lse, B: int, Hq: int, Hkv: int, S: int, D: int, scale
     pointers as ints; ``lse`` may be None.  ``stream`` defaults to PyTorch's
     current stream.  Raises AttnError on a non-zero code unless check=False.
     """
+    _fwd_sizes(q, k, v, out, lse, int(B), int(Hq), int(Hkv), int(S), int(D))
     rc = load().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), int(B), int(Hq),
                          int(Hkv), int(S), int(D), float(scale), 1 if causal else 0,
                          _stream(stream))
@@ -173,6 +226,8 @@ def attn_fwd_block_masked(q, k, v, out, lse, B: int, Hq: int, Hkv: int, S: int, 
                           check: bool = True) -> int:
     """The C entry point ``attn_fwd_block_masked``: ``block_mask`` is a uint8 CUDA
     tensor (or device pointer) [mask_heads, ceil(S/128), ceil(S/128)]."""
+    _fwd_sizes(q, k, v, out, lse, int(B), int(Hq), int(Hkv), int(S), int(D), block_mask=block_mask,
+               mask_heads=int(mask_heads))
     rc = load().attn_fwd_block_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), int(B),
                                       int(Hq), int(Hkv), int(S), int(D), float(scale),
                                       1 if causal else 0, _ptr(block_mask), int(mask_heads),
@@ -189,6 +244,8 @@ def attn_fwd_elem_masked(q, k, v, out, lse, B: int, Hq: int, Hkv: int, S: int, D
     """The C entry point ``attn_fwd_elem_masked``: ``keep_bits`` is a uint8 CUDA
     tensor (or device pointer) [keep_heads, S, 16*ceil(S/128)] of keep bits;
     ``block_mask`` optional as in ``attn_fwd_block_masked``."""
+    _fwd_sizes(q, k, v, out, lse, int(B), int(Hq), int(Hkv), int(S), int(D), block_mask=block_mask,
+               mask_heads=int(mask_heads), keep_bits=keep_bits, keep_heads=int(keep_heads))
     rc = load().attn_fwd_elem_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), int(B),
                                      int(Hq), int(Hkv), int(S), int(D), float(scale),
                                      1 if causal else 0, _ptr(keep_bits), int(keep_heads),
@@ -202,6 +259,7 @@ def attn_fwd_dropout(q, k, v, out, lse, B: int, Hq: int, Hkv: int, S: int, D: in
                      causal: bool | int, dropout_p: float, seed: int, offset: int, stream=None,
                      check: bool = True) -> int:
     """The C entry point ``attn_fwd_dropout`` (drop probability rounded to p8/256)."""
+    _fwd_sizes(q, k, v, out, lse, int(B), int(Hq), int(Hkv), int(S), int(D))
     rc = load().attn_fwd_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), int(B), int(Hq),
                                  int(Hkv), int(S), int(D), float(scale), 1 if causal else 0,
                                  float(dropout_p), int(seed) & (2**64 - 1), int(offset) & (2**64 - 1),
@@ -214,6 +272,9 @@ def attn_fwd_dropout(q, k, v, out, lse, B: int, Hq: int, Hkv: int, S: int, D: in
 def attn_out_proj(out, w, bias, y, B: int, H: int, S: int, D: int, E: int, stream=None,
                   check: bool = True) -> int:
     """The C entry point ``attn_out_proj``: Y = concat_heads(O) W^T + bias."""
+    B, H, S, D, E = int(B), int(H), int(S), int(D), int(E)
+    _sizes(("out", out, B * H * S * D * 2), ("w", w, E * H * D * 2), ("bias", bias, E * 4),
+           ("y", y, B * S * E * 2))
     rc = load().attn_out_proj(_ptr(out), _ptr(w), _ptr(bias), _ptr(y), int(B), int(H), int(S), int(D),
                               int(E), _stream(stream))
     if check and rc != ATTN_OK:
@@ -224,6 +285,7 @@ def attn_out_proj(out, w, bias, y, B: int, H: int, S: int, D: int, E: int, strea
 def attn_bwd(q, k, v, out, dout, lse, delta, dq, dk, dv, B: int, Hq: int, Hkv: int, S: int, D: int,
              scale: float, causal: bool | int, stream=None, check: bool = True) -> int:
     """The C entry point ``attn_bwd``: dQ, dK, dV (and delta) for upstream dO."""
+    _bwd_sizes(q, k, v, out, dout, lse, delta, dq, dk, dv, int(B), int(Hq), int(Hkv), int(S), int(D))
     rc = load().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(delta),
                          _ptr(dq), _ptr(dk), _ptr(dv), int(B), int(Hq), int(Hkv), int(S), int(D),
                          float(scale), 1 if causal else 0, _stream(stream))
@@ -236,6 +298,8 @@ def attn_bwd_block_masked(q, k, v, out, dout, lse, delta, dq, dk, dv, B: int, Hq
                           S: int, D: int, scale: float, causal: bool | int, block_mask, mask_heads: int,
                           stream=None, check: bool = True) -> int:
     """The C entry point ``attn_bwd_block_masked`` (the mask of the forward call)."""
+    _bwd_sizes(q, k, v, out, dout, lse, delta, dq, dk, dv, int(B), int(Hq), int(Hkv), int(S), int(D),
+               block_mask=block_mask, mask_heads=int(mask_heads))
     rc = load().attn_bwd_block_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse),
                                       _ptr(delta), _ptr(dq), _ptr(dk), _ptr(dv), int(B), int(Hq),
                                       int(Hkv), int(S), int(D), float(scale), 1 if causal else 0,
@@ -250,6 +314,9 @@ def attn_bwd_elem_masked(q, k, v, out, dout, lse, delta, dq, dk, dv, B: int, Hq:
                          keep_heads: int, block_mask=None, mask_heads: int = 1, stream=None,
                          check: bool = True) -> int:
     """The C entry point ``attn_bwd_elem_masked`` (masks as in ``attn_fwd_elem_masked``)."""
+    _bwd_sizes(q, k, v, out, dout, lse, delta, dq, dk, dv, int(B), int(Hq), int(Hkv), int(S), int(D),
+               block_mask=block_mask, mask_heads=int(mask_heads), keep_bits=keep_bits,
+               keep_heads=int(keep_heads))
     rc = load().attn_bwd_elem_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse),
                                      _ptr(delta), _ptr(dq), _ptr(dk), _ptr(dv), int(B), int(Hq),
                                      int(Hkv), int(S), int(D), float(scale), 1 if causal else 0,
@@ -264,6 +331,7 @@ def attn_bwd_dropout(q, k, v, out, dout, lse, delta, dq, dk, dv, B: int, Hq: int
                      D: int, scale: float, causal: bool | int, dropout_p: float, seed: int, offset: int,
                      stream=None, check: bool = True) -> int:
     """The C entry point ``attn_bwd_dropout`` (the dropout of the forward call)."""
+    _bwd_sizes(q, k, v, out, dout, lse, delta, dq, dk, dv, int(B), int(Hq), int(Hkv), int(S), int(D))
     rc = load().attn_bwd_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse),
                                  _ptr(delta), _ptr(dq), _ptr(dk), _ptr(dv), int(B), int(Hq), int(Hkv),
                                  int(S), int(D), float(scale), 1 if causal else 0, float(dropout_p),
@@ -276,6 +344,11 @@ def attn_bwd_dropout(q, k, v, out, dout, lse, delta, dq, dk, dv, B: int, Hq: int
 def attn_fwd_ex(q, k, v, out, lse, B: int, Hq: int, Hkv: int, S: int, D: int, scale: float,
                 causal: bool | int, opts: AttnOptions | None, stream=None, check: bool = True) -> int:
     """The C entry point ``attn_fwd_ex`` (``opts`` from ``options``, or None)."""
+    bm, kb = _opts_masks(opts)
+    _fwd_sizes(q, k, v, out, lse, int(B), int(Hq), int(Hkv), int(S), int(D),
+               in_bytes=1 if opts is not None and opts.input_format == ATTN_INPUT_E4M3 else 2,
+               block_mask=bm, mask_heads=opts.mask_heads if bm is not None else 1,
+               keep_bits=kb, keep_heads=opts.keep_heads if kb is not None else 1)
     rc = load().attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), int(B), int(Hq), int(Hkv),
                             int(S), int(D), float(scale), 1 if causal else 0,
                             None if opts is None else ctypes.byref(opts), _stream(stream))
@@ -288,6 +361,10 @@ def attn_bwd_ex(q, k, v, out, dout, lse, delta, dq, dk, dv, B: int, Hq: int, Hkv
                 scale: float, causal: bool | int, opts: AttnOptions | None, stream=None,
                 check: bool = True) -> int:
     """The C entry point ``attn_bwd_ex`` (``opts`` as given to ``attn_fwd_ex``)."""
+    bm, kb = _opts_masks(opts)
+    _bwd_sizes(q, k, v, out, dout, lse, delta, dq, dk, dv, int(B), int(Hq), int(Hkv), int(S), int(D),
+               block_mask=bm, mask_heads=opts.mask_heads if bm is not None else 1,
+               keep_bits=kb, keep_heads=opts.keep_heads if kb is not None else 1)
     rc = load().attn_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(delta),
                             _ptr(dq), _ptr(dk), _ptr(dv), int(B), int(Hq), int(Hkv), int(S), int(D),
                             float(scale), 1 if causal else 0, None if opts is None else ctypes.byref(opts),
@@ -302,6 +379,7 @@ def attn_fwd_fp8(q, k, v, q_descale: float, k_descale: float, v_descale: float, 
                  check: bool = True) -> int:
     """The C entry point ``attn_fwd_fp8`` (E4M3 inputs with per-tensor descales),
     same argument order; tensors or raw device pointers as in ``attn_fwd``."""
+    _fwd_sizes(q, k, v, out, lse, int(B), int(Hq), int(Hkv), int(S), int(D), in_bytes=1)
     rc = load().attn_fwd_fp8(_ptr(q), _ptr(k), _ptr(v), float(q_descale), float(k_descale),
                              float(v_descale), _ptr(out), _ptr(lse), int(B), int(Hq), int(Hkv),
                              int(S), int(D), float(scale), 1 if causal else 0, _stream(stream))

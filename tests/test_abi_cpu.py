@@ -358,3 +358,87 @@ def test_masked_bwd_rejects_bad_masks_before_launch():
     assert lib.attn_bwd_block_masked(*args, None, 1, None) == ATTN_ERR_INVALID_ARG
     assert lib.attn_bwd_block_masked(*args, 11 << 40, 3, None) == ATTN_ERR_INVALID_ARG
     assert lib.attn_bwd_block_masked(*args[:14], 96, *args[15:], 11 << 40, 1, None) == ATTN_ERR_UNSUPPORTED
+
+
+def _size_cases():
+    """(name, call, tensors) per Python wrapper: host tensors of exactly the sizes
+    that B=1, Hq=4, Hkv=2, S=130, D=64 (E=64) imply."""
+    import torch
+    B, Hq, Hkv, S, D, E = 1, 4, 2, 130, 64, 64
+    nt = 2
+    bf, u8, f32 = torch.bfloat16, torch.uint8, torch.float32
+    qs, kvs = (B, Hq, S, D), (B, Hkv, S, D)
+
+    def fwd(in_dtype=bf):
+        return dict(q=torch.zeros(qs, dtype=in_dtype), k=torch.zeros(kvs, dtype=in_dtype),
+                    v=torch.zeros(kvs, dtype=in_dtype), out=torch.zeros(qs, dtype=bf),
+                    lse=torch.zeros((B, Hq, S), dtype=f32))
+
+    def bwd():
+        t = fwd()
+        t.update(dout=torch.zeros(qs, dtype=bf), delta=torch.zeros((B, Hq, S), dtype=f32),
+                 dq=torch.zeros(qs, dtype=bf), dk=torch.zeros(kvs, dtype=bf), dv=torch.zeros(kvs, dtype=bf))
+        return t
+
+    bm = lambda: torch.zeros((Hq, nt, nt), dtype=u8)  # noqa: E731
+    kb = lambda: torch.zeros((1, S, 16 * nt), dtype=u8)  # noqa: E731
+    dims = (B, Hq, Hkv, S, D, 0.125, True)
+    F = ("q", "k", "v", "out", "lse")
+    G = ("q", "k", "v", "out", "dout", "lse", "delta", "dq", "dk", "dv")
+
+    def opts_with(t):
+        o = native.options()
+        o.tensors = (t.get("block_mask"), t.get("keep_bits"))
+        if "block_mask" in t:
+            o.block_mask, o.mask_heads = t["block_mask"].data_ptr(), Hq
+        if "keep_bits" in t:
+            o.keep_bits, o.keep_heads = t["keep_bits"].data_ptr(), 1
+        return o
+
+    cases = [
+        ("attn_fwd", lambda t: native.attn_fwd(*(t[n] for n in F), *dims, stream=0), fwd()),
+        ("attn_fwd_fp8", lambda t: native.attn_fwd_fp8(t["q"], t["k"], t["v"], 1.0, 1.0, 1.0, t["out"], t["lse"],
+                                                       *dims, stream=0), fwd(u8)),
+        ("attn_fwd_block_masked", lambda t: native.attn_fwd_block_masked(*(t[n] for n in F), *dims,
+                                                                         t["block_mask"], Hq, stream=0),
+         dict(fwd(), block_mask=bm())),
+        ("attn_fwd_elem_masked", lambda t: native.attn_fwd_elem_masked(*(t[n] for n in F), *dims, t["keep_bits"], 1,
+                                                                       t["block_mask"], Hq, stream=0),
+         dict(fwd(), keep_bits=kb(), block_mask=bm())),
+        ("attn_fwd_dropout", lambda t: native.attn_fwd_dropout(*(t[n] for n in F), *dims, 0.1, 1, 2, stream=0),
+         fwd()),
+        ("attn_fwd_ex", lambda t: native.attn_fwd_ex(*(t[n] for n in F), *dims, opts_with(t), stream=0),
+         dict(fwd(), keep_bits=kb(), block_mask=bm())),
+        ("attn_bwd", lambda t: native.attn_bwd(*(t[n] for n in G), *dims, stream=0), bwd()),
+        ("attn_bwd_block_masked", lambda t: native.attn_bwd_block_masked(*(t[n] for n in G), *dims,
+                                                                         t["block_mask"], Hq, stream=0),
+         dict(bwd(), block_mask=bm())),
+        ("attn_bwd_elem_masked", lambda t: native.attn_bwd_elem_masked(*(t[n] for n in G), *dims, t["keep_bits"], 1,
+                                                                       t["block_mask"], Hq, stream=0),
+         dict(bwd(), keep_bits=kb(), block_mask=bm())),
+        ("attn_bwd_dropout", lambda t: native.attn_bwd_dropout(*(t[n] for n in G), *dims, 0.1, 1, 2, stream=0),
+         bwd()),
+        ("attn_bwd_ex", lambda t: native.attn_bwd_ex(*(t[n] for n in G), *dims, opts_with(t), stream=0),
+         dict(bwd(), keep_bits=kb(), block_mask=bm())),
+        ("attn_out_proj", lambda t: native.attn_out_proj(t["out"], t["w"], t["bias"], t["y"], B, Hq, S, D, E,
+                                                         stream=0),
+         dict(out=torch.zeros(qs, dtype=bf), w=torch.zeros((E, Hq * D), dtype=bf), bias=torch.zeros(E, dtype=f32),
+              y=torch.zeros((B, S, E), dtype=bf))),
+    ]
+    return cases
+
+
+@pytest.mark.parametrize("case", range(12), ids=lambda i: _size_cases()[i][0])
+def test_python_binding_checks_tensor_sizes(case):
+    """Every wrapper checks, before it passes an address on, that each tensor
+    holds the bytes its sizes imply (the C entry points cannot): exactly sized
+    host tensors pass that check and are then refused as host memory; any one
+    argument one element short is refused by name as too small."""
+    name, call, tensors = _size_cases()[case]
+    with pytest.raises(ValueError, match="CUDA device memory"):
+        call(tensors)
+    for arg in tensors:
+        short = dict(tensors)
+        short[arg] = tensors[arg].reshape(-1)[:-1].clone()
+        with pytest.raises(ValueError, match=f"^{arg} holds"):
+            call(short)

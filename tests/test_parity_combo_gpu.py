@@ -101,7 +101,7 @@ def _bwd_ex(q, k, v, do, scale, causal, bm, p, kb=None):
     qd, kd, vd, dod = to_device(q), to_device(k), to_device(v), to_device(do)
     out = torch.empty_like(qd)
     lse = torch.empty((B, Hq, S), dtype=torch.float32, device="cuda")
-    bmd, kbd = _dev(bm), _dev(kb)  # held here: the options keep only their addresses
+    bmd, kbd = _dev(bm), _dev(kb)
     opts = native.options(block_mask=bmd, keep_bits=kbd, dropout_p=p, seed=SEED, offset=OFFSET)
     native.attn_fwd_ex(qd, kd, vd, out, lse, B, Hq, Hkv, S, D, scale, causal, opts)
     dq, dk, dv = (torch.full_like(t, float("nan")) for t in (qd, kd, vd))
