@@ -98,6 +98,10 @@ def test_python_binding_rejects_host_tensors():
         native.attn_fwd(q, q, q, q, None, 1, 1, 1, 8, 64, 0.125, True, stream=0)
     with pytest.raises(ValueError):
         native.attention(q, q, q)
+    with pytest.raises(ValueError, match="CUDA"):
+        native.attention_trainable(q, q, q)
+    with pytest.raises(ValueError, match="bf16"):
+        native.attention_trainable(q.float(), q, q)
 
 
 def test_selftest_rejects_bad_limits():
