@@ -11,6 +11,7 @@ query, so it needs no ``-lcuda`` at link time.
 from __future__ import annotations
 
 import argparse
+import concurrent.futures
 import glob
 import os
 import shutil
@@ -54,27 +55,47 @@ def is_stale() -> bool:
     return any(os.path.getmtime(f) > t for f in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False) -> str:
-    """Compile every .cu under csrc/ into one shared library; returns its path."""
-    if not force and not is_stale():
-        return LIBRARY
-    os.makedirs(BUILD_DIR, exist_ok=True)
-    nvcc = _nvcc()
-    cuda_lib = os.path.join(_cuda_home(nvcc), "lib64")
-    tmp = LIBRARY + f".tmp{os.getpid()}"
-    cmd = [nvcc, ARCH, "-O3", "-lineinfo", "-std=c++17", "-shared", "-Xcompiler", "-fPIC",
-           "-cudart", "shared", f"-I{INCLUDE}", "-Xlinker", f"-rpath,{cuda_lib}",
-           "-o", tmp] + sources()
-    if ptxas_verbose:
-        cmd.insert(1, "-Xptxas=-v")
+def _run(cmd: list[str], verbose: bool) -> subprocess.CompletedProcess:
     if verbose:
         print(" ".join(cmd), flush=True)
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"nvcc failed ({res.returncode}):\n{res.stdout}\n{res.stderr}")
-    if verbose or ptxas_verbose:
-        sys.stdout.write(res.stdout + res.stderr)
-    os.replace(tmp, LIBRARY)
+    return res
+
+
+def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False) -> str:
+    """Compile every .cu under csrc/ into one shared library; returns its path.
+
+    Each source is its own translation unit (no device code is shared across
+    them), so they compile in parallel to objects and are linked once."""
+    if not force and not is_stale():
+        return LIBRARY
+    os.makedirs(BUILD_DIR, exist_ok=True)
+    nvcc = _nvcc()
+    cuda_lib = os.path.join(_cuda_home(nvcc), "lib64")
+    tmp_dir = os.path.join(BUILD_DIR, f"obj.tmp{os.getpid()}")
+    os.makedirs(tmp_dir, exist_ok=True)
+    tmp = LIBRARY + f".tmp{os.getpid()}"
+    flags = [ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", f"-I{INCLUDE}"]
+    if ptxas_verbose:
+        flags.insert(0, "-Xptxas=-v")
+    try:
+        srcs = sources()
+        objs = [os.path.join(tmp_dir, os.path.basename(f)[:-3] + ".o") for f in srcs]
+        with concurrent.futures.ThreadPoolExecutor(max_workers=len(srcs)) as pool:
+            outs = list(pool.map(lambda so: _run([nvcc, *flags, "-c", so[0], "-o", so[1]], verbose),
+                                 zip(srcs, objs)))
+        _run([nvcc, ARCH, "-shared", "-cudart", "shared", "-Xlinker", f"-rpath,{cuda_lib}", "-o", tmp, *objs],
+             verbose)
+        if verbose or ptxas_verbose:
+            for res in outs:
+                sys.stdout.write(res.stdout + res.stderr)
+        os.replace(tmp, LIBRARY)
+    finally:
+        shutil.rmtree(tmp_dir, ignore_errors=True)
+        if os.path.exists(tmp):
+            os.remove(tmp)
     return LIBRARY
 
 
