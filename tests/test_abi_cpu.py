@@ -446,3 +446,19 @@ def test_python_binding_checks_tensor_sizes(case):
         short[arg] = tensors[arg].reshape(-1)[:-1].clone()
         with pytest.raises(ValueError, match=f"^{arg} holds"):
             call(short)
+
+
+def test_binding_fails_loudly_without_its_library(monkeypatch):
+    """With no library loaded and none that can be built, every entry point
+    raises: there is no other path to fall back on."""
+    def no_build(*args, **kwargs):
+        raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libattn")
+
+    monkeypatch.setattr(native, "_lib", None)
+    monkeypatch.setattr(native._build, "build", no_build)
+    with pytest.raises(RuntimeError, match="nvcc"):
+        native.load()
+    with pytest.raises(RuntimeError, match="nvcc"):
+        native.attn_version()
+    with pytest.raises(RuntimeError, match="nvcc"):
+        native.attn_fwd(None, None, None, None, None, 1, 1, 1, 8, 64, 0.125, True, stream=0)
