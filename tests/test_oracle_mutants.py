@@ -70,6 +70,15 @@ MUTANTS = {
     "keep_ignored": ("if (J->keep_bits) {", "if (0) {"),
     "bwd_dropout_dv_undropped": ("wij = dropout_keeps(J, bh, i, j) ? pij * (256.0 / (256.0 - (double)J->dropout_p8)) : 0.0;",
                                  "wij = pij;"),
+    "ex_descales_ignored": ("format == FMT_E4M3 ? ds : one", "one"),
+    "ex_mask_heads_collapsed": ("causal, block_mask, block_mask ? mask_heads : 1, keep_bits,\n",
+                                "causal, block_mask, 1, keep_bits,\n"),
+    "ex_dropout_dropped": ("keep_bits ? keep_heads : 1, p8, seed, offset, rows,",
+                           "keep_bits ? keep_heads : 1, 0, seed, offset, rows,"),
+    "ex_bwd_keep_dropped": ("keep_bits, keep_bits ? keep_heads : 1, p8, seed, offset,",
+                            "NULL, 1, p8, seed, offset,"),
+    "ex_bwd_seed_offset_swapped": ("keep_heads : 1, p8, seed, offset,\n                   kv_heads",
+                                   "keep_heads : 1, p8, offset, seed,\n                   kv_heads"),
     "bwd_dropout_dp_unscaled": ("if (p[j] != 0.0) dP[j] = dropout_keeps(J, bh, i, j) ? dP[j] * keep_scale : 0.0;",
                                 "if (p[j] != 0.0) dP[j] = dropout_keeps(J, bh, i, j) ? dP[j] : 0.0;"),
 }
@@ -107,6 +116,14 @@ def test_some_pin_catches_mutant(name, tmp_path):
     def fwd64(q, k, v, scale, causal):
         return oracle.attention_f64(q, k, v, scale, causal, nthreads=1, lib=lib)
 
+    def attnx(q, k, v, scale, causal, descales=None, block_mask=None, keep_bits=None, dropout=None):
+        return oracle.attention_ex(q, k, v, scale, causal, descales=descales, block_mask=block_mask,
+                                   keep_bits=keep_bits, dropout=dropout, lib=lib)
+
+    def bwdx(q, k, v, dout, scale, causal, block_mask, keep_bits, dropout):
+        return oracle.attention_bwd(q, k, v, dout, scale, causal, block_mask=block_mask, keep_bits=keep_bits,
+                                    dropout=dropout, lib=lib)
+
     checks = [(p.__name__, lambda p=p: p(attn)) for p in oracle_pins.ALL_PINS] + [
         ("pin_e4m3_decode", lambda: oracle_pins.pin_e4m3_decode(
             lambda c: oracle.e4m3_decode(c, lib=lib))),
@@ -127,7 +144,8 @@ def test_some_pin_catches_mutant(name, tmp_path):
             lambda q, k, v, d, sc, c, b: oracle.attention_bwd(q, k, v, d, sc, c, keep_bits=b, lib=lib))),
         ("pin_bwd_dropout_autograd", lambda: oracle_pins.pin_bwd_dropout_autograd(
             lambda q, k, v, d, sc, c, dr: oracle.attention_bwd(q, k, v, d, sc, c, dropout=dr, lib=lib))),
-    ]
+    ] + [(p.__name__, lambda p=p: p(attnx)) for p in oracle_pins.COMBO_PINS] + [
+        (p.__name__, lambda p=p: p(bwdx)) for p in oracle_pins.BWD_COMBO_PINS]
     caught = []
     for pin_name, run in checks:
         try:
