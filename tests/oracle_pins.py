@@ -550,8 +550,9 @@ def pin_philox_library(philox):
 def pin_dropout_mask_closed_form(attnd, attn):
     """V = identity rows turns O rows into the weights: with dropout each must be
     the undropped weight times keep(i, j) * 256/(256-p8), keep from the
-    documented byte mapping over numpy's Philox; the LSE is unchanged."""
-    B, H, S, D = 1, 2, 70, 128
+    documented byte mapping over numpy's Philox (counter word 2 = b * H + h, so
+    two batches draw different decisions); the LSE is unchanged."""
+    B, H, S, D = 2, 2, 70, 128
     q, k = _rand((B, H, S, D), 201, 0), _rand((B, H, S, D), 201, 1)
     v = bits(np.broadcast_to(np.eye(S, D), (B, H, S, D)))
     p8, seed, offset = 77, 0x1234abcd, 99
@@ -559,10 +560,11 @@ def pin_dropout_mask_closed_form(attnd, attn):
         O, L = attnd(q, k, v, 0.2, p8, seed, offset, causal)
         P, L0 = attn(q, k, v, 0.2, causal)
         assert np.array_equal(L, L0), "dropout changed the LSE"
-        for h in range(H):
-            keep = keep_table(h, S, p8, seed, offset)
-            want = P[0, h, :, :S] * keep * (256.0 / (256 - p8))
-            assert np.max(np.abs(O[0, h, :, :S] - want)) < 1e-15
+        for b in range(B):
+            for h in range(H):
+                keep = keep_table(b * H + h, S, p8, seed, offset)
+                want = P[b, h, :, :S] * keep * (256.0 / (256 - p8))
+                assert np.max(np.abs(O[b, h, :, :S] - want)) < 1e-15
 
 
 def pin_dropout_rate_and_identity(attnd, attn):
@@ -796,14 +798,16 @@ def pin_bwd_dropout_autograd(bwdd):
     """Gradients with dropout against torch's float64 autograd of
     O = ((softmax of the masked scores) * Z * 256/(256-p8)) V, Z the keep table
     written from the documented byte mapping over numpy's Philox; and p8 = 0
-    gives the gradients without dropout bit for bit."""
-    B, Hq, Hkv, S, D = 1, 4, 2, 70, 8
+    gives the gradients without dropout bit for bit.  Two batches, so the keep
+    table's counter carries the flat batch * head index."""
+    B, Hq, Hkv, S, D = 2, 4, 2, 70, 8
     q, k, v = (_rand((B, H, S, D), 261, t) for t, H in ((0, Hq), (1, Hkv), (2, Hkv)))
     dout = _rand((B, Hq, S, D), 261, 3)
     G = Hq // Hkv
     p8, seed, offset = 51, 0xBEEF, 7
     s = 256.0 / (256 - p8)
-    Z = torch.from_numpy(np.stack([keep_table(h, S, p8, seed, offset) for h in range(Hq)])[None].astype(np.float64))
+    Z = torch.from_numpy(np.stack([np.stack([keep_table(b * Hq + h, S, p8, seed, offset) for h in range(Hq)])
+                                   for b in range(B)]).astype(np.float64))
     for causal in (True, False):
         dq, dk, dv, delta = bwdd(q, k, v, dout, 0.4, causal, (p8, seed, offset))
         tq, tk, tv = (torch.from_numpy(f64(x)).requires_grad_() for x in (q, k, v))

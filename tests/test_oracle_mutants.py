@@ -79,6 +79,10 @@ MUTANTS = {
                             "NULL, 1, p8, seed, offset,"),
     "ex_bwd_seed_offset_swapped": ("keep_heads : 1, p8, seed, offset,\n                   kv_heads",
                                    "keep_heads : 1, p8, offset, seed,\n                   kv_heads"),
+    "dropout_counter_batch_dropped": ("s[j] = dropout_keeps(J, r / S, i, j) ? s[j] * keep_scale : 0.0;",
+                                      "s[j] = dropout_keeps(J, (r / S) % J->Hq, i, j) ? s[j] * keep_scale : 0.0;"),
+    "bwd_dropout_counter_batch_dropped": ("wij = dropout_keeps(J, bh, i, j) ?",
+                                          "wij = dropout_keeps(J, bh % J->Hq, i, j) ?"),
     "bwd_dropout_dp_unscaled": ("if (p[j] != 0.0) dP[j] = dropout_keeps(J, bh, i, j) ? dP[j] * keep_scale : 0.0;",
                                 "if (p[j] != 0.0) dP[j] = dropout_keeps(J, bh, i, j) ? dP[j] : 0.0;"),
 }
