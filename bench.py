@@ -23,7 +23,9 @@ attention output shape, E = Hq*D output features, FLOPs = 2*B*S*E*Hq*D.  Between
 steps a 256 MiB buffer is written to flush L2; each step is timed with CUDA
 events on the launching stream.  Under torchrun every rank runs the same
 workload on its own GPU (independent problems, no collective on the data
-path); rank 0 prints one JSON line with the slowest rank's time.
+path); rank 0 prints one JSON line with the slowest rank's time: the mean
+step (ms_per_step, from which value is computed) and the median and minimum
+step (ms_step_median, ms_step_min).
 """
 from __future__ import annotations
 
@@ -161,6 +163,13 @@ def reduce_max(value: float, world: int) -> float:
     t = torch.tensor([value], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def step_stats(per_step_ms, world: int) -> dict:
+    """Median and minimum of the timed steps' CUDA-event times (the slowest rank's,
+    as for ms_per_step); every rank must call it."""
+    return {"ms_step_median": reduce_max(float(np.median(per_step_ms)), world),
+            "ms_step_min": reduce_max(float(np.min(per_step_ms)), world)}
 
 
 def barrier(world: int):
@@ -518,6 +527,7 @@ def run_ours(args, w, rank, world, local):
     per_step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms_local = float(np.mean(per_step_ms))
     ms = reduce_max(ms_local, world)
+    stats = step_stats(per_step_ms, world)
     value = world * flops / (ms * 1e-3) / 1e12
 
     # End to end: every step copies its Q, K, V from pinned host buffers, runs
@@ -595,7 +605,7 @@ def run_ours(args, w, rank, world, local):
                          f"{dt:.1f} s; fp64 C oracle"}
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, **stats,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "fp8 (e4m3 inputs, bf16 output)" if fp8 else "bf16",
         "data": f"synthetic (seeded N(0,1) {'e4m3' if fp8 else 'bf16'}, no weights)",
@@ -708,8 +718,10 @@ def run_ours_bwd(args, w, rank, world, local):
         wall = time.perf_counter() - wall0
     barrier(world)
     native.attn_sync_status(stream)
-    ms_local = float(np.mean([a.elapsed_time(b) for a, b in zip(starts, ends)]))
+    per_step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    ms_local = float(np.mean(per_step_ms))
     ms = reduce_max(ms_local, world)
+    stats = step_stats(per_step_ms, world)
     value = world * flops / (ms * 1e-3) / 1e12
 
     # End to end: Q, K, V, O, dO, LSE from pinned host buffers, dQ, dK, dV back.
@@ -756,7 +768,7 @@ def run_ours_bwd(args, w, rank, world, local):
                          f"{dt:.1f} s; fp64 C oracle"}
     line = {
         "metric": BWD_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, **stats,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16 Q, K, V, dO; no weights)",
         "config": {"workload": w.name, **w.shape_dict, "causal": w.causal, "inputs": "bf16",
@@ -836,8 +848,10 @@ def run_ours_proj(args, w, rank, world, local):
         wall = time.perf_counter() - wall0
     barrier(world)
     native.attn_sync_status(stream)
-    ms_local = float(np.mean([a.elapsed_time(b) for a, b in zip(starts, ends)]))
+    per_step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    ms_local = float(np.mean(per_step_ms))
     ms = reduce_max(ms_local, world)
+    stats = step_stats(per_step_ms, world)
     value = world * flops / (ms * 1e-3) / 1e12
 
     yh = torch.empty(y.shape, dtype=y.dtype).pin_memory()
@@ -878,7 +892,7 @@ def run_ours_proj(args, w, rank, world, local):
                          f"entries), {dt:.1f} s; float64 numpy matmul"}
     line = {
         "metric": PROJ_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, **stats,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16 attention output, N(0, 1/(H*D)) weights; no trained weights)",
         "config": {"workload": w.name, **w.shape_dict, "E": E, "inputs": "bf16", "pass": "proj",

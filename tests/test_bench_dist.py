@@ -29,7 +29,9 @@ def _worker(rank, world, port, out):
     try:
         bench.barrier(world)
         got = bench.reduce_max(1.5 + rank, world)  # ranks report 1.5 and 2.5 ms
-        out[rank] = got
+        # per-step times: rank 0 [1, 3, 2] (median 2, min 1), rank 1 [4, 0.5, 5] (median 4, min 0.5)
+        stats = bench.step_stats([1.0, 3.0, 2.0] if rank == 0 else [4.0, 0.5, 5.0], world)
+        out[rank] = (got, stats["ms_step_median"], stats["ms_step_min"])
         bench.barrier(world)
     finally:
         dist.destroy_process_group()
@@ -45,7 +47,7 @@ def test_reduce_max_over_two_gloo_ranks():
     for p in procs:
         p.join(120)
         assert p.exitcode == 0
-    assert dict(out) == {0: 2.5, 1: 2.5}
+    assert dict(out) == {0: (2.5, 4.0, 1.0), 1: (2.5, 4.0, 1.0)}  # the slowest rank's figures
 
 
 def test_reference_arm_under_torchrun_two_ranks():
