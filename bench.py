@@ -35,6 +35,8 @@ import hashlib
 import io
 import json
 import os
+import platform
+import re
 import subprocess
 import sys
 import time
@@ -163,6 +165,25 @@ def reduce_max(value: float, world: int) -> float:
     t = torch.tensor([value], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def host_cpu(cpuinfo: str = "/proc/cpuinfo") -> str:
+    """The host CPU as the kernel names it (x86: the model name; Arm: implementer
+    and part codes), for the CPU baseline; never raises."""
+    machine = platform.machine() or "unknown"
+    try:
+        with open(cpuinfo) as f:
+            info = f.read()
+    except OSError:
+        return machine
+    name = re.search(r"^model name\s*:\s*(.+)$", info, re.M)
+    if name:
+        return f"{machine} {name.group(1).strip()}"
+    impl = re.search(r"^CPU implementer\s*:\s*(\S+)", info, re.M)
+    part = re.search(r"^CPU part\s*:\s*(\S+)", info, re.M)
+    if impl and part:
+        return f"{machine} implementer {impl.group(1)} part {part.group(1)}"
+    return machine
 
 
 def step_stats(per_step_ms, world: int) -> dict:
@@ -440,7 +461,7 @@ def run_reference(args, w, rank, world):
                    **mask_config(mask, args.mask_density), **window_config(w, args.window),
                    **({"dropout_p": dropout_p8(args) / 256, "dropout_key": [DROPOUT_SEED, DROPOUT_OFFSET]}
                       if args.dropout is not None else {})},
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": timer.threads,
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": timer.threads, "cpu": host_cpu(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
@@ -600,7 +621,7 @@ def run_ours(args, w, rank, world, local):
     if not args.no_cpu_baseline and world == 1:
         timer = OracleTimer(w, fp8=fp8, mask=mask, dropout_p8=dropout_p8(args), window=args.window)
         tf, n, dt = timer.sample(args.cpu_seconds, seed=7)
-        cpu = {"value": tf, "unit": "TFLOP/s", "cores": timer.threads, "kind": "oracle",
+        cpu = {"value": tf, "unit": "TFLOP/s", "cores": timer.threads, "cpu": host_cpu(), "kind": "oracle",
                "sample": f"{n} random query rows of {w.name} (of {timer.total}), "
                          f"{dt:.1f} s; fp64 C oracle"}
     line = {
@@ -763,7 +784,7 @@ def run_ours_bwd(args, w, rank, world, local):
     if not args.no_cpu_baseline and world == 1:
         timer = OracleBwdTimer(w, mask=mask, window=args.window, dropout_p8=dropout_p8(args))
         tf, n, dt = timer.sample(args.cpu_seconds, seed=7)
-        cpu = {"value": tf, "unit": "TFLOP/s", "cores": timer.threads, "kind": "oracle",
+        cpu = {"value": tf, "unit": "TFLOP/s", "cores": timer.threads, "cpu": host_cpu(), "kind": "oracle",
                "sample": f"gradients of {n} random key/value heads of {w.name} (of {timer.total}), "
                          f"{dt:.1f} s; fp64 C oracle"}
     line = {
@@ -887,7 +908,7 @@ def run_ours_proj(args, w, rank, world, local):
     if not args.no_cpu_baseline and world == 1:
         timer = OracleProjTimer(w)
         tf, n, dt = timer.sample(args.cpu_seconds, seed=7)
-        cpu = {"value": tf, "unit": "TFLOP/s", "cores": timer.threads, "kind": "oracle",
+        cpu = {"value": tf, "unit": "TFLOP/s", "cores": timer.threads, "cpu": host_cpu(), "kind": "oracle",
                "sample": f"{n} random sequence positions of {w.name} (of {timer.total}, all batch "
                          f"entries), {dt:.1f} s; float64 numpy matmul"}
     line = {

@@ -23,3 +23,15 @@ def test_all_ones_mask_counts_every_visible_pair():
     m = np.ones((1, 8, 8), np.uint8)
     assert np.array_equal(bench.visible_keys(m, S, True)[0], np.arange(1, S + 1))
     assert np.all(bench.visible_keys(m, S, False)[0] == S)
+
+
+def test_host_cpu_names_x86_and_arm_hosts(tmp_path):
+    import bench
+    x86 = tmp_path / "x86"
+    x86.write_text("processor\t: 0\nvendor_id\t: GenuineIntel\nmodel name\t: Some Xeon @ 2.70GHz\n")
+    assert bench.host_cpu(str(x86)).endswith("Some Xeon @ 2.70GHz")
+    arm = tmp_path / "arm"
+    arm.write_text("processor\t: 0\nBogoMIPS\t: 2000.00\nCPU implementer\t: 0x41\nCPU architecture: 8\n"
+                   "CPU variant\t: 0x0\nCPU part\t: 0xd4f\nCPU revision\t: 0\n")
+    assert bench.host_cpu(str(arm)).endswith("implementer 0x41 part 0xd4f")
+    assert bench.host_cpu(str(tmp_path / "missing")) != ""
