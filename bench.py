@@ -18,6 +18,7 @@ from attn_fwd beforehand) and FLOPs = 2.5x the forward's (five products per
 tile pair instead of two: the usual convention for attention backward);
 --mask-density, --window and --dropout select the matching backward entry
 points (attn_bwd_block_masked, attn_bwd_elem_masked, attn_bwd_dropout).
+--window with --dropout runs both in one call (attn_fwd_ex / attn_bwd_ex).
 With --pass proj the step is one attn_out_proj call on the workload's
 attention output shape, E = Hq*D output features, FLOPs = 2*B*S*E*Hq*D.  Between timed
 steps a 256 MiB buffer is written to flush L2; each step is timed with CUDA
@@ -267,7 +268,11 @@ class OracleTimer:
 
     def run(self, n, seed):
         rows = np.random.default_rng(seed).integers(0, self.total, n)
-        if self.window is not None:
+        if self.window is not None and self.p8:
+            self.oracle.attention_ex(self.q, self.k, self.v, self.w.scale, self.w.causal, block_mask=self.bm,
+                                     keep_bits=self.bits, dropout=(self.p8, DROPOUT_SEED, DROPOUT_OFFSET),
+                                     rows=rows, nthreads=self.threads)
+        elif self.window is not None:
             self.oracle.attention_keep(self.q, self.k, self.v, self.w.scale, self.bits, self.w.causal,
                                        block_mask=self.bm, rows=rows, nthreads=self.threads)
         elif self.mask is not None:
@@ -497,6 +502,9 @@ def run_ours(args, w, rank, world, local):
         keep_bits, keep_block = workload_window(w, args.window)
         flops = 4.0 * w.D * w.B * w.Hq * float(window_keys(w.S, args.window).sum())
         keep_d, keep_block_d = torch.from_numpy(keep_bits).to(dev), torch.from_numpy(keep_block).to(dev)
+        if args.dropout is not None:  # the window with dropout: one attn_fwd_ex call
+            combo = native.options(block_mask=keep_block_d, keep_bits=keep_d, dropout_p=args.dropout,
+                                   seed=DROPOUT_SEED, offset=DROPOUT_OFFSET)
     out = torch.empty((w.B, w.Hq, w.S, w.D), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((w.B, w.Hq, w.S), dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -509,6 +517,9 @@ def run_ours(args, w, rank, world, local):
         elif mask is not None:
             native.attn_fwd_block_masked(q, k, v, out, lse, w.B, w.Hq, w.Hkv, w.S, w.D, w.scale,
                                          w.causal, mask_d, mask.shape[0], stream)
+        elif args.window is not None and args.dropout is not None:
+            native.attn_fwd_ex(q, k, v, out, lse, w.B, w.Hq, w.Hkv, w.S, w.D, w.scale, w.causal, combo,
+                               stream)
         elif args.window is not None:
             native.attn_fwd_elem_masked(q, k, v, out, lse, w.B, w.Hq, w.Hkv, w.S, w.D, w.scale,
                                         w.causal, keep_d, 1, keep_block_d, 1, stream)
@@ -685,8 +696,13 @@ def run_ours_bwd(args, w, rank, world, local):
     elif args.window is not None:
         keep_bits, keep_block = workload_window(w, args.window)
         keep_d, keep_block_d = torch.from_numpy(keep_bits).to(dev), torch.from_numpy(keep_block).to(dev)
-        native.attn_fwd_elem_masked(q, k, v, out, lse, w.B, w.Hq, w.Hkv, w.S, w.D, w.scale, w.causal,
-                                    keep_d, 1, keep_block_d, 1, stream)
+        if args.dropout is not None:  # the window with dropout: attn_fwd_ex / attn_bwd_ex
+            combo = native.options(block_mask=keep_block_d, keep_bits=keep_d, dropout_p=args.dropout,
+                                   seed=DROPOUT_SEED, offset=DROPOUT_OFFSET)
+            native.attn_fwd_ex(q, k, v, out, lse, w.B, w.Hq, w.Hkv, w.S, w.D, w.scale, w.causal, combo, stream)
+        else:
+            native.attn_fwd_elem_masked(q, k, v, out, lse, w.B, w.Hq, w.Hkv, w.S, w.D, w.scale, w.causal,
+                                        keep_d, 1, keep_block_d, 1, stream)
     elif args.dropout is not None:
         native.attn_fwd_dropout(q, k, v, out, lse, w.B, w.Hq, w.Hkv, w.S, w.D, w.scale, w.causal,
                                 args.dropout, DROPOUT_SEED, DROPOUT_OFFSET, stream)
@@ -706,6 +722,9 @@ def run_ours_bwd(args, w, rank, world, local):
         if mask is not None:
             native.attn_bwd_block_masked(q, k, v, out, do, lse, delta, dq, dk, dv, w.B, w.Hq, w.Hkv,
                                          w.S, w.D, w.scale, w.causal, mask_d, mask.shape[0], stream)
+        elif args.window is not None and args.dropout is not None:
+            native.attn_bwd_ex(q, k, v, out, do, lse, delta, dq, dk, dv, w.B, w.Hq, w.Hkv, w.S, w.D,
+                               w.scale, w.causal, combo, stream)
         elif args.window is not None:
             native.attn_bwd_elem_masked(q, k, v, out, do, lse, delta, dq, dk, dv, w.B, w.Hq, w.Hkv,
                                         w.S, w.D, w.scale, w.causal, keep_d, 1, keep_block_d, 1, stream)
@@ -977,8 +996,8 @@ def main():
                                      or not 0 < round(args.dropout * 256) < 256):
         ap.error("--dropout takes 0 < p < 1 (at least 1/256), bf16 forward or backward, no mask")
     if args.window is not None and (args.window < 1 or args.pass_ == "proj" or args.dtype != "bf16"
-                                    or args.mask_density is not None or args.dropout is not None):
-        ap.error("--window takes a positive key count, bf16 forward or backward, no other mask or dropout")
+                                    or args.mask_density is not None):
+        ap.error("--window takes a positive key count, bf16 forward or backward, no other mask")
     w = BY_NAME[args.workload]
     rank, world, local = dist_init(args)
     if world != args.gpus and rank == 0:

@@ -70,3 +70,16 @@ def test_bench_rejects_too_few_warmup_steps():
     res = subprocess.run([sys.executable, "bench.py", "--warmup", "2", "--impl", "reference"],
                          cwd=ROOT, capture_output=True, text=True, timeout=120)
     assert res.returncode != 0 and "warmup" in res.stderr
+
+
+def test_reference_arm_times_a_window_with_dropout():
+    """--window with --dropout is one combined call; the oracle arm times the same
+    combination and the line's config names both."""
+    res = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "small_b1_h2_s256_d64",
+                          "--window", "100", "--dropout", "0.1", "--steps", "1", "--warmup", "3",
+                          "--ref-step-seconds", "1", "--ref-total-seconds", "10"],
+                         cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert res.returncode == 0, res.stderr
+    line = json.loads(res.stdout.strip().splitlines()[-1])
+    assert line["config"]["elem_mask"]["window"] == 100 and line["config"]["dropout_p"] == 26 / 256
+    assert line["value"] > 0 and line["cpu_baseline"]["cores"] >= 1
