@@ -1,8 +1,9 @@
 """fp64 CPU oracle for causal scaled dot-product attention -- TEST INFRASTRUCTURE.
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
-leg import this package.  The CUDA library never links, loads or calls it, and
-it imports nothing from the CUDA library's package.
+leg import this package (``__graft_entry__.build()`` compiles it without using
+it).  The CUDA library never links, loads or calls it, and it imports nothing
+from the CUDA library's package.
 
 The arithmetic lives in ``attn_oracle.c`` (plain C, double precision, one query
 row at a time, the five steps of the naive causal attention in the order the
