@@ -462,3 +462,43 @@ def test_binding_fails_loudly_without_its_library(monkeypatch):
         native.attn_version()
     with pytest.raises(RuntimeError, match="nvcc"):
         native.attn_fwd(None, None, None, None, None, 1, 1, 1, 8, 64, 0.125, True, stream=0)
+
+
+C_PROGRAM = r"""
+#include <stdio.h>
+#include <string.h>
+#include "attn.h"
+
+int main(void) {
+    attn_options_t o;
+    if (attn_version() < 100) return 1;
+    if (strncmp(attn_status_string(ATTN_ERR_MISALIGNED), "ATTN_", 5) != 0) return 2;
+    /* argument errors return before any device work */
+    if (attn_fwd(NULL, NULL, NULL, NULL, NULL, 1, 1, 1, 8, 64, 0.125f, 1, NULL) != ATTN_ERR_INVALID_ARG)
+        return 3;
+    memset(&o, 0, sizeof o);
+    o.input_format = 7;
+    if (attn_fwd_ex(NULL, NULL, NULL, NULL, NULL, 1, 1, 1, 8, 64, 0.125f, 1, &o, NULL) != ATTN_ERR_INVALID_ARG)
+        return 4;
+    if (attn_bwd(NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, 1, 1, 1, 8, 64, 0.125f, 1,
+                 NULL) != ATTN_ERR_INVALID_ARG)
+        return 5;
+    puts("ok");
+    return 0;
+}
+"""
+
+
+def test_plain_c_program_links_and_calls_the_library(tmp_path):
+    """A C99 program that includes only attn.h and links libattn.so: the entry
+    points have C linkage and the header's signatures resolve; calls that return
+    before any device work give their documented codes."""
+    lib_dir = os.path.dirname(native.library_path())
+    native.load()  # built and current
+    src = tmp_path / "use_attn.c"
+    src.write_text(C_PROGRAM)
+    exe = tmp_path / "use_attn"
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), str(src),
+                    "-L", lib_dir, "-lattn", f"-Wl,-rpath,{lib_dir}", "-o", str(exe)], check=True)
+    res = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert res.returncode == 0 and res.stdout.strip() == "ok", (res.returncode, res.stdout, res.stderr)
