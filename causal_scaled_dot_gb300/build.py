@@ -44,7 +44,7 @@ def sources() -> list[str]:
 
 
 def _inputs() -> list[str]:
-    return sources() + sorted(glob.glob(os.path.join(CSRC, "*.cuh"))) + [
+    return sources() + sorted(glob.glob(os.path.join(CSRC, "*.cuh"))) + sorted(glob.glob(os.path.join(CSRC, "*.h"))) + [
         os.path.join(INCLUDE, "attn.h"), os.path.abspath(__file__)]
 
 

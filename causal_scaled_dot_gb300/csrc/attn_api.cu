@@ -1,6 +1,7 @@
 // attn_api.cu -- the C ABI of libattn (include/attn.h): argument checks, TMA
-// descriptor encoding and caching, per-device setup, kernel launch, and the
-// device status word that bounded waits report timeouts through.
+// descriptor encoding (with a small cache of encoded maps), per-device setup,
+// kernel launch, and the device status word that bounded waits report
+// timeouts through.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -15,6 +16,7 @@
 #include "common.cuh"
 #include "kernel_simple.cuh"
 #include "kernel_ws.cuh"
+#include "tmap_cache.h"
 
 // Status word: bits set by device-side waits that ran out (ptx::kStatusTimeout).
 __device__ unsigned int g_attn_status;
@@ -28,6 +30,7 @@ constexpr int kMaxDevices = 64;
 
 struct DeviceState {
     bool ready = false;
+    int index = -1;
     int status = ATTN_OK;  // ATTN_OK, or why this device cannot run the kernels
     int sm_count = 0;
     unsigned int* status_word = nullptr;
@@ -66,6 +69,7 @@ bool allow_ws_all() {
 int setup_device_locked(int dev) {
     DeviceState& st = g_devices[dev];
     if (st.ready) return st.status;
+    st.index = dev;
     int major = 0, minor = 0, sms = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
@@ -119,8 +123,18 @@ int current_device_state(DeviceState** out) {
 // elements are `elem_bytes` wide, box {128 bytes of a row, box_rows, 1},
 // 128-byte swizzle: one box fills box_rows rows of 128 bytes, the canonical
 // K-major (and MN-major) SW128 operand layout.  Rows past S read as zero.
-int encode_3d(CUtensorMap* map, const void* ptr, int elem_bytes, int D, int S, long long outer,
+// Encoded maps are kept in a small cache keyed by every input of the encode
+// (tmap_cache.h), so repeated calls on the same buffers skip the encoder.
+std::mutex g_tmap_mutex;
+TmapCache<64> g_tmap_cache;
+
+int encode_3d(CUtensorMap* map, int device, const void* ptr, int elem_bytes, int D, int S, long long outer,
               int box_rows) {
+    const TmapKey key{device, ptr, elem_bytes, D, S, outer, box_rows};
+    {
+        std::lock_guard<std::mutex> lock(g_tmap_mutex);
+        if (g_tmap_cache.lookup(key, map)) return ATTN_OK;
+    }
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)outer};
     cuuint64_t strides[2] = {(cuuint64_t)D * elem_bytes, (cuuint64_t)S * (cuuint64_t)D * elem_bytes};
     cuuint32_t box[3] = {(cuuint32_t)(128 / elem_bytes), (cuuint32_t)box_rows, 1};
@@ -130,7 +144,10 @@ int encode_3d(CUtensorMap* map, const void* ptr, int elem_bytes, int D, int S, l
     CUresult r = g_encode(map, type, 3, const_cast<void*>(ptr), dims, strides, box, elem,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_INVALID_ARG;
+    if (r != CUDA_SUCCESS) return ATTN_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(g_tmap_mutex);
+    g_tmap_cache.insert(key, *map);
+    return ATTN_OK;
 }
 
 bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
@@ -185,40 +202,41 @@ int launch_simple(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMa
 }
 
 template <int D, bool F, bool M, bool DR = false, bool E = false>
-int launch_ws(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, FwdParams p,
-              int sm_count, cudaStream_t stream) {
+int launch_ws(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
+              FwdParams p, int sm_count, cudaStream_t stream) {
     const long long npairs = (p.num_q_tiles + 1) / 2;
     const long long units = (long long)p.B * p.Hq * npairs;
     if (units > (1ll << 31) - 1) return ATTN_ERR_UNSUPPORTED;
     p.num_units = (int)units;
     const int grid = (int)(units < sm_count ? units : sm_count);
     attn_fwd_ws_kernel<D, F, M, DR, E><<<grid, WsLayout<D, F>::kThreads, WsLayout<D, F>::kDynamicSmem, stream>>>(
-        tq, tk, tv, p);
+        tq, tk, tv, to, p);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
 // The persistent kernel's instantiation for the features a call uses: block
 // mask (M), dropout (DR, bf16 only) and keep bits (E).
 template <int D, bool F>
-int launch_any(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
+int launch_any(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
+               const FwdParams& p,
                int sm, cudaStream_t st, bool m, bool dr, bool e) {
     if constexpr (F) {
         if (dr) return ATTN_ERR_UNSUPPORTED;
-        if (m) return e ? launch_ws<D, F, true, false, true>(tq, tk, tv, p, sm, st)
-                        : launch_ws<D, F, true, false, false>(tq, tk, tv, p, sm, st);
-        return e ? launch_ws<D, F, false, false, true>(tq, tk, tv, p, sm, st)
-                 : launch_ws<D, F, false, false, false>(tq, tk, tv, p, sm, st);
+        if (m) return e ? launch_ws<D, F, true, false, true>(tq, tk, tv, to, p, sm, st)
+                        : launch_ws<D, F, true, false, false>(tq, tk, tv, to, p, sm, st);
+        return e ? launch_ws<D, F, false, false, true>(tq, tk, tv, to, p, sm, st)
+                 : launch_ws<D, F, false, false, false>(tq, tk, tv, to, p, sm, st);
     } else {
         if (m) {
-            if (dr) return e ? launch_ws<D, F, true, true, true>(tq, tk, tv, p, sm, st)
-                             : launch_ws<D, F, true, true, false>(tq, tk, tv, p, sm, st);
-            return e ? launch_ws<D, F, true, false, true>(tq, tk, tv, p, sm, st)
-                     : launch_ws<D, F, true, false, false>(tq, tk, tv, p, sm, st);
+            if (dr) return e ? launch_ws<D, F, true, true, true>(tq, tk, tv, to, p, sm, st)
+                             : launch_ws<D, F, true, true, false>(tq, tk, tv, to, p, sm, st);
+            return e ? launch_ws<D, F, true, false, true>(tq, tk, tv, to, p, sm, st)
+                     : launch_ws<D, F, true, false, false>(tq, tk, tv, to, p, sm, st);
         }
-        if (dr) return e ? launch_ws<D, F, false, true, true>(tq, tk, tv, p, sm, st)
-                         : launch_ws<D, F, false, true, false>(tq, tk, tv, p, sm, st);
-        return e ? launch_ws<D, F, false, false, true>(tq, tk, tv, p, sm, st)
-                 : launch_ws<D, F, false, false, false>(tq, tk, tv, p, sm, st);
+        if (dr) return e ? launch_ws<D, F, false, true, true>(tq, tk, tv, to, p, sm, st)
+                         : launch_ws<D, F, false, true, false>(tq, tk, tv, to, p, sm, st);
+        return e ? launch_ws<D, F, false, false, true>(tq, tk, tv, to, p, sm, st)
+                 : launch_ws<D, F, false, false, false>(tq, tk, tv, to, p, sm, st);
     }
 }
 
@@ -322,11 +340,15 @@ int fwd_bf16(const void* q, const void* k, const void* v, void* out, float* lse,
     rc = current_device_state(&dev);
     if (rc != ATTN_OK) return rc;
 
-    alignas(64) CUtensorMap tq, tk, tv;
+    alignas(64) CUtensorMap tq, tk, tv, to;
     const int eb = fp8 ? 1 : 2;
-    if (encode_3d(&tq, q, eb, D, S, (long long)B * Hq, kTile) != ATTN_OK ||
-        encode_3d(&tk, k, eb, D, S, (long long)B * Hkv, kTile) != ATTN_OK ||
-        encode_3d(&tv, v, eb, D, S, (long long)B * Hkv, kTile) != ATTN_OK)
+    // O (bf16 whatever the inputs) is stored by the correction warps in boxes
+    // of 32 rows, one per warp.
+    const int di = dev->index;
+    if (encode_3d(&tq, di, q, eb, D, S, (long long)B * Hq, kTile) != ATTN_OK ||
+        encode_3d(&tk, di, k, eb, D, S, (long long)B * Hkv, kTile) != ATTN_OK ||
+        encode_3d(&tv, di, v, eb, D, S, (long long)B * Hkv, kTile) != ATTN_OK ||
+        encode_3d(&to, di, out, 2, D, S, (long long)B * Hq, 32) != ATTN_OK)
         return ATTN_ERR_INVALID_ARG;
 
     FwdParams p{};
@@ -364,12 +386,12 @@ int fwd_bf16(const void* q, const void* k, const void* v, void* out, float* lse,
     }
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const bool m = block_mask != nullptr, dr = dropout_p8 > 0, e = keep_bits != nullptr;
-    if (fp8) return launch_any<128, true>(tq, tk, tv, p, dev->sm_count, st, m, false, e);
+    if (fp8) return launch_any<128, true>(tq, tk, tv, to, p, dev->sm_count, st, m, false, e);
     // The one-tile-per-CTA cross-check kernel covers the plain forward only.
     if (!m && !dr && !e && use_simple_kernel())
         return D == 64 ? launch_simple<64>(tq, tk, tv, p, st) : launch_simple<128>(tq, tk, tv, p, st);
-    return D == 64 ? launch_any<64, false>(tq, tk, tv, p, dev->sm_count, st, m, dr, e)
-                   : launch_any<128, false>(tq, tk, tv, p, dev->sm_count, st, m, dr, e);
+    return D == 64 ? launch_any<64, false>(tq, tk, tv, to, p, dev->sm_count, st, m, dr, e)
+                   : launch_any<128, false>(tq, tk, tv, to, p, dev->sm_count, st, m, dr, e);
 }
 }  // namespace
 }  // namespace attn
@@ -451,22 +473,24 @@ extern "C" int attn_version(void) { return kVersion; }
 namespace attn {
 namespace host {
 
-int current_device(int* sm_count, unsigned int** status_word) {
+int current_device(int* sm_count, unsigned int** status_word, int* device) {
     DeviceState* dev = nullptr;
     const int rc = current_device_state(&dev);
     if (rc != ATTN_OK) return rc;
     *sm_count = dev->sm_count;
     *status_word = dev->status_word;
+    *device = dev->index;
     return ATTN_OK;
 }
 
-int encode_bf16_tiles(CUtensorMap* map, const void* ptr, int D, int S, long long outer) {
-    return encode_3d(map, ptr, 2, D, S, outer, kTile);
+int encode_bf16_tiles(CUtensorMap* map, int device, const void* ptr, int D, int S, long long outer) {
+    return encode_3d(map, device, ptr, 2, D, S, outer, kTile);
 }
 
-int encode_bf16_box(CUtensorMap* map, const void* ptr, int D, int S, long long outer, int box_rows) {
+int encode_bf16_box(CUtensorMap* map, int device, const void* ptr, int D, int S, long long outer,
+                    int box_rows) {
     if (box_rows < 1 || box_rows > 256) return ATTN_ERR_INVALID_ARG;
-    return encode_3d(map, ptr, 2, D, S, outer, box_rows);
+    return encode_3d(map, device, ptr, 2, D, S, outer, box_rows);
 }
 
 bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {

@@ -222,16 +222,17 @@ int bwd(const void* q, const void* k, const void* v, const void* out, const void
     }
     int sm_count = 0;
     unsigned int* status = nullptr;
-    rc = host::current_device(&sm_count, &status);
+    int device = -1;
+    rc = host::current_device(&sm_count, &status, &device);
     if (rc != ATTN_OK) return rc;
     rc = setup_bwd_kernels();
     if (rc != ATTN_OK) return rc;
 
     alignas(64) CUtensorMap tq, tdo, tk, tv;
-    if (host::encode_bf16_tiles(&tq, q, D, S, (long long)B * Hq) != ATTN_OK ||
-        host::encode_bf16_tiles(&tdo, dout, D, S, (long long)B * Hq) != ATTN_OK ||
-        host::encode_bf16_tiles(&tk, k, D, S, (long long)B * Hkv) != ATTN_OK ||
-        host::encode_bf16_tiles(&tv, v, D, S, (long long)B * Hkv) != ATTN_OK)
+    if (host::encode_bf16_tiles(&tq, device, q, D, S, (long long)B * Hq) != ATTN_OK ||
+        host::encode_bf16_tiles(&tdo, device, dout, D, S, (long long)B * Hq) != ATTN_OK ||
+        host::encode_bf16_tiles(&tk, device, k, D, S, (long long)B * Hkv) != ATTN_OK ||
+        host::encode_bf16_tiles(&tv, device, v, D, S, (long long)B * Hkv) != ATTN_OK)
         return ATTN_ERR_INVALID_ARG;
 
     BwdParams p{};

@@ -57,14 +57,15 @@ extern "C" int attn_out_proj(const void* out, const void* w, const float* bias, 
 
     int sm_count = 0;
     unsigned int* status = nullptr;
-    int rc = host::current_device(&sm_count, &status);
+    int device = -1;
+    int rc = host::current_device(&sm_count, &status, &device);
     if (rc != ATTN_OK) return rc;
     if ((rc = setup_proj_kernels()) != ATTN_OK) return rc;
 
     // O as [B*H, S, D] (128-row boxes); W as [1, E, H*D] (256-row boxes).
     alignas(64) CUtensorMap to, tw;
-    if (host::encode_bf16_tiles(&to, out, D, S, (long long)B * H) != ATTN_OK ||
-        host::encode_bf16_box(&tw, w, H * D, E, 1, ProjLayout::kBN) != ATTN_OK)
+    if (host::encode_bf16_tiles(&to, device, out, D, S, (long long)B * H) != ATTN_OK ||
+        host::encode_bf16_box(&tw, device, w, H * D, E, 1, ProjLayout::kBN) != ATTN_OK)
         return ATTN_ERR_INVALID_ARG;
 
     ProjParams p{};

@@ -18,7 +18,11 @@
 //   warps 4-7   softmax warpgroup 0: one thread per row of query tile 2m.
 //   warps 8-11  softmax warpgroup 1: one thread per row of query tile 2m+1.
 // The two warpgroups ping-pong: while one runs its softmax the tensor core
-// computes the other's products.
+// computes the other's products.  At the end of a unit each softmax warp also
+// drains its 32 rows of O (tensor memory -> x 1/l -> bf16 -> a shared-memory
+// box -> TMA store) and writes their LSE.  The drain of query tile 2m
+// overlaps the tensor core's last products for tile 2m+1; a separate
+// correction warpgroup for the drain (16 warps) measured slower.
 //
 // Tensor memory (512 columns x 128 lanes, fp32): S_0 [0,128), S_1 [128,256),
 // O_0 [256, 256+D), O_1 [256+D, 256+2D).  P_i (bf16, two per column) is written
@@ -70,10 +74,15 @@ struct WsLayout {
     static constexpr int kStages = (kTileBytes == 32768) ? 4 : 8;    // K/V ring slots, one tile each
     static constexpr int kChunks = D / kRowElems;                    // 128-byte swizzle blocks
     static constexpr uint32_t kChunkBytes = kTile * 128;   // one block of a tile: 16 KB
+    // Output staging: per softmax warp, 32 rows x 64 columns of O as bf16 in
+    // the 128-byte swizzled layout of the O tensor map's {64 columns, 32 rows}
+    // box (4 KB), filled and stored once per 64-column block.
+    static constexpr uint32_t kOutBoxBytes = 32 * 128;
     static constexpr uint32_t kQ0 = 0;
     static constexpr uint32_t kQ1 = kTileBytes;
     static constexpr uint32_t kRing = 2 * kTileBytes;
-    static constexpr uint32_t kBars = kRing + kStages * kTileBytes;
+    static constexpr uint32_t kStage = kRing + kStages * kTileBytes;
+    static constexpr uint32_t kBars = kStage + 8 * kOutBoxBytes;
     // mbarrier indices
     static constexpr int kQFull = 0, kQEmpty = 2, kSFull = 4, kPFull = 6, kOFull = 8;
     static constexpr int kKVFull = 10, kKVEmpty = 10 + kStages, kDrain = 10 + 2 * kStages;
@@ -85,6 +94,7 @@ struct WsLayout {
     static constexpr uint32_t kDynamicSmem = kBytes + 1024;  // slack for 1024-byte alignment
     static constexpr uint32_t kTmemCols = 512;
     static_assert(kDynamicSmem <= 227 * 1024, "shared memory budget");
+    static_assert(kStage % 1024 == 0, "staging boxes need the swizzle atom's alignment");
 };
 
 // Unit u -> (bh, pair m).  Causal: heaviest pairs first.  Within a pair index
@@ -381,11 +391,13 @@ __device__ void ws_mma_role(const FwdParams& p, uint32_t base, uint32_t tmem,
 
 // ---------------------------------------------------------------- softmax
 template <int D, bool F, bool M, bool DR, bool E>
-__device__ void ws_softmax_role(const FwdParams& p, uint32_t base, uint32_t tmem, int wg,
-                                volatile int* abort_flag) {
+__device__ void ws_softmax_role(const CUtensorMap* tm_o, const FwdParams& p, uint32_t base, uint32_t tmem,
+                                int wg, volatile int* abort_flag) {
     using L = WsLayout<D, F>;
     const int r = threadIdx.x - (4 + 4 * wg) * 32;  // row within the query tile, 0..127
     const int warp_in_wg = r >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t stage = base + L::kStage + (uint32_t)(4 * wg + warp_in_wg) * L::kOutBoxBytes;
     const uint32_t lane_off = (uint32_t)(warp_in_wg * 32) << 16;
     const uint32_t tS = tmem + lane_off + (uint32_t)wg * kTile;
     const uint32_t tP = tS + 64u;
@@ -618,27 +630,38 @@ __device__ void ws_softmax_role(const FwdParams& p, uint32_t base, uint32_t tmem
         }
         const bool row_none = E && first;  // (only element masks leave single rows empty)
         const float inv_l = row_none ? 0.f : p.o_scale / l_run;  // o_scale: the V descale (1 for bf16)
+        // O / l -> bf16 -> this warp's staging box (rows 32 w .. 32 w + 31 of the
+        // tile, 64 columns at a time, swizzled as the tensor map expects) -> one
+        // TMA store per block; rows past S are clipped by the tensor map.
+        const int row0 = qt * kTile + 32 * warp_in_wg;
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            ptx::tmem_ld32(tO + c * 32, o);
-            ptx::tmem_ld_wait();
-            ptx::reg_fence32(o);
-            if (valid) {
-                uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+        for (int c = 0; c < D / 64; ++c) {
+            // The store issued from the box before (previous block or unit) has read it.
+            if (lane == 0) ptx::bulk_wait_group_read<0>();
+            __syncwarp();
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t o[32];
+                ptx::tmem_ld32(tO + 64 * c + 32 * h, o);
+                ptx::tmem_ld_wait();
+                ptx::reg_fence32(o);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    uint4 v;
-                    v.x = ptx::pack_bf16x2(__uint_as_float(o[8 * e + 0]) * inv_l,
-                                           __uint_as_float(o[8 * e + 1]) * inv_l);
-                    v.y = ptx::pack_bf16x2(__uint_as_float(o[8 * e + 2]) * inv_l,
-                                           __uint_as_float(o[8 * e + 3]) * inv_l);
-                    v.z = ptx::pack_bf16x2(__uint_as_float(o[8 * e + 4]) * inv_l,
-                                           __uint_as_float(o[8 * e + 5]) * inv_l);
-                    v.w = ptx::pack_bf16x2(__uint_as_float(o[8 * e + 6]) * inv_l,
-                                           __uint_as_float(o[8 * e + 7]) * inv_l);
-                    dst[e] = v;
+                    uint32_t v[4];
+#pragma unroll
+                    for (int t = 0; t < 4; ++t)
+                        v[t] = ptx::pack_bf16x2(__uint_as_float(o[8 * e + 2 * t]) * inv_l,
+                                                __uint_as_float(o[8 * e + 2 * t + 1]) * inv_l);
+                    // 16-byte piece 4h+e of this row, at its swizzled position.
+                    ptx::st_shared_v4(stage + (uint32_t)lane * 128u + ((uint32_t)((4 * h + e) ^ (lane & 7)) << 4),
+                                      v[0], v[1], v[2], v[3]);
                 }
+            }
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                if (row0 < p.S) ptx::tma_store_3d(tm_o, stage, 64 * c, row0, w.bh);
+                ptx::bulk_commit_group();
             }
         }
         if (valid && p.lse != nullptr)
@@ -651,12 +674,23 @@ __device__ void ws_softmax_role(const FwdParams& p, uint32_t base, uint32_t tmem
     }
 }
 
+// The softmax role plus the completion of this warp's output stores, which
+// must have finished reading shared memory before the CTA exits.
+template <int D, bool F, bool M, bool DR, bool E>
+__device__ void ws_softmax_warp(const CUtensorMap* tm_o, const FwdParams& p, uint32_t base, uint32_t tmem,
+                                int wg, volatile int* abort_flag) {
+    ws_softmax_role<D, F, M, DR, E>(tm_o, p, base, tmem, wg, abort_flag);
+    if ((threadIdx.x & 31) == 0) ptx::bulk_wait_group<0>();
+    __syncwarp();
+}
+
 // ---------------------------------------------------------------- kernel
 template <int D, bool F, bool M, bool DR, bool E>
 __global__ void __launch_bounds__(WsLayout<D, F>::kThreads, 1)
     attn_fwd_ws_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
-                       const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+                       const __grid_constant__ CUtensorMap tm_v,
+                       const __grid_constant__ CUtensorMap tm_o, const FwdParams p) {
     using L = WsLayout<D, F>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
@@ -686,6 +720,7 @@ __global__ void __launch_bounds__(WsLayout<D, F>::kThreads, 1)
         ptx::prefetch_tensormap(&tm_q);
         ptx::prefetch_tensormap(&tm_k);
         ptx::prefetch_tensormap(&tm_v);
+        ptx::prefetch_tensormap(&tm_o);
     }
     if (warp == 1) {
         ptx::tmem_alloc(ptx::smem_addr(tmem_slot), L::kTmemCols);
@@ -705,7 +740,7 @@ __global__ void __launch_bounds__(WsLayout<D, F>::kThreads, 1)
         }
     } else {
         ptx::regs_inc<L::kRegsSoftmax>();
-        ws_softmax_role<D, F, M, DR, E>(p, base, tmem, (warp - 4) >> 2, abort_flag);
+        ws_softmax_warp<D, F, M, DR, E>(&tm_o, p, base, tmem, (warp - 4) >> 2, abort_flag);
     }
 
     ptx::tc_fence_before();

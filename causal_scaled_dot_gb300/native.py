@@ -410,31 +410,70 @@ def attn_version() -> int:
     return load().attn_version()
 
 
+def _check_attention_tensors(named):
+    """Validate the tensors of ``attention`` / ``attention_trainable`` before any
+    library call: bf16 q, k, v that are contiguous 4-D CUDA tensors, and every
+    tensor given (outputs and masks included) on one and the same device.  The C
+    ABI runs on the calling thread's current device, so a tensor on another GPU
+    would hand that device's addresses to a kernel launched elsewhere.  Returns
+    that device."""
+    import torch
+    device = None
+    for name, t in named:
+        if t is None:
+            continue
+        if name in ("q", "k", "v"):
+            if not getattr(t, "is_cuda", False) or t.dtype != torch.bfloat16:
+                raise ValueError(f"{name} must be a bf16 CUDA tensor")
+            if t.dim() != 4 or not t.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous [B,H,S,D] tensor")
+        elif not getattr(t, "is_cuda", False):
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if device is None:
+            device = t.device
+        elif t.device != device:
+            raise ValueError(f"{name} is on {t.device} but q is on {device}: all tensors of one call "
+                             "must be on the same device")
+    return device
+
+
+def _device_stream(device, stream):
+    """The stream to launch on: the one given, else the current stream of ``device``."""
+    import torch
+    return torch.cuda.current_stream(device) if stream is None else stream
+
+
 def attention(q, k, v, causal: bool = True, scale: float | None = None, out=None, lse=None,
-              return_lse: bool = True, stream=None):
+              return_lse: bool = True, stream=None, check_status: bool = False):
     """O (and LSE) for CUDA tensors q [B,Hq,S,D], k/v [B,Hkv,S,D] in bf16.
 
     Allocates ``out`` (bf16 [B,Hq,S,D]) and ``lse`` (fp32 [B,Hq,S]) with
-    PyTorch when they are not given, checks dtypes, shapes and contiguity, and
-    calls ``attn_fwd`` on ``stream`` (default: the current stream).
+    PyTorch when they are not given, checks dtypes, shapes, contiguity and that
+    every tensor is on q's device, and calls ``attn_fwd`` with that device
+    current, on ``stream`` (default: that device's current stream).
+
+    ``check_status=True`` synchronises the stream afterwards and raises
+    AttnError if a device-side wait ran out (``attn_sync_status``).  The status
+    word behind it is one per device, shared by every stream and caller on that
+    device: reading it also clears a timeout that another stream's kernel left.
     """
     import torch
-    for name, t in (("q", q), ("k", k), ("v", v)):
-        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.bfloat16:
-            raise ValueError(f"{name} must be a bf16 CUDA tensor")
-        if t.dim() != 4 or not t.is_contiguous():
-            raise ValueError(f"{name} must be a contiguous [B,H,S,D] tensor")
+    device = _check_attention_tensors((("q", q), ("k", k), ("v", v), ("out", out), ("lse", lse)))
     B, Hq, S, D = q.shape
     Bk, Hkv, Sk, Dk = k.shape
     if tuple(v.shape) != tuple(k.shape) or (Bk, Sk, Dk) != (B, S, D):
         raise ValueError("q [B,Hq,S,D] and k, v [B,Hkv,S,D] disagree")
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    if out is None:
-        out = torch.empty_like(q)
-    if lse is None and return_lse:
-        lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
-    attn_fwd(q, k, v, out, lse, B, Hq, Hkv, S, D, scale, causal, stream)
+    with torch.cuda.device(device):
+        if out is None:
+            out = torch.empty_like(q)
+        if lse is None and return_lse:
+            lse = torch.empty((B, Hq, S), dtype=torch.float32, device=device)
+        st = _device_stream(device, stream)
+        attn_fwd(q, k, v, out, lse, B, Hq, Hkv, S, D, scale, causal, st)
+        if check_status:
+            attn_sync_status(st)
     return (out, lse) if return_lse else out
 
 
@@ -445,33 +484,44 @@ def _attention_function():
 
     class AttentionFunction(torch.autograd.Function):
         @staticmethod
-        def forward(ctx, q, k, v, causal, scale, block_mask, keep_bits, dropout_p, seed, offset):
+        def forward(ctx, q, k, v, causal, scale, block_mask, keep_bits, dropout_p, seed, offset,
+                    check_status):
             B, Hq, S, D = q.shape
             Hkv = k.shape[1]
-            out = torch.empty_like(q)
-            lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
-            opts = options(block_mask=block_mask, keep_bits=keep_bits, dropout_p=dropout_p, seed=seed,
-                           offset=offset)
-            attn_fwd_ex(q, k, v, out, lse, B, Hq, Hkv, S, D, scale, causal, opts)
+            with torch.cuda.device(q.device):
+                out = torch.empty_like(q)
+                lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
+                opts = options(block_mask=block_mask, keep_bits=keep_bits, dropout_p=dropout_p, seed=seed,
+                               offset=offset)
+                st = torch.cuda.current_stream(q.device)
+                attn_fwd_ex(q, k, v, out, lse, B, Hq, Hkv, S, D, scale, causal, opts, st)
+                if check_status:
+                    attn_sync_status(st)
             ctx.save_for_backward(q, k, v, out, lse)
             ctx.masks = (block_mask, keep_bits)
-            ctx.args = (causal, scale, dropout_p, seed, offset)
+            ctx.args = (causal, scale, dropout_p, seed, offset, check_status)
             return out
 
         @staticmethod
         def backward(ctx, dout):
             q, k, v, out, lse = ctx.saved_tensors
             block_mask, keep_bits = ctx.masks
-            causal, scale, dropout_p, seed, offset = ctx.args
+            causal, scale, dropout_p, seed, offset, check_status = ctx.args
             B, Hq, S, D = q.shape
             Hkv = k.shape[1]
             dout = dout.contiguous()
-            dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-            delta = torch.empty_like(lse)
-            opts = options(block_mask=block_mask, keep_bits=keep_bits, dropout_p=dropout_p, seed=seed,
-                           offset=offset)
-            attn_bwd_ex(q, k, v, out, dout, lse, delta, dq, dk, dv, B, Hq, Hkv, S, D, scale, causal, opts)
-            return dq, dk, dv, None, None, None, None, None, None, None
+            _check_attention_tensors((("q", q), ("dout", dout)))
+            with torch.cuda.device(q.device):
+                dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+                delta = torch.empty_like(lse)
+                opts = options(block_mask=block_mask, keep_bits=keep_bits, dropout_p=dropout_p, seed=seed,
+                               offset=offset)
+                st = torch.cuda.current_stream(q.device)
+                attn_bwd_ex(q, k, v, out, dout, lse, delta, dq, dk, dv, B, Hq, Hkv, S, D, scale, causal, opts,
+                            st)
+                if check_status:
+                    attn_sync_status(st)
+            return dq, dk, dv, None, None, None, None, None, None, None, None
 
     return AttentionFunction
 
@@ -480,19 +530,21 @@ _ATTENTION_FUNCTION = None
 
 
 def attention_trainable(q, k, v, causal: bool = True, scale: float | None = None, block_mask=None,
-                        keep_bits=None, dropout_p: float = 0.0, seed: int = 0, offset: int = 0):
+                        keep_bits=None, dropout_p: float = 0.0, seed: int = 0, offset: int = 0,
+                        check_status: bool = False):
     """O = attention(q, k, v) with gradients: forward and backward run the C ABI
-    (attn_fwd_ex / attn_bwd_ex with the given options).  q [B,Hq,S,D], k/v
-    [B,Hkv,S,D] bf16 CUDA tensors; block_mask uint8 [1 or Hq, nt, nt]; keep_bits
-    uint8 [1 or Hq, S, 16*nt]; dropout combines with either or both."""
+    (attn_fwd_ex / attn_bwd_ex with the given options) with q's device current,
+    on its current stream.  q [B,Hq,S,D], k/v [B,Hkv,S,D] bf16 CUDA tensors;
+    block_mask uint8 [1 or Hq, nt, nt]; keep_bits uint8 [1 or Hq, S, 16*nt];
+    dropout combines with either or both.  Every tensor must be on q's device.
+    ``check_status=True`` reads the per-device status word after each pass (as
+    ``attention`` does) and raises AttnError on a device-side timeout."""
     global _ATTENTION_FUNCTION
-    import torch
-    for name, t in (("q", q), ("k", k), ("v", v)):
-        if t.dtype != torch.bfloat16 or not t.is_cuda or t.dim() != 4 or not t.is_contiguous():
-            raise ValueError(f"{name} must be a contiguous bf16 CUDA [B,H,S,D] tensor")
+    _check_attention_tensors((("q", q), ("k", k), ("v", v), ("block_mask", block_mask),
+                              ("keep_bits", keep_bits)))
     if scale is None:
         scale = 1.0 / math.sqrt(q.shape[-1])
     if _ATTENTION_FUNCTION is None:
         _ATTENTION_FUNCTION = _attention_function()
     return _ATTENTION_FUNCTION.apply(q, k, v, bool(causal), float(scale), block_mask, keep_bits,
-                                     float(dropout_p), int(seed), int(offset))
+                                     float(dropout_p), int(seed), int(offset), bool(check_status))

@@ -29,11 +29,19 @@
  * is the usual companion output of a fused attention forward.
  *
  * Threading: every entry point may be called from any host thread.  The only
- * internal state is a cache of TMA descriptors and of per-device properties,
- * guarded by a mutex.  The work runs on the calling thread's current device
- * (cudaGetDevice), which must hold every buffer; its primary context is
- * bound to the thread on entry, so a thread that has made no CUDA call yet
- * (an autograd engine's worker, say) can call too.
+ * internal state is per-device setup (capability check, SM count, kernel
+ * attributes; done once per device) and a least-recently-used cache of 64
+ * encoded TMA descriptors, keyed by device, address, element size, extents and
+ * box -- every input of the encode, so a hit is exactly what a fresh encode
+ * would give, including for a buffer freed and reallocated at the same
+ * address -- each guarded by a mutex.  The work runs on the calling thread's
+ * current device (cudaGetDevice), which must hold every buffer; its primary
+ * context is bound to the thread on entry, so a thread that has made no CUDA
+ * call yet (an autograd engine's worker, say) can call too.
+ *
+ * Device status word: kernels whose bounded waits run out record it in one
+ * word per device (read and cleared by attn_sync_status).  It is shared by
+ * every stream and caller on that device.
  */
 #ifndef LIBATTN_ATTN_H_
 #define LIBATTN_ATTN_H_
@@ -95,7 +103,8 @@ typedef struct {
  *         (grouped-query attention; Hkv == Hq is plain multi-head, Hkv == 1
  *         is multi-query).
  *   D     head dimension: 64 or 128.
- *   scale finite and >= 0; the scores are multiplied by it (usually 1/sqrt(D)).
+ *   scale finite and > 0; the scores are multiplied by it (usually 1/sqrt(D)).
+ *         Zero, negative or non-finite: ATTN_ERR_INVALID_ARG.
  *   causal  non-zero: key j is masked for query i when j > i (query and key
  *         positions share one index, Sq == Sk == S).  Zero: no mask.
  *   stream  CUDA stream (cudaStream_t, passed as void*) the work is enqueued
@@ -329,7 +338,9 @@ int attn_out_proj(const void *out, const void *w, const float *bias, void *y, in
  * a per-device status word and makes the kernel exit cleanly (it never traps).
  * This call waits for `stream`, reads and clears that word, and returns
  * ATTN_OK, ATTN_ERR_TIMEOUT, or ATTN_ERR_DEVICE if the synchronisation itself
- * failed.
+ * failed.  The word is one per device, not per stream: a timeout left by a
+ * kernel on another stream of the same device is reported (and cleared) here
+ * too, and outputs of a kernel that timed out are only partly written.
  */
 int attn_sync_status(void *stream);
 

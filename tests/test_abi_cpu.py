@@ -104,6 +104,42 @@ def test_python_binding_rejects_host_tensors():
         native.attention_trainable(q.float(), q, q)
 
 
+class _FakeCudaTensor:
+    """Stands in for a bf16 CUDA tensor on a given device (no GPU needed)."""
+
+    def __init__(self, index, shape=(1, 2, 128, 64)):
+        import torch
+        self.is_cuda = True
+        self.dtype = torch.bfloat16
+        self.device = torch.device("cuda", index)
+        self.shape = shape
+
+    def dim(self):
+        return len(self.shape)
+
+    def is_contiguous(self):
+        return True
+
+
+def test_python_wrappers_reject_tensors_on_different_devices(monkeypatch):
+    """The C ABI runs on the calling thread's current device: tensors split over
+    two devices are refused before the library is loaded or called."""
+    def no_library():
+        raise AssertionError("the library must not be reached")
+
+    monkeypatch.setattr(native, "load", no_library)
+    a, b = _FakeCudaTensor(0), _FakeCudaTensor(1)
+    for args in ((a, b, a), (a, a, b), (b, a, a)):
+        with pytest.raises(ValueError, match="same device"):
+            native.attention(*args)
+        with pytest.raises(ValueError, match="same device"):
+            native.attention_trainable(*args)
+    with pytest.raises(ValueError, match="same device"):
+        native.attention(a, a, a, out=b)
+    with pytest.raises(ValueError, match="same device"):
+        native.attention_trainable(a, a, a, block_mask=b)
+
+
 def test_selftest_rejects_bad_limits():
     lib = native.load()
     assert lib.attn_selftest_wait_timeout(0, None) == ATTN_ERR_INVALID_ARG

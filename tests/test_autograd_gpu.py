@@ -54,7 +54,7 @@ def test_autograd_matches_direct_backward(variant):
     o = native.attention_trainable(tq, tk, tv, True, scale,
                                    block_mask=None if bm is None else torch.from_numpy(bm).cuda(),
                                    keep_bits=None if kb is None else torch.from_numpy(kb).cuda(),
-                                   dropout_p=p, seed=5, offset=6)
+                                   dropout_p=p, seed=5, offset=6, check_status=True)
     o.backward(to_device(do))
     got = [t.grad.double().cpu().numpy() for t in (tq, tk, tv)]
     if variant == "plain":
@@ -117,3 +117,17 @@ def test_entry_points_from_a_thread_with_no_cuda_call():
     side.synchronize()
     for a, b in zip(in_thread, in_main):
         assert torch.equal(a, b)
+
+
+def test_attention_wrapper_with_status_check():
+    """``attention`` runs on the tensors' device with its current stream and,
+    with check_status, reads the status word: the result equals the direct call."""
+    import torch
+    from causal_scaled_dot_gb300 import native
+    B, Hq, Hkv, S, D = 1, 2, 2, 257, 128
+    q, k, v = (to_device(x) for x in qkv_bf16(B, Hq, Hkv, S, D, seed=9300))
+    o, lse = native.attention(q, k, v, True, check_status=True)
+    o2, lse2 = torch.empty_like(q), torch.empty_like(lse)
+    native.attn_fwd(q, k, v, o2, lse2, B, Hq, Hkv, S, D, 1.0 / math.sqrt(D), True)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)
