@@ -189,22 +189,34 @@ __device__ void ws_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
     // Loads issued and possibly not yet landed, for the drain after an abort.
     uint32_t pend_kv = 0, pend_kv_par = 0, pend_q = 0, pend_q_par = 0;
     const uint64_t lim = p.wait_limit_ns;
+    // Q_i of a unit into its slot once the previous unit's last S_i = Q_i K^T
+    // has completed.
+    auto load_q = [&](const Unit& w, int i) -> bool {
+        if (!ptx::mbar_wait(ws_bar<D, F>(base, L::kQEmpty + i), qe_phase[i] ^ 1u, abort_flag, p.status, lim))
+            return false;
+        qe_phase[i] ^= 1u;
+        const uint32_t full = ws_bar<D, F>(base, L::kQFull + i);
+        ptx::mbar_arrive_expect_tx(full, L::kTileBytes);
+        const uint32_t dst = base + (i == 0 ? L::kQ0 : L::kQ1);
+#pragma unroll
+        for (int c = 0; c < L::kChunks; ++c)
+            ptx::tma_load_3d(dst + c * L::kChunkBytes, tm_q, full, c * L::kRowElems, (2 * w.m + i) * kTile,
+                             w.bh);
+        pend_q |= 1u << i;
+        pend_q_par = (pend_q_par & ~(1u << i)) | (((qe_phase[i] ^ 1u) & 1u) << i);
+        return true;
+    };
     for (int rnd = 0, u = unit_of_round(0); u < p.num_units; u = unit_of_round(++rnd)) {
         const Unit w = decode_unit(u, p);
-        for (int i = 0; i < 2; ++i) {
-            if (!ptx::mbar_wait(ws_bar<D, F>(base, L::kQEmpty + i), qe_phase[i] ^ 1u, abort_flag,
-                                p.status, lim))
-                goto drain;
-            qe_phase[i] ^= 1u;
-            const uint32_t full = ws_bar<D, F>(base, L::kQFull + i);
-            ptx::mbar_arrive_expect_tx(full, L::kTileBytes);
-            const uint32_t dst = base + (i == 0 ? L::kQ0 : L::kQ1);
-#pragma unroll
-            for (int c = 0; c < L::kChunks; ++c)
-                ptx::tma_load_3d(dst + c * L::kChunkBytes, tm_q, full, c * L::kRowElems, (2 * w.m + i) * kTile,
-                                 w.bh);
-            pend_q |= 1u << i;
-            pend_q_par = (pend_q_par & ~(1u << i)) | (((qe_phase[i] ^ 1u) & 1u) << i);
+        // Without a block mask the issuer starts a unit's first S_0 = Q_0 K_0^T
+        // while the previous unit's last softmax runs (see the MMA role), so
+        // the unit's first K is loaded right after Q_0: Q_1's slot frees only
+        // with the previous unit's last S_1, and K_0 need not wait for it.
+        bool q1_loaded = false;
+        if (!load_q(w, 0)) goto drain;
+        if (M) {
+            if (!load_q(w, 1)) goto drain;
+            q1_loaded = true;
         }
         for (int j = next_union<M>(p, w, -1); j < w.n; j = next_union<M>(p, w, j)) {
 #pragma unroll
@@ -225,8 +237,13 @@ __device__ void ws_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                     slot = 0;
                     ring_phase ^= 1u;
                 }
+                if (!q1_loaded) {
+                    if (!load_q(w, 1)) goto drain;
+                    q1_loaded = true;
+                }
             }
         }
+        if (!q1_loaded && !load_q(w, 1)) goto drain;
     }
     return;
 drain:
@@ -312,76 +329,156 @@ __device__ void ws_mma_role(const FwdParams& p, uint32_t base, uint32_t tmem,
         return true;
     };
 
-    for (int rnd = 0, u = unit_of_round(0); u < p.num_units; u = unit_of_round(++rnd)) {
-        const Unit w = decode_unit(u, p);
-        if (!ptx::mbar_wait(ws_bar<D, F>(base, L::kQFull + 0), qf_phase, abort_flag, p.status, lim) ||
-            !ptx::mbar_wait(ws_bar<D, F>(base, L::kQFull + 1), qf_phase, abort_flag, p.status, lim))
-            break;
-        qf_phase ^= 1u;
-        // Key tiles run over the union of both query tiles' active tiles; each
-        // product is issued only for a query tile that uses the key tile.
-        const int last0 = last_active<M>(p, w, 0), last1 = last_active<M>(p, w, 1);
-        if (last0 < 0) ptx::mma_commit(ws_bar<D, F>(base, L::kQEmpty + 0));
-        if (last1 < 0) ptx::mma_commit(ws_bar<D, F>(base, L::kQEmpty + 1));
-        bool first0 = true, first1 = true, ok = true;
-        int j = next_union<M>(p, w, -1);
-        int kslot, vslot;
-        if (j < w.n) {
-            if (!wait_ring(kslot)) break;
-            if (tile_active<M>(p, w, 0, j)) {
+    if constexpr (!M) {
+        // Without a block mask both query tiles use every key tile below their
+        // causal bound, and query tile 0 of a unit finishes one key tile before
+        // tile 1 (or with it).  The issuer then starts the next unit's first
+        // product S_0 = Q_0 K_0^T in the last step, before the final
+        // O_1 += P_1 V, whose P_1 the other softmax warpgroup is still
+        // computing: otherwise the tensor core idles through that softmax and
+        // again through the next unit's first one.  S_0's tensor memory is free
+        // (P_0 has been consumed) and the softmax warps of tile 0 publish the
+        // next P_0 only after reading O_0 out, so O_0 is not overwritten early.
+        bool pre = false;  // this unit's S_0(0) was issued during the previous unit
+        int pre_kslot = 0;
+        for (int rnd = 0, u = unit_of_round(0); u < p.num_units; u = unit_of_round(++rnd)) {
+            const Unit w = decode_unit(u, p);
+            if ((!pre && !ptx::mbar_wait(ws_bar<D, F>(base, L::kQFull + 0), qf_phase, abort_flag, p.status, lim)) ||
+                !ptx::mbar_wait(ws_bar<D, F>(base, L::kQFull + 1), qf_phase, abort_flag, p.status, lim))
+                break;
+            qf_phase ^= 1u;
+            ptx::tc_fence_after();
+            const int last0 = w.n0 - 1, last1 = w.n1 - 1;
+            int kslot, vslot;
+            if (pre) {
+                kslot = pre_kslot;
+            } else {
+                if (!wait_ring(kslot)) break;
                 issue_s(0, kslot);
-                if (j == last0) ptx::mma_commit(ws_bar<D, F>(base, L::kQEmpty + 0));
+                if (last0 == 0) ptx::mma_commit(ws_bar<D, F>(base, L::kQEmpty + 0));
             }
-            if (tile_active<M>(p, w, 1, j)) {
-                issue_s(1, kslot);
-                if (j == last1) ptx::mma_commit(ws_bar<D, F>(base, L::kQEmpty + 1));
-            }
+            pre = false;
+            issue_s(1, kslot);
+            if (last1 == 0) ptx::mma_commit(ws_bar<D, F>(base, L::kQEmpty + 1));
             ptx::mma_commit(ws_bar<D, F>(base, L::kKVEmpty + kslot));
-        }
-        while (j < w.n) {
-            const int jn = next_union<M>(p, w, j);
-            if (!(ok = wait_ring(vslot))) break;
-            if (tile_active<M>(p, w, 0, j)) {
-                if (!(ok = wait_p(0))) break;
-                if (M && first0 && !(ok = wait_o_empty(0))) break;
-                issue_pv(0, vslot, !first0);
-                first0 = false;
-                if (j == last0) ptx::mma_commit(ws_bar<D, F>(base, L::kOFull + 0));
-            }
-            const bool more = jn < w.n;
-            if (more) {
-                if (!(ok = wait_ring(kslot))) break;
-                if (tile_active<M>(p, w, 0, jn)) {
-                    issue_s(0, kslot);
-                    if (jn == last0) ptx::mma_commit(ws_bar<D, F>(base, L::kQEmpty + 0));
+            bool ok = true;
+            for (int j = 0; j < w.n; ++j) {
+                const int jn = j + 1;
+                if (!(ok = wait_ring(vslot))) break;
+                if (j < w.n0) {
+                    if (!(ok = wait_p(0))) break;
+                    issue_pv(0, vslot, j > 0);
+                    if (j == last0) ptx::mma_commit(ws_bar<D, F>(base, L::kOFull + 0));
+                }
+                const bool more = jn < w.n;
+                if (more) {
+                    if (!(ok = wait_ring(kslot))) break;
+                    if (jn < w.n0) {
+                        issue_s(0, kslot);
+                        if (jn == last0) ptx::mma_commit(ws_bar<D, F>(base, L::kQEmpty + 0));
+                    }
+                } else {
+                    const int u2 = unit_of_round(rnd + 1);
+                    if (u2 < p.num_units) {  // the next unit's S_0(0)
+                        const Unit w2 = decode_unit(u2, p);
+                        if (!(ok = ptx::mbar_wait(ws_bar<D, F>(base, L::kQFull + 0), qf_phase, abort_flag,
+                                                  p.status, lim)))
+                            break;
+                        ptx::tc_fence_after();
+                        if (!(ok = wait_ring(pre_kslot))) break;
+                        issue_s(0, pre_kslot);
+                        if (w2.n0 == 1) ptx::mma_commit(ws_bar<D, F>(base, L::kQEmpty + 0));
+                        pre = true;
+                    }
+                }
+                if (j < w.n1) {
+                    if (!(ok = wait_p(1))) break;
+                    issue_pv(1, vslot, j > 0);
+                    if (j == last1) ptx::mma_commit(ws_bar<D, F>(base, L::kOFull + 1));
+                }
+                ptx::mma_commit(ws_bar<D, F>(base, L::kKVEmpty + vslot));
+                if (more) {
+                    if (jn < w.n1) {
+                        issue_s(1, kslot);
+                        if (jn == last1) ptx::mma_commit(ws_bar<D, F>(base, L::kQEmpty + 1));
+                    }
+                    ptx::mma_commit(ws_bar<D, F>(base, L::kKVEmpty + kslot));
                 }
             }
-            if (tile_active<M>(p, w, 1, j)) {
-                if (!(ok = wait_p(1))) break;
-                if (M && first1 && !(ok = wait_o_empty(1))) break;
-                issue_pv(1, vslot, !first1);
-                first1 = false;
-                if (j == last1) ptx::mma_commit(ws_bar<D, F>(base, L::kOFull + 1));
-            }
-            ptx::mma_commit(ws_bar<D, F>(base, L::kKVEmpty + vslot));
-            if (more) {
-                if (tile_active<M>(p, w, 1, jn)) {
+            if (!ok) break;
+        }
+    } else {
+        for (int rnd = 0, u = unit_of_round(0); u < p.num_units; u = unit_of_round(++rnd)) {
+            const Unit w = decode_unit(u, p);
+            if (!ptx::mbar_wait(ws_bar<D, F>(base, L::kQFull + 0), qf_phase, abort_flag, p.status, lim) ||
+                !ptx::mbar_wait(ws_bar<D, F>(base, L::kQFull + 1), qf_phase, abort_flag, p.status, lim))
+                break;
+            qf_phase ^= 1u;
+            // Key tiles run over the union of both query tiles' active tiles; each
+            // product is issued only for a query tile that uses the key tile.
+            const int last0 = last_active<M>(p, w, 0), last1 = last_active<M>(p, w, 1);
+            if (last0 < 0) ptx::mma_commit(ws_bar<D, F>(base, L::kQEmpty + 0));
+            if (last1 < 0) ptx::mma_commit(ws_bar<D, F>(base, L::kQEmpty + 1));
+            bool first0 = true, first1 = true, ok = true;
+            int j = next_union<M>(p, w, -1);
+            int kslot, vslot;
+            if (j < w.n) {
+                if (!wait_ring(kslot)) break;
+                if (tile_active<M>(p, w, 0, j)) {
+                    issue_s(0, kslot);
+                    if (j == last0) ptx::mma_commit(ws_bar<D, F>(base, L::kQEmpty + 0));
+                }
+                if (tile_active<M>(p, w, 1, j)) {
                     issue_s(1, kslot);
-                    if (jn == last1) ptx::mma_commit(ws_bar<D, F>(base, L::kQEmpty + 1));
+                    if (j == last1) ptx::mma_commit(ws_bar<D, F>(base, L::kQEmpty + 1));
                 }
                 ptx::mma_commit(ws_bar<D, F>(base, L::kKVEmpty + kslot));
             }
-            j = jn;
-        }
-        if (!ok) break;
-        // A query tile with no key tile still completes its O phase.
-        if (last0 < 0) {
-            if (!wait_o_empty(0)) break;
-            ptx::mma_commit(ws_bar<D, F>(base, L::kOFull + 0));
-        }
-        if (last1 < 0) {
-            if (!wait_o_empty(1)) break;
-            ptx::mma_commit(ws_bar<D, F>(base, L::kOFull + 1));
+            while (j < w.n) {
+                const int jn = next_union<M>(p, w, j);
+                if (!(ok = wait_ring(vslot))) break;
+                if (tile_active<M>(p, w, 0, j)) {
+                    if (!(ok = wait_p(0))) break;
+                    if (M && first0 && !(ok = wait_o_empty(0))) break;
+                    issue_pv(0, vslot, !first0);
+                    first0 = false;
+                    if (j == last0) ptx::mma_commit(ws_bar<D, F>(base, L::kOFull + 0));
+                }
+                const bool more = jn < w.n;
+                if (more) {
+                    if (!(ok = wait_ring(kslot))) break;
+                    if (tile_active<M>(p, w, 0, jn)) {
+                        issue_s(0, kslot);
+                        if (jn == last0) ptx::mma_commit(ws_bar<D, F>(base, L::kQEmpty + 0));
+                    }
+                }
+                if (tile_active<M>(p, w, 1, j)) {
+                    if (!(ok = wait_p(1))) break;
+                    if (M && first1 && !(ok = wait_o_empty(1))) break;
+                    issue_pv(1, vslot, !first1);
+                    first1 = false;
+                    if (j == last1) ptx::mma_commit(ws_bar<D, F>(base, L::kOFull + 1));
+                }
+                ptx::mma_commit(ws_bar<D, F>(base, L::kKVEmpty + vslot));
+                if (more) {
+                    if (tile_active<M>(p, w, 1, jn)) {
+                        issue_s(1, kslot);
+                        if (jn == last1) ptx::mma_commit(ws_bar<D, F>(base, L::kQEmpty + 1));
+                    }
+                    ptx::mma_commit(ws_bar<D, F>(base, L::kKVEmpty + kslot));
+                }
+                j = jn;
+            }
+            if (!ok) break;
+            // A query tile with no key tile still completes its O phase.
+            if (last0 < 0) {
+                if (!wait_o_empty(0)) break;
+                ptx::mma_commit(ws_bar<D, F>(base, L::kOFull + 0));
+            }
+            if (last1 < 0) {
+                if (!wait_o_empty(1)) break;
+                ptx::mma_commit(ws_bar<D, F>(base, L::kOFull + 1));
+            }
         }
     }
     // Every MMA issued above completes before TMEM can be released.
