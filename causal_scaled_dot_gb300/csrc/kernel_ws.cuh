@@ -66,8 +66,8 @@ struct WsLayout {
     static constexpr int kThreads = 384;
     // Registers per thread after the split: warps 0-3 (producer, MMA issuer,
     // idle) shrink, the softmax warps grow.  Launch allocation: 384 x 168 =
-    // 64512 >= 128 x kRegsSmall + 256 x kRegsSoftmax = 62464.
-    static constexpr int kRegsSmall = 56;
+    // 64512 >= 128 x kRegsSmall + 256 x kRegsSoftmax = 63488.
+    static constexpr int kRegsSmall = 64;
     static constexpr int kRegsSoftmax = 216;
     static_assert(128 * kRegsSmall + 256 * kRegsSoftmax <= kThreads * 168, "register split");
     static constexpr uint32_t kTileBytes = kTile * D * kElemBytes;  // 32 KB at bf16 D = 128
@@ -99,12 +99,27 @@ struct WsLayout {
 
 // Unit u -> (bh, pair m).  Causal: heaviest pairs first.  Within a pair index
 // consecutive u walk bh = b*Hq + hq, so GQA siblings are adjacent.  n0 / n1
-// bound the key tiles of query tile 2m / 2m+1 (causality, sequence end); with
-// a block mask some tiles below the bound are dropped too (tile_active).
+// bound the key tiles of the unit's query tiles qt[0] / qt[1] (causality,
+// sequence end); with a block mask some tiles below the bound are dropped too
+// (tile_active).
+//
+// Key direction: units of odd rounds walk their key tiles from the highest
+// down to 0, and units of even rounds from 0 up.  The
+// CTAs of one round run their units roughly in step, so a round ends on the
+// key tiles the next round starts with and those are still in L2 (a
+// least-recently-used model of the profile shape, B4 H16 S4096, puts the
+// K/V bytes read from DRAM at 273 MB instead of 471 MB).  A descending unit
+// swaps its query tiles -- qt[0] = 2m+1, qt[1] = 2m -- so that query tile 0
+// always holds the key tile the other lacks at the unit's boundary with the
+// previous unit: first in a descending unit, last in an ascending one (the
+// issuer starts a unit's first S_0 inside the previous unit).  The order is
+// fixed by the unit's round, so results are deterministic for a given grid.
 struct Unit {
     int bh, hq, m, kv_bh, n0, n1, n;
+    int qt[2];  // query tiles of softmax warpgroups 0 and 1
+    bool desc;  // key tiles visited from n-1 down to 0
 };
-__device__ __forceinline__ Unit decode_unit(int u, const FwdParams& p) {
+__device__ __forceinline__ Unit decode_unit(int u, const FwdParams& p, bool desc = false) {
     const int BH = p.B * p.Hq;
     const int npairs = (p.num_q_tiles + 1) >> 1;
     Unit w;
@@ -114,18 +129,24 @@ __device__ __forceinline__ Unit decode_unit(int u, const FwdParams& p) {
     const int hq = w.bh - b * p.Hq;
     w.hq = hq;
     w.kv_bh = b * p.Hkv + hq / p.group;
-    const int qt0 = 2 * w.m, qt1 = 2 * w.m + 1;
+    w.desc = desc;
+    w.qt[0] = 2 * w.m + (desc ? 1 : 0);
+    w.qt[1] = 2 * w.m + (desc ? 0 : 1);
     if (p.causal) {
-        w.n0 = min(qt0 + 1, p.num_q_tiles);
-        w.n1 = min(qt1 + 1, p.num_q_tiles);
+        w.n0 = min(w.qt[0] + 1, p.num_q_tiles);
+        w.n1 = min(w.qt[1] + 1, p.num_q_tiles);
     } else {
         w.n0 = w.n1 = p.num_q_tiles;
     }
     w.n = max(w.n0, w.n1);
     return w;
 }
+// The key direction of the units of round r.
+__device__ __forceinline__ bool round_desc(int r) { return (r & 1) != 0; }
+// Key tile visited at step s (0 <= s < n) of a unit without a block mask.
+__device__ __forceinline__ int key_of_step(const Unit& w, int s) { return w.desc ? w.n - 1 - s : s; }
 
-// Does query tile 2m + i of unit w use key tile j?  M (block mask present) is
+// Does query tile qt[i] of unit w use key tile j?  M (block mask present) is
 // a template flag so that the unmasked kernel keeps its plain counting loops:
 // without a mask, tile i uses key tiles [0, n_i) (the odd last query tile of a
 // pair, past the sequence end, runs too and writes nothing).  With a mask, a
@@ -137,33 +158,41 @@ __device__ __forceinline__ bool tile_active(const FwdParams& p, const Unit& w, i
     if constexpr (!M) {
         return true;
     } else {
-        const int qt = 2 * w.m + i;
+        const int qt = w.qt[i];
         if (qt >= p.num_q_tiles) return false;
         const int nt = p.num_q_tiles;
         return __ldg(p.block_mask + ((size_t)(p.mask_heads == 1 ? 0 : w.hq) * nt + qt) * nt + j) != 0;
     }
 }
-// First key tile after j that either query tile uses (w.n if none).
+// Visit order of a unit's key tiles with a block mask: the union of both query
+// tiles' kept tiles, ascending or descending with the unit.  -1 ends the walk.
 template <bool M>
-__device__ __forceinline__ int next_union(const FwdParams& p, const Unit& w, int j) {
-    if constexpr (!M) {
-        return j + 1;  // every j < n = max(n0, n1) is used by one of the two
+__device__ __forceinline__ int next_visit(const FwdParams& p, const Unit& w, int j) {
+    if (w.desc) {
+        for (--j; j >= 0; --j)
+            if (tile_active<M>(p, w, 0, j) || tile_active<M>(p, w, 1, j)) return j;
     } else {
         for (++j; j < w.n; ++j)
             if (tile_active<M>(p, w, 0, j) || tile_active<M>(p, w, 1, j)) return j;
-        return w.n;
     }
+    return -1;
 }
-// Last key tile query tile i uses (-1 if none).
 template <bool M>
-__device__ __forceinline__ int last_active(const FwdParams& p, const Unit& w, int i) {
-    if constexpr (!M) {
-        return (i == 0 ? w.n0 : w.n1) - 1;
-    } else {
-        for (int j = (i == 0 ? w.n0 : w.n1) - 1; j >= 0; --j)
+__device__ __forceinline__ int first_visit(const FwdParams& p, const Unit& w) {
+    return next_visit<M>(p, w, w.desc ? w.n : -1);
+}
+// The key tile query tile i uses last in the unit's visit order (-1 if none).
+template <bool M>
+__device__ __forceinline__ int last_visit(const FwdParams& p, const Unit& w, int i) {
+    const int n_i = i == 0 ? w.n0 : w.n1;
+    if (w.desc) {
+        for (int j = 0; j < n_i; ++j)
             if (tile_active<M>(p, w, i, j)) return j;
-        return -1;
+    } else {
+        for (int j = n_i - 1; j >= 0; --j)
+            if (tile_active<M>(p, w, i, j)) return j;
     }
+    return -1;
 }
 
 // The unit this CTA runs in round r (>= num_units: no more work).
@@ -200,14 +229,13 @@ __device__ void ws_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
         const uint32_t dst = base + (i == 0 ? L::kQ0 : L::kQ1);
 #pragma unroll
         for (int c = 0; c < L::kChunks; ++c)
-            ptx::tma_load_3d(dst + c * L::kChunkBytes, tm_q, full, c * L::kRowElems, (2 * w.m + i) * kTile,
-                             w.bh);
+            ptx::tma_load_3d(dst + c * L::kChunkBytes, tm_q, full, c * L::kRowElems, w.qt[i] * kTile, w.bh);
         pend_q |= 1u << i;
         pend_q_par = (pend_q_par & ~(1u << i)) | (((qe_phase[i] ^ 1u) & 1u) << i);
         return true;
     };
     for (int rnd = 0, u = unit_of_round(0); u < p.num_units; u = unit_of_round(++rnd)) {
-        const Unit w = decode_unit(u, p);
+        const Unit w = decode_unit(u, p, round_desc(rnd));
         // Without a block mask the issuer starts a unit's first S_0 = Q_0 K_0^T
         // while the previous unit's last softmax runs (see the MMA role), so
         // the unit's first K is loaded right after Q_0: Q_1's slot frees only
@@ -218,7 +246,11 @@ __device__ void ws_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
             if (!load_q(w, 1)) goto drain;
             q1_loaded = true;
         }
-        for (int j = next_union<M>(p, w, -1); j < w.n; j = next_union<M>(p, w, j)) {
+        // Key tiles in the order the issuer consumes them: every step of the
+        // unit's direction without a block mask, the union of both query
+        // tiles' kept tiles in that direction with one.
+        for (int st = 0, j = M ? first_visit<M>(p, w) : key_of_step(w, 0); M ? j >= 0 : st < w.n;
+             ++st, j = M ? next_visit<M>(p, w, j) : key_of_step(w, st)) {
 #pragma unroll
             for (int t = 0; t < 2; ++t) {  // t = 0: K_j, t = 1: V_j
                 if (!ptx::mbar_wait(ws_bar<D, F>(base, L::kKVEmpty + slot), ring_phase ^ 1u, abort_flag,
@@ -331,24 +363,31 @@ __device__ void ws_mma_role(const FwdParams& p, uint32_t base, uint32_t tmem,
 
     if constexpr (!M) {
         // Without a block mask both query tiles use every key tile below their
-        // causal bound, and query tile 0 of a unit finishes one key tile before
-        // tile 1 (or with it).  The issuer then starts the next unit's first
-        // product S_0 = Q_0 K_0^T in the last step, before the final
-        // O_1 += P_1 V, whose P_1 the other softmax warpgroup is still
-        // computing: otherwise the tensor core idles through that softmax and
-        // again through the next unit's first one.  S_0's tensor memory is free
-        // (P_0 has been consumed) and the softmax warps of tile 0 publish the
-        // next P_0 only after reading O_0 out, so O_0 is not overwritten early.
-        bool pre = false;  // this unit's S_0(0) was issued during the previous unit
+        // causal bound.  In a unit's last step the issuer starts the next
+        // unit's first product S_0 = Q_0 K^T before the final O_1 += P_1 V,
+        // whose P_1 the other softmax warpgroup is still computing: otherwise
+        // the tensor core idles through that softmax and again through the
+        // next unit's first one.  S_0's tensor memory is free (P_0 has been
+        // consumed) and the softmax warps of tile 0 publish the next P_0 only
+        // after reading O_0 out, so O_0 is not overwritten early.
+        bool pre = false;  // this unit's first S_0 was issued during the previous unit
         int pre_kslot = 0;
         for (int rnd = 0, u = unit_of_round(0); u < p.num_units; u = unit_of_round(++rnd)) {
-            const Unit w = decode_unit(u, p);
+            const Unit w = decode_unit(u, p, round_desc(rnd));
             if ((!pre && !ptx::mbar_wait(ws_bar<D, F>(base, L::kQFull + 0), qf_phase, abort_flag, p.status, lim)) ||
                 !ptx::mbar_wait(ws_bar<D, F>(base, L::kQFull + 1), qf_phase, abort_flag, p.status, lim))
                 break;
             qf_phase ^= 1u;
             ptx::tc_fence_after();
-            const int last0 = w.n0 - 1, last1 = w.n1 - 1;
+            // Step s visits key tile key_of_step(w, s); query tile i uses it when
+            // that key tile is below n_i.  Ascending: tile i uses steps
+            // [0, n_i); descending: steps [n - n_i, n).  Tile 0 uses step 0
+            // either way (n0 >= n1 when descending).
+            const int n = w.n;
+            const int first1 = w.desc ? n - w.n1 : 0;
+            const int last0 = w.desc ? n - 1 : w.n0 - 1, last1 = w.desc ? n - 1 : w.n1 - 1;
+            auto act0 = [&](int st) { return w.desc || st < w.n0; };
+            auto act1 = [&](int st) { return st >= first1 && st <= last1; };
             int kslot, vslot;
             if (pre) {
                 kslot = pre_kslot;
@@ -358,49 +397,51 @@ __device__ void ws_mma_role(const FwdParams& p, uint32_t base, uint32_t tmem,
                 if (last0 == 0) ptx::mma_commit(ws_bar<D, F>(base, L::kQEmpty + 0));
             }
             pre = false;
-            issue_s(1, kslot);
-            if (last1 == 0) ptx::mma_commit(ws_bar<D, F>(base, L::kQEmpty + 1));
+            if (act1(0)) {
+                issue_s(1, kslot);
+                if (last1 == 0) ptx::mma_commit(ws_bar<D, F>(base, L::kQEmpty + 1));
+            }
             ptx::mma_commit(ws_bar<D, F>(base, L::kKVEmpty + kslot));
             bool ok = true;
-            for (int j = 0; j < w.n; ++j) {
-                const int jn = j + 1;
+            for (int st = 0; st < n; ++st) {
+                const int sn = st + 1;
                 if (!(ok = wait_ring(vslot))) break;
-                if (j < w.n0) {
+                if (act0(st)) {
                     if (!(ok = wait_p(0))) break;
-                    issue_pv(0, vslot, j > 0);
-                    if (j == last0) ptx::mma_commit(ws_bar<D, F>(base, L::kOFull + 0));
+                    issue_pv(0, vslot, st > 0);
+                    if (st == last0) ptx::mma_commit(ws_bar<D, F>(base, L::kOFull + 0));
                 }
-                const bool more = jn < w.n;
+                const bool more = sn < n;
                 if (more) {
                     if (!(ok = wait_ring(kslot))) break;
-                    if (jn < w.n0) {
+                    if (act0(sn)) {
                         issue_s(0, kslot);
-                        if (jn == last0) ptx::mma_commit(ws_bar<D, F>(base, L::kQEmpty + 0));
+                        if (sn == last0) ptx::mma_commit(ws_bar<D, F>(base, L::kQEmpty + 0));
                     }
                 } else {
                     const int u2 = unit_of_round(rnd + 1);
-                    if (u2 < p.num_units) {  // the next unit's S_0(0)
-                        const Unit w2 = decode_unit(u2, p);
+                    if (u2 < p.num_units) {  // the next unit's first S_0
+                        const Unit w2 = decode_unit(u2, p, round_desc(rnd + 1));
                         if (!(ok = ptx::mbar_wait(ws_bar<D, F>(base, L::kQFull + 0), qf_phase, abort_flag,
                                                   p.status, lim)))
                             break;
                         ptx::tc_fence_after();
                         if (!(ok = wait_ring(pre_kslot))) break;
                         issue_s(0, pre_kslot);
-                        if (w2.n0 == 1) ptx::mma_commit(ws_bar<D, F>(base, L::kQEmpty + 0));
+                        if ((w2.desc ? w2.n : w2.n0) == 1) ptx::mma_commit(ws_bar<D, F>(base, L::kQEmpty + 0));
                         pre = true;
                     }
                 }
-                if (j < w.n1) {
+                if (act1(st)) {
                     if (!(ok = wait_p(1))) break;
-                    issue_pv(1, vslot, j > 0);
-                    if (j == last1) ptx::mma_commit(ws_bar<D, F>(base, L::kOFull + 1));
+                    issue_pv(1, vslot, st > first1);
+                    if (st == last1) ptx::mma_commit(ws_bar<D, F>(base, L::kOFull + 1));
                 }
                 ptx::mma_commit(ws_bar<D, F>(base, L::kKVEmpty + vslot));
                 if (more) {
-                    if (jn < w.n1) {
+                    if (act1(sn)) {
                         issue_s(1, kslot);
-                        if (jn == last1) ptx::mma_commit(ws_bar<D, F>(base, L::kQEmpty + 1));
+                        if (sn == last1) ptx::mma_commit(ws_bar<D, F>(base, L::kQEmpty + 1));
                     }
                     ptx::mma_commit(ws_bar<D, F>(base, L::kKVEmpty + kslot));
                 }
@@ -409,20 +450,20 @@ __device__ void ws_mma_role(const FwdParams& p, uint32_t base, uint32_t tmem,
         }
     } else {
         for (int rnd = 0, u = unit_of_round(0); u < p.num_units; u = unit_of_round(++rnd)) {
-            const Unit w = decode_unit(u, p);
+            const Unit w = decode_unit(u, p, round_desc(rnd));
             if (!ptx::mbar_wait(ws_bar<D, F>(base, L::kQFull + 0), qf_phase, abort_flag, p.status, lim) ||
                 !ptx::mbar_wait(ws_bar<D, F>(base, L::kQFull + 1), qf_phase, abort_flag, p.status, lim))
                 break;
             qf_phase ^= 1u;
             // Key tiles run over the union of both query tiles' active tiles; each
             // product is issued only for a query tile that uses the key tile.
-            const int last0 = last_active<M>(p, w, 0), last1 = last_active<M>(p, w, 1);
+            const int last0 = last_visit<M>(p, w, 0), last1 = last_visit<M>(p, w, 1);
             if (last0 < 0) ptx::mma_commit(ws_bar<D, F>(base, L::kQEmpty + 0));
             if (last1 < 0) ptx::mma_commit(ws_bar<D, F>(base, L::kQEmpty + 1));
             bool first0 = true, first1 = true, ok = true;
-            int j = next_union<M>(p, w, -1);
+            int j = first_visit<M>(p, w);
             int kslot, vslot;
-            if (j < w.n) {
+            if (j >= 0) {
                 if (!wait_ring(kslot)) break;
                 if (tile_active<M>(p, w, 0, j)) {
                     issue_s(0, kslot);
@@ -434,8 +475,8 @@ __device__ void ws_mma_role(const FwdParams& p, uint32_t base, uint32_t tmem,
                 }
                 ptx::mma_commit(ws_bar<D, F>(base, L::kKVEmpty + kslot));
             }
-            while (j < w.n) {
-                const int jn = next_union<M>(p, w, j);
+            while (j >= 0) {
+                const int jn = next_visit<M>(p, w, j);
                 if (!(ok = wait_ring(vslot))) break;
                 if (tile_active<M>(p, w, 0, j)) {
                     if (!(ok = wait_p(0))) break;
@@ -444,7 +485,7 @@ __device__ void ws_mma_role(const FwdParams& p, uint32_t base, uint32_t tmem,
                     first0 = false;
                     if (j == last0) ptx::mma_commit(ws_bar<D, F>(base, L::kOFull + 0));
                 }
-                const bool more = jn < w.n;
+                const bool more = jn >= 0;
                 if (more) {
                     if (!(ok = wait_ring(kslot))) break;
                     if (tile_active<M>(p, w, 0, jn)) {
@@ -507,8 +548,8 @@ __device__ void ws_softmax_role(const CUtensorMap* tm_o, const FwdParams& p, uin
     uint32_t s_phase = 0, o_phase = 0;
 
     for (int rnd = 0, u = unit_of_round(0); u < p.num_units; u = unit_of_round(++rnd)) {
-        const Unit w = decode_unit(u, p);
-        const int qt = 2 * w.m + wg;
+        const Unit w = decode_unit(u, p, round_desc(rnd));
+        const int qt = w.qt[wg];
         const int n_i = wg == 0 ? w.n0 : w.n1;
         float m_run = 0.f;  // reference maximum (log2 units), set by the first tile
         float l_run = 0.f;
@@ -524,15 +565,17 @@ __device__ void ws_softmax_role(const CUtensorMap* tm_o, const FwdParams& p, uin
                 keep_row = p.keep_bits +
                            ((size_t)(p.keep_heads == 1 ? 0 : w.hq) * p.S + row) * (size_t)p.keep_row_bytes;
         }
-        for (int j = 0; j < n_i; ++j) {
+        for (int t = 0; t < n_i; ++t) {
+            const int j = w.desc ? n_i - 1 - t : t;  // the unit's key direction
             if (!tile_active<M>(p, w, wg, j)) continue;
             uint4 keep = make_uint4(~0u, ~0u, ~0u, ~0u);
             if constexpr (E) {
                 if (keep_row != nullptr) {
                     keep = keep_next_j == j ? keep_next : __ldg(reinterpret_cast<const uint4*>(keep_row + 16 * j));
-                    if (j + 1 < n_i) {
-                        keep_next = __ldg(reinterpret_cast<const uint4*>(keep_row + 16 * (j + 1)));
-                        keep_next_j = j + 1;
+                    if (t + 1 < n_i) {
+                        const int jn = w.desc ? j - 1 : j + 1;
+                        keep_next = __ldg(reinterpret_cast<const uint4*>(keep_row + 16 * jn));
+                        keep_next_j = jn;
                     }
                 }
             }
