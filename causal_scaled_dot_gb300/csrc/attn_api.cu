@@ -312,6 +312,7 @@ extern "C" int attn_fwd_dropout(const void* q, const void* k, const void* v, voi
     if (!std::isfinite(dropout_p) || dropout_p < 0.f) return ATTN_ERR_INVALID_ARG;
     const long p8 = std::lrint((double)dropout_p * 256.0);
     if (p8 > 255) return ATTN_ERR_INVALID_ARG;
+    if (p8 > 0 && offset > 0xFFFFFFFFull) return ATTN_ERR_INVALID_ARG;  // a 32-bit counter word
     return attn::fwd_bf16(q, k, v, out, lse, B, Hq, Hkv, S, D, scale, causal, nullptr, 1, (int)p8,
                           seed, offset, stream);
 }
@@ -421,6 +422,7 @@ extern "C" int attn_fwd_ex(const void* q, const void* k, const void* v, void* ou
     if (!std::isfinite(opts->dropout_p) || opts->dropout_p < 0.f) return ATTN_ERR_INVALID_ARG;
     const long p8 = std::lrint((double)opts->dropout_p * 256.0);
     if (p8 > 255) return ATTN_ERR_INVALID_ARG;
+    if (p8 > 0 && opts->offset > 0xFFFFFFFFull) return ATTN_ERR_INVALID_ARG;  // a 32-bit counter word
     const float ds[3] = {opts->q_descale, opts->k_descale, opts->v_descale};
     return attn::fwd_bf16(q, k, v, out, lse, B, Hq, Hkv, S, D, scale, causal, opts->block_mask,
                           opts->block_mask != nullptr ? opts->mask_heads : 1, (int)p8, opts->seed,

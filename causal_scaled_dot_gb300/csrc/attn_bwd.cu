@@ -179,6 +179,7 @@ extern "C" int attn_bwd_ex(const void* q, const void* k, const void* v, const vo
     if (!std::isfinite(opts->dropout_p) || opts->dropout_p < 0.f) return ATTN_ERR_INVALID_ARG;
     const long p8 = std::lrint((double)opts->dropout_p * 256.0);
     if (p8 > 255) return ATTN_ERR_INVALID_ARG;
+    if (p8 > 0 && opts->offset > 0xFFFFFFFFull) return ATTN_ERR_INVALID_ARG;  // a 32-bit counter word
     return attn::bwd(q, k, v, out, dout, lse, delta, dq, dk, dv, B, Hq, Hkv, S, D, scale, causal,
                      opts->block_mask, opts->block_mask != nullptr ? opts->mask_heads : 1, stream,
                      opts->keep_bits, opts->keep_bits != nullptr ? opts->keep_heads : 1, (int)p8,
@@ -193,6 +194,7 @@ extern "C" int attn_bwd_dropout(const void* q, const void* k, const void* v, con
     if (!std::isfinite(dropout_p) || dropout_p < 0.f) return ATTN_ERR_INVALID_ARG;
     const long p8 = std::lrint((double)dropout_p * 256.0);
     if (p8 > 255) return ATTN_ERR_INVALID_ARG;
+    if (p8 > 0 && offset > 0xFFFFFFFFull) return ATTN_ERR_INVALID_ARG;  // a 32-bit counter word
     return attn::bwd(q, k, v, out, dout, lse, delta, dq, dk, dv, B, Hq, Hkv, S, D, scale, causal,
                      nullptr, 1, stream, nullptr, 1, (int)p8, seed, offset);
 }

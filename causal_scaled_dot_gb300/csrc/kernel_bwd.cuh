@@ -83,9 +83,10 @@ struct BwdParams {
     const uint8_t* keep_bits;   // element-masked kernels: [keep_heads][S][keep_row_bytes]
     int keep_heads;             // 1 or Hq
     int keep_row_bytes;         // 16 per 128 keys
-    // Dropout kernels: weight (i, j) of head bh kept when byte j % 32 of the
-    // Philox block {j / 32, i, bh, 0} under key {seed, offset} is >= p8; kept
-    // weights are scaled by keep_scale = 256 / (256 - p8) (as in the forward).
+    // Dropout kernels: weight (i, j) of head bh kept when byte j % 16 of the
+    // Philox4x32-10 block {j / 16, i, bh, offset} under key {seed_lo, seed_hi}
+    // is >= p8 (philox.cuh); kept weights are scaled by keep_scale =
+    // 256 / (256 - p8) (as in the forward).
     int dropout_p8;
     unsigned long long dropout_seed, dropout_offset;
     float keep_scale;
@@ -133,7 +134,7 @@ struct StreamPos {
 template <int D>
 struct DqLayout {
     static constexpr int kThreads = 384;
-    static constexpr int kRegsSmall = 56;
+    static constexpr int kRegsSmall = 64;
     static constexpr int kRegsWork = 216;
     static_assert(128 * kRegsSmall + 256 * kRegsWork <= kThreads * 168, "register split");
     static constexpr uint32_t kTileBytes = kTile * D * 2;
@@ -528,22 +529,18 @@ __device__ void dq_work_role(const BwdParams& p, uint32_t base, const uint8_t* s
                         if ((((c < 32 ? keep.x : keep.y) >> (c & 31)) & 1u) == 0u) pr[c] = 0.f;
                 }
             }
-            // Dropout: keep decisions of this row's 64 keys (two Philox blocks),
-            // made while the dP product runs.  A dropped weight's dP is 0, a
-            // kept one's is scaled by keep_scale.
+            // Dropout: keep decisions of this row's 64 keys (four Philox
+            // blocks), made while the dP product runs.  A dropped weight's dP
+            // is 0, a kept one's is scaled by keep_scale.
             uint64_t zb = ~0ull;
             if constexpr (DR) {
                 zb = 0ull;
 #pragma unroll
-                for (int b = 0; b < 2; ++b) {
-                    uint64_t rnd[4];
-                    philox4x64_10((uint64_t)((key0 >> 5) + b), (uint64_t)row, (uint64_t)w.bh, 0ull,
-                                  p.dropout_seed, p.dropout_offset, rnd);
-#pragma unroll
-                    for (int c = 0; c < 32; ++c)
-                        zb |= (uint64_t)(((uint32_t)(rnd[c >> 3] >> (8 * (c & 7))) & 0xFFu) >= (uint32_t)p.dropout_p8)
-                              << (32 * b + c);
-                }
+                for (int b = 0; b < 4; ++b)
+                    zb |= (uint64_t)dropout_keep16((uint32_t)((key0 >> 4) + b), (uint32_t)row, (uint32_t)w.bh,
+                                                   (uint32_t)p.dropout_offset, (uint32_t)p.dropout_seed,
+                                                   (uint32_t)(p.dropout_seed >> 32), (256u - (uint32_t)p.dropout_p8) * 0x01010101u)
+                          << (16 * b);
             }
             const float ks = DR ? p.keep_scale : 1.f;
 
@@ -999,24 +996,25 @@ __device__ void dkv_work_role(const BwdParams& p, uint32_t base, const uint8_t* 
             dkv_iter(w, p, t, bh, qt);
             bool ok = ptx::mbar_wait(dkv_bar<L>(base, L::kStatFull + st), ring_phase, abort_flag, p.status, lim);
             if constexpr (DR) {
-                // The tile's 128 x 128 keep decisions: 512 Philox blocks (a query
-                // and 32 keys each), two per element-wise thread, written as bits
-                // into the stage in the element-mask layout while S^T is being
-                // computed; every thread then waits for all 256 to have written.
+                // The tile's 128 x 128 keep decisions: 1024 Philox blocks (a query
+                // and 16 keys each), four per element-wise thread, written as bits
+                // into the stage in the element-mask layout (a 32-bit word per
+                // query and 32 keys) while S^T is being computed; every thread
+                // then waits for all 256 to have written.
                 if (!__all_sync(0xffffffffu, ok)) return;
                 uint32_t* keepw = reinterpret_cast<uint32_t*>(
                     const_cast<uint8_t*>(smem) + L::kStat + (uint32_t)st * L::kStatBytes + L::kStatDrop);
                 const int et = threadIdx.x - 128;  // 0 .. 255
 #pragma unroll
                 for (int y = 0; y < 2; ++y) {
-                    const int x = 2 * et + y, qq = x >> 2, b = x & 3;
-                    uint64_t rnd[4];
-                    philox4x64_10((uint64_t)(w.kt * 4 + b), (uint64_t)(qt * kTile + qq), (uint64_t)bh, 0ull,
-                                  p.dropout_seed, p.dropout_offset, rnd);
+                    const int x = 2 * et + y, qq = x >> 2, b = x & 3;  // query qq, keys 32b .. 32b+31
                     uint32_t bits = 0u;
 #pragma unroll
-                    for (int c = 0; c < 32; ++c)
-                        bits |= (((uint32_t)(rnd[c >> 3] >> (8 * (c & 7))) & 0xFFu) >= (uint32_t)p.dropout_p8 ? 1u : 0u) << c;
+                    for (int h = 0; h < 2; ++h)
+                        bits |= dropout_keep16((uint32_t)(w.kt * 8 + 2 * b + h), (uint32_t)(qt * kTile + qq),
+                                               (uint32_t)bh, (uint32_t)p.dropout_offset, (uint32_t)p.dropout_seed,
+                                               (uint32_t)(p.dropout_seed >> 32), (256u - (uint32_t)p.dropout_p8) * 0x01010101u)
+                                << (16 * h);
                     keepw[4 * qq + b] = bits;
                 }
                 ptx::mbar_arrive(dkv_bar<L>(base, L::kBitsReady));

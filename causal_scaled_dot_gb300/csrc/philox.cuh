@@ -1,6 +1,12 @@
-// philox.cuh -- Philox4x64-10 counter-based random numbers (Salmon, Moraes,
+// philox.cuh -- Philox4x32-10 counter-based random numbers (Salmon, Moraes,
 // Dror and Shaw, "Parallel random numbers: as easy as 1, 2, 3", SC 2011), for
-// the dropout of attention weights.
+// the dropout of attention weights.  The 32-bit variant: each round is two
+// 32 x 32 -> 64-bit multiplies, which the GPU does natively.
+//
+// Keep rule shared by the forward and both backward kernels: weight (i, j) of
+// flat head bh = b*Hq + hq is kept when byte j % 16 of the block for counter
+// {j / 16, i, bh, offset} under key {seed_lo, seed_hi} is >= p8, the block's
+// 16 bytes taken word 0 first, each word little-endian.
 #pragma once
 
 #include <cstdint>
@@ -10,18 +16,18 @@ namespace attn {
 // Ten rounds of (x0, x1, x2, x3) <- (hi(M1 x2) ^ x1 ^ k0, lo(M1 x2),
 // hi(M0 x0) ^ x3 ^ k1, lo(M0 x0)), the key bumped by the Weyl constants after
 // every round.
-__device__ __forceinline__ void philox4x64_10(uint64_t x0, uint64_t x1, uint64_t x2, uint64_t x3,
-                                              uint64_t k0, uint64_t k1, uint64_t out[4]) {
-    constexpr uint64_t kM0 = 0xD2E7470EE14C6C93ull, kM1 = 0xCA5A826395121157ull;
-    constexpr uint64_t kW0 = 0x9E3779B97F4A7C15ull, kW1 = 0xBB67AE8584CAA73Bull;
+__device__ __forceinline__ void philox4x32_10(uint32_t x0, uint32_t x1, uint32_t x2, uint32_t x3, uint32_t k0,
+                                              uint32_t k1, uint32_t out[4]) {
+    constexpr uint32_t kM0 = 0xD2511F53u, kM1 = 0xCD9E8D57u;
+    constexpr uint32_t kW0 = 0x9E3779B9u, kW1 = 0xBB67AE85u;
 #pragma unroll
     for (int r = 0; r < 10; ++r) {
-        const uint64_t hi0 = __umul64hi(kM0, x0), lo0 = kM0 * x0;
-        const uint64_t hi1 = __umul64hi(kM1, x2), lo1 = kM1 * x2;
-        x0 = hi1 ^ x1 ^ k0;
-        x1 = lo1;
-        x2 = hi0 ^ x3 ^ k1;
-        x3 = lo0;
+        const uint64_t p0 = (uint64_t)kM0 * x0;
+        const uint64_t p1 = (uint64_t)kM1 * x2;
+        x0 = (uint32_t)(p1 >> 32) ^ x1 ^ k0;
+        x1 = (uint32_t)p1;
+        x2 = (uint32_t)(p0 >> 32) ^ x3 ^ k1;
+        x3 = (uint32_t)p0;
         k0 += kW0;
         k1 += kW1;
     }
@@ -29,6 +35,40 @@ __device__ __forceinline__ void philox4x64_10(uint64_t x0, uint64_t x1, uint64_t
     out[1] = x1;
     out[2] = x2;
     out[3] = x3;
+}
+
+// Keep decisions of four keys at once.  `x` holds four random bytes and `c4`
+// the byte 256 - p8 (1 <= p8 <= 255) in each of its bytes: byte b of x is
+// >= p8 exactly when x_b + (256 - p8) carries out of the byte.  The carry out
+// of bit 7 is the majority of the two top bits and the carry into bit 7 (bit
+// 7 of the sum of the low seven bits, which cannot overflow a byte); it is
+// returned in bit 7 of each byte, the other bits are not meaningful.
+__device__ __forceinline__ uint32_t bytes_ge(uint32_t x, uint32_t c4) {
+    const uint32_t low = (x & 0x7F7F7F7Fu) + (c4 & 0x7F7F7F7Fu);
+    return (x & c4) | ((x | c4) & low);
+}
+// A mask for a packed bf16 pair from two of those decisions: every bit of the
+// low (high) half copies bit 7 of byte `b0` (`b0` + 1) of `ge`; `sel` =
+// 0x9988 for bytes 0-1, 0xBBAA for bytes 2-3 (prmt with sign replication).
+__device__ __forceinline__ uint32_t pair_mask(uint32_t ge, uint32_t sel) {
+    uint32_t m;
+    asm("prmt.b32 %0, %1, 0, %2;" : "=r"(m) : "r"(ge), "r"(sel));
+    return m;
+}
+
+// The 16 keep decisions of block {key_block, row, bh, offset} (bit c for key
+// 16*key_block + c); c4 as in bytes_ge.  Each word's four decisions (bit 7 of
+// its bytes) are gathered into four adjacent bits by one multiply: bits 0, 8,
+// 16, 24 times 2^28 + 2^21 + 2^14 + 2^7 land on bits 28-31 with no carries.
+__device__ __forceinline__ uint32_t dropout_keep16(uint32_t key_block, uint32_t row, uint32_t bh, uint32_t offset,
+                                                   uint32_t seed_lo, uint32_t seed_hi, uint32_t c4) {
+    uint32_t r[4];
+    philox4x32_10(key_block, row, bh, offset, seed_lo, seed_hi, r);
+    uint32_t bits = 0u;
+#pragma unroll
+    for (int w = 0; w < 4; ++w)
+        bits |= ((((bytes_ge(r[w], c4) >> 7) & 0x01010101u) * 0x10204080u) >> 28) << (4 * w);
+    return bits;
 }
 
 }  // namespace attn

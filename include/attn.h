@@ -154,14 +154,17 @@ int attn_fwd_block_masked(const void *q, const void *k, const void *v, void *out
  *   dropout_p   0 <= p < 1, rounded to p8 / 256 with p8 = round(256 p), and
  *               p8 <= 255 (ATTN_ERR_INVALID_ARG otherwise); p8 = 0 is attn_fwd.
  *               Kept weights are scaled by 256 / (256 - p8).
- *   seed, offset  the Philox4x64-10 key {seed, offset}.
+ *   seed     the 64-bit Philox4x32-10 key {low 32 bits, high 32 bits}.
+ *   offset   a 32-bit counter word (0 <= offset < 2^32, ATTN_ERR_INVALID_ARG
+ *            otherwise): calls with different offsets draw independent masks.
  * Which weights are dropped: key j of query row i of head b*Hq + hq is kept
- * when byte (j mod 32) of Philox4x64-10(counter {j / 32, i, b*Hq + hq, 0},
- * key {seed, offset}) -- the four 64-bit output words in order, each
- * little-endian -- is >= p8 (Philox4x64-10: Salmon et al., "Parallel random
- * numbers: as easy as 1, 2, 3", SC 2011).  The same call with the same key
- * drops the same weights.  LSE is that of the undropped softmax.  Other
- * arguments, errors and rules as attn_fwd (bf16 inputs).
+ * when byte (j mod 16) of Philox4x32-10(counter {j / 16, i, b*Hq + hq,
+ * offset}, key {seed mod 2^32, seed / 2^32}) -- the four 32-bit output words
+ * in order, each little-endian -- is >= p8 (Philox4x32-10: Salmon et al.,
+ * "Parallel random numbers: as easy as 1, 2, 3", SC 2011).  The same call
+ * with the same seed and offset drops the same weights.  LSE is that of the
+ * undropped softmax.  Other arguments, errors and rules as attn_fwd (bf16
+ * inputs).
  */
 int attn_fwd_dropout(const void *q, const void *k, const void *v, void *out, float *lse, int B,
                      int Hq, int Hkv, int S, int D, float scale, int causal, float dropout_p,

@@ -77,7 +77,7 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     f.restype = ci
     f.argtypes = [vp, vp, vp, ci, ci, ci, ci, ci, cf, ci, ci, ctypes.c_uint64, ctypes.c_uint64, vp,
                   ctypes.c_int64, vp, vp, ci]
-    f = lib.oracle_philox4x64
+    f = lib.oracle_philox4x32
     f.restype = None
     f.argtypes = [vp, vp, vp]
     f = lib.oracle_attn_bwd
@@ -409,8 +409,9 @@ def attention_dropout(q_bits, k_bits, v_bits, scale: float, p8: int, seed: int, 
                       causal: bool = True, rows=None, nthreads: int | None = None,
                       lib: ctypes.CDLL | None = None):
     """``attention`` with dropout of the weights: each dropped with probability
-    p8/256 by Philox4x64-10 (key {seed, offset}), kept ones scaled by 256/(256-p8).
-    The LSE is that of the undropped softmax."""
+    p8/256 by Philox4x32-10 (key from the 64-bit seed, the 32-bit offset in the
+    counter), kept ones scaled by 256/(256-p8).  The LSE is that of the
+    undropped softmax."""
     lib = lib or load()
     q, k, v = (_as_bits(x, n) for x, n in ((q_bits, "q"), (k_bits, "k"), (v_bits, "v")))
     B, Hq, Hkv, S, D = _shapes(q, k, v)
@@ -425,13 +426,13 @@ def attention_dropout(q_bits, k_bits, v_bits, scale: float, p8: int, seed: int, 
     return out, lse
 
 
-def philox4x64(ctr, key, lib: ctypes.CDLL | None = None) -> np.ndarray:
-    """The oracle's Philox4x64-10 block for one counter (4 x uint64) and key (2 x uint64)."""
+def philox4x32(ctr, key, lib: ctypes.CDLL | None = None) -> np.ndarray:
+    """The oracle's Philox4x32-10 block for one counter (4 x uint32) and key (2 x uint32)."""
     lib = lib or load()
-    c = np.ascontiguousarray(ctr, dtype=np.uint64)
-    k = np.ascontiguousarray(key, dtype=np.uint64)
-    out = np.empty(4, dtype=np.uint64)
-    lib.oracle_philox4x64(c.ctypes.data, k.ctypes.data, out.ctypes.data)
+    c = np.ascontiguousarray(ctr, dtype=np.uint32)
+    k = np.ascontiguousarray(key, dtype=np.uint32)
+    out = np.empty(4, dtype=np.uint32)
+    lib.oracle_philox4x32(c.ctypes.data, k.ctypes.data, out.ctypes.data)
     return out
 
 

@@ -94,7 +94,8 @@ typedef struct {
     const uint8_t *keep_bits;  /* NULL, or [keep_heads][S][16 * nt] bytes, bit j % 8 of byte j / 8 keeps key j */
     int keep_heads;            /* 1 (shared by all heads) or Hq */
     int dropout_p8;            /* 0: no dropout; else weights dropped with probability p8 / 256 */
-    uint64_t dropout_key[2];   /* Philox key: {seed, offset} */
+    uint64_t dropout_seed;     /* Philox key (two 32-bit words) */
+    uint64_t dropout_offset;   /* fourth Philox counter word, < 2^32 */
     const int64_t *rows; /* flat query-row ids, or NULL for all rows */
     int64_t nrows;
     double *out; /* [nrows, D] */
@@ -176,20 +177,21 @@ static void attn_weights(const oracle_job_t *J, int64_t r, double *s, double *ls
 }
 
 /*
- * Philox4x64-10 (Salmon, Moraes, Dror and Shaw, "Parallel random numbers: as
- * easy as 1, 2, 3", SC 2011): ten rounds of
+ * Philox4x32-10 (Salmon, Moraes, Dror and Shaw, "Parallel random numbers: as
+ * easy as 1, 2, 3", SC 2011), the 32-bit-word variant: ten rounds of
  *   (x0, x1, x2, x3) <- (hi(M1 x2) ^ x1 ^ k0, lo(M1 x2), hi(M0 x0) ^ x3 ^ k1, lo(M0 x0))
- * with the key bumped by the Weyl constants after every round.
+ * with 32 x 32 -> 64-bit products split into high and low words, and the key
+ * bumped by the Weyl constants (golden ratio, sqrt(3) - 1) after every round.
  */
-static void philox4x64_10(const uint64_t ctr[4], const uint64_t key[2], uint64_t out[4]) {
-    const uint64_t M0 = 0xD2E7470EE14C6C93ull, M1 = 0xCA5A826395121157ull;
-    const uint64_t W0 = 0x9E3779B97F4A7C15ull, W1 = 0xBB67AE8584CAA73Bull;
-    uint64_t x0 = ctr[0], x1 = ctr[1], x2 = ctr[2], x3 = ctr[3], k0 = key[0], k1 = key[1];
+static void philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]) {
+    const uint64_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u;
+    const uint32_t W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
+    uint32_t x0 = ctr[0], x1 = ctr[1], x2 = ctr[2], x3 = ctr[3], k0 = key[0], k1 = key[1];
     for (int r = 0; r < 10; ++r) {
-        const unsigned __int128 p0 = (unsigned __int128)M0 * x0;
-        const unsigned __int128 p1 = (unsigned __int128)M1 * x2;
-        const uint64_t hi0 = (uint64_t)(p0 >> 64), lo0 = (uint64_t)p0;
-        const uint64_t hi1 = (uint64_t)(p1 >> 64), lo1 = (uint64_t)p1;
+        const uint64_t p0 = M0 * (uint64_t)x0;
+        const uint64_t p1 = M1 * (uint64_t)x2;
+        const uint32_t hi0 = (uint32_t)(p0 >> 32), lo0 = (uint32_t)p0;
+        const uint32_t hi1 = (uint32_t)(p1 >> 32), lo1 = (uint32_t)p1;
         x0 = hi1 ^ x1 ^ k0;
         x1 = lo1;
         x2 = hi0 ^ x3 ^ k1;
@@ -204,17 +206,18 @@ static void philox4x64_10(const uint64_t ctr[4], const uint64_t key[2], uint64_t
  * Dropout of the attention weights (the fused dropout the ai-manual.ru
  * article names in section 6, "Dropout"; the weights are dropped after the
  * softmax and the kept ones scaled by 1 / (1 - p), as in
- * scaled_dot_product_attention).  The random draw is Philox4x64-10 with
- * counter {j / 32, i, b*Hq + hq, 0} and key {seed, offset}: its 32 output
- * bytes (word 0 first, each word little-endian) give keys j = 32*(j/32) + 0..31
- * of query row i.  Key j is kept when its byte is >= p8 (probability
- * 1 - p8/256) and then scaled by 256 / (256 - p8).
+ * scaled_dot_product_attention).  The random draw is Philox4x32-10 with
+ * counter {j / 16, i, b*Hq + hq, offset} and key {seed mod 2^32, seed / 2^32}:
+ * its 16 output bytes (word 0 first, each word little-endian) give keys
+ * j = 16*(j/16) + 0..15 of query row i.  Key j is kept when its byte is
+ * >= p8 (probability 1 - p8/256) and then scaled by 256 / (256 - p8).
  */
 static int dropout_keeps(const oracle_job_t *J, int64_t bh, int64_t i, int64_t j) {
-    const uint64_t ctr[4] = {(uint64_t)(j / 32), (uint64_t)i, (uint64_t)bh, 0};
-    uint64_t out[4];
-    philox4x64_10(ctr, J->dropout_key, out);
-    const int byte = (int)((out[(j % 32) / 8] >> (8 * (j % 8))) & 0xFF);
+    const uint32_t ctr[4] = {(uint32_t)(j / 16), (uint32_t)i, (uint32_t)bh, (uint32_t)J->dropout_offset};
+    const uint32_t key[2] = {(uint32_t)(J->dropout_seed & 0xFFFFFFFFu), (uint32_t)(J->dropout_seed >> 32)};
+    uint32_t out[4];
+    philox4x32_10(ctr, key, out);
+    const int byte = (int)((out[(j % 16) / 4] >> (8 * (j % 4))) & 0xFF);
     return byte >= J->dropout_p8;
 }
 
@@ -298,7 +301,7 @@ static int run_rows_dropout(const void *q, const void *k, const void *v, int for
         J->block_mask = block_mask; J->mask_heads = mask_heads;
         J->keep_bits = keep_bits; J->keep_heads = keep_heads;
         J->dropout_p8 = dropout_p8;
-        J->dropout_key[0] = seed; J->dropout_key[1] = offset;
+        J->dropout_seed = seed; J->dropout_offset = offset;
         J->rows = rows; J->nrows = nrows;
         J->out = out; J->lse = lse;
         J->begin = nrows * t / nthreads;
@@ -605,9 +608,10 @@ static int bwd_run(const void *q, const void *k, const void *v, const void *dout
     J.keep_bits = keep_bits;
     J.keep_heads = keep_bits ? keep_heads : 1;
     if (dropout_p8 < 0 || dropout_p8 > 255) return 1;
+    if (dropout_p8 > 0 && offset > 0xFFFFFFFFull) return 1;  /* a 32-bit counter word */
     J.dropout_p8 = dropout_p8;
-    J.dropout_key[0] = seed;
-    J.dropout_key[1] = offset;
+    J.dropout_seed = seed;
+    J.dropout_offset = offset;
     const int64_t G = Hq / Hkv;
     double *P = (double *)malloc(sizeof(double) * (size_t)(G * S) * (size_t)S);
     double *dS = (double *)malloc(sizeof(double) * (size_t)(G * S) * (size_t)S);
@@ -641,8 +645,9 @@ static int bwd_run(const void *q, const void *k, const void *v, const void *dout
 
 /*
  * oracle_attn_rows_dropout -- oracle_attn_rows with dropout of the attention
- * weights: drop probability p8 / 256 (0 <= p8 < 256), Philox key {seed,
- * offset}; see dropout_keeps for which weights are dropped.
+ * weights: drop probability p8 / 256 (0 <= p8 < 256), Philox4x32-10 key
+ * seed and counter word offset (< 2^32); see dropout_keeps for which weights
+ * are dropped.
  */
 int oracle_attn_rows_dropout(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int Hq,
                              int Hkv, int S, int D, float scale, int causal, int p8, uint64_t seed,
@@ -650,13 +655,14 @@ int oracle_attn_rows_dropout(const uint16_t *q, const uint16_t *k, const uint16_
                              double *lse, int nthreads) {
     const double one[3] = {1.0, 1.0, 1.0};
     if (p8 < 0 || p8 > 255) return 1;
+    if (p8 > 0 && offset > 0xFFFFFFFFull) return 1;  /* a 32-bit counter word */
     return run_rows_dropout(q, k, v, FMT_BF16, one, B, Hq, Hkv, S, D, scale, causal, NULL, 1, NULL,
                             1, p8, seed, offset, rows, nrows, out, lse, nthreads);
 }
 
-/* Philox4x64-10 of one counter block (exposed so the generator can be pinned). */
-void oracle_philox4x64(const uint64_t *ctr, const uint64_t *key, uint64_t *out) {
-    philox4x64_10(ctr, key, out);
+/* Philox4x32-10 of one counter block (exposed so the generator can be pinned). */
+void oracle_philox4x32(const uint32_t *ctr, const uint32_t *key, uint32_t *out) {
+    philox4x32_10(ctr, key, out);
 }
 
 int oracle_attn_bwd(const void *q, const void *k, const void *v, const void *dout, int f64_inputs,
@@ -720,7 +726,7 @@ int oracle_attn_bwd_dropout(const void *q, const void *k, const void *v, const v
  * oracle_attn_rows_ex -- every forward variant at once: inputs as bf16 bit
  * patterns (format 0) or E4M3 codes with per-tensor descales (format 1); an
  * optional block mask and optional keep bits (NULL for none; the masks
- * combine); dropout of the weights with p8 > 0 (key {seed, offset}).
+ * combine); dropout of the weights with p8 > 0 (seed, offset as in dropout_keeps).
  */
 int oracle_attn_rows_ex(const void *q, const void *k, const void *v, int format, float q_descale,
                         float k_descale, float v_descale, int B, int Hq, int Hkv, int S, int D,
@@ -732,6 +738,7 @@ int oracle_attn_rows_ex(const void *q, const void *k, const void *v, int format,
     const double one[3] = {1.0, 1.0, 1.0};
     if (format != FMT_BF16 && format != FMT_E4M3) return 1;
     if (p8 < 0 || p8 > 255) return 1;
+    if (p8 > 0 && offset > 0xFFFFFFFFull) return 1;  /* a 32-bit counter word */
     return run_rows_dropout(q, k, v, format, format == FMT_E4M3 ? ds : one, B, Hq, Hkv, S, D, scale,
                             causal, block_mask, block_mask ? mask_heads : 1, keep_bits,
                             keep_bits ? keep_heads : 1, p8, seed, offset, rows, nrows, out, lse,

@@ -509,53 +509,137 @@ BWD_PINS = [pin_bwd_torch_autograd, pin_bwd_closed_forms, pin_bwd_invariants]
 # ---------------------------------------------------------------- dropout
 # ``attnd(q, k, v, scale, p8, seed, offset, causal, rows=None)`` -> (O, LSE).
 
-def numpy_philox_block(ctr, key):
-    """Philox4x64-10 of counter ``ctr`` (four 64-bit words, word 0 least
-    significant) from numpy's own implementation (a library routine).  numpy
-    advances its 256-bit counter before the first block, so it starts one below."""
-    value = sum(int(c) << (64 * w) for w, c in enumerate(ctr))
-    bg = np.random.Philox(counter=(value - 1) % (1 << 256), key=sum(int(x) << (64 * w) for w, x in enumerate(key)))
-    return bg.random_raw(4).astype(np.uint64)
+# The Random123 known-answer list (Salmon et al.'s distribution of the
+# generator), philox4x32 with 10 rounds: counter words 0..3, key words 0..1 ->
+# output words 0..3.
+PHILOX4X32_10_KNOWN_ANSWERS = [
+    ((0x00000000, 0x00000000, 0x00000000, 0x00000000), (0x00000000, 0x00000000),
+     (0x6627e8d5, 0xe169c58d, 0xbc57ac4c, 0x9b00dbd8)),
+    ((0xffffffff, 0xffffffff, 0xffffffff, 0xffffffff), (0xffffffff, 0xffffffff),
+     (0x408f276d, 0x41c83b0e, 0xa20bc7c6, 0x6d5451fd)),
+    ((0x243f6a88, 0x85a308d3, 0x13198a2e, 0x03707344), (0xa4093822, 0x299f31d0),
+     (0xd16cfe09, 0x94fdcceb, 0x5001e420, 0x24126ea1)),
+]
+
+
+def numpy_philox4x32(ctr, key):
+    """Philox4x32-10 of counters ``ctr`` ([n, 4] uint32 words) under ``key``
+    ([2] or [n, 2]), vectorised in numpy's uint64 arithmetic: a test-side
+    generator, itself checked against the published known answers
+    (pin_test_generator_known_answers) and Triton's implementation."""
+    x = np.array(ctr, dtype=np.uint64).reshape(-1, 4)
+    k = np.broadcast_to(np.array(key, dtype=np.uint64).reshape(-1, 2), (x.shape[0], 2)).copy()
+    lo = np.uint64(0xFFFFFFFF)
+    for _ in range(10):
+        p0 = np.uint64(0xD2511F53) * x[:, 0]  # both factors < 2^32: exact in uint64
+        p1 = np.uint64(0xCD9E8D57) * x[:, 2]
+        x = np.stack([(p1 >> np.uint64(32)) ^ x[:, 1] ^ k[:, 0], p1 & lo,
+                      (p0 >> np.uint64(32)) ^ x[:, 3] ^ k[:, 1], p0 & lo], axis=1)
+        k = (k + np.array([0x9E3779B9, 0xBB67AE85], dtype=np.uint64)) & lo
+    return x.astype(np.uint32)
+
+
+def pin_test_generator_known_answers():
+    for ctr, key, want in PHILOX4X32_10_KNOWN_ANSWERS:
+        assert [int(x) for x in numpy_philox4x32([ctr], key)[0]] == list(want)
 
 
 def keep_table(bh, S, p8, seed, offset):
     """[S, S] booleans: is key j of query i kept?  The documented mapping --
-    byte (j mod 32) of Philox(counter {j/32, i, bh, 0}, key {seed, offset}),
-    little-endian words in order, kept when >= p8 -- written from the
-    definition with numpy's Philox."""
-    keep = np.zeros((S, S), dtype=bool)
-    for i in range(S):
-        for blk in range((S + 31) // 32):
-            by = numpy_philox_block([blk, i, bh, 0], [seed, offset]).view(np.uint8)
-            for t in range(32):
-                j = 32 * blk + t
-                if j < S:
-                    keep[i, j] = by[t] >= p8
-    return keep
+    byte (j mod 16) of Philox4x32-10(counter {j/16, i, bh, offset}, key
+    {seed mod 2^32, seed / 2^32}), little-endian words in order, kept when
+    >= p8 -- written from the definition with the test-side generator."""
+    nblk = (S + 15) // 16
+    i, blk = np.meshgrid(np.arange(S), np.arange(nblk), indexing="ij")
+    ctr = np.stack([blk.ravel(), i.ravel(), np.full(i.size, bh), np.full(i.size, offset)], axis=1)
+    by = numpy_philox4x32(ctr, [seed & 0xFFFFFFFF, seed >> 32]).view(np.uint8).reshape(S, nblk * 16)
+    return by[:, :S] >= p8
+
+
+TRITON_PHILOX = r"""
+import json, sys
+import torch, triton, triton.language as tl
+
+@triton.jit
+def blocks(out_ptr, c_ptr, seed, N: tl.constexpr):
+    i = tl.arange(0, N)
+    a, b, c, d = tl.philox(seed, tl.load(c_ptr + 4 * i), tl.load(c_ptr + 4 * i + 1),
+                           tl.load(c_ptr + 4 * i + 2), tl.load(c_ptr + 4 * i + 3))
+    tl.store(out_ptr + 4 * i, a)
+    tl.store(out_ptr + 4 * i + 1, b)
+    tl.store(out_ptr + 4 * i + 2, c)
+    tl.store(out_ptr + 4 * i + 3, d)
+
+res = []
+for seed, ctrs in json.loads(sys.stdin.read()):
+    c = torch.tensor(ctrs, dtype=torch.int64).to(torch.int32).reshape(-1)
+    out = torch.zeros(c.numel(), dtype=torch.int32)
+    blocks[(1,)](out, c, seed, N=len(ctrs))
+    res.append([x & 0xFFFFFFFF for x in out.tolist()])
+print(json.dumps(res))
+"""
+
+
+def triton_philox4x32(cases):
+    """Philox4x32-10 blocks from Triton's own tl.philox (a library routine, key
+    {seed mod 2^32, seed / 2^32}), run by its CPU interpreter in a subprocess;
+    ``cases`` = [(seed, [[c0, c1, c2, c3], ...]), ...] with a power-of-two
+    count of counters each.  None when Triton's interpreter is unavailable."""
+    import json
+    import os
+    import subprocess
+    import sys
+    try:
+        import triton  # noqa: F401
+    except ImportError:
+        return None
+    env = dict(os.environ, TRITON_INTERPRET="1")
+    res = subprocess.run([sys.executable, "-c", TRITON_PHILOX], input=json.dumps(cases), env=env,
+                         capture_output=True, text=True, timeout=300)
+    if res.returncode != 0:
+        return None
+    return [np.array(r, dtype=np.uint64).reshape(-1, 4) for r in json.loads(res.stdout)]
+
+
+def pin_philox_known_answers(philox):
+    """The oracle's Philox4x32-10 block gives the published known answers."""
+    for ctr, key, want in PHILOX4X32_10_KNOWN_ANSWERS:
+        assert [int(x) for x in philox(ctr, key)] == list(want)
 
 
 def pin_philox_library(philox):
-    """The oracle's Philox4x64-10 block equals numpy's Philox for assorted counters
-    and keys, and the zero counter and key give the published test vector
-    (Random123 known-answer list, first entry)."""
+    """The oracle's Philox4x32-10 block equals the test-side generator and
+    Triton's tl.philox (when its interpreter runs here) for assorted counters
+    and keys."""
     rng = np.random.default_rng(191)
-    for _ in range(20):
-        ctr = [int(x) for x in rng.integers(0, 2**63, 4, dtype=np.int64)]
-        key = [int(x) for x in rng.integers(0, 2**63, 2, dtype=np.int64)]
-        assert np.array_equal(philox(ctr, key), numpy_philox_block(ctr, key))
-    want = [0x16554d9eca36314c, 0xdb20fe9d672d0fdc, 0xd7e772cee186176b, 0x7e68b68aec7ba23b]
-    assert [int(x) for x in philox([0, 0, 0, 0], [0, 0])] == want
+    cases = []
+    for _ in range(8):
+        seed = int(rng.integers(0, 2**63)) * 2 + int(rng.integers(0, 2))
+        ctrs = [[int(x) for x in rng.integers(0, 2**32, 4, dtype=np.uint64)] for _ in range(4)]
+        cases.append((seed, ctrs))
+        key = [seed & 0xFFFFFFFF, seed >> 32]
+        for c in ctrs:
+            assert np.array_equal(philox(c, key).astype(np.uint64),
+                                  numpy_philox4x32([c], key)[0].astype(np.uint64))
+    lib = triton_philox4x32(cases)
+    if lib is not None:
+        for (seed, ctrs), blocks in zip(cases, lib):
+            key = [seed & 0xFFFFFFFF, seed >> 32]
+            for c, want in zip(ctrs, blocks):
+                assert np.array_equal(philox(c, key).astype(np.uint64), want)
 
 
 def pin_dropout_mask_closed_form(attnd, attn):
     """V = identity rows turns O rows into the weights: with dropout each must be
     the undropped weight times keep(i, j) * 256/(256-p8), keep from the
-    documented byte mapping over numpy's Philox (counter word 2 = b * H + h, so
-    two batches draw different decisions); the LSE is unchanged."""
+    documented byte mapping over the test-side Philox4x32-10 (counter word 2 =
+    b * H + h, so two batches draw different decisions; counter word 3 = the
+    offset; a seed above 2^32 puts both key words to use); the LSE is
+    unchanged."""
     B, H, S, D = 2, 2, 70, 128
     q, k = _rand((B, H, S, D), 201, 0), _rand((B, H, S, D), 201, 1)
     v = bits(np.broadcast_to(np.eye(S, D), (B, H, S, D)))
-    p8, seed, offset = 77, 0x1234abcd, 99
+    p8, seed, offset = 77, 0x5eed0001234abcd, 99
     for causal in (True, False):
         O, L = attnd(q, k, v, 0.2, p8, seed, offset, causal)
         P, L0 = attn(q, k, v, 0.2, causal)
@@ -797,7 +881,7 @@ BWD_KEEP_PINS = [pin_bwd_keep_library]
 def pin_bwd_dropout_autograd(bwdd):
     """Gradients with dropout against torch's float64 autograd of
     O = ((softmax of the masked scores) * Z * 256/(256-p8)) V, Z the keep table
-    written from the documented byte mapping over numpy's Philox; and p8 = 0
+    written from the documented byte mapping over the test-side Philox4x32-10; and p8 = 0
     gives the gradients without dropout bit for bit.  Two batches, so the keep
     table's counter carries the flat batch * head index."""
     B, Hq, Hkv, S, D = 2, 4, 2, 70, 8
@@ -860,7 +944,7 @@ def _combo_torch(qf, kf, vf, scale, causal, bm, keep, Z, s):
 def pin_combo_library(attnx):
     """Block mask, keep bits and dropout together against the float64 formula in
     torch (masked softmax, rows without keys 0, weights times Z * 256/(256-p8) with
-    Z from numpy's Philox)."""
+    Z from the test-side Philox4x32-10)."""
     q, k, v, bm, keep, bits = _combo_inputs(351)
     Hq, Hkv, S = 4, 2, 200
     p8, seed, offset = 60, 0xABC, 3

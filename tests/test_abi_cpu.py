@@ -369,6 +369,24 @@ def test_dropout_argument_errors_are_rejected_before_launch(kw, code):
     assert _call_dropout(**kw) == code
 
 
+def test_dropout_offsets_past_32_bits_are_rejected_before_launch():
+    """The offset is the fourth 32-bit counter word of the generator: 2^32 and
+    above are argument errors in every dropout entry point (with dropout on);
+    without dropout the offset is not used."""
+    lib = native.load()
+    q, k, v, out = 1 << 40, 2 << 40, 3 << 40, 4 << 40
+    f = ctypes.c_float(0.1)
+    big = 1 << 32
+    assert lib.attn_fwd_dropout(q, k, v, out, None, 1, 2, 2, 300, 128, f, 1, f, 1, big, None) == ATTN_ERR_INVALID_ARG
+    bargs = [q, k, v, out, 6 << 40, 5 << 40, 7 << 40, 8 << 40, 9 << 40, 10 << 40, 1, 2, 2, 300, 128, f, 1]
+    assert lib.attn_bwd_dropout(*bargs, f, 1, big, None) == ATTN_ERR_INVALID_ARG
+    drop = native.options(dropout_p=0.1, seed=1, offset=big)
+    assert lib.attn_fwd_ex(q, k, v, out, None, 1, 2, 2, 300, 128, f, 1, ctypes.byref(drop), None) == ATTN_ERR_INVALID_ARG
+    assert lib.attn_bwd_ex(*bargs, ctypes.byref(drop), None) == ATTN_ERR_INVALID_ARG
+    # the largest offset passes the argument checks (and then fails only for want of a device here)
+    assert lib.attn_fwd_dropout(q, k, v, out, None, 1, 2, 2, 300, 128, f, 1, f, 1, big - 1, None) != ATTN_ERR_INVALID_ARG
+
+
 def _call_proj(out=1 << 40, w=2 << 40, bias=None, y=3 << 40, B=1, H=4, S=300, D=128, E=512):
     lib = native.load()
     return lib.attn_out_proj(out, w, bias, y, B, H, S, D, E, None)

@@ -39,9 +39,12 @@ MUTANTS = {
     "block_mask_heads_ignored": ("(J->mask_heads == 1 ? 0 : hq)", "(0)"),
     "block_mask_ignored": ("if (J->block_mask) {", "if (0) {"),
     "dropout_keep_flipped": ("return byte >= J->dropout_p8;", "return byte < J->dropout_p8;"),
-    "dropout_byte_order": ("(out[(j % 32) / 8] >> (8 * (j % 8)))", "(out[(j % 32) % 4] >> (8 * ((j % 32) / 4)))"),
-    "dropout_counter_swapped": ("const uint64_t ctr[4] = {(uint64_t)(j / 32), (uint64_t)i, (uint64_t)bh, 0};",
-                                "const uint64_t ctr[4] = {(uint64_t)i, (uint64_t)(j / 32), (uint64_t)bh, 0};"),
+    "dropout_byte_order": ("(out[(j % 16) / 4] >> (8 * (j % 4)))", "(out[(j % 16) % 4] >> (8 * ((j % 16) / 4)))"),
+    "dropout_counter_swapped": ("{(uint32_t)(j / 16), (uint32_t)i, (uint32_t)bh,",
+                                "{(uint32_t)i, (uint32_t)(j / 16), (uint32_t)bh,"),
+    "dropout_offset_dropped": ("(uint32_t)bh, (uint32_t)J->dropout_offset};", "(uint32_t)bh, 0u};"),
+    "dropout_key_words_swapped": ("{(uint32_t)(J->dropout_seed & 0xFFFFFFFFu), (uint32_t)(J->dropout_seed >> 32)}",
+                                  "{(uint32_t)(J->dropout_seed >> 32), (uint32_t)(J->dropout_seed & 0xFFFFFFFFu)}"),
     "dropout_unscaled": ("s[j] = dropout_keeps(J, r / S, i, j) ? s[j] * keep_scale : 0.0;",
                          "s[j] = dropout_keeps(J, r / S, i, j) ? s[j] : 0.0;"),
     "philox_weyl_swapped": ("k0 += W0;\n        k1 += W1;", "k0 += W1;\n        k1 += W0;"),
@@ -137,8 +140,8 @@ def test_some_pin_catches_mutant(name, tmp_path):
         ("pin_block_mask_all_ones", lambda: oracle_pins.pin_block_mask_all_ones(attnm, attn)),
         ("pin_bwd_finite_differences", lambda: oracle_pins.pin_bwd_finite_differences(bwd, fwd64)),
     ] + [(p.__name__, lambda p=p: p(bwd)) for p in oracle_pins.BWD_PINS] + [
-        ("pin_philox_library", lambda: oracle_pins.pin_philox_library(
-            lambda c, k: oracle.philox4x64(c, k, lib=lib))),
+        ("pin_philox_known_answers", lambda: oracle_pins.pin_philox_known_answers(
+            lambda c, k: oracle.philox4x32(c, k, lib=lib))),
     ] + [(p.__name__, lambda p=p: p(attnd, attn)) for p in oracle_pins.DROPOUT_PINS] + [
         ("pin_bwd_masked_library", lambda: oracle_pins.pin_bwd_masked_library(
             lambda q, k, v, d, sc, c, m: oracle.attention_bwd(q, k, v, d, sc, c, block_mask=m, lib=lib))),

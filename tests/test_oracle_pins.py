@@ -61,8 +61,24 @@ def test_oracle_bwd_thread_count_does_not_change_bits():
     assert all(np.array_equal(x, y) for x, y in zip(a, b))
 
 
+def test_test_side_philox_gives_the_published_known_answers():
+    oracle_pins.pin_test_generator_known_answers()
+
+
+def test_oracle_philox_known_answers():
+    oracle_pins.pin_philox_known_answers(oracle.philox4x32)
+
+
 def test_oracle_philox_pin():
-    oracle_pins.pin_philox_library(oracle.philox4x64)
+    oracle_pins.pin_philox_library(oracle.philox4x32)
+
+
+def test_oracle_rejects_offsets_past_32_bits():
+    from causal_scaled_dot_gb300.inputs import qkv_bf16
+    q, k, v = qkv_bf16(1, 1, 1, 20, 8, seed=11)
+    oracle.attention_dropout(q, k, v, 0.3, 10, 1, 2**32 - 1, True)
+    with pytest.raises(ValueError):
+        oracle.attention_dropout(q, k, v, 0.3, 10, 1, 2**32, True)
 
 
 def _attnd(q, k, v, scale, p8, seed, offset, causal, rows=None):
