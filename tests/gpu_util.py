@@ -98,13 +98,58 @@ def fp8_tolerances(v_values, o_ref):
     return max_abs, 2.0 ** -4, TOL_LSE_MAX_ABS
 
 
-def compare_fp8(o_gpu, o_ref, l_gpu, l_ref, v_values, label=""):
+def fp8_rounding_model(q_codes, k_codes, v_codes, descales, scale, causal, rows=None):
+    """Relative L2 error of O that rounding the probabilities to E4M3 gives on
+    these inputs, in a model of the kernel: the exact scores t_ij (log2 units),
+    weights 2^(t_ij - M_i) with M_i the row maximum, each rounded to E4M3 with
+    round-to-nearest-even (torch's float8_e4m3fn conversion), and
+    O_i = sum_j round(w_ij) v_j / sum_j w_ij (the row sum stays unrounded, as in
+    the kernel) against the same sum with unrounded weights; over the given
+    flat rows (b*Hq + h)*S + i, or all rows.
+
+    The kernel's reference maximum lies 0 to 8 binades below M_i (it is the
+    first key tile's maximum unless a later tile exceeds it by more than 8), so
+    its probabilities are the model's times one factor per row: relative
+    rounding errors of normal E4M3 numbers have the same distribution, and
+    fewer probabilities fall below the normal range than in the model."""
+    import torch
+    import oracle
+    q = oracle.e4m3_decode(q_codes) * descales[0]
+    k = oracle.e4m3_decode(k_codes) * descales[1]
+    v = oracle.e4m3_decode(v_codes) * descales[2]
+    B, Hq, S, D = q.shape
+    G = Hq // k.shape[1]
+    rows = np.arange(B * Hq * S) if rows is None else np.asarray(rows)
+    num = den = 0.0
+    for bh in np.unique(rows // S):
+        b, h = divmod(int(bh), Hq)
+        ii = rows[rows // S == bh] % S
+        t = (q[b, h, ii] @ k[b, h // G].T) * (float(np.float32(scale)) / math.log(2.0))
+        if causal:
+            t = np.where(np.arange(S)[None, :] > ii[:, None], -np.inf, t)
+        w = np.exp2(t - t.max(axis=1, keepdims=True))
+        wq = torch.from_numpy(w).to(torch.float8_e4m3fn).double().numpy()
+        l = w.sum(axis=1, keepdims=True)
+        o = (w @ v[b, h // G]) / l
+        oq = (wq @ v[b, h // G]) / l
+        num += float(((oq - o) ** 2).sum())
+        den += float((o ** 2).sum())
+    return math.sqrt(num / den) if den > 0 else 0.0
+
+
+def compare_fp8(o_gpu, o_ref, l_gpu, l_ref, v_values, label="", model_rel=None):
+    """As ``fp8_tolerances``; with ``model_rel`` (``fp8_rounding_model`` on the
+    same inputs and rows) the relative L2 bound tightens to twice the model's
+    error plus 2^-8 (the bf16 output rounding, 2^-9, taken twice), never above
+    the worst-case 2^-4."""
     tol_abs, tol_rel, tol_lse = fp8_tolerances(v_values, o_ref)
+    if model_rel is not None:
+        tol_rel = min(tol_rel, 2.0 * model_rel + 2.0 ** -8)
     assert np.all(np.isfinite(o_gpu)), f"{label}: non-finite output (unwritten rows?)"
     diff = o_gpu - o_ref
     max_abs = float(np.max(np.abs(diff)))
     rel_l2 = float(np.linalg.norm(diff) / np.linalg.norm(o_ref))
-    stats = {"max_abs": max_abs, "rel_l2": rel_l2, "tol_abs": tol_abs}
+    stats = {"max_abs": max_abs, "rel_l2": rel_l2, "tol_abs": tol_abs, "tol_rel": tol_rel}
     assert max_abs <= tol_abs, f"{label}: O max abs error {max_abs:.3e} > {tol_abs:.3e}"
     assert rel_l2 <= tol_rel, f"{label}: O rel L2 error {rel_l2:.3e} > {tol_rel:.3e}"
     if l_gpu is not None:
