@@ -383,6 +383,7 @@ int fwd_bf16(const void* q, const void* k, const void* v, void* out, float* lse,
         p.dropout_p8 = dropout_p8;
         p.dropout_seed = seed;
         p.dropout_offset = offset;
+        philox_round_keys(seed, p.philox_round_keys);
         p.o_scale = 256.f / (float)(256 - dropout_p8);
     }
     cudaStream_t st = static_cast<cudaStream_t>(stream);

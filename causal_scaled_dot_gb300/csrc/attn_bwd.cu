@@ -264,6 +264,7 @@ int bwd(const void* q, const void* k, const void* v, const void* out, const void
     p.dropout_p8 = dropout_p8;
     p.dropout_seed = seed;
     p.dropout_offset = offset;
+    philox_round_keys(seed, p.philox_round_keys);
     p.keep_scale = dropout_p8 > 0 ? 256.f / (float)(256 - dropout_p8) : 1.f;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const bool m = block_mask != nullptr, e = keep_bits != nullptr, dr = dropout_p8 > 0;

@@ -1,5 +1,6 @@
 // common.cuh -- constants and the kernel parameter block shared by the
-// attention kernels and their host launcher.
+// attention kernels and their host launcher, and the Philox key schedule
+// that the host precomputes for them.
 #pragma once
 
 #include <cstdint>
@@ -27,10 +28,25 @@ struct FwdParams {
     const uint8_t* block_mask;      // null, or [mask_heads][nt][nt], nt = num_q_tiles
     int mask_heads;                 // 1 (one mask for all heads) or Hq
     int dropout_p8;                 // dropout kernels: weights dropped with probability p8 / 256
-    unsigned long long dropout_seed, dropout_offset;  // Philox key
+    unsigned long long dropout_seed, dropout_offset;  // Philox key (seed) and counter word (offset)
+    unsigned int philox_round_keys[20];  // dropout kernels: round r's key words at [2r], [2r + 1]
     const uint8_t* keep_bits;       // element-masked kernels: [keep_heads][S][keep_row_bytes]
     int keep_heads;                 // 1 (one mask for all heads) or Hq
     int keep_row_bytes;             // 16 per 128 keys
 };
+
+// The Philox4x32-10 key schedule of `seed`: round r uses key words
+// (lo32(seed) + r * 0x9E3779B9, hi32(seed) + r * 0xBB67AE85) mod 2^32.  The
+// same for every thread of a launch, so the host computes it once and the
+// kernels read each round's words from the parameter block.
+inline void philox_round_keys(unsigned long long seed, unsigned int keys[20]) {
+    unsigned int k0 = (unsigned int)seed, k1 = (unsigned int)(seed >> 32);
+    for (int r = 0; r < 10; ++r) {
+        keys[2 * r] = k0;
+        keys[2 * r + 1] = k1;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+}
 
 }  // namespace attn

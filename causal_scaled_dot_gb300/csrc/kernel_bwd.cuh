@@ -89,6 +89,7 @@ struct BwdParams {
     // 256 / (256 - p8) (as in the forward).
     int dropout_p8;
     unsigned long long dropout_seed, dropout_offset;
+    unsigned int philox_round_keys[20];  // the key schedule of dropout_seed (philox_round_keys)
     float keep_scale;
 };
 
@@ -538,8 +539,8 @@ __device__ void dq_work_role(const BwdParams& p, uint32_t base, const uint8_t* s
 #pragma unroll
                 for (int b = 0; b < 4; ++b)
                     zb |= (uint64_t)dropout_keep16((uint32_t)((key0 >> 4) + b), (uint32_t)row, (uint32_t)w.bh,
-                                                   (uint32_t)p.dropout_offset, (uint32_t)p.dropout_seed,
-                                                   (uint32_t)(p.dropout_seed >> 32), (256u - (uint32_t)p.dropout_p8) * 0x01010101u)
+                                                   (uint32_t)p.dropout_offset, p.philox_round_keys,
+                                                   (256u - (uint32_t)p.dropout_p8) * 0x01010101u)
                           << (16 * b);
             }
             const float ks = DR ? p.keep_scale : 1.f;
@@ -1012,8 +1013,8 @@ __device__ void dkv_work_role(const BwdParams& p, uint32_t base, const uint8_t* 
 #pragma unroll
                     for (int h = 0; h < 2; ++h)
                         bits |= dropout_keep16((uint32_t)(w.kt * 8 + 2 * b + h), (uint32_t)(qt * kTile + qq),
-                                               (uint32_t)bh, (uint32_t)p.dropout_offset, (uint32_t)p.dropout_seed,
-                                               (uint32_t)(p.dropout_seed >> 32), (256u - (uint32_t)p.dropout_p8) * 0x01010101u)
+                                               (uint32_t)bh, (uint32_t)p.dropout_offset, p.philox_round_keys,
+                                               (256u - (uint32_t)p.dropout_p8) * 0x01010101u)
                                 << (16 * h);
                     keepw[4 * qq + b] = bits;
                 }

@@ -675,12 +675,11 @@ __device__ void ws_softmax_role(const CUtensorMap* tm_o, const FwdParams& p, uin
             } else if constexpr (DR) {
                 // Dropout: key kv0 + e is kept when byte e mod 16 of the Philox
                 // block {(kv0 + e) / 16, query row, b*Hq + hq, offset} under key
-                // {seed_lo, seed_hi} is >= p8.  The row sum takes every
+                // {seed mod 2^32, seed / 2^32} is >= p8.  The row sum takes every
                 // probability; the tensor core gets the kept ones (the
                 // 256 / (256 - p8) factor is in o_scale).
                 const uint32_t qrow = (uint32_t)(qt * kTile + r);
                 const uint32_t p8 = (uint32_t)p.dropout_p8;
-                const uint32_t seed_lo = (uint32_t)p.dropout_seed, seed_hi = (uint32_t)(p.dropout_seed >> 32);
                 // One block per 16 keys, interleaved with their exponentials so
                 // that the generator's integer work and the exp2 unit overlap
                 // (generating a half tile's bits first measured 16 % slower).
@@ -692,7 +691,7 @@ __device__ void ws_softmax_role(const CUtensorMap* tm_o, const FwdParams& p, uin
                     for (int b = 0; b < 4; ++b) {
                         uint32_t rnd[4];
                         philox4x32_10((uint32_t)((kv0 + 64 * h + 16 * b) >> 4), qrow, (uint32_t)w.bh,
-                                      (uint32_t)p.dropout_offset, seed_lo, seed_hi, rnd);
+                                      (uint32_t)p.dropout_offset, p.philox_round_keys, rnd);
 #pragma unroll
                         for (int c = 0; c < 8; ++c) {
                             const int e = 64 * h + 16 * b + 2 * c;
