@@ -295,6 +295,11 @@ drain:
 }
 
 // ---------------------------------------------------------------- MMA issuer
+// The issuing thread spins on its barriers (mbar_wait_spin): it alone feeds
+// the tensor core, which idles while it waits, so it should see a completed
+// phase at once (+0.8 % at B4 H16 S4096 D128 against suspend-hinted waits);
+// the other roles keep the suspend hint, so that their waiting warps leave
+// issue slots to the softmax warps on their schedulers.
 template <int D, bool F, bool M, bool DR, bool E>
 __device__ void ws_mma_role(const FwdParams& p, uint32_t base, uint32_t tmem,
                             volatile int* abort_flag) {
@@ -337,7 +342,7 @@ __device__ void ws_mma_role(const FwdParams& p, uint32_t base, uint32_t tmem,
         }
     };
     auto wait_ring = [&](int& got) -> bool {
-        if (!ptx::mbar_wait(ws_bar<D, F>(base, L::kKVFull + slot), ring_phase, abort_flag, p.status, lim))
+        if (!ptx::mbar_wait_spin(ws_bar<D, F>(base, L::kKVFull + slot), ring_phase, abort_flag, p.status, lim))
             return false;
         got = slot;
         if (++slot == L::kStages) {
@@ -348,7 +353,7 @@ __device__ void ws_mma_role(const FwdParams& p, uint32_t base, uint32_t tmem,
         return true;
     };
     auto wait_p = [&](int i) -> bool {
-        if (!ptx::mbar_wait(ws_bar<D, F>(base, L::kPFull + i), pf_phase[i], abort_flag, p.status, lim))
+        if (!ptx::mbar_wait_spin(ws_bar<D, F>(base, L::kPFull + i), pf_phase[i], abort_flag, p.status, lim))
             return false;
         pf_phase[i] ^= 1u;
         ptx::tc_fence_after();
@@ -360,7 +365,7 @@ __device__ void ws_mma_role(const FwdParams& p, uint32_t base, uint32_t tmem,
     // phases ahead of the softmax warps waiting on it.  Once per tile per unit.
     uint32_t oe_phase[2] = {1u, 1u};
     auto wait_o_empty = [&](int i) -> bool {
-        if (!ptx::mbar_wait(ws_bar<D, F>(base, L::kOEmpty + i), oe_phase[i], abort_flag, p.status, lim))
+        if (!ptx::mbar_wait_spin(ws_bar<D, F>(base, L::kOEmpty + i), oe_phase[i], abort_flag, p.status, lim))
             return false;
         oe_phase[i] ^= 1u;
         ptx::tc_fence_after();
@@ -380,8 +385,8 @@ __device__ void ws_mma_role(const FwdParams& p, uint32_t base, uint32_t tmem,
         int pre_kslot = 0;
         for (int rnd = 0, u = unit_of_round(0); u < p.num_units; u = unit_of_round(++rnd)) {
             const Unit w = decode_unit(u, p, round_desc(rnd));
-            if ((!pre && !ptx::mbar_wait(ws_bar<D, F>(base, L::kQFull + 0), qf_phase, abort_flag, p.status, lim)) ||
-                !ptx::mbar_wait(ws_bar<D, F>(base, L::kQFull + 1), qf_phase, abort_flag, p.status, lim))
+            if ((!pre && !ptx::mbar_wait_spin(ws_bar<D, F>(base, L::kQFull + 0), qf_phase, abort_flag, p.status, lim)) ||
+                !ptx::mbar_wait_spin(ws_bar<D, F>(base, L::kQFull + 1), qf_phase, abort_flag, p.status, lim))
                 break;
             qf_phase ^= 1u;
             ptx::tc_fence_after();
@@ -428,7 +433,7 @@ __device__ void ws_mma_role(const FwdParams& p, uint32_t base, uint32_t tmem,
                     const int u2 = unit_of_round(rnd + 1);
                     if (u2 < p.num_units) {  // the next unit's first S_0
                         const Unit w2 = decode_unit(u2, p, round_desc(rnd + 1));
-                        if (!(ok = ptx::mbar_wait(ws_bar<D, F>(base, L::kQFull + 0), qf_phase, abort_flag,
+                        if (!(ok = ptx::mbar_wait_spin(ws_bar<D, F>(base, L::kQFull + 0), qf_phase, abort_flag,
                                                   p.status, lim)))
                             break;
                         ptx::tc_fence_after();
@@ -457,8 +462,8 @@ __device__ void ws_mma_role(const FwdParams& p, uint32_t base, uint32_t tmem,
     } else {
         for (int rnd = 0, u = unit_of_round(0); u < p.num_units; u = unit_of_round(++rnd)) {
             const Unit w = decode_unit(u, p, round_desc(rnd));
-            if (!ptx::mbar_wait(ws_bar<D, F>(base, L::kQFull + 0), qf_phase, abort_flag, p.status, lim) ||
-                !ptx::mbar_wait(ws_bar<D, F>(base, L::kQFull + 1), qf_phase, abort_flag, p.status, lim))
+            if (!ptx::mbar_wait_spin(ws_bar<D, F>(base, L::kQFull + 0), qf_phase, abort_flag, p.status, lim) ||
+                !ptx::mbar_wait_spin(ws_bar<D, F>(base, L::kQFull + 1), qf_phase, abort_flag, p.status, lim))
                 break;
             qf_phase ^= 1u;
             // Key tiles run over the union of both query tiles' active tiles; each
