@@ -29,7 +29,7 @@ cudaError_t allow_smem(K kernel, uint32_t bytes) {
 template <int D, bool M, bool E, bool DR>
 bool allow_all() {
     return allow_smem(attn_bwd_dq_kernel<D, M, E, DR>, DqLayout<D>::kDynamicSmem) == cudaSuccess &&
-           allow_smem(attn_bwd_dkdv_kernel<D, M, E, DR>, DkvLayout<D, E && DR>::kDynamicSmem) == cudaSuccess;
+           allow_smem(attn_bwd_dkdv_kernel<D, M, E, DR>, DkvLayout<D>::kDynamicSmem) == cudaSuccess;
 }
 
 // Every combination of block mask (M), keep bits (E) and dropout (DR).
@@ -100,7 +100,7 @@ int launch_bwd(const CUtensorMap& tq, const CUtensorMap& tdo, const CUtensorMap&
     p.num_units = (int)dkv_units;
     grid = (int)(dkv_units < sm_count ? dkv_units : sm_count);
     p.head_block = std::min(p.B * p.Hkv, (8 * grid + p.num_tiles - 1) / p.num_tiles);
-    using KL = DkvLayout<D, E && DR>;
+    using KL = DkvLayout<D>;
     attn_bwd_dkdv_kernel<D, M, E, DR><<<grid, KL::kThreads, KL::kDynamicSmem, stream>>>(tq, tdo, tk, tv, p);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }

@@ -683,7 +683,7 @@ __global__ void __launch_bounds__(DqLayout<D>::kThreads, 1)
 // ====================================================================== dK, dV
 // ED: the kernel applies keep bits and dropout together, and each statistics
 // stage holds both bit sets.
-template <int D, bool ED = false>
+template <int D>
 struct DkvLayout {
     static constexpr int kThreads = 384;
     static constexpr int kRegsSmall = 56;
@@ -694,12 +694,9 @@ struct DkvLayout {
     static constexpr uint32_t kChunkBytes = kTile * 128;
     static constexpr int kStatStages = 4;  // per-query LSE / delta rows
     // Stage s: lse2[128], delta[128] (fp32), then (element-masked kernels) the
-    // 16 keep bytes of the unit's key tile for each of the 128 queries; the
-    // dropout bits of the tile take the same layout, at kStatDrop: in place of
-    // the keep bytes, or after them when the kernel applies both.
+    // 16 keep bytes of the unit's key tile for each of the 128 queries.
     static constexpr uint32_t kStatKeep = 2 * kTile * 4;
-    static constexpr uint32_t kStatDrop = kStatKeep + (ED ? kTile * 16 : 0);
-    static constexpr uint32_t kStatBytes = kStatDrop + kTile * 16;
+    static constexpr uint32_t kStatBytes = kStatKeep + kTile * 16;
     // Q_i, dO_i ring, one tile per slot: as many as fit (4 at D = 128, 10 or 11 at D = 64).
     static constexpr int kStages =
         (227 * 1024 - 2 * (int)kTileBytes - kStatStages * (int)kStatBytes - 2048) / (int)kTileBytes > 12
@@ -713,9 +710,8 @@ struct DkvLayout {
     static constexpr int kKVFull = 0, kKVEmpty = 1, kSFull = 2, kDPFull = 3, kPFull = 4, kDSFull = 5,
                          kAccFull = 6, kStFull = 7, kStEmpty = 7 + kStages, kStatFull = 7 + 2 * kStages,
                          kStatEmpty = 7 + 2 * kStages + kStatStages, kDrain = 7 + 2 * kStages + 2 * kStatStages,
-                         kAccEmpty = kDrain + 1,  // block-masked kernels: dK, dV read out
-                         kBitsReady = kDrain + 2;  // dropout kernels: a tile's keep bits written
-    static constexpr int kNumBars = kDrain + 3;
+                         kAccEmpty = kDrain + 1;  // block-masked kernels: dK, dV read out
+    static constexpr int kNumBars = kDrain + 2;
     static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8;
     static constexpr uint32_t kAbort = kTmemSlot + 4;
     static constexpr uint32_t kDynamicSmem = kAbort + 4 + 1024;
@@ -765,7 +761,7 @@ template <int D, bool M, bool E, bool DR>
 __device__ void dkv_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_do,
                               const CUtensorMap* tm_k, const CUtensorMap* tm_v, const BwdParams& p,
                               uint32_t base, volatile int* abort_flag) {
-    using L = DkvLayout<D, E && DR>;
+    using L = DkvLayout<D>;
     const uint64_t lim = p.wait_limit_ns;
     uint32_t kve_phase = 0, ring_phase = 0;
     int slot = 0;
@@ -824,7 +820,7 @@ drain:
 // their weights vanish.
 template <int D, bool M, bool E, bool DR>
 __device__ void dkv_stat_role(const BwdParams& p, uint32_t base, uint8_t* smem, volatile int* abort_flag) {
-    using L = DkvLayout<D, E && DR>;
+    using L = DkvLayout<D>;
     const int tid = threadIdx.x - 64;  // 0..63
     const uint64_t lim = p.wait_limit_ns;
     uint32_t ring_phase = 0;
@@ -878,7 +874,7 @@ __device__ void dkv_stat_role(const BwdParams& p, uint32_t base, uint8_t* smem, 
 
 template <int D, bool M, bool E, bool DR>
 __device__ void dkv_mma_role(const BwdParams& p, uint32_t base, uint32_t tmem, volatile int* abort_flag) {
-    using L = DkvLayout<D, E && DR>;
+    using L = DkvLayout<D>;
     constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(kTile, kTile, false);  // S^T, dP^T: N = 128 queries
     constexpr uint32_t kIdescA = ptx::idesc_bf16_f32(kTile, D, true);       // dV, dK: N = D, MN-major
     const uint64_t lim = p.wait_limit_ns;
@@ -978,7 +974,7 @@ __device__ void dkv_mma_role(const BwdParams& p, uint32_t base, uint32_t tmem, v
 template <int D, bool M, bool E, bool DR>
 __device__ void dkv_work_role(const BwdParams& p, uint32_t base, const uint8_t* smem, uint32_t tmem,
                               int wg, volatile int* abort_flag) {
-    using L = DkvLayout<D, E && DR>;
+    using L = DkvLayout<D>;
     const int warp = threadIdx.x >> 5;
     const int r = (warp & 3) * 32 + (threadIdx.x & 31);  // key row of the tile = TMEM lane
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
@@ -986,7 +982,7 @@ __device__ void dkv_work_role(const BwdParams& p, uint32_t base, const uint8_t* 
     const uint32_t tDP = tmem + lane_off + 128u + 64u * (uint32_t)wg;  // dS^T (bf16) written over it
     const float sl2 = p.scale_log2;
     const uint64_t lim = p.wait_limit_ns;
-    uint32_t s_phase = 0, dp_phase = 0, acc_phase = 0, ring_phase = 0, bits_phase = 0;
+    uint32_t s_phase = 0, dp_phase = 0, acc_phase = 0, ring_phase = 0;
     int st = 0;
 
     for (int rnd = 0, u = bwd_unit_of_round(0); u < p.num_units; u = bwd_unit_of_round(++rnd)) {
@@ -995,33 +991,30 @@ __device__ void dkv_work_role(const BwdParams& p, uint32_t base, const uint8_t* 
         for (int t = dkv_next<M>(p, w, -1); t < w.n; t = dkv_next<M>(p, w, t)) {
             int bh, qt;
             dkv_iter(w, p, t, bh, qt);
-            bool ok = ptx::mbar_wait(dkv_bar<L>(base, L::kStatFull + st), ring_phase, abort_flag, p.status, lim);
+            // Dropout: bit c of zb keeps (query 64 wg + c, this key).  The
+            // warp's 32 keys (32 (warp % 4) + k) need, for each of the
+            // warpgroup's 64 queries, two 16-key Philox blocks: lane l runs the
+            // four of queries 64 wg + l and 64 wg + 32 + l, as one 32-bit word
+            // per query (bit k: key 32 (warp % 4) + k), and two bit transposes
+            // across the warp hand every lane its own key's 64 decisions --
+            // while S^T is being computed, with no exchange between warps.
+            uint64_t zb = ~0ull;
             if constexpr (DR) {
-                // The tile's 128 x 128 keep decisions: 1024 Philox blocks (a query
-                // and 16 keys each), four per element-wise thread, written as bits
-                // into the stage in the element-mask layout (a 32-bit word per
-                // query and 32 keys) while S^T is being computed; every thread
-                // then waits for all 256 to have written.
-                if (!__all_sync(0xffffffffu, ok)) return;
-                uint32_t* keepw = reinterpret_cast<uint32_t*>(
-                    const_cast<uint8_t*>(smem) + L::kStat + (uint32_t)st * L::kStatBytes + L::kStatDrop);
-                const int et = threadIdx.x - 128;  // 0 .. 255
+                const uint32_t c4 = (256u - (uint32_t)p.dropout_p8) * 0x01010101u;
+                uint32_t word[2];
 #pragma unroll
                 for (int y = 0; y < 2; ++y) {
-                    const int x = 2 * et + y, qq = x >> 2, b = x & 3;  // query qq, keys 32b .. 32b+31
-                    uint32_t bits = 0u;
+                    const uint32_t query = (uint32_t)(qt * kTile + 64 * wg + 32 * y) + (threadIdx.x & 31u);
+                    word[y] = 0u;
 #pragma unroll
                     for (int h = 0; h < 2; ++h)
-                        bits |= dropout_keep16((uint32_t)(w.kt * 8 + 2 * b + h), (uint32_t)(qt * kTile + qq),
-                                               (uint32_t)bh, (uint32_t)p.dropout_offset, p.philox_round_keys,
-                                               (256u - (uint32_t)p.dropout_p8) * 0x01010101u)
-                                << (16 * h);
-                    keepw[4 * qq + b] = bits;
+                        word[y] |= dropout_keep16((uint32_t)(w.kt * 8 + 2 * (warp & 3) + h), query, (uint32_t)bh,
+                                                  (uint32_t)p.dropout_offset, p.philox_round_keys, c4)
+                                   << (16 * h);
                 }
-                ptx::mbar_arrive(dkv_bar<L>(base, L::kBitsReady));
-                ok = ptx::mbar_wait(dkv_bar<L>(base, L::kBitsReady), bits_phase, abort_flag, p.status, lim);
-                bits_phase ^= 1u;
+                zb = (uint64_t)warp_transpose_bits(word[0]) | ((uint64_t)warp_transpose_bits(word[1]) << 32);
             }
+            bool ok = ptx::mbar_wait(dkv_bar<L>(base, L::kStatFull + st), ring_phase, abort_flag, p.status, lim);
             ok = ok && ptx::mbar_wait(dkv_bar<L>(base, L::kSFull), s_phase, abort_flag, p.status, lim);
             if (!__all_sync(0xffffffffu, ok)) return;
             s_phase ^= 1u;
@@ -1059,18 +1052,9 @@ __device__ void dkv_work_role(const BwdParams& p, uint32_t base, const uint8_t* 
                 for (int c = 0; c < 64; ++c)
                     if (((kw[4 * (64 * wg + c)] >> (r & 31)) & 1u) == 0u) pr[c] = 0.f;
             }
-            // Dropout: bit c of zb keeps (query 64 wg + c, this key), read from
-            // the stage like an element mask.  dV takes the kept weights times
-            // keep_scale, and dP of a dropped weight is 0.
-            uint64_t zb = ~0ull;
+            // dV takes the kept weights times keep_scale, and dP of a dropped
+            // weight is 0.
             const float ks = DR ? p.keep_scale : 1.f;
-            if constexpr (DR) {
-                const uint32_t* kw = reinterpret_cast<const uint32_t*>(
-                    smem + L::kStat + (uint32_t)st * L::kStatBytes + L::kStatDrop) + (r >> 5);
-                zb = 0ull;
-#pragma unroll
-                for (int c = 0; c < 64; ++c) zb |= (uint64_t)((kw[4 * (64 * wg + c)] >> (r & 31)) & 1u) << c;
-            }
             auto kept = [&](int c) -> bool { return !DR || ((zb >> c) & 1ull) != 0ull; };
             uint32_t pk[32];
 #pragma unroll
@@ -1167,7 +1151,7 @@ __global__ void __launch_bounds__(DkvLayout<D>::kThreads, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                          const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                          const BwdParams p) {
-    using L = DkvLayout<D, E && DR>;
+    using L = DkvLayout<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -1194,7 +1178,6 @@ __global__ void __launch_bounds__(DkvLayout<D>::kThreads, 1)
         }
         ptx::mbar_init(dkv_bar<L>(base, L::kDrain), 1);
         ptx::mbar_init(dkv_bar<L>(base, L::kAccEmpty), 8);  // one per element-wise warp
-        ptx::mbar_init(dkv_bar<L>(base, L::kBitsReady), 256);  // one per element-wise thread
         *abort_flag = 0;
         ptx::fence_barrier_init();
         ptx::prefetch_tensormap(&tm_q);

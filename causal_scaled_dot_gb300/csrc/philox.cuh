@@ -72,4 +72,22 @@ __device__ __forceinline__ uint32_t dropout_keep16(uint32_t key_block, uint32_t 
     return bits;
 }
 
+// 32 x 32 bit-matrix transpose across a warp: lane l holds row l (bit b =
+// element (l, b)) and gets back column l (bit b = element (b, l)).  Stage j =
+// 16, 8, 4, 2, 1 swaps the off-diagonal j x j blocks of every 2j x 2j block
+// between lanes l and l ^ j: the lane with bit j clear keeps the columns with
+// bit j clear and takes its partner's, shifted up by j; its partner keeps the
+// other columns and takes the rest, shifted down.
+__device__ __forceinline__ uint32_t warp_transpose_bits(uint32_t x) {
+    const uint32_t lane = threadIdx.x & 31u;
+    uint32_t low = 0x0000FFFFu;  // columns with bit j clear
+#pragma unroll
+    for (uint32_t j = 16; j > 0; j >>= 1) {
+        const uint32_t y = __shfl_xor_sync(0xffffffffu, x, (int)j);
+        x = (lane & j) ? (x & ~low) | ((y & ~low) >> j) : (x & low) | ((y & low) << j);
+        low ^= low << (j >> 1);
+    }
+    return x;
+}
+
 }  // namespace attn
