@@ -265,7 +265,8 @@ int bwd(const void* q, const void* k, const void* v, const void* out, const void
     p.dropout_seed = seed;
     p.dropout_offset = offset;
     philox_round_keys(seed, p.philox_round_keys);
-    p.keep_scale = dropout_p8 > 0 ? 256.f / (float)(256 - dropout_p8) : 1.f;
+    p.log2_keep_scale = dropout_p8 > 0 ? (float)(8.0 - std::log2((double)(256 - dropout_p8))) : 0.f;
+    p.inv_keep_scale = (float)(256 - dropout_p8) / 256.f;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const bool m = block_mask != nullptr, e = keep_bits != nullptr, dr = dropout_p8 > 0;
     return D == 64 ? launch_variant<64>(m, e, dr, tq, tdo, tk, tv, p, sm_count, st)

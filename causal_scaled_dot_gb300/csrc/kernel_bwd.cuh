@@ -85,12 +85,15 @@ struct BwdParams {
     int keep_row_bytes;         // 16 per 128 keys
     // Dropout kernels: weight (i, j) of head bh kept when byte j % 16 of the
     // Philox4x32-10 block {j / 16, i, bh, offset} under key {seed_lo, seed_hi}
-    // is >= p8 (philox.cuh); kept weights are scaled by keep_scale =
-    // 256 / (256 - p8) (as in the forward).
+    // is >= p8 (philox.cuh); kept weights are scaled by ks = 256 / (256 - p8)
+    // (as in the forward).  The kernels fold ks into the weights,
+    // P ks = 2^(s * scale_log2 - (LSE log2 e - log2 ks)), and with them
+    // dS = P (Z ks dP - delta) = (P ks) (Z dP - delta / ks).
     int dropout_p8;
     unsigned long long dropout_seed, dropout_offset;
     unsigned int philox_round_keys[20];  // the key schedule of dropout_seed (philox_round_keys)
-    float keep_scale;
+    float log2_keep_scale;  // log2(ks)
+    float inv_keep_scale;   // (256 - p8) / 256, exact
 };
 
 // Block mask entry of (query head bh, query tile qt, key tile kt).
@@ -463,7 +466,10 @@ __device__ void dq_work_role(const BwdParams& p, uint32_t base, const uint8_t* s
             if (!__all_sync(0xffffffffu, ok)) return;
         }
         const float* rows = reinterpret_cast<const float*>(smem + L::kStat + (uint32_t)st * L::kStatBytes);
-        const float lse2 = rows[r], delta = rows[kTile + r];
+        // Dropout: the weights come out already scaled by ks, and delta
+        // is divided by it (BwdParams::log2_keep_scale).
+        const float lse2 = DR ? rows[r] - p.log2_keep_scale : rows[r];
+        const float delta = DR ? rows[kTile + r] * p.inv_keep_scale : rows[kTile + r];
         __syncwarp();
         if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(dq_bar<D>(base, L::kStatEmpty + st));
         if (++st == L::kStatStages) {
@@ -532,7 +538,7 @@ __device__ void dq_work_role(const BwdParams& p, uint32_t base, const uint8_t* s
             }
             // Dropout: keep decisions of this row's 64 keys (four Philox
             // blocks), made while the dP product runs.  A dropped weight's dP
-            // is 0, a kept one's is scaled by keep_scale.
+            // is 0 (pr holds P ks, delta is delta / ks).
             uint64_t zb = ~0ull;
             if constexpr (DR) {
                 zb = 0ull;
@@ -543,7 +549,6 @@ __device__ void dq_work_role(const BwdParams& p, uint32_t base, const uint8_t* s
                                                    (256u - (uint32_t)p.dropout_p8) * 0x01010101u)
                           << (16 * b);
             }
-            const float ks = DR ? p.keep_scale : 1.f;
 
             ok = ptx::mbar_wait(dq_bar<D>(base, L::kDPFull), dp_phase, abort_flag, p.status, lim);
             if (!__all_sync(0xffffffffu, ok)) return;
@@ -557,16 +562,13 @@ __device__ void dq_work_role(const BwdParams& p, uint32_t base, const uint8_t* s
             ptx::reg_fence32(dr + 32);
             // dS = P (dP - delta), bf16 pairs over the first 32 of this
             // warpgroup's dP columns.
-            auto dp = [&](int e) {
-                return (!DR || ((zb >> e) & 1ull) != 0ull) ? __uint_as_float(dr[e]) * ks : 0.f;
+            auto dpd = [&](int e) {
+                const float t = __uint_as_float(dr[e]) - delta;
+                return (!DR || ((zb >> e) & 1ull) != 0ull) ? t : -delta;
             };
             uint32_t pk[32];
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-                const float d0 = pr[2 * c] * (dp(2 * c) - delta);
-                const float d1 = pr[2 * c + 1] * (dp(2 * c + 1) - delta);
-                pk[c] = ptx::pack_bf16x2(d0, d1);
-            }
+            for (int c = 0; c < 32; ++c) pk[c] = ptx::pack_bf16x2(pr[2 * c] * dpd(2 * c), pr[2 * c + 1] * dpd(2 * c + 1));
             ptx::tmem_st32(tDP, pk);
             ptx::tmem_st_wait();
             ptx::tc_fence_before();
@@ -681,8 +683,6 @@ __global__ void __launch_bounds__(DqLayout<D>::kThreads, 1)
 }
 
 // ====================================================================== dK, dV
-// ED: the kernel applies keep bits and dropout together, and each statistics
-// stage holds both bit sets.
 template <int D>
 struct DkvLayout {
     static constexpr int kThreads = 384;
@@ -837,6 +837,10 @@ __device__ void dkv_stat_role(const BwdParams& p, uint32_t base, uint8_t* smem, 
                 const bool valid = row < p.S;
                 l2[h] = valid ? __ldg(p.lse + (size_t)bh * p.S + row) * kLog2e : INFINITY;
                 dl[h] = valid ? p.delta[(size_t)bh * p.S + row] : 0.f;
+                if constexpr (DR) {  // weights scaled by ks, delta divided by it
+                    l2[h] -= p.log2_keep_scale;
+                    dl[h] *= p.inv_keep_scale;
+                }
             }
             uint4 kb[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
             if constexpr (E) {  // each query's keep bits for this key tile
@@ -1052,16 +1056,15 @@ __device__ void dkv_work_role(const BwdParams& p, uint32_t base, const uint8_t* 
                 for (int c = 0; c < 64; ++c)
                     if (((kw[4 * (64 * wg + c)] >> (r & 31)) & 1u) == 0u) pr[c] = 0.f;
             }
-            // dV takes the kept weights times keep_scale, and dP of a dropped
-            // weight is 0.
-            const float ks = DR ? p.keep_scale : 1.f;
+            // Dropout: pr holds P ks (the stage's LSE and delta carry
+            // the scaling), dV takes it where kept, and dP of a dropped weight
+            // is 0.
             auto kept = [&](int c) -> bool { return !DR || ((zb >> c) & 1ull) != 0ull; };
             uint32_t pk[32];
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
                 if constexpr (DR)
-                    pk[c] = ptx::pack_bf16x2(kept(2 * c) ? pr[2 * c] * ks : 0.f,
-                                             kept(2 * c + 1) ? pr[2 * c + 1] * ks : 0.f);
+                    pk[c] = ptx::pack_bf16x2(kept(2 * c) ? pr[2 * c] : 0.f, kept(2 * c + 1) ? pr[2 * c + 1] : 0.f);
                 else
                     pk[c] = ptx::pack_bf16x2(pr[2 * c], pr[2 * c + 1]);
             }
@@ -1084,11 +1087,14 @@ __device__ void dkv_work_role(const BwdParams& p, uint32_t base, const uint8_t* 
 #pragma unroll
             for (int c = 0; c < 64; c += 4) {
                 const float4 d4 = *reinterpret_cast<const float4*>(dlt + c);
-                auto dp = [&](int e) { return kept(e) ? __uint_as_float(dr[e]) * ks : 0.f; };
-                const float a0 = pr[c + 0] * (dp(c + 0) - d4.x);
-                const float a1 = pr[c + 1] * (dp(c + 1) - d4.y);
-                const float a2 = pr[c + 2] * (dp(c + 2) - d4.z);
-                const float a3 = pr[c + 3] * (dp(c + 3) - d4.w);
+                auto dpd = [&](int e, float d) {
+                    const float t = __uint_as_float(dr[e]) - d;
+                    return kept(e) ? t : -d;
+                };
+                const float a0 = pr[c + 0] * dpd(c + 0, d4.x);
+                const float a1 = pr[c + 1] * dpd(c + 1, d4.y);
+                const float a2 = pr[c + 2] * dpd(c + 2, d4.z);
+                const float a3 = pr[c + 3] * dpd(c + 3, d4.w);
                 pk[c / 2] = ptx::pack_bf16x2(a0, a1);
                 pk[c / 2 + 1] = ptx::pack_bf16x2(a2, a3);
             }
