@@ -385,10 +385,8 @@ __device__ void ws_mma_role(const FwdParams& p, uint32_t base, uint32_t tmem,
         int pre_kslot = 0;
         for (int rnd = 0, u = unit_of_round(0); u < p.num_units; u = unit_of_round(++rnd)) {
             const Unit w = decode_unit(u, p, round_desc(rnd));
-            if ((!pre && !ptx::mbar_wait_spin(ws_bar<D, F>(base, L::kQFull + 0), qf_phase, abort_flag, p.status, lim)) ||
-                !ptx::mbar_wait_spin(ws_bar<D, F>(base, L::kQFull + 1), qf_phase, abort_flag, p.status, lim))
+            if (!pre && !ptx::mbar_wait_spin(ws_bar<D, F>(base, L::kQFull + 0), qf_phase, abort_flag, p.status, lim))
                 break;
-            qf_phase ^= 1u;
             ptx::tc_fence_after();
             // Step s visits key tile key_of_step(w, s); query tile i uses it when
             // that key tile is below n_i.  Ascending: tile i uses steps
@@ -408,6 +406,11 @@ __device__ void ws_mma_role(const FwdParams& p, uint32_t base, uint32_t tmem,
                 if (last0 == 0) ptx::mma_commit(ws_bar<D, F>(base, L::kQEmpty + 0));
             }
             pre = false;
+            // Q_1 is waited for only now: at the kernel's start S_0 need not wait
+            // for Q_1's copy too.
+            if (!ptx::mbar_wait_spin(ws_bar<D, F>(base, L::kQFull + 1), qf_phase, abort_flag, p.status, lim)) break;
+            qf_phase ^= 1u;
+            ptx::tc_fence_after();
             if (act1(0)) {
                 issue_s(1, kslot);
                 if (last1 == 0) ptx::mma_commit(ws_bar<D, F>(base, L::kQEmpty + 1));
