@@ -278,6 +278,8 @@ drain:
     if (pend_q) ptx::drain_wait(dq_bar<D>(base, L::kQFull), pend_q_par, lim);
 }
 
+// The MMA issuers of both kernels spin on their barriers (mbar_wait_spin) as
+// the forward's does: the tensor core idles while its only feeding thread waits.
 template <int D, bool M, bool E, bool DR>
 __device__ void dq_mma_role(const BwdParams& p, uint32_t base, uint32_t tmem, volatile int* abort_flag) {
     using L = DqLayout<D>;
@@ -293,7 +295,7 @@ __device__ void dq_mma_role(const BwdParams& p, uint32_t base, uint32_t tmem, vo
     int slot = 0;
 
     auto wait_ring = [&](int& got) -> bool {
-        if (!ptx::mbar_wait(dq_bar<D>(base, L::kKVFull + slot), ring_phase, abort_flag, p.status, lim))
+        if (!ptx::mbar_wait_spin(dq_bar<D>(base, L::kKVFull + slot), ring_phase, abort_flag, p.status, lim))
             return false;
         got = slot;
         if (++slot == L::kStages) {
@@ -304,7 +306,7 @@ __device__ void dq_mma_role(const BwdParams& p, uint32_t base, uint32_t tmem, vo
         return true;
     };
     auto wait_bar = [&](int bar, uint32_t& phase) -> bool {
-        if (!ptx::mbar_wait(dq_bar<D>(base, bar), phase, abort_flag, p.status, lim)) return false;
+        if (!ptx::mbar_wait_spin(dq_bar<D>(base, bar), phase, abort_flag, p.status, lim)) return false;
         phase ^= 1u;
         ptx::tc_fence_after();
         return true;
@@ -889,13 +891,13 @@ __device__ void dkv_mma_role(const BwdParams& p, uint32_t base, uint32_t tmem, v
     int slot = 0;
 
     auto wait_bar = [&](int bar, uint32_t& phase) -> bool {
-        if (!ptx::mbar_wait(dkv_bar<L>(base, bar), phase, abort_flag, p.status, lim)) return false;
+        if (!ptx::mbar_wait_spin(dkv_bar<L>(base, bar), phase, abort_flag, p.status, lim)) return false;
         phase ^= 1u;
         ptx::tc_fence_after();
         return true;
     };
     auto wait_ring = [&](int& got) -> bool {
-        if (!ptx::mbar_wait(dkv_bar<L>(base, L::kStFull + slot), ring_phase, abort_flag, p.status, lim))
+        if (!ptx::mbar_wait_spin(dkv_bar<L>(base, L::kStFull + slot), ring_phase, abort_flag, p.status, lim))
             return false;
         got = slot;
         if (++slot == L::kStages) {
