@@ -16,6 +16,7 @@
 #include "common.cuh"
 #include "kernel_simple.cuh"
 #include "kernel_ws.cuh"
+#include "fwd_schedule.h"
 #include "tmap_cache.h"
 
 // Status word: bits set by device-side waits that ran out (ptx::kStatusTimeout).
@@ -201,6 +202,45 @@ int launch_simple(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMa
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
+// The forward kernel's unit order for a shape and CTA count (fwd_schedule.h),
+// from a small least-recently-used cache: building one takes a few tens of
+// microseconds, a lookup well under one.  `enabled` = 0 when the table cannot
+// hold the shape.
+struct SchedEntry {
+    int bh, nq, causal, grid;
+    unsigned long long last_use;
+    FwdSchedule sched;
+};
+std::mutex g_sched_mutex;
+SchedEntry g_sched_cache[8];
+unsigned long long g_sched_clock = 0;
+
+void fwd_schedule(int bh, int nq, bool causal, int grid, FwdSchedule* out) {
+    std::lock_guard<std::mutex> lock(g_sched_mutex);
+    SchedEntry* victim = &g_sched_cache[0];
+    for (SchedEntry& e : g_sched_cache) {
+        if (e.last_use != 0 && e.bh == bh && e.nq == nq && e.causal == (int)causal && e.grid == grid) {
+            e.last_use = ++g_sched_clock;
+            std::memcpy(out, &e.sched, sizeof *out);
+            return;
+        }
+        if (e.last_use < victim->last_use) victim = &e;
+    }
+    std::memset(&victim->sched, 0, sizeof victim->sched);
+    const long long units = (long long)bh * ((nq + 1) / 2);
+    victim->sched.enabled = host::fwd_schedule_wanted(units, grid) &&
+                                    host::build_fwd_schedule(bh, nq, causal, grid, kSchedMaxUnits, kSchedMaxCtas,
+                                                             victim->sched.start, victim->sched.order)
+                                ? 1
+                                : 0;
+    victim->bh = bh;
+    victim->nq = nq;
+    victim->causal = (int)causal;
+    victim->grid = grid;
+    victim->last_use = ++g_sched_clock;
+    std::memcpy(out, &victim->sched, sizeof *out);
+}
+
 template <int D, bool F, bool M, bool DR = false, bool E = false>
 int launch_ws(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
               FwdParams p, int sm_count, cudaStream_t stream) {
@@ -209,8 +249,10 @@ int launch_ws(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& t
     if (units > (1ll << 31) - 1) return ATTN_ERR_UNSUPPORTED;
     p.num_units = (int)units;
     const int grid = (int)(units < sm_count ? units : sm_count);
+    FwdSchedule sched;
+    fwd_schedule(p.B * p.Hq, p.num_q_tiles, p.causal != 0, grid, &sched);
     attn_fwd_ws_kernel<D, F, M, DR, E><<<grid, WsLayout<D, F>::kThreads, WsLayout<D, F>::kDynamicSmem, stream>>>(
-        tq, tk, tv, to, p);
+        tq, tk, tv, to, p, sched);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
@@ -469,6 +511,18 @@ extern "C" const char* attn_status_string(int status) {
 }
 
 extern "C" int attn_version(void) { return kVersion; }
+
+extern "C" int attn_fwd_schedule(int batch_heads, int num_q_tiles, int causal, int num_ctas,
+                                 unsigned short* order, unsigned short* start) {
+    if (order == nullptr || start == nullptr || batch_heads <= 0 || num_q_tiles <= 0 || num_ctas <= 0)
+        return ATTN_ERR_INVALID_ARG;
+    if (!attn::host::fwd_schedule_wanted((long long)batch_heads * ((num_q_tiles + 1) / 2), num_ctas))
+        return ATTN_ERR_UNSUPPORTED;
+    return attn::host::build_fwd_schedule(batch_heads, num_q_tiles, causal != 0, num_ctas, attn::kSchedMaxUnits,
+                                          attn::kSchedMaxCtas, start, order)
+               ? ATTN_OK
+               : ATTN_ERR_UNSUPPORTED;
+}
 
 // ---------------------------------------------------------------- shared host services
 #include "host.h"

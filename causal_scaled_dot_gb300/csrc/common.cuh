@@ -35,6 +35,19 @@ struct FwdParams {
     int keep_row_bytes;             // 16 per 128 keys
 };
 
+// The order in which the persistent forward kernel's CTAs take their units,
+// computed on the host (attn_api.cu, fwd_schedule) and passed as a kernel
+// parameter: CTA c runs units order[start[c]] .. order[start[c + 1] - 1] in
+// turn.  `enabled` = 0 (more units or CTAs than the table holds) selects the
+// arithmetic order of unit_of_round instead.
+constexpr int kSchedMaxCtas = 160;
+constexpr int kSchedMaxUnits = 4096;
+struct FwdSchedule {
+    int enabled;
+    unsigned short start[kSchedMaxCtas + 1];
+    unsigned short order[kSchedMaxUnits];
+};
+
 // The Philox4x32-10 key schedule of `seed`: round r uses key words
 // (lo32(seed) + r * 0x9E3779B9, hi32(seed) + r * 0xBB67AE85) mod 2^32.  The
 // same for every thread of a launch, so the host computes it once and the

@@ -66,8 +66,8 @@ struct WsLayout {
     static constexpr int kThreads = 384;
     // Registers per thread after the split: warps 0-3 (producer, MMA issuer,
     // idle) shrink, the softmax warps grow.  Launch allocation: 384 x 168 =
-    // 64512 >= 128 x kRegsSmall + 256 x kRegsSoftmax = 63488.
-    static constexpr int kRegsSmall = 64;
+    // 64512 = 128 x kRegsSmall + 256 x kRegsSoftmax.
+    static constexpr int kRegsSmall = 72;
     static constexpr int kRegsSoftmax = 216;
     static_assert(128 * kRegsSmall + 256 * kRegsSoftmax <= kThreads * 168, "register split");
     static constexpr uint32_t kTileBytes = kTile * D * kElemBytes;  // 32 KB at bf16 D = 128
@@ -195,9 +195,18 @@ __device__ __forceinline__ int last_visit(const FwdParams& p, const Unit& w, int
     return -1;
 }
 
-// The unit this CTA runs in round r (>= num_units: no more work).
-__device__ __forceinline__ int unit_of_round(int r) {
-    const int G = gridDim.x, c = blockIdx.x;
+// The unit this CTA runs in round r (>= num_units: no more work): from the
+// host's table when it has one, else the boustrophedon order -- round r
+// takes units [rG, rG + G), even rounds by CTA index, odd rounds in reverse,
+// so that with units sorted heaviest first a CTA's heavy unit of one round
+// pairs with a light one of the next.
+__device__ __forceinline__ int unit_of_round(const FwdSchedule& sc, int num_units, int r) {
+    const int c = blockIdx.x;
+    if (sc.enabled) {
+        const int i = (int)sc.start[c] + r;
+        return i < (int)sc.start[c + 1] ? (int)sc.order[i] : num_units;
+    }
+    const int G = gridDim.x;
     return r * G + ((r & 1) ? (G - 1 - c) : c);
 }
 
@@ -209,7 +218,7 @@ __device__ __forceinline__ uint32_t ws_bar(uint32_t base, int i) {
 // ---------------------------------------------------------------- producer
 template <int D, bool F, bool M, bool DR, bool E>
 __device__ void ws_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
-                             const CUtensorMap* tm_v, const FwdParams& p, uint32_t base,
+                             const CUtensorMap* tm_v, const FwdParams& p, const FwdSchedule& sc, uint32_t base,
                              volatile int* abort_flag) {
     using L = WsLayout<D, F>;
     uint32_t qe_phase[2] = {0u, 0u};
@@ -240,7 +249,8 @@ __device__ void ws_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
         pend_q_par = (pend_q_par & ~(1u << i)) | (((qe_phase[i] ^ 1u) & 1u) << i);
         return true;
     };
-    for (int rnd = 0, u = unit_of_round(0); u < p.num_units; u = unit_of_round(++rnd)) {
+    for (int rnd = 0, u = unit_of_round(sc, p.num_units, 0); u < p.num_units;
+             u = unit_of_round(sc, p.num_units, ++rnd)) {
         const Unit w = decode_unit(u, p, round_desc(rnd));
         // Without a block mask the issuer starts a unit's first S_0 = Q_0 K_0^T
         // while the previous unit's last softmax runs (see the MMA role), so
@@ -301,7 +311,7 @@ drain:
 // the other roles keep the suspend hint, so that their waiting warps leave
 // issue slots to the softmax warps on their schedulers.
 template <int D, bool F, bool M, bool DR, bool E>
-__device__ void ws_mma_role(const FwdParams& p, uint32_t base, uint32_t tmem,
+__device__ void ws_mma_role(const FwdParams& p, const FwdSchedule& sc, uint32_t base, uint32_t tmem,
                             volatile int* abort_flag) {
     using L = WsLayout<D, F>;
     constexpr uint32_t kIdescS = F ? ptx::idesc_e4m3_f32(kTile, kTile, false)
@@ -383,7 +393,8 @@ __device__ void ws_mma_role(const FwdParams& p, uint32_t base, uint32_t tmem,
         // after reading O_0 out, so O_0 is not overwritten early.
         bool pre = false;  // this unit's first S_0 was issued during the previous unit
         int pre_kslot = 0;
-        for (int rnd = 0, u = unit_of_round(0); u < p.num_units; u = unit_of_round(++rnd)) {
+        for (int rnd = 0, u = unit_of_round(sc, p.num_units, 0); u < p.num_units;
+             u = unit_of_round(sc, p.num_units, ++rnd)) {
             const Unit w = decode_unit(u, p, round_desc(rnd));
             if (!pre && !ptx::mbar_wait_spin(ws_bar<D, F>(base, L::kQFull + 0), qf_phase, abort_flag, p.status, lim))
                 break;
@@ -433,7 +444,7 @@ __device__ void ws_mma_role(const FwdParams& p, uint32_t base, uint32_t tmem,
                         if (sn == last0) ptx::mma_commit(ws_bar<D, F>(base, L::kQEmpty + 0));
                     }
                 } else {
-                    const int u2 = unit_of_round(rnd + 1);
+                    const int u2 = unit_of_round(sc, p.num_units, rnd + 1);
                     if (u2 < p.num_units) {  // the next unit's first S_0
                         const Unit w2 = decode_unit(u2, p, round_desc(rnd + 1));
                         if (!(ok = ptx::mbar_wait_spin(ws_bar<D, F>(base, L::kQFull + 0), qf_phase, abort_flag,
@@ -463,7 +474,8 @@ __device__ void ws_mma_role(const FwdParams& p, uint32_t base, uint32_t tmem,
             if (!ok) break;
         }
     } else {
-        for (int rnd = 0, u = unit_of_round(0); u < p.num_units; u = unit_of_round(++rnd)) {
+        for (int rnd = 0, u = unit_of_round(sc, p.num_units, 0); u < p.num_units;
+             u = unit_of_round(sc, p.num_units, ++rnd)) {
             const Unit w = decode_unit(u, p, round_desc(rnd));
             if (!ptx::mbar_wait_spin(ws_bar<D, F>(base, L::kQFull + 0), qf_phase, abort_flag, p.status, lim) ||
                 !ptx::mbar_wait_spin(ws_bar<D, F>(base, L::kQFull + 1), qf_phase, abort_flag, p.status, lim))
@@ -543,8 +555,8 @@ __device__ void ws_mma_role(const FwdParams& p, uint32_t base, uint32_t tmem,
 
 // ---------------------------------------------------------------- softmax
 template <int D, bool F, bool M, bool DR, bool E>
-__device__ void ws_softmax_role(const CUtensorMap* tm_o, const FwdParams& p, uint32_t base, uint32_t tmem,
-                                int wg, volatile int* abort_flag) {
+__device__ void ws_softmax_role(const CUtensorMap* tm_o, const FwdParams& p, const FwdSchedule& sc, uint32_t base,
+                                uint32_t tmem, int wg, volatile int* abort_flag) {
     using L = WsLayout<D, F>;
     const int r = threadIdx.x - (4 + 4 * wg) * 32;  // row within the query tile, 0..127
     const int warp_in_wg = r >> 5;
@@ -562,7 +574,8 @@ __device__ void ws_softmax_role(const CUtensorMap* tm_o, const FwdParams& p, uin
     const uint64_t lim = p.wait_limit_ns;
     uint32_t s_phase = 0, o_phase = 0;
 
-    for (int rnd = 0, u = unit_of_round(0); u < p.num_units; u = unit_of_round(++rnd)) {
+    for (int rnd = 0, u = unit_of_round(sc, p.num_units, 0); u < p.num_units;
+             u = unit_of_round(sc, p.num_units, ++rnd)) {
         const Unit w = decode_unit(u, p, round_desc(rnd));
         const int qt = w.qt[wg];
         const int n_i = wg == 0 ? w.n0 : w.n1;
@@ -837,9 +850,9 @@ __device__ void ws_softmax_role(const CUtensorMap* tm_o, const FwdParams& p, uin
 // The softmax role plus the completion of this warp's output stores, which
 // must have finished reading shared memory before the CTA exits.
 template <int D, bool F, bool M, bool DR, bool E>
-__device__ void ws_softmax_warp(const CUtensorMap* tm_o, const FwdParams& p, uint32_t base, uint32_t tmem,
-                                int wg, volatile int* abort_flag) {
-    ws_softmax_role<D, F, M, DR, E>(tm_o, p, base, tmem, wg, abort_flag);
+__device__ void ws_softmax_warp(const CUtensorMap* tm_o, const FwdParams& p, const FwdSchedule& sc, uint32_t base,
+                                uint32_t tmem, int wg, volatile int* abort_flag) {
+    ws_softmax_role<D, F, M, DR, E>(tm_o, p, sc, base, tmem, wg, abort_flag);
     if ((threadIdx.x & 31) == 0) ptx::bulk_wait_group<0>();
     __syncwarp();
 }
@@ -850,7 +863,8 @@ __global__ void __launch_bounds__(WsLayout<D, F>::kThreads, 1)
     attn_fwd_ws_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v,
-                       const __grid_constant__ CUtensorMap tm_o, const FwdParams p) {
+                       const __grid_constant__ CUtensorMap tm_o, const FwdParams p,
+                       const __grid_constant__ FwdSchedule sched) {
     using L = WsLayout<D, F>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
@@ -894,13 +908,13 @@ __global__ void __launch_bounds__(WsLayout<D, F>::kThreads, 1)
     if (warp < 4) {
         ptx::regs_dec<L::kRegsSmall>();
         if (warp == 0) {
-            if (lane == 0) ws_load_role<D, F, M, DR, E>(&tm_q, &tm_k, &tm_v, p, base, abort_flag);
+            if (lane == 0) ws_load_role<D, F, M, DR, E>(&tm_q, &tm_k, &tm_v, p, sched, base, abort_flag);
         } else if (warp == 1) {
-            if (lane == 0) ws_mma_role<D, F, M, DR, E>(p, base, tmem, abort_flag);
+            if (lane == 0) ws_mma_role<D, F, M, DR, E>(p, sched, base, tmem, abort_flag);
         }
     } else {
         ptx::regs_inc<L::kRegsSoftmax>();
-        ws_softmax_warp<D, F, M, DR, E>(&tm_o, p, base, tmem, (warp - 4) >> 2, abort_flag);
+        ws_softmax_warp<D, F, M, DR, E>(&tm_o, p, sched, base, tmem, (warp - 4) >> 2, abort_flag);
     }
 
     ptx::tc_fence_before();

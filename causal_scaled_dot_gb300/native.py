@@ -85,6 +85,9 @@ def load() -> ctypes.CDLL:
         lib.attn_status_string.restype = ctypes.c_char_p
         lib.attn_version.argtypes = []
         lib.attn_version.restype = ci
+        u16p = ctypes.POINTER(ctypes.c_ushort)
+        lib.attn_fwd_schedule.argtypes = [ci, ci, ci, ci, u16p, u16p]
+        lib.attn_fwd_schedule.restype = ci
         _lib = lib
         return lib
 
@@ -408,6 +411,24 @@ def attn_status_string(code: int) -> str:
 
 def attn_version() -> int:
     return load().attn_version()
+
+
+def fwd_schedule(batch_heads: int, num_q_tiles: int, causal: bool, num_ctas: int):
+    """The forward kernel's work order (``attn_fwd_schedule``): a list with, for
+    each CTA, the unit numbers it runs in turn; None when the kernel falls back
+    to its arithmetic order for this shape."""
+    import numpy as np
+    npairs = (num_q_tiles + 1) // 2
+    order = np.zeros(max(batch_heads * npairs, 1), dtype=np.uint16)
+    start = np.zeros(num_ctas + 1, dtype=np.uint16)
+    u16p = ctypes.POINTER(ctypes.c_ushort)
+    rc = load().attn_fwd_schedule(int(batch_heads), int(num_q_tiles), 1 if causal else 0, int(num_ctas),
+                                  order.ctypes.data_as(u16p), start.ctypes.data_as(u16p))
+    if rc == ATTN_ERR_UNSUPPORTED:
+        return None
+    if rc != ATTN_OK:
+        raise ValueError(attn_status_string(rc))
+    return [order[start[c]:start[c + 1]].astype(int).tolist() for c in range(num_ctas)]
 
 
 def _check_attention_tensors(named):

@@ -7,9 +7,10 @@
  * the weights attn_fwd_dropout; their combinations attn_fwd_ex), the matching
  * gradients (attn_bwd, attn_bwd_block_masked, attn_bwd_elem_masked,
  * attn_bwd_dropout, attn_bwd_ex), the output
- * projection of the attention output (attn_out_proj), and status helpers
+ * projection of the attention output (attn_out_proj), status helpers
  * (attn_sync_status, attn_selftest_wait_timeout, attn_status_string,
- * attn_version).
+ * attn_version), and the forward's work order for inspection
+ * (attn_fwd_schedule).
  *
  * The operation (one output row per query position i of every batch b and
  * query head hq) is the five-step naive causal attention that the
@@ -34,7 +35,9 @@
  * encoded TMA descriptors, keyed by device, address, element size, extents and
  * box -- every input of the encode, so a hit is exactly what a fresh encode
  * would give, including for a buffer freed and reallocated at the same
- * address -- each guarded by a mutex.  The work runs on the calling thread's
+ * address -- and a least-recently-used cache of the forward kernel's work
+ * order for 8 shapes (attn_fwd_schedule; a pure function of the shape and the
+ * SM count), each guarded by a mutex.  The work runs on the calling thread's
  * current device (cudaGetDevice), which must hold every buffer; its primary
  * context is bound to the thread on entry, so a thread that has made no CUDA
  * call yet (an autograd engine's worker, say) can call too.
@@ -362,6 +365,29 @@ const char *attn_status_string(int status);
 
 /* Library version, major*10000 + minor*100 + patch. */
 int attn_version(void);
+
+/*
+ * attn_fwd_schedule -- the order in which the forward kernel's `num_ctas`
+ * persistent CTAs take their work units, for inspection and tests; the pages
+ * have no counterpart (it is this library's scheduling, not part of the
+ * method).  A unit is one flat head bh = b*Hq + hq (0 <= bh < batch_heads)
+ * and one pair of query tiles m (tiles 2m and 2m+1 of num_q_tiles =
+ * ceil(S / 128)), numbered u = (npairs - 1 - m) * batch_heads + bh with
+ * npairs = ceil(num_q_tiles / 2).  On ATTN_OK, CTA c runs
+ * order[start[c]] .. order[start[c + 1] - 1] in turn: `start` receives
+ * num_ctas + 1 entries and `order` batch_heads * npairs (caller-owned host
+ * arrays).  Units go out head block by head block (16 query heads), the
+ * heaviest pair of a block first, each to the CTA that frees up first under
+ * a cost of its tile products (causal != 0: a pair's tiles need key tiles up
+ * to their diagonal).  Pure host computation: no device, no stream.
+ * Returns ATTN_ERR_INVALID_ARG for a null array or a size <= 0, and
+ * ATTN_ERR_UNSUPPORTED when the forward does not use a table for the shape:
+ * fewer than two units per CTA, or more than the table holds (4096 units,
+ * 160 CTAs).  The forward then uses its arithmetic order (round r: units
+ * rG .. rG+G-1 for G CTAs, even rounds by CTA index, odd rounds reversed).
+ */
+int attn_fwd_schedule(int batch_heads, int num_q_tiles, int causal, int num_ctas, unsigned short *order,
+                      unsigned short *start);
 
 #ifdef __cplusplus
 } /* extern "C" */
