@@ -108,10 +108,11 @@ def host_us_per_call(call, n: int = 200) -> float:
     return sorted(per)[2]
 
 
-# The sources of the timed kernels, per pass (the forward's launch geometry --
-# one CTA per SM, 384 threads -- is fixed in attn_api.cu; re-take the record if
-# it changes).
-FWD_SOURCES = ("common.cuh", "kernel_ws.cuh", "philox.cuh", "ptx.cuh")
+# The sources of the timed kernels, per pass, with the forward's unit order
+# (fwd_schedule.h), which decides what stays in L2 (the launch geometry -- one
+# CTA per SM, 384 threads -- is fixed in attn_api.cu; re-take the record if it
+# changes).
+FWD_SOURCES = ("common.cuh", "fwd_schedule.h", "kernel_ws.cuh", "philox.cuh", "ptx.cuh")
 BWD_SOURCES = ("attn_bwd.cu", "common.cuh", "kernel_bwd.cuh", "ptx.cuh")
 PROJ_SOURCES = ("attn_proj.cu", "common.cuh", "kernel_proj.cuh", "ptx.cuh")
 

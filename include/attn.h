@@ -380,6 +380,8 @@ int attn_version(void);
  * heaviest pair of a block first, each to the CTA that frees up first under
  * a cost of its tile products (causal != 0: a pair's tiles need key tiles up
  * to their diagonal).  Pure host computation: no device, no stream.
+ * The block-masked forwards (a block mask given) always use the arithmetic
+ * order, whose CTAs get equal unit counts whatever the mask keeps.
  * Returns ATTN_ERR_INVALID_ARG for a null array or a size <= 0, and
  * ATTN_ERR_UNSUPPORTED when the forward does not use a table for the shape:
  * fewer than two units per CTA, or more than the table holds (4096 units,
