@@ -607,6 +607,24 @@ __device__ void ws_softmax_role(const CUtensorMap* tm_o, const FwdParams& p, con
                     }
                 }
             }
+            // Dropout: this tile's keep decisions, made while the warpgroup
+            // waits for its scores (the tensor core is still on the other
+            // query tile's products): one Philox4x32-10 block per 16 keys of
+            // the row, kept as carry-test words (bit 7 of byte b: key
+            // 16 blk + 4 w + b is kept).
+            uint32_t gw[DR ? 32 : 1];
+            if constexpr (DR) {
+                const uint32_t c4 = (256u - (uint32_t)p.dropout_p8) * 0x01010101u;
+                const uint32_t qrow = (uint32_t)(qt * kTile + r);
+#pragma unroll
+                for (int b = 0; b < 8; ++b) {
+                    uint32_t rnd[4];
+                    philox4x32_10((uint32_t)(j * 8 + b), qrow, (uint32_t)w.bh, (uint32_t)p.dropout_offset,
+                                  p.philox_round_keys, rnd);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) gw[4 * b + k] = bytes_ge(rnd[k], c4);
+                }
+            }
             bool ok = ptx::mbar_wait(bar_s, s_phase, abort_flag, p.status, lim);
             if (!__all_sync(0xffffffffu, ok)) return;
             s_phase ^= 1u;
@@ -694,37 +712,22 @@ __device__ void ws_softmax_role(const CUtensorMap* tm_o, const FwdParams& p, con
                     ptx::tmem_st16(tP + 32u + 16u * h, pk);
                 }
             } else if constexpr (DR) {
-                // Dropout: key kv0 + e is kept when byte e mod 16 of the Philox
-                // block {(kv0 + e) / 16, query row, b*Hq + hq, offset} under key
-                // {seed mod 2^32, seed / 2^32} is >= p8.  The row sum takes every
-                // probability; the tensor core gets the kept ones (the
-                // 256 / (256 - p8) factor is in o_scale).
-                const uint32_t qrow = (uint32_t)(qt * kTile + r);
-                const uint32_t p8 = (uint32_t)p.dropout_p8;
-                // One block per 16 keys, interleaved with their exponentials so
-                // that the generator's integer work and the exp2 unit overlap
-                // (generating a half tile's bits first measured 16 % slower).
-                const uint32_t c4 = (256u - p8) * 0x01010101u;
+                // Dropout: the row sum takes every probability; the tensor core
+                // gets the kept ones (the 256 / (256 - p8) factor is in o_scale).
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     uint32_t pk[32];
 #pragma unroll
-                    for (int b = 0; b < 4; ++b) {
-                        uint32_t rnd[4];
-                        philox4x32_10((uint32_t)((kv0 + 64 * h + 16 * b) >> 4), qrow, (uint32_t)w.bh,
-                                      (uint32_t)p.dropout_offset, p.philox_round_keys, rnd);
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            const int e = 64 * h + 16 * b + 2 * c;
-                            float x0, x1;
-                            ptx::f2_split(ptx::fma2(ptx::f2(s[e], s[e + 1]), sl2x2, negm2), x0, x1);
-                            const float p0 = ptx::ex2(x0);
-                            const float p1 = ptx::ex2(x1);
-                            acc[c & 3] = ptx::add2(acc[c & 3], ptx::f2(p0, p1));
-                            // keys e, e+1: bytes 2c, 2c+1 of the block
-                            const uint32_t keep = pair_mask(bytes_ge(rnd[c >> 1], c4), (c & 1) ? 0xBBAAu : 0x9988u);
-                            pk[8 * b + c] = ptx::pack_bf16x2(p0, p1) & keep;
-                        }
+                    for (int c = 0; c < 32; ++c) {
+                        const int e = 64 * h + 2 * c;
+                        float x0, x1;
+                        ptx::f2_split(ptx::fma2(ptx::f2(s[e], s[e + 1]), sl2x2, negm2), x0, x1);
+                        const float p0 = ptx::ex2(x0);
+                        const float p1 = ptx::ex2(x1);
+                        acc[c & 3] = ptx::add2(acc[c & 3], ptx::f2(p0, p1));
+                        // keys e, e+1: bytes 2 (c mod 2), 2 (c mod 2) + 1 of word e / 4
+                        const uint32_t keep = pair_mask(gw[e >> 2], (c & 1) ? 0xBBAAu : 0x9988u);
+                        pk[c] = ptx::pack_bf16x2(p0, p1) & keep;
                     }
                     ptx::tmem_st32(tP + 32 * h, pk);
                 }
