@@ -117,12 +117,21 @@ BWD_SOURCES = ("attn_bwd.cu", "common.cuh", "kernel_bwd.cuh", "ptx.cuh")
 PROJ_SOURCES = ("attn_proj.cu", "common.cuh", "kernel_proj.cuh", "ptx.cuh")
 
 
+def _code_only(text: str) -> bytes:
+    """Source text without comments and with whitespace runs collapsed, so that
+    a comment edit leaves the hash (and the traffic record keyed by it) alone.
+    String literals in these sources hold no comment markers."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split()).encode()
+
+
 def kernel_source_hash(sources=FWD_SOURCES) -> str:
     csrc = os.path.join(ROOT, "causal_scaled_dot_gb300", "csrc")
     h = hashlib.sha256()
     for fn in sources:
-        with open(os.path.join(csrc, fn), "rb") as f:
-            h.update(fn.encode() + b"\0" + f.read())
+        with open(os.path.join(csrc, fn), encoding="utf-8") as f:
+            h.update(fn.encode() + b"\0" + _code_only(f.read()))
     return h.hexdigest()[:16]
 
 

@@ -3,10 +3,12 @@
 // Work unit: one (batch, query head) and a pair of adjacent 128-row query
 // tiles (2m, 2m+1).  Units are numbered heaviest causal pairs first (pair
 // index descending), query heads that share a key/value head next to each
-// other so their K/V tiles are reused from L2.  One CTA per SM takes one unit
-// per round in boustrophedon order -- round r gives unit r*G + c to CTA c on
-// even rounds and to CTA G-1-c on odd ones -- which balances the sorted unit
-// costs about as well as a dynamic queue, with no global state.
+// other.  One CTA per SM takes its units in the order of a table the host
+// computes per shape (fwd_schedule.h: head block by head block, so that the
+// K/V tiles of the heads in flight stay in L2, each unit to the CTA that
+// frees up first), or, without a table, in boustrophedon rounds -- round r
+// gives unit r*G + c to CTA c on even rounds and to CTA G-1-c on odd ones --
+// which balances the sorted unit costs with no global state either way.
 //
 // Roles (384 threads, 12 warps):
 //   warp 0      TMA producer: Q tiles of the unit, then K_j, V_j into a ring
@@ -14,7 +16,7 @@
 //   warp 1      MMA issuer (one thread) and TMEM owner: S_i = Q_i K_j^T
 //               (both operands in shared memory) and O_i += P_i V_j (P read
 //               from tensor memory).
-//   warps 2-3   idle.
+//   warps 2-3   idle (a separate correction warpgroup measured slower).
 //   warps 4-7   softmax warpgroup 0: one thread per row of query tile 2m.
 //   warps 8-11  softmax warpgroup 1: one thread per row of query tile 2m+1.
 // The two warpgroups ping-pong: while one runs its softmax the tensor core
