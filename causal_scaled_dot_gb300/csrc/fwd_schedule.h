@@ -30,8 +30,7 @@
 
 #include <cstdint>
 #include <functional>
-#include <queue>
-#include <utility>
+#include <algorithm>
 #include <vector>
 
 namespace attn {
@@ -60,28 +59,33 @@ inline bool build_fwd_schedule(int bh_count, int nq, bool causal, int grid, int 
     const long long npairs = (nq + 1) / 2;
     const long long units = (long long)bh_count * npairs;
     if (units > max_units || units > 65535) return false;
-    std::vector<std::vector<uint16_t>> lists((size_t)grid);
-    // (time the CTA frees up, CTA): the smallest first, ties to the lower CTA.
-    using Slot = std::pair<long long, int>;
-    std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> free_at;
-    for (int c = 0; c < grid; ++c) free_at.push(Slot(0, c));
+    // Pass 1: the CTA of each unit in hand-out order, from a min-heap of
+    // (time the CTA frees up) << 8 | CTA: the earliest first, ties to the lower CTA.
+    std::vector<uint16_t> unit_of((size_t)units), cta_of((size_t)units);
+    std::vector<uint64_t> heap;
+    heap.reserve((size_t)grid);
+    for (int c = 0; c < grid; ++c) heap.push_back((uint64_t)c);  // already a valid min-heap
+    const auto later = std::greater<uint64_t>();
+    size_t k = 0;
     for (int b0 = 0; b0 < bh_count; b0 += kHeadBlock) {
         const int b1 = b0 + kHeadBlock < bh_count ? b0 + kHeadBlock : bh_count;
         for (long long m = npairs - 1; m >= 0; --m) {
-            for (int bh = b0; bh < b1; ++bh) {
-                const Slot s = free_at.top();
-                free_at.pop();
-                lists[(size_t)s.second].push_back((uint16_t)((npairs - 1 - m) * bh_count + bh));
-                free_at.push(Slot(s.first + fwd_unit_cost((int)m, nq, causal), s.second));
+            const uint64_t cost = (uint64_t)fwd_unit_cost((int)m, nq, causal) << 8;
+            for (int bh = b0; bh < b1; ++bh, ++k) {
+                std::pop_heap(heap.begin(), heap.end(), later);
+                unit_of[k] = (uint16_t)((npairs - 1 - m) * bh_count + bh);
+                cta_of[k] = (uint16_t)(heap.back() & 0xFFu);
+                heap.back() += cost;
+                std::push_heap(heap.begin(), heap.end(), later);
             }
         }
     }
-    int pos = 0;
-    for (int c = 0; c < grid; ++c) {
-        start[c] = (uint16_t)pos;
-        for (uint16_t u : lists[(size_t)c]) order[pos++] = u;
-    }
-    start[grid] = (uint16_t)pos;
+    // Pass 2: group by CTA, keeping each CTA's units in hand-out order.
+    std::vector<int> fill((size_t)grid + 1, 0);
+    for (size_t i = 0; i < k; ++i) ++fill[(size_t)cta_of[i] + 1];
+    for (int c = 0; c < grid; ++c) fill[(size_t)c + 1] += fill[(size_t)c];
+    for (int c = 0; c <= grid; ++c) start[c] = (uint16_t)fill[(size_t)c];
+    for (size_t i = 0; i < k; ++i) order[fill[cta_of[i]]++] = unit_of[i];
     return true;
 }
 

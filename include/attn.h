@@ -36,8 +36,9 @@
  * box -- every input of the encode, so a hit is exactly what a fresh encode
  * would give, including for a buffer freed and reallocated at the same
  * address -- and a least-recently-used cache of the forward kernel's work
- * order for 8 shapes (attn_fwd_schedule; a pure function of the shape and the
- * SM count), each guarded by a mutex.  The work runs on the calling thread's
+ * order for 32 shapes (attn_fwd_schedule; a pure function of the shape and
+ * the SM count; the first call with a new shape spends up to about 0.2 ms of
+ * host time building it), each guarded by a mutex.  The work runs on the calling thread's
  * current device (cudaGetDevice), which must hold every buffer; its primary
  * context is bound to the thread on entry, so a thread that has made no CUDA
  * call yet (an autograd engine's worker, say) can call too.
