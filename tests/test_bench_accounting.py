@@ -35,3 +35,23 @@ def test_host_cpu_names_x86_and_arm_hosts(tmp_path):
                    "CPU variant\t: 0x0\nCPU part\t: 0xd4f\nCPU revision\t: 0\n")
     assert bench.host_cpu(str(arm)).endswith("implementer 0x41 part 0xd4f")
     assert bench.host_cpu(str(tmp_path / "missing")) != ""
+
+
+def test_sources_hash_ignores_comments_and_layout_only():
+    """The DRAM-traffic records are keyed by a hash of the kernel code without
+    comments: a comment or whitespace edit keeps the key, a code edit changes it."""
+    base = "int f(int x) {\n    // doubles x\n    return 2 * x; /* no overflow check */\n}\n"
+    comment_edit = "int f(int x) {\n    // doubles its argument\n    return 2 * x;\n}\n"
+    layout_edit = "int f(int x) { return 2 * x; }\n"
+    code_edit = "int f(int x) {\n    // doubles x\n    return 3 * x;\n}\n"
+    assert bench._code_only(base) == bench._code_only(comment_edit) == bench._code_only(layout_edit)
+    assert bench._code_only(base) != bench._code_only(code_edit)
+
+
+def test_traffic_records_are_well_formed():
+    """Every record line holds a 16-digit sources key, a workload name and a
+    positive byte count."""
+    import os
+    path = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "profiles", "dram_traffic.txt")
+    rows = [line.split() for line in open(path) if line.strip() and not line.startswith("#")]
+    assert rows and all(len(r) == 3 and len(r[0]) == 16 and int(r[2]) > 0 for r in rows)
